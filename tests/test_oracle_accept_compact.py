@@ -1,0 +1,186 @@
+"""Pins for acceptance and compaction of the oracle.
+
+The pages describe the nine-row fixture's winners but do not print its target
+distributions, so two distributions are constructed here to satisfy that
+description; their expected outcomes are derived by hand in the comments.
+"""
+import json
+import math
+import os
+
+import numpy as np
+import pytest
+
+from oracle import accept, compact, tree
+from oracle.round import tree_fill
+
+GOLD = os.path.join(os.path.dirname(__file__), "golden")
+EPS, DELTA = 0.09, 0.3
+V = 64
+
+
+def gold():
+    with open(os.path.join(GOLD, "a31_nine_row.json")) as f:
+        return json.load(f)
+
+
+def a31():
+    g = gold()
+    t = tree.compile_template(g["paths"], g["topk"])
+    pool = np.array([g["head0_ranks"], g["head1_ranks"]])
+    tokens, _ = tree_fill(t, g["root_token"], pool, g["prefix_len"])
+    return g, t, tokens
+
+
+def dist(mass: dict, rest_over: int = None):
+    """log of a distribution over V ids: given masses, the remainder spread uniformly over the others."""
+    p = np.zeros(V)
+    for tok, m in mass.items():
+        p[tok] = m
+    others = [i for i in range(V) if i not in mass]
+    p[others] = (1.0 - sum(mass.values())) / len(others)
+    return np.log(p)
+
+
+def fixture_one():
+    """Row 0 (root 11): p(21)=.40, p(22)=.35.  Row 1 (token 21): p(31)=.30, p(32)=.06, p(33)=.005.
+    Row 2 (token 22): p(31)=.90, p(32)=.02, p(33)=.005.  Leaves get uniform logits.
+
+    Thresholds tau = min(.09, .3 e^-H):  H0 = 2.1123 -> tau0 = .03629;
+    H1 = 3.4553 -> tau1 = .009471;  H2 = .70214 -> .3 e^-H2 = .14866 -> tau2 = .09.
+    Typical lengths per path (0,0),(0,1),(0,2),(1,0),(1,1),(1,2) = 2,2,1,2,1,1;
+    log-likelihoods of the length-2 paths: -2.1203, -3.7297, -1.1552 -> winner (1,0)
+    = tokens [11,22,31], rows [0,2,6].  Greedy: argmax row0 = 21, rows 1 and 2 -> 31;
+    lengths 2,1,1,0,0,0 -> winner path 0 = [11,21,31].
+    """
+    logits = np.zeros((9, V))
+    logits[0] = dist({21: .40, 22: .35})
+    logits[1] = dist({31: .30, 32: .06, 33: .005})
+    logits[2] = dist({31: .90, 32: .02, 33: .005})
+    return logits
+
+
+def fixture_two():
+    """Separates the log-likelihood tie-break from a raw-probability sum.
+    Row 0: p(21)=.40, p(22)=.58.  Row 1: p(31)=.50.  Row 2: p(31)=.34, p(40)=.30.
+    tau0 = .09, tau1 = .0189, tau2 = .02271; all other candidates fall below their threshold.
+    Length-2 paths: (0,0) with log(.4*.5) = -1.6094 and (1,0) with log(.58*.34) = -1.6235,
+    so (0,0) wins, although .58+.34 > .40+.50.
+    """
+    logits = np.zeros((9, V))
+    logits[0] = dist({21: .40, 22: .58})
+    logits[1] = dist({31: .50})
+    logits[2] = dist({31: .34, 40: .30})
+    return logits
+
+
+def test_greedy_winner_a31():
+    g, t, tokens = a31()
+    r = accept.accept(fixture_one(), tokens, t.retrieve, "greedy")
+    assert list(r.per_path_len) == [2, 1, 1, 0, 0, 0]
+    assert list(r.out_tokens) == g["greedy_winner_tokens"]
+    assert r.accept_len == g["greedy_accept_len"]
+    assert r.best_path == 0 and r.frontier_row == 3
+
+
+def test_typical_winner_a31():
+    g, t, tokens = a31()
+    r = accept.accept(fixture_one(), tokens, t.retrieve, "typical", epsilon=EPS, delta=DELTA)
+    assert list(r.per_path_len) == [2, 2, 1, 2, 1, 1]
+    assert list(r.out_tokens) == g["typical_winner_tokens"]
+    assert r.accept_len == g["typical_accept_len"]
+    assert list(r.out_rows) == g["commit_rows"]
+    assert r.frontier_row == 6
+    np.testing.assert_allclose(r.per_path_score[[0, 1, 3]],
+                               [math.log(.4 * .3), math.log(.4 * .06), math.log(.35 * .9)], rtol=1e-12)
+
+
+def test_typical_tie_break_uses_log_likelihood():
+    g, t, tokens = a31()
+    r = accept.accept(fixture_two(), tokens, t.retrieve, "typical", epsilon=EPS, delta=DELTA)
+    assert list(r.per_path_len) == [2, 1, 1, 2, 1, 1]
+    assert list(r.out_tokens) == [11, 21, 31]
+
+
+def test_root_only_progress():
+    g, t, tokens = a31()
+    logits = np.zeros((9, V))
+    logits[0] = dist({5: .9})           # target wants a token no head proposed
+    for mode in ("greedy", "typical"):
+        r = accept.accept(logits, tokens, t.retrieve, mode, epsilon=EPS, delta=DELTA)
+        assert r.accept_len == 0 and r.best_path == 0
+        assert list(r.out_tokens) == g["root_only_tokens"]
+        assert list(r.out_rows) == [0] and r.frontier_row == 0
+
+
+def test_prefix_only_counting():
+    """[PartII] Part 7: raw matches [T, F, T, T] give accepted length 1."""
+    t = tree.compile_template(tree.regular_paths((1, 1, 1, 1)), topk=1)
+    tokens = np.array([100, 101, 102, 103, 104])
+    logits = np.zeros((5, 200))
+    wanted = [101, 999 % 200, 103, 104]           # edge 1 fails, later edges would match
+    for u, w in enumerate(wanted):
+        logits[u, w] = 5.0
+    r = accept.accept(logits, tokens, t.retrieve, "greedy")
+    assert r.accept_len == 1 and list(r.out_rows) == [0, 1]
+
+
+def test_argmax_ties_lowest_id():
+    t = tree.compile_template([(0,), (1,)], topk=2)
+    tokens = np.array([0, 7, 3])
+    logits = np.zeros((3, 10))
+    logits[0, [3, 7]] = 2.0                        # tie between ids 3 and 7: argmax is 3
+    r = accept.accept(logits, tokens, t.retrieve, "greedy")
+    assert r.best_path == 1 and list(r.out_tokens) == [0, 3]
+
+
+def test_entropy_closed_forms():
+    """Uniform over n ids: H = ln n; one-hot: H = 0; two-point (p, 1-p): binary entropy."""
+    st = accept.row_stats(np.zeros(1000))
+    assert st.entropy == pytest.approx(math.log(1000), rel=1e-13)
+    one = np.full(50, -1e4)
+    one[3] = 0.0
+    assert accept.row_stats(one).entropy == pytest.approx(0.0, abs=1e-12)
+    p = 0.2
+    two = np.full(2, 0.0)
+    two[1] = math.log((1 - p) / p)
+    assert accept.row_stats(two).entropy == pytest.approx(-(p * math.log(p) + (1 - p) * math.log(1 - p)))
+    # temperature scales logits before the softmax: T -> infinity approaches uniform
+    x = np.array([0.0, 1.0, 2.0])
+    assert accept.row_stats(x, temperature=1e9).entropy == pytest.approx(math.log(3), rel=1e-6)
+
+
+def test_five_token_entropy():
+    """[PartII] Part 8 distribution p = [.35,.25,.18,.12,.10]: H = 1.5073652 nats, e^-H = .221493.
+    (The page's printed value was lost; these digits come from the definition.)"""
+    p = np.array([.35, .25, .18, .12, .10])
+    st = accept.row_stats(np.log(p))
+    assert st.entropy == pytest.approx(1.5073652, abs=2e-7)
+    assert math.exp(-st.entropy) == pytest.approx(0.221493, abs=1e-6)
+    tau = min(EPS, DELTA * math.exp(-st.entropy))
+    assert tau == pytest.approx(0.066448, abs=1e-6)
+    assert all(x > tau for x in p)                 # every listed token passes at this position
+
+
+def test_commit_trace():
+    """[M7.2] §0x06B: rows [0,2,6], P = 5 -> sources [5,7,11] -> destinations [5,6,7], length 8."""
+    g = gold()
+    src, dst = compact.compaction_map(g["prefix_len"], g["commit_rows"])
+    assert list(src) == g["commit_sources"] and list(dst) == g["commit_destinations"]
+    Hkv, dh, cap = 2, 4, 16
+    ck = np.arange(Hkv * cap * dh, dtype=np.float64).reshape(Hkv, cap, dh)
+    cv = -ck.copy()
+    before_k, before_v = ck.copy(), cv.copy()
+    new_len = compact.kv_compact(ck, cv, g["prefix_len"], g["commit_rows"])
+    assert new_len == g["commit_new_len"] and new_len - g["prefix_len"] == g["commit_published"]
+    for s, d in zip(src, dst):
+        assert (ck[:, d] == before_k[:, s]).all() and (cv[:, d] == before_v[:, s]).all()
+    assert (ck[:, :5] == before_k[:, :5]).all()   # committed prefix untouched
+
+
+def test_compact_overlap_needs_snapshot():
+    """rows [0,2,5] at L = 0: destination 2 is also the source of edge 1."""
+    ck = np.arange(8, dtype=np.float64).reshape(1, 8, 1)
+    cv = ck.copy()
+    compact.kv_compact(ck, cv, 0, [0, 2, 5])
+    assert list(ck[0, :3, 0]) == [0.0, 2.0, 5.0]
