@@ -1,0 +1,280 @@
+/*
+ * medusa_gb300.h - C ABI of libmedusa_gb300.so: one Medusa verify round on one GPU.
+ *
+ * A round has five device calls, issued in this order on one stream:
+ *   medusa_heads_topk -> medusa_tree_fill -> medusa_tree_attn_verify
+ *   -> medusa_tree_accept -> medusa_kv_compact
+ * plus host-side template construction (medusa_tree_regular, medusa_tree_greedy,
+ * medusa_tree_compile, medusa_tree_upload).
+ *
+ * Pages that define the operations (cited by title and section):
+ *   [M7.2]   "M7.2 - Medusa: Multi-Head Candidates, Tree Attention, and Verification"
+ *   [CN]     "Medusa 完全拆解：多头树式候选如何用一次验证解码多个 Token"
+ *   [PartII] "Medusa Part II: Candidate Trees, Verification, and Acceptance"
+ *   [Math]   "Medusa — Multi-Head Speculative Decoding Math"
+ *
+ * Conventions shared by every call
+ *   - Pointers are device memory unless the comment says [host].  All device
+ *     buffers are owned by the caller; no call allocates or frees memory.
+ *   - Arrays are row-major with the last dimension contiguous.  Float tensors
+ *     read with 128-bit loads must be 16-byte aligned (the base pointer and
+ *     every row); medusa_tree_attn_verify's bf16 path also needs the KV cache
+ *     base 16-byte aligned for its TMA descriptors.
+ *   - Token ids, row indices and lengths are int32.  Per-sequence lengths live
+ *     in device memory, so a round needs no host synchronisation.
+ *   - Device calls are asynchronous on `stream` (a cudaStream_t; NULL is the
+ *     legacy default stream).  They return MEDUSA_OK after enqueueing, or a
+ *     negative status with nothing enqueued when an argument that the host can
+ *     see is invalid.  Conditions only the device can see (a prefix length past
+ *     the cache capacity, a corrupt accepted path) are reported per sequence in
+ *     `status[b]`, and that sequence is left unmodified.
+ *   - No kernel waits on another kernel, a flag or a peer; there are no spin
+ *     loops.  Split work is merged by the last CTA to finish (an atomic ticket).
+ */
+#ifndef MEDUSA_GB300_H
+#define MEDUSA_GB300_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef int32_t medusa_status;
+#define MEDUSA_OK            0
+#define MEDUSA_EINVAL       -1   /* bad pointer, size or enum */
+#define MEDUSA_ECAPACITY    -2   /* cache too small for L + N rows */
+#define MEDUSA_EUNSUPPORTED -3   /* shape outside what the kernels implement */
+#define MEDUSA_ETEMPLATE    -4   /* rank paths not prefix-closed, duplicated or out of range */
+#define MEDUSA_ECUDA        -5   /* a CUDA runtime call failed */
+#define MEDUSA_EWORKSPACE   -6   /* workspace or output buffer too small */
+#define MEDUSA_EPATH        -7   /* per-sequence: accepted path is not a valid tree chain */
+
+typedef int32_t medusa_dtype;
+#define MEDUSA_F32  0
+#define MEDUSA_BF16 1
+
+#define MEDUSA_ACCEPT_GREEDY  0
+#define MEDUSA_ACCEPT_TYPICAL 1
+
+/* Largest supported sizes. */
+#define MEDUSA_MAX_ROWS   4096   /* packed tree rows N, root included */
+#define MEDUSA_MAX_DEPTH  16     /* Medusa depth D (paths hold D + 1 rows) */
+#define MEDUSA_MAX_TOPK   32     /* candidate pool width TOPK */
+
+/*
+ * Compiled tree template: the four coupled buffers of [M7.2] §0x04A plus the
+ * structure derived from them.  Rows are numbered canonically: row 0 is the
+ * LM-head root (empty path); non-root rank paths are sorted by (length, path)
+ * and row(path) = 1 + index ([M7.2] §0x04A "Canonical row map").
+ *
+ * The struct is a host value whose array pointers point either into a host
+ * buffer (after medusa_tree_compile) or into a device buffer (after
+ * medusa_tree_upload).  Device calls take the device form.
+ */
+typedef struct {
+  int32_t n_rows;       /* N = 1 + number of rank paths */
+  int32_t n_words;      /* ceil(N / 64): 64-bit words per ancestor mask row */
+  int32_t max_depth;    /* D = longest path */
+  int32_t n_paths;      /* maximal root-to-node paths (retrieval rows) */
+  int32_t topk;         /* TOPK of the slot formula */
+  int32_t n_internal;   /* rows with at least one child */
+  const int32_t *slot;           /* [N] tree_indices: 0 for the root, 1 + (t-1)*TOPK + r_t ([M7.2] §0x01B) */
+  const int32_t *depth;          /* [N] path length; position = L + depth ([M7.2] §0x03C) */
+  const int32_t *parent;         /* [N] parent row, -1 for the root */
+  const int32_t *retrieve;       /* [n_paths][D+1] row chains from the root, -1 padded ([M7.2] §0x04A) */
+  const int32_t *internal;       /* [n_internal] rows with children, ascending */
+  const int32_t *internal_index; /* [N] position of a row in `internal`, -1 for leaves */
+  const uint64_t *anc;           /* [N][n_words] bit (v % 64) of word v / 64 set iff path(v) is a prefix of path(u) ([M7.2] §0x04A) */
+} medusa_tree_t;
+
+/* One layer's KV cache, contiguous or paged. */
+typedef struct {
+  void *k;                /* contiguous: [B][n_kv_heads][capacity][head_dim];
+                             paged:      [n_pages][n_kv_heads][page_size][head_dim] */
+  void *v;                /* same layout as k */
+  medusa_dtype dtype;     /* MEDUSA_F32 or MEDUSA_BF16 */
+  int32_t n_kv_heads;
+  int32_t head_dim;       /* 64 or 128 */
+  int32_t capacity;       /* rows addressable per sequence (paged: max_blocks * page_size) */
+  int32_t page_size;      /* 0 = contiguous; otherwise 16 */
+  const int32_t *block_table; /* paged: [B][max_blocks] physical page of rows [16j, 16j+16) */
+  int32_t max_blocks;
+  int32_t n_pages;
+} medusa_kv_t;
+
+/* ---------------------------------------------------------------------------
+ * Host-side template construction (no GPU needed)
+ * ------------------------------------------------------------------------- */
+
+/* All rank paths of a regular Cartesian tree with widths s_1..s_K, in canonical
+ * order ([M7.2] §0x02B; [CN] "多个 Medusa Head 如何产生候选树"; [Math] "From heads
+ * to a candidate tree").  paths_out [host] [max_paths][K], -1 padded.  *n_out gets
+ * sum_k prod_{i<=k} s_i.  MEDUSA_EWORKSPACE if max_paths is too small. */
+medusa_status medusa_tree_regular(const int32_t *widths /*[host] K*/, int32_t K,
+                                  int32_t *paths_out, int32_t max_paths, int32_t *n_out);
+
+/* Greedy frontier search of [M7.2] §0x04C / [PartII] Part 3: starting from the
+ * root, repeatedly admit the frontier path of largest weight
+ * w(r_1..r_t) = prod_j acc[j][r_j] (computed left to right in double), then open
+ * its children, until `budget` paths are chosen.  Weights within 1e-12 relative
+ * tie; ties go to the shorter path, then the lexicographically smaller one.
+ * acc [host] [K][R] exact-rank accuracies in [0, 1].  paths_out [host] [budget][K],
+ * -1 padded, in admission order.  *n_out = paths chosen (< budget only when every
+ * path of depth <= K is taken). */
+medusa_status medusa_tree_greedy(const double *acc, int32_t K, int32_t R, int32_t budget,
+                                 int32_t *paths_out, int32_t *n_out);
+
+/* Bytes of the template blob for up to n_paths rank paths of length <= max_len. */
+size_t medusa_tree_bytes(int32_t n_paths, int32_t max_len);
+
+/* Compile rank paths into a template ([M7.2] §0x04A).  paths [host]
+ * [n_paths][max_len], -1 padded, any order.  Rejects (MEDUSA_ETEMPLATE) duplicate
+ * paths, empty paths, ranks outside [0, topk), paths longer than n_heads and
+ * families that are not prefix-closed.  The arrays are written into host_buf
+ * [host, host_bytes >= medusa_tree_bytes(...), 8-byte aligned]; *out points into it. */
+medusa_status medusa_tree_compile(const int32_t *paths, int32_t n_paths, int32_t max_len,
+                                  int32_t topk, int32_t n_heads, void *host_buf,
+                                  size_t host_bytes, medusa_tree_t *out);
+
+/* Copy a compiled template blob to device memory (one cudaMemcpyAsync on
+ * `stream`; host_buf must stay alive until the copy completes) and fill *dev
+ * with pointers into dev_buf.  dev_buf 16-byte aligned, dev_bytes >= the blob. */
+medusa_status medusa_tree_upload(const medusa_tree_t *host_tree, const void *host_buf,
+                                 void *dev_buf, size_t dev_bytes, medusa_tree_t *dev,
+                                 void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Round step 1: heads + top-k
+ * ------------------------------------------------------------------------- */
+
+size_t medusa_heads_topk_workspace(int32_t T, int32_t d, int32_t V, int32_t K, int32_t topk);
+
+/* For each of T frontier rows h[t] ([CN] "Medusa 的核心思路与系统位置"; [Math]
+ * "The Medusa head"; [M7.2] §0x02A with one residual block):
+ *   root[t]        = argmax_v (W_LM h[t])_v                          ([M7.2] §0x04D)
+ *   z_k            = h[t] + SiLU(W1_k h[t] + b1_k)
+ *   pool[t][k][:]  = the topk ids of W2_k z_k, by value descending   ([PartII] Part 4)
+ * Ties in value go to the lower token id.  Arithmetic: fp32 accumulation of
+ * the dtype inputs; z_k is kept in fp32.
+ *   h [T][d]; w1 [K][d][d]; b1 [K][d] or NULL; w2: head k's [V][d] matrix starts
+ *   at w2 + k * w2_head_stride elements (stride 0 = one projection shared by all
+ *   heads, [M7.2] §0x02D); w_lm [V][d].  All in dtype `dt`.
+ *   root [T]; pool [T][K][topk]; logits_out [T][K+1][V] fp32 or NULL (slot 0 =
+ *   LM head, slot 1+k = head k).
+ * Limits: 1 <= T <= 64, d % 8 == 0, topk <= MEDUSA_MAX_TOPK, topk <= V. */
+medusa_status medusa_heads_topk(const void *h, int32_t T, int32_t d, int32_t V, int32_t K,
+                                const void *w1, const void *b1, const void *w2,
+                                int64_t w2_head_stride, const void *w_lm, int32_t topk,
+                                medusa_dtype dt, int32_t *root, int32_t *pool,
+                                float *logits_out, void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Round step 2: tree fill
+ * ------------------------------------------------------------------------- */
+
+/* tokens[b][u] = cand_b[slot[u]] with cand_b = [root[b], pool[b][0][:], pool[b][1][:], ...]
+ * and pos[b][u] = L[b] + depth[u] ([M7.2] §0x01B, §0x04A "Candidate gather",
+ * "Visibility and position"; [CN] "手算一棵两层候选树").
+ *   t: device template; root [B]; pool [B][K][t->topk] (K >= t->max_depth);
+ *   L [B]; tokens, pos [B][N]. */
+medusa_status medusa_tree_fill(const medusa_tree_t *t, int32_t B, int32_t K, const int32_t *root,
+                               const int32_t *pool, const int32_t *L, int32_t *tokens,
+                               int32_t *pos, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Round step 3: tree verification attention
+ * ------------------------------------------------------------------------- */
+
+size_t medusa_tree_attn_workspace(const medusa_tree_t *t, int32_t B, int32_t n_q_heads,
+                                  const medusa_kv_t *cache, int32_t max_prefix);
+
+/* Tree attention of [M7.2] §0x03C ([CN] "Tree Attention"; [Math] "Tree attention:
+ * the mask math").  For sequence b with committed length L = L[b] and each tree
+ * row u at logical position L + depth[u]:
+ *   q' = RoPE(q[b][u][h], L + depth[u]),  k'_u = RoPE(k_new[b][u][kv], L + depth[u])
+ *   (rotate-half pairs (i, i + dh/2), angle pos * rope_base^(-2i/dh));
+ *   out[b][u][h] = softmax(scale * q' . K^T) V over keys {cache rows 0..L-1}
+ *                  union {tree rows v with anc[u] bit v}, with tree keys k'_v and values v_new[v];
+ *   the staged rows L + u of the cache receive k'_u and v_new[b][u] ([M7.2] §0x03E).
+ * Query head h reads KV head h / (n_q_heads / n_kv_heads).  The cache prefix K is
+ * already rotated.  Rows >= L of the cache are never read as prefix keys.
+ *   q [B][N][n_q_heads][head_dim]; k_new, v_new [B][N][n_kv_heads][head_dim] in the
+ *   cache dtype; L [B]; max_prefix >= every L[b] (sizes the split-KV grid);
+ *   out [B][N][n_q_heads][head_dim] fp32 (the accumulation precision: a bf16 output
+ *   would add ~1.6e-3 relative rounding error); lse [B][N][n_q_heads] fp32
+ *   natural-log log-sum-exp, or NULL; status [B] (0, or MEDUSA_ECAPACITY when
+ *   L[b] + N > capacity, in which case sequence b is not touched).
+ *   ws: workspace of medusa_tree_attn_workspace(...) bytes (16-byte aligned),
+ *   zero-filled once before its first use.  Its first 256 KiB hold split-KV ticket
+ *   counters that every call returns to zero, so one workspace can serve later
+ *   calls of any shape without clearing; the rest is scratch.  Calls that share a
+ *   workspace must not run concurrently.
+ * Arithmetic: fp32 kernels for MEDUSA_F32; for MEDUSA_BF16 the prefix part runs
+ * on tcgen05 tensor cores with fp16 operands (q' and P rounded to fp16, bf16 K/V
+ * converted exactly) and fp32 accumulation, the tree part in fp32. */
+medusa_status medusa_tree_attn_verify(const medusa_tree_t *t, int32_t B, int32_t n_q_heads,
+                                      const void *q, const void *k_new, const void *v_new,
+                                      const medusa_kv_t *cache, const int32_t *L,
+                                      int32_t max_prefix, float rope_base, float scale,
+                                      float *out, float *lse, int32_t *status, void *ws,
+                                      size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Round step 4: acceptance
+ * ------------------------------------------------------------------------- */
+
+size_t medusa_tree_accept_workspace(const medusa_tree_t *t, int32_t B, int32_t V);
+
+/* Greedy or fast-typical acceptance ([M7.2] §0x03D, §0x04D, §0x04E; [PartII] Part 7;
+ * [CN] "接受机制").  Target row u scores the token of its child: along retrieval
+ * path p = [u_0, u_1, ...] edge j passes when
+ *   greedy:  tokens[u_{j+1}] == argmax(logits[u_j])   (lowest id among maxima)
+ *   typical: p_j > min(epsilon, delta * exp(-H_j)) with p = softmax(logits[u_j] / T)
+ *            evaluated at tokens[u_{j+1}] and H_j its entropy (entropy_guard = 1
+ *            uses -sum p log(p + 1e-5) instead of the exact entropy).
+ * a_p = edges before the first failure.  Winner: largest a_p; greedy takes the
+ * first such path (path 0 when none passes); typical takes the largest
+ * sum_{j<a} log p_j, then the lowest path index.  Row statistics are computed
+ * once per internal row (rows without children are never read).
+ *   logits [B][N][V] in dtype dt; tokens [B][N];
+ *   best_path [B]; accept_len [B] (a); out_tokens, out_rows [B][D+1] (G = a + 1
+ *   entries, then -1); frontier_row [B] (u_a, [M7.2] §0x06C).
+ * ws: medusa_tree_accept_workspace(...) bytes. */
+medusa_status medusa_tree_accept(const medusa_tree_t *t, int32_t B, int32_t V, const void *logits,
+                                 medusa_dtype dt, const int32_t *tokens, int32_t mode,
+                                 float temperature, float epsilon, float delta,
+                                 int32_t entropy_guard, int32_t *best_path, int32_t *accept_len,
+                                 int32_t *out_tokens, int32_t *out_rows, int32_t *frontier_row,
+                                 void *ws, size_t ws_bytes, void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Round step 5: winning-path K/V compaction
+ * ------------------------------------------------------------------------- */
+
+/* Gather-and-compact of [M7.2] §0x06A-§0x06B: with G = accept_len[b] + 1 and
+ * rows u_j = out_rows[b][j], cache rows L + u_j are read into a snapshot first
+ * and then written to rows L + j, for K and V of every KV head; L_out[b] = L + G.
+ * The path is validated first (G <= D + 1, u_0 = 0, each u_j a child of u_{j-1},
+ * L + N <= capacity); an invalid sequence gets status[b] = MEDUSA_EPATH or
+ * MEDUSA_ECAPACITY, L_out[b] = L[b] and no cache write.
+ *   t: device template (its parent array validates the chain); L, accept_len [B];
+ *   out_rows [B][D+1]; L_out [B]; status [B]. */
+medusa_status medusa_kv_compact(const medusa_kv_t *cache, const medusa_tree_t *t, int32_t B,
+                                const int32_t *L, const int32_t *accept_len,
+                                const int32_t *out_rows, int32_t *L_out, int32_t *status,
+                                void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Misc
+ * ------------------------------------------------------------------------- */
+
+const char *medusa_status_string(medusa_status s);
+int32_t medusa_abi_version(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* MEDUSA_GB300_H */

@@ -1,0 +1,94 @@
+"""ctypes declarations of the C ABI in include/medusa_gb300.h.
+
+Loading fails loudly when libmedusa_gb300.so has not been built: there is no
+fallback implementation of any step.
+"""
+from __future__ import annotations
+
+import ctypes as C
+import os
+
+_PKG = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_PKG, "libmedusa_gb300.so")
+
+OK, EINVAL, ECAPACITY, EUNSUPPORTED, ETEMPLATE, ECUDA, EWORKSPACE, EPATH = 0, -1, -2, -3, -4, -5, -6, -7
+F32, BF16 = 0, 1
+GREEDY, TYPICAL = 0, 1
+MAX_ROWS, MAX_DEPTH, MAX_TOPK = 4096, 16, 32
+
+EXPORTED = [
+    "medusa_tree_regular", "medusa_tree_greedy", "medusa_tree_bytes", "medusa_tree_compile",
+    "medusa_tree_upload", "medusa_heads_topk_workspace", "medusa_heads_topk", "medusa_tree_fill",
+    "medusa_tree_attn_workspace", "medusa_tree_attn_verify", "medusa_tree_accept_workspace",
+    "medusa_tree_accept", "medusa_kv_compact", "medusa_status_string", "medusa_abi_version",
+]
+
+
+class MedusaTree(C.Structure):
+    _fields_ = [
+        ("n_rows", C.c_int32), ("n_words", C.c_int32), ("max_depth", C.c_int32),
+        ("n_paths", C.c_int32), ("topk", C.c_int32), ("n_internal", C.c_int32),
+        ("slot", C.c_void_p), ("depth", C.c_void_p), ("parent", C.c_void_p),
+        ("retrieve", C.c_void_p), ("internal", C.c_void_p), ("internal_index", C.c_void_p),
+        ("anc", C.c_void_p),
+    ]
+
+
+class MedusaKV(C.Structure):
+    _fields_ = [
+        ("k", C.c_void_p), ("v", C.c_void_p), ("dtype", C.c_int32), ("n_kv_heads", C.c_int32),
+        ("head_dim", C.c_int32), ("capacity", C.c_int32), ("page_size", C.c_int32),
+        ("block_table", C.c_void_p), ("max_blocks", C.c_int32), ("n_pages", C.c_int32),
+    ]
+
+
+class MedusaError(RuntimeError):
+    def __init__(self, fn: str, status: int, msg: str):
+        super().__init__(f"{fn} failed: {msg} (status {status})")
+        self.status = status
+
+
+_lib = None
+
+
+def lib() -> C.CDLL:
+    """The loaded library; raises if it is missing."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(LIB_PATH):
+        raise RuntimeError(
+            f"{LIB_PATH} is missing: build it with medusa_speculative_tree_gb300.build.build()")
+    L = C.CDLL(LIB_PATH)
+    P, I32, I64, SZ, F, VP = C.POINTER, C.c_int32, C.c_int64, C.c_size_t, C.c_float, C.c_void_p
+    sig = {
+        "medusa_tree_regular": (I32, [VP, I32, VP, I32, P(I32)]),
+        "medusa_tree_greedy": (I32, [VP, I32, I32, I32, VP, P(I32)]),
+        "medusa_tree_bytes": (SZ, [I32, I32]),
+        "medusa_tree_compile": (I32, [VP, I32, I32, I32, I32, VP, SZ, P(MedusaTree)]),
+        "medusa_tree_upload": (I32, [P(MedusaTree), VP, VP, SZ, P(MedusaTree), VP]),
+        "medusa_heads_topk_workspace": (SZ, [I32, I32, I32, I32, I32]),
+        "medusa_heads_topk": (I32, [VP, I32, I32, I32, I32, VP, VP, VP, I64, VP, I32, I32, VP, VP,
+                                    VP, VP, SZ, VP]),
+        "medusa_tree_fill": (I32, [P(MedusaTree), I32, I32, VP, VP, VP, VP, VP, VP]),
+        "medusa_tree_attn_workspace": (SZ, [P(MedusaTree), I32, I32, P(MedusaKV), I32]),
+        "medusa_tree_attn_verify": (I32, [P(MedusaTree), I32, I32, VP, VP, VP, P(MedusaKV), VP, I32,
+                                          F, F, VP, VP, VP, VP, SZ, VP]),
+        "medusa_tree_accept_workspace": (SZ, [P(MedusaTree), I32, I32]),
+        "medusa_tree_accept": (I32, [P(MedusaTree), I32, I32, VP, I32, VP, I32, F, F, F, I32, VP, VP,
+                                     VP, VP, VP, VP, SZ, VP]),
+        "medusa_kv_compact": (I32, [P(MedusaKV), P(MedusaTree), I32, VP, VP, VP, VP, VP, VP]),
+        "medusa_status_string": (C.c_char_p, [I32]),
+        "medusa_abi_version": (I32, []),
+    }
+    for name, (res, args) in sig.items():
+        fn = getattr(L, name)
+        fn.restype = res
+        fn.argtypes = args
+    _lib = L
+    return L
+
+
+def check(fn: str, status: int) -> None:
+    if status != OK:
+        raise MedusaError(fn, status, lib().medusa_status_string(status).decode())

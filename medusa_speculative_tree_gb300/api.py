@@ -1,0 +1,289 @@
+"""Python binding of the C ABI, same names as the C entry points.
+
+Argument marshalling only: tensors are passed as device pointers with the
+current CUDA stream; every step of the round runs in libmedusa_gb300.so.
+PyTorch supplies device memory (outputs and workspaces) and streams.
+"""
+from __future__ import annotations
+
+import ctypes as C
+from dataclasses import dataclass
+from typing import Optional, Sequence
+
+import numpy as np
+import torch
+
+from . import _native as nat
+from ._native import check, lib
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    return None if t is None else C.c_void_p(t.data_ptr())
+
+
+def _stream(device=None):
+    return C.c_void_p(torch.cuda.current_stream(device).cuda_stream)
+
+
+def _dtype_code(dt: torch.dtype) -> int:
+    if dt == torch.float32:
+        return nat.F32
+    if dt == torch.bfloat16:
+        return nat.BF16
+    raise TypeError(f"unsupported dtype {dt}")
+
+
+def _need_cuda(*ts):
+    for t in ts:
+        if t is not None and (not t.is_cuda or not t.is_contiguous()):
+            raise ValueError("expected contiguous CUDA tensors")
+
+
+class _Workspace:
+    """Zero-initialised device scratch, grown on demand and reused between calls.
+
+    Kernels that keep ticket counters in their workspace return those counters to
+    zero, so a reused buffer needs no clearing."""
+
+    def __init__(self):
+        self.buf = {}
+
+    def get(self, key, nbytes: int, device) -> torch.Tensor:
+        cur = self.buf.get((key, device))
+        if cur is None or cur.numel() < nbytes:
+            cur = torch.zeros(max(nbytes, 256), dtype=torch.uint8, device=device)
+            self.buf[(key, device)] = cur
+        return cur
+
+
+_WS = _Workspace()
+
+
+# ----------------------------------------------------------------------------- templates
+
+def medusa_tree_regular(widths: Sequence[int]) -> list:
+    """Rank paths of a regular Cartesian tree (host, C++)."""
+    K = len(widths)
+    n = C.c_int32(0)
+    w = np.ascontiguousarray(widths, dtype=np.int32)
+    cap = 1
+    total, prod = 0, 1
+    for s in widths:
+        prod *= int(s)
+        total += prod
+    cap = max(total, 1)
+    out = np.full((cap, max(K, 1)), -1, dtype=np.int32)
+    check("medusa_tree_regular", lib().medusa_tree_regular(w.ctypes.data, K, out.ctypes.data, cap,
+                                                           C.byref(n)))
+    return [tuple(int(x) for x in row if x >= 0) for row in out[:n.value]]
+
+
+def medusa_tree_greedy(acc: np.ndarray, budget: int) -> list:
+    """Greedy frontier tree search (host, C++); paths in admission order."""
+    acc = np.ascontiguousarray(acc, dtype=np.float64)
+    K, R = acc.shape
+    out = np.full((max(budget, 1), K), -1, dtype=np.int32)
+    n = C.c_int32(0)
+    check("medusa_tree_greedy", lib().medusa_tree_greedy(acc.ctypes.data, K, R, budget,
+                                                         out.ctypes.data, C.byref(n)))
+    return [tuple(int(x) for x in row if x >= 0) for row in out[:n.value]]
+
+
+class Template:
+    """A compiled tree template: host blob (for inspection) and its device copy."""
+
+    def __init__(self, paths, topk: int, n_heads: int = 0, device=None):
+        paths = [tuple(int(r) for r in p) for p in paths]
+        max_len = max([len(p) for p in paths], default=0)
+        arr = np.full((max(len(paths), 1), max(max_len, 1)), -1, dtype=np.int32)
+        for i, p in enumerate(paths):
+            arr[i, :len(p)] = p
+        nbytes = lib().medusa_tree_bytes(len(paths), max_len)
+        self._host = np.zeros(nbytes // 8 + 2, dtype=np.uint64)     # 8-byte aligned blob
+        self.host = nat.MedusaTree()
+        check("medusa_tree_compile",
+              lib().medusa_tree_compile(arr.ctypes.data, len(paths), max_len, topk, n_heads,
+                                        self._host.ctypes.data, self._host.nbytes, C.byref(self.host)))
+        self.n_rows = self.host.n_rows
+        self.n_words = self.host.n_words
+        self.max_depth = self.host.max_depth
+        self.n_paths = self.host.n_paths
+        self.topk = self.host.topk
+        self.n_internal = self.host.n_internal
+        self.dev = None
+        self.device = None
+        if device is not None:
+            self.to(device)
+
+    def _arr(self, field, count, dtype=np.int32):
+        addr = getattr(self.host, field)
+        buf = (C.c_char * (count * np.dtype(dtype).itemsize)).from_address(addr)
+        return np.frombuffer(buf, dtype=dtype).copy()
+
+    @property
+    def slot(self):
+        return self._arr("slot", self.n_rows)
+
+    @property
+    def depth(self):
+        return self._arr("depth", self.n_rows)
+
+    @property
+    def parent(self):
+        return self._arr("parent", self.n_rows)
+
+    @property
+    def retrieve(self):
+        return self._arr("retrieve", self.n_paths * (self.max_depth + 1)).reshape(
+            self.n_paths, self.max_depth + 1)
+
+    @property
+    def internal(self):
+        return self._arr("internal", self.n_internal)
+
+    @property
+    def anc(self):
+        return self._arr("anc", self.n_rows * self.n_words, np.uint64).reshape(self.n_rows, self.n_words)
+
+    def to(self, device):
+        device = torch.device(device)
+        self._dev_buf = torch.empty(self._host.nbytes, dtype=torch.uint8, device=device)
+        self.dev = nat.MedusaTree()
+        check("medusa_tree_upload",
+              lib().medusa_tree_upload(C.byref(self.host), self._host.ctypes.data,
+                                       C.c_void_p(self._dev_buf.data_ptr()), self._dev_buf.numel(),
+                                       C.byref(self.dev), _stream(device)))
+        torch.cuda.current_stream(device).synchronize()     # host blob copied before it may change
+        self.device = device
+        return self
+
+
+# ----------------------------------------------------------------------------- KV cache
+
+@dataclass
+class KVCache:
+    """One layer's cache: contiguous [B, Hkv, cap, dh] or paged [pages, Hkv, 16, dh]."""
+
+    k: torch.Tensor
+    v: torch.Tensor
+    block_table: Optional[torch.Tensor] = None    # int32 [B, max_blocks] for paged caches
+    capacity: Optional[int] = None
+
+    def desc(self) -> nat.MedusaKV:
+        _need_cuda(self.k, self.v, self.block_table)
+        d = nat.MedusaKV()
+        d.k, d.v = self.k.data_ptr(), self.v.data_ptr()
+        d.dtype = _dtype_code(self.k.dtype)
+        if self.block_table is None:
+            _, Hkv, cap, dh = self.k.shape
+            d.n_kv_heads, d.head_dim, d.capacity = Hkv, dh, cap
+            d.page_size, d.block_table, d.max_blocks, d.n_pages = 0, None, 0, 0
+        else:
+            n_pages, Hkv, ps, dh = self.k.shape
+            mb = self.block_table.shape[1]
+            d.n_kv_heads, d.head_dim = Hkv, dh
+            d.capacity = self.capacity if self.capacity is not None else mb * ps
+            d.page_size, d.block_table, d.max_blocks, d.n_pages = ps, self.block_table.data_ptr(), mb, n_pages
+        return d
+
+
+# ----------------------------------------------------------------------------- round steps
+
+def medusa_heads_topk(h, w1, w2, w_lm, topk: int, b1=None, logits_out=None, shared_w2=False):
+    """root [T] int32, pool [T, K, topk] int32 (and fills logits_out [T, K+1, V] fp32 if given)."""
+    _need_cuda(h, w1, w2, w_lm, b1, logits_out)
+    T, d = h.shape
+    V = w_lm.shape[0]
+    K = w1.shape[0]
+    dev = h.device
+    stride = 0 if shared_w2 else V * d
+    root = torch.empty(T, dtype=torch.int32, device=dev)
+    pool = torch.empty((T, K, topk), dtype=torch.int32, device=dev)
+    nb = lib().medusa_heads_topk_workspace(T, d, V, K, topk)
+    ws = _WS.get("heads", nb, dev)
+    check("medusa_heads_topk",
+          lib().medusa_heads_topk(_ptr(h), T, d, V, K, _ptr(w1), _ptr(b1), _ptr(w2), stride, _ptr(w_lm),
+                                  topk, _dtype_code(h.dtype), _ptr(root), _ptr(pool), _ptr(logits_out),
+                                  _ptr(ws), ws.numel(), _stream(dev)))
+    return root, pool
+
+
+def medusa_tree_fill(tmpl: Template, root, pool, L):
+    """tokens [B, N], pos [B, N] int32."""
+    _need_cuda(root, pool, L)
+    B = root.shape[0]
+    K = pool.shape[1] if pool.dim() == 3 else 0
+    tokens = torch.empty((B, tmpl.n_rows), dtype=torch.int32, device=root.device)
+    pos = torch.empty_like(tokens)
+    check("medusa_tree_fill",
+          lib().medusa_tree_fill(C.byref(tmpl.dev), B, K, _ptr(root), _ptr(pool), _ptr(L), _ptr(tokens),
+                                 _ptr(pos), _stream(root.device)))
+    return tokens, pos
+
+
+def medusa_tree_attn_workspace(tmpl: Template, B: int, n_q_heads: int, cache: KVCache, max_prefix: int) -> int:
+    d = cache.desc()
+    return lib().medusa_tree_attn_workspace(C.byref(tmpl.dev), B, n_q_heads, C.byref(d), max_prefix)
+
+
+def medusa_tree_attn_verify(tmpl: Template, q, k_new, v_new, cache: KVCache, L, max_prefix: int,
+                            rope_base: float = 10000.0, scale: Optional[float] = None, want_lse=False,
+                            out=None, ws=None):
+    """out [B, N, Hq, dh] fp32, lse [B, N, Hq] fp32 or None, status [B] int32."""
+    _need_cuda(q, k_new, v_new, L, out)
+    B, N, Hq, dh = q.shape
+    dev = q.device
+    if scale is None:
+        scale = 1.0 / float(dh) ** 0.5
+    d = cache.desc()
+    if out is None:
+        out = torch.empty(q.shape, dtype=torch.float32, device=dev)
+    lse = torch.empty((B, N, Hq), dtype=torch.float32, device=dev) if want_lse else None
+    status = torch.empty(B, dtype=torch.int32, device=dev)
+    nb = lib().medusa_tree_attn_workspace(C.byref(tmpl.dev), B, Hq, C.byref(d), max_prefix)
+    if nb == 0:
+        raise ValueError("invalid tree attention shapes")
+    if ws is None:
+        ws = _WS.get("attn", nb, dev)
+    check("medusa_tree_attn_verify",
+          lib().medusa_tree_attn_verify(C.byref(tmpl.dev), B, Hq, _ptr(q), _ptr(k_new), _ptr(v_new),
+                                        C.byref(d), _ptr(L), max_prefix, float(rope_base), float(scale),
+                                        _ptr(out), _ptr(lse), _ptr(status), _ptr(ws), ws.numel(),
+                                        _stream(dev)))
+    return out, lse, status
+
+
+def medusa_tree_accept(tmpl: Template, logits, tokens, mode: str = "greedy", temperature: float = 1.0,
+                       epsilon: float = 0.09, delta: float = 0.3, entropy_guard: bool = False):
+    """dict of best_path, accept_len, out_tokens, out_rows, frontier_row (int32 device tensors)."""
+    _need_cuda(logits, tokens)
+    B, N, V = logits.shape
+    dev = logits.device
+    W = tmpl.max_depth + 1
+    r = {k: torch.empty(B, dtype=torch.int32, device=dev) for k in ("best_path", "accept_len", "frontier_row")}
+    r["out_tokens"] = torch.empty((B, W), dtype=torch.int32, device=dev)
+    r["out_rows"] = torch.empty((B, W), dtype=torch.int32, device=dev)
+    nb = lib().medusa_tree_accept_workspace(C.byref(tmpl.dev), B, V)
+    ws = _WS.get("accept", nb, dev)
+    m = nat.GREEDY if mode == "greedy" else nat.TYPICAL
+    check("medusa_tree_accept",
+          lib().medusa_tree_accept(C.byref(tmpl.dev), B, V, _ptr(logits), _dtype_code(logits.dtype),
+                                   _ptr(tokens), m, float(temperature), float(epsilon), float(delta),
+                                   int(entropy_guard), _ptr(r["best_path"]), _ptr(r["accept_len"]),
+                                   _ptr(r["out_tokens"]), _ptr(r["out_rows"]), _ptr(r["frontier_row"]),
+                                   _ptr(ws), ws.numel(), _stream(dev)))
+    return r
+
+
+def medusa_kv_compact(cache: KVCache, tmpl: Template, L, accept_len, out_rows):
+    """L_out [B], status [B] int32; the cache is compacted in place."""
+    _need_cuda(L, accept_len, out_rows)
+    B = L.shape[0]
+    dev = L.device
+    L_out = torch.empty(B, dtype=torch.int32, device=dev)
+    status = torch.empty(B, dtype=torch.int32, device=dev)
+    d = cache.desc()
+    check("medusa_kv_compact",
+          lib().medusa_kv_compact(C.byref(d), C.byref(tmpl.dev), B, _ptr(L), _ptr(accept_len),
+                                  _ptr(out_rows), _ptr(L_out), _ptr(status), _stream(dev)))
+    return L_out, status

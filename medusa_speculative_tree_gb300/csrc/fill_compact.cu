@@ -1,0 +1,123 @@
+// Tree fill ([M7.2] §0x01B, §0x04A) and winning-path K/V compaction
+// ([M7.2] §0x06A-§0x06B).  Both are small integer / data-movement kernels.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace medusa {
+
+namespace {
+
+// tokens[b][u] = cand_b[slot[u]], cand_b = [root[b], pool[b][0][:], pool[b][1][:], ...]
+// pos[b][u]    = L[b] + depth[u]
+__global__ void tree_fill_kernel(medusa_tree_t t, int K, const int32_t* __restrict__ root,
+                                 const int32_t* __restrict__ pool, const int32_t* __restrict__ L,
+                                 int32_t* __restrict__ tokens, int32_t* __restrict__ pos) {
+  const int b = blockIdx.y;
+  const int u = blockIdx.x * blockDim.x + threadIdx.x;
+  if (u >= t.n_rows) return;
+  const int s = t.slot[u];
+  int tok;
+  if (s == 0) {
+    tok = root[b];
+  } else {
+    const int head = (s - 1) / t.topk, rank = (s - 1) % t.topk;
+    tok = pool[((int64_t)b * K + head) * t.topk + rank];
+  }
+  tokens[(int64_t)b * t.n_rows + u] = tok;
+  pos[(int64_t)b * t.n_rows + u] = L[b] + t.depth[u];
+}
+
+__device__ __forceinline__ int64_t cache_row_offset(const medusa_kv_t& c, int b, int kvh, int row) {
+  if (c.page_size == 0)
+    return (((int64_t)b * c.n_kv_heads + kvh) * c.capacity + row) * c.head_dim;
+  const int page = c.block_table[(int64_t)b * c.max_blocks + row / c.page_size];
+  return (((int64_t)page * c.n_kv_heads + kvh) * c.page_size + row % c.page_size) * c.head_dim;
+}
+
+// One CTA per (kv head, sequence).  The whole path is validated first; the G source
+// rows of K and V are then read into shared memory before any destination row is
+// written, so overlapping source/destination rows are safe.
+template <typename EL>
+__global__ void kv_compact_kernel(medusa_kv_t c, medusa_tree_t t, const int32_t* __restrict__ L,
+                                  const int32_t* __restrict__ accept_len,
+                                  const int32_t* __restrict__ out_rows, int32_t* __restrict__ L_out,
+                                  int32_t* __restrict__ status) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  EL* snap = reinterpret_cast<EL*>(smem_raw);       // [2][D+1][dh]
+  __shared__ int rows_s[MEDUSA_MAX_DEPTH + 1];
+  __shared__ int verdict;
+  const int kvh = blockIdx.x, b = blockIdx.y;
+  const int dh = c.head_dim, W = t.max_depth + 1;
+  const int Lb = L[b];
+  const int a = accept_len[b];
+  if (threadIdx.x == 0) {
+    int v = MEDUSA_OK;
+    if (Lb < 0 || !seq_rows_ok(c, b, (int64_t)Lb + t.n_rows)) v = MEDUSA_ECAPACITY;
+    else if (a < 0 || a > t.max_depth) v = MEDUSA_EPATH;
+    else {
+      for (int j = 0; j <= a; ++j) {
+        const int u = out_rows[(int64_t)b * W + j];
+        rows_s[j] = u;
+        if (u < 0 || u >= t.n_rows) { v = MEDUSA_EPATH; break; }
+        if (j == 0 ? (u != 0) : (t.parent[u] != rows_s[j - 1])) { v = MEDUSA_EPATH; break; }
+      }
+    }
+    verdict = v;
+  }
+  __syncthreads();
+  const int v = verdict;
+  if (v != MEDUSA_OK) {
+    if (kvh == 0 && threadIdx.x == 0) {
+      status[b] = v;
+      L_out[b] = Lb;
+    }
+    return;
+  }
+  const int G = a + 1;
+  EL* ck = (EL*)c.k;
+  EL* cv = (EL*)c.v;
+  for (int idx = threadIdx.x; idx < G * dh; idx += blockDim.x) {
+    const int j = idx / dh, e = idx % dh;
+    const int64_t src = cache_row_offset(c, b, kvh, Lb + rows_s[j]) + e;
+    snap[j * dh + e] = ck[src];
+    snap[(W + j) * dh + e] = cv[src];
+  }
+  __syncthreads();
+  for (int idx = threadIdx.x; idx < G * dh; idx += blockDim.x) {
+    const int j = idx / dh, e = idx % dh;
+    const int64_t dst = cache_row_offset(c, b, kvh, Lb + j) + e;
+    ck[dst] = snap[j * dh + e];
+    cv[dst] = snap[(W + j) * dh + e];
+  }
+  if (kvh == 0 && threadIdx.x == 0) {
+    status[b] = MEDUSA_OK;
+    L_out[b] = Lb + G;
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_tree_fill(const medusa_tree_t& t, int B, int K, const int32_t* root,
+                             const int32_t* pool, const int32_t* L, int32_t* tokens,
+                             int32_t* pos, cudaStream_t st) {
+  const int threads = 128;
+  dim3 grid((t.n_rows + threads - 1) / threads, B);
+  tree_fill_kernel<<<grid, threads, 0, st>>>(t, K, root, pool, L, tokens, pos);
+  return cudaGetLastError();
+}
+
+cudaError_t launch_kv_compact(const medusa_kv_t& c, const medusa_tree_t& t, int B,
+                              const int32_t* L, const int32_t* accept_len,
+                              const int32_t* out_rows, int32_t* L_out, int32_t* status,
+                              cudaStream_t st) {
+  const size_t esz = c.dtype == MEDUSA_BF16 ? 2 : 4;
+  const size_t smem = 2 * (size_t)(t.max_depth + 1) * c.head_dim * esz;
+  dim3 grid(c.n_kv_heads, B);
+  if (c.dtype == MEDUSA_BF16)
+    kv_compact_kernel<uint16_t><<<grid, 128, smem, st>>>(c, t, L, accept_len, out_rows, L_out, status);
+  else
+    kv_compact_kernel<float><<<grid, 128, smem, st>>>(c, t, L, accept_len, out_rows, L_out, status);
+  return cudaGetLastError();
+}
+
+}  // namespace medusa

@@ -1,0 +1,365 @@
+// Medusa heads + top-k ([CN] "Medusa 的核心思路与系统位置"; [Math] "The Medusa head:
+// math and shapes"; [M7.2] §0x02A, §0x04D; [PartII] Part 4).
+//
+// Three phases, all HBM-bound at small T (weights are read exactly once):
+//   1. residual GEMV  z_k = h + SiLU(W1_k h + b1_k)      rows: K*d,  x = h
+//   2. vocabulary GEMV logits[m] = W_m x_m               rows: (K+1)*V, x_0 = h, x_k = z_{k-1}
+//   3. top-k: per-chunk candidates, then one merge per (row t, matrix m).
+// The GEMV streams each weight row with 128-bit L1-bypassing loads, keeps the
+// fp32 input rows in shared memory and reduces each dot product with warp shuffles.
+#include <float.h>
+#include <limits.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace medusa {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kWarps = kThreads / 32;
+
+struct GemvArgs {
+  const void* w0;           // matrix 0
+  const void* w_rest;       // matrix 1 (further matrices at w_rest_stride elements)
+  int64_t w_rest_stride;
+  int n_rows, d;
+  const void* x0;           // input rows of matrix 0 (dtype EL when x0_el, else fp32)
+  int x0_el;
+  int64_t x0_tok_stride;
+  const float* x_rest;      // fp32 input rows of matrix m >= 1, or nullptr to reuse x0
+  int64_t x_rest_tok_stride, x_rest_mat_stride;
+  int t0, tcount;           // token rows [t0, t0 + tcount)
+  float* out;
+  int64_t out_tok_stride, out_mat_stride;
+  int resid;                // 1: out = hres + SiLU(acc + b1[m]) (residual block epilogue)
+  const void* b1;
+};
+
+template <typename EL, int TT, int R, int U>
+__global__ void __launch_bounds__(kThreads) gemv_kernel(GemvArgs a) {
+  extern __shared__ float xs[];               // [TT][d]
+  constexpr int EPV = Elem<EL>::kPerVec;
+  const int m = blockIdx.y;
+  const int d = a.d;
+  const EL* W = (const EL*)(m == 0 ? a.w0 : (const void*)((const EL*)a.w_rest +
+                                                          (int64_t)(m - 1) * a.w_rest_stride));
+  // Stage the fp32 input rows of this matrix.
+  for (int tt = 0; tt < TT; ++tt) {
+    const int t = a.t0 + tt;
+    for (int i = threadIdx.x; i < d; i += kThreads) {
+      float v = 0.f;
+      if (tt < a.tcount) {
+        if (m == 0 || a.x_rest == nullptr) {
+          v = a.x0_el ? Elem<EL>::load((const EL*)a.x0, (int64_t)t * a.x0_tok_stride + i)
+                      : ((const float*)a.x0)[(int64_t)t * a.x0_tok_stride + i];
+        } else {
+          v = a.x_rest[(int64_t)t * a.x_rest_tok_stride + (int64_t)(m - 1) * a.x_rest_mat_stride + i];
+        }
+      }
+      xs[tt * d + i] = v;
+    }
+  }
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int nvec = d / EPV;
+  const int rows_per_iter = kWarps * R;
+  for (int base = blockIdx.x * rows_per_iter; base < a.n_rows; base += gridDim.x * rows_per_iter) {
+    const int row0 = base + warp * R;
+    float acc[R][TT];
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int t = 0; t < TT; ++t) acc[r][t] = 0.f;
+
+    for (int v0 = 0; v0 < nvec; v0 += 32 * U) {
+      uint4 w[R][U];
+#pragma unroll
+      for (int r = 0; r < R; ++r)
+#pragma unroll
+        for (int j = 0; j < U; ++j) {
+          const int vi = v0 + j * 32 + lane;
+          const int row = row0 + r;
+          if (row < a.n_rows && vi < nvec)
+            w[r][j] = ldg_stream(W + (int64_t)row * d + (int64_t)vi * EPV);
+          else
+            w[r][j] = make_uint4(0, 0, 0, 0);
+        }
+#pragma unroll
+      for (int j = 0; j < U; ++j) {
+        const int vi = v0 + j * 32 + lane;
+        if (vi >= nvec) break;
+        float wf[R][EPV];
+#pragma unroll
+        for (int r = 0; r < R; ++r) Elem<EL>::unpack(w[r][j], wf[r]);
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          const float4* xp = reinterpret_cast<const float4*>(xs + t * d + vi * EPV);
+          float xf[EPV];
+#pragma unroll
+          for (int e = 0; e < EPV / 4; ++e) {
+            float4 q = xp[e];
+            xf[4 * e] = q.x; xf[4 * e + 1] = q.y; xf[4 * e + 2] = q.z; xf[4 * e + 3] = q.w;
+          }
+#pragma unroll
+          for (int r = 0; r < R; ++r)
+#pragma unroll
+            for (int e = 0; e < EPV; ++e) acc[r][t] = fmaf(wf[r][e], xf[e], acc[r][t]);
+        }
+      }
+    }
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int t = 0; t < TT; ++t) acc[r][t] = warp_sum(acc[r][t]);
+
+    if (lane == 0) {
+#pragma unroll
+      for (int r = 0; r < R; ++r) {
+        const int row = row0 + r;
+        if (row >= a.n_rows) continue;
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          if (t >= a.tcount) continue;
+          const int tg = a.t0 + t;
+          float v = acc[r][t];
+          if (a.resid) {
+            if (a.b1) v += Elem<EL>::load((const EL*)a.b1, (int64_t)m * d + row);
+            const float s = v / (1.f + expf(-v));                 // SiLU
+            v = xs[t * d + row] + s;                              // residual: x0 is h
+          }
+          a.out[(int64_t)tg * a.out_tok_stride + (int64_t)m * a.out_mat_stride + row] = v;
+        }
+      }
+    }
+  }
+}
+
+// ---- top-k -------------------------------------------------------------------
+
+struct Cand {
+  float v;
+  int i;
+};
+
+__device__ __forceinline__ Cand better(Cand a, Cand b) { return ranks_before(a.v, a.i, b.v, b.i) ? a : b; }
+
+__device__ Cand block_best(Cand c, Cand* red) {
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    Cand other{__shfl_xor_sync(0xffffffffu, c.v, o), __shfl_xor_sync(0xffffffffu, c.i, o)};
+    c = better(c, other);
+  }
+  if (lane == 0) red[warp] = c;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    Cand b = red[0];
+    for (int w = 1; w < kWarps; ++w) b = better(b, red[w]);
+    red[kWarps] = b;
+  }
+  __syncthreads();
+  Cand r = red[kWarps];
+  __syncthreads();
+  return r;
+}
+
+// Candidates of one chunk of one logits row: its `topk` best (value desc, id asc).
+__global__ void __launch_bounds__(kThreads) topk_partial_kernel(const float* __restrict__ logits,
+                                                                int V, int chunk, int topk,
+                                                                Cand* __restrict__ cand) {
+  extern __shared__ unsigned char smem_raw[];
+  float* vals = reinterpret_cast<float*>(smem_raw);
+  unsigned char* taken = smem_raw + (size_t)chunk * sizeof(float);
+  __shared__ Cand red[kWarps + 1];
+  const int row = blockIdx.y, c = blockIdx.x;
+  const int start = c * chunk;
+  const int n = min(chunk, V - start);
+  const float* src = logits + (int64_t)row * V + start;
+  for (int i = threadIdx.x; i < n; i += kThreads) {
+    vals[i] = src[i];
+    taken[i] = 0;
+  }
+  __syncthreads();
+  Cand* out = cand + ((int64_t)row * gridDim.x + c) * topk;
+  for (int r = 0; r < topk; ++r) {
+    Cand best{-FLT_MAX, INT_MAX};
+    bool any = false;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      if (taken[i]) continue;
+      Cand x{vals[i], start + i};
+      if (!any || ranks_before(x.v, x.i, best.v, best.i)) best = x;
+      any = true;
+    }
+    if (!any) best = Cand{-INFINITY, INT_MAX};
+    Cand b = block_best(best, red);
+    if (threadIdx.x == 0) {
+      out[r] = b;
+      if (b.i != INT_MAX) taken[b.i - start] = 1;
+    }
+    __syncthreads();
+  }
+}
+
+// Merge the chunk candidates of one (row t, matrix m); write root (m = 0) or pool.
+__global__ void __launch_bounds__(kThreads) topk_merge_kernel(const Cand* __restrict__ cand,
+                                                              int n_chunks, int topk, int Kp1,
+                                                              int32_t* __restrict__ root,
+                                                              int32_t* __restrict__ pool) {
+  extern __shared__ unsigned char smem_raw[];
+  Cand* c = reinterpret_cast<Cand*>(smem_raw);
+  __shared__ Cand red[kWarps + 1];
+  const int row = blockIdx.x;
+  const int t = row / Kp1, m = row % Kp1;
+  const int n = n_chunks * topk;
+  for (int i = threadIdx.x; i < n; i += kThreads) c[i] = cand[(int64_t)row * n + i];
+  __syncthreads();
+  const int rounds = (m == 0) ? 1 : topk;
+  for (int r = 0; r < rounds; ++r) {
+    Cand best{-INFINITY, INT_MAX};
+    int where = -1;
+    for (int i = threadIdx.x; i < n; i += kThreads) {
+      Cand x = c[i];
+      if (x.i == INT_MAX) continue;
+      if (where < 0 || ranks_before(x.v, x.i, best.v, best.i)) { best = x; where = i; }
+    }
+    Cand b = block_best(best, red);
+    if (where >= 0 && best.i == b.i) c[where].i = INT_MAX;   // ids are unique: exactly one owner
+    if (threadIdx.x == 0) {
+      if (m == 0) root[t] = b.i;
+      else pool[((int64_t)t * (Kp1 - 1) + (m - 1)) * topk + r] = b.i;
+    }
+    __syncthreads();
+  }
+}
+
+template <typename EL, int TT, int R, int U>
+cudaError_t run_gemv(const GemvArgs& a, int n_mats, cudaStream_t st) {
+  const size_t smem = (size_t)TT * a.d * sizeof(float);
+  auto kern = gemv_kernel<EL, TT, R, U>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0, sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) per_sm = 1;
+  const int groups = (a.n_rows + kWarps * R - 1) / (kWarps * R);
+  int gx = (sms * per_sm + n_mats - 1) / n_mats;
+  if (gx > groups) gx = groups;
+  if (gx < 1) gx = 1;
+  kern<<<dim3(gx, n_mats), kThreads, smem, st>>>(a);
+  return cudaGetLastError();
+}
+
+template <typename EL>
+cudaError_t gemv_dispatch(int TT, const GemvArgs& a, int n_mats, cudaStream_t st) {
+  switch (TT) {
+    case 1: return run_gemv<EL, 1, 2, 8>(a, n_mats, st);
+    case 2: return run_gemv<EL, 2, 2, 8>(a, n_mats, st);
+    case 4: return run_gemv<EL, 4, 4, 4>(a, n_mats, st);
+    case 8: return run_gemv<EL, 8, 4, 4>(a, n_mats, st);
+    default: return run_gemv<EL, 16, 4, 4>(a, n_mats, st);
+  }
+}
+
+int pow2_at_least(int x) {
+  int p = 1;
+  while (p < x) p <<= 1;
+  return p;
+}
+
+}  // namespace
+
+HeadsPlan plan_heads(int T, int d, int V, int K, int topk) {
+  HeadsPlan p{};
+  p.T = T; p.d = d; p.V = V; p.K = K; p.topk = topk;
+  const size_t smem_budget = 160 * 1024;
+  int fit = (int)(smem_budget / ((size_t)d * sizeof(float)));
+  if (fit > 16) fit = 16;
+  if (fit < 1) fit = 1;
+  int tpp = T < fit ? T : fit;
+  // round down to a supported tile (1, 2, 4, 8, 16)
+  int tile = 1;
+  while (tile * 2 <= tpp) tile *= 2;
+  p.tokens_per_pass = tile;
+  int chunk = (V + 63) / 64;
+  chunk = (chunk + 255) / 256 * 256;
+  if (chunk < 1024) chunk = 1024;
+  if (chunk > 8192) chunk = 8192;
+  p.chunk = chunk;
+  p.n_chunks = (V + chunk - 1) / chunk;
+  size_t off = 0;
+  p.off_z = off;
+  off = align_up(off + (size_t)T * K * d * sizeof(float), 256);
+  p.off_logits = off;
+  off = align_up(off + (size_t)T * (K + 1) * V * sizeof(float), 256);
+  p.off_cand = off;
+  off = align_up(off + (size_t)T * (K + 1) * p.n_chunks * topk * sizeof(Cand), 256);
+  p.bytes = off;
+  (void)pow2_at_least;
+  return p;
+}
+
+cudaError_t launch_heads(const HeadsPlan& p, const void* h, const void* w1, const void* b1,
+                         const void* w2, int64_t w2_stride, const void* w_lm, medusa_dtype dt,
+                         int32_t* root, int32_t* pool, float* logits_out, void* ws,
+                         cudaStream_t st) {
+  char* base = (char*)ws;
+  float* z = (float*)(base + p.off_z);
+  float* logits = logits_out ? logits_out : (float*)(base + p.off_logits);
+  Cand* cand = (Cand*)(base + p.off_cand);
+  const int d = p.d, V = p.V, K = p.K, T = p.T;
+  const size_t esz = dt == MEDUSA_BF16 ? 2 : 4;
+  cudaError_t e = cudaSuccess;
+  for (int t0 = 0; t0 < T; t0 += p.tokens_per_pass) {
+    const int tc = (T - t0) < p.tokens_per_pass ? (T - t0) : p.tokens_per_pass;
+    // 1. residual block per head: rows i of W1_k, x = h
+    GemvArgs r{};
+    r.w0 = w1;
+    r.w_rest = (const char*)w1 + (size_t)d * d * esz;
+    r.w_rest_stride = (int64_t)d * d;
+    r.n_rows = d; r.d = d;
+    r.x0 = h; r.x0_el = 1; r.x0_tok_stride = d;
+    r.x_rest = nullptr;
+    r.t0 = t0; r.tcount = tc;
+    r.out = z; r.out_tok_stride = (int64_t)K * d; r.out_mat_stride = d;
+    r.resid = 1; r.b1 = b1;
+    if (K > 0) {
+      e = dt == MEDUSA_BF16 ? gemv_dispatch<uint16_t>(p.tokens_per_pass, r, K, st)
+                            : gemv_dispatch<float>(p.tokens_per_pass, r, K, st);
+      if (e != cudaSuccess) return e;
+    }
+    // 2. vocabulary projections: matrix 0 = LM head on h, matrix 1 + k = W2_k on z_k
+    GemvArgs g{};
+    g.w0 = w_lm;
+    g.w_rest = w2;
+    g.w_rest_stride = w2_stride;
+    g.n_rows = V; g.d = d;
+    g.x0 = h; g.x0_el = 1; g.x0_tok_stride = d;
+    g.x_rest = z; g.x_rest_tok_stride = (int64_t)K * d; g.x_rest_mat_stride = d;
+    g.t0 = t0; g.tcount = tc;
+    g.out = logits; g.out_tok_stride = (int64_t)(K + 1) * V; g.out_mat_stride = V;
+    g.resid = 0; g.b1 = nullptr;
+    e = dt == MEDUSA_BF16 ? gemv_dispatch<uint16_t>(p.tokens_per_pass, g, K + 1, st)
+                          : gemv_dispatch<float>(p.tokens_per_pass, g, K + 1, st);
+    if (e != cudaSuccess) return e;
+  }
+  // 3. top-k
+  const size_t smem_p = (size_t)p.chunk * (sizeof(float) + 1);
+  e = cudaFuncSetAttribute(topk_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_p);
+  if (e != cudaSuccess) return e;
+  topk_partial_kernel<<<dim3(p.n_chunks, T * (K + 1)), kThreads, smem_p, st>>>(logits, V, p.chunk,
+                                                                               p.topk, cand);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const size_t smem_m = (size_t)p.n_chunks * p.topk * sizeof(Cand);
+  e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_m);
+  if (e != cudaSuccess) return e;
+  topk_merge_kernel<<<T * (K + 1), kThreads, smem_m, st>>>(cand, p.n_chunks, p.topk, K + 1, root, pool);
+  return cudaGetLastError();
+}
+
+}  // namespace medusa

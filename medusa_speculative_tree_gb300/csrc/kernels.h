@@ -1,0 +1,73 @@
+// Internal launcher declarations shared by the C ABI (medusa_api.cpp) and the
+// kernel translation units.  Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "medusa_gb300.h"
+
+namespace medusa {
+
+// ---- heads + top-k ---------------------------------------------------------
+struct HeadsPlan {
+  int T, d, V, K, topk;
+  int tokens_per_pass;   // tokens whose fp32 x rows fit in shared memory at once
+  int chunk;             // logits per partial top-k CTA
+  int n_chunks;          // ceil(V / chunk)
+  size_t off_z, off_logits, off_cand, bytes;
+};
+HeadsPlan plan_heads(int T, int d, int V, int K, int topk);
+cudaError_t launch_heads(const HeadsPlan& p, const void* h, const void* w1, const void* b1,
+                         const void* w2, int64_t w2_stride, const void* w_lm, medusa_dtype dt,
+                         int32_t* root, int32_t* pool, float* logits_out, void* ws,
+                         cudaStream_t st);
+
+// ---- tree fill ----------------------------------------------------------------
+cudaError_t launch_tree_fill(const medusa_tree_t& t, int B, int K, const int32_t* root,
+                             const int32_t* pool, const int32_t* L, int32_t* tokens,
+                             int32_t* pos, cudaStream_t st);
+
+// ---- tree attention -------------------------------------------------------------
+struct AttnPlan {
+  int B, Hq, Hkv, g, dh, N, D, max_prefix;
+  int path;              // 0 = CUDA-core kernel, 1 = tcgen05 kernel
+  int mt_rows;           // query rows (tree row x group member) per CTA
+  int n_mt;              // ceil(N * g / mt_rows)
+  int key_tile;          // keys per pipeline stage
+  int n_split;           // CTAs along the prefix per (b, kv head, m tile)
+  int chunk;             // prefix keys per split (multiple of key_tile)
+  size_t off_counter, off_part_o, off_part_ml, off_tmap, bytes;
+};
+// Bytes reserved for split-KV ticket counters at the start of the attention workspace.
+constexpr size_t kAttnCounterBytes = 256 * 1024;
+constexpr size_t kAttnMaxUnits = kAttnCounterBytes / sizeof(int);
+AttnPlan plan_attn(const medusa_tree_t& t, int B, int Hq, const medusa_kv_t& c, int max_prefix);
+size_t attn_units(const AttnPlan& p);
+cudaError_t launch_attn(const AttnPlan& p, const medusa_tree_t& t, const void* q,
+                        const void* k_new, const void* v_new, const medusa_kv_t& c,
+                        const int32_t* L, float rope_base, float scale, float* out, float* lse,
+                        int32_t* status, void* ws, cudaStream_t st);
+
+// ---- acceptance -------------------------------------------------------------------
+struct AcceptPlan {
+  int B, V, chunk, n_chunks;
+  size_t off_part, off_guard, bytes;
+};
+AcceptPlan plan_accept(const medusa_tree_t& t, int B, int V);
+cudaError_t launch_accept(const AcceptPlan& p, const medusa_tree_t& t, const void* logits,
+                          medusa_dtype dt, const int32_t* tokens, int mode, float temperature,
+                          float epsilon, float delta, int entropy_guard, int32_t* best_path,
+                          int32_t* accept_len, int32_t* out_tokens, int32_t* out_rows,
+                          int32_t* frontier_row, void* ws, cudaStream_t st);
+
+// ---- compaction -----------------------------------------------------------------------
+cudaError_t launch_kv_compact(const medusa_kv_t& c, const medusa_tree_t& t, int B,
+                              const int32_t* L, const int32_t* accept_len,
+                              const int32_t* out_rows, int32_t* L_out, int32_t* status,
+                              cudaStream_t st);
+
+inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
+
+}  // namespace medusa

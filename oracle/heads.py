@@ -69,25 +69,25 @@ def medusa_heads(h, w1, w2, w_lm, topk: int, b1=None):
     return root, pool, logits
 
 
-def head_logit_rows(h_t, w1, w2, w_lm, rows, b1=None):
+def head_logit_rows(h_t, w1_head, w2_row, lm_row, rows, b1_head=None):
     """Selected logits of one frontier row, for sampled checks at full size.
 
     rows: list of (m, v) with m = 0 for the LM head or 1 + k for Medusa head k.
-    Only the weights those entries touch are read.
+    Weights are fetched through accessors so that only the touched ones are read:
+    w1_head(k) -> [d, d], w2_row(k, v) -> [d], lm_row(v) -> [d], b1_head(k) -> [d].
     """
     h_t = np.asarray(h_t, dtype=np.float64)
     out = np.zeros(len(rows), dtype=np.float64)
     z_cache = {}
     for i, (m, v) in enumerate(rows):
         if m == 0:
-            out[i] = float(np.asarray(w_lm[v], dtype=np.float64) @ h_t)
+            out[i] = float(np.asarray(lm_row(v), dtype=np.float64) @ h_t)
             continue
         k = m - 1
         if k not in z_cache:
-            pre = np.asarray(w1[k], dtype=np.float64) @ h_t
-            if b1 is not None:
-                pre = pre + np.asarray(b1[k], dtype=np.float64)
+            pre = np.asarray(w1_head(k), dtype=np.float64) @ h_t
+            if b1_head is not None:
+                pre = pre + np.asarray(b1_head(k), dtype=np.float64)
             z_cache[k] = h_t + silu(pre)
-        wrow = w2[v] if np.asarray(w2).ndim == 2 else w2[k][v]
-        out[i] = float(np.asarray(wrow, dtype=np.float64) @ z_cache[k])
+        out[i] = float(np.asarray(w2_row(k, v), dtype=np.float64) @ z_cache[k])
     return out

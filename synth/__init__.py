@@ -244,3 +244,21 @@ def plant_argmax(logits: torch.Tensor, pool: np.ndarray, row_depth: np.ndarray,
                     logits[b, u, tok] = torch.tensor(val, dtype=logits.dtype)
                     break
     return logits
+
+
+def random_pool(w: Workload, seed_sub: int = 0):
+    """Seeded stand-in for the heads' output: root [B] and per-head candidate pools
+    [B, K, topk] of distinct token ids (int64, host)."""
+    g = generator(w.seed, "misc", sub=100 + seed_sub)
+    root = torch.randint(0, w.vocab, (w.batch,), generator=g).numpy().astype(np.int64)
+    pool = np.zeros((w.batch, w.n_heads, w.topk), dtype=np.int64)
+    for b in range(w.batch):
+        for k in range(w.n_heads):
+            pool[b, k] = torch.randperm(w.vocab, generator=g)[:w.topk].numpy()
+    return root, pool
+
+
+def small_variant(w: Workload, **kw) -> Workload:
+    """A copy of a workload with some fields replaced (for scaled-down parity cases)."""
+    from dataclasses import replace
+    return replace(w, **kw)

@@ -1,0 +1,116 @@
+"""CPU tests of libmedusa_gb300.so: exported symbols and the host-side template
+construction, compared bit for bit with the oracle.  No GPU calls."""
+import ctypes as C
+import os
+import re
+
+import numpy as np
+import pytest
+
+import synth
+from oracle import tree as otree
+from oracle.round import template_for
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="session")
+def native():
+    from medusa_speculative_tree_gb300 import build, _native
+    build.build()
+    return _native
+
+
+def header_functions():
+    src = open(os.path.join(ROOT, "include", "medusa_gb300.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(medusa_[a-z0-9_]+)\s*\(", src)))
+
+
+def test_every_declared_symbol_is_exported(native):
+    names = header_functions()
+    assert len(names) >= 15
+    lib = C.CDLL(native.LIB_PATH)
+    for n in names:
+        assert hasattr(lib, n), n
+    assert set(names) == set(native.EXPORTED)
+    assert native.lib().medusa_abi_version() == 1
+    assert native.lib().medusa_status_string(-2).decode() == "cache capacity exceeded"
+
+
+def compare(t_nat, t_ora):
+    assert t_nat.n_rows == t_ora.n_rows
+    assert t_nat.max_depth == t_ora.max_depth
+    assert t_nat.n_paths == t_ora.n_paths
+    assert (t_nat.slot == t_ora.slot).all()
+    assert (t_nat.depth == t_ora.depth).all()
+    assert (t_nat.parent == t_ora.parent).all()
+    assert (t_nat.retrieve == t_ora.retrieve).all()
+    N = t_ora.n_rows
+    anc = t_nat.anc
+    for u in range(N):
+        bits = [(int(anc[u, v // 64]) >> (v % 64)) & 1 for v in range(N)]
+        assert bits == list(t_ora.mask[u].astype(int))
+    kids = np.zeros(N, dtype=int)
+    for u in range(1, N):
+        kids[t_ora.parent[u]] += 1
+    assert list(t_nat.internal) == [u for u in range(N) if kids[u] > 0]
+
+
+@pytest.mark.parametrize("name", synth.WORKLOAD_ORDER)
+def test_workload_templates_match_oracle(native, name):
+    from medusa_speculative_tree_gb300.api import Template, medusa_tree_greedy, medusa_tree_regular
+    w = synth.WORKLOADS[name]
+    acc = synth.rank_accuracy(w.n_heads, 10)
+    t_ora = template_for(w.template, w.topk, w.n_heads, acc)
+    if w.template[0] == "regular":
+        paths = medusa_tree_regular(w.template[1])
+        assert paths == otree.regular_paths(w.template[1])
+    else:
+        paths = medusa_tree_greedy(acc[:, :w.template[2]], w.template[1])
+        assert paths == otree.greedy_tree(acc[:, :w.template[2]], w.template[1])
+    compare(Template(paths, w.topk, w.n_heads), t_ora)
+
+
+@pytest.mark.parametrize("seed", range(8))
+def test_random_templates_match_oracle(native, seed):
+    from medusa_speculative_tree_gb300.api import Template
+    rng = np.random.default_rng(100 + seed)
+    topk = int(rng.integers(1, 8))
+    paths = set()
+    for _ in range(int(rng.integers(0, 120))):
+        L = int(rng.integers(1, 6))
+        p = tuple(int(x) for x in rng.integers(0, topk, size=L))
+        for t in range(1, L + 1):
+            paths.add(p[:t])
+    paths = list(paths)
+    rng.shuffle(paths)
+    compare(Template(paths, topk), otree.compile_template(paths, topk))
+
+
+@pytest.mark.parametrize("K,R,budget", [(3, 4, 10), (4, 10, 63), (4, 10, 255), (2, 3, 50)])
+def test_greedy_matches_oracle(native, K, R, budget):
+    from medusa_speculative_tree_gb300.api import medusa_tree_greedy
+    rng = np.random.default_rng(K * 31 + R)
+    acc = np.sort(rng.uniform(0.0, 1.0, size=(K, R)), axis=1)[:, ::-1].copy()
+    assert medusa_tree_greedy(acc, budget) == otree.greedy_tree(acc, budget)
+    acc2 = synth.rank_accuracy(K, R)             # many mathematically tied weights
+    assert medusa_tree_greedy(acc2, budget) == otree.greedy_tree(acc2, budget)
+
+
+@pytest.mark.parametrize("bad", [[(0, 1)], [(0,), (0,)], [(0,), (9,)], [(0,), (0, 0), (0, 0, 0)]])
+def test_compile_rejects(native, bad):
+    from medusa_speculative_tree_gb300.api import Template
+    with pytest.raises(native.MedusaError) as e:
+        Template(bad, topk=4, n_heads=2)
+    assert e.value.status == native.ETEMPLATE
+
+
+def test_root_only_and_limits(native):
+    from medusa_speculative_tree_gb300.api import Template
+    t = Template([], topk=3)
+    assert t.n_rows == 1 and t.n_paths == 1 and list(t.retrieve[0]) == [0]
+    lib = native.lib()
+    assert lib.medusa_tree_greedy(None, 1, 1, 1, None, None) == native.EINVAL
+    out = native.MedusaTree()
+    assert lib.medusa_tree_compile(None, 1, 1, 4, 0, None, 0, C.byref(out)) == native.EINVAL

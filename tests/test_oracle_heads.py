@@ -81,5 +81,5 @@ def test_head_logit_rows_matches_full():
     w_lm = rng.standard_normal((V, d))
     _, _, full = heads.medusa_heads(h, w1, w2, w_lm, topk=3)
     rows = [(0, 3), (1, 7), (2, 39), (2, 0)]
-    got = heads.head_logit_rows(h[0], w1, w2, w_lm, rows)
+    got = heads.head_logit_rows(h[0], lambda k: w1[k], lambda k, v: w2[k, v], lambda v: w_lm[v], rows)
     np.testing.assert_allclose(got, [full[0, m, v] for m, v in rows], rtol=1e-12)
