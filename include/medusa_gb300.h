@@ -221,6 +221,35 @@ medusa_status medusa_tree_attn_verify(const medusa_tree_t *t, int32_t B, int32_t
                                       float *out, float *lse, int32_t *status, void *ws,
                                       size_t ws_bytes, void *stream);
 
+/* Size of the fixed device scratch used by medusa_tree_attn_verify_static. */
+#define MEDUSA_ATTN_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+/* medusa_tree_attn_verify without a workspace argument, for callers that cannot
+ * allocate device memory where they call it: for example a plugin or custom-op
+ * interface that is handed only its input and output pointers, or a serving loop
+ * whose device memory is reserved up front, where a cudaMalloc would fail or would
+ * synchronise the device.  The pages describe no such variant; it exists only for
+ * these callers.
+ *
+ * Arguments and results are those of medusa_tree_attn_verify.  The scratch is a
+ * file-scope device array of MEDUSA_ATTN_STATIC_SCRATCH_BYTES (32 MiB) that every
+ * GPU loading this library holds until the process exits.  A shape whose scratch
+ * would exceed it returns MEDUSA_EWORKSPACE with nothing enqueued; use
+ * medusa_tree_attn_verify with a caller workspace for such shapes.
+ * The call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
+ * routine.  The first call on a device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and caches it; make that first
+ * call before any stream capture.  Each call clears the ticket counters it will use
+ * (one cudaMemsetAsync on `stream`) and otherwise reuses whatever the previous call
+ * left in the array.  All calls share that one array, so calls that can overlap on
+ * the GPU (different streams without ordering between them) race and must not be
+ * issued. */
+medusa_status medusa_tree_attn_verify_static(const medusa_tree_t *t, int32_t B, int32_t n_q_heads,
+                                             const void *q, const void *k_new, const void *v_new,
+                                             const medusa_kv_t *cache, const int32_t *L,
+                                             int32_t max_prefix, float rope_base, float scale,
+                                             float *out, float *lse, int32_t *status, void *stream);
+
 /* ---------------------------------------------------------------------------
  * Round step 4: acceptance
  * ------------------------------------------------------------------------- */

@@ -15,11 +15,13 @@ OK, EINVAL, ECAPACITY, EUNSUPPORTED, ETEMPLATE, ECUDA, EWORKSPACE, EPATH = 0, -1
 F32, BF16 = 0, 1
 GREEDY, TYPICAL = 0, 1
 MAX_ROWS, MAX_DEPTH, MAX_TOPK = 4096, 16, 32
+ATTN_STATIC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 EXPORTED = [
     "medusa_tree_regular", "medusa_tree_greedy", "medusa_tree_bytes", "medusa_tree_compile",
     "medusa_tree_upload", "medusa_heads_topk_workspace", "medusa_heads_topk", "medusa_tree_fill",
-    "medusa_tree_attn_workspace", "medusa_tree_attn_verify", "medusa_tree_accept_workspace",
+    "medusa_tree_attn_workspace", "medusa_tree_attn_verify", "medusa_tree_attn_verify_static",
+    "medusa_tree_accept_workspace",
     "medusa_tree_accept", "medusa_kv_compact", "medusa_status_string", "medusa_abi_version",
 ]
 
@@ -74,6 +76,8 @@ def lib() -> C.CDLL:
         "medusa_tree_attn_workspace": (SZ, [P(MedusaTree), I32, I32, P(MedusaKV), I32]),
         "medusa_tree_attn_verify": (I32, [P(MedusaTree), I32, I32, VP, VP, VP, P(MedusaKV), VP, I32,
                                           F, F, VP, VP, VP, VP, SZ, VP]),
+        "medusa_tree_attn_verify_static": (I32, [P(MedusaTree), I32, I32, VP, VP, VP, P(MedusaKV), VP,
+                                                 I32, F, F, VP, VP, VP, VP]),
         "medusa_tree_accept_workspace": (SZ, [P(MedusaTree), I32, I32]),
         "medusa_tree_accept": (I32, [P(MedusaTree), I32, I32, VP, I32, VP, I32, F, F, F, I32, VP, VP,
                                      VP, VP, VP, VP, SZ, VP]),

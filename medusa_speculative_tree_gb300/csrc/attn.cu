@@ -15,6 +15,8 @@
 // Softmax runs in the log2 domain (scores pre-multiplied by scale * log2 e).
 #include <math.h>
 
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -388,6 +390,34 @@ cudaError_t launch_attn(const AttnPlan& p, const medusa_tree_t& t, const void* q
   const bool bf = c.dtype == MEDUSA_BF16;
   if (p.dh == 128) return bf ? run_simt<uint16_t, 128>(p, a, st) : run_simt<float, 128>(p, a, st);
   return bf ? run_simt<uint16_t, 64>(p, a, st) : run_simt<float, 64>(p, a, st);
+}
+
+// ---- fixed scratch for medusa_tree_attn_verify_static -----------------------------
+// Device memory for callers that cannot allocate: a file-scope array, zero at module
+// load.  Host code must not use the symbol itself as a pointer (on the host it only
+// names the variable); the device address comes from cudaGetSymbolAddress below.
+static __device__ __align__(256) unsigned char g_attn_static_scratch[MEDUSA_ATTN_STATIC_SCRATCH_BYTES];
+
+namespace {
+constexpr int kMaxDevices = 64;
+std::mutex g_static_mu;
+void* g_static_ptr[kMaxDevices] = {};
+}  // namespace
+
+cudaError_t attn_static_scratch(void** ptr) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  if (dev < 0 || dev >= kMaxDevices) return cudaErrorInvalidDevice;
+  std::lock_guard<std::mutex> lock(g_static_mu);
+  if (g_static_ptr[dev] == nullptr) {
+    void* p = nullptr;
+    e = cudaGetSymbolAddress(&p, g_attn_static_scratch);   // with `dev` current
+    if (e != cudaSuccess) return e;
+    g_static_ptr[dev] = p;
+  }
+  *ptr = g_static_ptr[dev];
+  return cudaSuccess;
 }
 
 }  // namespace medusa

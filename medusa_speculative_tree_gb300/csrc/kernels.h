@@ -45,6 +45,9 @@ constexpr size_t kAttnCounterBytes = 256 * 1024;
 constexpr size_t kAttnMaxUnits = kAttnCounterBytes / sizeof(int);
 AttnPlan plan_attn(const medusa_tree_t& t, int B, int Hq, const medusa_kv_t& c, int max_prefix);
 size_t attn_units(const AttnPlan& p);
+// Device address of the fixed scratch array of medusa_tree_attn_verify_static on the
+// current device (looked up once per device, then cached).
+cudaError_t attn_static_scratch(void** ptr);
 cudaError_t launch_attn(const AttnPlan& p, const medusa_tree_t& t, const void* q,
                         const void* k_new, const void* v_new, const medusa_kv_t& c,
                         const int32_t* L, float rope_base, float scale, float* out, float* lse,

@@ -353,6 +353,32 @@ medusa_status medusa_tree_attn_verify(const medusa_tree_t* t, int32_t B, int32_t
                                          lse, status, ws, as_stream(stream)));
 }
 
+// Same computation as medusa_tree_attn_verify, with the scratch taken from a fixed
+// device array instead of a caller workspace, for callers that cannot allocate.
+medusa_status medusa_tree_attn_verify_static(const medusa_tree_t* t, int32_t B, int32_t n_q_heads,
+                                             const void* q, const void* k_new, const void* v_new,
+                                             const medusa_kv_t* cache, const int32_t* L,
+                                             int32_t max_prefix, float rope_base, float scale,
+                                             float* out, float* lse, int32_t* status, void* stream) {
+  if (!tree_ok(t) || !kv_ok(cache) || B < 1 || n_q_heads < 1 || n_q_heads % cache->n_kv_heads ||
+      !q || !k_new || !v_new || !L || !out || !status || max_prefix < 0 ||
+      !(rope_base > 1.0f) || !(scale > 0.0f) || !std::isfinite(scale))
+    return MEDUSA_EINVAL;
+  if (!aligned16(q) || !aligned16(k_new) || !aligned16(v_new) || !aligned16(out)) return MEDUSA_EINVAL;
+  if ((int64_t)max_prefix + t->n_rows > cache->capacity) return MEDUSA_ECAPACITY;
+  const medusa::AttnPlan p = medusa::plan_attn(*t, B, n_q_heads, *cache, max_prefix);
+  if (medusa::attn_units(p) > medusa::kAttnMaxUnits) return MEDUSA_EUNSUPPORTED;
+  if (p.bytes > (size_t)MEDUSA_ATTN_STATIC_SCRATCH_BYTES) return MEDUSA_EWORKSPACE;
+  void* ws = nullptr;
+  if (medusa::attn_static_scratch(&ws) != cudaSuccess) return MEDUSA_ECUDA;
+  // the array keeps the previous call's contents: zero the counters this call uses
+  const size_t counters = medusa::attn_units(p) * sizeof(int);
+  if (cudaMemsetAsync(static_cast<char*>(ws) + p.off_counter, 0, counters, as_stream(stream)) != cudaSuccess)
+    return MEDUSA_ECUDA;
+  return cuda_status(medusa::launch_attn(p, *t, q, k_new, v_new, *cache, L, rope_base, scale, out,
+                                         lse, status, ws, as_stream(stream)));
+}
+
 size_t medusa_tree_accept_workspace(const medusa_tree_t* t, int32_t B, int32_t V) {
   if (!tree_ok(t) || B < 1 || V < 1) return 0;
   return medusa::plan_accept(*t, B, V).bytes;
