@@ -50,6 +50,8 @@ typedef int32_t medusa_status;
 #define MEDUSA_ECUDA        -5   /* a CUDA runtime call failed */
 #define MEDUSA_EWORKSPACE   -6   /* workspace or output buffer too small */
 #define MEDUSA_EPATH        -7   /* per-sequence: accepted path is not a valid tree chain */
+#define MEDUSA_ETIMEOUT     -8   /* per-sequence: a bounded device wait gave up; the sequence's
+                                    outputs are invalid and the workspace must be re-zeroed */
 
 typedef int32_t medusa_dtype;
 #define MEDUSA_F32  0

@@ -11,7 +11,7 @@ import os
 _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmedusa_gb300.so")
 
-OK, EINVAL, ECAPACITY, EUNSUPPORTED, ETEMPLATE, ECUDA, EWORKSPACE, EPATH = 0, -1, -2, -3, -4, -5, -6, -7
+OK, EINVAL, ECAPACITY, EUNSUPPORTED, ETEMPLATE, ECUDA, EWORKSPACE, EPATH, ETIMEOUT = 0, -1, -2, -3, -4, -5, -6, -7, -8
 F32, BF16 = 0, 1
 GREEDY, TYPICAL = 0, 1
 MAX_ROWS, MAX_DEPTH, MAX_TOPK = 4096, 16, 32

@@ -1,24 +1,782 @@
-// tcgen05 tensor-core path of the tree attention prefix pass (bf16 caches).
+// Tree verification attention on tcgen05 tensor cores (bf16 KV cache, head_dim 128).
+//
+// Same decomposition as the CUDA-core kernel in attn.cu (split-KV over the committed
+// prefix, last CTA of a unit merges the splits), written for sm_103a.  Split 0 also
+// streams the N tree rows as extra 64-key tiles, masked by one 64-bit ancestor word
+// per row and tile, so the whole tree block runs on the tensor cores as well:
+//   - one CTA = 128 query rows (tree row x GQA member) = the M of the MMA, one split
+//     of the prefix; 128 threads, thread t owns row t (= TMEM lane t); 2 CTAs per SM;
+//   - K/V tiles of 64 keys stream in by TMA (128-byte swizzle) into a 2-stage ring,
+//     completion tracked by mbarriers;
+//   - operands are fp16: the bf16 K/V tiles are re-encoded in place (bf16 -> fp16 is
+//     exact for |x| in [2^-14, 65504]), the rotated queries and the probabilities P
+//     are rounded to fp16 (10-bit mantissa; bf16's 7 bits would cost ~1.6e-3 relative
+//     error each);
+//   - S = Q K^T (M=128, N=64, K=128) and O_tile = P V (M=128, N=128, K=64) run as
+//     tcgen05.mma with fp32 accumulators in TMEM; one elected thread issues them;
+//   - the online softmax reads S with tcgen05.ld, writes P (fp16) over the K tile it
+//     no longer needs, and accumulates O in registers.
+// Every mbarrier wait is bounded; on timeout the CTA records MEDUSA_ETIMEOUT for the
+// sequence, waits (bounded) for its outstanding copies and MMAs, frees TMEM and exits.
+#include <cuda.h>
+#include <cudaTypedefs.h>
+#include <cuda_fp16.h>
+
+#include <mutex>
+
 #include "common.cuh"
 #include "kernels.h"
 
 namespace medusa {
 
-bool attn_tc_supported(const medusa_tree_t& t, int Hq, const medusa_kv_t& c) {
-  (void)t; (void)Hq; (void)c;
-  return false;
+namespace {
+
+constexpr int kTcThreads = 128;
+constexpr int kTcRows = 128;        // query rows per CTA
+constexpr int kTcKeys = 64;         // keys per tile
+constexpr int kDH = 128;
+constexpr int kHalf = kDH / 2;
+constexpr uint32_t kTmemCols = 256; // S in columns [0, 64), O_tile in [128, 256)
+constexpr uint32_t kTmemS = 0, kTmemO = 128;
+
+constexpr int kQBytes = kTcRows * kDH * 2;       // 2 K-blocks of [128 rows x 128 B]
+constexpr int kKBytes = kTcKeys * kDH * 2;       // 2 K-blocks of [64 rows x 128 B]
+constexpr int kVBytes = kTcKeys * kDH * 2;       // 2 MN-blocks of [64 keys x 128 B]
+constexpr int kStageBytes = kKBytes + kVBytes;
+constexpr int kStages = 2;
+constexpr int kOffQ = 0;
+constexpr int kOffStage = kQBytes;
+constexpr int kOffTable = kOffStage + kStages * kStageBytes;   // rope cos/sin, then barriers
+
+constexpr int kErrTimeout = MEDUSA_ETIMEOUT;
+
+struct TcArgs {
+  medusa_tree_t t;
+  medusa_kv_t c;
+  const uint16_t* q;
+  const uint16_t* k_new;
+  const uint16_t* v_new;
+  const int32_t* L;
+  float* out;
+  float* lse;
+  int32_t* status;
+  int* counter;
+  float* part_o;
+  float* part_ml;
+  int Hq, Hkv, g, n_mt, n_split, chunk;
+  float scale_log2;
+  float th_hi[64], th_lo[64];
+};
+
+// ---- PTX wrappers --------------------------------------------------------------
+
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return (uint32_t)__cvta_generic_to_shared(p);
 }
 
-void attn_tc_plan(AttnPlan& p) { (void)p; }
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes) : "memory");
+}
+
+__device__ __forceinline__ uint64_t global_ns() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Wait for the phase with the given parity to complete; gives up after ~`limit_ns`.
+__device__ __forceinline__ bool mbar_wait(uint32_t bar, uint32_t parity, uint64_t limit_ns = 2000000000ull) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0;; ++it) {
+    uint32_t done;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(done)
+        : "r"(bar), "r"(parity)
+        : "memory");
+    if (done) return true;
+    if ((it & 1023u) == 1023u && global_ns() - t0 > limit_ns) return false;
+  }
+}
+
+__device__ __forceinline__ void tma_load_4d(uint32_t dst, const CUtensorMap* map, int c0, int c1, int c2,
+                                            int c3, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.4d.shared::cluster.global.tile.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4, %5}], [%6];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(c0), "r"(c1), "r"(c2), "r"(c3), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_before() {
+  asm volatile("tcgen05.fence::before_thread_sync;" ::: "memory");
+}
+__device__ __forceinline__ void tc_fence_after() {
+  asm volatile("tcgen05.fence::after_thread_sync;" ::: "memory");
+}
+
+// Shared-memory matrix descriptor, 128-byte swizzle: start address, leading and
+// stride byte offsets (16-byte units), descriptor version 1, layout SWIZZLE_128B.
+__device__ __forceinline__ uint64_t sw128_desc(uint32_t saddr, uint32_t lbo, uint32_t sbo) {
+  uint64_t d = 0;
+  d |= (uint64_t)((saddr & 0x3FFFFu) >> 4);
+  d |= (uint64_t)((lbo >> 4) & 0x3FFFu) << 16;
+  d |= (uint64_t)((sbo >> 4) & 0x3FFFu) << 32;
+  d |= (uint64_t)1 << 46;
+  d |= (uint64_t)2 << 61;
+  return d;
+}
+
+// Instruction descriptor of kind::f16: fp16 A and B, fp32 accumulator, A K-major,
+// B K-major or MN-major, shape M x N.
+__host__ __device__ constexpr uint32_t idesc_f16(int M, int N, bool b_mn_major) {
+  return (1u << 4) | (0u << 7) | (0u << 10) | ((b_mn_major ? 1u : 0u) << 16) |
+         ((uint32_t)(N >> 3) << 17) | ((uint32_t)(M >> 4) << 24);
+}
+
+__device__ __forceinline__ void umma_f16(uint32_t d_tmem, uint64_t adesc, uint64_t bdesc, uint32_t idesc,
+                                         uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], %1, %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "l"(adesc), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+__device__ __forceinline__ void umma_commit(uint32_t bar) {
+  asm volatile("tcgen05.commit.cta_group::1.mbarrier::arrive::one.shared::cluster.b64 [%0];" ::"r"(bar)
+               : "memory");
+}
+
+__device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
+  uint32_t r[32];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x32.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,"
+      "%16,%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31}, [%32];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]),
+        "=r"(r[15]), "=r"(r[16]), "=r"(r[17]), "=r"(r[18]), "=r"(r[19]), "=r"(r[20]), "=r"(r[21]),
+        "=r"(r[22]), "=r"(r[23]), "=r"(r[24]), "=r"(r[25]), "=r"(r[26]), "=r"(r[27]), "=r"(r[28]),
+        "=r"(r[29]), "=r"(r[30]), "=r"(r[31])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 32; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x32.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16,"
+      "%17,%18,%19,%20,%21,%22,%23,%24,%25,%26,%27,%28,%29,%30,%31,%32};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15])), "r"(__float_as_uint(v[16])), "r"(__float_as_uint(v[17])),
+      "r"(__float_as_uint(v[18])), "r"(__float_as_uint(v[19])), "r"(__float_as_uint(v[20])),
+      "r"(__float_as_uint(v[21])), "r"(__float_as_uint(v[22])), "r"(__float_as_uint(v[23])),
+      "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
+      "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
+      "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+__device__ __forceinline__ uint32_t pack_half2(float a, float b) {
+  __half2 h = __floats2half2_rn(a, b);
+  return *reinterpret_cast<uint32_t*>(&h);
+}
+
+// bf16 x8 (uint4) -> fp16 x8 (uint4), exact for normal-range values.
+__device__ __forceinline__ uint4 bf16x8_to_f16x8(uint4 v) {
+  uint4 o;
+  o.x = pack_half2(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u));
+  o.y = pack_half2(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+  o.z = pack_half2(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u));
+  o.w = pack_half2(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u));
+  return o;
+}
+
+__device__ __forceinline__ int64_t row_off_tc(const medusa_kv_t& c, int b, int kvh, int row) {
+  if (c.page_size == 0) return (((int64_t)b * c.n_kv_heads + kvh) * c.capacity + row) * c.head_dim;
+  const int page = c.block_table[(int64_t)b * c.max_blocks + row / c.page_size];
+  return (((int64_t)page * c.n_kv_heads + kvh) * c.page_size + row % c.page_size) * c.head_dim;
+}
+
+// Re-encode one K or V tile (2 blocks of [64 rows x 128 B], bf16) to fp16 in place;
+// rows of keys >= k_valid become zero.
+__device__ __forceinline__ void convert_tile(uint8_t* tile, int k_valid) {
+  uint4* p = reinterpret_cast<uint4*>(tile);
+#pragma unroll
+  for (int i = 0; i < (kKBytes / 16) / kTcThreads; ++i) {
+    const int idx = i * kTcThreads + threadIdx.x;
+    const int row = (idx % (kKBytes / 32)) / 8;      // 16-byte chunks: 8 per row, 512 per block
+    uint4 v = p[idx];
+    p[idx] = row < k_valid ? bf16x8_to_f16x8(v) : make_uint4(0, 0, 0, 0);
+  }
+}
+
+// Tree-row key tile: bf16 -> RoPE at L + depth[v] (fp32) -> fp16, in place.  Row r of
+// the tile is tree row v0 + r; dims i and i + 64 sit in the two blocks at the same
+// swizzled position.  Rows >= n_valid become zero.
+__device__ __forceinline__ void convert_rotate_tile(uint8_t* tile, int n_valid, int v0, const int32_t* depth,
+                                                    const float* tab_c, const float* tab_s) {
+#pragma unroll
+  for (int i = 0; i < (kTcKeys * 8) / kTcThreads; ++i) {
+    const int idx = i * kTcThreads + threadIdx.x;
+    const int row = idx >> 3, c = idx & 7;
+    const int off = row * 128 + ((c ^ (row & 7)) * 16);
+    uint4* p0 = reinterpret_cast<uint4*>(tile + off);
+    uint4* p1 = reinterpret_cast<uint4*>(tile + 8192 + off);
+    if (row < n_valid) {
+      float x1[8], x2[8];
+      Elem<uint16_t>::unpack(*p0, x1);
+      Elem<uint16_t>::unpack(*p1, x2);
+      const int ti = depth[v0 + row] * kHalf + 8 * c;
+      float y1[8], y2[8];
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float cs = tab_c[ti + e], sn = tab_s[ti + e];
+        y1[e] = x1[e] * cs - x2[e] * sn;
+        y2[e] = x2[e] * cs + x1[e] * sn;
+      }
+      *p0 = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]), pack_half2(y1[4], y1[5]),
+                       pack_half2(y1[6], y1[7]));
+      *p1 = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]), pack_half2(y2[4], y2[5]),
+                       pack_half2(y2[6], y2[7]));
+    } else {
+      *p0 = make_uint4(0, 0, 0, 0);
+      *p1 = make_uint4(0, 0, 0, 0);
+    }
+  }
+}
+
+template <bool PAGED>
+__global__ void __launch_bounds__(kTcThreads, 2)
+    attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
+                   const __grid_constant__ CUtensorMap tmKn, const __grid_constant__ CUtensorMap tmVn,
+                   const TcArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+  const medusa_tree_t& t = a.t;
+  const int D = t.max_depth;
+  float* tab_c = reinterpret_cast<float*>(sm + kOffTable);     // [(D+1)][64]
+  float* tab_s = tab_c + (D + 1) * kHalf;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(
+      (reinterpret_cast<uintptr_t>(tab_s + (D + 1) * kHalf) + 7) & ~uintptr_t(7));
+  // bars[0..1] = stage full, bars[2] = S ready, bars[3] = O_tile ready
+  __shared__ uint32_t tmem_slot;
+  __shared__ int flag;                 // ticket result, then error flag
+  __shared__ int err;
+
+  const int mt = blockIdx.x, s = blockIdx.y;
+  const int b = blockIdx.z / a.Hkv, kvh = blockIdx.z % a.Hkv;
+  const int N = t.n_rows, g = a.g, M = N * g;
+  const int tid = threadIdx.x, warp = tid >> 5;
+  const int Lb = a.L[b];
+  const bool first_cta = (s == 0 && mt == 0 && kvh == 0 && tid == 0);
+  if (Lb < 0 || !seq_rows_ok(a.c, b, (int64_t)Lb + N)) {
+    if (first_cta) a.status[b] = MEDUSA_ECAPACITY;
+    return;
+  }
+  if (Lb > a.n_split * a.chunk) {
+    if (first_cta) a.status[b] = MEDUSA_EINVAL;
+    return;
+  }
+  if (first_cta) a.status[b] = MEDUSA_OK;
+
+  const uint32_t sQ = smem_u32(sm + kOffQ);
+  const uint32_t bar_full0 = smem_u32(&bars[0]);
+  const uint32_t bar_s = smem_u32(&bars[2]);
+  const uint32_t bar_o = smem_u32(&bars[3]);
+  if (tid == 0) {
+    mbar_init(bar_full0, 1);
+    mbar_init(bar_full0 + 8, 1);
+    mbar_init(bar_s, 1);
+    mbar_init(bar_o, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    err = 0;
+  }
+  if (warp == 0) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                 "r"(kTmemCols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  for (int idx = tid; idx < (D + 1) * kHalf; idx += kTcThreads) {
+    const int dep = idx / kHalf, i = idx % kHalf;
+    float sn, cs;
+    sincosf(rope_angle(Lb + dep, a.th_hi[i], a.th_lo[i]), &sn, &cs);
+    tab_c[idx] = cs;
+    tab_s[idx] = sn;
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+
+  const int k_begin = s * a.chunk;
+  const int k_end = min(Lb, k_begin + a.chunk);
+  // Tiles: the split's prefix keys, then (split 0 only) the N tree rows, 64 per tile.
+  // A tree tile t covers rows [64t, 64t + 64), exactly ancestor-mask word t.
+  const int n_pre = k_end > k_begin ? (k_end - k_begin + kTcKeys - 1) / kTcKeys : 0;
+  const int n_tree = (s == 0) ? (N + kTcKeys - 1) / kTcKeys : 0;
+  const int n_tiles = n_pre + n_tree;
+
+  auto issue_tile = [&](int j) {
+    const int stage = j & 1;
+    const int k0 = k_begin + j * kTcKeys;
+    const uint32_t bar = bar_full0 + 8 * stage;
+    const uint32_t dK = smem_u32(sm + kOffStage + stage * kStageBytes);
+    const uint32_t dV = dK + kKBytes;
+    if (j >= n_pre) {
+      const int v0 = (j - n_pre) * kTcKeys;
+      mbar_expect_tx(bar, 4 * 8192);
+      tma_load_4d(dK, &tmKn, 0, kvh, v0, b, bar);
+      tma_load_4d(dK + 8192, &tmKn, 64, kvh, v0, b, bar);
+      tma_load_4d(dV, &tmVn, 0, kvh, v0, b, bar);
+      tma_load_4d(dV + 8192, &tmVn, 64, kvh, v0, b, bar);
+    } else if (!PAGED) {
+      mbar_expect_tx(bar, 4 * 8192);
+      tma_load_4d(dK, &tmK, 0, k0, kvh, b, bar);
+      tma_load_4d(dK + 8192, &tmK, 64, k0, kvh, b, bar);
+      tma_load_4d(dV, &tmV, 0, k0, kvh, b, bar);
+      tma_load_4d(dV + 8192, &tmV, 64, k0, kvh, b, bar);
+    } else {
+      const int nk = min(kTcKeys, k_end - k0);
+      const int np = (nk + 15) / 16;
+      mbar_expect_tx(bar, (uint32_t)np * 4 * 2048);
+      for (int p = 0; p < np; ++p) {
+        const int page = a.c.block_table[(int64_t)b * a.c.max_blocks + k0 / 16 + p];
+        tma_load_4d(dK + p * 2048, &tmK, 0, 0, kvh, page, bar);
+        tma_load_4d(dK + 8192 + p * 2048, &tmK, 64, 0, kvh, page, bar);
+        tma_load_4d(dV + p * 2048, &tmV, 0, 0, kvh, page, bar);
+        tma_load_4d(dV + 8192 + p * 2048, &tmV, 64, 0, kvh, page, bar);
+      }
+    }
+  };
+  if (tid == 0) {
+    for (int j = 0; j < n_tiles && j < kStages; ++j) issue_tile(j);
+  }
+
+  // Rotated queries of this tile's rows, fp16, K-major 128-byte swizzle (2 blocks of 64 dims).
+  const int R = mt * kTcRows + tid;
+  const bool row_ok = R < M;
+  const int u = row_ok ? R / g : 0;
+  const int h = kvh * g + (row_ok ? R % g : 0);
+  {
+    const uint16_t* qrow = a.q + (((int64_t)b * N + u) * a.Hq + h) * kDH;
+    const int ti0 = t.depth[u] * kHalf;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {            // dims [8c, 8c+8) and [64+8c, 64+8c+8)
+      uint4 o1 = make_uint4(0, 0, 0, 0), o2 = o1;
+      if (row_ok) {
+        float x1[8], x2[8];
+        Elem<uint16_t>::unpack(*reinterpret_cast<const uint4*>(qrow + 8 * c), x1);
+        Elem<uint16_t>::unpack(*reinterpret_cast<const uint4*>(qrow + kHalf + 8 * c), x2);
+        float y1[8], y2[8];
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float cs = tab_c[ti0 + 8 * c + e], sn = tab_s[ti0 + 8 * c + e];
+          y1[e] = x1[e] * cs - x2[e] * sn;
+          y2[e] = x2[e] * cs + x1[e] * sn;
+        }
+        o1 = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]), pack_half2(y1[4], y1[5]),
+                        pack_half2(y1[6], y1[7]));
+        o2 = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]), pack_half2(y2[4], y2[5]),
+                        pack_half2(y2[6], y2[7]));
+      }
+      const int phys = c ^ (tid & 7);
+      *reinterpret_cast<uint4*>(sm + kOffQ + tid * 128 + phys * 16) = o1;            // dims 0..63
+      *reinterpret_cast<uint4*>(sm + kOffQ + 16384 + tid * 128 + phys * 16) = o2;    // dims 64..127
+    }
+  }
+  // Stage rotated tree keys and tree values at cache rows L + u (split 0 only).
+  if (s == 0 && row_ok && (R % g) == 0) {
+    const int64_t src = (((int64_t)b * N + u) * a.Hkv + kvh) * kDH;
+    const int64_t dst = row_off_tc(a.c, b, kvh, Lb + u);
+    uint16_t* ck = (uint16_t*)a.c.k;
+    uint16_t* cv = (uint16_t*)a.c.v;
+    const int ti0 = t.depth[u] * kHalf;
+    for (int c = 0; c < 8; ++c) {
+      float x1[8], x2[8];
+      Elem<uint16_t>::unpack(*reinterpret_cast<const uint4*>(a.k_new + src + 8 * c), x1);
+      Elem<uint16_t>::unpack(*reinterpret_cast<const uint4*>(a.k_new + src + kHalf + 8 * c), x2);
+      uint32_t y1[4], y2[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float c0 = tab_c[ti0 + 8 * c + 2 * e], s0 = tab_s[ti0 + 8 * c + 2 * e];
+        const float c1 = tab_c[ti0 + 8 * c + 2 * e + 1], s1 = tab_s[ti0 + 8 * c + 2 * e + 1];
+        const uint32_t a0 = f32_to_bf16_bits(x1[2 * e] * c0 - x2[2 * e] * s0);
+        const uint32_t a1 = f32_to_bf16_bits(x1[2 * e + 1] * c1 - x2[2 * e + 1] * s1);
+        const uint32_t b0 = f32_to_bf16_bits(x2[2 * e] * c0 + x1[2 * e] * s0);
+        const uint32_t b1 = f32_to_bf16_bits(x2[2 * e + 1] * c1 + x1[2 * e + 1] * s1);
+        y1[e] = a0 | (a1 << 16);
+        y2[e] = b0 | (b1 << 16);
+      }
+      *reinterpret_cast<uint4*>(ck + dst + 8 * c) = make_uint4(y1[0], y1[1], y1[2], y1[3]);
+      *reinterpret_cast<uint4*>(ck + dst + kHalf + 8 * c) = make_uint4(y2[0], y2[1], y2[2], y2[3]);
+    }
+    for (int c = 0; c < 16; ++c)
+      *reinterpret_cast<uint4*>(cv + dst + 8 * c) = *reinterpret_cast<const uint4*>(a.v_new + src + 8 * c);
+  }
+  fence_proxy_async();
+  __syncthreads();
+
+  // ---- prefix pass ------------------------------------------------------------
+  // O accumulates in TMEM across tiles.  The running max m_run is raised only when a
+  // tile's max exceeds it by more than 2^8 (log2 units); then O and l are rescaled.
+  // Otherwise P = 2^(s - m_run) <= 256, which fp16 and the fp32 accumulators hold
+  // exactly enough; the final normalisation uses the same m_run, so the result is
+  // the same softmax.
+  constexpr uint32_t kIdS = idesc_f16(kTcRows, kTcKeys, false);
+  constexpr uint32_t kIdO = idesc_f16(kTcRows, kDH, true);
+  constexpr float kRescale = 8.f;
+  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+  float m_run = -INFINITY, l_run = 0.f;
+  bool ok = true;
+  for (int j = 0; j < n_tiles; ++j) {
+    const int stage = j & 1;
+    uint8_t* tK = sm + kOffStage + stage * kStageBytes;
+    uint8_t* tV = tK + kKBytes;
+    const bool tree_tile = j >= n_pre;
+    const int v0 = (j - n_pre) * kTcKeys;
+    const int k_valid = tree_tile ? N - v0 : k_end - (k_begin + j * kTcKeys);   // rows before the end
+    const uint64_t vis = tree_tile ? (row_ok ? t.anc[(int64_t)u * t.n_words + (j - n_pre)] : 0ull) : 0ull;
+    // every wait outcome is made CTA-uniform, so that no thread leaves the loop alone
+    if (__syncthreads_or(!mbar_wait(bar_full0 + 8 * stage, (j >> 1) & 1))) { ok = false; break; }
+    if (tree_tile) convert_rotate_tile(tK, k_valid, v0, t.depth, tab_c, tab_s);
+    else convert_tile(tK, k_valid);
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t aK = smem_u32(tK);
+#pragma unroll
+      for (int kk = 0; kk < kDH / 16; ++kk) {
+        const uint64_t ad = sw128_desc(sQ + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024);
+        const uint64_t bd = sw128_desc(aK + (kk / 4) * 8192 + (kk % 4) * 32, 16, 1024);
+        umma_f16(tmem + kTmemS, ad, bd, kIdS, kk > 0 ? 1u : 0u);
+      }
+      umma_commit(bar_s);
+    }
+    convert_tile(tV, k_valid);
+    fence_proxy_async();
+    if (__syncthreads_or(!mbar_wait(bar_s, j & 1))) { ok = false; break; }
+    tc_fence_after();
+    // softmax of row tid over this tile's 64 keys
+    float sv[kTcKeys];
+    tmem_ld32(tmem + lane_base + kTmemS, sv);
+    tmem_ld32(tmem + lane_base + kTmemS + 32, sv + 32);
+    float mx = -INFINITY;
+#pragma unroll
+    for (int c = 0; c < kTcKeys; ++c) {
+      const bool keep = tree_tile ? ((vis >> c) & 1ull) != 0 : c < k_valid;
+      sv[c] = keep ? sv[c] * a.scale_log2 : -INFINITY;
+      mx = fmaxf(mx, sv[c]);
+    }
+    // The TMEM accesses of a rescale are warp-collective (.sync.aligned): the warp
+    // rescales when any of its rows needs it, the other rows scale by 1.
+    const bool first = (m_run == -INFINITY);
+    const bool need = !first && (mx > m_run + kRescale);
+    if (first) m_run = mx;                           // O holds nothing yet for this row
+    if (__any_sync(0xffffffffu, need)) {
+      const float alpha = need ? exp2f(m_run - mx) : 1.f;
+      l_run *= alpha;
+#pragma unroll
+      for (int q4 = 0; q4 < kDH / 32; ++q4) {
+        float ov[32];
+        tmem_ld32(tmem + lane_base + kTmemO + 32 * q4, ov);
+#pragma unroll
+        for (int i = 0; i < 32; ++i) ov[i] *= alpha;
+        tmem_st32(tmem + lane_base + kTmemO + 32 * q4, ov);
+      }
+      if (need) m_run = mx;
+    }
+    float psum = 0.f;
+#pragma unroll
+    for (int c = 0; c < kTcKeys; ++c) {
+      const float p = (sv[c] != -INFINITY) ? exp2f(sv[c] - m_run) : 0.f;
+      sv[c] = p;
+      psum += p;
+    }
+    l_run += psum;
+    // P (fp16) over the consumed K tile: one block of [128 rows x 128 B], swizzled
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      const uint4 v = make_uint4(pack_half2(sv[8 * c], sv[8 * c + 1]), pack_half2(sv[8 * c + 2], sv[8 * c + 3]),
+                                 pack_half2(sv[8 * c + 4], sv[8 * c + 5]), pack_half2(sv[8 * c + 6], sv[8 * c + 7]));
+      *reinterpret_cast<uint4*>(tK + tid * 128 + ((c ^ (tid & 7)) * 16)) = v;
+    }
+    fence_proxy_async();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0) {
+      tc_fence_after();
+      const uint32_t aP = smem_u32(tK), aV = smem_u32(tV);
+#pragma unroll
+      for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+        const uint64_t ad = sw128_desc(aP + kk * 32, 16, 1024);
+        const uint64_t bd = sw128_desc(aV + kk * 2048, 8192, 1024);   // MN-major: dim blocks 8 KiB apart
+        umma_f16(tmem + kTmemO, ad, bd, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+      }
+      umma_commit(bar_o);
+    }
+    if (__syncthreads_or(!mbar_wait(bar_o, j & 1))) { ok = false; break; }
+    tc_fence_after();
+    tc_fence_before();
+    __syncthreads();
+    if (tid == 0 && j + kStages < n_tiles) issue_tile(j + kStages);
+  }
+  if (!ok) {
+    // Give up: record the error, drain what this CTA may still have in flight (bounded).
+    if (tid == 0) {
+      atomicExch(&a.status[b], kErrTimeout);
+      mbar_wait(bar_s, 0, 100000000ull);
+      mbar_wait(bar_o, 0, 100000000ull);
+      mbar_wait(bar_full0, 0, 100000000ull);
+      mbar_wait(bar_full0 + 8, 0, 100000000ull);
+    }
+    tc_fence_before();
+    __syncthreads();
+    if (warp == 0) {
+      tc_fence_after();
+      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    }
+    return;
+  }
+  float o[kDH];
+  if (n_tiles > 0) {
+#pragma unroll
+    for (int q4 = 0; q4 < kDH / 32; ++q4) tmem_ld32(tmem + lane_base + kTmemO + 32 * q4, o + 32 * q4);
+  } else {
+#pragma unroll
+    for (int i = 0; i < kDH; ++i) o[i] = 0.f;
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 0) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+
+  // ---- split partial, ticket ------------------------------------------------------
+  const int unit = (b * a.Hkv + kvh) * a.n_mt + mt;
+  const int64_t prow = ((int64_t)unit * a.n_split + s) * kTcRows + tid;
+  if (row_ok) {
+    float4* dst = reinterpret_cast<float4*>(a.part_o + prow * kDH);
+#pragma unroll
+    for (int i = 0; i < kDH / 4; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
+    a.part_ml[prow * 2] = m_run;
+    a.part_ml[prow * 2 + 1] = l_run;
+  }
+  __threadfence();
+  __syncthreads();
+  if (tid == 0) flag = (atomicAdd(&a.counter[unit], 1) == a.n_split - 1);
+  __syncthreads();
+  if (!flag) return;
+  if (tid == 0) a.counter[unit] = 0;
+  __threadfence();
+
+  // ---- last CTA: merge the splits (the tree block came with split 0) --------------
+  // Per-row weights 2^(m_s - M) first (thread per row), then warps over rows and lanes
+  // over dims read each split's partial rows with coalesced 16-byte loads.
+  float* wsm = reinterpret_cast<float*>(sm);                  // [128][n_split]
+  float* inv_l = wsm + kTcRows * a.n_split;                   // [128]
+  if (row_ok) {
+    float Mx = -INFINITY;
+    for (int s2 = 0; s2 < a.n_split; ++s2)
+      Mx = fmaxf(Mx, __ldcg(&a.part_ml[(((int64_t)unit * a.n_split + s2) * kTcRows + tid) * 2]));
+    float l = 0.f;
+    for (int s2 = 0; s2 < a.n_split; ++s2) {
+      const int64_t pr = ((int64_t)unit * a.n_split + s2) * kTcRows + tid;
+      const float ms = __ldcg(&a.part_ml[pr * 2]);
+      const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - Mx);
+      l = fmaf(__ldcg(&a.part_ml[pr * 2 + 1]), w, l);
+      wsm[tid * a.n_split + s2] = w;
+    }
+    inv_l[tid] = 1.f / l;
+    if (a.lse) a.lse[((int64_t)b * N + u) * a.Hq + h] = (Mx + log2f(l)) * kLn2;
+  }
+  __syncthreads();
+  const int lane = tid & 31;
+  for (int r = warp; r < kTcRows; r += kTcThreads / 32) {
+    const int Rr = mt * kTcRows + r;
+    if (Rr >= M) break;
+    const int ur = Rr / g, hr = kvh * g + Rr % g;
+    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll 4
+    for (int s2 = 0; s2 < a.n_split; ++s2) {
+      const float w = wsm[r * a.n_split + s2];
+      const float4 v = __ldcg(reinterpret_cast<const float4*>(
+                                  a.part_o + (((int64_t)unit * a.n_split + s2) * kTcRows + r) * kDH) + lane);
+      acc.x = fmaf(v.x, w, acc.x);
+      acc.y = fmaf(v.y, w, acc.y);
+      acc.z = fmaf(v.z, w, acc.z);
+      acc.w = fmaf(v.w, w, acc.w);
+    }
+    const float il = inv_l[r];
+    reinterpret_cast<float4*>(a.out + (((int64_t)b * N + ur) * a.Hq + hr) * kDH)[lane] =
+        make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
+  }
+}
+
+// ---- host side --------------------------------------------------------------------
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* p = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &p, 12000, cudaEnableDefault, &q) ==
+            cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(p);
+  });
+  return fn;
+}
+
+bool encode_kv_map(CUtensorMap* map, void* base, const medusa_kv_t& c, int B) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[4], strides[3];
+  cuuint32_t box[4], estr[4] = {1, 1, 1, 1};
+  const cuuint64_t row = (cuuint64_t)c.head_dim * 2;
+  if (c.page_size == 0) {
+    dims[0] = c.head_dim; dims[1] = c.capacity; dims[2] = c.n_kv_heads; dims[3] = B;
+    strides[0] = row; strides[1] = row * c.capacity; strides[2] = row * c.capacity * c.n_kv_heads;
+    box[0] = 64; box[1] = kTcKeys; box[2] = 1; box[3] = 1;
+  } else {
+    dims[0] = c.head_dim; dims[1] = c.page_size; dims[2] = c.n_kv_heads; dims[3] = c.n_pages;
+    strides[0] = row; strides[1] = row * c.page_size; strides[2] = row * c.page_size * c.n_kv_heads;
+    box[0] = 64; box[1] = c.page_size; box[2] = 1; box[3] = 1;
+  }
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, base, dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// Tree rows k_new / v_new [B][N][Hkv][dh] as a 4-D tensor (dh, Hkv, N, B); a box is
+// 64 dims of 64 consecutive tree rows of one KV head.
+bool encode_tree_map(CUtensorMap* map, const void* base, int B, int N, int Hkv) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  const cuuint64_t row = (cuuint64_t)kDH * 2;
+  cuuint64_t dims[4] = {(cuuint64_t)kDH, (cuuint64_t)Hkv, (cuuint64_t)N, (cuuint64_t)B};
+  cuuint64_t strides[3] = {row, row * Hkv, row * Hkv * N};
+  cuuint32_t box[4] = {64, 1, (cuuint32_t)kTcKeys, 1}, estr[4] = {1, 1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
+                  CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+                  CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+size_t tc_smem_bytes(int D) {
+  return 1024 + kOffTable + (size_t)2 * (D + 1) * kHalf * sizeof(float) + 64;
+}
+
+}  // namespace
+
+bool attn_tc_supported(const medusa_tree_t& t, int Hq, const medusa_kv_t& c) {
+  (void)t;
+  (void)Hq;
+  return c.dtype == MEDUSA_BF16 && c.head_dim == kDH && (c.page_size == 0 || c.page_size == 16) &&
+         encode_fn() != nullptr;
+}
+
+// Split choice: enough CTAs to fill the SMs two per SM, in whole waves where possible,
+// while every CTA streams at least rows/16 tiles so that its fp32 partial stays below
+// a quarter of the K/V bytes it reads.
+void attn_tc_plan(AttnPlan& p) {
+  p.mt_rows = kTcRows;
+  p.key_tile = kTcKeys;
+  const int M = p.N * p.g;
+  p.n_mt = (M + kTcRows - 1) / kTcRows;
+  const int units = p.B * p.Hkv * p.n_mt;
+  int sms = 148, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const double slots = 2.0 * sms;
+  const int tiles_unit = (p.max_prefix + kTcKeys - 1) / kTcKeys;
+  const int rows = M < kTcRows ? M : kTcRows;
+  int min_tiles = (rows + 15) / 16;
+  if (min_tiles < 2) min_tiles = 2;
+  int max_split = tiles_unit / min_tiles;
+  if (max_split < 1) max_split = 1;
+  int best = 1;
+  double best_score = -1e9;
+  for (int n = 1; n <= max_split; ++n) {
+    const double waves = units * (double)n / slots;
+    const double eff = waves / std::ceil(waves);
+    const double score = eff - 0.004 * n;
+    if (score > best_score + 1e-9) { best_score = score; best = n; }
+  }
+  int tiles_per = (tiles_unit + best - 1) / best;
+  if (tiles_per < 1) tiles_per = 1;
+  p.chunk = tiles_per * kTcKeys;
+  p.n_split = p.max_prefix > 0 ? (p.max_prefix + p.chunk - 1) / p.chunk : 1;
+}
 
 cudaError_t launch_attn_tc(const AttnPlan& p, const medusa_tree_t& t, const void* q,
                            const void* k_new, const void* v_new, const medusa_kv_t& c,
                            const int32_t* L, const float* th_hi, const float* th_lo,
                            float scale_log2, float* out, float* lse, int32_t* status, void* ws,
                            cudaStream_t st) {
-  (void)p; (void)t; (void)q; (void)k_new; (void)v_new; (void)c; (void)L; (void)th_hi;
-  (void)th_lo; (void)scale_log2; (void)out; (void)lse; (void)status; (void)ws; (void)st;
-  return cudaErrorNotSupported;
+  CUtensorMap mk, mv, mkn, mvn;
+  if (!encode_kv_map(&mk, c.k, c, p.B) || !encode_kv_map(&mv, c.v, c, p.B) ||
+      !encode_tree_map(&mkn, k_new, p.B, t.n_rows, p.Hkv) || !encode_tree_map(&mvn, v_new, p.B, t.n_rows, p.Hkv))
+    return cudaErrorInvalidValue;
+  TcArgs a{};
+  a.t = t;
+  a.c = c;
+  a.q = (const uint16_t*)q;
+  a.k_new = (const uint16_t*)k_new;
+  a.v_new = (const uint16_t*)v_new;
+  a.L = L;
+  a.out = out;
+  a.lse = lse;
+  a.status = status;
+  char* base = (char*)ws;
+  a.counter = (int*)(base + p.off_counter);
+  a.part_o = (float*)(base + p.off_part_o);
+  a.part_ml = (float*)(base + p.off_part_ml);
+  a.Hq = p.Hq;
+  a.Hkv = p.Hkv;
+  a.g = p.g;
+  a.n_mt = p.n_mt;
+  a.n_split = p.n_split;
+  a.chunk = p.chunk;
+  a.scale_log2 = scale_log2;
+  for (int i = 0; i < 64; ++i) {
+    a.th_hi[i] = th_hi[i];
+    a.th_lo[i] = th_lo[i];
+  }
+  const size_t smem = tc_smem_bytes(p.D);
+  dim3 grid(p.n_mt, p.n_split, p.B * p.Hkv);
+  cudaError_t e;
+  if (c.page_size == 0) {
+    e = cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attn_tc_kernel<false><<<grid, kTcThreads, smem, st>>>(mk, mv, mkn, mvn, a);
+  } else {
+    e = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    attn_tc_kernel<true><<<grid, kTcThreads, smem, st>>>(mk, mv, mkn, mvn, a);
+  }
+  return cudaGetLastError();
 }
 
 }  // namespace medusa

@@ -104,6 +104,7 @@ const char* medusa_status_string(medusa_status s) {
     case MEDUSA_ECUDA: return "CUDA runtime error";
     case MEDUSA_EWORKSPACE: return "workspace or output buffer too small";
     case MEDUSA_EPATH: return "accepted path is not a valid tree chain";
+    case MEDUSA_ETIMEOUT: return "a bounded device wait gave up";
     default: return "unknown status";
   }
 }
