@@ -340,6 +340,11 @@ AttnPlan plan_attn(const medusa_tree_t& t, int B, int Hq, const medusa_kv_t& c, 
     p.chunk = tiles_per * kSimtKT;
     p.n_split = max_prefix > 0 ? (max_prefix + p.chunk - 1) / p.chunk : 1;
   }
+  if (p.path == 1) {            // the tensor-core path merges through DSMEM: no scratch
+    p.off_counter = p.off_part_o = p.off_part_ml = p.off_tmap = 0;
+    p.bytes = 256;
+    return p;
+  }
   const size_t units = (size_t)B * p.Hkv * p.n_mt;
   // The ticket counters live in a fixed region at the start of the workspace that
   // nothing else ever writes: the last CTA of each unit resets its counter, so the

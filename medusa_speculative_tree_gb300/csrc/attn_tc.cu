@@ -1,9 +1,11 @@
 // Tree verification attention on tcgen05 tensor cores (bf16 KV cache, head_dim 128).
 //
-// Same decomposition as the CUDA-core kernel in attn.cu (split-KV over the committed
-// prefix, last CTA of a unit merges the splits), written for sm_103a.  Split 0 also
-// streams the N tree rows as extra 64-key tiles, masked by one 64-bit ancestor word
-// per row and tile, so the whole tree block runs on the tensor cores as well:
+// Split-KV over the committed prefix like the CUDA-core kernel in attn.cu, written for
+// sm_103a.  The splits of one (sequence, KV head, 128-row tile) unit form a thread-block
+// cluster and merge their partials through distributed shared memory, so no partial
+// ever goes to global memory.  Split 0 also streams the N tree rows as extra 64-key
+// tiles, masked by one 64-bit ancestor word per row and tile, so the whole tree block
+// runs on the tensor cores as well:
 //   - one CTA = 128 query rows (tree row x GQA member) = the M of the MMA, one split
 //     of the prefix; 128 threads, thread t owns row t (= TMEM lane t); 2 CTAs per SM;
 //   - K/V tiles of 64 keys stream in by TMA (128-byte swizzle) into a 2-stage ring,
@@ -49,6 +51,7 @@ constexpr int kOffStage = kQBytes;
 constexpr int kOffTable = kOffStage + kStages * kStageBytes;   // rope cos/sin, then barriers
 
 constexpr int kErrTimeout = MEDUSA_ETIMEOUT;
+constexpr int kMaxClusterSplits = 8;   // splits of a unit form one portable cluster
 
 struct TcArgs {
   medusa_tree_t t;
@@ -60,9 +63,6 @@ struct TcArgs {
   float* out;
   float* lse;
   int32_t* status;
-  int* counter;
-  float* part_o;
-  float* part_ml;
   int Hq, Hkv, g, n_mt, n_split, chunk;
   float scale_log2;
   float th_hi[64], th_lo[64];
@@ -193,6 +193,35 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
 
+// 2^x on the MUFU unit (ex2.approx, relative error ~2^-22); 2^-inf = +0.
+__device__ __forceinline__ float fast_exp2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void cluster_sync_all() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\n\tbarrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
+
+// Shared::cluster address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t dsmem_addr(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ float4 ld_dsmem_f4(uint32_t addr) {
+  float4 v;
+  asm volatile("ld.shared::cluster.v4.f32 {%0,%1,%2,%3}, [%4];" : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "r"(addr) : "memory");
+  return v;
+}
+__device__ __forceinline__ float2 ld_dsmem_f2(uint32_t addr) {
+  float2 v;
+  asm volatile("ld.shared::cluster.v2.f32 {%0,%1}, [%2];" : "=f"(v.x), "=f"(v.y) : "r"(addr) : "memory");
+  return v;
+}
+
 __device__ __forceinline__ uint32_t pack_half2(float a, float b) {
   __half2 h = __floats2half2_rn(a, b);
   return *reinterpret_cast<uint32_t*>(&h);
@@ -277,8 +306,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       (reinterpret_cast<uintptr_t>(tab_s + (D + 1) * kHalf) + 7) & ~uintptr_t(7));
   // bars[0..1] = stage full, bars[2] = S ready, bars[3] = O_tile ready
   __shared__ uint32_t tmem_slot;
-  __shared__ int flag;                 // ticket result, then error flag
-  __shared__ int err;
 
   const int mt = blockIdx.x, s = blockIdx.y;
   const int b = blockIdx.z / a.Hkv, kvh = blockIdx.z % a.Hkv;
@@ -306,7 +333,6 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     mbar_init(bar_s, 1);
     mbar_init(bar_o, 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    err = 0;
   }
   if (warp == 0) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
@@ -376,27 +402,30 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const int u = row_ok ? R / g : 0;
   const int h = kvh * g + (row_ok ? R % g : 0);
   {
+    // all 16 global loads first, so that they overlap; then rotate and store
     const uint16_t* qrow = a.q + (((int64_t)b * N + u) * a.Hq + h) * kDH;
     const int ti0 = t.depth[u] * kHalf;
+    uint4 qa[8], qb[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      qa[c] = row_ok ? __ldg(reinterpret_cast<const uint4*>(qrow + 8 * c)) : make_uint4(0, 0, 0, 0);
+      qb[c] = row_ok ? __ldg(reinterpret_cast<const uint4*>(qrow + kHalf + 8 * c)) : make_uint4(0, 0, 0, 0);
+    }
 #pragma unroll
     for (int c = 0; c < 8; ++c) {            // dims [8c, 8c+8) and [64+8c, 64+8c+8)
-      uint4 o1 = make_uint4(0, 0, 0, 0), o2 = o1;
-      if (row_ok) {
-        float x1[8], x2[8];
-        Elem<uint16_t>::unpack(*reinterpret_cast<const uint4*>(qrow + 8 * c), x1);
-        Elem<uint16_t>::unpack(*reinterpret_cast<const uint4*>(qrow + kHalf + 8 * c), x2);
-        float y1[8], y2[8];
+      float x1[8], x2[8], y1[8], y2[8];
+      Elem<uint16_t>::unpack(qa[c], x1);
+      Elem<uint16_t>::unpack(qb[c], x2);
 #pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float cs = tab_c[ti0 + 8 * c + e], sn = tab_s[ti0 + 8 * c + e];
-          y1[e] = x1[e] * cs - x2[e] * sn;
-          y2[e] = x2[e] * cs + x1[e] * sn;
-        }
-        o1 = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]), pack_half2(y1[4], y1[5]),
-                        pack_half2(y1[6], y1[7]));
-        o2 = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]), pack_half2(y2[4], y2[5]),
-                        pack_half2(y2[6], y2[7]));
+      for (int e = 0; e < 8; ++e) {
+        const float cs = tab_c[ti0 + 8 * c + e], sn = tab_s[ti0 + 8 * c + e];
+        y1[e] = x1[e] * cs - x2[e] * sn;
+        y2[e] = x2[e] * cs + x1[e] * sn;
       }
+      const uint4 o1 = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]), pack_half2(y1[4], y1[5]),
+                                  pack_half2(y1[6], y1[7]));
+      const uint4 o2 = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]), pack_half2(y2[4], y2[5]),
+                                  pack_half2(y2[6], y2[7]));
       const int phys = c ^ (tid & 7);
       *reinterpret_cast<uint4*>(sm + kOffQ + tid * 128 + phys * 16) = o1;            // dims 0..63
       *reinterpret_cast<uint4*>(sm + kOffQ + 16384 + tid * 128 + phys * 16) = o2;    // dims 64..127
@@ -409,10 +438,17 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     uint16_t* ck = (uint16_t*)a.c.k;
     uint16_t* cv = (uint16_t*)a.c.v;
     const int ti0 = t.depth[u] * kHalf;
+    uint4 ka[8], kb[8];
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      ka[c] = __ldg(reinterpret_cast<const uint4*>(a.k_new + src + 8 * c));
+      kb[c] = __ldg(reinterpret_cast<const uint4*>(a.k_new + src + kHalf + 8 * c));
+    }
+#pragma unroll
     for (int c = 0; c < 8; ++c) {
       float x1[8], x2[8];
-      Elem<uint16_t>::unpack(*reinterpret_cast<const uint4*>(a.k_new + src + 8 * c), x1);
-      Elem<uint16_t>::unpack(*reinterpret_cast<const uint4*>(a.k_new + src + kHalf + 8 * c), x2);
+      Elem<uint16_t>::unpack(ka[c], x1);
+      Elem<uint16_t>::unpack(kb[c], x2);
       uint32_t y1[4], y2[4];
 #pragma unroll
       for (int e = 0; e < 4; ++e) {
@@ -428,8 +464,11 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       *reinterpret_cast<uint4*>(ck + dst + 8 * c) = make_uint4(y1[0], y1[1], y1[2], y1[3]);
       *reinterpret_cast<uint4*>(ck + dst + kHalf + 8 * c) = make_uint4(y2[0], y2[1], y2[2], y2[3]);
     }
-    for (int c = 0; c < 16; ++c)
-      *reinterpret_cast<uint4*>(cv + dst + 8 * c) = *reinterpret_cast<const uint4*>(a.v_new + src + 8 * c);
+    uint4 vv[16];
+#pragma unroll
+    for (int c = 0; c < 16; ++c) vv[c] = __ldg(reinterpret_cast<const uint4*>(a.v_new + src + 8 * c));
+#pragma unroll
+    for (int c = 0; c < 16; ++c) *reinterpret_cast<uint4*>(cv + dst + 8 * c) = vv[c];
   }
   fence_proxy_async();
   __syncthreads();
@@ -480,20 +519,21 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     float sv[kTcKeys];
     tmem_ld32(tmem + lane_base + kTmemS, sv);
     tmem_ld32(tmem + lane_base + kTmemS + 32, sv + 32);
-    float mx = -INFINITY;
+    float mxp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
     for (int c = 0; c < kTcKeys; ++c) {
       const bool keep = tree_tile ? ((vis >> c) & 1ull) != 0 : c < k_valid;
       sv[c] = keep ? sv[c] * a.scale_log2 : -INFINITY;
-      mx = fmaxf(mx, sv[c]);
+      mxp[c & 3] = fmaxf(mxp[c & 3], sv[c]);
     }
+    const float mx = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
     // The TMEM accesses of a rescale are warp-collective (.sync.aligned): the warp
     // rescales when any of its rows needs it, the other rows scale by 1.
     const bool first = (m_run == -INFINITY);
     const bool need = !first && (mx > m_run + kRescale);
     if (first) m_run = mx;                           // O holds nothing yet for this row
     if (__any_sync(0xffffffffu, need)) {
-      const float alpha = need ? exp2f(m_run - mx) : 1.f;
+      const float alpha = need ? fast_exp2(m_run - mx) : 1.f;
       l_run *= alpha;
 #pragma unroll
       for (int q4 = 0; q4 < kDH / 32; ++q4) {
@@ -505,14 +545,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       }
       if (need) m_run = mx;
     }
-    float psum = 0.f;
+    const float mref = (m_run == -INFINITY) ? 0.f : m_run;   // a fully masked row keeps P = 0
+    float ps[4] = {0.f, 0.f, 0.f, 0.f};
 #pragma unroll
     for (int c = 0; c < kTcKeys; ++c) {
-      const float p = (sv[c] != -INFINITY) ? exp2f(sv[c] - m_run) : 0.f;
+      const float p = fast_exp2(sv[c] - mref);
       sv[c] = p;
-      psum += p;
+      ps[c & 3] += p;
     }
-    l_run += psum;
+    l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
     // P (fp16) over the consumed K tile: one block of [128 rows x 128 B], swizzled
 #pragma unroll
     for (int c = 0; c < 8; ++c) {
@@ -541,7 +582,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     if (tid == 0 && j + kStages < n_tiles) issue_tile(j + kStages);
   }
   if (!ok) {
-    // Give up: record the error, drain what this CTA may still have in flight (bounded).
+    // Give up: record the error, drain what this CTA may still have in flight (bounded),
+    // then still take part in the cluster barriers below.
     if (tid == 0) {
       atomicExch(&a.status[b], kErrTimeout);
       mbar_wait(bar_s, 0, 100000000ull);
@@ -549,88 +591,75 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       mbar_wait(bar_full0, 0, 100000000ull);
       mbar_wait(bar_full0 + 8, 0, 100000000ull);
     }
-    tc_fence_before();
     __syncthreads();
-    if (warp == 0) {
-      tc_fence_after();
-      asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+  }
+  // ---- merge the splits of this unit inside the cluster --------------------------
+  // Every CTA leaves its row partials (O, m, l) in its own shared memory (the Q and
+  // stage buffers are free now), the cluster synchronises, and CTA `s` merges rows
+  // s, s + n_split, ... by reading all splits' partials through distributed shared
+  // memory.  A second cluster barrier keeps every CTA's partials alive until all
+  // readers are done.  Every CTA reaches both barriers on every path.
+  float4* po = reinterpret_cast<float4*>(sm);                  // [128 rows][32] float4, swizzled
+  float2* pml = reinterpret_cast<float2*>(sm + kTcRows * kDH * 4);   // [128] (m, l)
+  if (ok && n_tiles > 0) {
+#pragma unroll
+    for (int q4 = 0; q4 < kDH / 32; ++q4) {
+      float ov[32];
+      tmem_ld32(tmem + lane_base + kTmemO + 32 * q4, ov);
+#pragma unroll
+      for (int i = 0; i < 8; ++i)
+        po[tid * 32 + ((q4 * 8 + i) ^ (tid & 31))] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
     }
-    return;
-  }
-  float o[kDH];
-  if (n_tiles > 0) {
-#pragma unroll
-    for (int q4 = 0; q4 < kDH / 32; ++q4) tmem_ld32(tmem + lane_base + kTmemO + 32 * q4, o + 32 * q4);
   } else {
-#pragma unroll
-    for (int i = 0; i < kDH; ++i) o[i] = 0.f;
+#pragma unroll 4
+    for (int k = 0; k < 32; ++k) po[tid * 32 + k] = make_float4(0.f, 0.f, 0.f, 0.f);
   }
+  pml[tid] = ok ? make_float2(m_run, l_run) : make_float2(-INFINITY, 0.f);
   tc_fence_before();
   __syncthreads();
   if (warp == 0) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
+  cluster_sync_all();
 
-  // ---- split partial, ticket ------------------------------------------------------
-  const int unit = (b * a.Hkv + kvh) * a.n_mt + mt;
-  const int64_t prow = ((int64_t)unit * a.n_split + s) * kTcRows + tid;
-  if (row_ok) {
-    float4* dst = reinterpret_cast<float4*>(a.part_o + prow * kDH);
-#pragma unroll
-    for (int i = 0; i < kDH / 4; ++i) dst[i] = make_float4(o[4 * i], o[4 * i + 1], o[4 * i + 2], o[4 * i + 3]);
-    a.part_ml[prow * 2] = m_run;
-    a.part_ml[prow * 2 + 1] = l_run;
-  }
-  __threadfence();
-  __syncthreads();
-  if (tid == 0) flag = (atomicAdd(&a.counter[unit], 1) == a.n_split - 1);
-  __syncthreads();
-  if (!flag) return;
-  if (tid == 0) a.counter[unit] = 0;
-  __threadfence();
-
-  // ---- last CTA: merge the splits (the tree block came with split 0) --------------
-  // Per-row weights 2^(m_s - M) first (thread per row), then warps over rows and lanes
-  // over dims read each split's partial rows with coalesced 16-byte loads.
-  float* wsm = reinterpret_cast<float*>(sm);                  // [128][n_split]
-  float* inv_l = wsm + kTcRows * a.n_split;                   // [128]
-  if (row_ok) {
-    float Mx = -INFINITY;
-    for (int s2 = 0; s2 < a.n_split; ++s2)
-      Mx = fmaxf(Mx, __ldcg(&a.part_ml[(((int64_t)unit * a.n_split + s2) * kTcRows + tid) * 2]));
-    float l = 0.f;
-    for (int s2 = 0; s2 < a.n_split; ++s2) {
-      const int64_t pr = ((int64_t)unit * a.n_split + s2) * kTcRows + tid;
-      const float ms = __ldcg(&a.part_ml[pr * 2]);
-      const float w = (ms == -INFINITY) ? 0.f : exp2f(ms - Mx);
-      l = fmaf(__ldcg(&a.part_ml[pr * 2 + 1]), w, l);
-      wsm[tid * a.n_split + s2] = w;
-    }
-    inv_l[tid] = 1.f / l;
-    if (a.lse) a.lse[((int64_t)b * N + u) * a.Hq + h] = (Mx + log2f(l)) * kLn2;
-  }
-  __syncthreads();
   const int lane = tid & 31;
-  for (int r = warp; r < kTcRows; r += kTcThreads / 32) {
+  const int ns = a.n_split;
+  const uint32_t po_base = smem_u32(po), pml_base = smem_u32(pml);
+  for (int r = s + warp * ns; r < kTcRows; r += 4 * ns) {
     const int Rr = mt * kTcRows + r;
     if (Rr >= M) break;
-    const int ur = Rr / g, hr = kvh * g + Rr % g;
+    // (m, l) of split `lane`
+    float2 ml = make_float2(-INFINITY, 0.f);
+    if (lane < ns) ml = ld_dsmem_f2(dsmem_addr(pml_base + r * 8, lane));
+    float Mx = ml.x;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
+    const float w_l = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - Mx);
+    float l = w_l * ml.y;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-    for (int s2 = 0; s2 < a.n_split; ++s2) {
-      const float w = wsm[r * a.n_split + s2];
-      const float4 v = __ldcg(reinterpret_cast<const float4*>(
-                                  a.part_o + (((int64_t)unit * a.n_split + s2) * kTcRows + r) * kDH) + lane);
+    const uint32_t off = po_base + (uint32_t)(r * 32 + (lane ^ (r & 31))) * 16;
+#pragma unroll
+    for (int s2 = 0; s2 < 8; ++s2) {
+      if (s2 >= ns) break;
+      const float w = __shfl_sync(0xffffffffu, w_l, s2);
+      const float4 v = ld_dsmem_f4(dsmem_addr(off, s2));
       acc.x = fmaf(v.x, w, acc.x);
       acc.y = fmaf(v.y, w, acc.y);
       acc.z = fmaf(v.z, w, acc.z);
       acc.w = fmaf(v.w, w, acc.w);
     }
-    const float il = inv_l[r];
-    reinterpret_cast<float4*>(a.out + (((int64_t)b * N + ur) * a.Hq + hr) * kDH)[lane] =
-        make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
+    const float il = 1.f / l;
+    const int ur = Rr / g, hr = kvh * g + Rr % g;
+    if (ok) {
+      reinterpret_cast<float4*>(a.out + (((int64_t)b * N + ur) * a.Hq + hr) * kDH)[lane] =
+          make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
+      if (a.lse && lane == 0) a.lse[((int64_t)b * N + ur) * a.Hq + hr] = (Mx + log2f(l)) * kLn2;
+    }
   }
+  cluster_sync_all();
 }
 
 // ---- host side --------------------------------------------------------------------
@@ -715,6 +744,7 @@ void attn_tc_plan(AttnPlan& p) {
   int min_tiles = (rows + 15) / 16;
   if (min_tiles < 2) min_tiles = 2;
   int max_split = tiles_unit / min_tiles;
+  if (max_split > kMaxClusterSplits) max_split = kMaxClusterSplits;
   if (max_split < 1) max_split = 1;
   int best = 1;
   double best_score = -1e9;
@@ -728,6 +758,10 @@ void attn_tc_plan(AttnPlan& p) {
   if (tiles_per < 1) tiles_per = 1;
   p.chunk = tiles_per * kTcKeys;
   p.n_split = p.max_prefix > 0 ? (p.max_prefix + p.chunk - 1) / p.chunk : 1;
+  if (p.n_split > kMaxClusterSplits) {            // keep the unit in one cluster
+    p.chunk = ((p.max_prefix + kMaxClusterSplits - 1) / kMaxClusterSplits + kTcKeys - 1) / kTcKeys * kTcKeys;
+    p.n_split = (p.max_prefix + p.chunk - 1) / p.chunk;
+  }
 }
 
 cudaError_t launch_attn_tc(const AttnPlan& p, const medusa_tree_t& t, const void* q,
@@ -749,10 +783,7 @@ cudaError_t launch_attn_tc(const AttnPlan& p, const medusa_tree_t& t, const void
   a.out = out;
   a.lse = lse;
   a.status = status;
-  char* base = (char*)ws;
-  a.counter = (int*)(base + p.off_counter);
-  a.part_o = (float*)(base + p.off_part_o);
-  a.part_ml = (float*)(base + p.off_part_ml);
+  (void)ws;                                        // the cluster merge needs no workspace
   a.Hq = p.Hq;
   a.Hkv = p.Hkv;
   a.g = p.g;
@@ -765,17 +796,29 @@ cudaError_t launch_attn_tc(const AttnPlan& p, const medusa_tree_t& t, const void
     a.th_lo[i] = th_lo[i];
   }
   const size_t smem = tc_smem_bytes(p.D);
-  dim3 grid(p.n_mt, p.n_split, p.B * p.Hkv);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(p.n_mt, p.n_split, p.B * p.Hkv);
+  cfg.blockDim = dim3(kTcThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 1;
+  attr[0].val.clusterDim.y = p.n_split;           // the splits of one unit
+  attr[0].val.clusterDim.z = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
   cudaError_t e;
   if (c.page_size == 0) {
     e = cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attn_tc_kernel<false><<<grid, kTcThreads, smem, st>>>(mk, mv, mkn, mvn, a);
+    e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<false>, mk, mv, mkn, mvn, a);
   } else {
     e = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attn_tc_kernel<true><<<grid, kTcThreads, smem, st>>>(mk, mv, mkn, mvn, a);
+    e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<true>, mk, mv, mkn, mvn, a);
   }
+  if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }
 

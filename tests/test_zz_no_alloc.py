@@ -88,9 +88,10 @@ def test_static_scratch_matches_workspace_entry(m, name):
 
 
 def test_static_scratch_refuses_oversized_shapes(m):
-    """A batch whose split partials need more than the fixed 32 MiB is refused up front."""
+    """A batch whose split partials need more than the fixed 32 MiB is refused up front
+    (fp32 caches take the CUDA-core path, whose splits merge through this scratch)."""
     w, t_g, q, k, v, K, V, lengths = _setup(m, "longctx-341", batch=4, prefix_len=64, n_q_heads=64,
-                                            n_kv_heads=16)
+                                            n_kv_heads=16, dtype="f32")
     nat = m.api.nat
     cache = m.KVCache(K, V)
     need = m.medusa_tree_attn_workspace(t_g, w.batch, w.n_q_heads, cache, 64)
