@@ -257,37 +257,59 @@ def time_loop(fn, steps, stream):
     return start.elapsed_time(end)            # ms
 
 
-def stage_times(rd: Round, reps: int, stream, flush):
-    """Per-stage device time (µs, mean) with CUDA events on the launching stream.
-    The L2 is flushed before each stage so that every stage streams from HBM."""
-    names = ["heads", "fill", "attn", "accept", "compact"]
-    tot = {n: 0.0 for n in names}
-    for _ in range(reps):
-        ev = [torch.cuda.Event(enable_timing=True) for _ in range(2 * len(names))]
-        flush()
-        ev[0].record(stream)
-        root, pool = rd.heads()
-        ev[1].record(stream)
-        flush()
-        ev[2].record(stream)
-        tokens, _ = rd.fill(root, pool)
-        ev[3].record(stream)
-        flush()
-        ev[4].record(stream)
-        rd.attn()
-        ev[5].record(stream)
-        flush()
-        ev[6].record(stream)
-        r = rd.accept(tokens)
-        ev[7].record(stream)
-        flush()
-        ev[8].record(stream)
-        rd.compact(r)
-        ev[9].record(stream)
-        ev[9].synchronize()
-        for i, n in enumerate(names):
-            tot[n] += ev[2 * i].elapsed_time(ev[2 * i + 1]) * 1e3
-    return {n: tot[n] / reps for n in names}
+class RoundGraphs:
+    """The round captured as CUDA graphs: one graph of the whole round (the timed step)
+    and one graph per stage (for the per-stage split).  The library's calls are
+    stream-ordered and neither allocate nor synchronise, so they capture as they are;
+    workspaces and outputs are created by the warm-up calls before capture."""
+
+    NAMES = ["heads", "fill", "attn", "accept", "compact"]
+
+    def __init__(self, rd: Round, dev):
+        side = torch.cuda.Stream(dev)
+        side.wait_stream(torch.cuda.current_stream(dev))
+        with torch.cuda.stream(side):
+            for _ in range(3):
+                rd.step()
+        torch.cuda.current_stream(dev).wait_stream(side)
+        torch.cuda.synchronize(dev)
+        self.full = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(self.full):
+            self._keep = rd.step()
+        self.stage = {n: torch.cuda.CUDAGraph() for n in self.NAMES}
+        with torch.cuda.graph(self.stage["heads"]):
+            root, pool = rd.heads()
+        with torch.cuda.graph(self.stage["fill"]):
+            tokens, _ = rd.fill(root, pool)
+        with torch.cuda.graph(self.stage["attn"]):
+            rd.attn()
+        with torch.cuda.graph(self.stage["accept"]):
+            r = rd.accept(tokens)
+        with torch.cuda.graph(self.stage["compact"]):
+            rd.compact(r)
+        self._stage_keep = (root, pool, tokens, r)
+        torch.cuda.synchronize(dev)
+
+    def step(self):
+        self.full.replay()
+
+    def stage_times(self, reps: int, stream, flush):
+        """Per-stage device time (µs, mean), CUDA events on the replay stream, with the
+        L2 flushed before every stage so that each streams its inputs from HBM."""
+        tot = {n: 0.0 for n in self.NAMES}
+        for _ in range(reps):
+            ev = []
+            for n in self.NAMES:
+                flush()
+                a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+                a.record(stream)
+                self.stage[n].replay()
+                b.record(stream)
+                ev.append((n, a, b))
+            ev[-1][2].synchronize()
+            for n, a, b in ev:
+                tot[n] += a.elapsed_time(b) * 1e3
+        return {n: tot[n] / reps for n in self.NAMES}
 
 
 def e2e_loop(rd: Round, steps: int, stream):
@@ -385,7 +407,8 @@ def config_of(w: synth.Workload, rd):
          "medusa_heads": w.n_heads, "hidden": w.hidden, "vocab": w.vocab, "accept": w.accept[0],
          "paged": bool(w.page_size),
          "l2": "inputs larger than L2: each step streams the head weights (>= 1.4 GB) before the KV; "
-               "stage timings flush L2 with a 512 MB write"}
+               "stage timings flush L2 with a 512 MB write",
+         "launch": "each step replays a CUDA graph of the five library calls; e2e calls the API eagerly"}
     if rd is not None:
         c["tree_rows"] = rd.N
     return c
@@ -396,7 +419,7 @@ def config_of(w: synth.Workload, rd):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=400)
+    ap.add_argument("--steps", type=int, default=2000)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--workload", default="vicuna7b-64", choices=synth.WORKLOAD_ORDER)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
@@ -421,17 +444,20 @@ def main():
 
     for _ in range(args.warmup):
         rd.step()
+    graphs = RoundGraphs(rd, dev)
+    for _ in range(args.warmup):
+        graphs.step()
     torch.cuda.synchronize(dev)
     barrier(ws)
     torch.cuda.synchronize(dev)
     with ClockSampler(local) as clk:
-        ms = time_loop(rd.step, args.steps, stream)
+        ms = time_loop(graphs.step, args.steps, stream)
         torch.cuda.synchronize(dev)
     barrier(ws)
     ms_step = max_over_ranks(ms / args.steps, ws, dev)
     us_round = 1e3 * ms_step / ws                      # whole job: ws rounds per step
 
-    stages = stage_times(rd, 20, stream, flush)
+    stages = graphs.stage_times(20, stream, flush)
     hbm, bf16, src = peaks()
     attn_us = stages["attn"]
     attn_gbs = rd.attn_bytes() / (attn_us * 1e-6) / 1e9

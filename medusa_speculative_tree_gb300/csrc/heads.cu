@@ -137,6 +137,132 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(GemvArgs a) {
   }
 }
 
+// ---- bulk-copy streaming GEMV (T <= 2) -------------------------------------------
+// One CTA per SM and matrix slice.  A producer warp streams groups of 8 weight rows,
+// one row segment of up to 8 KiB per consumer warp, with cp.async.bulk into a
+// two-stage shared-memory ring (up to 128 KiB in flight per SM); 8 consumer warps
+// each dot their row segment against the fp32 input rows kept in shared memory.
+// Rows longer than one segment are streamed as several column chunks.
+constexpr int kBulkConsumers = 8;
+constexpr int kBulkThreads = (kBulkConsumers + 1) * 32;
+constexpr int kBulkStages = 2;
+constexpr int kBulkSegBytes = 8192;
+
+template <typename EL, int TT>
+__global__ void __launch_bounds__(kBulkThreads, 1) gemv_bulk_kernel(GemvArgs a, int* __restrict__ err) {
+  extern __shared__ __align__(1024) uint8_t smem_b[];
+  constexpr int EPV = Elem<EL>::kPerVec;
+  constexpr int CW = kBulkSegBytes / (int)sizeof(EL);            // columns per segment
+  const int d = a.d;
+  const int m = blockIdx.y;
+  float* xs = reinterpret_cast<float*>(smem_b);                    // [TT][d]
+  const int x_bytes = ((TT * d * 4) + 1023) & ~1023;
+  uint8_t* ring = smem_b + x_bytes;                                 // [stages][8][CW]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(ring + kBulkStages * kBulkConsumers * kBulkSegBytes);
+  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[kBulkStages]);
+  const EL* W = (const EL*)(m == 0 ? a.w0 : (const void*)((const EL*)a.w_rest +
+                                                          (int64_t)(m - 1) * a.w_rest_stride));
+  for (int tt = 0; tt < TT; ++tt) {
+    const int t = a.t0 + tt;
+    for (int i = threadIdx.x; i < d; i += kBulkThreads) {
+      float v = 0.f;
+      if (tt < a.tcount) {
+        if (m == 0 || a.x_rest == nullptr)
+          v = a.x0_el ? Elem<EL>::load((const EL*)a.x0, (int64_t)t * a.x0_tok_stride + i)
+                      : ((const float*)a.x0)[(int64_t)t * a.x0_tok_stride + i];
+        else
+          v = a.x_rest[(int64_t)t * a.x_rest_tok_stride + (int64_t)(m - 1) * a.x_rest_mat_stride + i];
+      }
+      xs[tt * d + i] = v;
+    }
+  }
+  if (threadIdx.x == 0) {
+    for (int s = 0; s < kBulkStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kBulkConsumers);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int n_chunks = (d + CW - 1) / CW;
+  const int n_groups = (a.n_rows + kBulkConsumers - 1) / kBulkConsumers;
+  const int my_groups = n_groups > (int)blockIdx.x ? (n_groups - 1 - blockIdx.x) / gridDim.x + 1 : 0;
+  const int total = my_groups * n_chunks;
+
+  if (warp == kBulkConsumers) {                      // producer
+    if (lane == 0) {
+      for (int it = 0; it < total; ++it) {
+        const int s = it % kBulkStages, ph = (it / kBulkStages) & 1;
+        if (!mbar_wait(empty0 + 8 * s, ph ^ 1)) { atomicExch(err, 1); break; }
+        const int g = blockIdx.x + (it / n_chunks) * gridDim.x, c = it % n_chunks;
+        const int rows = min(kBulkConsumers, a.n_rows - g * kBulkConsumers);
+        const int cols = min(CW, d - c * CW);
+        const uint32_t bytes = (uint32_t)cols * sizeof(EL);
+        mbar_expect_tx(full0 + 8 * s, bytes * rows);
+        for (int r = 0; r < rows; ++r)
+          bulk_copy_g2s(smem_u32(ring + (s * kBulkConsumers + r) * kBulkSegBytes),
+                        W + (int64_t)(g * kBulkConsumers + r) * d + (int64_t)c * CW, bytes, full0 + 8 * s);
+      }
+    }
+    return;
+  }
+
+  float acc[TT];
+#pragma unroll
+  for (int t = 0; t < TT; ++t) acc[t] = 0.f;
+  for (int it = 0; it < total; ++it) {
+    const int s = it % kBulkStages, ph = (it / kBulkStages) & 1;
+    const bool timed_out = !mbar_wait(full0 + 8 * s, ph);
+    if (__any_sync(0xffffffffu, timed_out)) { if (lane == 0) atomicExch(err, 1); break; }
+    const int g = blockIdx.x + (it / n_chunks) * gridDim.x, c = it % n_chunks;
+    const int row = g * kBulkConsumers + warp;
+    if (row < a.n_rows) {
+      const int cols = min(CW, d - c * CW);
+      const uint8_t* seg = ring + (s * kBulkConsumers + warp) * kBulkSegBytes;
+      const float* xc = xs + c * CW;
+#pragma unroll 4
+      for (int j = lane; j < cols / EPV; j += 32) {
+        float wf[EPV];
+        Elem<EL>::unpack(*reinterpret_cast<const uint4*>(seg + j * 16), wf);
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          const float4* xp = reinterpret_cast<const float4*>(xc + t * d + j * EPV);
+#pragma unroll
+          for (int e4 = 0; e4 < EPV / 4; ++e4) {
+            const float4 x4 = xp[e4];
+            acc[t] = fmaf(wf[4 * e4], x4.x, acc[t]);
+            acc[t] = fmaf(wf[4 * e4 + 1], x4.y, acc[t]);
+            acc[t] = fmaf(wf[4 * e4 + 2], x4.z, acc[t]);
+            acc[t] = fmaf(wf[4 * e4 + 3], x4.w, acc[t]);
+          }
+        }
+      }
+    }
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);      // this warp is done with the stage
+    if (c == n_chunks - 1) {
+#pragma unroll
+      for (int t = 0; t < TT; ++t) acc[t] = warp_sum(acc[t]);
+      if (lane == 0 && row < a.n_rows) {
+#pragma unroll
+        for (int t = 0; t < TT; ++t) {
+          if (t >= a.tcount) continue;
+          float v = acc[t];
+          if (a.resid) {
+            if (a.b1) v += Elem<EL>::load((const EL*)a.b1, (int64_t)m * d + row);
+            v = xs[t * d + row] + v / (1.f + expf(-v));    // h + SiLU(W1 h + b1)
+          }
+          a.out[(int64_t)(a.t0 + t) * a.out_tok_stride + (int64_t)m * a.out_mat_stride + row] = v;
+        }
+      }
+#pragma unroll
+      for (int t = 0; t < TT; ++t) acc[t] = 0.f;
+    }
+  }
+}
+
 // ---- top-k -------------------------------------------------------------------
 
 struct Cand {
@@ -207,7 +333,8 @@ __global__ void __launch_bounds__(kThreads) topk_partial_kernel(const float* __r
 __global__ void __launch_bounds__(kThreads) topk_merge_kernel(const Cand* __restrict__ cand,
                                                               int n_chunks, int topk, int Kp1,
                                                               int32_t* __restrict__ root,
-                                                              int32_t* __restrict__ pool) {
+                                                              int32_t* __restrict__ pool,
+                                                              const int* __restrict__ err) {
   extern __shared__ unsigned char smem_raw[];
   Cand* c = reinterpret_cast<Cand*>(smem_raw);
   __shared__ Cand red[kWarps + 1];
@@ -228,8 +355,9 @@ __global__ void __launch_bounds__(kThreads) topk_merge_kernel(const Cand* __rest
     Cand b = block_best(best, red);
     if (where >= 0 && best.i == b.i) c[where].i = INT_MAX;   // ids are unique: exactly one owner
     if (threadIdx.x == 0) {
-      if (m == 0) root[t] = b.i;
-      else pool[((int64_t)t * (Kp1 - 1) + (m - 1)) * topk + r] = b.i;
+      const int id = *err ? -1 : b.i;               // -1: the weight stream gave up waiting
+      if (m == 0) root[t] = id;
+      else pool[((int64_t)t * (Kp1 - 1) + (m - 1)) * topk + r] = id;
     }
     __syncthreads();
   }
@@ -266,6 +394,35 @@ cudaError_t gemv_dispatch(int TT, const GemvArgs& a, int n_mats, cudaStream_t st
   }
 }
 
+template <typename EL, int TT>
+cudaError_t run_gemv_bulk(const GemvArgs& a, int n_mats, int* err, cudaStream_t st) {
+  const size_t smem = (size_t)((TT * a.d * 4 + 1023) & ~1023) +
+                      (size_t)kBulkStages * kBulkConsumers * kBulkSegBytes + 2 * kBulkStages * sizeof(uint64_t);
+  auto kern = gemv_bulk_kernel<EL, TT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int sms = 0, dev = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  const int groups = (a.n_rows + kBulkConsumers - 1) / kBulkConsumers;
+  int gx = sms / n_mats;
+  if (gx < 1) gx = 1;
+  if (gx > groups) gx = groups;
+  kern<<<dim3(gx, n_mats), kBulkThreads, smem, st>>>(a, err);
+  return cudaGetLastError();
+}
+
+// T <= 2 and an input row that fits next to the ring: the bulk-copy kernel; else the
+// register-blocked kernel.
+template <typename EL>
+cudaError_t gemv_any(int TT, const GemvArgs& a, int n_mats, int* err, cudaStream_t st) {
+  if (TT <= 2 && (size_t)TT * a.d * 4 <= 64 * 1024) {
+    return TT == 1 ? run_gemv_bulk<EL, 1>(a, n_mats, err, st) : run_gemv_bulk<EL, 2>(a, n_mats, err, st);
+  }
+  return gemv_dispatch<EL>(TT, a, n_mats, st);
+}
+
+
 int pow2_at_least(int x) {
   int p = 1;
   while (p < x) p <<= 1;
@@ -299,6 +456,8 @@ HeadsPlan plan_heads(int T, int d, int V, int K, int topk) {
   off = align_up(off + (size_t)T * (K + 1) * V * sizeof(float), 256);
   p.off_cand = off;
   off = align_up(off + (size_t)T * (K + 1) * p.n_chunks * topk * sizeof(Cand), 256);
+  p.off_err = off;
+  off = align_up(off + sizeof(int), 256);
   p.bytes = off;
   (void)pow2_at_least;
   return p;
@@ -312,7 +471,10 @@ cudaError_t launch_heads(const HeadsPlan& p, const void* h, const void* w1, cons
   float* z = (float*)(base + p.off_z);
   float* logits = logits_out ? logits_out : (float*)(base + p.off_logits);
   Cand* cand = (Cand*)(base + p.off_cand);
+  int* err = (int*)(base + p.off_err);
   const int d = p.d, V = p.V, K = p.K, T = p.T;
+  cudaError_t e0 = cudaMemsetAsync(err, 0, sizeof(int), st);   // set by a weight-stream wait that gave up
+  if (e0 != cudaSuccess) return e0;
   const size_t esz = dt == MEDUSA_BF16 ? 2 : 4;
   cudaError_t e = cudaSuccess;
   for (int t0 = 0; t0 < T; t0 += p.tokens_per_pass) {
@@ -329,8 +491,8 @@ cudaError_t launch_heads(const HeadsPlan& p, const void* h, const void* w1, cons
     r.out = z; r.out_tok_stride = (int64_t)K * d; r.out_mat_stride = d;
     r.resid = 1; r.b1 = b1;
     if (K > 0) {
-      e = dt == MEDUSA_BF16 ? gemv_dispatch<uint16_t>(p.tokens_per_pass, r, K, st)
-                            : gemv_dispatch<float>(p.tokens_per_pass, r, K, st);
+      e = dt == MEDUSA_BF16 ? gemv_any<uint16_t>(p.tokens_per_pass, r, K, err, st)
+                            : gemv_any<float>(p.tokens_per_pass, r, K, err, st);
       if (e != cudaSuccess) return e;
     }
     // 2. vocabulary projections: matrix 0 = LM head on h, matrix 1 + k = W2_k on z_k
@@ -344,8 +506,8 @@ cudaError_t launch_heads(const HeadsPlan& p, const void* h, const void* w1, cons
     g.t0 = t0; g.tcount = tc;
     g.out = logits; g.out_tok_stride = (int64_t)(K + 1) * V; g.out_mat_stride = V;
     g.resid = 0; g.b1 = nullptr;
-    e = dt == MEDUSA_BF16 ? gemv_dispatch<uint16_t>(p.tokens_per_pass, g, K + 1, st)
-                          : gemv_dispatch<float>(p.tokens_per_pass, g, K + 1, st);
+    e = dt == MEDUSA_BF16 ? gemv_any<uint16_t>(p.tokens_per_pass, g, K + 1, err, st)
+                          : gemv_any<float>(p.tokens_per_pass, g, K + 1, err, st);
     if (e != cudaSuccess) return e;
   }
   // 3. top-k
@@ -358,7 +520,7 @@ cudaError_t launch_heads(const HeadsPlan& p, const void* h, const void* w1, cons
   const size_t smem_m = (size_t)p.n_chunks * p.topk * sizeof(Cand);
   e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_m);
   if (e != cudaSuccess) return e;
-  topk_merge_kernel<<<T * (K + 1), kThreads, smem_m, st>>>(cand, p.n_chunks, p.topk, K + 1, root, pool);
+  topk_merge_kernel<<<T * (K + 1), kThreads, smem_m, st>>>(cand, p.n_chunks, p.topk, K + 1, root, pool, err);
   return cudaGetLastError();
 }
 

@@ -16,7 +16,7 @@ struct HeadsPlan {
   int tokens_per_pass;   // tokens whose fp32 x rows fit in shared memory at once
   int chunk;             // logits per partial top-k CTA
   int n_chunks;          // ceil(V / chunk)
-  size_t off_z, off_logits, off_cand, bytes;
+  size_t off_z, off_logits, off_cand, off_err, bytes;
 };
 HeadsPlan plan_heads(int T, int d, int V, int K, int topk);
 cudaError_t launch_heads(const HeadsPlan& p, const void* h, const void* w1, const void* b1,
