@@ -339,6 +339,7 @@ AttnPlan plan_attn(const medusa_tree_t& t, int B, int Hq, const medusa_kv_t& c, 
     if (tiles_per < 1) tiles_per = 1;
     p.chunk = tiles_per * kSimtKT;
     p.n_split = max_prefix > 0 ? (max_prefix + p.chunk - 1) / p.chunk : 1;
+    p.first = p.chunk;
   }
   if (p.path == 1) {            // the tensor-core path merges through DSMEM: no scratch
     p.off_counter = p.off_part_o = p.off_part_ml = p.off_tmap = 0;

@@ -5,21 +5,29 @@
 // cluster and merge their partials through distributed shared memory, so no partial
 // ever goes to global memory.  Split 0 also streams the N tree rows as extra 64-key
 // tiles, masked by one 64-bit ancestor word per row and tile, so the whole tree block
-// runs on the tensor cores as well:
-//   - one CTA = 128 query rows (tree row x GQA member) = the M of the MMA, one split
-//     of the prefix; 128 threads, thread t owns row t (= TMEM lane t); 2 CTAs per SM;
-//   - K/V tiles of 64 keys stream in by TMA (128-byte swizzle) into a 2-stage ring,
-//     completion tracked by mbarriers;
-//   - operands are fp16: the bf16 K/V tiles are re-encoded in place (bf16 -> fp16 is
-//     exact for |x| in [2^-14, 65504]), the rotated queries and the probabilities P
-//     are rounded to fp16 (10-bit mantissa; bf16's 7 bits would cost ~1.6e-3 relative
-//     error each);
-//   - S = Q K^T (M=128, N=64, K=128) and O_tile = P V (M=128, N=128, K=64) run as
-//     tcgen05.mma with fp32 accumulators in TMEM; one elected thread issues them;
-//   - the online softmax reads S with tcgen05.ld, writes P (fp16) over the K tile it
-//     no longer needs, and accumulates O in registers.
-// Every mbarrier wait is bounded; on timeout the CTA records MEDUSA_ETIMEOUT for the
-// sequence, waits (bounded) for its outstanding copies and MMAs, frees TMEM and exits.
+// runs on the tensor cores as well.
+//
+// One CTA = 128 query rows (tree row x GQA member, the M of the MMA) and one split of
+// the prefix, 2 CTAs per SM.  Its eight warps are specialised and run as a pipeline
+// coupled by mbarriers, so loading, converting, multiplying and the softmax of
+// successive 64-key tiles overlap:
+//   - warp 4 (one lane): TMA producer, K and V tiles (128-byte swizzle) into a 2-stage
+//     ring;
+//   - warps 6-7: re-encode each landed tile from bf16 to fp16 in place (exact for
+//     |x| in [2^-14, 65504]); tree-row key tiles are rotated (RoPE at L + depth) on
+//     the way;
+//   - warp 5 (one lane): allocates TMEM and issues tcgen05.mma: S = Q K^T (M=128,
+//     N=64, K=128) into one of two TMEM S buffers, then O += P V (M=128, N=128, K=64)
+//     with P read from TMEM and O accumulated in TMEM;
+//   - warps 0-3: thread t owns query row t (= TMEM lane t).  They rotate and stage
+//     the queries, then run the online softmax: read S with tcgen05.ld, write P over
+//     it as fp16 with tcgen05.st, and rescale O in TMEM when the running max grows.
+// Operands are fp16: the rotated queries (pre-multiplied by scale * log2 e, so S comes
+// out in log2 units) and P are rounded to fp16 (10-bit mantissa; bf16's 7 bits would
+// cost ~1.6e-3 relative error each).
+// Every mbarrier wait is bounded and also ends when another role has given up; then
+// the CTA records MEDUSA_ETIMEOUT for the sequence, waits (bounded) for its
+// outstanding copies and MMAs, frees TMEM and still joins the cluster barriers.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
@@ -33,13 +41,18 @@ namespace medusa {
 
 namespace {
 
-constexpr int kTcThreads = 128;
+constexpr int kTcThreads = 256;
+constexpr int kSoftWarps = 4;       // warps 0-3: one thread per query row
+constexpr int kProdWarp = 4;        // TMA producer
+constexpr int kMmaWarp = 5;         // TMEM owner and MMA issuer
+constexpr int kConvWarp0 = 6;       // warps 6-7: tile conversion
+constexpr int kConvThreads = 64;
 constexpr int kTcRows = 128;        // query rows per CTA
 constexpr int kTcKeys = 64;         // keys per tile
 constexpr int kDH = 128;
 constexpr int kHalf = kDH / 2;
-constexpr uint32_t kTmemCols = 256; // S in columns [0, 64), O_tile in [128, 256)
-constexpr uint32_t kTmemS = 0, kTmemO = 128;
+constexpr uint32_t kTmemCols = 256; // S buffers in columns [0, 64) and [64, 128), O in [128, 256)
+constexpr uint32_t kTmemO = 128;
 
 constexpr int kQBytes = kTcRows * kDH * 2;       // 2 K-blocks of [128 rows x 128 B]
 constexpr int kKBytes = kTcKeys * kDH * 2;       // 2 K-blocks of [64 rows x 128 B]
@@ -49,6 +62,18 @@ constexpr int kStages = 2;
 constexpr int kOffQ = 0;
 constexpr int kOffStage = kQBytes;
 constexpr int kOffTable = kOffStage + kStages * kStageBytes;   // rope cos/sin, then barriers
+constexpr int kNumBars = 16;
+
+// barrier slots
+constexpr int kBarFull = 0;      // [2] stage landed (TMA transaction bytes)
+constexpr int kBarConvK = 2;     // [2] K tile converted (64 converter arrivals)
+constexpr int kBarConvV = 4;     // [2] V tile converted
+constexpr int kBarEmpty = 6;     // [2] stage consumed by the P V MMA (tcgen05.commit)
+constexpr int kBarSFull = 8;     // [2] S buffer written (tcgen05.commit)
+constexpr int kBarPFull = 10;    // [2] P written over S (one arrival per softmax warp)
+constexpr int kBarODone = 12;    // P V MMA of a tile complete (tcgen05.commit)
+constexpr int kBarQReady = 13;   // queries staged (one arrival per softmax warp)
+constexpr int kBarDrain = 14;    // final commit on the error path
 
 constexpr int kErrTimeout = MEDUSA_ETIMEOUT;
 constexpr int kMaxClusterSplits = 8;   // splits of a unit form one portable cluster
@@ -63,7 +88,7 @@ struct TcArgs {
   float* out;
   float* lse;
   int32_t* status;
-  int Hq, Hkv, g, n_mt, n_split, chunk;
+  int Hq, Hkv, g, n_mt, n_split, chunk, first;
   float scale_log2;
   float th_hi[64], th_lo[64];
 };
@@ -123,6 +148,19 @@ __device__ __forceinline__ void umma_commit(uint32_t bar) {
                : "memory");
 }
 
+// Same MMA with A read from tensor memory (M rows = TMEM lanes, K packed two fp16 per
+// 32-bit column, lower index in the low half).
+__device__ __forceinline__ void umma_f16_ts(uint32_t d_tmem, uint32_t a_tmem, uint64_t bdesc, uint32_t idesc,
+                                            uint32_t accumulate) {
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "setp.ne.b32 p, %4, 0;\n\t"
+      "tcgen05.mma.cta_group::1.kind::f16 [%0], [%1], %2, %3, p;\n\t}" ::"r"(d_tmem),
+      "r"(a_tmem), "l"(bdesc), "r"(idesc), "r"(accumulate)
+      : "memory");
+}
+
+
 __device__ __forceinline__ void tmem_ld32(uint32_t taddr, float* v) {
   uint32_t r[32];
   asm volatile(
@@ -154,6 +192,32 @@ __device__ __forceinline__ void tmem_st32(uint32_t taddr, const float* v) {
       "r"(__float_as_uint(v[24])), "r"(__float_as_uint(v[25])), "r"(__float_as_uint(v[26])),
       "r"(__float_as_uint(v[27])), "r"(__float_as_uint(v[28])), "r"(__float_as_uint(v[29])),
       "r"(__float_as_uint(v[30])), "r"(__float_as_uint(v[31]))
+      : "memory");
+  asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
+}
+
+// 16 columns of this warp's 32 lanes (32-bit each), for the rarely taken O rescale.
+__device__ __forceinline__ void tmem_ld16(uint32_t taddr, float* v) {
+  uint32_t r[16];
+  asm volatile(
+      "tcgen05.ld.sync.aligned.32x32b.x16.b32 {%0,%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15}, [%16];"
+      : "=r"(r[0]), "=r"(r[1]), "=r"(r[2]), "=r"(r[3]), "=r"(r[4]), "=r"(r[5]), "=r"(r[6]), "=r"(r[7]),
+        "=r"(r[8]), "=r"(r[9]), "=r"(r[10]), "=r"(r[11]), "=r"(r[12]), "=r"(r[13]), "=r"(r[14]), "=r"(r[15])
+      : "r"(taddr));
+  asm volatile("tcgen05.wait::ld.sync.aligned;" ::: "memory");
+#pragma unroll
+  for (int i = 0; i < 16; ++i) v[i] = __uint_as_float(r[i]);
+}
+
+__device__ __forceinline__ void tmem_st16(uint32_t taddr, const float* v) {
+  asm volatile(
+      "tcgen05.st.sync.aligned.32x32b.x16.b32 [%0], {%1,%2,%3,%4,%5,%6,%7,%8,%9,%10,%11,%12,%13,%14,%15,%16};" ::"r"(taddr),
+      "r"(__float_as_uint(v[0])), "r"(__float_as_uint(v[1])), "r"(__float_as_uint(v[2])),
+      "r"(__float_as_uint(v[3])), "r"(__float_as_uint(v[4])), "r"(__float_as_uint(v[5])),
+      "r"(__float_as_uint(v[6])), "r"(__float_as_uint(v[7])), "r"(__float_as_uint(v[8])),
+      "r"(__float_as_uint(v[9])), "r"(__float_as_uint(v[10])), "r"(__float_as_uint(v[11])),
+      "r"(__float_as_uint(v[12])), "r"(__float_as_uint(v[13])), "r"(__float_as_uint(v[14])),
+      "r"(__float_as_uint(v[15]))
       : "memory");
   asm volatile("tcgen05.wait::st.sync.aligned;" ::: "memory");
 }
@@ -208,16 +272,36 @@ __device__ __forceinline__ int64_t row_off_tc(const medusa_kv_t& c, int b, int k
   return (((int64_t)page * c.n_kv_heads + kvh) * c.page_size + row % c.page_size) * c.head_dim;
 }
 
+
+// Wait for a phase; gives up (false) after ~2 s or as soon as another role of the CTA
+// has set the abort flag.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if ((it & 255u) == 255u && global_ns() - t0 > 2000000000ull) return false;
+  }
+}
+
 // Re-encode one K or V tile (2 blocks of [64 rows x 128 B], bf16) to fp16 in place;
-// rows of keys >= k_valid become zero.
-__device__ __forceinline__ void convert_tile(uint8_t* tile, int k_valid) {
+// rows of keys >= k_valid become zero.  Thread ct of the 64 converter threads.
+__device__ __forceinline__ void convert_tile(uint8_t* tile, int k_valid, int ct) {
   uint4* p = reinterpret_cast<uint4*>(tile);
-#pragma unroll
-  for (int i = 0; i < (kKBytes / 16) / kTcThreads; ++i) {
-    const int idx = i * kTcThreads + threadIdx.x;
-    const int row = (idx % (kKBytes / 32)) / 8;      // 16-byte chunks: 8 per row, 512 per block
-    uint4 v = p[idx];
-    p[idx] = row < k_valid ? bf16x8_to_f16x8(v) : make_uint4(0, 0, 0, 0);
+  constexpr int kIter = (kKBytes / 16) / kConvThreads;
+  if (k_valid >= kTcKeys) {
+#pragma unroll 8
+    for (int i = 0; i < kIter; ++i) {
+      const int idx = i * kConvThreads + ct;
+      p[idx] = bf16x8_to_f16x8(p[idx]);
+    }
+  } else {
+#pragma unroll 8
+    for (int i = 0; i < kIter; ++i) {
+      const int idx = i * kConvThreads + ct;
+      const int row = (idx % (kKBytes / 32)) / 8;      // 16-byte chunks: 8 per row, 512 per block
+      p[idx] = row < k_valid ? bf16x8_to_f16x8(p[idx]) : make_uint4(0, 0, 0, 0);
+    }
   }
 }
 
@@ -225,10 +309,10 @@ __device__ __forceinline__ void convert_tile(uint8_t* tile, int k_valid) {
 // the tile is tree row v0 + r; dims i and i + 64 sit in the two blocks at the same
 // swizzled position.  Rows >= n_valid become zero.
 __device__ __forceinline__ void convert_rotate_tile(uint8_t* tile, int n_valid, int v0, const int32_t* depth,
-                                                    const float* tab_c, const float* tab_s) {
-#pragma unroll
-  for (int i = 0; i < (kTcKeys * 8) / kTcThreads; ++i) {
-    const int idx = i * kTcThreads + threadIdx.x;
+                                                    const float* tab_c, const float* tab_s, int ct) {
+#pragma unroll 2
+  for (int i = 0; i < (kTcKeys * 8) / kConvThreads; ++i) {
+    const int idx = i * kConvThreads + ct;
     const int row = idx >> 3, c = idx & 7;
     const int off = row * 128 + ((c ^ (row & 7)) * 16);
     uint4* p0 = reinterpret_cast<uint4*>(tile + off);
@@ -237,7 +321,7 @@ __device__ __forceinline__ void convert_rotate_tile(uint8_t* tile, int n_valid, 
       float x1[8], x2[8];
       Elem<uint16_t>::unpack(*p0, x1);
       Elem<uint16_t>::unpack(*p1, x2);
-      const int ti = depth[v0 + row] * kHalf + 8 * c;
+      const int ti = __ldg(depth + v0 + row) * kHalf + 8 * c;
       float y1[8], y2[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -256,6 +340,7 @@ __device__ __forceinline__ void convert_rotate_tile(uint8_t* tile, int n_valid, 
   }
 }
 
+
 template <bool PAGED>
 __global__ void __launch_bounds__(kTcThreads, 2)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
@@ -269,37 +354,63 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   float* tab_s = tab_c + (D + 1) * kHalf;
   uint64_t* bars = reinterpret_cast<uint64_t*>(
       (reinterpret_cast<uintptr_t>(tab_s + (D + 1) * kHalf) + 7) & ~uintptr_t(7));
-  // bars[0..1] = stage full, bars[2] = S ready, bars[3] = O_tile ready
   __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
 
   const int mt = blockIdx.x, s = blockIdx.y;
   const int b = blockIdx.z / a.Hkv, kvh = blockIdx.z % a.Hkv;
   const int N = t.n_rows, g = a.g, M = N * g;
-  const int tid = threadIdx.x, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Lb = a.L[b];
   const bool first_cta = (s == 0 && mt == 0 && kvh == 0 && tid == 0);
   if (Lb < 0 || !seq_rows_ok(a.c, b, (int64_t)Lb + N)) {
     if (first_cta) a.status[b] = MEDUSA_ECAPACITY;
     return;
   }
-  if (Lb > a.n_split * a.chunk) {
+  if (Lb > a.first + (a.n_split - 1) * a.chunk) {
     if (first_cta) a.status[b] = MEDUSA_EINVAL;
     return;
   }
   if (first_cta) a.status[b] = MEDUSA_OK;
 
-  const uint32_t sQ = smem_u32(sm + kOffQ);
-  const uint32_t bar_full0 = smem_u32(&bars[0]);
-  const uint32_t bar_s = smem_u32(&bars[2]);
-  const uint32_t bar_o = smem_u32(&bars[3]);
+  // Rows of this tile.  A softmax warp whose 32 rows all lie past the end is idle.
+  const int rows_valid = min(kTcRows, M - mt * kTcRows);
+  const bool soft = warp < kSoftWarps;
+  const bool live = soft && warp * 32 < rows_valid;            // warp-uniform
+  const int R = mt * kTcRows + tid;
+  const bool row_ok = soft && R < M;
+  const int u = row_ok ? R / g : 0;
+  const int h = kvh * g + (row_ok ? R % g : 0);
+
+  // Query loads first, so they are not queued behind the K/V stream.
+  uint4 qa[8], qb[8];
+  if (live) {
+    const uint16_t* qrow = a.q + (((int64_t)b * N + u) * a.Hq + h) * kDH;
+#pragma unroll
+    for (int c = 0; c < 8; ++c) {
+      qa[c] = row_ok ? __ldg(reinterpret_cast<const uint4*>(qrow + 8 * c)) : make_uint4(0, 0, 0, 0);
+      qb[c] = row_ok ? __ldg(reinterpret_cast<const uint4*>(qrow + kHalf + 8 * c)) : make_uint4(0, 0, 0, 0);
+    }
+  }
+
+  const uint32_t bar0 = smem_u32(bars);
+  auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
   if (tid == 0) {
-    mbar_init(bar_full0, 1);
-    mbar_init(bar_full0 + 8, 1);
-    mbar_init(bar_s, 1);
-    mbar_init(bar_o, 1);
+    abort_flag = 0;
+    for (int st = 0; st < kStages; ++st) {
+      mbar_init(BAR(kBarFull + st), 1);
+      mbar_init(BAR(kBarConvK + st), kConvThreads);
+      mbar_init(BAR(kBarConvV + st), kConvThreads);
+      mbar_init(BAR(kBarEmpty + st), 1);
+      mbar_init(BAR(kBarSFull + st), 1);
+      mbar_init(BAR(kBarPFull + st), kSoftWarps);
+    }
+    mbar_init(BAR(kBarODone), 1);
+    mbar_init(BAR(kBarQReady), kSoftWarps);
+    mbar_init(BAR(kBarDrain), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
                  "r"(kTmemCols)
                  : "memory");
@@ -316,284 +427,358 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
+  const volatile int* abortp = &abort_flag;
 
-  const int k_begin = s * a.chunk;
-  const int k_end = min(Lb, k_begin + a.chunk);
+  // Keys of this split: split 0 takes the first a.first prefix keys (fewer than the
+  // others, because it also runs the tree tiles), split s > 0 the a.chunk keys after.
+  const int k_begin = s == 0 ? 0 : a.first + (s - 1) * a.chunk;
+  const int k_end = min(Lb, k_begin + (s == 0 ? a.first : a.chunk));
   // Tiles: the split's prefix keys, then (split 0 only) the N tree rows, 64 per tile.
   // A tree tile t covers rows [64t, 64t + 64), exactly ancestor-mask word t.
   const int n_pre = k_end > k_begin ? (k_end - k_begin + kTcKeys - 1) / kTcKeys : 0;
   const int n_tree = (s == 0) ? (N + kTcKeys - 1) / kTcKeys : 0;
   const int n_tiles = n_pre + n_tree;
-
-  auto issue_tile = [&](int j) {
-    const int stage = j & 1;
-    const int k0 = k_begin + j * kTcKeys;
-    const uint32_t bar = bar_full0 + 8 * stage;
-    const uint32_t dK = smem_u32(sm + kOffStage + stage * kStageBytes);
-    const uint32_t dV = dK + kKBytes;
-    if (j >= n_pre) {
-      const int v0 = (j - n_pre) * kTcKeys;
-      mbar_expect_tx(bar, 4 * 8192);
-      tma_load_4d(dK, &tmKn, 0, kvh, v0, b, bar);
-      tma_load_4d(dK + 8192, &tmKn, 64, kvh, v0, b, bar);
-      tma_load_4d(dV, &tmVn, 0, kvh, v0, b, bar);
-      tma_load_4d(dV + 8192, &tmVn, 64, kvh, v0, b, bar);
-    } else if (!PAGED) {
-      mbar_expect_tx(bar, 4 * 8192);
-      tma_load_4d(dK, &tmK, 0, k0, kvh, b, bar);
-      tma_load_4d(dK + 8192, &tmK, 64, k0, kvh, b, bar);
-      tma_load_4d(dV, &tmV, 0, k0, kvh, b, bar);
-      tma_load_4d(dV + 8192, &tmV, 64, k0, kvh, b, bar);
-    } else {
-      const int nk = min(kTcKeys, k_end - k0);
-      const int np = (nk + 15) / 16;
-      mbar_expect_tx(bar, (uint32_t)np * 4 * 2048);
-      for (int p = 0; p < np; ++p) {
-        const int page = a.c.block_table[(int64_t)b * a.c.max_blocks + k0 / 16 + p];
-        tma_load_4d(dK + p * 2048, &tmK, 0, 0, kvh, page, bar);
-        tma_load_4d(dK + 8192 + p * 2048, &tmK, 64, 0, kvh, page, bar);
-        tma_load_4d(dV + p * 2048, &tmV, 0, 0, kvh, page, bar);
-        tma_load_4d(dV + 8192 + p * 2048, &tmV, 64, 0, kvh, page, bar);
-      }
-    }
+  auto tile_valid = [&](int j) -> int {        // rows of tile j before the end of its range
+    return j >= n_pre ? N - (j - n_pre) * kTcKeys : k_end - (k_begin + j * kTcKeys);
   };
-  if (tid == 0) {
-    for (int j = 0; j < n_tiles && j < kStages; ++j) issue_tile(j);
-  }
 
-  // Rotated queries of this tile's rows, fp16, K-major 128-byte swizzle (2 blocks of 64 dims).
-  const int R = mt * kTcRows + tid;
-  const bool row_ok = R < M;
-  const int u = row_ok ? R / g : 0;
-  const int h = kvh * g + (row_ok ? R % g : 0);
-  {
-    // all 16 global loads first, so that they overlap; then rotate and store
-    const uint16_t* qrow = a.q + (((int64_t)b * N + u) * a.Hq + h) * kDH;
-    const int ti0 = t.depth[u] * kHalf;
-    uint4 qa[8], qb[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      qa[c] = row_ok ? __ldg(reinterpret_cast<const uint4*>(qrow + 8 * c)) : make_uint4(0, 0, 0, 0);
-      qb[c] = row_ok ? __ldg(reinterpret_cast<const uint4*>(qrow + kHalf + 8 * c)) : make_uint4(0, 0, 0, 0);
-    }
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {            // dims [8c, 8c+8) and [64+8c, 64+8c+8)
-      float x1[8], x2[8], y1[8], y2[8];
-      Elem<uint16_t>::unpack(qa[c], x1);
-      Elem<uint16_t>::unpack(qb[c], x2);
-#pragma unroll
-      for (int e = 0; e < 8; ++e) {
-        const float cs = tab_c[ti0 + 8 * c + e], sn = tab_s[ti0 + 8 * c + e];
-        y1[e] = x1[e] * cs - x2[e] * sn;
-        y2[e] = x2[e] * cs + x1[e] * sn;
-      }
-      const uint4 o1 = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]), pack_half2(y1[4], y1[5]),
-                                  pack_half2(y1[6], y1[7]));
-      const uint4 o2 = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]), pack_half2(y2[4], y2[5]),
-                                  pack_half2(y2[6], y2[7]));
-      const int phys = c ^ (tid & 7);
-      *reinterpret_cast<uint4*>(sm + kOffQ + tid * 128 + phys * 16) = o1;            // dims 0..63
-      *reinterpret_cast<uint4*>(sm + kOffQ + 16384 + tid * 128 + phys * 16) = o2;    // dims 64..127
-    }
-  }
-  // Stage rotated tree keys and tree values at cache rows L + u (split 0 only).
-  if (s == 0 && row_ok && (R % g) == 0) {
-    const int64_t src = (((int64_t)b * N + u) * a.Hkv + kvh) * kDH;
-    const int64_t dst = row_off_tc(a.c, b, kvh, Lb + u);
-    uint16_t* ck = (uint16_t*)a.c.k;
-    uint16_t* cv = (uint16_t*)a.c.v;
-    const int ti0 = t.depth[u] * kHalf;
-    uint4 ka[8], kb[8];
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      ka[c] = __ldg(reinterpret_cast<const uint4*>(a.k_new + src + 8 * c));
-      kb[c] = __ldg(reinterpret_cast<const uint4*>(a.k_new + src + kHalf + 8 * c));
-    }
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      float x1[8], x2[8];
-      Elem<uint16_t>::unpack(ka[c], x1);
-      Elem<uint16_t>::unpack(kb[c], x2);
-      uint32_t y1[4], y2[4];
-#pragma unroll
-      for (int e = 0; e < 4; ++e) {
-        const float c0 = tab_c[ti0 + 8 * c + 2 * e], s0 = tab_s[ti0 + 8 * c + 2 * e];
-        const float c1 = tab_c[ti0 + 8 * c + 2 * e + 1], s1 = tab_s[ti0 + 8 * c + 2 * e + 1];
-        const uint32_t a0 = f32_to_bf16_bits(x1[2 * e] * c0 - x2[2 * e] * s0);
-        const uint32_t a1 = f32_to_bf16_bits(x1[2 * e + 1] * c1 - x2[2 * e + 1] * s1);
-        const uint32_t b0 = f32_to_bf16_bits(x2[2 * e] * c0 + x1[2 * e] * s0);
-        const uint32_t b1 = f32_to_bf16_bits(x2[2 * e + 1] * c1 + x1[2 * e + 1] * s1);
-        y1[e] = a0 | (a1 << 16);
-        y2[e] = b0 | (b1 << 16);
-      }
-      *reinterpret_cast<uint4*>(ck + dst + 8 * c) = make_uint4(y1[0], y1[1], y1[2], y1[3]);
-      *reinterpret_cast<uint4*>(ck + dst + kHalf + 8 * c) = make_uint4(y2[0], y2[1], y2[2], y2[3]);
-    }
-    uint4 vv[16];
-#pragma unroll
-    for (int c = 0; c < 16; ++c) vv[c] = __ldg(reinterpret_cast<const uint4*>(a.v_new + src + 8 * c));
-#pragma unroll
-    for (int c = 0; c < 16; ++c) *reinterpret_cast<uint4*>(cv + dst + 8 * c) = vv[c];
-  }
-  fence_proxy_async();
-  __syncthreads();
-
-  // ---- prefix pass ------------------------------------------------------------
-  // O accumulates in TMEM across tiles.  The running max m_run is raised only when a
-  // tile's max exceeds it by more than 2^8 (log2 units); then O and l are rescaled.
-  // Otherwise P = 2^(s - m_run) <= 256, which fp16 and the fp32 accumulators hold
-  // exactly enough; the final normalisation uses the same m_run, so the result is
-  // the same softmax.
   constexpr uint32_t kIdS = idesc_f16(kTcRows, kTcKeys, false);
   constexpr uint32_t kIdO = idesc_f16(kTcRows, kDH, true);
-  constexpr float kRescale = 8.f;
-  const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-  float m_run = -INFINITY, l_run = 0.f;
   bool ok = true;
-  for (int j = 0; j < n_tiles; ++j) {
-    const int stage = j & 1;
-    uint8_t* tK = sm + kOffStage + stage * kStageBytes;
-    uint8_t* tV = tK + kKBytes;
-    const bool tree_tile = j >= n_pre;
-    const int v0 = (j - n_pre) * kTcKeys;
-    const int k_valid = tree_tile ? N - v0 : k_end - (k_begin + j * kTcKeys);   // rows before the end
-    const uint64_t vis = tree_tile ? (row_ok ? t.anc[(int64_t)u * t.n_words + (j - n_pre)] : 0ull) : 0ull;
-    // every wait outcome is made CTA-uniform, so that no thread leaves the loop alone
-    if (__syncthreads_or(!mbar_wait(bar_full0 + 8 * stage, (j >> 1) & 1))) { ok = false; break; }
-    if (tree_tile) convert_rotate_tile(tK, k_valid, v0, t.depth, tab_c, tab_s);
-    else convert_tile(tK, k_valid);
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t aK = smem_u32(tK);
+  int n_issued = 0;
+  float m_run = -INFINITY, l_run = 0.f;
+
+
+  if (warp == kProdWarp) {
+    // ---- TMA producer -------------------------------------------------------------
+    if (lane == 0) {
+      for (int j = 0; j < n_tiles; ++j) {
+        const int st = j & 1;
+        if (j >= kStages && !wait_or_abort(BAR(kBarEmpty + st), ((j >> 1) - 1) & 1, abortp)) {
+          ok = false;
+          break;
+        }
+        const uint32_t bar = BAR(kBarFull + st);
+        const uint32_t dK = smem_u32(sm + kOffStage + st * kStageBytes);
+        const uint32_t dV = dK + kKBytes;
+        const int k0 = k_begin + j * kTcKeys;
+        if (j >= n_pre) {
+          const int v0 = (j - n_pre) * kTcKeys;
+          mbar_expect_tx(bar, 4 * 8192);
+          tma_load_4d(dK, &tmKn, 0, kvh, v0, b, bar);
+          tma_load_4d(dK + 8192, &tmKn, 64, kvh, v0, b, bar);
+          tma_load_4d(dV, &tmVn, 0, kvh, v0, b, bar);
+          tma_load_4d(dV + 8192, &tmVn, 64, kvh, v0, b, bar);
+        } else if (!PAGED) {
+          mbar_expect_tx(bar, 4 * 8192);
+          tma_load_4d(dK, &tmK, 0, k0, kvh, b, bar);
+          tma_load_4d(dK + 8192, &tmK, 64, k0, kvh, b, bar);
+          tma_load_4d(dV, &tmV, 0, k0, kvh, b, bar);
+          tma_load_4d(dV + 8192, &tmV, 64, k0, kvh, b, bar);
+        } else {
+          const int nk = min(kTcKeys, k_end - k0);
+          const int np = (nk + 15) / 16;
+          const int32_t* bt = a.c.block_table + (int64_t)b * a.c.max_blocks + k0 / 16;
+          int page[4];
 #pragma unroll
-      for (int kk = 0; kk < kDH / 16; ++kk) {
-        const uint64_t ad = sw128_desc(sQ + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024);
-        const uint64_t bd = sw128_desc(aK + (kk / 4) * 8192 + (kk % 4) * 32, 16, 1024);
-        umma_f16(tmem + kTmemS, ad, bd, kIdS, kk > 0 ? 1u : 0u);
+          for (int p = 0; p < 4; ++p) page[p] = p < np ? __ldg(bt + p) : 0;
+          mbar_expect_tx(bar, (uint32_t)np * 4 * 2048);
+          for (int p = 0; p < np; ++p) {
+            tma_load_4d(dK + p * 2048, &tmK, 0, 0, kvh, page[p], bar);
+            tma_load_4d(dK + 8192 + p * 2048, &tmK, 64, 0, kvh, page[p], bar);
+            tma_load_4d(dV + p * 2048, &tmV, 0, 0, kvh, page[p], bar);
+            tma_load_4d(dV + 8192 + p * 2048, &tmV, 64, 0, kvh, page[p], bar);
+          }
+        }
+        n_issued = j + 1;
       }
-      umma_commit(bar_s);
     }
-    convert_tile(tV, k_valid);
-    fence_proxy_async();
-    if (__syncthreads_or(!mbar_wait(bar_s, j & 1))) { ok = false; break; }
-    tc_fence_after();
-    // softmax of row tid over this tile's 64 keys
-    float sv[kTcKeys];
-    tmem_ld32(tmem + lane_base + kTmemS, sv);
-    tmem_ld32(tmem + lane_base + kTmemS + 32, sv + 32);
-    float mxp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  } else if (warp == kMmaWarp) {
+    // ---- MMA issue: S(j) = Q K_j^T, then O += P(j-1) V(j-1) -----------------------------
+    // S(j) goes to TMEM buffer j & 1, which P(j-2) occupied: it waits for the P V MMA
+    // of tile j - 2.  Every commit covers all MMAs issued before it.
+    if (lane == 0) {
+      const uint32_t sQ = smem_u32(sm + kOffQ);
+      if (!wait_or_abort(BAR(kBarQReady), 0, abortp)) ok = false;
+      for (int j = 0; ok && j <= n_tiles; ++j) {
+        if (j < n_tiles) {
+          const int st = j & 1;
+          if (!wait_or_abort(BAR(kBarConvK + st), (j >> 1) & 1, abortp) ||
+              (j >= 2 && !wait_or_abort(BAR(kBarODone), (j - 2) & 1, abortp))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t aK = smem_u32(sm + kOffStage + st * kStageBytes);
 #pragma unroll
-    for (int c = 0; c < kTcKeys; ++c) {
-      const bool keep = tree_tile ? ((vis >> c) & 1ull) != 0 : c < k_valid;
-      sv[c] = keep ? sv[c] * a.scale_log2 : -INFINITY;
-      mxp[c & 3] = fmaxf(mxp[c & 3], sv[c]);
+          for (int kk = 0; kk < kDH / 16; ++kk) {
+            const uint64_t ad = sw128_desc(sQ + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024);
+            const uint64_t bd = sw128_desc(aK + (kk / 4) * 8192 + (kk % 4) * 32, 16, 1024);
+            umma_f16(tmem + 64u * st, ad, bd, kIdS, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(BAR(kBarSFull + st));
+        }
+        if (j >= 1) {
+          const int jj = j - 1, st = jj & 1;
+          if (!wait_or_abort(BAR(kBarPFull + st), (jj >> 1) & 1, abortp) ||
+              !wait_or_abort(BAR(kBarConvV + st), (jj >> 1) & 1, abortp)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const uint32_t aV = smem_u32(sm + kOffStage + st * kStageBytes + kKBytes);
+#pragma unroll
+          for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+            const uint64_t bd = sw128_desc(aV + kk * 2048, 8192, 1024);   // MN-major: dim blocks 8 KiB apart
+            umma_f16_ts(tmem + kTmemO, tmem + 64u * st + 8u * kk, bd, kIdO, (jj > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(BAR(kBarEmpty + st));
+          umma_commit(BAR(kBarODone));
+        }
+      }
+      // O is final once the last P V MMA has completed.
+      if (ok && n_tiles > 0 && !wait_or_abort(BAR(kBarODone), (n_tiles - 1) & 1, abortp)) ok = false;
     }
-    const float mx = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
-    // The TMEM accesses of a rescale are warp-collective (.sync.aligned): the warp
-    // rescales when any of its rows needs it, the other rows scale by 1.
-    const bool first = (m_run == -INFINITY);
-    const bool need = !first && (mx > m_run + kRescale);
-    if (first) m_run = mx;                           // O holds nothing yet for this row
-    if (__any_sync(0xffffffffu, need)) {
-      const float alpha = need ? fast_exp2(m_run - mx) : 1.f;
-      l_run *= alpha;
+  } else if (warp >= kConvWarp0) {
+    // ---- bf16 -> fp16 conversion (tree keys also rotated) ------------------------------
+    const int ct = tid - kConvWarp0 * 32;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int st = j & 1;
+      uint8_t* tK = sm + kOffStage + st * kStageBytes;
+      uint8_t* tV = tK + kKBytes;
+      const int k_valid = tile_valid(j);
+      if (!wait_or_abort(BAR(kBarFull + st), (j >> 1) & 1, abortp)) {
+        ok = false;
+        break;
+      }
+      if (j >= n_pre) convert_rotate_tile(tK, k_valid, (j - n_pre) * kTcKeys, t.depth, tab_c, tab_s, ct);
+      else convert_tile(tK, k_valid, ct);
+      fence_proxy_async();
+      mbar_arrive(BAR(kBarConvK + st));
+      convert_tile(tV, k_valid, ct);
+      fence_proxy_async();
+      mbar_arrive(BAR(kBarConvV + st));
+    }
+  } else {
+
+    // ---- softmax warps: thread tid owns query row tid (TMEM lane tid) ----------------
+    // Rotated queries, pre-multiplied by scale * log2 e, fp16, K-major 128-byte swizzle
+    // (2 blocks of 64 dims).
+    if (live) {
+      const int ti0 = __ldg(t.depth + u) * kHalf;
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {            // dims [8c, 8c+8) and [64+8c, 64+8c+8)
+        float x1[8], x2[8], y1[8], y2[8];
+        Elem<uint16_t>::unpack(qa[c], x1);
+        Elem<uint16_t>::unpack(qb[c], x2);
+#pragma unroll
+        for (int e = 0; e < 8; ++e) {
+          const float cs = tab_c[ti0 + 8 * c + e], sn = tab_s[ti0 + 8 * c + e];
+          y1[e] = (x1[e] * cs - x2[e] * sn) * a.scale_log2;
+          y2[e] = (x2[e] * cs + x1[e] * sn) * a.scale_log2;
+        }
+        const uint4 o1 = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]), pack_half2(y1[4], y1[5]),
+                                    pack_half2(y1[6], y1[7]));
+        const uint4 o2 = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]), pack_half2(y2[4], y2[5]),
+                                    pack_half2(y2[6], y2[7]));
+        const int phys = c ^ (tid & 7);
+        *reinterpret_cast<uint4*>(sm + kOffQ + tid * 128 + phys * 16) = o1;            // dims 0..63
+        *reinterpret_cast<uint4*>(sm + kOffQ + 16384 + tid * 128 + phys * 16) = o2;    // dims 64..127
+      }
+    }
+    fence_proxy_async();
+    __syncwarp();
+    if (lane == 0) mbar_arrive(BAR(kBarQReady));
+
+    // Stage rotated tree keys and tree values at cache rows L + u (split 0 only).
+    if (s == 0 && row_ok && (R % g) == 0) {
+      const int64_t src = (((int64_t)b * N + u) * a.Hkv + kvh) * kDH;
+      const int64_t dst = row_off_tc(a.c, b, kvh, Lb + u);
+      uint16_t* ck = (uint16_t*)a.c.k;
+      uint16_t* cv = (uint16_t*)a.c.v;
+      const int ti0 = __ldg(t.depth + u) * kHalf;
+      uint4 ka[8], kb[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        ka[c] = __ldg(reinterpret_cast<const uint4*>(a.k_new + src + 8 * c));
+        kb[c] = __ldg(reinterpret_cast<const uint4*>(a.k_new + src + kHalf + 8 * c));
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        float x1[8], x2[8];
+        Elem<uint16_t>::unpack(ka[c], x1);
+        Elem<uint16_t>::unpack(kb[c], x2);
+        uint32_t y1[4], y2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float c0 = tab_c[ti0 + 8 * c + 2 * e], s0 = tab_s[ti0 + 8 * c + 2 * e];
+          const float c1 = tab_c[ti0 + 8 * c + 2 * e + 1], s1 = tab_s[ti0 + 8 * c + 2 * e + 1];
+          const uint32_t a0 = f32_to_bf16_bits(x1[2 * e] * c0 - x2[2 * e] * s0);
+          const uint32_t a1 = f32_to_bf16_bits(x1[2 * e + 1] * c1 - x2[2 * e + 1] * s1);
+          const uint32_t b0 = f32_to_bf16_bits(x2[2 * e] * c0 + x1[2 * e] * s0);
+          const uint32_t b1 = f32_to_bf16_bits(x2[2 * e + 1] * c1 + x1[2 * e + 1] * s1);
+          y1[e] = a0 | (a1 << 16);
+          y2[e] = b0 | (b1 << 16);
+        }
+        *reinterpret_cast<uint4*>(ck + dst + 8 * c) = make_uint4(y1[0], y1[1], y1[2], y1[3]);
+        *reinterpret_cast<uint4*>(ck + dst + kHalf + 8 * c) = make_uint4(y2[0], y2[1], y2[2], y2[3]);
+      }
+      uint4 vv[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) vv[c] = __ldg(reinterpret_cast<const uint4*>(a.v_new + src + 8 * c));
+#pragma unroll
+      for (int c = 0; c < 16; ++c) *reinterpret_cast<uint4*>(cv + dst + 8 * c) = vv[c];
+    }
+
+    // Online softmax.  O accumulates in TMEM across tiles.  The running max m_run is
+    // raised only when a tile's max exceeds it by more than 2^8 (log2 units); then O
+    // and l are rescaled.  Otherwise P = 2^(s - m_run) <= 256, which fp16 and the fp32
+    // accumulators hold exactly enough; the final normalisation uses the same m_run,
+    // so the result is the same softmax.
+    constexpr float kRescale = 8.f;
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    for (int j = 0; j < n_tiles; ++j) {
+      const int sb = j & 1;
+      const bool tree_tile = j >= n_pre;
+      const int k_valid = tile_valid(j);
+      const uint64_t vis = (tree_tile && row_ok) ? __ldg(t.anc + (int64_t)u * t.n_words + (j - n_pre)) : 0ull;
+      // wait outcomes are made warp-uniform: the TMEM accesses below are warp-collective
+      if (!__all_sync(0xffffffffu, wait_or_abort(BAR(kBarSFull + sb), (j >> 1) & 1, abortp))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (live) {
+        float sv[kTcKeys];
+        tmem_ld32(tmem + lane_base + 64u * sb, sv);
+        tmem_ld32(tmem + lane_base + 64u * sb + 32, sv + 32);
+        float mxp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+        if (tree_tile) {
+#pragma unroll
+          for (int c = 0; c < kTcKeys; ++c) {
+            sv[c] = ((vis >> c) & 1ull) ? sv[c] : -INFINITY;
+            mxp[c & 3] = fmaxf(mxp[c & 3], sv[c]);
+          }
+        } else if (k_valid < kTcKeys) {
+#pragma unroll
+          for (int c = 0; c < kTcKeys; ++c) {
+            sv[c] = c < k_valid ? sv[c] : -INFINITY;
+            mxp[c & 3] = fmaxf(mxp[c & 3], sv[c]);
+          }
+        } else {
+#pragma unroll
+          for (int c = 0; c < kTcKeys; ++c) mxp[c & 3] = fmaxf(mxp[c & 3], sv[c]);
+        }
+        const float mx = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
+        // The TMEM accesses of a rescale are warp-collective: the warp rescales when any
+        // of its rows needs it, the other rows scale by 1.  O must hold P V of tile j - 1
+        // first (a row that needs a rescale has seen an earlier tile, so j >= 1).
+        const bool first = (m_run == -INFINITY);
+        const bool need = !first && (mx > m_run + kRescale);
+        if (first) m_run = mx;                           // O holds nothing yet for this row
+        if (__any_sync(0xffffffffu, need)) {
+          if (!__all_sync(0xffffffffu, wait_or_abort(BAR(kBarODone), (j - 1) & 1, abortp))) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          const float alpha = need ? fast_exp2(m_run - mx) : 1.f;
+          l_run *= alpha;
+#pragma unroll 1
+          for (int q8 = 0; q8 < kDH / 16; ++q8) {
+            float ov[16];
+            tmem_ld16(tmem + lane_base + kTmemO + 16 * q8, ov);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[i] *= alpha;
+            tmem_st16(tmem + lane_base + kTmemO + 16 * q8, ov);
+          }
+          if (need) m_run = mx;
+        }
+        const float mref = (m_run == -INFINITY) ? 0.f : m_run;   // a fully masked row keeps P = 0
+        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        float pk[kTcKeys / 2];                   // P as fp16 pairs, key 2i in the low half
+#pragma unroll
+        for (int i = 0; i < kTcKeys / 2; ++i) {
+          const float p0 = fast_exp2(sv[2 * i] - mref), p1 = fast_exp2(sv[2 * i + 1] - mref);
+          ps[(2 * i) & 3] += p0;
+          ps[(2 * i + 1) & 3] += p1;
+          pk[i] = __uint_as_float(pack_half2(p0, p1));
+        }
+        l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        tmem_st32(tmem + lane_base + 64u * sb, pk);
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(kBarPFull + sb));
+    }
+  }
+
+
+  // ---- join ------------------------------------------------------------------------
+  if (!ok) {
+    *const_cast<volatile int*>(abortp) = 1;
+    atomicExch(&a.status[b], kErrTimeout);
+  }
+  __syncthreads();
+  const bool failed = *abortp != 0;
+  if (failed) {
+    // Drain (bounded) what this CTA may still have in flight before its shared memory
+    // and TMEM are reused or released: the last copy into each stage, and all MMAs.
+    if (warp == kProdWarp && lane == 0) {
+      for (int st = 0; st < kStages; ++st) {
+        const int jl = (n_issued - 1 - st) >= 0 ? ((n_issued - 1 - st) & ~1) + st : -1;
+        if (jl >= 0) mbar_wait(BAR(kBarFull + st), (jl >> 1) & 1, 100000000ull);
+      }
+    }
+    if (warp == kMmaWarp && lane == 0) {
+      umma_commit(BAR(kBarDrain));
+      mbar_wait(BAR(kBarDrain), 0, 100000000ull);
+    }
+    __syncthreads();
+  }
+
+  // ---- merge the splits of this unit inside the cluster --------------------------
+  // Every CTA leaves its row partials (O, m, l) in its own shared memory (the Q and
+  // stage buffers are free now: all copies and MMAs have completed), the cluster
+  // synchronises, and CTA `s` merges rows s, s + n_split, ... by reading all splits'
+  // partials through distributed shared memory.  A second cluster barrier keeps every
+  // CTA's partials alive until all readers are done.  Every CTA reaches both barriers
+  // on every path.
+  float4* po = reinterpret_cast<float4*>(sm);                  // [128 rows][32] float4, swizzled
+  float2* pml = reinterpret_cast<float2*>(sm + kTcRows * kDH * 4);   // [128] (m, l)
+  if (live) {
+    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    if (!failed && n_tiles > 0) {
+      tc_fence_after();
 #pragma unroll
       for (int q4 = 0; q4 < kDH / 32; ++q4) {
         float ov[32];
         tmem_ld32(tmem + lane_base + kTmemO + 32 * q4, ov);
 #pragma unroll
-        for (int i = 0; i < 32; ++i) ov[i] *= alpha;
-        tmem_st32(tmem + lane_base + kTmemO + 32 * q4, ov);
+        for (int i = 0; i < 8; ++i)
+          po[tid * 32 + ((q4 * 8 + i) ^ (tid & 31))] =
+              make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
       }
-      if (need) m_run = mx;
-    }
-    const float mref = (m_run == -INFINITY) ? 0.f : m_run;   // a fully masked row keeps P = 0
-    float ps[4] = {0.f, 0.f, 0.f, 0.f};
-#pragma unroll
-    for (int c = 0; c < kTcKeys; ++c) {
-      const float p = fast_exp2(sv[c] - mref);
-      sv[c] = p;
-      ps[c & 3] += p;
-    }
-    l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
-    // P (fp16) over the consumed K tile: one block of [128 rows x 128 B], swizzled
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      const uint4 v = make_uint4(pack_half2(sv[8 * c], sv[8 * c + 1]), pack_half2(sv[8 * c + 2], sv[8 * c + 3]),
-                                 pack_half2(sv[8 * c + 4], sv[8 * c + 5]), pack_half2(sv[8 * c + 6], sv[8 * c + 7]));
-      *reinterpret_cast<uint4*>(tK + tid * 128 + ((c ^ (tid & 7)) * 16)) = v;
-    }
-    fence_proxy_async();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0) {
-      tc_fence_after();
-      const uint32_t aP = smem_u32(tK), aV = smem_u32(tV);
-#pragma unroll
-      for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-        const uint64_t ad = sw128_desc(aP + kk * 32, 16, 1024);
-        const uint64_t bd = sw128_desc(aV + kk * 2048, 8192, 1024);   // MN-major: dim blocks 8 KiB apart
-        umma_f16(tmem + kTmemO, ad, bd, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
-      }
-      umma_commit(bar_o);
-    }
-    if (__syncthreads_or(!mbar_wait(bar_o, j & 1))) { ok = false; break; }
-    tc_fence_after();
-    tc_fence_before();
-    __syncthreads();
-    if (tid == 0 && j + kStages < n_tiles) issue_tile(j + kStages);
-  }
-  if (!ok) {
-    // Give up: record the error, drain what this CTA may still have in flight (bounded),
-    // then still take part in the cluster barriers below.
-    if (tid == 0) {
-      atomicExch(&a.status[b], kErrTimeout);
-      mbar_wait(bar_s, 0, 100000000ull);
-      mbar_wait(bar_o, 0, 100000000ull);
-      mbar_wait(bar_full0, 0, 100000000ull);
-      mbar_wait(bar_full0 + 8, 0, 100000000ull);
-    }
-    __syncthreads();
-  }
-  // ---- merge the splits of this unit inside the cluster --------------------------
-  // Every CTA leaves its row partials (O, m, l) in its own shared memory (the Q and
-  // stage buffers are free now), the cluster synchronises, and CTA `s` merges rows
-  // s, s + n_split, ... by reading all splits' partials through distributed shared
-  // memory.  A second cluster barrier keeps every CTA's partials alive until all
-  // readers are done.  Every CTA reaches both barriers on every path.
-  float4* po = reinterpret_cast<float4*>(sm);                  // [128 rows][32] float4, swizzled
-  float2* pml = reinterpret_cast<float2*>(sm + kTcRows * kDH * 4);   // [128] (m, l)
-  if (ok && n_tiles > 0) {
-#pragma unroll
-    for (int q4 = 0; q4 < kDH / 32; ++q4) {
-      float ov[32];
-      tmem_ld32(tmem + lane_base + kTmemO + 32 * q4, ov);
-#pragma unroll
-      for (int i = 0; i < 8; ++i)
-        po[tid * 32 + ((q4 * 8 + i) ^ (tid & 31))] = make_float4(ov[4 * i], ov[4 * i + 1], ov[4 * i + 2], ov[4 * i + 3]);
-    }
-  } else {
+      pml[tid] = make_float2(m_run, l_run);
+    } else {
 #pragma unroll 4
-    for (int k = 0; k < 32; ++k) po[tid * 32 + k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int k = 0; k < 32; ++k) po[tid * 32 + k] = make_float4(0.f, 0.f, 0.f, 0.f);
+      pml[tid] = make_float2(-INFINITY, 0.f);
+    }
   }
-  pml[tid] = ok ? make_float2(m_run, l_run) : make_float2(-INFINITY, 0.f);
   tc_fence_before();
   __syncthreads();
-  if (warp == 0) {
+  if (warp == kMmaWarp) {
     tc_fence_after();
     asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
   }
   cluster_sync_all();
 
-  const int lane = tid & 31;
   const int ns = a.n_split;
   const uint32_t po_base = smem_u32(po), pml_base = smem_u32(pml);
-  for (int r = s + warp * ns; r < kTcRows; r += 4 * ns) {
+  constexpr int kWarps = kTcThreads / 32;
+  for (int r = s + warp * ns; r < rows_valid; r += kWarps * ns) {
     const int Rr = mt * kTcRows + r;
-    if (Rr >= M) break;
     // (m, l) of split `lane`
     float2 ml = make_float2(-INFINITY, 0.f);
     if (lane < ns) ml = ld_dsmem_f2(dsmem_addr(pml_base + r * 8, lane));
@@ -607,7 +792,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
     const uint32_t off = po_base + (uint32_t)(r * 32 + (lane ^ (r & 31))) * 16;
 #pragma unroll
-    for (int s2 = 0; s2 < 8; ++s2) {
+    for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
       if (s2 >= ns) break;
       const float w = __shfl_sync(0xffffffffu, w_l, s2);
       const float4 v = ld_dsmem_f4(dsmem_addr(off, s2));
@@ -618,7 +803,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     }
     const float il = 1.f / l;
     const int ur = Rr / g, hr = kvh * g + Rr % g;
-    if (ok) {
+    if (!failed) {
       reinterpret_cast<float4*>(a.out + (((int64_t)b * N + ur) * a.Hq + hr) * kDH)[lane] =
           make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
       if (a.lse && lane == 0) a.lse[((int64_t)b * N + ur) * a.Hq + hr] = (Mx + log2f(l)) * kLn2;
@@ -680,7 +865,7 @@ bool encode_tree_map(CUtensorMap* map, const void* base, int B, int N, int Hkv) 
 }
 
 size_t tc_smem_bytes(int D) {
-  return 1024 + kOffTable + (size_t)2 * (D + 1) * kHalf * sizeof(float) + 64;
+  return 1024 + kOffTable + (size_t)2 * (D + 1) * kHalf * sizeof(float) + 8 + kNumBars * 8;
 }
 
 }  // namespace
@@ -693,8 +878,9 @@ bool attn_tc_supported(const medusa_tree_t& t, int Hq, const medusa_kv_t& c) {
 }
 
 // Split choice: enough CTAs to fill the SMs two per SM, in whole waves where possible,
-// while every CTA streams at least rows/16 tiles so that its fp32 partial stays below
-// a quarter of the K/V bytes it reads.
+// with at most kMaxClusterSplits splits (one cluster) per unit and at least rows/16
+// tiles per split.  The tree tiles count as work of split 0, which takes that many
+// fewer prefix tiles, so that the splits end together.
 void attn_tc_plan(AttnPlan& p) {
   p.mt_rows = kTcRows;
   p.key_tile = kTcKeys;
@@ -705,6 +891,7 @@ void attn_tc_plan(AttnPlan& p) {
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const double slots = 2.0 * sms;
   const int tiles_unit = (p.max_prefix + kTcKeys - 1) / kTcKeys;
+  const int n_tree = (p.N + kTcKeys - 1) / kTcKeys;
   const int rows = M < kTcRows ? M : kTcRows;
   int min_tiles = (rows + 15) / 16;
   if (min_tiles < 2) min_tiles = 2;
@@ -719,14 +906,16 @@ void attn_tc_plan(AttnPlan& p) {
     const double score = eff - 0.004 * n;
     if (score > best_score + 1e-9) { best_score = score; best = n; }
   }
-  int tiles_per = (tiles_unit + best - 1) / best;
-  if (tiles_per < 1) tiles_per = 1;
-  p.chunk = tiles_per * kTcKeys;
-  p.n_split = p.max_prefix > 0 ? (p.max_prefix + p.chunk - 1) / p.chunk : 1;
-  if (p.n_split > kMaxClusterSplits) {            // keep the unit in one cluster
-    p.chunk = ((p.max_prefix + kMaxClusterSplits - 1) / kMaxClusterSplits + kTcKeys - 1) / kTcKeys * kTcKeys;
-    p.n_split = (p.max_prefix + p.chunk - 1) / p.chunk;
-  }
+  const int per = (tiles_unit + n_tree + best - 1) / best;
+  int first_tiles = per - n_tree;
+  if (first_tiles < 0) first_tiles = 0;
+  if (first_tiles > tiles_unit || best == 1) first_tiles = tiles_unit;
+  const int rest = tiles_unit - first_tiles;
+  int chunk_tiles = best > 1 ? (rest + best - 2) / (best - 1) : 1;
+  if (chunk_tiles < 1) chunk_tiles = 1;
+  p.first = first_tiles * kTcKeys;
+  p.chunk = chunk_tiles * kTcKeys;
+  p.n_split = 1 + (rest + chunk_tiles - 1) / chunk_tiles;
 }
 
 cudaError_t launch_attn_tc(const AttnPlan& p, const medusa_tree_t& t, const void* q,
@@ -755,6 +944,7 @@ cudaError_t launch_attn_tc(const AttnPlan& p, const medusa_tree_t& t, const void
   a.n_mt = p.n_mt;
   a.n_split = p.n_split;
   a.chunk = p.chunk;
+  a.first = p.first;
   a.scale_log2 = scale_log2;
   for (int i = 0; i < 64; ++i) {
     a.th_hi[i] = th_hi[i];
