@@ -62,7 +62,7 @@ constexpr int kStages = 2;
 constexpr int kOffQ = 0;
 constexpr int kOffStage = kQBytes;
 constexpr int kOffTable = kOffStage + kStages * kStageBytes;   // rope cos/sin, then barriers
-constexpr int kNumBars = 16;
+constexpr int kNumBars = 17;
 
 // barrier slots
 constexpr int kBarFull = 0;      // [2] stage landed (TMA transaction bytes)
@@ -71,9 +71,10 @@ constexpr int kBarConvV = 4;     // [2] V tile converted
 constexpr int kBarEmpty = 6;     // [2] stage consumed by the P V MMA (tcgen05.commit)
 constexpr int kBarSFull = 8;     // [2] S buffer written (tcgen05.commit)
 constexpr int kBarPFull = 10;    // [2] P written over S (one arrival per softmax warp)
-constexpr int kBarODone = 12;    // P V MMA of a tile complete (tcgen05.commit)
-constexpr int kBarQReady = 13;   // queries staged (one arrival per softmax warp)
-constexpr int kBarDrain = 14;    // final commit on the error path
+constexpr int kBarODone = 12;    // [2] P V MMA of tile j complete, slot j & 1 (tcgen05.commit)
+constexpr int kBarQReady = 14;   // queries staged (one arrival per softmax warp)
+constexpr int kBarDrain = 15;    // final commit on the error path
+constexpr int kBarQFull = 16;    // query tile landed (TMA transaction bytes)
 
 constexpr int kErrTimeout = MEDUSA_ETIMEOUT;
 constexpr int kMaxClusterSplits = 8;   // splits of a unit form one portable cluster
@@ -285,33 +286,33 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
 }
 
 // Re-encode one K or V tile (2 blocks of [64 rows x 128 B], bf16) to fp16 in place;
-// rows of keys >= k_valid become zero.  Thread ct of the 64 converter threads.
+// rows of keys >= k_valid become zero.  Thread ct of the 64 converter threads; all its
+// loads are issued before the first store, so their latencies overlap.
 __device__ __forceinline__ void convert_tile(uint8_t* tile, int k_valid, int ct) {
   uint4* p = reinterpret_cast<uint4*>(tile);
   constexpr int kIter = (kKBytes / 16) / kConvThreads;
-  if (k_valid >= kTcKeys) {
-#pragma unroll 8
-    for (int i = 0; i < kIter; ++i) {
-      const int idx = i * kConvThreads + ct;
-      p[idx] = bf16x8_to_f16x8(p[idx]);
-    }
-  } else {
-#pragma unroll 8
-    for (int i = 0; i < kIter; ++i) {
-      const int idx = i * kConvThreads + ct;
-      const int row = (idx % (kKBytes / 32)) / 8;      // 16-byte chunks: 8 per row, 512 per block
-      p[idx] = row < k_valid ? bf16x8_to_f16x8(p[idx]) : make_uint4(0, 0, 0, 0);
-    }
+  uint4 v[kIter];
+#pragma unroll
+  for (int i = 0; i < kIter; ++i) v[i] = p[i * kConvThreads + ct];
+#pragma unroll
+  for (int i = 0; i < kIter; ++i) {
+    const int idx = i * kConvThreads + ct;
+    const int row = (idx % (kKBytes / 32)) / 8;      // 16-byte chunks: 8 per row, 512 per block
+    p[idx] = row < k_valid ? bf16x8_to_f16x8(v[i]) : make_uint4(0, 0, 0, 0);
   }
 }
 
 // Tree-row key tile: bf16 -> RoPE at L + depth[v] (fp32) -> fp16, in place.  Row r of
 // the tile is tree row v0 + r; dims i and i + 64 sit in the two blocks at the same
-// swizzled position.  Rows >= n_valid become zero.
-__device__ __forceinline__ void convert_rotate_tile(uint8_t* tile, int n_valid, int v0, const int32_t* depth,
+// swizzled position.  Rows >= n_valid become zero.  `dep[i]` is the depth of the row
+// that iteration i of thread ct touches (loaded before the tile landed).
+constexpr int kRotIter = (kTcKeys * 8) / kConvThreads;
+__device__ __forceinline__ int rotate_row(int i, int ct) { return (i * kConvThreads + ct) >> 3; }
+
+__device__ __forceinline__ void convert_rotate_tile(uint8_t* tile, int n_valid, const int* dep,
                                                     const float* tab_c, const float* tab_s, int ct) {
-#pragma unroll 2
-  for (int i = 0; i < (kTcKeys * 8) / kConvThreads; ++i) {
+#pragma unroll
+  for (int i = 0; i < kRotIter; ++i) {
     const int idx = i * kConvThreads + ct;
     const int row = idx >> 3, c = idx & 7;
     const int off = row * 128 + ((c ^ (row & 7)) * 16);
@@ -321,7 +322,7 @@ __device__ __forceinline__ void convert_rotate_tile(uint8_t* tile, int n_valid, 
       float x1[8], x2[8];
       Elem<uint16_t>::unpack(*p0, x1);
       Elem<uint16_t>::unpack(*p1, x2);
-      const int ti = __ldg(depth + v0 + row) * kHalf + 8 * c;
+      const int ti = dep[i] * kHalf + 8 * c;
       float y1[8], y2[8];
 #pragma unroll
       for (int e = 0; e < 8; ++e) {
@@ -340,12 +341,11 @@ __device__ __forceinline__ void convert_rotate_tile(uint8_t* tile, int n_valid, 
   }
 }
 
-
 template <bool PAGED>
 __global__ void __launch_bounds__(kTcThreads, 2)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmKn, const __grid_constant__ CUtensorMap tmVn,
-                   const TcArgs a) {
+                   const __grid_constant__ CUtensorMap tmQ, const TcArgs a) {
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const medusa_tree_t& t = a.t;
@@ -380,22 +380,72 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const int R = mt * kTcRows + tid;
   const bool row_ok = soft && R < M;
   const int u = row_ok ? R / g : 0;
-  const int h = kvh * g + (row_ok ? R % g : 0);
-
-  // Query loads first, so they are not queued behind the K/V stream.
-  uint4 qa[8], qb[8];
-  if (live) {
-    const uint16_t* qrow = a.q + (((int64_t)b * N + u) * a.Hq + h) * kDH;
-#pragma unroll
-    for (int c = 0; c < 8; ++c) {
-      qa[c] = row_ok ? __ldg(reinterpret_cast<const uint4*>(qrow + 8 * c)) : make_uint4(0, 0, 0, 0);
-      qb[c] = row_ok ? __ldg(reinterpret_cast<const uint4*>(qrow + kHalf + 8 * c)) : make_uint4(0, 0, 0, 0);
-    }
-  }
 
   const uint32_t bar0 = smem_u32(bars);
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
-  if (tid == 0) {
+
+  // Keys of this split.  Each sequence spreads its own ceil(L / 64) prefix tiles over
+  // the n_split splits, so a short sequence does not leave splits idle while one of
+  // them streams everything.  The tree tiles count as work of split 0, which takes
+  // that many fewer prefix tiles.
+  const int ns = a.n_split;
+  const int tiles_b = (Lb + kTcKeys - 1) / kTcKeys;
+  const int n_tree_all = (N + kTcKeys - 1) / kTcKeys;
+  const int first_t = ns > 1 ? min(max((tiles_b + n_tree_all + ns - 1) / ns - n_tree_all, 0), tiles_b) : tiles_b;
+  const int chunk_t = ns > 1 ? (tiles_b - first_t + ns - 2) / (ns - 1) : 0;
+  const int t_begin = s == 0 ? 0 : min(tiles_b, first_t + (s - 1) * chunk_t);
+  const int t_end = s == 0 ? first_t : min(tiles_b, first_t + s * chunk_t);
+  const int k_begin = t_begin * kTcKeys;
+  const int k_end = min(Lb, t_end * kTcKeys);
+  // Tiles: the split's prefix keys, then (split 0 only) the N tree rows, 64 per tile.
+  // A tree tile t covers rows [64t, 64t + 64), exactly ancestor-mask word t.
+  const int n_pre = k_end > k_begin ? (k_end - k_begin + kTcKeys - 1) / kTcKeys : 0;
+  const int n_tree = (s == 0) ? (N + kTcKeys - 1) / kTcKeys : 0;
+  const int n_tiles = n_pre + n_tree;
+  auto tile_valid = [&](int j) -> int {        // rows of tile j before the end of its range
+    return j >= n_pre ? N - (j - n_pre) * kTcKeys : k_end - (k_begin + j * kTcKeys);
+  };
+  // TMA of tile j into stage j & 1 (its full barrier counts the bytes).
+  auto issue_tile = [&](int j) {
+    const int st = j & 1;
+    const uint32_t bar = BAR(kBarFull + st);
+    const uint32_t dK = smem_u32(sm + kOffStage + st * kStageBytes);
+    const uint32_t dV = dK + kKBytes;
+    const int k0 = k_begin + j * kTcKeys;
+    if (j >= n_pre) {
+      const int v0 = (j - n_pre) * kTcKeys;
+      mbar_expect_tx(bar, 4 * 8192);
+      tma_load_4d(dK, &tmKn, 0, kvh, v0, b, bar);
+      tma_load_4d(dK + 8192, &tmKn, 64, kvh, v0, b, bar);
+      tma_load_4d(dV, &tmVn, 0, kvh, v0, b, bar);
+      tma_load_4d(dV + 8192, &tmVn, 64, kvh, v0, b, bar);
+    } else if (!PAGED) {
+      mbar_expect_tx(bar, 4 * 8192);
+      tma_load_4d(dK, &tmK, 0, k0, kvh, b, bar);
+      tma_load_4d(dK + 8192, &tmK, 64, k0, kvh, b, bar);
+      tma_load_4d(dV, &tmV, 0, k0, kvh, b, bar);
+      tma_load_4d(dV + 8192, &tmV, 64, k0, kvh, b, bar);
+    } else {
+      const int nk = min(kTcKeys, k_end - k0);
+      const int np = (nk + 15) / 16;
+      const int32_t* bt = a.c.block_table + (int64_t)b * a.c.max_blocks + k0 / 16;
+      int page[4];
+#pragma unroll
+      for (int p = 0; p < 4; ++p) page[p] = p < np ? __ldg(bt + p) : 0;
+      mbar_expect_tx(bar, (uint32_t)np * 4 * 2048);
+      for (int p = 0; p < np; ++p) {
+        tma_load_4d(dK + p * 2048, &tmK, 0, 0, kvh, page[p], bar);
+        tma_load_4d(dK + 8192 + p * 2048, &tmK, 64, 0, kvh, page[p], bar);
+        tma_load_4d(dV + p * 2048, &tmV, 0, 0, kvh, page[p], bar);
+        tma_load_4d(dV + 8192 + p * 2048, &tmV, 64, 0, kvh, page[p], bar);
+      }
+    }
+  };
+
+  // The producer lane initialises the barriers and starts the first copies at once;
+  // the other threads touch the barriers only after the __syncthreads below.
+  int n_issued = 0;
+  if (tid == kProdWarp * 32) {
     abort_flag = 0;
     for (int st = 0; st < kStages; ++st) {
       mbar_init(BAR(kBarFull + st), 1);
@@ -404,11 +454,18 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       mbar_init(BAR(kBarEmpty + st), 1);
       mbar_init(BAR(kBarSFull + st), 1);
       mbar_init(BAR(kBarPFull + st), kSoftWarps);
+      mbar_init(BAR(kBarODone + st), 1);
     }
-    mbar_init(BAR(kBarODone), 1);
     mbar_init(BAR(kBarQReady), kSoftWarps);
     mbar_init(BAR(kBarDrain), 1);
+    mbar_init(BAR(kBarQFull), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+    // the query tile first: rows (u, group member) of this tile, 64 dims per copy
+    const uint32_t sQ = smem_u32(sm + kOffQ);
+    mbar_expect_tx(BAR(kBarQFull), kQBytes);
+    tma_load_4d(sQ, &tmQ, 0, kvh * g, mt * (kTcRows / g), b, BAR(kBarQFull));
+    tma_load_4d(sQ + 16384, &tmQ, 64, kvh * g, mt * (kTcRows / g), b, BAR(kBarQFull));
+    for (; n_issued < n_tiles && n_issued < kStages; ++n_issued) issue_tile(n_issued);
   }
   if (warp == kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
@@ -429,115 +486,83 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const uint32_t tmem = tmem_slot;
   const volatile int* abortp = &abort_flag;
 
-  // Keys of this split: split 0 takes the first a.first prefix keys (fewer than the
-  // others, because it also runs the tree tiles), split s > 0 the a.chunk keys after.
-  const int k_begin = s == 0 ? 0 : a.first + (s - 1) * a.chunk;
-  const int k_end = min(Lb, k_begin + (s == 0 ? a.first : a.chunk));
-  // Tiles: the split's prefix keys, then (split 0 only) the N tree rows, 64 per tile.
-  // A tree tile t covers rows [64t, 64t + 64), exactly ancestor-mask word t.
-  const int n_pre = k_end > k_begin ? (k_end - k_begin + kTcKeys - 1) / kTcKeys : 0;
-  const int n_tree = (s == 0) ? (N + kTcKeys - 1) / kTcKeys : 0;
-  const int n_tiles = n_pre + n_tree;
-  auto tile_valid = [&](int j) -> int {        // rows of tile j before the end of its range
-    return j >= n_pre ? N - (j - n_pre) * kTcKeys : k_end - (k_begin + j * kTcKeys);
-  };
-
   constexpr uint32_t kIdS = idesc_f16(kTcRows, kTcKeys, false);
   constexpr uint32_t kIdO = idesc_f16(kTcRows, kDH, true);
   bool ok = true;
-  int n_issued = 0;
   float m_run = -INFINITY, l_run = 0.f;
 
 
   if (warp == kProdWarp) {
-    // ---- TMA producer -------------------------------------------------------------
+    // ---- TMA producer: tile j >= 2 once the P V MMA of tile j - 2 freed its stage ----
     if (lane == 0) {
-      for (int j = 0; j < n_tiles; ++j) {
-        const int st = j & 1;
-        if (j >= kStages && !wait_or_abort(BAR(kBarEmpty + st), ((j >> 1) - 1) & 1, abortp)) {
+      for (int j = n_issued; j < n_tiles; ++j) {
+        if (!wait_or_abort(BAR(kBarEmpty + (j & 1)), ((j >> 1) - 1) & 1, abortp)) {
           ok = false;
           break;
         }
-        const uint32_t bar = BAR(kBarFull + st);
-        const uint32_t dK = smem_u32(sm + kOffStage + st * kStageBytes);
-        const uint32_t dV = dK + kKBytes;
-        const int k0 = k_begin + j * kTcKeys;
-        if (j >= n_pre) {
-          const int v0 = (j - n_pre) * kTcKeys;
-          mbar_expect_tx(bar, 4 * 8192);
-          tma_load_4d(dK, &tmKn, 0, kvh, v0, b, bar);
-          tma_load_4d(dK + 8192, &tmKn, 64, kvh, v0, b, bar);
-          tma_load_4d(dV, &tmVn, 0, kvh, v0, b, bar);
-          tma_load_4d(dV + 8192, &tmVn, 64, kvh, v0, b, bar);
-        } else if (!PAGED) {
-          mbar_expect_tx(bar, 4 * 8192);
-          tma_load_4d(dK, &tmK, 0, k0, kvh, b, bar);
-          tma_load_4d(dK + 8192, &tmK, 64, k0, kvh, b, bar);
-          tma_load_4d(dV, &tmV, 0, k0, kvh, b, bar);
-          tma_load_4d(dV + 8192, &tmV, 64, k0, kvh, b, bar);
-        } else {
-          const int nk = min(kTcKeys, k_end - k0);
-          const int np = (nk + 15) / 16;
-          const int32_t* bt = a.c.block_table + (int64_t)b * a.c.max_blocks + k0 / 16;
-          int page[4];
-#pragma unroll
-          for (int p = 0; p < 4; ++p) page[p] = p < np ? __ldg(bt + p) : 0;
-          mbar_expect_tx(bar, (uint32_t)np * 4 * 2048);
-          for (int p = 0; p < np; ++p) {
-            tma_load_4d(dK + p * 2048, &tmK, 0, 0, kvh, page[p], bar);
-            tma_load_4d(dK + 8192 + p * 2048, &tmK, 64, 0, kvh, page[p], bar);
-            tma_load_4d(dV + p * 2048, &tmV, 0, 0, kvh, page[p], bar);
-            tma_load_4d(dV + 8192 + p * 2048, &tmV, 64, 0, kvh, page[p], bar);
-          }
-        }
+        issue_tile(j);
         n_issued = j + 1;
       }
     }
   } else if (warp == kMmaWarp) {
-    // ---- MMA issue: S(j) = Q K_j^T, then O += P(j-1) V(j-1) -----------------------------
-    // S(j) goes to TMEM buffer j & 1, which P(j-2) occupied: it waits for the P V MMA
-    // of tile j - 2.  Every commit covers all MMAs issued before it.
+    // ---- MMA issue ------------------------------------------------------------------
+    // S(j) = Q K_j^T into TMEM buffer j & 1 once K_j is converted and the P V MMA of
+    // tile j - 2 (whose P occupied that buffer) has completed; O += P(j) V(j) once the
+    // softmax has written P(j) and V_j is converted.  Whichever is ready goes first,
+    // S before P V when both are.  Completion of P V(j) is signalled on slot j & 1, so
+    // that a slot's phase never runs more than one ahead of its waiters.  Every commit
+    // covers all MMAs issued before it.
     if (lane == 0) {
       const uint32_t sQ = smem_u32(sm + kOffQ);
       if (!wait_or_abort(BAR(kBarQReady), 0, abortp)) ok = false;
-      for (int j = 0; ok && j <= n_tiles; ++j) {
-        if (j < n_tiles) {
-          const int st = j & 1;
-          if (!wait_or_abort(BAR(kBarConvK + st), (j >> 1) & 1, abortp) ||
-              (j >= 2 && !wait_or_abort(BAR(kBarODone), (j - 2) & 1, abortp))) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t aK = smem_u32(sm + kOffStage + st * kStageBytes);
+      int js = 0, jp = 0;
+      uint64_t t_idle = global_ns();
+      for (uint32_t spin = 0; ok && jp < n_tiles;) {
+        bool did = false;
+        if (js < n_tiles && js <= jp + 1) {
+          const int st = js & 1;
+          if (mbar_test(BAR(kBarConvK + st), (js >> 1) & 1) &&
+              (js < 2 || mbar_test(BAR(kBarODone + st), ((js - 2) >> 1) & 1))) {
+            tc_fence_after();
+            const uint32_t aK = smem_u32(sm + kOffStage + st * kStageBytes);
 #pragma unroll
-          for (int kk = 0; kk < kDH / 16; ++kk) {
-            const uint64_t ad = sw128_desc(sQ + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024);
-            const uint64_t bd = sw128_desc(aK + (kk / 4) * 8192 + (kk % 4) * 32, 16, 1024);
-            umma_f16(tmem + 64u * st, ad, bd, kIdS, kk > 0 ? 1u : 0u);
+            for (int kk = 0; kk < kDH / 16; ++kk) {
+              const uint64_t ad = sw128_desc(sQ + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024);
+              const uint64_t bd = sw128_desc(aK + (kk / 4) * 8192 + (kk % 4) * 32, 16, 1024);
+              umma_f16(tmem + 64u * st, ad, bd, kIdS, kk > 0 ? 1u : 0u);
+            }
+            umma_commit(BAR(kBarSFull + st));
+            ++js;
+            did = true;
           }
-          umma_commit(BAR(kBarSFull + st));
         }
-        if (j >= 1) {
-          const int jj = j - 1, st = jj & 1;
-          if (!wait_or_abort(BAR(kBarPFull + st), (jj >> 1) & 1, abortp) ||
-              !wait_or_abort(BAR(kBarConvV + st), (jj >> 1) & 1, abortp)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          const uint32_t aV = smem_u32(sm + kOffStage + st * kStageBytes + kKBytes);
+        if (jp < js) {
+          const int st = jp & 1;
+          if (mbar_test(BAR(kBarPFull + st), (jp >> 1) & 1) && mbar_test(BAR(kBarConvV + st), (jp >> 1) & 1)) {
+            tc_fence_after();
+            const uint32_t aV = smem_u32(sm + kOffStage + st * kStageBytes + kKBytes);
 #pragma unroll
-          for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-            const uint64_t bd = sw128_desc(aV + kk * 2048, 8192, 1024);   // MN-major: dim blocks 8 KiB apart
-            umma_f16_ts(tmem + kTmemO, tmem + 64u * st + 8u * kk, bd, kIdO, (jj > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kTcKeys / 16; ++kk) {
+              const uint64_t bd = sw128_desc(aV + kk * 2048, 8192, 1024);   // MN-major: dim blocks 8 KiB apart
+              umma_f16_ts(tmem + kTmemO, tmem + 64u * st + 8u * kk, bd, kIdO, (jp > 0 || kk > 0) ? 1u : 0u);
+            }
+            umma_commit(BAR(kBarEmpty + st));
+            umma_commit(BAR(kBarODone + st));
+            ++jp;
+            did = true;
           }
-          umma_commit(BAR(kBarEmpty + st));
-          umma_commit(BAR(kBarODone));
+        }
+        if (did) {
+          spin = 0;
+          t_idle = global_ns();
+        } else if (*abortp || ((++spin & 255u) == 0 && global_ns() - t_idle > 2000000000ull)) {
+          ok = false;
         }
       }
       // O is final once the last P V MMA has completed.
-      if (ok && n_tiles > 0 && !wait_or_abort(BAR(kBarODone), (n_tiles - 1) & 1, abortp)) ok = false;
+      if (ok && n_tiles > 0 &&
+          !wait_or_abort(BAR(kBarODone + ((n_tiles - 1) & 1)), ((n_tiles - 1) >> 1) & 1, abortp))
+        ok = false;
     }
   } else if (warp >= kConvWarp0) {
     // ---- bf16 -> fp16 conversion (tree keys also rotated) ------------------------------
@@ -547,11 +572,19 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       uint8_t* tK = sm + kOffStage + st * kStageBytes;
       uint8_t* tV = tK + kKBytes;
       const int k_valid = tile_valid(j);
+      int dep[kRotIter];
+      if (j >= n_pre) {
+#pragma unroll
+        for (int i = 0; i < kRotIter; ++i) {
+          const int r = rotate_row(i, ct);
+          dep[i] = r < k_valid ? __ldg(t.depth + (j - n_pre) * kTcKeys + r) : 0;
+        }
+      }
       if (!wait_or_abort(BAR(kBarFull + st), (j >> 1) & 1, abortp)) {
         ok = false;
         break;
       }
-      if (j >= n_pre) convert_rotate_tile(tK, k_valid, (j - n_pre) * kTcKeys, t.depth, tab_c, tab_s, ct);
+      if (j >= n_pre) convert_rotate_tile(tK, k_valid, dep, tab_c, tab_s, ct);
       else convert_tile(tK, k_valid, ct);
       fence_proxy_async();
       mbar_arrive(BAR(kBarConvK + st));
@@ -562,10 +595,20 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   } else {
 
     // ---- softmax warps: thread tid owns query row tid (TMEM lane tid) ----------------
-    // Rotated queries, pre-multiplied by scale * log2 e, fp16, K-major 128-byte swizzle
-    // (2 blocks of 64 dims).
-    if (live) {
+    // The query tile landed by TMA as bf16, K-major with the 128-byte swizzle (dims
+    // i and i + 64 of a row at the same position of the two 64-dim blocks).  Rotate
+    // each row in place at L + depth, pre-multiply by scale * log2 e, store fp16.
+    if (!__all_sync(0xffffffffu, wait_or_abort(BAR(kBarQFull), 0, abortp))) ok = false;
+    if (ok && live) {
       const int ti0 = __ldg(t.depth + u) * kHalf;
+      uint4* q0 = reinterpret_cast<uint4*>(sm + kOffQ + tid * 128);
+      uint4* q1 = reinterpret_cast<uint4*>(sm + kOffQ + 16384 + tid * 128);
+      uint4 qa[8], qb[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        qa[c] = q0[c ^ (tid & 7)];
+        qb[c] = q1[c ^ (tid & 7)];
+      }
 #pragma unroll
       for (int c = 0; c < 8; ++c) {            // dims [8c, 8c+8) and [64+8c, 64+8c+8)
         float x1[8], x2[8], y1[8], y2[8];
@@ -577,58 +620,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           y1[e] = (x1[e] * cs - x2[e] * sn) * a.scale_log2;
           y2[e] = (x2[e] * cs + x1[e] * sn) * a.scale_log2;
         }
-        const uint4 o1 = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]), pack_half2(y1[4], y1[5]),
-                                    pack_half2(y1[6], y1[7]));
-        const uint4 o2 = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]), pack_half2(y2[4], y2[5]),
-                                    pack_half2(y2[6], y2[7]));
-        const int phys = c ^ (tid & 7);
-        *reinterpret_cast<uint4*>(sm + kOffQ + tid * 128 + phys * 16) = o1;            // dims 0..63
-        *reinterpret_cast<uint4*>(sm + kOffQ + 16384 + tid * 128 + phys * 16) = o2;    // dims 64..127
+        q0[c ^ (tid & 7)] = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]),
+                                       pack_half2(y1[4], y1[5]), pack_half2(y1[6], y1[7]));
+        q1[c ^ (tid & 7)] = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]),
+                                       pack_half2(y2[4], y2[5]), pack_half2(y2[6], y2[7]));
       }
     }
     fence_proxy_async();
     __syncwarp();
     if (lane == 0) mbar_arrive(BAR(kBarQReady));
-
-    // Stage rotated tree keys and tree values at cache rows L + u (split 0 only).
-    if (s == 0 && row_ok && (R % g) == 0) {
-      const int64_t src = (((int64_t)b * N + u) * a.Hkv + kvh) * kDH;
-      const int64_t dst = row_off_tc(a.c, b, kvh, Lb + u);
-      uint16_t* ck = (uint16_t*)a.c.k;
-      uint16_t* cv = (uint16_t*)a.c.v;
-      const int ti0 = __ldg(t.depth + u) * kHalf;
-      uint4 ka[8], kb[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        ka[c] = __ldg(reinterpret_cast<const uint4*>(a.k_new + src + 8 * c));
-        kb[c] = __ldg(reinterpret_cast<const uint4*>(a.k_new + src + kHalf + 8 * c));
-      }
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        float x1[8], x2[8];
-        Elem<uint16_t>::unpack(ka[c], x1);
-        Elem<uint16_t>::unpack(kb[c], x2);
-        uint32_t y1[4], y2[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float c0 = tab_c[ti0 + 8 * c + 2 * e], s0 = tab_s[ti0 + 8 * c + 2 * e];
-          const float c1 = tab_c[ti0 + 8 * c + 2 * e + 1], s1 = tab_s[ti0 + 8 * c + 2 * e + 1];
-          const uint32_t a0 = f32_to_bf16_bits(x1[2 * e] * c0 - x2[2 * e] * s0);
-          const uint32_t a1 = f32_to_bf16_bits(x1[2 * e + 1] * c1 - x2[2 * e + 1] * s1);
-          const uint32_t b0 = f32_to_bf16_bits(x2[2 * e] * c0 + x1[2 * e] * s0);
-          const uint32_t b1 = f32_to_bf16_bits(x2[2 * e + 1] * c1 + x1[2 * e + 1] * s1);
-          y1[e] = a0 | (a1 << 16);
-          y2[e] = b0 | (b1 << 16);
-        }
-        *reinterpret_cast<uint4*>(ck + dst + 8 * c) = make_uint4(y1[0], y1[1], y1[2], y1[3]);
-        *reinterpret_cast<uint4*>(ck + dst + kHalf + 8 * c) = make_uint4(y2[0], y2[1], y2[2], y2[3]);
-      }
-      uint4 vv[16];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) vv[c] = __ldg(reinterpret_cast<const uint4*>(a.v_new + src + 8 * c));
-#pragma unroll
-      for (int c = 0; c < 16; ++c) *reinterpret_cast<uint4*>(cv + dst + 8 * c) = vv[c];
-    }
 
     // Online softmax.  O accumulates in TMEM across tiles.  The running max m_run is
     // raised only when a tile's max exceeds it by more than 2^8 (log2 units); then O
@@ -637,7 +637,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     // so the result is the same softmax.
     constexpr float kRescale = 8.f;
     const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    for (int j = 0; j < n_tiles; ++j) {
+    for (int j = 0; ok && j < n_tiles; ++j) {
       const int sb = j & 1;
       const bool tree_tile = j >= n_pre;
       const int k_valid = tile_valid(j);
@@ -677,7 +677,8 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         const bool need = !first && (mx > m_run + kRescale);
         if (first) m_run = mx;                           // O holds nothing yet for this row
         if (__any_sync(0xffffffffu, need)) {
-          if (!__all_sync(0xffffffffu, wait_or_abort(BAR(kBarODone), (j - 1) & 1, abortp))) {
+          if (!__all_sync(0xffffffffu,
+                          wait_or_abort(BAR(kBarODone + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abortp))) {
             ok = false;
             break;
           }
@@ -711,6 +712,50 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       __syncwarp();
       if (lane == 0) mbar_arrive(BAR(kBarPFull + sb));
     }
+
+    // Stage rotated tree keys and tree values at cache rows L + u.  Split 0 runs the
+    // tree tiles and is the last to finish, so the other splits share this work
+    // (row u goes to split 1 + u mod (n_split - 1)) once their own tiles are done.
+    const int stagers = a.n_split > 1 ? a.n_split - 1 : 1;
+    const int my_stage = a.n_split > 1 ? s - 1 : 0;
+    if (ok && row_ok && (R % g) == 0 && my_stage >= 0 && u % stagers == my_stage) {
+      const int64_t src = (((int64_t)b * N + u) * a.Hkv + kvh) * kDH;
+      const int64_t dst = row_off_tc(a.c, b, kvh, Lb + u);
+      uint16_t* ck = (uint16_t*)a.c.k;
+      uint16_t* cv = (uint16_t*)a.c.v;
+      const int ti0 = __ldg(t.depth + u) * kHalf;
+      uint4 ka[8], kb[8];
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        ka[c] = __ldg(reinterpret_cast<const uint4*>(a.k_new + src + 8 * c));
+        kb[c] = __ldg(reinterpret_cast<const uint4*>(a.k_new + src + kHalf + 8 * c));
+      }
+#pragma unroll
+      for (int c = 0; c < 8; ++c) {
+        float x1[8], x2[8];
+        Elem<uint16_t>::unpack(ka[c], x1);
+        Elem<uint16_t>::unpack(kb[c], x2);
+        uint32_t y1[4], y2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float c0 = tab_c[ti0 + 8 * c + 2 * e], s0 = tab_s[ti0 + 8 * c + 2 * e];
+          const float c1 = tab_c[ti0 + 8 * c + 2 * e + 1], s1 = tab_s[ti0 + 8 * c + 2 * e + 1];
+          const uint32_t a0 = f32_to_bf16_bits(x1[2 * e] * c0 - x2[2 * e] * s0);
+          const uint32_t a1 = f32_to_bf16_bits(x1[2 * e + 1] * c1 - x2[2 * e + 1] * s1);
+          const uint32_t b0 = f32_to_bf16_bits(x2[2 * e] * c0 + x1[2 * e] * s0);
+          const uint32_t b1 = f32_to_bf16_bits(x2[2 * e + 1] * c1 + x1[2 * e + 1] * s1);
+          y1[e] = a0 | (a1 << 16);
+          y2[e] = b0 | (b1 << 16);
+        }
+        *reinterpret_cast<uint4*>(ck + dst + 8 * c) = make_uint4(y1[0], y1[1], y1[2], y1[3]);
+        *reinterpret_cast<uint4*>(ck + dst + kHalf + 8 * c) = make_uint4(y2[0], y2[1], y2[2], y2[3]);
+      }
+      uint4 vv[16];
+#pragma unroll
+      for (int c = 0; c < 16; ++c) vv[c] = __ldg(reinterpret_cast<const uint4*>(a.v_new + src + 8 * c));
+#pragma unroll
+      for (int c = 0; c < 16; ++c) *reinterpret_cast<uint4*>(cv + dst + 8 * c) = vv[c];
+    }
   }
 
 
@@ -725,6 +770,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     // Drain (bounded) what this CTA may still have in flight before its shared memory
     // and TMEM are reused or released: the last copy into each stage, and all MMAs.
     if (warp == kProdWarp && lane == 0) {
+      mbar_wait(BAR(kBarQFull), 0, 100000000ull);
       for (int st = 0; st < kStages; ++st) {
         const int jl = (n_issued - 1 - st) >= 0 ? ((n_issued - 1 - st) & ~1) + st : -1;
         if (jl >= 0) mbar_wait(BAR(kBarFull + st), (jl >> 1) & 1, 100000000ull);
@@ -774,14 +820,19 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   }
   cluster_sync_all();
 
-  const int ns = a.n_split;
   const uint32_t po_base = smem_u32(po), pml_base = smem_u32(pml);
   constexpr int kWarps = kTcThreads / 32;
   for (int r = s + warp * ns; r < rows_valid; r += kWarps * ns) {
     const int Rr = mt * kTcRows + r;
-    // (m, l) of split `lane`
+    // (m, l) of split `lane` and this lane's float4 of every split's O, all requested
+    // before any is used: one round trip through distributed shared memory.
+    const uint32_t off = po_base + (uint32_t)(r * 32 + (lane ^ (r & 31))) * 16;
     float2 ml = make_float2(-INFINITY, 0.f);
     if (lane < ns) ml = ld_dsmem_f2(dsmem_addr(pml_base + r * 8, lane));
+    float4 v[kMaxClusterSplits];
+#pragma unroll
+    for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
+      v[s2] = s2 < ns ? ld_dsmem_f4(dsmem_addr(off, s2)) : make_float4(0.f, 0.f, 0.f, 0.f);
     float Mx = ml.x;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
@@ -790,16 +841,13 @@ __global__ void __launch_bounds__(kTcThreads, 2)
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
     float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-    const uint32_t off = po_base + (uint32_t)(r * 32 + (lane ^ (r & 31))) * 16;
 #pragma unroll
     for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
-      if (s2 >= ns) break;
       const float w = __shfl_sync(0xffffffffu, w_l, s2);
-      const float4 v = ld_dsmem_f4(dsmem_addr(off, s2));
-      acc.x = fmaf(v.x, w, acc.x);
-      acc.y = fmaf(v.y, w, acc.y);
-      acc.z = fmaf(v.z, w, acc.z);
-      acc.w = fmaf(v.w, w, acc.w);
+      acc.x = fmaf(v[s2].x, w, acc.x);
+      acc.y = fmaf(v[s2].y, w, acc.y);
+      acc.z = fmaf(v[s2].z, w, acc.z);
+      acc.w = fmaf(v[s2].w, w, acc.w);
     }
     const float il = 1.f / l;
     const int ur = Rr / g, hr = kvh * g + Rr % g;
@@ -849,15 +897,16 @@ bool encode_kv_map(CUtensorMap* map, void* base, const medusa_kv_t& c, int B) {
   return r == CUDA_SUCCESS;
 }
 
-// Tree rows k_new / v_new [B][N][Hkv][dh] as a 4-D tensor (dh, Hkv, N, B); a box is
-// 64 dims of 64 consecutive tree rows of one KV head.
-bool encode_tree_map(CUtensorMap* map, const void* base, int B, int N, int Hkv) {
+// Rows [B][N][H][dh] (queries, or the tree rows k_new / v_new) as a 4-D tensor
+// (dh, H, N, B); a box is 64 dims of `box_h` consecutive heads of `box_n`
+// consecutive tree rows.
+bool encode_rows_map(CUtensorMap* map, const void* base, int B, int N, int H, int box_h, int box_n) {
   auto fn = encode_fn();
   if (!fn) return false;
   const cuuint64_t row = (cuuint64_t)kDH * 2;
-  cuuint64_t dims[4] = {(cuuint64_t)kDH, (cuuint64_t)Hkv, (cuuint64_t)N, (cuuint64_t)B};
-  cuuint64_t strides[3] = {row, row * Hkv, row * Hkv * N};
-  cuuint32_t box[4] = {64, 1, (cuuint32_t)kTcKeys, 1}, estr[4] = {1, 1, 1, 1};
+  cuuint64_t dims[4] = {(cuuint64_t)kDH, (cuuint64_t)H, (cuuint64_t)N, (cuuint64_t)B};
+  cuuint64_t strides[3] = {row, row * H, row * H * N};
+  cuuint32_t box[4] = {64, (cuuint32_t)box_h, (cuuint32_t)box_n, 1}, estr[4] = {1, 1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 4, const_cast<void*>(base), dims, strides, box, estr,
                   CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
                   CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
@@ -872,9 +921,10 @@ size_t tc_smem_bytes(int D) {
 
 bool attn_tc_supported(const medusa_tree_t& t, int Hq, const medusa_kv_t& c) {
   (void)t;
-  (void)Hq;
-  return c.dtype == MEDUSA_BF16 && c.head_dim == kDH && (c.page_size == 0 || c.page_size == 16) &&
-         encode_fn() != nullptr;
+  // a query tile is one TMA box of whole GQA groups
+  const int g = c.n_kv_heads > 0 ? Hq / c.n_kv_heads : 0;
+  return c.dtype == MEDUSA_BF16 && c.head_dim == kDH && (c.page_size == 0 || c.page_size == 16) && g > 0 &&
+         kTcRows % g == 0 && encode_fn() != nullptr;
 }
 
 // Split choice: enough CTAs to fill the SMs two per SM, in whole waves where possible,
@@ -923,9 +973,11 @@ cudaError_t launch_attn_tc(const AttnPlan& p, const medusa_tree_t& t, const void
                            const int32_t* L, const float* th_hi, const float* th_lo,
                            float scale_log2, float* out, float* lse, int32_t* status, void* ws,
                            cudaStream_t st) {
-  CUtensorMap mk, mv, mkn, mvn;
+  CUtensorMap mk, mv, mkn, mvn, mq;
   if (!encode_kv_map(&mk, c.k, c, p.B) || !encode_kv_map(&mv, c.v, c, p.B) ||
-      !encode_tree_map(&mkn, k_new, p.B, t.n_rows, p.Hkv) || !encode_tree_map(&mvn, v_new, p.B, t.n_rows, p.Hkv))
+      !encode_rows_map(&mkn, k_new, p.B, t.n_rows, p.Hkv, 1, kTcKeys) ||
+      !encode_rows_map(&mvn, v_new, p.B, t.n_rows, p.Hkv, 1, kTcKeys) ||
+      !encode_rows_map(&mq, q, p.B, t.n_rows, p.Hq, p.g, kTcRows / p.g))
     return cudaErrorInvalidValue;
   TcArgs a{};
   a.t = t;
@@ -967,11 +1019,11 @@ cudaError_t launch_attn_tc(const AttnPlan& p, const medusa_tree_t& t, const void
   if (c.page_size == 0) {
     e = cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<false>, mk, mv, mkn, mvn, a);
+    e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<false>, mk, mv, mkn, mvn, mq, a);
   } else {
     e = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<true>, mk, mv, mkn, mvn, a);
+    e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<true>, mk, mv, mkn, mvn, mq, a);
   }
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
