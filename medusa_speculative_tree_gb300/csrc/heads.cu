@@ -140,15 +140,20 @@ __global__ void __launch_bounds__(kThreads) gemv_kernel(GemvArgs a) {
 // ---- bulk-copy streaming GEMV (T <= 2) -------------------------------------------
 // One CTA per SM and matrix slice.  A producer warp streams groups of 8 weight rows,
 // one row segment of up to 8 KiB per consumer warp, with cp.async.bulk into a
-// two-stage shared-memory ring (up to 128 KiB in flight per SM); 8 consumer warps
+// shared-memory ring of NS stages of 64 KiB (three when the input rows leave room,
+// so that up to 192 KiB are in flight per SM); 8 consumer warps
 // each dot their row segment against the fp32 input rows kept in shared memory.
 // Rows longer than one segment are streamed as several column chunks.
 constexpr int kBulkConsumers = 8;
 constexpr int kBulkThreads = (kBulkConsumers + 1) * 32;
-constexpr int kBulkStages = 2;
 constexpr int kBulkSegBytes = 8192;
 
-template <typename EL, int TT>
+inline size_t bulk_smem_bytes(int TT, int d, int stages) {
+  return (size_t)((TT * d * 4 + 1023) & ~1023) + (size_t)stages * kBulkConsumers * kBulkSegBytes +
+         2 * (size_t)stages * sizeof(uint64_t);
+}
+
+template <typename EL, int TT, int kBulkStages>
 __global__ void __launch_bounds__(kBulkThreads, 1) gemv_bulk_kernel(GemvArgs a, int* __restrict__ err) {
   extern __shared__ __align__(1024) uint8_t smem_b[];
   constexpr int EPV = Elem<EL>::kPerVec;
@@ -394,11 +399,10 @@ cudaError_t gemv_dispatch(int TT, const GemvArgs& a, int n_mats, cudaStream_t st
   }
 }
 
-template <typename EL, int TT>
+template <typename EL, int TT, int NS>
 cudaError_t run_gemv_bulk(const GemvArgs& a, int n_mats, int* err, cudaStream_t st) {
-  const size_t smem = (size_t)((TT * a.d * 4 + 1023) & ~1023) +
-                      (size_t)kBulkStages * kBulkConsumers * kBulkSegBytes + 2 * kBulkStages * sizeof(uint64_t);
-  auto kern = gemv_bulk_kernel<EL, TT>;
+  const size_t smem = bulk_smem_bytes(TT, a.d, NS);
+  auto kern = gemv_bulk_kernel<EL, TT, NS>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int sms = 0, dev = 0;
@@ -412,12 +416,16 @@ cudaError_t run_gemv_bulk(const GemvArgs& a, int n_mats, int* err, cudaStream_t 
   return cudaGetLastError();
 }
 
-// T <= 2 and an input row that fits next to the ring: the bulk-copy kernel; else the
-// register-blocked kernel.
+constexpr size_t kSmemOptin = 227 * 1024;
+
+// T <= 2 and an input row that fits next to the ring: the bulk-copy kernel (three
+// stages when they fit); else the register-blocked kernel.
 template <typename EL>
 cudaError_t gemv_any(int TT, const GemvArgs& a, int n_mats, int* err, cudaStream_t st) {
   if (TT <= 2 && (size_t)TT * a.d * 4 <= 64 * 1024) {
-    return TT == 1 ? run_gemv_bulk<EL, 1>(a, n_mats, err, st) : run_gemv_bulk<EL, 2>(a, n_mats, err, st);
+    const bool three = bulk_smem_bytes(TT, a.d, 3) <= kSmemOptin;
+    if (TT == 1) return three ? run_gemv_bulk<EL, 1, 3>(a, n_mats, err, st) : run_gemv_bulk<EL, 1, 2>(a, n_mats, err, st);
+    return three ? run_gemv_bulk<EL, 2, 3>(a, n_mats, err, st) : run_gemv_bulk<EL, 2, 2>(a, n_mats, err, st);
   }
   return gemv_dispatch<EL>(TT, a, n_mats, st);
 }
@@ -456,8 +464,10 @@ HeadsPlan plan_heads(int T, int d, int V, int K, int topk) {
   off = align_up(off + (size_t)T * (K + 1) * V * sizeof(float), 256);
   p.off_cand = off;
   off = align_up(off + (size_t)T * (K + 1) * p.n_chunks * topk * sizeof(Cand), 256);
+  p.off_scand = off;                                       // weight-stream path: per-CTA lists
+  off = align_up(off + (size_t)(K + 1) * kHeadsStreamMaxGrid * topk * sizeof(Cand), 256);
   p.off_err = off;
-  off = align_up(off + sizeof(int), 256);
+  off = align_up(off + kHeadsCounterBytes, 256);
   p.bytes = off;
   (void)pow2_at_least;
   return p;
@@ -473,6 +483,9 @@ cudaError_t launch_heads(const HeadsPlan& p, const void* h, const void* w1, cons
   Cand* cand = (Cand*)(base + p.off_cand);
   int* err = (int*)(base + p.off_err);
   const int d = p.d, V = p.V, K = p.K, T = p.T;
+  // One hidden row in bf16: the persistent weight stream with in-stream top-k.
+  if (heads_stream_supported(T, d, V, K, p.topk, dt, h, w1, w2, w2_stride, w_lm, b1))
+    return launch_heads_stream(p, h, w1, b1, w2, w2_stride, w_lm, root, pool, logits_out, ws, st);
   cudaError_t e0 = cudaMemsetAsync(err, 0, sizeof(int), st);   // set by a weight-stream wait that gave up
   if (e0 != cudaSuccess) return e0;
   const size_t esz = dt == MEDUSA_BF16 ? 2 : 4;

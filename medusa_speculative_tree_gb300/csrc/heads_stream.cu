@@ -1,0 +1,526 @@
+// Medusa heads as one persistent weight stream with in-stream top-k ([CN] "Medusa
+// 的核心思路与系统位置"; [Math] "The Medusa head: math and shapes"; [M7.2] §0x02A,
+// §0x04D; [PartII] Part 4).
+//
+// For one hidden row (T = 1, bf16), the round streams every head weight exactly once:
+//   W1_k (K x [d, d]), then W_LM ([V, d], root = argmax), then W2_k (K x [V, d]).
+// A cooperative grid of one CTA per SM walks all 8-row groups of these matrices in one
+// interleaved order (group i goes to CTA i mod G), so the stream never stops between
+// matrices:
+//   - warp 8 (one lane) copies each group's 8 rows (up to 8 KiB each) with
+//     cp.async.bulk into a 3-stage ring (192 KiB in flight per SM at d = 4096);
+//   - warps 0-7 each dot one row of a stage against the input row held in registers
+//     (h for W1 and W_LM, z_k = h + SiLU(W1_k h + b1_k) for W2_k), element pairs
+//     through packed fp32x2 FMAs, so shared memory serves only the weights;
+//   - a W1 row writes z_k; a vocabulary row feeds a per-warp top-k list kept sorted
+//     across the warp's lanes (value desc, id asc);
+//   - warp 9 merges the 8 warp lists of a matrix into the CTA's top-k, publishes it,
+//     and the CTA that completes a matrix merges all CTAs' lists into root or pool.
+// W2_k rows need all of z: the CTAs count finished W1 work in global memory and a warp
+// waits (bounded) for the full count before its first W2 row; every CTA takes its W1
+// groups first and the W_LM groups next, so the count is complete long before.
+// All waits are bounded; on a timeout the call records an error and root / pool
+// become -1.
+#include <float.h>
+#include <limits.h>
+
+#include "common.cuh"
+#include "kernels.h"
+
+namespace medusa {
+
+namespace {
+
+constexpr int kSConsumers = 8;                 // consumer warps = rows per group
+constexpr int kSProducer = 8;                  // warp index
+constexpr int kSMerger = 9;                    // warp index
+constexpr int kSThreads = 10 * 32;
+constexpr int kSStages = 3;
+constexpr int kSMaxU4 = 16;                    // 16-byte pieces of a row per lane (d <= 4096)
+constexpr int kSSegMax = 8192;                 // bytes of one row chunk in a stage
+constexpr int kSMaxGrid = kHeadsStreamMaxGrid;
+
+struct SCand {
+  float v;
+  int i;
+};
+
+struct StreamArgs {
+  const uint16_t* h;          // [d]
+  const uint16_t* w1;         // [K][d][d]
+  const uint16_t* b1;         // [K][d] or null
+  const uint16_t* w2;         // W2_k = w2 + k * w2_stride, [V][d]
+  int64_t w2_stride;
+  const uint16_t* w_lm;       // [V][d] or null (then no root)
+  int d, V, K, topk;
+  float* z;                   // [K][d]
+  float* logits_out;          // [K + 1][V] or null
+  SCand* scand;               // [K + 1][G][topk]
+  int* err;
+  int* cnt;                   // [0] warps done with W1, [1 + j] CTAs done with top-k matrix j
+  int32_t* root;
+  int32_t* pool;              // [K][topk]
+};
+
+// Matrices in stream order: 0..K-1 = W1_k, K = W_LM (if present), then W2_k.
+// Top-k matrix index j: 0 = W_LM, 1 + k = W2_k.
+struct Item {
+  int kind;      // 0 W1, 1 LM, 2 W2
+  int k;         // head (W1, W2)
+  int grp;       // row group within the matrix
+  int mat;       // stream matrix index
+};
+
+__device__ __forceinline__ Item map_item(int i, int K, int g_w1, int g_v, bool lm) {
+  Item it;
+  const int n_w1 = K * g_w1;
+  if (i < n_w1) {
+    it.kind = 0; it.k = (int)(i / g_w1); it.grp = (int)(i % g_w1); it.mat = it.k;
+    return it;
+  }
+  int r = i - n_w1;
+  if (lm) {
+    if (r < g_v) {
+      it.kind = 1; it.k = 0; it.grp = (int)r; it.mat = K;
+      return it;
+    }
+    r -= g_v;
+  }
+  it.kind = 2; it.k = (int)(r / g_v); it.grp = (int)(r % g_v); it.mat = K + 1 + it.k;
+  return it;
+}
+
+// Bounded wait that also ends when another warp of the CTA has given up.
+__device__ __forceinline__ bool s_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if ((it & 255u) == 255u && global_ns() - t0 > 2000000000ull) return false;
+  }
+}
+
+__device__ __forceinline__ void warp_argbest(float& v, int& i) {
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+    const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+    if (ranks_before(ov, oi, v, i)) { v = ov; i = oi; }
+  }
+}
+
+// 10 warps: the register file is shared as if by 12, 168 registers each; the input
+// row takes 128 of them.
+__global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const StreamArgs a) {
+  extern __shared__ __align__(1024) uint8_t smem_s[];
+  const int d = a.d, K = a.K, V = a.V;
+  const int n_chunks = (2 * d + kSSegMax - 1) / kSSegMax;  // 1 while d <= 4096
+  const int seg = 2 * d / n_chunks;                         // bytes of one row chunk
+  const int u4c = seg / 512;                                // 16-byte pieces per lane per chunk (<= 16)
+  uint8_t* ring = smem_s;                                  // [stages][8][seg]
+  SCand* lists = reinterpret_cast<SCand*>(ring + kSStages * kSConsumers * seg);   // [2][consumers][32]
+  uint64_t* bars = reinterpret_cast<uint64_t*>(lists + 2 * kSConsumers * 32);
+  __shared__ int abort_flag;
+  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[kSStages]);
+  const uint32_t lfull0 = smem_u32(&bars[2 * kSStages]), lfree0 = smem_u32(&bars[2 * kSStages + 2]);
+  const volatile int* abortp = &abort_flag;
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = gridDim.x, c = blockIdx.x;
+  const bool lm = a.w_lm != nullptr;
+  const int g_w1 = (d + kSConsumers - 1) / kSConsumers, g_v = (V + kSConsumers - 1) / kSConsumers;
+  const int n_items = K * g_w1 + (lm ? g_v : 0) + K * g_v;
+  const int my_items = n_items > c ? (n_items - 1 - c) / G + 1 : 0;
+  const int my_units = my_items * n_chunks;                 // (item, row chunk) stages of this CTA
+  const int n_top = K + 1;                                  // top-k matrices j = 0..K
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < kSStages; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, kSConsumers);
+    }
+    for (int p = 0; p < 2; ++p) {
+      mbar_init(lfull0 + 8 * p, kSConsumers);
+      mbar_init(lfree0 + 8 * p, 1);
+    }
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  __syncthreads();
+  auto give_up = [&]() {
+    *const_cast<volatile int*>(abortp) = 1;
+    atomicExch(a.err, 1);
+  };
+
+  if (warp == kSProducer) {
+    // ---- weight stream --------------------------------------------------------------
+    if (lane != 0) return;
+    int issued = 0;
+    for (int u = 0; u < my_units; ++u) {
+      const int s = u % kSStages;
+      const uint32_t ph = (uint32_t)((u / kSStages) & 1);
+      if (!s_wait(empty0 + 8 * s, ph ^ 1u, abortp)) { give_up(); break; }
+      const int n = u / n_chunks, ch = u - n * n_chunks;
+      const Item it = map_item(c + n * G, K, g_w1, g_v, lm);
+      const uint16_t* base = it.kind == 0 ? a.w1 + (int64_t)it.k * d * d
+                           : it.kind == 1 ? a.w_lm : a.w2 + (int64_t)it.k * a.w2_stride;
+      const int n_rows = it.kind == 0 ? d : V;
+      const int row0 = it.grp * kSConsumers;
+      const int rows = min(kSConsumers, n_rows - row0);
+      mbar_expect_tx(full0 + 8 * s, (uint32_t)(rows * seg));
+      for (int r = 0; r < rows; ++r)
+        bulk_copy_g2s(smem_u32(ring + (s * kSConsumers + r) * seg),
+                      base + (int64_t)(row0 + r) * d + (int64_t)ch * (seg / 2), (uint32_t)seg, full0 + 8 * s);
+      issued = u + 1;
+    }
+    // Copies still in flight (only after giving up) must land before the CTA exits.
+    for (int u = issued - kSStages; u < issued; ++u)
+      if (u >= 0) mbar_wait(full0 + 8 * (u % kSStages), (uint32_t)((u / kSStages) & 1), 100000000ull);
+    return;
+  }
+
+  if (warp == kSMerger) {
+    // ---- per-matrix top-k merges --------------------------------------------------
+    uint32_t ph_full[2] = {0u, 0u};
+    // matrices this CTA touches: its items are c, c + G, ...; matrix ranges are contiguous
+    const int n_w1 = K * g_w1;
+    for (int j = 0; j < n_top; ++j) {
+      if (j == 0 && !lm) {                              // keeps the buffer-0 arrivals one per j
+        if (lane == 0) mbar_arrive(lfree0);
+        continue;
+      }
+      const int kk = j == 0 ? 1 : a.topk;
+      const int lo = n_w1 + (j == 0 ? 0 : (lm ? g_v : 0) + (j - 1) * g_v);
+      const int hi = lo + g_v;                          // items [lo, hi) belong to matrix j
+      const int first = lo <= c ? c : c + ((lo - c + G - 1) / G) * G;
+      const bool mine = first < hi && first < n_items;
+      const int p = j & 1;
+      float bv = -INFINITY;
+      int bi = INT_MAX;
+      bool ok = false;
+      if (mine && !*abortp) {
+        ok = __all_sync(0xffffffffu, s_wait(lfull0 + 8 * p, ph_full[p], abortp));
+        ph_full[p] ^= 1u;
+        if (!ok) give_up();
+      }
+      SCand* out = a.scand + ((int64_t)j * G + c) * a.topk;
+      if (ok) {
+        // one sorted list of kk entries per consumer warp: entry e of warp w at lists[p][w][e]
+        float ev[8];
+        int ei[8];
+#pragma unroll
+        for (int q = 0; q < 8; ++q) {
+          const int f = lane + 32 * q;                  // flattened index w * kk + e
+          const int w = f / kk, e = f % kk;
+          const bool valid = f < kSConsumers * kk;
+          ev[q] = valid ? lists[(p * kSConsumers + w) * 32 + e].v : -INFINITY;
+          ei[q] = valid ? lists[(p * kSConsumers + w) * 32 + e].i : INT_MAX;
+        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(lfree0 + 8 * p);     // the lists buffer may be refilled
+        for (int r = 0; r < kk; ++r) {
+          float v = -INFINITY;
+          int i = INT_MAX, q_best = -1;
+#pragma unroll
+          for (int q = 0; q < 8; ++q)
+            if (ei[q] != INT_MAX && (q_best < 0 || ranks_before(ev[q], ei[q], v, i))) { v = ev[q]; i = ei[q]; q_best = q; }
+          float wv = v;
+          int wi = i;
+          warp_argbest(wv, wi);
+          if (q_best >= 0 && wi == i && wi != INT_MAX) {
+#pragma unroll
+            for (int q = 0; q < 8; ++q)
+              if (q == q_best) ei[q] = INT_MAX;
+          }
+          if (lane == r) { bv = wv; bi = wi; }
+        }
+      } else {
+        if (lane == 0) mbar_arrive(lfree0 + 8 * p);
+      }
+      if (lane < a.topk) out[lane] = SCand{lane < kk ? bv : -INFINITY, lane < kk ? bi : INT_MAX};
+      __threadfence();
+      __syncwarp();
+      int t = 0;
+      if (lane == 0) t = atomicAdd(&a.cnt[1 + j], 1);
+      t = __shfl_sync(0xffffffffu, t, 0);
+      if (t != G - 1) continue;
+      // ---- this CTA completed matrix j: merge all CTAs' sorted lists ----------------
+      __threadfence();
+      constexpr int kLpl = kSMaxGrid / 32;             // lists per lane
+      float hv[kLpl];
+      int hid[kLpl], hp[kLpl];
+#pragma unroll
+      for (int q = 0; q < kLpl; ++q) {
+        const int l = lane + 32 * q;
+        hp[q] = 0;
+        if (l < G) {
+          hv[q] = __ldcg(&a.scand[((int64_t)j * G + l) * a.topk].v);
+          hid[q] = __ldcg(&a.scand[((int64_t)j * G + l) * a.topk].i);
+        } else {
+          hv[q] = -INFINITY;
+          hid[q] = INT_MAX;
+        }
+      }
+      const bool bad = *reinterpret_cast<volatile int*>(a.err) != 0;
+      for (int r = 0; r < kk; ++r) {
+        float v = -INFINITY;
+        int i = INT_MAX, q_best = -1;
+#pragma unroll
+        for (int q = 0; q < kLpl; ++q)
+          if (hid[q] != INT_MAX && (q_best < 0 || ranks_before(hv[q], hid[q], v, i))) { v = hv[q]; i = hid[q]; q_best = q; }
+        float wv = v;
+        int wi = i;
+        warp_argbest(wv, wi);
+        if (q_best >= 0 && wi == i && wi != INT_MAX) {
+#pragma unroll
+          for (int q = 0; q < kLpl; ++q) {
+            if (q != q_best) continue;
+            const int l = lane + 32 * q;
+            hp[q] += 1;
+            if (hp[q] < kk) {
+              hv[q] = __ldcg(&a.scand[((int64_t)j * G + l) * a.topk + hp[q]].v);
+              hid[q] = __ldcg(&a.scand[((int64_t)j * G + l) * a.topk + hp[q]].i);
+            } else {
+              hv[q] = -INFINITY;
+              hid[q] = INT_MAX;
+            }
+          }
+        }
+        if (lane == 0) {
+          const int id = (bad || wi == INT_MAX) ? -1 : wi;
+          if (j == 0) a.root[0] = id;
+          else a.pool[(int64_t)(j - 1) * a.topk + r] = id;
+        }
+      }
+    }
+    return;
+  }
+
+  // ---- consumer warps: one row of each group ------------------------------------------
+  const int nv = d / 256;                                   // 16-byte chunks per lane
+  float2 xr[kSMaxU4][4];                                    // input row, element pairs
+  int cur_mat = -1;
+  bool w1_signalled = false;
+  float lv = -INFINITY;                                     // this lane's entry of the warp's list
+  int li = INT_MAX;
+  bool ok = true;
+  auto publish = [&](int j) {
+    const int p = j & 1;
+    lists[(p * kSConsumers + warp) * 32 + lane] = SCand{lv, li};
+    __syncwarp();
+    if (lane == 0) mbar_arrive(lfull0 + 8 * p);
+    lv = -INFINITY;
+    li = INT_MAX;
+  };
+  auto signal_w1 = [&]() {
+    __threadfence();
+    __syncwarp();
+    if (lane == 0) atomicAdd(&a.cnt[0], 1);
+    w1_signalled = true;
+  };
+  for (int n = 0; n < my_items && ok; ++n) {
+    const Item it = map_item(c + n * G, K, g_w1, g_v, lm);
+    if (it.mat != cur_mat) {
+      if (cur_mat > K || (cur_mat == K && lm)) publish(cur_mat - K);   // leaving a top-k matrix
+      if (!w1_signalled && it.kind != 0) signal_w1();
+      if (it.kind == 2) {
+        // z must be complete: every consumer warp of every CTA has finished its W1 rows
+        bool done = false;
+        if (lane == 0) {
+          const uint64_t t0 = global_ns();
+          for (uint32_t sp = 0;; ++sp) {
+            int v;
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.cnt) : "memory");
+            if (v >= G * kSConsumers) { done = true; break; }
+            if (*abortp) break;
+            if ((sp & 63u) == 63u && global_ns() - t0 > 2000000000ull) break;
+          }
+        }
+        done = __shfl_sync(0xffffffffu, done, 0);
+        if (!done) { if (lane == 0) give_up(); ok = false; break; }
+      }
+      if (it.kind == 2 || it.kind == 1) {
+        const int j = it.kind == 1 ? 0 : 1 + it.k;
+        if (j >= 2) {
+          // The lists buffer of j was used by j - 2: wait until the merge warp read it.
+          // The merge warp arrives once for every j in order, so the arrival for j - 2
+          // completes phase (j - 2) / 2 of its buffer.
+          const int p = j & 1;
+          if (!__all_sync(0xffffffffu, s_wait(lfree0 + 8 * p, ((j - 2) >> 1) & 1, abortp))) {
+            if (lane == 0) give_up();
+            ok = false;
+            break;
+          }
+        }
+      }
+      // input row of this matrix into registers
+      if (it.kind == 2) {
+        const float* zk = a.z + (int64_t)it.k * d;
+#pragma unroll
+        for (int q = 0; q < kSMaxU4; ++q) {
+          if (q < nv) {
+            const float4 u0 = __ldcg(reinterpret_cast<const float4*>(zk + 8 * (lane + 32 * q)));
+            const float4 u1 = __ldcg(reinterpret_cast<const float4*>(zk + 8 * (lane + 32 * q) + 4));
+            xr[q][0] = make_float2(u0.x, u0.y);
+            xr[q][1] = make_float2(u0.z, u0.w);
+            xr[q][2] = make_float2(u1.x, u1.y);
+            xr[q][3] = make_float2(u1.z, u1.w);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int q = 0; q < kSMaxU4; ++q) {
+          if (q < nv) {
+            float f[8];
+            Elem<uint16_t>::unpack(__ldg(reinterpret_cast<const uint4*>(a.h + 8 * (lane + 32 * q))), f);
+#pragma unroll
+            for (int e = 0; e < 4; ++e) xr[q][e] = make_float2(f[2 * e], f[2 * e + 1]);
+          }
+        }
+      }
+      cur_mat = it.mat;
+    }
+    const int n_rows = it.kind == 0 ? d : V;
+    const int row = it.grp * kSConsumers + warp;
+    float2 p[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+    for (int ch = 0; ch < n_chunks; ++ch) {
+      const int u = n * n_chunks + ch;
+      const int s = u % kSStages;
+      if (!__all_sync(0xffffffffu, s_wait(full0 + 8 * s, (uint32_t)((u / kSStages) & 1), abortp))) {
+        if (lane == 0) give_up();
+        ok = false;
+        break;
+      }
+      const uint8_t* w = ring + (s * kSConsumers + warp) * seg;
+      if (row < n_rows) {
+#pragma unroll
+        for (int q = 0; q < kSMaxU4; ++q) {
+          if (q < u4c) {
+            const uint4 v = *reinterpret_cast<const uint4*>(w + (lane + 32 * q) * 16);
+            const uint32_t wq[4] = {v.x, v.y, v.z, v.w};
+#pragma unroll
+            for (int e = 0; e < 4; ++e) {
+              const float2 wf = make_float2(__uint_as_float(wq[e] << 16), __uint_as_float(wq[e] & 0xFFFF0000u));
+              p[e] = __ffma2_rn(wf, xr[q][e], p[e]);
+            }
+          }
+        }
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+    }
+    if (!ok) break;
+    if (row >= n_rows) continue;
+    float acc = ((p[0].x + p[0].y) + (p[1].x + p[1].y)) + ((p[2].x + p[2].y) + (p[3].x + p[3].y));
+    acc = warp_sum(acc);
+    acc = __shfl_sync(0xffffffffu, acc, 0);                   // one value for every lane
+    if (it.kind == 0) {
+      if (lane == 0) {
+        float v = acc;
+        if (a.b1) v += Elem<uint16_t>::load(a.b1, (int64_t)it.k * d + row);
+        const float hv = Elem<uint16_t>::load(a.h, row);
+        a.z[(int64_t)it.k * d + row] = hv + v / (1.f + expf(-v));   // h + SiLU(W1 h + b1)
+      }
+    } else {
+      const int j = it.kind == 1 ? 0 : 1 + it.k;
+      const int kk = j == 0 ? 1 : a.topk;
+      if (a.logits_out && lane == 0) a.logits_out[(int64_t)j * V + row] = acc;
+      // insert (acc, row) into the sorted list held one entry per lane
+      const bool before = lane < kk && ranks_before(acc, row, lv, li);
+      const unsigned mask = __ballot_sync(0xffffffffu, before);
+      if (mask) {
+        const int pos = __ffs(mask) - 1;
+        const float uv = __shfl_up_sync(0xffffffffu, lv, 1);
+        const int ui = __shfl_up_sync(0xffffffffu, li, 1);
+        if (lane == pos) { lv = acc; li = row; }
+        else if (lane > pos && lane < kk) { lv = uv; li = ui; }
+      }
+    }
+  }
+  if (ok && (cur_mat > K || (cur_mat == K && lm))) publish(cur_mat - K);
+  if (!w1_signalled) signal_w1();
+}
+
+}  // namespace
+
+size_t heads_stream_smem(int d) {
+  const int n_chunks = (2 * d + kSSegMax - 1) / kSSegMax;
+  return (size_t)kSStages * kSConsumers * (2 * d / n_chunks) + 2 * kSConsumers * 32 * sizeof(SCand) +
+         4 * kSStages * sizeof(uint64_t);
+}
+
+bool heads_stream_supported(int T, int d, int V, int K, int topk, medusa_dtype dt, const void* h, const void* w1,
+                            const void* w2, int64_t w2_stride, const void* w_lm, const void* b1) {
+  auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  // one stage segment per row: d <= 4096 (8 KiB rows)
+  if (T != 1 || dt != MEDUSA_BF16 || K < 1 || d % 256 != 0 || d > 4096 || V < 1 || topk > 32)
+    return false;
+  if (!al(h) || !al(w1) || !al(w2) || !al(w_lm) || (w2_stride * 2) % 16 != 0 || w2_stride < 0) return false;
+  (void)b1;
+  int dev = 0, coop = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  if (coop == 0 || sms < 1 || heads_stream_smem(d) > 227 * 1024) return false;
+  // every CTA must be resident at once (one per SM)
+  if (cudaFuncSetAttribute(heads_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                           (int)heads_stream_smem(d)) != cudaSuccess)
+    return false;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, heads_stream_kernel, kSThreads, heads_stream_smem(d)) !=
+      cudaSuccess)
+    return false;
+  return per_sm >= 1;
+}
+
+cudaError_t launch_heads_stream(const HeadsPlan& p, const void* h, const void* w1, const void* b1, const void* w2,
+                                int64_t w2_stride, const void* w_lm, int32_t* root, int32_t* pool,
+                                float* logits_out, void* ws, cudaStream_t st) {
+  char* base = (char*)ws;
+  StreamArgs a{};
+  a.h = (const uint16_t*)h;
+  a.w1 = (const uint16_t*)w1;
+  a.b1 = (const uint16_t*)b1;
+  a.w2 = (const uint16_t*)w2;
+  a.w2_stride = w2_stride;
+  a.w_lm = (const uint16_t*)w_lm;
+  a.d = p.d;
+  a.V = p.V;
+  a.K = p.K;
+  a.topk = p.topk;
+  a.z = (float*)(base + p.off_z);
+  a.logits_out = logits_out;
+  a.scand = (SCand*)(base + p.off_scand);
+  a.err = (int*)(base + p.off_err);
+  a.cnt = a.err + 4;
+  a.root = root;
+  a.pool = pool;
+  const size_t smem = heads_stream_smem(p.d);
+  cudaError_t e = cudaFuncSetAttribute(heads_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0, per_sm = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, heads_stream_kernel, kSThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
+  int G = sms < kSMaxGrid ? sms : kSMaxGrid;
+  // error flag and counters start at zero
+  e = cudaMemsetAsync(a.err, 0, kHeadsCounterBytes, st);
+  if (e != cudaSuccess) return e;
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(G);
+  cfg.blockDim = dim3(kSThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, heads_stream_kernel, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace medusa

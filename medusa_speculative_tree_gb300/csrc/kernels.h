@@ -16,9 +16,18 @@ struct HeadsPlan {
   int tokens_per_pass;   // tokens whose fp32 x rows fit in shared memory at once
   int chunk;             // logits per partial top-k CTA
   int n_chunks;          // ceil(V / chunk)
-  size_t off_z, off_logits, off_cand, off_err, bytes;
+  size_t off_z, off_logits, off_cand, off_scand, off_err, bytes;
 };
+// Weight-stream path (heads_stream.cu): at most this many CTAs, and an error flag plus
+// completion counters in the first kHeadsCounterBytes at off_err (zeroed every call).
+constexpr int kHeadsStreamMaxGrid = 256;
+constexpr size_t kHeadsCounterBytes = 256;
 HeadsPlan plan_heads(int T, int d, int V, int K, int topk);
+bool heads_stream_supported(int T, int d, int V, int K, int topk, medusa_dtype dt, const void* h, const void* w1,
+                            const void* w2, int64_t w2_stride, const void* w_lm, const void* b1);
+cudaError_t launch_heads_stream(const HeadsPlan& p, const void* h, const void* w1, const void* b1, const void* w2,
+                                int64_t w2_stride, const void* w_lm, int32_t* root, int32_t* pool,
+                                float* logits_out, void* ws, cudaStream_t st);
 cudaError_t launch_heads(const HeadsPlan& p, const void* h, const void* w1, const void* b1,
                          const void* w2, int64_t w2_stride, const void* w_lm, medusa_dtype dt,
                          int32_t* root, int32_t* pool, float* logits_out, void* ws,
