@@ -100,6 +100,12 @@ __device__ __forceinline__ bool s_wait(uint32_t bar, uint32_t parity, const vola
   }
 }
 
+// One candidate from global memory, through L2 (written by other CTAs).
+__device__ __forceinline__ SCand ld_cand_cg(const SCand* p) {
+  const float2 f = __ldcg(reinterpret_cast<const float2*>(p));
+  return SCand{f.x, __float_as_int(f.y)};
+}
+
 __device__ __forceinline__ void warp_argbest(float& v, int& i) {
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) {
@@ -118,11 +124,13 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
   const int seg = 2 * d / n_chunks;                         // bytes of one row chunk
   const int u4c = seg / 512;                                // 16-byte pieces per lane per chunk (<= 16)
   uint8_t* ring = smem_s;                                  // [stages][8][seg]
-  SCand* lists = reinterpret_cast<SCand*>(ring + kSStages * kSConsumers * seg);   // [2][consumers][32]
+  uint8_t* xbuf = ring + kSStages * kSConsumers * seg;      // input row of the current matrix (h bf16 or z_k fp32)
+  SCand* lists = reinterpret_cast<SCand*>(xbuf + 4 * d);   // [2][consumers][32]
   uint64_t* bars = reinterpret_cast<uint64_t*>(lists + 2 * kSConsumers * 32);
   __shared__ int abort_flag;
   const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[kSStages]);
   const uint32_t lfull0 = smem_u32(&bars[2 * kSStages]), lfree0 = smem_u32(&bars[2 * kSStages + 2]);
+  const uint32_t xfull = smem_u32(&bars[2 * kSStages + 4]), xempty = smem_u32(&bars[2 * kSStages + 5]);
   const volatile int* abortp = &abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -144,6 +152,8 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
       mbar_init(lfull0 + 8 * p, kSConsumers);
       mbar_init(lfree0 + 8 * p, 1);
     }
+    mbar_init(xfull, 1);
+    mbar_init(xempty, kSConsumers);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -155,13 +165,38 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
   if (warp == kSProducer) {
     // ---- weight stream --------------------------------------------------------------
     if (lane != 0) return;
-    int issued = 0;
+    int issued = 0, x_loads = 0, x_src = -2;
     for (int u = 0; u < my_units; ++u) {
       const int s = u % kSStages;
       const uint32_t ph = (uint32_t)((u / kSStages) & 1);
-      if (!s_wait(empty0 + 8 * s, ph ^ 1u, abortp)) { give_up(); break; }
       const int n = u / n_chunks, ch = u - n * n_chunks;
       const Item it = map_item(c + n * G, K, g_w1, g_v, lm);
+      // The input row of the item's matrix (h, or z_k for W2_k) goes through the same
+      // stream into the x buffer, once all consumer warps took the previous one.
+      const int src = it.kind == 2 ? it.k : -1;
+      if (ch == 0 && src != x_src) {
+        if (x_loads > 0 && !s_wait(xempty, (uint32_t)((x_loads - 1) & 1), abortp)) { give_up(); break; }
+        if (src >= 0 && x_src < 0) {
+          // z is complete once every consumer warp of every CTA has finished its W1 rows
+          bool done = false;
+          const uint64_t t0 = global_ns();
+          for (uint32_t sp = 0;; ++sp) {
+            int v;
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.cnt) : "memory");
+            if (v >= G * kSConsumers) { done = true; break; }
+            if (*abortp) break;
+            if ((sp & 63u) == 63u && global_ns() - t0 > 2000000000ull) break;
+          }
+          if (!done) { give_up(); break; }
+          asm volatile("fence.proxy.async.global;" ::: "memory");   // the bulk copy reads what other SMs wrote
+        }
+        const uint32_t xb = src >= 0 ? 4u * d : 2u * d;
+        mbar_expect_tx(xfull, xb);
+        bulk_copy_g2s(smem_u32(xbuf), src >= 0 ? (const void*)(a.z + (int64_t)src * d) : (const void*)a.h, xb, xfull);
+        x_src = src;
+        ++x_loads;
+      }
+      if (!s_wait(empty0 + 8 * s, ph ^ 1u, abortp)) { give_up(); break; }
       const uint16_t* base = it.kind == 0 ? a.w1 + (int64_t)it.k * d * d
                            : it.kind == 1 ? a.w_lm : a.w2 + (int64_t)it.k * a.w2_stride;
       const int n_rows = it.kind == 0 ? d : V;
@@ -176,6 +211,7 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
     // Copies still in flight (only after giving up) must land before the CTA exits.
     for (int u = issued - kSStages; u < issued; ++u)
       if (u >= 0) mbar_wait(full0 + 8 * (u % kSStages), (uint32_t)((u / kSStages) & 1), 100000000ull);
+    if (x_loads > 0) mbar_wait(xfull, (uint32_t)((x_loads - 1) & 1), 100000000ull);
     return;
   }
 
@@ -245,7 +281,19 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
       t = __shfl_sync(0xffffffffu, t, 0);
       if (t != G - 1) continue;
       // ---- this CTA completed matrix j: merge all CTAs' sorted lists ----------------
+      // Lane l keeps the current head of lists l, l + 32, ...; each round takes the best
+      // head and advances its list.  For the last matrix the lists are first staged in
+      // the idle ring (this CTA has streamed all its items), so that advancing a list
+      // is a shared-memory load.
       __threadfence();
+      const SCand* gl = a.scand + (int64_t)j * G * a.topk;
+      const bool staged = mine && j == n_top - 1;
+      SCand* st = reinterpret_cast<SCand*>(ring);
+      if (staged) {
+        for (int i = lane; i < G * a.topk; i += 32) st[i] = ld_cand_cg(gl + i);
+        __syncwarp();
+      }
+      auto entry = [&](int l, int e) -> SCand { return staged ? st[l * a.topk + e] : ld_cand_cg(gl + l * a.topk + e); };
       constexpr int kLpl = kSMaxGrid / 32;             // lists per lane
       float hv[kLpl];
       int hid[kLpl], hp[kLpl];
@@ -253,12 +301,12 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
       for (int q = 0; q < kLpl; ++q) {
         const int l = lane + 32 * q;
         hp[q] = 0;
+        hv[q] = -INFINITY;
+        hid[q] = INT_MAX;
         if (l < G) {
-          hv[q] = __ldcg(&a.scand[((int64_t)j * G + l) * a.topk].v);
-          hid[q] = __ldcg(&a.scand[((int64_t)j * G + l) * a.topk].i);
-        } else {
-          hv[q] = -INFINITY;
-          hid[q] = INT_MAX;
+          const SCand e = entry(l, 0);
+          hv[q] = e.v;
+          hid[q] = e.i;
         }
       }
       const bool bad = *reinterpret_cast<volatile int*>(a.err) != 0;
@@ -278,8 +326,9 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
             const int l = lane + 32 * q;
             hp[q] += 1;
             if (hp[q] < kk) {
-              hv[q] = __ldcg(&a.scand[((int64_t)j * G + l) * a.topk + hp[q]].v);
-              hid[q] = __ldcg(&a.scand[((int64_t)j * G + l) * a.topk + hp[q]].i);
+              const SCand e = entry(l, hp[q]);
+              hv[q] = e.v;
+              hid[q] = e.i;
             } else {
               hv[q] = -INFINITY;
               hid[q] = INT_MAX;
@@ -299,7 +348,7 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
   // ---- consumer warps: one row of each group ------------------------------------------
   const int nv = d / 256;                                   // 16-byte chunks per lane
   float2 xr[kSMaxU4][4];                                    // input row, element pairs
-  int cur_mat = -1;
+  int cur_mat = -1, x_src = -2, x_loads = 0;
   bool w1_signalled = false;
   float lv = -INFINITY;                                     // this lane's entry of the warp's list
   int li = INT_MAX;
@@ -323,22 +372,6 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
     if (it.mat != cur_mat) {
       if (cur_mat > K || (cur_mat == K && lm)) publish(cur_mat - K);   // leaving a top-k matrix
       if (!w1_signalled && it.kind != 0) signal_w1();
-      if (it.kind == 2) {
-        // z must be complete: every consumer warp of every CTA has finished its W1 rows
-        bool done = false;
-        if (lane == 0) {
-          const uint64_t t0 = global_ns();
-          for (uint32_t sp = 0;; ++sp) {
-            int v;
-            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.cnt) : "memory");
-            if (v >= G * kSConsumers) { done = true; break; }
-            if (*abortp) break;
-            if ((sp & 63u) == 63u && global_ns() - t0 > 2000000000ull) break;
-          }
-        }
-        done = __shfl_sync(0xffffffffu, done, 0);
-        if (!done) { if (lane == 0) give_up(); ok = false; break; }
-      }
       if (it.kind == 2 || it.kind == 1) {
         const int j = it.kind == 1 ? 0 : 1 + it.k;
         if (j >= 2) {
@@ -353,30 +386,43 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
           }
         }
       }
-      // input row of this matrix into registers
-      if (it.kind == 2) {
-        const float* zk = a.z + (int64_t)it.k * d;
+      // input row into registers when its source changes (h for W1 and W_LM, z_k for
+      // W2_k): the producer staged it in the x buffer
+      const int src = it.kind == 2 ? it.k : -1;
+      if (src != x_src) {
+        if (!__all_sync(0xffffffffu, s_wait(xfull, (uint32_t)(x_loads & 1), abortp))) {
+          if (lane == 0) give_up();
+          ok = false;
+          break;
+        }
+        if (src >= 0) {
+          const float* zk = reinterpret_cast<const float*>(xbuf);
 #pragma unroll
-        for (int q = 0; q < kSMaxU4; ++q) {
-          if (q < nv) {
-            const float4 u0 = __ldcg(reinterpret_cast<const float4*>(zk + 8 * (lane + 32 * q)));
-            const float4 u1 = __ldcg(reinterpret_cast<const float4*>(zk + 8 * (lane + 32 * q) + 4));
-            xr[q][0] = make_float2(u0.x, u0.y);
-            xr[q][1] = make_float2(u0.z, u0.w);
-            xr[q][2] = make_float2(u1.x, u1.y);
-            xr[q][3] = make_float2(u1.z, u1.w);
+          for (int q = 0; q < kSMaxU4; ++q) {
+            if (q < nv) {
+              const float4 u0 = *reinterpret_cast<const float4*>(zk + 8 * (lane + 32 * q));
+              const float4 u1 = *reinterpret_cast<const float4*>(zk + 8 * (lane + 32 * q) + 4);
+              xr[q][0] = make_float2(u0.x, u0.y);
+              xr[q][1] = make_float2(u0.z, u0.w);
+              xr[q][2] = make_float2(u1.x, u1.y);
+              xr[q][3] = make_float2(u1.z, u1.w);
+            }
+          }
+        } else {
+#pragma unroll
+          for (int q = 0; q < kSMaxU4; ++q) {
+            if (q < nv) {
+              float f[8];
+              Elem<uint16_t>::unpack(*reinterpret_cast<const uint4*>(xbuf + 16 * (lane + 32 * q)), f);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) xr[q][e] = make_float2(f[2 * e], f[2 * e + 1]);
+            }
           }
         }
-      } else {
-#pragma unroll
-        for (int q = 0; q < kSMaxU4; ++q) {
-          if (q < nv) {
-            float f[8];
-            Elem<uint16_t>::unpack(__ldg(reinterpret_cast<const uint4*>(a.h + 8 * (lane + 32 * q))), f);
-#pragma unroll
-            for (int e = 0; e < 4; ++e) xr[q][e] = make_float2(f[2 * e], f[2 * e + 1]);
-          }
-        }
+        __syncwarp();
+        if (lane == 0) mbar_arrive(xempty);               // the x buffer may be refilled
+        x_src = src;
+        ++x_loads;
       }
       cur_mat = it.mat;
     }
@@ -445,8 +491,8 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
 
 size_t heads_stream_smem(int d) {
   const int n_chunks = (2 * d + kSSegMax - 1) / kSSegMax;
-  return (size_t)kSStages * kSConsumers * (2 * d / n_chunks) + 2 * kSConsumers * 32 * sizeof(SCand) +
-         4 * kSStages * sizeof(uint64_t);
+  return (size_t)kSStages * kSConsumers * (2 * d / n_chunks) + 4 * (size_t)d + 2 * kSConsumers * 32 * sizeof(SCand) +
+         (2 * kSStages + 8) * sizeof(uint64_t);
 }
 
 bool heads_stream_supported(int T, int d, int V, int K, int topk, medusa_dtype dt, const void* h, const void* w1,
