@@ -3,22 +3,24 @@
 // §0x04D; [PartII] Part 4).
 //
 // For one hidden row (T = 1, bf16), the round streams every head weight exactly once:
-//   W1_k (K x [d, d]), then W_LM ([V, d], root = argmax), then W2_k (K x [V, d]).
-// A cooperative grid of one CTA per SM walks all 8-row groups of these matrices in one
-// interleaved order (group i goes to CTA i mod G), so the stream never stops between
-// matrices:
+// W1_k (K x [d, d]), W_LM ([V, d], root = argmax) and W2_k (K x [V, d]).  A cooperative
+// grid of one CTA per SM walks all 8-row groups of these matrices in one interleaved
+// order (group i goes to CTA i mod G), so the stream never stops between matrices:
+//   W1_0..W1_{K-1}, the first half of W_LM, W2_0..W2_{K-1}, the second half of W_LM.
+// The first half of W_LM sits between W1 and W2, so z is complete everywhere by the
+// time any CTA needs it; the second half comes last, so the matrix whose top-k merge
+// is exposed at the end is W_LM, whose top-k is a single entry.
 //   - warp 8 (one lane) copies each group's 8 rows (up to 8 KiB each) with
-//     cp.async.bulk into a 3-stage ring (192 KiB in flight per SM at d = 4096);
-//   - warps 0-7 each dot one row of a stage against the input row held in registers
-//     (h for W1 and W_LM, z_k = h + SiLU(W1_k h + b1_k) for W2_k), element pairs
-//     through packed fp32x2 FMAs, so shared memory serves only the weights;
-//   - a W1 row writes z_k; a vocabulary row feeds a per-warp top-k list kept sorted
-//     across the warp's lanes (value desc, id asc);
-//   - warp 9 merges the 8 warp lists of a matrix into the CTA's top-k, publishes it,
-//     and the CTA that completes a matrix merges all CTAs' lists into root or pool.
-// W2_k rows need all of z: the CTAs count finished W1 work in global memory and a warp
-// waits (bounded) for the full count before its first W2 row; every CTA takes its W1
-// groups first and the W_LM groups next, so the count is complete long before.
+//     cp.async.bulk into a 3-stage ring (192 KiB in flight per SM at d = 4096), and
+//     copies the input row of the next matrix (h, or z_k once all W1 rows are counted)
+//     into an x buffer ahead of the consumers;
+//   - warps 0-7 each dot one row of a stage against the input row held in registers,
+//     element pairs through packed fp32x2 FMAs, so shared memory serves only the
+//     weights;
+//   - a W1 row writes z_k = h + SiLU(W1_k h + b1_k); a vocabulary row feeds a
+//     per-warp top-k list kept sorted across the warp's lanes (value desc, id asc);
+//   - warp 9 merges the 8 warp lists of a matrix into the CTA's top-k and publishes
+//     it; the CTA that completes a matrix merges all CTAs' lists into root or pool.
 // All waits are bounded; on a timeout the call records an error and root / pool
 // become -1.
 #include <float.h>
@@ -37,7 +39,6 @@ constexpr int kSMerger = 9;                    // warp index
 constexpr int kSThreads = 10 * 32;
 constexpr int kSStages = 3;
 constexpr int kSMaxU4 = 16;                    // 16-byte pieces of a row per lane (d <= 4096)
-constexpr int kSSegMax = 8192;                 // bytes of one row chunk in a stage
 constexpr int kSMaxGrid = kHeadsStreamMaxGrid;
 
 struct SCand {
@@ -51,43 +52,53 @@ struct StreamArgs {
   const uint16_t* b1;         // [K][d] or null
   const uint16_t* w2;         // W2_k = w2 + k * w2_stride, [V][d]
   int64_t w2_stride;
-  const uint16_t* w_lm;       // [V][d] or null (then no root)
+  const uint16_t* w_lm;       // [V][d]
   int d, V, K, topk;
   float* z;                   // [K][d]
   float* logits_out;          // [K + 1][V] or null
-  SCand* scand;               // [K + 1][G][topk]
+  SCand* scand;               // [K + 1][G][topk], indexed by top-k matrix t
   int* err;
-  int* cnt;                   // [0] warps done with W1, [1 + j] CTAs done with top-k matrix j
+  int* cnt;                   // [0] warps done with W1, [1 + t] CTAs done with top-k matrix t
   int32_t* root;
   int32_t* pool;              // [K][topk]
 };
 
-// Matrices in stream order: 0..K-1 = W1_k, K = W_LM (if present), then W2_k.
-// Top-k matrix index j: 0 = W_LM, 1 + k = W2_k.
-struct Item {
-  int kind;      // 0 W1, 1 LM, 2 W2
-  int k;         // head (W1, W2)
-  int grp;       // row group within the matrix
-  int mat;       // stream matrix index
+// Stream segments: W1 (K * g1 groups), W_LM first half (ga), W2 (K * gv), W_LM rest (gv - ga).
+// Top-k matrix t: W2_t for t < K, W_LM for t = K; they publish in that order.
+struct Layout {
+  int K, g1, gv, ga;
+  __device__ int base_lm_a() const { return K * g1; }
+  __device__ int base_w2() const { return K * g1 + ga; }
+  __device__ int base_lm_b() const { return K * g1 + ga + K * gv; }
+  __device__ int total() const { return K * g1 + K * gv + gv; }
 };
 
-__device__ __forceinline__ Item map_item(int i, int K, int g_w1, int g_v, bool lm) {
+struct Item {
+  int kind;      // 0 W1, 1 W_LM, 2 W2
+  int k;         // head (W1, W2)
+  int grp;       // 8-row group within the matrix
+  int seq;       // stream matrix index: W1_k -> k, W_LM first half -> K, W2_k -> K + 1 + k, rest -> 2K + 1
+};
+
+__device__ __forceinline__ Item map_item(int i, const Layout& L) {
   Item it;
-  const int n_w1 = K * g_w1;
-  if (i < n_w1) {
-    it.kind = 0; it.k = (int)(i / g_w1); it.grp = (int)(i % g_w1); it.mat = it.k;
-    return it;
+  if (i < L.base_lm_a()) {
+    it.kind = 0; it.k = i / L.g1; it.grp = i % L.g1; it.seq = it.k;
+  } else if (i < L.base_w2()) {
+    it.kind = 1; it.k = 0; it.grp = i - L.base_lm_a(); it.seq = L.K;
+  } else if (i < L.base_lm_b()) {
+    const int r = i - L.base_w2();
+    it.kind = 2; it.k = r / L.gv; it.grp = r % L.gv; it.seq = L.K + 1 + it.k;
+  } else {
+    it.kind = 1; it.k = 0; it.grp = L.ga + (i - L.base_lm_b()); it.seq = 2 * L.K + 1;
   }
-  int r = i - n_w1;
-  if (lm) {
-    if (r < g_v) {
-      it.kind = 1; it.k = 0; it.grp = (int)r; it.mat = K;
-      return it;
-    }
-    r -= g_v;
-  }
-  it.kind = 2; it.k = (int)(r / g_v); it.grp = (int)(r % g_v); it.mat = K + 1 + it.k;
   return it;
+}
+
+// Whether CTA c of G owns an item in [lo, hi) (its items are c, c + G, ...).
+__device__ __forceinline__ bool owns_in(int c, int G, int lo, int hi) {
+  const int first = lo <= c ? c : c + ((lo - c + G - 1) / G) * G;
+  return first < hi;
 }
 
 // Bounded wait that also ends when another warp of the CTA has given up.
@@ -115,14 +126,27 @@ __device__ __forceinline__ void warp_argbest(float& v, int& i) {
   }
 }
 
+// Insert (v, id) into the sorted list of kk entries held one per lane (lv, li).
+__device__ __forceinline__ void list_insert(float v, int id, int kk, float& lv, int& li) {
+  const int lane = threadIdx.x & 31;
+  const bool before = lane < kk && ranks_before(v, id, lv, li);
+  const unsigned mask = __ballot_sync(0xffffffffu, before);
+  if (mask) {
+    const int pos = __ffs(mask) - 1;
+    const float uv = __shfl_up_sync(0xffffffffu, lv, 1);
+    const int ui = __shfl_up_sync(0xffffffffu, li, 1);
+    if (lane == pos) { lv = v; li = id; }
+    else if (lane > pos && lane < kk) { lv = uv; li = ui; }
+  }
+}
+
 // 10 warps: the register file is shared as if by 12, 168 registers each; the input
 // row takes 128 of them.
 __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const StreamArgs a) {
   extern __shared__ __align__(1024) uint8_t smem_s[];
   const int d = a.d, K = a.K, V = a.V;
-  const int n_chunks = (2 * d + kSSegMax - 1) / kSSegMax;  // 1 while d <= 4096
-  const int seg = 2 * d / n_chunks;                         // bytes of one row chunk
-  const int u4c = seg / 512;                                // 16-byte pieces per lane per chunk (<= 16)
+  const int seg = 2 * d;                                    // bytes of one row
+  const int u4c = seg / 512;                                // 16-byte pieces per lane (<= 16)
   uint8_t* ring = smem_s;                                  // [stages][8][seg]
   uint8_t* xbuf = ring + kSStages * kSConsumers * seg;      // input row of the current matrix (h bf16 or z_k fp32)
   SCand* lists = reinterpret_cast<SCand*>(xbuf + 4 * d);   // [2][consumers][32]
@@ -135,12 +159,13 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, c = blockIdx.x;
-  const bool lm = a.w_lm != nullptr;
-  const int g_w1 = (d + kSConsumers - 1) / kSConsumers, g_v = (V + kSConsumers - 1) / kSConsumers;
-  const int n_items = K * g_w1 + (lm ? g_v : 0) + K * g_v;
+  Layout L;
+  L.K = K;
+  L.g1 = (d + kSConsumers - 1) / kSConsumers;
+  L.gv = (V + kSConsumers - 1) / kSConsumers;
+  L.ga = L.gv / 2;
+  const int n_items = L.total();
   const int my_items = n_items > c ? (n_items - 1 - c) / G + 1 : 0;
-  const int my_units = my_items * n_chunks;                 // (item, row chunk) stages of this CTA
-  const int n_top = K + 1;                                  // top-k matrices j = 0..K
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -166,28 +191,27 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
     // ---- weight stream --------------------------------------------------------------
     if (lane != 0) return;
     int issued = 0, x_loads = 0, x_src = -2;
-    for (int u = 0; u < my_units; ++u) {
-      const int s = u % kSStages;
-      const uint32_t ph = (uint32_t)((u / kSStages) & 1);
-      const int n = u / n_chunks, ch = u - n * n_chunks;
-      const Item it = map_item(c + n * G, K, g_w1, g_v, lm);
+    bool z_ready = false;
+    for (int n = 0; n < my_items; ++n) {
+      const int s = n % kSStages;
+      const uint32_t ph = (uint32_t)((n / kSStages) & 1);
+      const Item it = map_item(c + n * G, L);
       // The input row of the item's matrix (h, or z_k for W2_k) goes through the same
       // stream into the x buffer, once all consumer warps took the previous one.
       const int src = it.kind == 2 ? it.k : -1;
-      if (ch == 0 && src != x_src) {
+      if (src != x_src) {
         if (x_loads > 0 && !s_wait(xempty, (uint32_t)((x_loads - 1) & 1), abortp)) { give_up(); break; }
-        if (src >= 0 && x_src < 0) {
+        if (src >= 0 && !z_ready) {
           // z is complete once every consumer warp of every CTA has finished its W1 rows
-          bool done = false;
           const uint64_t t0 = global_ns();
           for (uint32_t sp = 0;; ++sp) {
             int v;
             asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.cnt) : "memory");
-            if (v >= G * kSConsumers) { done = true; break; }
+            if (v >= G * kSConsumers) { z_ready = true; break; }
             if (*abortp) break;
             if ((sp & 63u) == 63u && global_ns() - t0 > 2000000000ull) break;
           }
-          if (!done) { give_up(); break; }
+          if (!z_ready) { give_up(); break; }
           asm volatile("fence.proxy.async.global;" ::: "memory");   // the bulk copy reads what other SMs wrote
         }
         const uint32_t xb = src >= 0 ? 4u * d : 2u * d;
@@ -204,42 +228,34 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
       const int rows = min(kSConsumers, n_rows - row0);
       mbar_expect_tx(full0 + 8 * s, (uint32_t)(rows * seg));
       for (int r = 0; r < rows; ++r)
-        bulk_copy_g2s(smem_u32(ring + (s * kSConsumers + r) * seg),
-                      base + (int64_t)(row0 + r) * d + (int64_t)ch * (seg / 2), (uint32_t)seg, full0 + 8 * s);
-      issued = u + 1;
+        bulk_copy_g2s(smem_u32(ring + (s * kSConsumers + r) * seg), base + (int64_t)(row0 + r) * d, (uint32_t)seg,
+                      full0 + 8 * s);
+      issued = n + 1;
     }
     // Copies still in flight (only after giving up) must land before the CTA exits.
-    for (int u = issued - kSStages; u < issued; ++u)
-      if (u >= 0) mbar_wait(full0 + 8 * (u % kSStages), (uint32_t)((u / kSStages) & 1), 100000000ull);
+    for (int n = issued - kSStages; n < issued; ++n)
+      if (n >= 0) mbar_wait(full0 + 8 * (n % kSStages), (uint32_t)((n / kSStages) & 1), 100000000ull);
     if (x_loads > 0) mbar_wait(xfull, (uint32_t)((x_loads - 1) & 1), 100000000ull);
     return;
   }
 
   if (warp == kSMerger) {
-    // ---- per-matrix top-k merges --------------------------------------------------
+    // ---- per-matrix top-k merges, in publication order t = 0..K ---------------------
     uint32_t ph_full[2] = {0u, 0u};
-    // matrices this CTA touches: its items are c, c + G, ...; matrix ranges are contiguous
-    const int n_w1 = K * g_w1;
-    for (int j = 0; j < n_top; ++j) {
-      if (j == 0 && !lm) {                              // keeps the buffer-0 arrivals one per j
-        if (lane == 0) mbar_arrive(lfree0);
-        continue;
-      }
-      const int kk = j == 0 ? 1 : a.topk;
-      const int lo = n_w1 + (j == 0 ? 0 : (lm ? g_v : 0) + (j - 1) * g_v);
-      const int hi = lo + g_v;                          // items [lo, hi) belong to matrix j
-      const int first = lo <= c ? c : c + ((lo - c + G - 1) / G) * G;
-      const bool mine = first < hi && first < n_items;
-      const int p = j & 1;
+    for (int t = 0; t <= K; ++t) {
+      const int kk = t == K ? 1 : a.topk;
+      const bool mine = t < K ? owns_in(c, G, L.base_w2() + t * L.gv, L.base_w2() + (t + 1) * L.gv)
+                              : owns_in(c, G, L.base_lm_a(), L.base_w2()) || owns_in(c, G, L.base_lm_b(), n_items);
+      const int p = t & 1;
       float bv = -INFINITY;
       int bi = INT_MAX;
       bool ok = false;
       if (mine && !*abortp) {
         ok = __all_sync(0xffffffffu, s_wait(lfull0 + 8 * p, ph_full[p], abortp));
         ph_full[p] ^= 1u;
-        if (!ok) give_up();
+        if (!ok && lane == 0) give_up();
       }
-      SCand* out = a.scand + ((int64_t)j * G + c) * a.topk;
+      SCand* out = a.scand + ((int64_t)t * G + c) * a.topk;
       if (ok) {
         // one sorted list of kk entries per consumer warp: entry e of warp w at lists[p][w][e]
         float ev[8];
@@ -276,21 +292,35 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
       if (lane < a.topk) out[lane] = SCand{lane < kk ? bv : -INFINITY, lane < kk ? bi : INT_MAX};
       __threadfence();
       __syncwarp();
-      int t = 0;
-      if (lane == 0) t = atomicAdd(&a.cnt[1 + j], 1);
-      t = __shfl_sync(0xffffffffu, t, 0);
-      if (t != G - 1) continue;
-      // ---- this CTA completed matrix j: merge all CTAs' sorted lists ----------------
+      int done = 0;
+      if (lane == 0) done = atomicAdd(&a.cnt[1 + t], 1);
+      done = __shfl_sync(0xffffffffu, done, 0);
+      if (done != G - 1) continue;
+      // ---- this CTA completed matrix t: merge all CTAs' sorted lists ----------------
       // Lane l keeps the current head of lists l, l + 32, ...; each round takes the best
       // head and advances its list.  For the last matrix the lists are first staged in
       // the idle ring (this CTA has streamed all its items), so that advancing a list
       // is a shared-memory load.
       __threadfence();
-      const SCand* gl = a.scand + (int64_t)j * G * a.topk;
-      const bool staged = mine && j == n_top - 1;
+      const SCand* gl = a.scand + (int64_t)t * G * a.topk;
+      // (a one-entry top-k reads only each list's head: no staging)
+      const bool staged = mine && t == K && kk > 1;
       SCand* st = reinterpret_cast<SCand*>(ring);
       if (staged) {
-        for (int i = lane; i < G * a.topk; i += 32) st[i] = ld_cand_cg(gl + i);
+        const int n = G * a.topk;
+        for (int i0 = 0; i0 < n; i0 += 32 * 8) {
+          SCand tmp[8];
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            const int i = i0 + 32 * b + lane;
+            if (i < n) tmp[b] = ld_cand_cg(gl + i);
+          }
+#pragma unroll
+          for (int b = 0; b < 8; ++b) {
+            const int i = i0 + 32 * b + lane;
+            if (i < n) st[i] = tmp[b];
+          }
+        }
         __syncwarp();
       }
       auto entry = [&](int l, int e) -> SCand { return staged ? st[l * a.topk + e] : ld_cand_cg(gl + l * a.topk + e); };
@@ -337,8 +367,8 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
         }
         if (lane == 0) {
           const int id = (bad || wi == INT_MAX) ? -1 : wi;
-          if (j == 0) a.root[0] = id;
-          else a.pool[(int64_t)(j - 1) * a.topk + r] = id;
+          if (t == K) a.root[0] = id;
+          else a.pool[(int64_t)t * a.topk + r] = id;
         }
       }
     }
@@ -346,20 +376,27 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
   }
 
   // ---- consumer warps: one row of each group ------------------------------------------
-  const int nv = d / 256;                                   // 16-byte chunks per lane
+  const int nv = d / 256;                                   // 16-byte pieces per lane
   float2 xr[kSMaxU4][4];                                    // input row, element pairs
-  int cur_mat = -1, x_src = -2, x_loads = 0;
-  bool w1_signalled = false;
-  float lv = -INFINITY;                                     // this lane's entry of the warp's list
-  int li = INT_MAX;
+  int cur_seq = -1, x_src = -2, x_loads = 0, cur_t = -1;
+  bool w1_signalled = false, any_lm = false;
+  float lv = -INFINITY, lvm = -INFINITY;                    // this lane's entry of the W2 / W_LM list
+  int li = INT_MAX, lim = INT_MAX;
   bool ok = true;
-  auto publish = [&](int j) {
-    const int p = j & 1;
-    lists[(p * kSConsumers + warp) * 32 + lane] = SCand{lv, li};
+  // Hand the warp's sorted list of top-k matrix t to the merge warp.
+  auto publish = [&](int t, float& pv, int& pi) -> bool {
+    const int p = t & 1;
+    if (t >= 2) {
+      // The buffer was used by t - 2: wait until the merge warp read it.  The merge
+      // warp arrives once for every t in order, so that is phase (t - 2) / 2.
+      if (!__all_sync(0xffffffffu, s_wait(lfree0 + 8 * p, ((t - 2) >> 1) & 1, abortp))) return false;
+    }
+    lists[(p * kSConsumers + warp) * 32 + lane] = SCand{pv, pi};
     __syncwarp();
     if (lane == 0) mbar_arrive(lfull0 + 8 * p);
-    lv = -INFINITY;
-    li = INT_MAX;
+    pv = -INFINITY;
+    pi = INT_MAX;
+    return true;
   };
   auto signal_w1 = [&]() {
     __threadfence();
@@ -368,24 +405,11 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
     w1_signalled = true;
   };
   for (int n = 0; n < my_items && ok; ++n) {
-    const Item it = map_item(c + n * G, K, g_w1, g_v, lm);
-    if (it.mat != cur_mat) {
-      if (cur_mat > K || (cur_mat == K && lm)) publish(cur_mat - K);   // leaving a top-k matrix
+    const Item it = map_item(c + n * G, L);
+    if (it.seq != cur_seq) {
+      if (cur_t >= 0 && !publish(cur_t, lv, li)) { if (lane == 0) give_up(); ok = false; break; }   // leaving W2_t
+      cur_t = it.kind == 2 ? it.k : -1;
       if (!w1_signalled && it.kind != 0) signal_w1();
-      if (it.kind == 2 || it.kind == 1) {
-        const int j = it.kind == 1 ? 0 : 1 + it.k;
-        if (j >= 2) {
-          // The lists buffer of j was used by j - 2: wait until the merge warp read it.
-          // The merge warp arrives once for every j in order, so the arrival for j - 2
-          // completes phase (j - 2) / 2 of its buffer.
-          const int p = j & 1;
-          if (!__all_sync(0xffffffffu, s_wait(lfree0 + 8 * p, ((j - 2) >> 1) & 1, abortp))) {
-            if (lane == 0) give_up();
-            ok = false;
-            break;
-          }
-        }
-      }
       // input row into registers when its source changes (h for W1 and W_LM, z_k for
       // W2_k): the producer staged it in the x buffer
       const int src = it.kind == 2 ? it.k : -1;
@@ -424,42 +448,38 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
         x_src = src;
         ++x_loads;
       }
-      cur_mat = it.mat;
+      cur_seq = it.seq;
+    }
+    const int s = n % kSStages;
+    if (!__all_sync(0xffffffffu, s_wait(full0 + 8 * s, (uint32_t)((n / kSStages) & 1), abortp))) {
+      if (lane == 0) give_up();
+      ok = false;
+      break;
     }
     const int n_rows = it.kind == 0 ? d : V;
     const int row = it.grp * kSConsumers + warp;
     float2 p[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-    for (int ch = 0; ch < n_chunks; ++ch) {
-      const int u = n * n_chunks + ch;
-      const int s = u % kSStages;
-      if (!__all_sync(0xffffffffu, s_wait(full0 + 8 * s, (uint32_t)((u / kSStages) & 1), abortp))) {
-        if (lane == 0) give_up();
-        ok = false;
-        break;
-      }
+    if (row < n_rows) {
       const uint8_t* w = ring + (s * kSConsumers + warp) * seg;
-      if (row < n_rows) {
 #pragma unroll
-        for (int q = 0; q < kSMaxU4; ++q) {
-          if (q < u4c) {
-            const uint4 v = *reinterpret_cast<const uint4*>(w + (lane + 32 * q) * 16);
-            const uint32_t wq[4] = {v.x, v.y, v.z, v.w};
+      for (int q = 0; q < kSMaxU4; ++q) {
+        if (q < u4c) {
+          const uint4 v = *reinterpret_cast<const uint4*>(w + (lane + 32 * q) * 16);
+          const uint32_t wq[4] = {v.x, v.y, v.z, v.w};
 #pragma unroll
-            for (int e = 0; e < 4; ++e) {
-              const float2 wf = make_float2(__uint_as_float(wq[e] << 16), __uint_as_float(wq[e] & 0xFFFF0000u));
-              p[e] = __ffma2_rn(wf, xr[q][e], p[e]);
-            }
+          for (int e = 0; e < 4; ++e) {
+            const float2 wf = make_float2(__uint_as_float(wq[e] << 16), __uint_as_float(wq[e] & 0xFFFF0000u));
+            p[e] = __ffma2_rn(wf, xr[q][e], p[e]);
           }
         }
       }
-      __syncwarp();
-      if (lane == 0) mbar_arrive(empty0 + 8 * s);
     }
-    if (!ok) break;
+    __syncwarp();
+    if (lane == 0) mbar_arrive(empty0 + 8 * s);            // this warp is done with the stage
     if (row >= n_rows) continue;
     float acc = ((p[0].x + p[0].y) + (p[1].x + p[1].y)) + ((p[2].x + p[2].y) + (p[3].x + p[3].y));
     acc = warp_sum(acc);
-    acc = __shfl_sync(0xffffffffu, acc, 0);                   // one value for every lane
+    acc = __shfl_sync(0xffffffffu, acc, 0);                 // one value for every lane
     if (it.kind == 0) {
       if (lane == 0) {
         float v = acc;
@@ -467,41 +487,35 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
         const float hv = Elem<uint16_t>::load(a.h, row);
         a.z[(int64_t)it.k * d + row] = hv + v / (1.f + expf(-v));   // h + SiLU(W1 h + b1)
       }
+    } else if (it.kind == 2) {
+      if (a.logits_out && lane == 0) a.logits_out[(int64_t)(1 + it.k) * V + row] = acc;
+      list_insert(acc, row, a.topk, lv, li);
     } else {
-      const int j = it.kind == 1 ? 0 : 1 + it.k;
-      const int kk = j == 0 ? 1 : a.topk;
-      if (a.logits_out && lane == 0) a.logits_out[(int64_t)j * V + row] = acc;
-      // insert (acc, row) into the sorted list held one entry per lane
-      const bool before = lane < kk && ranks_before(acc, row, lv, li);
-      const unsigned mask = __ballot_sync(0xffffffffu, before);
-      if (mask) {
-        const int pos = __ffs(mask) - 1;
-        const float uv = __shfl_up_sync(0xffffffffu, lv, 1);
-        const int ui = __shfl_up_sync(0xffffffffu, li, 1);
-        if (lane == pos) { lv = acc; li = row; }
-        else if (lane > pos && lane < kk) { lv = uv; li = ui; }
-      }
+      if (a.logits_out && lane == 0) a.logits_out[row] = acc;
+      list_insert(acc, row, 1, lvm, lim);
+      any_lm = true;
     }
   }
-  if (ok && (cur_mat > K || (cur_mat == K && lm))) publish(cur_mat - K);
+  if (ok && cur_t >= 0 && !publish(cur_t, lv, li)) { if (lane == 0) give_up(); ok = false; }
+  if (ok && any_lm && !publish(K, lvm, lim)) { if (lane == 0) give_up(); ok = false; }
   if (!w1_signalled) signal_w1();
 }
 
 }  // namespace
 
 size_t heads_stream_smem(int d) {
-  const int n_chunks = (2 * d + kSSegMax - 1) / kSSegMax;
-  return (size_t)kSStages * kSConsumers * (2 * d / n_chunks) + 4 * (size_t)d + 2 * kSConsumers * 32 * sizeof(SCand) +
+  return (size_t)kSStages * kSConsumers * 2 * d + 4 * (size_t)d + 2 * kSConsumers * 32 * sizeof(SCand) +
          (2 * kSStages + 8) * sizeof(uint64_t);
 }
 
 bool heads_stream_supported(int T, int d, int V, int K, int topk, medusa_dtype dt, const void* h, const void* w1,
                             const void* w2, int64_t w2_stride, const void* w_lm, const void* b1) {
-  auto al = [](const void* p) { return p == nullptr || (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   // one stage segment per row: d <= 4096 (8 KiB rows)
-  if (T != 1 || dt != MEDUSA_BF16 || K < 1 || d % 256 != 0 || d > 4096 || V < 1 || topk > 32)
+  if (T != 1 || dt != MEDUSA_BF16 || K < 1 || d % 256 != 0 || d > 4096 || V < 2 || topk > 32) return false;
+  if (!h || !w1 || !w2 || !w_lm || !al(h) || !al(w1) || !al(w2) || !al(w_lm) || (w2_stride * 2) % 16 != 0 ||
+      w2_stride < 0)
     return false;
-  if (!al(h) || !al(w1) || !al(w2) || !al(w_lm) || (w2_stride * 2) % 16 != 0 || w2_stride < 0) return false;
   (void)b1;
   int dev = 0, coop = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
@@ -544,13 +558,10 @@ cudaError_t launch_heads_stream(const HeadsPlan& p, const void* h, const void* w
   const size_t smem = heads_stream_smem(p.d);
   cudaError_t e = cudaFuncSetAttribute(heads_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
-  int dev = 0, sms = 0, per_sm = 0;
+  int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, heads_stream_kernel, kSThreads, smem);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) return cudaErrorCooperativeLaunchTooLarge;
-  int G = sms < kSMaxGrid ? sms : kSMaxGrid;
+  const int G = sms < kSMaxGrid ? sms : kSMaxGrid;
   // error flag and counters start at zero
   e = cudaMemsetAsync(a.err, 0, kHeadsCounterBytes, st);
   if (e != cudaSuccess) return e;
