@@ -4,8 +4,9 @@
 //
 // For one hidden row (T = 1, bf16), the round streams every head weight exactly once:
 // W1_k (K x [d, d]), W_LM ([V, d], root = argmax) and W2_k (K x [V, d]).  A cooperative
-// grid of one CTA per SM walks all 8-row groups of these matrices in one interleaved
-// order (group i goes to CTA i mod G), so the stream never stops between matrices:
+// grid of one CTA per SM takes the 8-row groups of these matrices from one global
+// counter, in stream order, so the stream never stops between matrices and a CTA that
+// gets less bandwidth simply takes fewer groups:
 //   W1_0..W1_{K-1}, the first half of W_LM, W2_0..W2_{K-1}, the second half of W_LM.
 // The first half of W_LM sits between W1 and W2, so z is complete everywhere by the
 // time any CTA needs it; the second half comes last, so the matrix whose top-k merge
@@ -58,7 +59,8 @@ struct StreamArgs {
   float* logits_out;          // [K + 1][V] or null
   SCand* scand;               // [K + 1][G][topk], indexed by top-k matrix t
   int* err;
-  int* cnt;                   // [0] warps done with W1, [1 + t] CTAs done with top-k matrix t
+  int* cnt;                   // [0] warps done with W1, [1 + t] CTAs done with top-k matrix t,
+                              // [K + 2] next group to hand out
   int32_t* root;
   int32_t* pool;              // [K][topk]
 };
@@ -93,12 +95,6 @@ __device__ __forceinline__ Item map_item(int i, const Layout& L) {
     it.kind = 1; it.k = 0; it.grp = L.ga + (i - L.base_lm_b()); it.seq = 2 * L.K + 1;
   }
   return it;
-}
-
-// Whether CTA c of G owns an item in [lo, hi) (its items are c, c + G, ...).
-__device__ __forceinline__ bool owns_in(int c, int G, int lo, int hi) {
-  const int first = lo <= c ? c : c + ((lo - c + G - 1) / G) * G;
-  return first < hi;
 }
 
 // Bounded wait that also ends when another warp of the CTA has given up.
@@ -165,7 +161,7 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
   L.gv = (V + kSConsumers - 1) / kSConsumers;
   L.ga = L.gv / 2;
   const int n_items = L.total();
-  const int my_items = n_items > c ? (n_items - 1 - c) / G + 1 : 0;
+  __shared__ int stage_item[kSStages];                      // group in each stage, -1 = no more
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -190,18 +186,39 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
   if (warp == kSProducer) {
     // ---- weight stream --------------------------------------------------------------
     if (lane != 0) return;
-    int issued = 0, x_loads = 0, x_src = -2;
+    // Stage slots carry a group index, -2 (a marker: leave the W1 phase) or -1 (the end).
+    int slot = 0, x_loads = 0, x_src = -2;
     bool z_ready = false;
-    for (int n = 0; n < my_items; ++n) {
-      const int s = n % kSStages;
-      const uint32_t ph = (uint32_t)((n / kSStages) & 1);
-      const Item it = map_item(c + n * G, L);
+    auto take_slot = [&](int& s) -> bool {
+      s = slot % kSStages;
+      return s_wait(empty0 + 8 * s, (uint32_t)(((slot / kSStages) & 1) ^ 1), abortp);
+    };
+    int next = atomicAdd(&a.cnt[K + 2], 1);
+    for (;;) {
+      const int idx = next;
+      int s;
+      if (idx >= n_items) {
+        // no groups left: an empty-handed stage tells the consumers to stop
+        if (!take_slot(s)) { give_up(); break; }
+        stage_item[s] = -1;
+        mbar_arrive(full0 + 8 * s);
+        ++slot;
+        break;
+      }
+      next = atomicAdd(&a.cnt[K + 2], 1);                   // the following group, ahead of time
+      const Item it = map_item(idx, L);
       // The input row of the item's matrix (h, or z_k for W2_k) goes through the same
       // stream into the x buffer, once all consumer warps took the previous one.
       const int src = it.kind == 2 ? it.k : -1;
       if (src != x_src) {
         if (x_loads > 0 && !s_wait(xempty, (uint32_t)((x_loads - 1) & 1), abortp)) { give_up(); break; }
         if (src >= 0 && !z_ready) {
+          // This CTA's consumers must be able to report their W1 rows before the wait
+          // for everybody's: a marker stage lets them leave the W1 phase.
+          if (!take_slot(s)) { give_up(); break; }
+          stage_item[s] = -2;
+          mbar_arrive(full0 + 8 * s);
+          ++slot;
           // z is complete once every consumer warp of every CTA has finished its W1 rows
           const uint64_t t0 = global_ns();
           for (uint32_t sp = 0;; ++sp) {
@@ -220,7 +237,8 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
         x_src = src;
         ++x_loads;
       }
-      if (!s_wait(empty0 + 8 * s, ph ^ 1u, abortp)) { give_up(); break; }
+      if (!take_slot(s)) { give_up(); break; }
+      stage_item[s] = idx;
       const uint16_t* base = it.kind == 0 ? a.w1 + (int64_t)it.k * d * d
                            : it.kind == 1 ? a.w_lm : a.w2 + (int64_t)it.k * a.w2_stride;
       const int n_rows = it.kind == 0 ? d : V;
@@ -230,10 +248,10 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
       for (int r = 0; r < rows; ++r)
         bulk_copy_g2s(smem_u32(ring + (s * kSConsumers + r) * seg), base + (int64_t)(row0 + r) * d, (uint32_t)seg,
                       full0 + 8 * s);
-      issued = n + 1;
+      ++slot;
     }
     // Copies still in flight (only after giving up) must land before the CTA exits.
-    for (int n = issued - kSStages; n < issued; ++n)
+    for (int n = slot - kSStages; n < slot; ++n)
       if (n >= 0) mbar_wait(full0 + 8 * (n % kSStages), (uint32_t)((n / kSStages) & 1), 100000000ull);
     if (x_loads > 0) mbar_wait(xfull, (uint32_t)((x_loads - 1) & 1), 100000000ull);
     return;
@@ -243,14 +261,13 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
     // ---- per-matrix top-k merges, in publication order t = 0..K ---------------------
     uint32_t ph_full[2] = {0u, 0u};
     for (int t = 0; t <= K; ++t) {
+      // every CTA publishes one list per t (empty when it took no group of t)
       const int kk = t == K ? 1 : a.topk;
-      const bool mine = t < K ? owns_in(c, G, L.base_w2() + t * L.gv, L.base_w2() + (t + 1) * L.gv)
-                              : owns_in(c, G, L.base_lm_a(), L.base_w2()) || owns_in(c, G, L.base_lm_b(), n_items);
       const int p = t & 1;
       float bv = -INFINITY;
       int bi = INT_MAX;
       bool ok = false;
-      if (mine && !*abortp) {
+      if (!*abortp) {
         ok = __all_sync(0xffffffffu, s_wait(lfull0 + 8 * p, ph_full[p], abortp));
         ph_full[p] ^= 1u;
         if (!ok && lane == 0) give_up();
@@ -298,32 +315,11 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
       if (done != G - 1) continue;
       // ---- this CTA completed matrix t: merge all CTAs' sorted lists ----------------
       // Lane l keeps the current head of lists l, l + 32, ...; each round takes the best
-      // head and advances its list.  For the last matrix the lists are first staged in
-      // the idle ring (this CTA has streamed all its items), so that advancing a list
-      // is a shared-memory load.
+      // head and advances its list (an L2 load).  The last matrix is W_LM, whose
+      // one-entry top-k needs the heads only.
       __threadfence();
       const SCand* gl = a.scand + (int64_t)t * G * a.topk;
-      // (a one-entry top-k reads only each list's head: no staging)
-      const bool staged = mine && t == K && kk > 1;
-      SCand* st = reinterpret_cast<SCand*>(ring);
-      if (staged) {
-        const int n = G * a.topk;
-        for (int i0 = 0; i0 < n; i0 += 32 * 8) {
-          SCand tmp[8];
-#pragma unroll
-          for (int b = 0; b < 8; ++b) {
-            const int i = i0 + 32 * b + lane;
-            if (i < n) tmp[b] = ld_cand_cg(gl + i);
-          }
-#pragma unroll
-          for (int b = 0; b < 8; ++b) {
-            const int i = i0 + 32 * b + lane;
-            if (i < n) st[i] = tmp[b];
-          }
-        }
-        __syncwarp();
-      }
-      auto entry = [&](int l, int e) -> SCand { return staged ? st[l * a.topk + e] : ld_cand_cg(gl + l * a.topk + e); };
+      auto entry = [&](int l, int e) -> SCand { return ld_cand_cg(gl + l * a.topk + e); };
       constexpr int kLpl = kSMaxGrid / 32;             // lists per lane
       float hv[kLpl];
       int hid[kLpl], hp[kLpl];
@@ -379,7 +375,7 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
   const int nv = d / 256;                                   // 16-byte pieces per lane
   float2 xr[kSMaxU4][4];                                    // input row, element pairs
   int cur_seq = -1, x_src = -2, x_loads = 0, cur_t = -1;
-  bool w1_signalled = false, any_lm = false;
+  bool w1_signalled = false;
   float lv = -INFINITY, lvm = -INFINITY;                    // this lane's entry of the W2 / W_LM list
   int li = INT_MAX, lim = INT_MAX;
   bool ok = true;
@@ -404,10 +400,41 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
     if (lane == 0) atomicAdd(&a.cnt[0], 1);
     w1_signalled = true;
   };
-  for (int n = 0; n < my_items && ok; ++n) {
-    const Item it = map_item(c + n * G, L);
+  // W2 lists t < target are final for this CTA (groups arrive in stream order): hand
+  // them out in order, the current one or an empty list for a matrix it never touched.
+  int pub_next = 0;
+  auto publish_upto = [&](int target) -> bool {
+    while (pub_next < target) {
+      const int t = pub_next;
+      float ev = -INFINITY;
+      int ei = INT_MAX;
+      if (!(t == cur_t ? publish(t, lv, li) : publish(t, ev, ei))) return false;
+      ++pub_next;
+    }
+    return true;
+  };
+  for (int n = 0; ok; ++n) {
+    const int s = n % kSStages;
+    if (!__all_sync(0xffffffffu, s_wait(full0 + 8 * s, (uint32_t)((n / kSStages) & 1), abortp))) {
+      if (lane == 0) give_up();
+      ok = false;
+      break;
+    }
+    const int idx = stage_item[s];
+    if (idx == -1) break;                                   // no groups left
+    if (idx == -2) {                                        // marker: leave the W1 phase
+      if (!w1_signalled) signal_w1();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      continue;
+    }
+    const Item it = map_item(idx, L);
     if (it.seq != cur_seq) {
-      if (cur_t >= 0 && !publish(cur_t, lv, li)) { if (lane == 0) give_up(); ok = false; break; }   // leaving W2_t
+      if (!publish_upto(it.kind == 2 ? it.k : (it.seq == 2 * K + 1 ? K : 0))) {
+        if (lane == 0) give_up();
+        ok = false;
+        break;
+      }
       cur_t = it.kind == 2 ? it.k : -1;
       if (!w1_signalled && it.kind != 0) signal_w1();
       // input row into registers when its source changes (h for W1 and W_LM, z_k for
@@ -450,12 +477,6 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
       }
       cur_seq = it.seq;
     }
-    const int s = n % kSStages;
-    if (!__all_sync(0xffffffffu, s_wait(full0 + 8 * s, (uint32_t)((n / kSStages) & 1), abortp))) {
-      if (lane == 0) give_up();
-      ok = false;
-      break;
-    }
     const int n_rows = it.kind == 0 ? d : V;
     const int row = it.grp * kSConsumers + warp;
     float2 p[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
@@ -493,11 +514,9 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
     } else {
       if (a.logits_out && lane == 0) a.logits_out[row] = acc;
       list_insert(acc, row, 1, lvm, lim);
-      any_lm = true;
     }
   }
-  if (ok && cur_t >= 0 && !publish(cur_t, lv, li)) { if (lane == 0) give_up(); ok = false; }
-  if (ok && any_lm && !publish(K, lvm, lim)) { if (lane == 0) give_up(); ok = false; }
+  if (ok && (!publish_upto(K) || !publish(K, lvm, lim))) { if (lane == 0) give_up(); ok = false; }
   if (!w1_signalled) signal_w1();
 }
 
