@@ -41,60 +41,92 @@ __device__ __forceinline__ void merge_stats(float& m, float& z, float& s1, float
   m = mn;
 }
 
-template <typename EL>
+// Merge (m, z, s1) and the argmax of another lane into this lane's.
+__device__ __forceinline__ void shfl_merge(float& m, float& z, float& s1, float& av, int& ai, int o) {
+  const float om = __shfl_xor_sync(0xffffffffu, m, o);
+  const float oz = __shfl_xor_sync(0xffffffffu, z, o);
+  const float os = __shfl_xor_sync(0xffffffffu, s1, o);
+  const float ov = __shfl_xor_sync(0xffffffffu, av, o);
+  const int oi = __shfl_xor_sync(0xffffffffu, ai, o);
+  merge_stats(m, z, s1, om, oz, os);
+  if (ranks_before(ov, oi, av, ai)) { av = ov; ai = oi; }
+}
+
+// Fold a batch of n scaled values y[] (ids i0..i0+n-1, raw values x[]) into the running
+// statistics: argmax of x; for typical acceptance also the max m of y, Z = sum e^{y-m}
+// and S1 = sum e^{y-m} (y - m).
+template <bool TYP, int NB>
+__device__ __forceinline__ void fold(const float* x, int i0, float inv_temp, float& m, float& z, float& s1,
+                                     float& av, int& ai) {
+#pragma unroll
+  for (int e = 0; e < NB; ++e)
+    if (ranks_before(x[e], i0 + e, av, ai)) { av = x[e]; ai = i0 + e; }
+  if (TYP) {
+    float y[NB], mb = -INFINITY;
+#pragma unroll
+    for (int e = 0; e < NB; ++e) { y[e] = x[e] * inv_temp; mb = fmaxf(mb, y[e]); }
+    if (z == 0.f) {
+      m = mb;
+    } else if (mb > m) {
+      const float sc = expf(m - mb);
+      s1 = sc * (s1 + (m - mb) * z);
+      z *= sc;
+      m = mb;
+    }
+#pragma unroll
+    for (int e = 0; e < NB; ++e) {
+      const float d = y[e] - m;
+      const float ev = expf(d);
+      z += ev;
+      s1 = fmaf(ev, d, s1);
+    }
+  }
+}
+
+// One pass over a chunk of one internal row: argmax (greedy), plus max, partition
+// function and first moment (typical).  16-byte loads when the chunk is aligned.
+template <typename EL, bool TYP>
 __global__ void __launch_bounds__(kThreads) row_stats_kernel(medusa_tree_t t, int V, int chunk,
                                                              const EL* __restrict__ logits,
                                                              float inv_temp,
                                                              RowPart* __restrict__ part) {
+  constexpr int EPV = Elem<EL>::kPerVec;
   const int c = blockIdx.x, ii = blockIdx.y, b = blockIdx.z;
   const int u = t.internal[ii];
   const EL* row = logits + ((int64_t)b * t.n_rows + u) * V;
   const int start = c * chunk, end = min(V, start + chunk);
-  // pass 1: max and argmax
-  float mx = -INFINITY, av = -INFINITY;
+  float m = -INFINITY, z = 0.f, s1 = 0.f, av = -INFINITY;
   int ai = INT_MAX;
-  for (int i = start + threadIdx.x; i < end; i += kThreads) {
-    const float x = Elem<EL>::load(row, i);
-    if (ranks_before(x, i, av, ai)) { av = x; ai = i; }
+  const bool vec = (reinterpret_cast<uintptr_t>(row + start) & 15u) == 0;
+  int i = start;
+  if (vec) {
+    const int nvec = (end - start) / EPV;
+    const uint4* rv = reinterpret_cast<const uint4*>(row + start);
+    for (int q = threadIdx.x; q < nvec; q += kThreads) {
+      float x[EPV];
+      Elem<EL>::unpack(__ldg(rv + q), x);
+      fold<TYP, EPV>(x, start + q * EPV, inv_temp, m, z, s1, av, ai);
+    }
+    i = start + nvec * EPV;
   }
-  __shared__ float red_v[kWarps];
-  __shared__ int red_i[kWarps];
+  for (int k = i + threadIdx.x; k < end; k += kThreads) {
+    float x[1] = {Elem<EL>::load(row, k)};
+    fold<TYP, 1>(x, k, inv_temp, m, z, s1, av, ai);
+  }
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    const float ov = __shfl_xor_sync(0xffffffffu, av, o);
-    const int oi = __shfl_xor_sync(0xffffffffu, ai, o);
-    if (ranks_before(ov, oi, av, ai)) { av = ov; ai = oi; }
-  }
+  for (int o = 16; o > 0; o >>= 1) shfl_merge(m, z, s1, av, ai, o);
+  __shared__ float r_m[kWarps], r_z[kWarps], r_s[kWarps], r_v[kWarps];
+  __shared__ int r_i[kWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  if (lane == 0) { red_v[warp] = av; red_i[warp] = ai; }
+  if (lane == 0) { r_m[warp] = m; r_z[warp] = z; r_s[warp] = s1; r_v[warp] = av; r_i[warp] = ai; }
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int w = 1; w < kWarps; ++w)
-      if (ranks_before(red_v[w], red_i[w], av, ai)) { av = red_v[w]; ai = red_i[w]; }
-    red_v[0] = av; red_i[0] = ai;
-  }
-  __syncthreads();
-  av = red_v[0]; ai = red_i[0];
-  mx = av * inv_temp;                         // T > 0: the max of x/T is at the argmax of x
-  // pass 2: partition function and first moment relative to mx
-  float z = 0.f, s1 = 0.f;
-  for (int i = start + threadIdx.x; i < end; i += kThreads) {
-    const float y = Elem<EL>::load(row, i) * inv_temp - mx;
-    const float e = expf(y);
-    z += e;
-    s1 = fmaf(e, y, s1);
-  }
-  z = warp_sum(z);
-  s1 = warp_sum(s1);
-  __shared__ float red_z[kWarps], red_s[kWarps];
-  __syncthreads();
-  if (lane == 0) { red_z[warp] = z; red_s[warp] = s1; }
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    z = 0.f; s1 = 0.f;
-    for (int w = 0; w < kWarps; ++w) { z += red_z[w]; s1 += red_s[w]; }
+    for (int w = 1; w < kWarps; ++w) {
+      merge_stats(m, z, s1, r_m[w], r_z[w], r_s[w]);
+      if (ranks_before(r_v[w], r_i[w], av, ai)) { av = r_v[w]; ai = r_i[w]; }
+    }
     RowPart p;
-    p.m = mx; p.z = z; p.s1 = s1; p.amax_v = av; p.amax_i = ai;
+    p.m = m; p.z = z; p.s1 = s1; p.amax_v = av; p.amax_i = ai;
     p.pad[0] = p.pad[1] = p.pad[2] = 0;
     part[(((int64_t)b * t.n_internal) + ii) * gridDim.x + c] = p;
   }
@@ -140,72 +172,109 @@ __global__ void __launch_bounds__(kThreads) guard_kernel(medusa_tree_t t, int V,
   }
 }
 
+// Shared-memory layout of select_kernel: per internal row m, log Z, tau, argmax; per
+// node the acceptance of its incoming edge and its log-probability; the retrieval
+// table when it fits.
+struct SelectSmem {
+  size_t off_lp, off_ok, off_ret, bytes;
+  bool ret_staged;
+};
+inline SelectSmem select_smem(const medusa_tree_t& t) {
+  SelectSmem L{};
+  const size_t ni = t.n_internal > 0 ? t.n_internal : 1;
+  L.off_lp = align_up(4 * ni * sizeof(float), 16);
+  L.off_ok = align_up(L.off_lp + (size_t)t.n_rows * sizeof(float), 16);
+  L.off_ret = align_up(L.off_ok + (size_t)t.n_rows, 16);
+  const size_t ret = (size_t)t.n_paths * (t.max_depth + 1) * sizeof(int32_t);
+  L.ret_staged = L.off_ret + ret <= 96 * 1024;
+  L.bytes = L.ret_staged ? L.off_ret + ret : L.off_ret;
+  return L;
+}
+
 template <typename EL>
 __global__ void __launch_bounds__(kThreads) select_kernel(
     medusa_tree_t t, int V, int n_chunks, const EL* __restrict__ logits,
     const int32_t* __restrict__ tokens, int mode, float inv_temp, float epsilon, float delta,
-    const RowPart* __restrict__ part, const float* __restrict__ guard,
+    const RowPart* __restrict__ part, const float* __restrict__ guard, SelectSmem lay,
     int32_t* __restrict__ best_path, int32_t* __restrict__ accept_len,
     int32_t* __restrict__ out_tokens, int32_t* __restrict__ out_rows,
     int32_t* __restrict__ frontier_row) {
-  extern __shared__ float sm[];
+  extern __shared__ __align__(16) unsigned char smem_sel[];
+  float* s_m = reinterpret_cast<float*>(smem_sel);
   const int b = blockIdx.x;
-  const int NI = t.n_internal;
-  float* s_m = sm;             // [NI] max of x/T
-  float* s_lz = sm + NI;       // [NI] log Z
-  float* s_tau = sm + 2 * NI;  // [NI] typical threshold
-  int* s_am = (int*)(sm + 3 * NI);  // [NI] argmax id
-  // 1. merged statistics per internal row
-  for (int ii = threadIdx.x; ii < NI; ii += kThreads) {
+  const int NI = t.n_internal, N = t.n_rows;
+  float* s_lz = s_m + NI;                        // [NI] log Z
+  float* s_tau = s_m + 2 * NI;                   // [NI] typical threshold
+  int* s_am = reinterpret_cast<int*>(s_m + 3 * NI);   // [NI] argmax id
+  float* s_lp = reinterpret_cast<float*>(smem_sel + lay.off_lp);   // [N] log p of the edge into v
+  uint8_t* s_ok = smem_sel + lay.off_ok;         // [N] edge into v accepted
+  int32_t* s_ret = reinterpret_cast<int32_t*>(smem_sel + lay.off_ret);
+  const int W = t.max_depth + 1;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const bool typ = mode != MEDUSA_ACCEPT_GREEDY;
+  const int32_t* tok = tokens + (int64_t)b * N;
+  // 1. merged statistics per internal row (one warp per row, one lane per chunk) and
+  //    the retrieval table into shared memory
+  if (lay.ret_staged)
+    for (int i = threadIdx.x; i < t.n_paths * W; i += kThreads) s_ret[i] = t.retrieve[i];
+  for (int ii = warp; ii < NI; ii += kWarps) {
     const RowPart* rp = part + (((int64_t)b * NI) + ii) * n_chunks;
-    float m, z, s1, av;
-    int ai;
-    merged_row(rp, n_chunks, m, z, s1, av, ai);
-    const float lz = logf(z);
-    float H;
-    if (guard) {
-      H = 0.f;
-      for (int c = 0; c < n_chunks; ++c) H += guard[(((int64_t)b * NI) + ii) * n_chunks + c];
-    } else {
-      H = lz - s1 / z;          // -sum p ln p = ln Z - sum p (x/T - m)
+    float m = -INFINITY, z = 0.f, s1 = 0.f, av = -INFINITY, g = 0.f;
+    int ai = INT_MAX;
+    for (int c = lane; c < n_chunks; c += 32) {
+      const RowPart q = rp[c];
+      merge_stats(m, z, s1, q.m, q.z, q.s1);
+      if (ranks_before(q.amax_v, q.amax_i, av, ai)) { av = q.amax_v; ai = q.amax_i; }
+      if (guard) g += guard[(((int64_t)b * NI) + ii) * n_chunks + c];
     }
-    s_m[ii] = m;
-    s_lz[ii] = lz;
-    s_tau[ii] = fminf(epsilon, delta * expf(-H));
-    s_am[ii] = ai;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) shfl_merge(m, z, s1, av, ai, o);
+    if (guard) g = warp_sum(g);
+    if (lane == 0) {
+      const float lz = logf(z);
+      const float H = guard ? g : lz - s1 / z;     // -sum p ln p = ln Z - sum p (x/T - m)
+      s_m[ii] = m;
+      s_lz[ii] = lz;
+      s_tau[ii] = fminf(epsilon, delta * expf(-H));
+      s_am[ii] = ai;
+    }
   }
   __syncthreads();
-  // 2. every retrieval path
-  const int W = t.max_depth + 1;
-  const int32_t* tok = tokens + (int64_t)b * t.n_rows;
+  // 2. every edge parent(v) -> v at once: accepted? and log p_parent(token of v)
+  for (int v = 1 + threadIdx.x; v < N; v += kThreads) {
+    const int u = t.parent[v];
+    const int ii = t.internal_index[u];
+    const int ct = tok[v];
+    bool ok = false;
+    float lp = 0.f;
+    if (ct >= 0 && ct < V) {                     // else: not a vocabulary id, never accepted
+      if (!typ) {
+        ok = ct == s_am[ii];
+      } else {
+        const float x = Elem<EL>::load(logits, ((int64_t)b * N + u) * V + ct) * inv_temp;
+        lp = x - s_m[ii] - s_lz[ii];
+        ok = expf(lp) > s_tau[ii];
+      }
+    }
+    s_ok[v] = ok ? 1 : 0;
+    s_lp[v] = lp;
+  }
+  __syncthreads();
+  // 3. every retrieval path: accepted prefix length and its log-probability
   int best_p = INT_MAX, best_a = -1;
   float best_s = -INFINITY;
   for (int p = threadIdx.x; p < t.n_paths; p += kThreads) {
-    const int32_t* r = t.retrieve + (int64_t)p * W;
+    const int32_t* r = lay.ret_staged ? s_ret + p * W : t.retrieve + (int64_t)p * W;
     int a = 0;
     float score = 0.f;
-    for (int j = 0; j + 1 < W; ++j) {
-      const int u = r[j], cnode = r[j + 1];
-      if (cnode < 0) break;
-      const int ii = t.internal_index[u];
-      const int ct = tok[cnode];
-      bool ok;
-      if (ct < 0 || ct >= V) {
-        ok = false;                          // not a vocabulary id: never accepted
-      } else if (mode == MEDUSA_ACCEPT_GREEDY) {
-        ok = (ct == s_am[ii]);
-      } else {
-        const float x = Elem<EL>::load(logits, ((int64_t)b * t.n_rows + u) * V + ct) * inv_temp;
-        const float lp = x - s_m[ii] - s_lz[ii];
-        ok = expf(lp) > s_tau[ii];
-        if (ok) score += lp;
-      }
-      if (!ok) break;
+    for (int j = 1; j < W; ++j) {
+      const int cnode = r[j];
+      if (cnode < 0 || !s_ok[cnode]) break;
+      score += s_lp[cnode];
       ++a;
     }
-    const bool take = mode == MEDUSA_ACCEPT_GREEDY
-                          ? (a > best_a || (a == best_a && p < best_p))
-                          : (a > best_a || (a == best_a && (score > best_s || (score == best_s && p < best_p))));
+    const bool take = !typ ? (a > best_a || (a == best_a && p < best_p))
+                           : (a > best_a || (a == best_a && (score > best_s || (score == best_s && p < best_p))));
     if (take) { best_a = a; best_s = score; best_p = p; }
   }
   // 3. block arg-best over paths
@@ -223,7 +292,6 @@ __global__ void __launch_bounds__(kThreads) select_kernel(
     const int op = __shfl_xor_sync(0xffffffffu, best_p, o);
     if (better(oa, os, op, best_a, best_s, best_p)) { best_a = oa; best_s = os; best_p = op; }
   }
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   if (lane == 0) { r_a[warp] = best_a; r_s[warp] = best_s; r_p[warp] = best_p; }
   __syncthreads();
   if (threadIdx.x == 0) {
@@ -231,7 +299,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(
       if (better(r_a[w], r_s[w], r_p[w], best_a, best_s, best_p)) {
         best_a = r_a[w]; best_s = r_s[w]; best_p = r_p[w];
       }
-    const int32_t* r = t.retrieve + (int64_t)best_p * W;
+    const int32_t* r = lay.ret_staged ? s_ret + best_p * W : t.retrieve + (int64_t)best_p * W;
     best_path[b] = best_p;
     accept_len[b] = best_a;
     for (int j = 0; j < W; ++j) {
@@ -249,7 +317,7 @@ AcceptPlan plan_accept(const medusa_tree_t& t, int B, int V) {
   AcceptPlan p{};
   p.B = B;
   p.V = V;
-  int chunk = 8192;
+  int chunk = 4096;
   if (V < chunk) chunk = (V + 255) / 256 * 256;
   p.chunk = chunk;
   p.n_chunks = (V + chunk - 1) / chunk;
@@ -269,28 +337,37 @@ cudaError_t launch_accept(const AcceptPlan& p, const medusa_tree_t& t, const voi
   float* guard = (float*)((char*)ws + p.off_guard);
   const float inv_t = 1.f / temperature;
   const bool bf = dt == MEDUSA_BF16;
+  const bool typ = mode == MEDUSA_ACCEPT_TYPICAL;
   if (t.n_internal > 0) {
     dim3 g(p.n_chunks, t.n_internal, p.B);
-    if (bf) row_stats_kernel<uint16_t><<<g, kThreads, 0, st>>>(t, p.V, p.chunk, (const uint16_t*)logits, inv_t, part);
-    else row_stats_kernel<float><<<g, kThreads, 0, st>>>(t, p.V, p.chunk, (const float*)logits, inv_t, part);
+    if (bf && typ) row_stats_kernel<uint16_t, true><<<g, kThreads, 0, st>>>(t, p.V, p.chunk, (const uint16_t*)logits, inv_t, part);
+    else if (bf) row_stats_kernel<uint16_t, false><<<g, kThreads, 0, st>>>(t, p.V, p.chunk, (const uint16_t*)logits, inv_t, part);
+    else if (typ) row_stats_kernel<float, true><<<g, kThreads, 0, st>>>(t, p.V, p.chunk, (const float*)logits, inv_t, part);
+    else row_stats_kernel<float, false><<<g, kThreads, 0, st>>>(t, p.V, p.chunk, (const float*)logits, inv_t, part);
     cudaError_t e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    if (entropy_guard && mode == MEDUSA_ACCEPT_TYPICAL) {
+    if (entropy_guard && typ) {
       if (bf) guard_kernel<uint16_t><<<g, kThreads, 0, st>>>(t, p.V, p.chunk, (const uint16_t*)logits, inv_t, part, guard);
       else guard_kernel<float><<<g, kThreads, 0, st>>>(t, p.V, p.chunk, (const float*)logits, inv_t, part, guard);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
   }
-  const float* gptr = (entropy_guard && mode == MEDUSA_ACCEPT_TYPICAL) ? guard : nullptr;
-  const size_t smem = (size_t)4 * (t.n_internal > 0 ? t.n_internal : 1) * sizeof(float);
-  if (bf)
-    select_kernel<uint16_t><<<p.B, kThreads, smem, st>>>(t, p.V, p.n_chunks, (const uint16_t*)logits, tokens, mode,
-                                                         inv_t, epsilon, delta, part, gptr, best_path,
-                                                         accept_len, out_tokens, out_rows, frontier_row);
-  else
-    select_kernel<float><<<p.B, kThreads, smem, st>>>(t, p.V, p.n_chunks, (const float*)logits, tokens, mode,
-                                                      inv_t, epsilon, delta, part, gptr, best_path,
-                                                      accept_len, out_tokens, out_rows, frontier_row);
+  const float* gptr = (entropy_guard && typ) ? guard : nullptr;
+  const SelectSmem lay = select_smem(t);
+  cudaError_t e;
+  if (bf) {
+    e = cudaFuncSetAttribute(select_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lay.bytes);
+    if (e != cudaSuccess) return e;
+    select_kernel<uint16_t><<<p.B, kThreads, lay.bytes, st>>>(t, p.V, p.n_chunks, (const uint16_t*)logits, tokens,
+                                                              mode, inv_t, epsilon, delta, part, gptr, lay, best_path,
+                                                              accept_len, out_tokens, out_rows, frontier_row);
+  } else {
+    e = cudaFuncSetAttribute(select_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lay.bytes);
+    if (e != cudaSuccess) return e;
+    select_kernel<float><<<p.B, kThreads, lay.bytes, st>>>(t, p.V, p.n_chunks, (const float*)logits, tokens, mode,
+                                                           inv_t, epsilon, delta, part, gptr, lay, best_path,
+                                                           accept_len, out_tokens, out_rows, frontier_row);
+  }
   return cudaGetLastError();
 }
 

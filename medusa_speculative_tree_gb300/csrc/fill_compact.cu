@@ -34,9 +34,11 @@ __device__ __forceinline__ int64_t cache_row_offset(const medusa_kv_t& c, int b,
   return (((int64_t)page * c.n_kv_heads + kvh) * c.page_size + row % c.page_size) * c.head_dim;
 }
 
-// One CTA per (kv head, sequence).  The whole path is validated first; the G source
-// rows of K and V are then read into shared memory before any destination row is
-// written, so overlapping source/destination rows are safe.
+// One CTA per (kv head, sequence).  The whole path is validated first (lane j of warp
+// 0 checks row j: 0 for the root, else a child of row j - 1); the G source rows of K
+// and V are then read into shared memory before any destination row is written, so
+// overlapping source/destination rows are safe.  Rows move as 16-byte vectors when
+// their length allows.
 template <typename EL>
 __global__ void kv_compact_kernel(medusa_kv_t c, medusa_tree_t t, const int32_t* __restrict__ L,
                                   const int32_t* __restrict__ accept_len,
@@ -50,19 +52,25 @@ __global__ void kv_compact_kernel(medusa_kv_t c, medusa_tree_t t, const int32_t*
   const int dh = c.head_dim, W = t.max_depth + 1;
   const int Lb = L[b];
   const int a = accept_len[b];
-  if (threadIdx.x == 0) {
-    int v = MEDUSA_OK;
-    if (Lb < 0 || !seq_rows_ok(c, b, (int64_t)Lb + t.n_rows)) v = MEDUSA_ECAPACITY;
-    else if (a < 0 || a > t.max_depth) v = MEDUSA_EPATH;
-    else {
-      for (int j = 0; j <= a; ++j) {
-        const int u = out_rows[(int64_t)b * W + j];
-        rows_s[j] = u;
-        if (u < 0 || u >= t.n_rows) { v = MEDUSA_EPATH; break; }
-        if (j == 0 ? (u != 0) : (t.parent[u] != rows_s[j - 1])) { v = MEDUSA_EPATH; break; }
-      }
+  if (threadIdx.x < 32) {
+    const int j = threadIdx.x;
+    const int u = j < W ? out_rows[(int64_t)b * W + j] : -1;
+    const int prev = (j >= 1 && j < W) ? out_rows[(int64_t)b * W + j - 1] : -1;
+    const bool in = a >= 0 && a <= t.max_depth && j <= a;
+    bool bad = false;
+    if (in) {
+      rows_s[j] = u;
+      if (u < 0 || u >= t.n_rows) bad = true;
+      else if (j == 0) bad = u != 0;
+      else bad = t.parent[u] != prev;
     }
-    verdict = v;
+    const bool any_bad = __any_sync(0xffffffffu, bad);
+    if (j == 0) {
+      int v = MEDUSA_OK;
+      if (Lb < 0 || !seq_rows_ok(c, b, (int64_t)Lb + t.n_rows)) v = MEDUSA_ECAPACITY;
+      else if (a < 0 || a > t.max_depth || any_bad) v = MEDUSA_EPATH;
+      verdict = v;
+    }
   }
   __syncthreads();
   const int v = verdict;
@@ -76,18 +84,36 @@ __global__ void kv_compact_kernel(medusa_kv_t c, medusa_tree_t t, const int32_t*
   const int G = a + 1;
   EL* ck = (EL*)c.k;
   EL* cv = (EL*)c.v;
-  for (int idx = threadIdx.x; idx < G * dh; idx += blockDim.x) {
-    const int j = idx / dh, e = idx % dh;
-    const int64_t src = cache_row_offset(c, b, kvh, Lb + rows_s[j]) + e;
-    snap[j * dh + e] = ck[src];
-    snap[(W + j) * dh + e] = cv[src];
-  }
-  __syncthreads();
-  for (int idx = threadIdx.x; idx < G * dh; idx += blockDim.x) {
-    const int j = idx / dh, e = idx % dh;
-    const int64_t dst = cache_row_offset(c, b, kvh, Lb + j) + e;
-    ck[dst] = snap[j * dh + e];
-    cv[dst] = snap[(W + j) * dh + e];
+  if ((dh * (int)sizeof(EL)) % 16 == 0) {
+    const int pr = dh * (int)sizeof(EL) / 16;           // 16-byte pieces per row
+    uint4* s4 = reinterpret_cast<uint4*>(snap);
+    for (int idx = threadIdx.x; idx < G * pr; idx += blockDim.x) {
+      const int j = idx / pr, e = idx % pr;
+      const int64_t src = cache_row_offset(c, b, kvh, Lb + rows_s[j]);
+      s4[j * pr + e] = reinterpret_cast<const uint4*>(ck + src)[e];
+      s4[(W + j) * pr + e] = reinterpret_cast<const uint4*>(cv + src)[e];
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < G * pr; idx += blockDim.x) {
+      const int j = idx / pr, e = idx % pr;
+      const int64_t dst = cache_row_offset(c, b, kvh, Lb + j);
+      reinterpret_cast<uint4*>(ck + dst)[e] = s4[j * pr + e];
+      reinterpret_cast<uint4*>(cv + dst)[e] = s4[(W + j) * pr + e];
+    }
+  } else {
+    for (int idx = threadIdx.x; idx < G * dh; idx += blockDim.x) {
+      const int j = idx / dh, e = idx % dh;
+      const int64_t src = cache_row_offset(c, b, kvh, Lb + rows_s[j]) + e;
+      snap[j * dh + e] = ck[src];
+      snap[(W + j) * dh + e] = cv[src];
+    }
+    __syncthreads();
+    for (int idx = threadIdx.x; idx < G * dh; idx += blockDim.x) {
+      const int j = idx / dh, e = idx % dh;
+      const int64_t dst = cache_row_offset(c, b, kvh, Lb + j) + e;
+      ck[dst] = snap[j * dh + e];
+      cv[dst] = snap[(W + j) * dh + e];
+    }
   }
   if (kvh == 0 && threadIdx.x == 0) {
     status[b] = MEDUSA_OK;
