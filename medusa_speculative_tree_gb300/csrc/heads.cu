@@ -466,6 +466,10 @@ HeadsPlan plan_heads(int T, int d, int V, int K, int topk) {
   off = align_up(off + (size_t)T * (K + 1) * p.n_chunks * topk * sizeof(Cand), 256);
   p.off_scand = off;                                       // weight-stream path: per-CTA lists
   off = align_up(off + (size_t)(K + 1) * kHeadsStreamMaxGrid * topk * sizeof(Cand), 256);
+  p.off_hhl = off;                                         // tensor-core path: input rows as bf16 pairs
+  off = align_up(off + (T >= 2 ? heads_mma_rows(T) * d * 2 : 0), 256);
+  p.off_zhl = off;
+  off = align_up(off + (T >= 2 ? (size_t)K * heads_mma_rows(T) * d * 2 : 0), 256);
   p.off_err = off;
   off = align_up(off + kHeadsCounterBytes, 256);
   p.bytes = off;
@@ -486,10 +490,15 @@ cudaError_t launch_heads(const HeadsPlan& p, const void* h, const void* w1, cons
   // One hidden row in bf16: the persistent weight stream with in-stream top-k.
   if (heads_stream_supported(T, d, V, K, p.topk, dt, h, w1, w2, w2_stride, w_lm, b1))
     return launch_heads_stream(p, h, w1, b1, w2, w2_stride, w_lm, root, pool, logits_out, ws, st);
+  cudaError_t e = cudaSuccess;
+  const size_t esz = dt == MEDUSA_BF16 ? 2 : 4;
+  if (heads_mma_supported(T, d, V, K, dt, h, w1, w2, w2_stride, w_lm)) {
+    // several bf16 hidden rows: tensor-core weight stream, then top-k on the logits
+    e = launch_heads_mma(p, h, w1, b1, w2, w2_stride, w_lm, logits, ws, st);
+    if (e != cudaSuccess) return e;
+  } else {
   cudaError_t e0 = cudaMemsetAsync(err, 0, sizeof(int), st);   // set by a weight-stream wait that gave up
   if (e0 != cudaSuccess) return e0;
-  const size_t esz = dt == MEDUSA_BF16 ? 2 : 4;
-  cudaError_t e = cudaSuccess;
   for (int t0 = 0; t0 < T; t0 += p.tokens_per_pass) {
     const int tc = (T - t0) < p.tokens_per_pass ? (T - t0) : p.tokens_per_pass;
     // 1. residual block per head: rows i of W1_k, x = h
@@ -522,6 +531,7 @@ cudaError_t launch_heads(const HeadsPlan& p, const void* h, const void* w1, cons
     e = dt == MEDUSA_BF16 ? gemv_any<uint16_t>(p.tokens_per_pass, g, K + 1, err, st)
                           : gemv_any<float>(p.tokens_per_pass, g, K + 1, err, st);
     if (e != cudaSuccess) return e;
+  }
   }
   // 3. top-k
   const size_t smem_p = (size_t)p.chunk * (sizeof(float) + 1);

@@ -1,0 +1,420 @@
+// Medusa heads for several hidden rows at once on tcgen05 tensor cores ([CN] "Medusa
+// 的核心思路与系统位置"; [Math] "The Medusa head: math and shapes"; [M7.2] §0x02A,
+// §0x04D; [PartII] Part 4).
+//
+// With T >= 2 rows (batched serving: one frontier row per sequence) each weight row
+// meets T inputs, which the CUDA cores can no longer absorb at HBM speed; the weight
+// stream becomes a skinny GEMM: D[r][n] = sum_k W[r][k] X[n][k] for 128-row groups of
+// W (the M of the MMA) against N = 2T input rows (rounded up to 32).  The input rows are bf16 pairs: row
+// 2t holds bf16(x_t), row 2t + 1 holds bf16(x_t - bf16(x_t)), so the sum of the two
+// columns carries x_t to ~2^-16 relative (h itself is bf16: its second part is 0).
+//
+// One persistent CTA per SM (cooperative launch) takes 128-row groups from a global
+// counter in stream order: W1_0..W1_{K-1}, the first half of W_LM, W2_0..W2_{K-1}, the
+// rest of W_LM.
+//   - warp 0 (one lane): TMA producer.  Each stage holds one 64-column K chunk of the
+//     group (128 x 64 bf16, 16 KiB) and of the inputs (N x 64 bf16), both K-major with
+//     the 128-byte swizzle; W2 stages wait until every W1 group has written z;
+//   - warp 1: owns TMEM; one lane issues tcgen05.mma (kind::f16, bf16 in, fp32 out)
+//     into one of two TMEM accumulators of N columns;
+//   - warps 2-5: epilogue, thread = output row (TMEM lane).  A W1 row writes
+//     z_k = h + SiLU(W1_k h + b1_k) for every input row as a bf16 pair; a vocabulary
+//     row writes its T logits.  Top-k then runs on the logits.
+// All waits are bounded; on a timeout the call records an error (the top-k merge then
+// writes -1).
+#include "common.cuh"
+#include "kernels.h"
+#include "tc.cuh"
+
+namespace medusa {
+
+namespace {
+
+constexpr int kMThreads = 6 * 32;
+constexpr int kMRows = 128;                  // rows of W per group (MMA M)
+constexpr int kMKc = 64;                     // K columns per stage (one 128-byte swizzle row)
+
+struct MmaArgs {
+  const uint16_t* h;          // [T][d] bf16
+  const uint16_t* b1;         // [K][d] or null
+  int d, V, K, T, N;          // N = input rows of the MMA (2T rounded up to 32)
+  int w2_shared;              // W2 heads share one matrix
+  uint16_t* z_hl;             // [K][N][d] bf16 pairs of z
+  float* logits;              // [T][K + 1][V]
+  int* err;
+  int* cnt;                   // [0] W1 row quarters written (4 per group), [1] next group to hand out
+  int n_stages;
+  uint32_t stage_bytes;
+};
+
+struct MLayout {
+  int K, g1, gv, ga;
+  __device__ int base_lm_a() const { return K * g1; }
+  __device__ int base_w2() const { return K * g1 + ga; }
+  __device__ int base_lm_b() const { return K * g1 + ga + K * gv; }
+  __device__ int total() const { return K * g1 + K * gv + gv; }
+};
+
+struct MItem {
+  int kind;      // 0 W1, 1 W_LM, 2 W2
+  int k;
+  int grp;
+};
+
+__device__ __forceinline__ MItem mmap_item(int i, const MLayout& L) {
+  MItem it;
+  if (i < L.base_lm_a()) {
+    it.kind = 0; it.k = i / L.g1; it.grp = i % L.g1;
+  } else if (i < L.base_w2()) {
+    it.kind = 1; it.k = 0; it.grp = i - L.base_lm_a();
+  } else if (i < L.base_lm_b()) {
+    const int r = i - L.base_w2();
+    it.kind = 2; it.k = r / L.gv; it.grp = r % L.gv;
+  } else {
+    it.kind = 1; it.k = 0; it.grp = L.ga + (i - L.base_lm_b());
+  }
+  return it;
+}
+
+__device__ __forceinline__ bool m_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+  const uint64_t t0 = global_ns();
+  for (uint32_t it = 0;; ++it) {
+    if (mbar_try(bar, parity)) return true;
+    if (*abort_flag) return false;
+    if ((it & 255u) == 255u && global_ns() - t0 > 2000000000ull) return false;
+  }
+}
+
+__global__ void __launch_bounds__(kMThreads, 1)
+    heads_mma_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmLM,
+                     const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmH,
+                     const __grid_constant__ CUtensorMap tmZ, const MmaArgs a) {
+  extern __shared__ uint8_t smem_m[];
+  uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_m) + 1023) & ~uintptr_t(1023));
+  const int S = a.n_stages, N = a.N, d = a.d, K = a.K, V = a.V, T = a.T;
+  uint64_t* bars = reinterpret_cast<uint64_t*>(sm + (size_t)S * a.stage_bytes);
+  __shared__ uint32_t tmem_slot;
+  __shared__ int abort_flag;
+  __shared__ int stage_item[16];                     // group of each stage, -1 = no more groups
+  __shared__ int dgrp[2];                            // group of each accumulator, -1 = no more
+  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[S]);
+  const uint32_t dfull0 = smem_u32(&bars[2 * S]), dempty0 = smem_u32(&bars[2 * S + 2]);
+  const uint32_t drain = smem_u32(&bars[2 * S + 4]);
+  const volatile int* abortp = &abort_flag;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  MLayout L;
+  L.K = K;
+  L.g1 = (d + kMRows - 1) / kMRows;
+  L.gv = (V + kMRows - 1) / kMRows;
+  L.ga = L.gv / 2;
+  const int n_items = L.total();
+  const int n_k = d / kMKc;
+  const uint32_t tmem_cols = (uint32_t)(2 * N <= 32 ? 32 : 2 * N <= 64 ? 64 : 2 * N <= 128 ? 128 : 2 * N <= 256 ? 256 : 512);
+
+  if (threadIdx.x == 0) {
+    abort_flag = 0;
+    for (int s = 0; s < S; ++s) {
+      mbar_init(full0 + 8 * s, 1);
+      mbar_init(empty0 + 8 * s, 1);
+    }
+    for (int p = 0; p < 2; ++p) {
+      mbar_init(dfull0 + 8 * p, 1);
+      mbar_init(dempty0 + 8 * p, 4);                 // the four epilogue warps
+    }
+    mbar_init(drain, 1);
+    asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+  }
+  if (warp == 1) {
+    asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
+                 "r"(tmem_cols)
+                 : "memory");
+    asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = tmem_slot;
+  bool ok = true;
+  int slot = 0;                                      // producer: stage slots used
+  auto give_up = [&]() {
+    *const_cast<volatile int*>(abortp) = 1;
+    atomicExch(a.err, 1);
+  };
+
+  if (warp == 0) {
+    // ---- TMA producer ----------------------------------------------------------------
+    if (lane == 0) {
+      bool z_ready = false;
+      auto take_slot = [&](int& s) -> bool {
+        s = slot % S;
+        return m_wait(empty0 + 8 * s, (uint32_t)(((slot / S) & 1) ^ 1), abortp);
+      };
+      int next = atomicAdd(&a.cnt[1], 1);
+      for (;;) {
+        const int idx = next;
+        int s;
+        if (idx >= n_items) {
+          if (!take_slot(s)) { ok = false; break; }
+          stage_item[s] = -1;
+          mbar_arrive(full0 + 8 * s);
+          ++slot;
+          break;
+        }
+        next = atomicAdd(&a.cnt[1], 1);
+        const MItem it = mmap_item(idx, L);
+        if (it.kind == 2 && !z_ready) {
+          // W2 inputs are z: every W1 group must have written its rows
+          const uint64_t t0 = global_ns();
+          for (uint32_t sp = 0;; ++sp) {
+            int v;
+            asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.cnt) : "memory");
+            if (v >= 4 * K * L.g1) { z_ready = true; break; }   // four epilogue warps per group
+            if (*abortp) break;
+            if ((sp & 63u) == 63u && global_ns() - t0 > 2000000000ull) break;
+          }
+          if (!z_ready) { ok = false; break; }
+          asm volatile("fence.proxy.async.global;" ::: "memory");   // TMA reads what other SMs wrote
+        }
+        for (int kc = 0; kc < n_k && ok; ++kc) {
+          if (!take_slot(s)) { ok = false; break; }
+          stage_item[s] = idx;
+          const uint32_t sA = smem_u32(sm + (size_t)s * a.stage_bytes), sB = sA + kMRows * kMKc * 2;
+          const uint32_t bar = full0 + 8 * s;
+          mbar_expect_tx(bar, a.stage_bytes);
+          const int r0 = it.grp * kMRows;
+          if (it.kind == 0) tma_load_2d(sA, &tmW1, kc * kMKc, it.k * d + r0, bar);
+          else if (it.kind == 1) tma_load_2d(sA, &tmLM, kc * kMKc, r0, bar);
+          else if (a.w2_shared) tma_load_2d(sA, &tmW2, kc * kMKc, r0, bar);
+          else tma_load_3d(sA, &tmW2, kc * kMKc, r0, it.k, bar);
+          if (it.kind == 2) tma_load_2d(sB, &tmZ, kc * kMKc, it.k * N, bar);
+          else tma_load_2d(sB, &tmH, kc * kMKc, 0, bar);
+          ++slot;
+        }
+        if (!ok) break;
+      }
+      if (!ok) give_up();
+    }
+  } else if (warp == 1) {
+    // ---- MMA issue: one group = n_k stages into accumulator g & 1 ------------------------
+    if (lane == 0) {
+      const uint32_t idesc = idesc_bf16(kMRows, N);
+      int u = 0;
+      for (int g = 0; ok; ++g) {
+        const int db = g & 1;
+        for (int kc = 0; kc < n_k; ++kc, ++u) {
+          const int s = u % S;
+          if (!m_wait(full0 + 8 * s, (uint32_t)((u / S) & 1), abortp)) { ok = false; break; }
+          if (kc == 0) {
+            const int idx = stage_item[s];
+            // the accumulator must have been read out (group g - 2) before it is reused
+            if (g >= 2 && !m_wait(dempty0 + 8 * db, (uint32_t)(((g >> 1) - 1) & 1), abortp)) { ok = false; break; }
+            if (idx < 0) {                               // no more groups: tell the epilogue
+              dgrp[db] = -1;
+              mbar_arrive(dfull0 + 8 * db);
+              g = -2;                                    // leave the outer loop
+              break;
+            }
+            dgrp[db] = idx;
+            __threadfence_block();
+          }
+          tc_fence_after();
+          const uint32_t sA = smem_u32(sm + (size_t)s * a.stage_bytes), sB = sA + kMRows * kMKc * 2;
+#pragma unroll
+          for (int kk = 0; kk < kMKc / 16; ++kk)
+            umma_f16(tmem + (uint32_t)(db * N), sw128_desc(sA + kk * 32, 16, 1024), sw128_desc(sB + kk * 32, 16, 1024),
+                     idesc, (kc > 0 || kk > 0) ? 1u : 0u);
+          umma_commit(empty0 + 8 * s);                   // the stage is free once these MMAs are done
+          if (kc == n_k - 1) umma_commit(dfull0 + 8 * db);
+        }
+        if (g < 0) break;
+      }
+      if (!ok) give_up();
+    }
+  } else {
+    // ---- epilogue: thread = output row ---------------------------------------------------
+    const int q = warp & 3;                            // TMEM lane quadrant of this warp
+    const int r = 32 * q + lane;
+    for (int g = 0;; ++g) {
+      const int db = g & 1;
+      if (!__all_sync(0xffffffffu, m_wait(dfull0 + 8 * db, (uint32_t)((g >> 1) & 1), abortp))) { ok = false; break; }
+      const int idx = *reinterpret_cast<volatile int*>(&dgrp[db]);
+      if (idx < 0) break;
+      tc_fence_after();
+      const MItem it = mmap_item(idx, L);
+      const int n_rows = it.kind == 0 ? d : V;
+      const int row = it.grp * kMRows + r;
+      for (int c0 = 0; c0 < N; c0 += 32) {
+        float v[32];
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(db * N + c0), v);
+        if (row < n_rows) {
+#pragma unroll
+          for (int j = 0; j < 16; ++j) {
+            const int t = c0 / 2 + j;
+            if (t >= T) break;
+            const float x = v[2 * j] + v[2 * j + 1];
+            if (it.kind == 0) {
+              float zv = x;
+              if (a.b1) zv += Elem<uint16_t>::load(a.b1, (int64_t)it.k * d + row);
+              const float z = Elem<uint16_t>::load(a.h, (int64_t)t * d + row) + zv / (1.f + expf(-zv));
+              const uint16_t hi = f32_to_bf16_bits(z);
+              const uint16_t lo = f32_to_bf16_bits(z - __uint_as_float((uint32_t)hi << 16));
+              a.z_hl[((int64_t)it.k * N + 2 * t) * d + row] = hi;
+              a.z_hl[((int64_t)it.k * N + 2 * t + 1) * d + row] = lo;
+            } else {
+              const int m = it.kind == 1 ? 0 : 1 + it.k;
+              a.logits[((int64_t)t * (K + 1) + m) * V + row] = x;
+            }
+          }
+        }
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(dempty0 + 8 * db);
+      if (it.kind == 0) {
+        // this warp's 32 rows of z are written: count them (4 per W1 group)
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) atomicAdd(&a.cnt[0], 1);
+      }
+    }
+    if (!ok && lane == 0) give_up();
+  }
+
+  // ---- join, drain after a failure, free TMEM ----------------------------------------
+  __syncthreads();
+  if (*abortp) {
+    if (warp == 0 && lane == 0)
+      for (int n = slot - S; n < slot; ++n)
+        if (n >= 0) mbar_wait(full0 + 8 * (n % S), (uint32_t)((n / S) & 1), 100000000ull);
+    if (warp == 1 && lane == 0) {
+      umma_commit(drain);
+      mbar_wait(drain, 0, 100000000ull);
+    }
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (warp == 1) {
+    tc_fence_after();
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(tmem_cols) : "memory");
+  }
+}
+
+// Input rows as bf16 pairs: H[2t] = h_t, H[2t + 1] = 0 (h is bf16), padding rows 0;
+// the padding rows of every z_k are cleared too.
+__global__ void heads_mma_prep_kernel(const uint16_t* __restrict__ h, int T, int d, int N, int K,
+                                      uint16_t* __restrict__ h_hl, uint16_t* __restrict__ z_hl) {
+  const int i = blockIdx.x * blockDim.x + threadIdx.x;
+  if (i >= d) return;
+  for (int n = 0; n < N; ++n) h_hl[(int64_t)n * d + i] = (n < 2 * T && (n & 1) == 0) ? h[(int64_t)(n >> 1) * d + i] : 0;
+  for (int k = 0; k < K; ++k)
+    for (int n = 2 * T; n < N; ++n) z_hl[((int64_t)k * N + n) * d + i] = 0;
+}
+
+}  // namespace
+
+size_t heads_mma_rows(int T) { return (size_t)((2 * T + 31) / 32 * 32); }
+
+namespace {
+size_t mma_stage_bytes(int N) { return (size_t)kMRows * kMKc * 2 + (size_t)N * kMKc * 2; }
+int mma_stages(int N) {
+  const size_t budget = 227 * 1024 - 1024 - 32 * 8;
+  int s = (int)(budget / mma_stage_bytes(N));
+  return s > 12 ? 12 : s;
+}
+size_t mma_smem(int N) { return 1024 + (size_t)mma_stages(N) * mma_stage_bytes(N) + 32 * 8; }
+
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {inner, rows};
+  cuuint64_t strides[1] = {inner * 2};
+  cuuint32_t box[2] = {(cuuint32_t)kMKc, box_rows}, estr[2] = {1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
+bool encode_w2(CUtensorMap* map, const void* base, int d, int V, int K, int64_t stride) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)d, (cuuint64_t)V, (cuuint64_t)K};
+  cuuint64_t strides[2] = {(cuuint64_t)d * 2, (cuuint64_t)stride * 2};
+  cuuint32_t box[3] = {(cuuint32_t)kMKc, (cuuint32_t)kMRows, 1}, estr[3] = {1, 1, 1};
+  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+}  // namespace
+
+bool heads_mma_supported(int T, int d, int V, int K, medusa_dtype dt, const void* h, const void* w1, const void* w2,
+                         int64_t w2_stride, const void* w_lm) {
+  auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
+  if (T < 2 || T > 128 || dt != MEDUSA_BF16 || K < 1 || d % kMKc != 0 || V < 1) return false;
+  if (!h || !w1 || !w2 || !w_lm || !al(h) || !al(w1) || !al(w2) || !al(w_lm)) return false;
+  if (w2_stride < 0 || (w2_stride * 2) % 16 != 0 || (w2_stride != 0 && w2_stride < (int64_t)V * d)) return false;
+  if (!encode_fn()) return false;
+  int dev = 0, coop = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return false;
+  cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
+  const int N = (int)heads_mma_rows(T);
+  if (coop == 0 || mma_stages(N) < 2) return false;
+  if (cudaFuncSetAttribute(heads_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mma_smem(N)) !=
+      cudaSuccess)
+    return false;
+  int per_sm = 0;
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, heads_mma_kernel, kMThreads, mma_smem(N)) != cudaSuccess)
+    return false;
+  return per_sm >= 1;
+}
+
+cudaError_t launch_heads_mma(const HeadsPlan& p, const void* h, const void* w1, const void* b1, const void* w2,
+                             int64_t w2_stride, const void* w_lm, float* logits, void* ws, cudaStream_t st) {
+  char* base = (char*)ws;
+  const int T = p.T, d = p.d, V = p.V, K = p.K;
+  const int N = (int)heads_mma_rows(T);
+  uint16_t* h_hl = (uint16_t*)(base + p.off_hhl);
+  uint16_t* z_hl = (uint16_t*)(base + p.off_zhl);
+  int* err = (int*)(base + p.off_err);
+  CUtensorMap mw1, mlm, mw2, mh, mz;
+  const bool shared = w2_stride == 0;
+  if (!encode_2d(&mw1, w1, d, (uint64_t)K * d, kMRows) || !encode_2d(&mlm, w_lm, d, V, kMRows) ||
+      !(shared ? encode_2d(&mw2, w2, d, V, kMRows) : encode_w2(&mw2, w2, d, V, K, w2_stride)) ||
+      !encode_2d(&mh, h_hl, d, N, N) || !encode_2d(&mz, z_hl, d, (uint64_t)K * N, N))
+    return cudaErrorInvalidValue;
+  MmaArgs a{};
+  a.h = (const uint16_t*)h;
+  a.b1 = (const uint16_t*)b1;
+  a.d = d; a.V = V; a.K = K; a.T = T; a.N = N;
+  a.w2_shared = shared ? 1 : 0;
+  a.z_hl = z_hl;
+  a.logits = logits;
+  a.err = err;
+  a.cnt = err + 4;
+  a.n_stages = mma_stages(N);
+  a.stage_bytes = (uint32_t)mma_stage_bytes(N);
+  cudaError_t e = cudaMemsetAsync(err, 0, kHeadsCounterBytes, st);
+  if (e != cudaSuccess) return e;
+  heads_mma_prep_kernel<<<(d + 255) / 256, 256, 0, st>>>((const uint16_t*)h, T, d, N, K, h_hl, z_hl);
+  if ((e = cudaGetLastError()) != cudaSuccess) return e;
+  const size_t smem = mma_smem(N);
+  e = cudaFuncSetAttribute(heads_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int dev = 0, sms = 0;
+  cudaGetDevice(&dev);
+  cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3(sms);
+  cfg.blockDim = dim3(kMThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeCooperative;
+  attr[0].val.cooperative = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, heads_mma_kernel, mw1, mlm, mw2, mh, mz, a);
+  if (e != cudaSuccess) return e;
+  return cudaGetLastError();
+}
+
+}  // namespace medusa

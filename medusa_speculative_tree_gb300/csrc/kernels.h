@@ -16,7 +16,7 @@ struct HeadsPlan {
   int tokens_per_pass;   // tokens whose fp32 x rows fit in shared memory at once
   int chunk;             // logits per partial top-k CTA
   int n_chunks;          // ceil(V / chunk)
-  size_t off_z, off_logits, off_cand, off_scand, off_err, bytes;
+  size_t off_z, off_logits, off_cand, off_scand, off_hhl, off_zhl, off_err, bytes;
 };
 // Weight-stream path (heads_stream.cu): at most this many CTAs, and an error flag plus
 // completion counters in the first kHeadsCounterBytes at off_err (zeroed every call).
@@ -28,6 +28,13 @@ bool heads_stream_supported(int T, int d, int V, int K, int topk, medusa_dtype d
 cudaError_t launch_heads_stream(const HeadsPlan& p, const void* h, const void* w1, const void* b1, const void* w2,
                                 int64_t w2_stride, const void* w_lm, int32_t* root, int32_t* pool,
                                 float* logits_out, void* ws, cudaStream_t st);
+// Tensor-core path for 2 <= T <= 128 hidden rows (heads_mma.cu): writes all logits,
+// the top-k kernels then select.  Input rows of the MMA: 2T rounded up to 32.
+size_t heads_mma_rows(int T);
+bool heads_mma_supported(int T, int d, int V, int K, medusa_dtype dt, const void* h, const void* w1, const void* w2,
+                         int64_t w2_stride, const void* w_lm);
+cudaError_t launch_heads_mma(const HeadsPlan& p, const void* h, const void* w1, const void* b1, const void* w2,
+                             int64_t w2_stride, const void* w_lm, float* logits, void* ws, cudaStream_t st);
 cudaError_t launch_heads(const HeadsPlan& p, const void* h, const void* w1, const void* b1,
                          const void* w2, int64_t w2_stride, const void* w_lm, medusa_dtype dt,
                          int32_t* root, int32_t* pool, float* logits_out, void* ws,
