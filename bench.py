@@ -234,14 +234,20 @@ class Round:
         return 4.0 * w.head_dim * float(self.lengths.sum()) * self.N * w.n_q_heads
 
     def launches_per_step(self):
-        from medusa_speculative_tree_gb300 import _native  # noqa: F401
+        """Kernels of this library launched by one step (memsets not counted)."""
         w = self.w
-        tpp = 1
-        fit = max(1, min(16, (160 * 1024) // (w.hidden * 4)))
-        while tpp * 2 <= min(w.batch, fit):
-            tpp *= 2
-        passes = math.ceil(w.batch / tpp)
-        heads = 2 * passes + 2
+        bf16 = w.dtype == "bf16"
+        T = w.batch
+        if bf16 and T == 1 and w.hidden % 256 == 0 and w.hidden <= 4096 and w.n_heads >= 1:
+            heads = 1                                   # one persistent weight stream with top-k
+        elif bf16 and 2 <= T <= 128 and w.hidden % 64 == 0 and w.n_heads >= 1:
+            heads = 3                                   # input pairs, tensor-core stream, top-k
+        else:
+            tpp = 1
+            fit = max(1, min(16, (160 * 1024) // (w.hidden * 4)))
+            while tpp * 2 <= min(T, fit):
+                tpp *= 2
+            heads = 2 * math.ceil(T / tpp) + 1         # two GEMV kernels per pass, then top-k
         accept = 2 if self.tmpl.n_internal > 0 else 1
         return heads + 1 + 1 + accept + 1
 

@@ -19,6 +19,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kTopkMaxSpans = 64;     // CTAs per logits row in the top-k
 
 struct GemvArgs {
   const void* w0;           // matrix 0
@@ -275,96 +276,130 @@ struct Cand {
   int i;
 };
 
-__device__ __forceinline__ Cand better(Cand a, Cand b) { return ranks_before(a.v, a.i, b.v, b.i) ? a : b; }
+// Top-k of the logits rows (row = t * (K + 1) + m), each row split over gridDim.x CTAs.
+// Every warp of a CTA scans a slice of the CTA's span and keeps its own top-k sorted
+// across its lanes (lane i holds the i-th best, value desc, id asc); a value enters
+// only when it ranks before the current k-th entry (a ballot over 32 values at a time,
+// rare after the first few hundred values), so the scan runs at load speed.  The CTA
+// merges its warps' lists and publishes them; the last CTA of the row (a ticket it
+// resets) merges all spans into root (m = 0, top-1) or pool.
+__device__ __forceinline__ void topk_insert(float v, int id, int kk, float& lv, int& li) {
+  const int lane = threadIdx.x & 31;
+  const bool before = lane < kk && ranks_before(v, id, lv, li);
+  const unsigned mask = __ballot_sync(0xffffffffu, before);
+  if (mask) {
+    const int pos = __ffs(mask) - 1;
+    const float uv = __shfl_up_sync(0xffffffffu, lv, 1);
+    const int ui = __shfl_up_sync(0xffffffffu, li, 1);
+    if (lane == pos) { lv = v; li = id; }
+    else if (lane > pos && lane < kk) { lv = uv; li = ui; }
+  }
+}
 
-__device__ Cand block_best(Cand c, Cand* red) {
-  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+// Merge n sorted lists of kk entries (list l at lists[l * stride], l < n <= 64) into
+// the first kk entries of the union; warp-wide, every lane gets the result r in round r.
+template <typename Load>
+__device__ __forceinline__ void merge_lists(int n, int kk, Load load, float* out_v, int* out_i) {
+  const int lane = threadIdx.x & 31;
+  int hp[2] = {0, 0};
+  Cand head[2];
 #pragma unroll
-  for (int o = 16; o > 0; o >>= 1) {
-    Cand other{__shfl_xor_sync(0xffffffffu, c.v, o), __shfl_xor_sync(0xffffffffu, c.i, o)};
-    c = better(c, other);
-  }
-  if (lane == 0) red[warp] = c;
-  __syncthreads();
-  if (threadIdx.x == 0) {
-    Cand b = red[0];
-    for (int w = 1; w < kWarps; ++w) b = better(b, red[w]);
-    red[kWarps] = b;
-  }
-  __syncthreads();
-  Cand r = red[kWarps];
-  __syncthreads();
-  return r;
-}
-
-// Candidates of one chunk of one logits row: its `topk` best (value desc, id asc).
-__global__ void __launch_bounds__(kThreads) topk_partial_kernel(const float* __restrict__ logits,
-                                                                int V, int chunk, int topk,
-                                                                Cand* __restrict__ cand) {
-  extern __shared__ unsigned char smem_raw[];
-  float* vals = reinterpret_cast<float*>(smem_raw);
-  unsigned char* taken = smem_raw + (size_t)chunk * sizeof(float);
-  __shared__ Cand red[kWarps + 1];
-  const int row = blockIdx.y, c = blockIdx.x;
-  const int start = c * chunk;
-  const int n = min(chunk, V - start);
-  const float* src = logits + (int64_t)row * V + start;
-  for (int i = threadIdx.x; i < n; i += kThreads) {
-    vals[i] = src[i];
-    taken[i] = 0;
-  }
-  __syncthreads();
-  Cand* out = cand + ((int64_t)row * gridDim.x + c) * topk;
-  for (int r = 0; r < topk; ++r) {
-    Cand best{-FLT_MAX, INT_MAX};
-    bool any = false;
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-      if (taken[i]) continue;
-      Cand x{vals[i], start + i};
-      if (!any || ranks_before(x.v, x.i, best.v, best.i)) best = x;
-      any = true;
+  for (int q = 0; q < 2; ++q) head[q] = lane + 32 * q < n ? load(lane + 32 * q, 0) : Cand{-INFINITY, INT_MAX};
+  for (int r = 0; r < kk; ++r) {
+    int qb = (head[1].i != INT_MAX && (head[0].i == INT_MAX || ranks_before(head[1].v, head[1].i, head[0].v, head[0].i))) ? 1 : 0;
+    float bv = head[qb].v;
+    int bi = head[qb].i;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, bv, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, bi, o);
+      if (ranks_before(ov, oi, bv, bi)) { bv = ov; bi = oi; }
     }
-    if (!any) best = Cand{-INFINITY, INT_MAX};
-    Cand b = block_best(best, red);
-    if (threadIdx.x == 0) {
-      out[r] = b;
-      if (b.i != INT_MAX) taken[b.i - start] = 1;
+    if (bi != INT_MAX && head[qb].i == bi) {
+      ++hp[qb];
+      head[qb] = hp[qb] < kk ? load(lane + 32 * qb, hp[qb]) : Cand{-INFINITY, INT_MAX};
     }
-    __syncthreads();
+    out_v[r] = bv;
+    out_i[r] = bi;
   }
 }
 
-// Merge the chunk candidates of one (row t, matrix m); write root (m = 0) or pool.
-__global__ void __launch_bounds__(kThreads) topk_merge_kernel(const Cand* __restrict__ cand,
-                                                              int n_chunks, int topk, int Kp1,
-                                                              int32_t* __restrict__ root,
-                                                              int32_t* __restrict__ pool,
-                                                              const int* __restrict__ err) {
-  extern __shared__ unsigned char smem_raw[];
-  Cand* c = reinterpret_cast<Cand*>(smem_raw);
-  __shared__ Cand red[kWarps + 1];
-  const int row = blockIdx.x;
+__global__ void __launch_bounds__(kThreads) topk_rows_kernel(const float* __restrict__ logits, int V, int topk,
+                                                             int Kp1, int span, Cand* __restrict__ cand,
+                                                             int* __restrict__ tick, int32_t* __restrict__ root,
+                                                             int32_t* __restrict__ pool, const int* __restrict__ err) {
+  __shared__ Cand lists[kWarps][32];
+  __shared__ float mv[32];
+  __shared__ int mi[32];
+  __shared__ int last;
+  const int row = blockIdx.y, c = blockIdx.x, ns = gridDim.x;
   const int t = row / Kp1, m = row % Kp1;
-  const int n = n_chunks * topk;
-  for (int i = threadIdx.x; i < n; i += kThreads) c[i] = cand[(int64_t)row * n + i];
-  __syncthreads();
-  const int rounds = (m == 0) ? 1 : topk;
-  for (int r = 0; r < rounds; ++r) {
-    Cand best{-INFINITY, INT_MAX};
-    int where = -1;
-    for (int i = threadIdx.x; i < n; i += kThreads) {
-      Cand x = c[i];
-      if (x.i == INT_MAX) continue;
-      if (where < 0 || ranks_before(x.v, x.i, best.v, best.i)) { best = x; where = i; }
+  const int kk = m == 0 ? 1 : topk;
+  const float* src = logits + (int64_t)row * V;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int c_lo = c * span, c_hi = min(V, c_lo + span);
+  float lv = -INFINITY;
+  int li = INT_MAX;
+  // warp w scans part of [c_lo, c_hi); 128 values per step as one float4 per lane when
+  // rows are 16-byte aligned (span is a multiple of 128 then)
+  auto offer = [&](float v, int i, bool valid) {
+    const float tv = __shfl_sync(0xffffffffu, lv, kk - 1);   // the current k-th entry
+    const int ti = __shfl_sync(0xffffffffu, li, kk - 1);
+    unsigned cm = __ballot_sync(0xffffffffu, valid && ranks_before(v, i, tv, ti));
+    while (cm) {
+      const int sl = __ffs(cm) - 1;
+      cm &= cm - 1;
+      topk_insert(__shfl_sync(0xffffffffu, v, sl), __shfl_sync(0xffffffffu, i, sl), kk, lv, li);
     }
-    Cand b = block_best(best, red);
-    if (where >= 0 && best.i == b.i) c[where].i = INT_MAX;   // ids are unique: exactly one owner
-    if (threadIdx.x == 0) {
-      const int id = *err ? -1 : b.i;               // -1: the weight stream gave up waiting
+  };
+  if ((V & 3) == 0) {
+#pragma unroll 2
+    for (int base = c_lo + 128 * warp; base < c_hi; base += 128 * kWarps) {
+      const int i0 = base + 4 * lane;
+      const float4 q = i0 < c_hi ? __ldg(reinterpret_cast<const float4*>(src + i0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      offer(q.x, i0, i0 < c_hi);
+      offer(q.y, i0 + 1, i0 + 1 < c_hi);
+      offer(q.z, i0 + 2, i0 + 2 < c_hi);
+      offer(q.w, i0 + 3, i0 + 3 < c_hi);
+    }
+  } else {
+    for (int base = c_lo + 32 * warp; base < c_hi; base += 32 * kWarps) {
+      const int i = base + lane;
+      offer(i < c_hi ? __ldg(src + i) : -INFINITY, i, i < c_hi);
+    }
+  }
+  lists[warp][lane] = Cand{lv, li};
+  __syncthreads();
+  if (warp == 0) {
+    merge_lists(kWarps, kk, [&](int l, int e) { return lists[l][e]; }, mv, mi);
+    __syncwarp();
+    Cand* out = cand + ((int64_t)row * ns + c) * topk;
+    if (lane < kk) out[lane] = Cand{mv[lane], mi[lane]};
+    __threadfence();
+    __syncwarp();
+    int tk = 0;
+    if (lane == 0) tk = atomicAdd(&tick[row], 1);
+    tk = __shfl_sync(0xffffffffu, tk, 0);
+    last = tk == ns - 1;
+  }
+  __syncthreads();
+  if (!last || warp != 0) return;
+  // the last CTA of the row: merge every span's list
+  __threadfence();
+  const Cand* rl = cand + (int64_t)row * ns * topk;
+  merge_lists(ns, kk, [&](int l, int e) {
+    const float2 f = __ldcg(reinterpret_cast<const float2*>(rl + (int64_t)l * topk + e));
+    return Cand{f.x, __float_as_int(f.y)};
+  }, mv, mi);
+  __syncwarp();
+  if (lane == 0) {
+    const bool bad = *reinterpret_cast<const volatile int*>(err) != 0;   // a weight-stream wait gave up
+    for (int r = 0; r < kk; ++r) {
+      const int id = (bad || mi[r] == INT_MAX) ? -1 : mi[r];
       if (m == 0) root[t] = id;
       else pool[((int64_t)t * (Kp1 - 1) + (m - 1)) * topk + r] = id;
     }
-    __syncthreads();
+    tick[row] = 0;                                       // ready for the next call
   }
 }
 
@@ -451,27 +486,21 @@ HeadsPlan plan_heads(int T, int d, int V, int K, int topk) {
   int tile = 1;
   while (tile * 2 <= tpp) tile *= 2;
   p.tokens_per_pass = tile;
-  int chunk = (V + 63) / 64;
-  chunk = (chunk + 255) / 256 * 256;
-  if (chunk < 1024) chunk = 1024;
-  if (chunk > 8192) chunk = 8192;
-  p.chunk = chunk;
-  p.n_chunks = (V + chunk - 1) / chunk;
   size_t off = 0;
   p.off_z = off;
   off = align_up(off + (size_t)T * K * d * sizeof(float), 256);
   p.off_logits = off;
   off = align_up(off + (size_t)T * (K + 1) * V * sizeof(float), 256);
-  p.off_cand = off;
-  off = align_up(off + (size_t)T * (K + 1) * p.n_chunks * topk * sizeof(Cand), 256);
   p.off_scand = off;                                       // weight-stream path: per-CTA lists
   off = align_up(off + (size_t)(K + 1) * kHeadsStreamMaxGrid * topk * sizeof(Cand), 256);
   p.off_hhl = off;                                         // tensor-core path: input rows as bf16 pairs
   off = align_up(off + (T >= 2 ? heads_mma_rows(T) * d * 2 : 0), 256);
   p.off_zhl = off;
   off = align_up(off + (T >= 2 ? (size_t)K * heads_mma_rows(T) * d * 2 : 0), 256);
-  p.off_err = off;
-  off = align_up(off + kHeadsCounterBytes, 256);
+  p.off_cand = off;                                        // top-k: per-span sorted lists
+  off = align_up(off + (size_t)T * (K + 1) * kTopkMaxSpans * topk * sizeof(Cand), 256);
+  p.off_err = off;                                         // error flag and counters, then tickets
+  off = align_up(off + kHeadsCounterBytes + (size_t)T * (K + 1) * sizeof(int), 256);
   p.bytes = off;
   (void)pow2_at_least;
   return p;
@@ -484,21 +513,21 @@ cudaError_t launch_heads(const HeadsPlan& p, const void* h, const void* w1, cons
   char* base = (char*)ws;
   float* z = (float*)(base + p.off_z);
   float* logits = logits_out ? logits_out : (float*)(base + p.off_logits);
-  Cand* cand = (Cand*)(base + p.off_cand);
   int* err = (int*)(base + p.off_err);
   const int d = p.d, V = p.V, K = p.K, T = p.T;
   // One hidden row in bf16: the persistent weight stream with in-stream top-k.
   if (heads_stream_supported(T, d, V, K, p.topk, dt, h, w1, w2, w2_stride, w_lm, b1))
     return launch_heads_stream(p, h, w1, b1, w2, w2_stride, w_lm, root, pool, logits_out, ws, st);
-  cudaError_t e = cudaSuccess;
   const size_t esz = dt == MEDUSA_BF16 ? 2 : 4;
+  const int rows = T * (K + 1);
+  // error flag, counters and top-k tickets start at zero
+  cudaError_t e = cudaMemsetAsync(err, 0, kHeadsCounterBytes + (size_t)rows * sizeof(int), st);
+  if (e != cudaSuccess) return e;
   if (heads_mma_supported(T, d, V, K, dt, h, w1, w2, w2_stride, w_lm)) {
     // several bf16 hidden rows: tensor-core weight stream, then top-k on the logits
     e = launch_heads_mma(p, h, w1, b1, w2, w2_stride, w_lm, logits, ws, st);
     if (e != cudaSuccess) return e;
   } else {
-  cudaError_t e0 = cudaMemsetAsync(err, 0, sizeof(int), st);   // set by a weight-stream wait that gave up
-  if (e0 != cudaSuccess) return e0;
   for (int t0 = 0; t0 < T; t0 += p.tokens_per_pass) {
     const int tc = (T - t0) < p.tokens_per_pass ? (T - t0) : p.tokens_per_pass;
     // 1. residual block per head: rows i of W1_k, x = h
@@ -533,17 +562,17 @@ cudaError_t launch_heads(const HeadsPlan& p, const void* h, const void* w1, cons
     if (e != cudaSuccess) return e;
   }
   }
-  // 3. top-k
-  const size_t smem_p = (size_t)p.chunk * (sizeof(float) + 1);
-  e = cudaFuncSetAttribute(topk_partial_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_p);
-  if (e != cudaSuccess) return e;
-  topk_partial_kernel<<<dim3(p.n_chunks, T * (K + 1)), kThreads, smem_p, st>>>(logits, V, p.chunk,
-                                                                               p.topk, cand);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const size_t smem_m = (size_t)p.n_chunks * p.topk * sizeof(Cand);
-  e = cudaFuncSetAttribute(topk_merge_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem_m);
-  if (e != cudaSuccess) return e;
-  topk_merge_kernel<<<T * (K + 1), kThreads, smem_m, st>>>(cand, p.n_chunks, p.topk, K + 1, root, pool, err);
+  // 3. top-k, one CTA per (row t, matrix m)
+  int sms = 148, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int ns = (2 * sms + rows - 1) / rows;                    // spans per row: about two CTAs per SM
+  if (ns > kTopkMaxSpans) ns = kTopkMaxSpans;
+  if (ns > (V + 1023) / 1024) ns = (V + 1023) / 1024;      // at least ~1024 logits per span
+  if (ns < 1) ns = 1;
+  const int span = ((V + ns - 1) / ns + 127) / 128 * 128;
+  ns = (V + span - 1) / span;
+  topk_rows_kernel<<<dim3(ns, rows), kThreads, 0, st>>>(logits, V, p.topk, K + 1, span, (Cand*)(base + p.off_cand),
+                                                        err + kHeadsCounterBytes / sizeof(int), root, pool, err);
   return cudaGetLastError();
 }
 

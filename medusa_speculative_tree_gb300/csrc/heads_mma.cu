@@ -392,8 +392,7 @@ cudaError_t launch_heads_mma(const HeadsPlan& p, const void* h, const void* w1, 
   a.cnt = err + 4;
   a.n_stages = mma_stages(N);
   a.stage_bytes = (uint32_t)mma_stage_bytes(N);
-  cudaError_t e = cudaMemsetAsync(err, 0, kHeadsCounterBytes, st);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   heads_mma_prep_kernel<<<(d + 255) / 256, 256, 0, st>>>((const uint16_t*)h, T, d, N, K, h_hl, z_hl);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t smem = mma_smem(N);

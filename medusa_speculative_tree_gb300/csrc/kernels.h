@@ -14,9 +14,7 @@ namespace medusa {
 struct HeadsPlan {
   int T, d, V, K, topk;
   int tokens_per_pass;   // tokens whose fp32 x rows fit in shared memory at once
-  int chunk;             // logits per partial top-k CTA
-  int n_chunks;          // ceil(V / chunk)
-  size_t off_z, off_logits, off_cand, off_scand, off_hhl, off_zhl, off_err, bytes;
+  size_t off_z, off_logits, off_scand, off_hhl, off_zhl, off_cand, off_err, bytes;
 };
 // Weight-stream path (heads_stream.cu): at most this many CTAs, and an error flag plus
 // completion counters in the first kHeadsCounterBytes at off_err (zeroed every call).
