@@ -12,9 +12,10 @@
 // One persistent CTA per SM (cooperative launch) takes 128-row groups from a global
 // counter in stream order: W1_0..W1_{K-1}, the first half of W_LM, W2_0..W2_{K-1}, the
 // rest of W_LM.
-//   - warp 0 (one lane): TMA producer.  Each stage holds one 64-column K chunk of the
-//     group (128 x 64 bf16, 16 KiB) and of the inputs (N x 64 bf16), both K-major with
-//     the 128-byte swizzle; W2 stages wait until every W1 group has written z;
+//   - warp 0 (one lane): TMA producer.  Each stage holds up to four 64-column K chunks
+//     of the group (128 x 64 bf16, 16 KiB each) and of the inputs (N x 64 bf16), both
+//     K-major with the 128-byte swizzle; W2 stages wait until every W1 group has
+//     written z;
 //   - warp 1: owns TMEM; one lane issues tcgen05.mma (kind::f16, bf16 in, fp32 out)
 //     into one of two TMEM accumulators of N columns;
 //   - warps 2-5: epilogue, thread = output row (TMEM lane).  A W1 row writes
@@ -44,6 +45,7 @@ struct MmaArgs {
   int* err;
   int* cnt;                   // [0] W1 row quarters written (4 per group), [1] next group to hand out
   int n_stages;
+  int bps;                    // 64-column K chunks (TMA boxes) per stage
   uint32_t stage_bytes;
 };
 
@@ -108,7 +110,9 @@ __global__ void __launch_bounds__(kMThreads, 1)
   L.gv = (V + kMRows - 1) / kMRows;
   L.ga = L.gv / 2;
   const int n_items = L.total();
-  const int n_k = d / kMKc;
+  const int bps = a.bps;
+  const int n_k = d / (kMKc * bps);                  // stages per group
+  const uint32_t a_bytes = kMRows * kMKc * 2, b_bytes = (uint32_t)N * kMKc * 2;   // one box each
   const uint32_t tmem_cols = (uint32_t)(2 * N <= 32 ? 32 : 2 * N <= 64 ? 64 : 2 * N <= 128 ? 128 : 2 * N <= 256 ? 256 : 512);
 
   if (threadIdx.x == 0) {
@@ -178,16 +182,21 @@ __global__ void __launch_bounds__(kMThreads, 1)
         for (int kc = 0; kc < n_k && ok; ++kc) {
           if (!take_slot(s)) { ok = false; break; }
           stage_item[s] = idx;
-          const uint32_t sA = smem_u32(sm + (size_t)s * a.stage_bytes), sB = sA + kMRows * kMKc * 2;
+          // A boxes (weights) first, then B boxes (inputs), bps of each
+          const uint32_t sA = smem_u32(sm + (size_t)s * a.stage_bytes), sB = sA + bps * a_bytes;
           const uint32_t bar = full0 + 8 * s;
           mbar_expect_tx(bar, a.stage_bytes);
           const int r0 = it.grp * kMRows;
-          if (it.kind == 0) tma_load_2d(sA, &tmW1, kc * kMKc, it.k * d + r0, bar);
-          else if (it.kind == 1) tma_load_2d(sA, &tmLM, kc * kMKc, r0, bar);
-          else if (a.w2_shared) tma_load_2d(sA, &tmW2, kc * kMKc, r0, bar);
-          else tma_load_3d(sA, &tmW2, kc * kMKc, r0, it.k, bar);
-          if (it.kind == 2) tma_load_2d(sB, &tmZ, kc * kMKc, it.k * N, bar);
-          else tma_load_2d(sB, &tmH, kc * kMKc, 0, bar);
+          for (int bx = 0; bx < bps; ++bx) {
+            const int col = (kc * bps + bx) * kMKc;
+            const uint32_t dA = sA + bx * a_bytes, dB = sB + bx * b_bytes;
+            if (it.kind == 0) tma_load_2d(dA, &tmW1, col, it.k * d + r0, bar);
+            else if (it.kind == 1) tma_load_2d(dA, &tmLM, col, r0, bar);
+            else if (a.w2_shared) tma_load_2d(dA, &tmW2, col, r0, bar);
+            else tma_load_3d(dA, &tmW2, col, r0, it.k, bar);
+            if (it.kind == 2) tma_load_2d(dB, &tmZ, col, it.k * N, bar);
+            else tma_load_2d(dB, &tmH, col, 0, bar);
+          }
           ++slot;
         }
         if (!ok) break;
@@ -218,11 +227,13 @@ __global__ void __launch_bounds__(kMThreads, 1)
             __threadfence_block();
           }
           tc_fence_after();
-          const uint32_t sA = smem_u32(sm + (size_t)s * a.stage_bytes), sB = sA + kMRows * kMKc * 2;
+          const uint32_t sA = smem_u32(sm + (size_t)s * a.stage_bytes), sB = sA + bps * a_bytes;
+          for (int bx = 0; bx < bps; ++bx) {
 #pragma unroll
-          for (int kk = 0; kk < kMKc / 16; ++kk)
-            umma_f16(tmem + (uint32_t)(db * N), sw128_desc(sA + kk * 32, 16, 1024), sw128_desc(sB + kk * 32, 16, 1024),
-                     idesc, (kc > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < kMKc / 16; ++kk)
+              umma_f16(tmem + (uint32_t)(db * N), sw128_desc(sA + bx * a_bytes + kk * 32, 16, 1024),
+                       sw128_desc(sB + bx * b_bytes + kk * 32, 16, 1024), idesc, (kc > 0 || bx > 0 || kk > 0) ? 1u : 0u);
+          }
           umma_commit(empty0 + 8 * s);                   // the stage is free once these MMAs are done
           if (kc == n_k - 1) umma_commit(dfull0 + 8 * db);
         }
@@ -315,13 +326,21 @@ __global__ void heads_mma_prep_kernel(const uint16_t* __restrict__ h, int T, int
 size_t heads_mma_rows(int T) { return (size_t)((2 * T + 31) / 32 * 32); }
 
 namespace {
-size_t mma_stage_bytes(int N) { return (size_t)kMRows * kMKc * 2 + (size_t)N * kMKc * 2; }
-int mma_stages(int N) {
-  const size_t budget = 227 * 1024 - 1024 - 32 * 8;
-  int s = (int)(budget / mma_stage_bytes(N));
+// A stage holds bps boxes of weights (128 x 64) and of inputs (N x 64): as many K
+// chunks per stage as still leave two stages (fewer, larger stages cost the MMA lane
+// fewer waits per byte).
+size_t mma_stage_bytes(int N, int bps) { return (size_t)bps * ((size_t)kMRows * kMKc * 2 + (size_t)N * kMKc * 2); }
+constexpr size_t kMBudget = 227 * 1024 - 1024 - 32 * 8;
+int mma_bps(int N, int d) {
+  for (int bps = 4; bps > 1; bps >>= 1)
+    if ((d / kMKc) % bps == 0 && kMBudget / mma_stage_bytes(N, bps) >= 2) return bps;
+  return 1;
+}
+int mma_stages(int N, int d) {
+  int s = (int)(kMBudget / mma_stage_bytes(N, mma_bps(N, d)));
   return s > 12 ? 12 : s;
 }
-size_t mma_smem(int N) { return 1024 + (size_t)mma_stages(N) * mma_stage_bytes(N) + 32 * 8; }
+size_t mma_smem(int N, int d) { return 1024 + (size_t)mma_stages(N, d) * mma_stage_bytes(N, mma_bps(N, d)) + 32 * 8; }
 
 bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
   auto fn = encode_fn();
@@ -357,12 +376,13 @@ bool heads_mma_supported(int T, int d, int V, int K, medusa_dtype dt, const void
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
   const int N = (int)heads_mma_rows(T);
-  if (coop == 0 || mma_stages(N) < 2) return false;
-  if (cudaFuncSetAttribute(heads_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mma_smem(N)) !=
+  if (coop == 0 || mma_stages(N, d) < 2) return false;
+  if (cudaFuncSetAttribute(heads_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mma_smem(N, d)) !=
       cudaSuccess)
     return false;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, heads_mma_kernel, kMThreads, mma_smem(N)) != cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, heads_mma_kernel, kMThreads, mma_smem(N, d)) !=
+      cudaSuccess)
     return false;
   return per_sm >= 1;
 }
@@ -390,12 +410,13 @@ cudaError_t launch_heads_mma(const HeadsPlan& p, const void* h, const void* w1, 
   a.logits = logits;
   a.err = err;
   a.cnt = err + 4;
-  a.n_stages = mma_stages(N);
-  a.stage_bytes = (uint32_t)mma_stage_bytes(N);
+  a.bps = mma_bps(N, d);
+  a.n_stages = mma_stages(N, d);
+  a.stage_bytes = (uint32_t)mma_stage_bytes(N, a.bps);
   cudaError_t e;
   heads_mma_prep_kernel<<<(d + 255) / 256, 256, 0, st>>>((const uint16_t*)h, T, d, N, K, h_hl, z_hl);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const size_t smem = mma_smem(N);
+  const size_t smem = mma_smem(N, d);
   e = cudaFuncSetAttribute(heads_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
