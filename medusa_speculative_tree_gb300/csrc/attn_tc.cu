@@ -32,6 +32,9 @@
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
+#include <cmath>
+#include <cstdio>
+#include <cstdlib>
 #include <mutex>
 
 #include "common.cuh"
@@ -42,40 +45,16 @@ namespace medusa {
 
 namespace {
 
-constexpr int kTcThreads = 256;
-constexpr int kSoftWarps = 4;       // warps 0-3: one thread per query row
-constexpr int kProdWarp = 4;        // TMA producer
-constexpr int kMmaWarp = 5;         // TMEM owner and MMA issuer
-constexpr int kConvWarp0 = 6;       // warps 6-7: tile conversion
-constexpr int kConvThreads = 64;
 constexpr int kTcRows = 128;        // query rows per CTA
 constexpr int kTcKeys = 64;         // keys per tile
 constexpr int kDH = 128;
 constexpr int kHalf = kDH / 2;
-constexpr uint32_t kTmemCols = 256; // S buffers in columns [0, 64) and [64, 128), O in [128, 256)
-constexpr uint32_t kTmemO = 128;
+constexpr uint32_t kTmemO = 128;   // per query tile: S buffers in columns [0, 64), [64, 128); O in [128, 256)
 
 constexpr int kQBytes = kTcRows * kDH * 2;       // 2 K-blocks of [128 rows x 128 B]
 constexpr int kKBytes = kTcKeys * kDH * 2;       // 2 K-blocks of [64 rows x 128 B]
 constexpr int kVBytes = kTcKeys * kDH * 2;       // 2 MN-blocks of [64 keys x 128 B]
 constexpr int kStageBytes = kKBytes + kVBytes;
-constexpr int kStages = 2;
-constexpr int kOffQ = 0;
-constexpr int kOffStage = kQBytes;
-constexpr int kOffTable = kOffStage + kStages * kStageBytes;   // rope cos/sin, then barriers
-constexpr int kNumBars = 17;
-
-// barrier slots
-constexpr int kBarFull = 0;      // [2] stage landed (TMA transaction bytes)
-constexpr int kBarConvK = 2;     // [2] K tile converted (64 converter arrivals)
-constexpr int kBarConvV = 4;     // [2] V tile converted
-constexpr int kBarEmpty = 6;     // [2] stage consumed by the P V MMA (tcgen05.commit)
-constexpr int kBarSFull = 8;     // [2] S buffer written (tcgen05.commit)
-constexpr int kBarPFull = 10;    // [2] P written over S (one arrival per softmax warp)
-constexpr int kBarODone = 12;    // [2] P V MMA of tile j complete, slot j & 1 (tcgen05.commit)
-constexpr int kBarQReady = 14;   // queries staged (one arrival per softmax warp)
-constexpr int kBarDrain = 15;    // final commit on the error path
-constexpr int kBarQFull = 16;    // query tile landed (TMA transaction bytes)
 
 constexpr int kErrTimeout = MEDUSA_ETIMEOUT;
 constexpr int kMaxClusterSplits = 8;   // splits of a unit form one portable cluster
@@ -96,6 +75,37 @@ struct TcArgs {
 };
 
 // 2^x on the MUFU unit (ex2.approx, relative error ~2^-22); 2^-inf = +0.
+// Eight non-blocking phase tests in one round trip: all tests are issued before any
+// result is used.  Bit i of the result: phase parity p[i] of barrier b[i] has completed.
+__device__ __forceinline__ uint32_t mbar_test8(const uint32_t (&b)[8], const uint32_t (&p)[8]) {
+  uint32_t m;
+  asm volatile(
+      "{\n\t.reg .pred q0, q1, q2, q3, q4, q5, q6, q7;\n\t.reg .u32 r0, r1, r2, r3, r4, r5, r6, r7;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q0, [%1], %9;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q1, [%2], %10;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q2, [%3], %11;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q3, [%4], %12;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q4, [%5], %13;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q5, [%6], %14;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q6, [%7], %15;\n\t"
+      "mbarrier.test_wait.parity.shared::cta.b64 q7, [%8], %16;\n\t"
+      "selp.u32 r0, 1, 0, q0;\n\tselp.u32 r1, 2, 0, q1;\n\tselp.u32 r2, 4, 0, q2;\n\tselp.u32 r3, 8, 0, q3;\n\t"
+      "selp.u32 r4, 16, 0, q4;\n\tselp.u32 r5, 32, 0, q5;\n\tselp.u32 r6, 64, 0, q6;\n\tselp.u32 r7, 128, 0, q7;\n\t"
+      "or.b32 r0, r0, r1;\n\tor.b32 r2, r2, r3;\n\tor.b32 r4, r4, r5;\n\tor.b32 r6, r6, r7;\n\t"
+      "or.b32 r0, r0, r2;\n\tor.b32 r4, r4, r6;\n\tor.b32 %0, r0, r4;\n\t}"
+      : "=r"(m)
+      : "r"(b[0]), "r"(b[1]), "r"(b[2]), "r"(b[3]), "r"(b[4]), "r"(b[5]), "r"(b[6]), "r"(b[7]), "r"(p[0]),
+        "r"(p[1]), "r"(p[2]), "r"(p[3]), "r"(p[4]), "r"(p[5]), "r"(p[6]), "r"(p[7])
+      : "memory");
+  return m;
+}
+
+__device__ __forceinline__ float fmax3(float a, float b, float c) {
+  float d;
+  asm("max.f32 %0, %1, %2, %3;" : "=f"(d) : "f"(a), "f"(b), "f"(c));
+  return d;
+}
+
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -158,8 +168,9 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
 }
 
 // Re-encode one K or V tile (2 blocks of [64 rows x 128 B], bf16) to fp16 in place;
-// rows of keys >= k_valid become zero.  Thread ct of the 64 converter threads; all its
-// loads are issued before the first store, so their latencies overlap.
+// rows of keys >= k_valid become zero.  Thread ct of the kConvThreads converter
+// threads; all its loads are issued before the first store, so their latencies overlap.
+template <int kConvThreads>
 __device__ __forceinline__ void convert_tile(uint8_t* tile, int k_valid, int ct) {
   uint4* p = reinterpret_cast<uint4*>(tile);
   constexpr int kIter = (kKBytes / 16) / kConvThreads;
@@ -178,11 +189,13 @@ __device__ __forceinline__ void convert_tile(uint8_t* tile, int k_valid, int ct)
 // the tile is tree row v0 + r; dims i and i + 64 sit in the two blocks at the same
 // swizzled position.  Rows >= n_valid become zero.  `dep[i]` is the depth of the row
 // that iteration i of thread ct touches (loaded before the tile landed).
-constexpr int kRotIter = (kTcKeys * 8) / kConvThreads;
+template <int kConvThreads>
 __device__ __forceinline__ int rotate_row(int i, int ct) { return (i * kConvThreads + ct) >> 3; }
 
+template <int kConvThreads>
 __device__ __forceinline__ void convert_rotate_tile(uint8_t* tile, int n_valid, const int* dep,
                                                     const float* tab_c, const float* tab_s, int ct) {
+  constexpr int kRotIter = (kTcKeys * 8) / kConvThreads;
 #pragma unroll
   for (int i = 0; i < kRotIter; ++i) {
     const int idx = i * kConvThreads + ct;
@@ -213,28 +226,61 @@ __device__ __forceinline__ void convert_rotate_tile(uint8_t* tile, int n_valid, 
   }
 }
 
-template <bool PAGED>
-__global__ void __launch_bounds__(kTcThreads, 2)
+// Kernel configuration: QT query tiles of 128 rows per CTA share every K/V tile (one
+// conversion, one copy); NS stages of 64 keys in the ring.
+template <int QT, int NS>
+struct TcCfg {
+  static constexpr int kSoftWarps = 4 * QT;          // warps [0, 4 QT): one thread per query row
+  static constexpr int kProdWarp = 4 * QT;           // TMA producer
+  static constexpr int kMmaWarp = 4 * QT + 1;        // TMEM owner and MMA issuer
+  static constexpr int kConvWarp0 = 4 * QT + 2;      // converter warps: one per SM sub-partition
+  static constexpr int kConvWarps = QT == 2 ? 4 : 2; // (two when two CTAs share an SM)
+  static constexpr int kConvThreads = 32 * kConvWarps;
+  static constexpr int kRotIter = (kTcKeys * 8) / kConvThreads;
+  static constexpr int kThreads = 32 * (4 * QT + 2 + kConvWarps);
+  static constexpr int kRows = kTcRows * QT;
+  static constexpr uint32_t kTmemCols = 256u * QT;   // per query tile: S0 [0,64), S1 [64,128), O [128,256)
+  static constexpr int kOffStage = kQBytes * QT;
+  static constexpr int kOffTable = kOffStage + NS * kStageBytes;   // rope cos/sin, then barriers
+  // barrier slots
+  static constexpr int kBarFull = 0;                 // [NS] stage landed (TMA transaction bytes)
+  static constexpr int kBarConvK = NS;               // [NS] K tile converted (64 converter arrivals)
+  static constexpr int kBarConvV = 2 * NS;           // [NS] V tile converted
+  static constexpr int kBarEmpty = 3 * NS;           // [NS] stage consumed by the P V MMAs (tcgen05.commit)
+  static constexpr int kBarSFull = 4 * NS;           // [QT][2] S buffers written (tcgen05.commit)
+  static constexpr int kBarPFull = 4 * NS + 2 * QT;  // [QT][2] P written over S (one arrival per softmax warp)
+  static constexpr int kBarODone = 4 * NS + 4 * QT;  // [QT][2] P V MMAs of (q, j) complete, slot j & 1
+  static constexpr int kBarQReady = 4 * NS + 6 * QT; // queries staged (one arrival per softmax warp)
+  static constexpr int kBarDrain = kBarQReady + 1;   // final commit on the error path
+  static constexpr int kBarQFull = kBarQReady + 2;   // query tiles landed
+  static constexpr int kNumBars = kBarQReady + 3;
+  // the merge reuses the query and stage buffers: [rows][32] float4 O, then (m, l)
+  static_assert(QT * kQBytes + NS * kStageBytes >= kRows * (kDH * 4 + 8), "merge buffers do not fit");
+};
+
+template <bool PAGED, int QT, int NS>
+__global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) ? 2 : 1)
     attn_tc_kernel(const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV,
                    const __grid_constant__ CUtensorMap tmKn, const __grid_constant__ CUtensorMap tmVn,
                    const __grid_constant__ CUtensorMap tmQ, const TcArgs a) {
+  using C = TcCfg<QT, NS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
   const medusa_tree_t& t = a.t;
   const int D = t.max_depth;
-  float* tab_c = reinterpret_cast<float*>(sm + kOffTable);     // [(D+1)][64]
+  float* tab_c = reinterpret_cast<float*>(sm + C::kOffTable);     // [(D+1)][64]
   float* tab_s = tab_c + (D + 1) * kHalf;
   uint64_t* bars = reinterpret_cast<uint64_t*>(
       (reinterpret_cast<uintptr_t>(tab_s + (D + 1) * kHalf) + 7) & ~uintptr_t(7));
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
 
-  const int mt = blockIdx.x, s = blockIdx.y;
+  const int ct_idx = blockIdx.x, s = blockIdx.y;     // ct_idx: which QT row tiles
   const int b = blockIdx.z / a.Hkv, kvh = blockIdx.z % a.Hkv;
   const int N = t.n_rows, g = a.g, M = N * g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Lb = a.L[b];
-  const bool first_cta = (s == 0 && mt == 0 && kvh == 0 && tid == 0);
+  const bool first_cta = (s == 0 && ct_idx == 0 && kvh == 0 && tid == 0);
   if (Lb < 0 || !seq_rows_ok(a.c, b, (int64_t)Lb + N)) {
     if (first_cta) a.status[b] = MEDUSA_ECAPACITY;
     return;
@@ -245,13 +291,18 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   }
   if (first_cta) a.status[b] = MEDUSA_OK;
 
-  // Rows of this tile.  A softmax warp whose 32 rows all lie past the end is idle.
-  const int rows_valid = min(kTcRows, M - mt * kTcRows);
-  const bool soft = warp < kSoftWarps;
+  // Rows of this CTA: tiles QT * ct_idx .. + QT - 1 of 128 rows; CTA row r (= softmax
+  // thread r) is global row R = 128 * QT * ct_idx + r.  A softmax warp whose 32 rows
+  // all lie past the end is idle.
+  const int row0 = C::kRows * ct_idx;
+  const int rows_valid = min(C::kRows, M - row0);
+  const bool soft = warp < C::kSoftWarps;
   const bool live = soft && warp * 32 < rows_valid;            // warp-uniform
-  const int R = mt * kTcRows + tid;
+  const int R = row0 + tid;
   const bool row_ok = soft && R < M;
   const int u = row_ok ? R / g : 0;
+  const int qt = warp >> 2;                                   // query tile of a softmax warp
+  const int qt_live = min(QT, (rows_valid + kTcRows - 1) / kTcRows);   // tiles with rows
 
   const uint32_t bar0 = smem_u32(bars);
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
@@ -277,11 +328,24 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   auto tile_valid = [&](int j) -> int {        // rows of tile j before the end of its range
     return j >= n_pre ? N - (j - n_pre) * kTcKeys : k_end - (k_begin + j * kTcKeys);
   };
-  // TMA of tile j into stage j & 1 (its full barrier counts the bytes).
-  auto issue_tile = [&](int j) {
-    const int st = j & 1;
-    const uint32_t bar = BAR(kBarFull + st);
-    const uint32_t dK = smem_u32(sm + kOffStage + st * kStageBytes);
+  // Pages of a paged prefix tile j (block-table entries), loaded ahead of its copy.
+  auto load_pages = [&](int j, int* pg) {
+    if (PAGED && j < n_pre) {
+      const int k0 = k_begin + j * kTcKeys;
+      const int np = (min(kTcKeys, k_end - k0) + 15) / 16;
+      const int32_t* bt = a.c.block_table + (int64_t)b * a.c.max_blocks + k0 / 16;
+#pragma unroll
+      for (int p = 0; p < 4; ++p) pg[p] = p < np ? __ldg(bt + p) : 0;
+    } else {
+#pragma unroll
+      for (int p = 0; p < 4; ++p) pg[p] = 0;
+    }
+  };
+  // TMA of tile j into stage j % NS (its full barrier counts the bytes).
+  auto issue_tile = [&](int j, const int* page) {
+    const int st = j % NS;
+    const uint32_t bar = BAR(C::kBarFull + st);
+    const uint32_t dK = smem_u32(sm + C::kOffStage + st * kStageBytes);
     const uint32_t dV = dK + kKBytes;
     const int k0 = k_begin + j * kTcKeys;
     if (j >= n_pre) {
@@ -298,18 +362,16 @@ __global__ void __launch_bounds__(kTcThreads, 2)
       tma_load_4d(dV, &tmV, 0, k0, kvh, b, bar);
       tma_load_4d(dV + 8192, &tmV, 64, k0, kvh, b, bar);
     } else {
-      const int nk = min(kTcKeys, k_end - k0);
-      const int np = (nk + 15) / 16;
-      const int32_t* bt = a.c.block_table + (int64_t)b * a.c.max_blocks + k0 / 16;
-      int page[4];
-#pragma unroll
-      for (int p = 0; p < 4; ++p) page[p] = p < np ? __ldg(bt + p) : 0;
+      const int np = (min(kTcKeys, k_end - k0) + 15) / 16;
       mbar_expect_tx(bar, (uint32_t)np * 4 * 2048);
-      for (int p = 0; p < np; ++p) {
-        tma_load_4d(dK + p * 2048, &tmK, 0, 0, kvh, page[p], bar);
-        tma_load_4d(dK + 8192 + p * 2048, &tmK, 64, 0, kvh, page[p], bar);
-        tma_load_4d(dV + p * 2048, &tmV, 0, 0, kvh, page[p], bar);
-        tma_load_4d(dV + 8192 + p * 2048, &tmV, 64, 0, kvh, page[p], bar);
+#pragma unroll
+      for (int p = 0; p < 4; ++p) {
+        if (p < np) {
+          tma_load_4d(dK + p * 2048, &tmK, 0, 0, kvh, page[p], bar);
+          tma_load_4d(dK + 8192 + p * 2048, &tmK, 64, 0, kvh, page[p], bar);
+          tma_load_4d(dV + p * 2048, &tmV, 0, 0, kvh, page[p], bar);
+          tma_load_4d(dV + 8192 + p * 2048, &tmV, 64, 0, kvh, page[p], bar);
+        }
       }
     }
   };
@@ -317,35 +379,46 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   // The producer lane initialises the barriers and starts the first copies at once;
   // the other threads touch the barriers only after the __syncthreads below.
   int n_issued = 0;
-  if (tid == kProdWarp * 32) {
+  if (tid == C::kProdWarp * 32) {
     abort_flag = 0;
-    for (int st = 0; st < kStages; ++st) {
-      mbar_init(BAR(kBarFull + st), 1);
-      mbar_init(BAR(kBarConvK + st), kConvThreads);
-      mbar_init(BAR(kBarConvV + st), kConvThreads);
-      mbar_init(BAR(kBarEmpty + st), 1);
-      mbar_init(BAR(kBarSFull + st), 1);
-      mbar_init(BAR(kBarPFull + st), kSoftWarps);
-      mbar_init(BAR(kBarODone + st), 1);
+    for (int st = 0; st < NS; ++st) {
+      mbar_init(BAR(C::kBarFull + st), 1);
+      mbar_init(BAR(C::kBarConvK + st), C::kConvThreads);
+      mbar_init(BAR(C::kBarConvV + st), C::kConvThreads);
+      mbar_init(BAR(C::kBarEmpty + st), 1);
     }
-    mbar_init(BAR(kBarQReady), kSoftWarps);
-    mbar_init(BAR(kBarDrain), 1);
-    mbar_init(BAR(kBarQFull), 1);
+    for (int p = 0; p < 2 * QT; ++p) {
+      mbar_init(BAR(C::kBarSFull + p), 1);
+      mbar_init(BAR(C::kBarPFull + p), 4);
+      mbar_init(BAR(C::kBarODone + p), 1);
+    }
+    mbar_init(BAR(C::kBarQReady), C::kSoftWarps);
+    mbar_init(BAR(C::kBarDrain), 1);
+    mbar_init(BAR(C::kBarQFull), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
-    // the query tile first: rows (u, group member) of this tile, 64 dims per copy
-    const uint32_t sQ = smem_u32(sm + kOffQ);
-    mbar_expect_tx(BAR(kBarQFull), kQBytes);
-    tma_load_4d(sQ, &tmQ, 0, kvh * g, mt * (kTcRows / g), b, BAR(kBarQFull));
-    tma_load_4d(sQ + 16384, &tmQ, 64, kvh * g, mt * (kTcRows / g), b, BAR(kBarQFull));
-    for (; n_issued < n_tiles && n_issued < kStages; ++n_issued) issue_tile(n_issued);
+    // the query tiles first: rows (u, group member) of each tile, 64 dims per copy
+    mbar_expect_tx(BAR(C::kBarQFull), kQBytes * QT);
+    for (int q = 0; q < QT; ++q) {
+      const uint32_t sQ = smem_u32(sm + q * kQBytes);
+      const int u0 = (QT * ct_idx + q) * (kTcRows / g);
+      tma_load_4d(sQ, &tmQ, 0, kvh * g, u0, b, BAR(C::kBarQFull));
+      tma_load_4d(sQ + 16384, &tmQ, 64, kvh * g, u0, b, BAR(C::kBarQFull));
+    }
+    int pgs[NS][4];                // all first-stage lookups in flight together
+#pragma unroll
+    for (int k = 0; k < NS; ++k) load_pages(k, pgs[k]);
+#pragma unroll
+    for (int k = 0; k < NS; ++k)
+      if (k < n_tiles) issue_tile(k, pgs[k]);
+    n_issued = min(n_tiles, NS);
   }
-  if (warp == kMmaWarp) {
+  if (warp == C::kMmaWarp) {
     asm volatile("tcgen05.alloc.cta_group::1.sync.aligned.shared::cta.b32 [%0], %1;" ::"r"(smem_u32(&tmem_slot)),
-                 "r"(kTmemCols)
+                 "r"(C::kTmemCols)
                  : "memory");
     asm volatile("tcgen05.relinquish_alloc_permit.cta_group::1.sync.aligned;" ::: "memory");
   }
-  for (int idx = tid; idx < (D + 1) * kHalf; idx += kTcThreads) {
+  for (int idx = tid; idx < (D + 1) * kHalf; idx += C::kThreads) {
     const int dep = idx / kHalf, i = idx % kHalf;
     float sn, cs;
     sincosf(rope_angle(Lb + dep, a.th_hi[i], a.th_lo[i]), &sn, &cs);
@@ -363,64 +436,98 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   bool ok = true;
   float m_run = -INFINITY, l_run = 0.f;
 
-
-  if (warp == kProdWarp) {
-    // ---- TMA producer: tile j >= 2 once the P V MMA of tile j - 2 freed its stage ----
+  if (warp == C::kProdWarp) {
+    // ---- TMA producer: tile j >= NS once the P V MMAs of tile j - NS freed its stage ----
+    // The block-table entries of a paged tile are loaded one tile ahead of its copy.
     if (lane == 0) {
+      int pa[4], pb[4];
+      load_pages(n_issued, pa);
+      load_pages(n_issued + 1, pb);
       for (int j = n_issued; j < n_tiles; ++j) {
-        if (!wait_or_abort(BAR(kBarEmpty + (j & 1)), ((j >> 1) - 1) & 1, abortp)) {
+        if (!wait_or_abort(BAR(C::kBarEmpty + j % NS), ((j / NS) - 1) & 1, abortp)) {
           ok = false;
           break;
         }
-        issue_tile(j);
+        issue_tile(j, pa);
         n_issued = j + 1;
+#pragma unroll
+        for (int p = 0; p < 4; ++p) pa[p] = pb[p];
+        load_pages(j + 2, pb);
       }
     }
-  } else if (warp == kMmaWarp) {
+  } else if (warp == C::kMmaWarp) {
     // ---- MMA issue ------------------------------------------------------------------
-    // S(j) = Q K_j^T into TMEM buffer j & 1 once K_j is converted and the P V MMA of
-    // tile j - 2 (whose P occupied that buffer) has completed; O += P(j) V(j) once the
-    // softmax has written P(j) and V_j is converted.  Whichever is ready goes first,
-    // S before P V when both are.  Completion of P V(j) is signalled on slot j & 1, so
-    // that a slot's phase never runs more than one ahead of its waiters.  Every commit
-    // covers all MMAs issued before it.
+    // Per query tile q: S(q, j) = Q_q K_j^T into TMEM buffer (q, j & 1) once K_j is
+    // converted and the P V MMAs of (q, j - 2), whose P occupied that buffer, have
+    // completed; O_q += P(q, j) V_j once the softmax of tile q has written P(q, j) and V_j
+    // is converted.  The query tiles run independently, so that the tensor cores work on
+    // one tile while the softmax warps of the other run.  Whichever MMA is ready goes
+    // first, S before P V when both are.  Completion of P V(q, j) is signalled on slot
+    // (q, j & 1), so that a slot's phase never runs more than one ahead of its waiters;
+    // the stage of K_j / V_j is released after the last query tile's P V(j).  Every
+    // commit covers all MMAs issued before it.
     if (lane == 0) {
-      const uint32_t sQ = smem_u32(sm + kOffQ);
-      if (!wait_or_abort(BAR(kBarQReady), 0, abortp)) ok = false;
-      int js = 0, jp = 0;
+      if (!wait_or_abort(BAR(C::kBarQReady), 0, abortp)) ok = false;
+      int js[QT], jp[QT];
+#pragma unroll
+      for (int q = 0; q < QT; ++q) js[q] = jp[q] = (q < qt_live) ? 0 : n_tiles;
       uint64_t t_idle = global_ns();
-      for (uint32_t spin = 0; ok && jp < n_tiles;) {
+      auto jp_min = [&]() {
+        int m = jp[0];
+#pragma unroll
+        for (int q = 1; q < QT; ++q) m = min(m, jp[q]);
+        return m;
+      };
+      for (uint32_t spin = 0; ok && jp_min() < n_tiles;) {
         bool did = false;
-        if (js < n_tiles && js <= jp + 1) {
-          const int st = js & 1;
-          if (mbar_test(BAR(kBarConvK + st), (js >> 1) & 1) &&
-              (js < 2 || mbar_test(BAR(kBarODone + st), ((js - 2) >> 1) & 1))) {
+        // every condition of every candidate MMA, tested in one round trip (a test of
+        // a tile that does not exist reads a barrier harmlessly and is ignored)
+        uint32_t tb[8], tp[8];
+#pragma unroll
+        for (int q = 0; q < 2; ++q) {
+          const int qq = q < QT ? q : 0;
+          const int a_ = js[qq], p_ = jp[qq];
+          tb[4 * q + 0] = BAR(C::kBarConvK + a_ % NS);
+          tp[4 * q + 0] = (a_ / NS) & 1;
+          tb[4 * q + 1] = BAR(C::kBarODone + 2 * qq + (a_ & 1));
+          tp[4 * q + 1] = ((a_ - 2) >> 1) & 1;
+          tb[4 * q + 2] = BAR(C::kBarPFull + 2 * qq + (p_ & 1));
+          tp[4 * q + 2] = (p_ >> 1) & 1;
+          tb[4 * q + 3] = BAR(C::kBarConvV + p_ % NS);
+          tp[4 * q + 3] = (p_ / NS) & 1;
+        }
+        const uint32_t ready = mbar_test8(tb, tp);
+#pragma unroll
+        for (int q = 0; q < QT; ++q) {
+          const uint32_t rq = ready >> (4 * q);
+          if (js[q] < n_tiles && js[q] <= jp[q] + 1 && (rq & 1u) && (js[q] < 2 || (rq & 2u))) {
+            const int j = js[q], st = j % NS, sb = j & 1;
             tc_fence_after();
-            const uint32_t aK = smem_u32(sm + kOffStage + st * kStageBytes);
+            const uint32_t aK = smem_u32(sm + C::kOffStage + st * kStageBytes);
+            const uint32_t sQ = smem_u32(sm + q * kQBytes);
 #pragma unroll
             for (int kk = 0; kk < kDH / 16; ++kk) {
               const uint64_t ad = sw128_desc(sQ + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024);
               const uint64_t bd = sw128_desc(aK + (kk / 4) * 8192 + (kk % 4) * 32, 16, 1024);
-              umma_f16(tmem + 64u * st, ad, bd, kIdS, kk > 0 ? 1u : 0u);
+              umma_f16(tmem + 256u * q + 64u * sb, ad, bd, kIdS, kk > 0 ? 1u : 0u);
             }
-            umma_commit(BAR(kBarSFull + st));
-            ++js;
+            umma_commit(BAR(C::kBarSFull + 2 * q + sb));
+            ++js[q];
             did = true;
           }
-        }
-        if (jp < js) {
-          const int st = jp & 1;
-          if (mbar_test(BAR(kBarPFull + st), (jp >> 1) & 1) && mbar_test(BAR(kBarConvV + st), (jp >> 1) & 1)) {
+          if (jp[q] < js[q] && (rq & 4u) && (rq & 8u)) {
+            const int j = jp[q], st = j % NS, sb = j & 1;
             tc_fence_after();
-            const uint32_t aV = smem_u32(sm + kOffStage + st * kStageBytes + kKBytes);
+            const uint32_t aV = smem_u32(sm + C::kOffStage + st * kStageBytes + kKBytes);
 #pragma unroll
             for (int kk = 0; kk < kTcKeys / 16; ++kk) {
               const uint64_t bd = sw128_desc(aV + kk * 2048, 8192, 1024);   // MN-major: dim blocks 8 KiB apart
-              umma_f16_ts(tmem + kTmemO, tmem + 64u * st + 8u * kk, bd, kIdO, (jp > 0 || kk > 0) ? 1u : 0u);
+              umma_f16_ts(tmem + 256u * q + kTmemO, tmem + 256u * q + 64u * sb + 8u * kk, bd, kIdO,
+                          (j > 0 || kk > 0) ? 1u : 0u);
             }
-            umma_commit(BAR(kBarEmpty + st));
-            umma_commit(BAR(kBarODone + st));
-            ++jp;
+            umma_commit(BAR(C::kBarODone + 2 * q + sb));
+            ++jp[q];
+            if (jp_min() > j) umma_commit(BAR(C::kBarEmpty + st));
             did = true;
           }
         }
@@ -431,55 +538,100 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           ok = false;
         }
       }
-      // O is final once the last P V MMA has completed.
-      if (ok && n_tiles > 0 &&
-          !wait_or_abort(BAR(kBarODone + ((n_tiles - 1) & 1)), ((n_tiles - 1) >> 1) & 1, abortp))
-        ok = false;
+      // O is final once the last P V MMAs have completed.
+      for (int q = 0; q < qt_live; ++q)
+        if (ok && n_tiles > 0 &&
+            !wait_or_abort(BAR(C::kBarODone + 2 * q + ((n_tiles - 1) & 1)), ((n_tiles - 1) >> 1) & 1, abortp))
+          ok = false;
     }
-  } else if (warp >= kConvWarp0) {
+  } else if (warp >= C::kConvWarp0) {
     // ---- bf16 -> fp16 conversion (tree keys also rotated) ------------------------------
-    const int ct = tid - kConvWarp0 * 32;
+    const int ct = tid - C::kConvWarp0 * 32;
     for (int j = 0; j < n_tiles; ++j) {
-      const int st = j & 1;
-      uint8_t* tK = sm + kOffStage + st * kStageBytes;
+      const int st = j % NS;
+      uint8_t* tK = sm + C::kOffStage + st * kStageBytes;
       uint8_t* tV = tK + kKBytes;
       const int k_valid = tile_valid(j);
-      int dep[kRotIter];
+      int dep[C::kRotIter];
       if (j >= n_pre) {
 #pragma unroll
-        for (int i = 0; i < kRotIter; ++i) {
-          const int r = rotate_row(i, ct);
+        for (int i = 0; i < C::kRotIter; ++i) {
+          const int r = rotate_row<C::kConvThreads>(i, ct);
           dep[i] = r < k_valid ? __ldg(t.depth + (j - n_pre) * kTcKeys + r) : 0;
         }
       }
-      if (!wait_or_abort(BAR(kBarFull + st), (j >> 1) & 1, abortp)) {
+      if (!wait_or_abort(BAR(C::kBarFull + st), (j / NS) & 1, abortp)) {
         ok = false;
         break;
       }
-      if (j >= n_pre) convert_rotate_tile(tK, k_valid, dep, tab_c, tab_s, ct);
-      else convert_tile(tK, k_valid, ct);
+      if (j >= n_pre) convert_rotate_tile<C::kConvThreads>(tK, k_valid, dep, tab_c, tab_s, ct);
+      else convert_tile<C::kConvThreads>(tK, k_valid, ct);
       fence_proxy_async();
-      mbar_arrive(BAR(kBarConvK + st));
-      convert_tile(tV, k_valid, ct);
+      mbar_arrive(BAR(C::kBarConvK + st));
+      convert_tile<C::kConvThreads>(tV, k_valid, ct);
       fence_proxy_async();
-      mbar_arrive(BAR(kBarConvV + st));
+      mbar_arrive(BAR(C::kBarConvV + st));
+    }
+    // Stage the rotated tree keys and the tree values at cache rows L + u while the
+    // softmax finishes.  Split 0 runs the tree tiles and finishes last, so the other
+    // splits share this work (unit u goes to split 1 + u mod (n_split - 1)).  An item
+    // is one unit's dims [8c, 8c + 8) and [64 + 8c, 64 + 8c + 8), the pairs that the
+    // rotation mixes.
+    const int stagers = ns > 1 ? ns - 1 : 1;
+    const int my_stage = ns > 1 ? s - 1 : 0;
+    if (ok && my_stage >= 0) {
+      const int u_lo = row0 / g, u_hi = (row0 + rows_valid - 1) / g + 1;
+      const int u_first = u_lo + ((my_stage - u_lo % stagers) % stagers + stagers) % stagers;
+      const int n_mine = u_first < u_hi ? (u_hi - u_first + stagers - 1) / stagers : 0;
+      uint16_t* ck = (uint16_t*)a.c.k;
+      uint16_t* cv = (uint16_t*)a.c.v;
+      for (int it = ct; it < n_mine * 8; it += C::kConvThreads) {
+        const int uu = u_first + (it >> 3) * stagers, c = it & 7;
+        const int64_t src = (((int64_t)b * N + uu) * a.Hkv + kvh) * kDH + 8 * c;
+        const uint4 ka = __ldg(reinterpret_cast<const uint4*>(a.k_new + src));
+        const uint4 kb = __ldg(reinterpret_cast<const uint4*>(a.k_new + src + kHalf));
+        const uint4 va = __ldg(reinterpret_cast<const uint4*>(a.v_new + src));
+        const uint4 vb = __ldg(reinterpret_cast<const uint4*>(a.v_new + src + kHalf));
+        const int ti0 = __ldg(t.depth + uu) * kHalf + 8 * c;
+        const int64_t dst = row_off_tc(a.c, b, kvh, Lb + uu) + 8 * c;
+        float x1[8], x2[8];
+        Elem<uint16_t>::unpack(ka, x1);
+        Elem<uint16_t>::unpack(kb, x2);
+        uint32_t y1[4], y2[4];
+#pragma unroll
+        for (int e = 0; e < 4; ++e) {
+          const float c0 = tab_c[ti0 + 2 * e], s0 = tab_s[ti0 + 2 * e];
+          const float c1 = tab_c[ti0 + 2 * e + 1], s1 = tab_s[ti0 + 2 * e + 1];
+          const uint32_t a0 = f32_to_bf16_bits(x1[2 * e] * c0 - x2[2 * e] * s0);
+          const uint32_t a1 = f32_to_bf16_bits(x1[2 * e + 1] * c1 - x2[2 * e + 1] * s1);
+          const uint32_t b0 = f32_to_bf16_bits(x2[2 * e] * c0 + x1[2 * e] * s0);
+          const uint32_t b1 = f32_to_bf16_bits(x2[2 * e + 1] * c1 + x1[2 * e + 1] * s1);
+          y1[e] = a0 | (a1 << 16);
+          y2[e] = b0 | (b1 << 16);
+        }
+        *reinterpret_cast<uint4*>(ck + dst) = make_uint4(y1[0], y1[1], y1[2], y1[3]);
+        *reinterpret_cast<uint4*>(ck + dst + kHalf) = make_uint4(y2[0], y2[1], y2[2], y2[3]);
+        *reinterpret_cast<uint4*>(cv + dst) = va;
+        *reinterpret_cast<uint4*>(cv + dst + kHalf) = vb;
+      }
     }
   } else {
-
-    // ---- softmax warps: thread tid owns query row tid (TMEM lane tid) ----------------
-    // The query tile landed by TMA as bf16, K-major with the 128-byte swizzle (dims
+    // ---- softmax warps: thread tid owns CTA row tid; warp w reads TMEM lanes of
+    //      quadrant w % 4 of query tile w / 4 --------------------------------------------
+    // The query tiles landed by TMA as bf16, K-major with the 128-byte swizzle (dims
     // i and i + 64 of a row at the same position of the two 64-dim blocks).  Rotate
     // each row in place at L + depth, pre-multiply by scale * log2 e, store fp16.
-    if (!__all_sync(0xffffffffu, wait_or_abort(BAR(kBarQFull), 0, abortp))) ok = false;
+    if (!__all_sync(0xffffffffu, wait_or_abort(BAR(C::kBarQFull), 0, abortp))) ok = false;
+    const int tr = tid & (kTcRows - 1);                     // row within its query tile
     if (ok && live) {
       const int ti0 = __ldg(t.depth + u) * kHalf;
-      uint4* q0 = reinterpret_cast<uint4*>(sm + kOffQ + tid * 128);
-      uint4* q1 = reinterpret_cast<uint4*>(sm + kOffQ + 16384 + tid * 128);
+      uint4* q0 = reinterpret_cast<uint4*>(sm + qt * kQBytes + tr * 128);
+      uint4* q1 = reinterpret_cast<uint4*>(sm + qt * kQBytes + 16384 + tr * 128);
       uint4 qa[8], qb[8];
 #pragma unroll
       for (int c = 0; c < 8; ++c) {
-        qa[c] = q0[c ^ (tid & 7)];
-        qb[c] = q1[c ^ (tid & 7)];
+        qa[c] = q0[c ^ (tr & 7)];
+        qb[c] = q1[c ^ (tr & 7)];
       }
 #pragma unroll
       for (int c = 0; c < 8; ++c) {            // dims [8c, 8c+8) and [64+8c, 64+8c+8)
@@ -492,15 +644,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           y1[e] = (x1[e] * cs - x2[e] * sn) * a.scale_log2;
           y2[e] = (x2[e] * cs + x1[e] * sn) * a.scale_log2;
         }
-        q0[c ^ (tid & 7)] = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]),
-                                       pack_half2(y1[4], y1[5]), pack_half2(y1[6], y1[7]));
-        q1[c ^ (tid & 7)] = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]),
-                                       pack_half2(y2[4], y2[5]), pack_half2(y2[6], y2[7]));
+        q0[c ^ (tr & 7)] = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]),
+                                      pack_half2(y1[4], y1[5]), pack_half2(y1[6], y1[7]));
+        q1[c ^ (tr & 7)] = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]),
+                                      pack_half2(y2[4], y2[5]), pack_half2(y2[6], y2[7]));
       }
     }
     fence_proxy_async();
     __syncwarp();
-    if (lane == 0) mbar_arrive(BAR(kBarQReady));
+    if (lane == 0) mbar_arrive(BAR(C::kBarQReady));
 
     // Online softmax.  O accumulates in TMEM across tiles.  The running max m_run is
     // raised only when a tile's max exceeds it by more than 2^8 (log2 units); then O
@@ -508,14 +660,15 @@ __global__ void __launch_bounds__(kTcThreads, 2)
     // accumulators hold exactly enough; the final normalisation uses the same m_run,
     // so the result is the same softmax.
     constexpr float kRescale = 8.f;
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
-    for (int j = 0; ok && j < n_tiles; ++j) {
+    const uint32_t lane_base = ((uint32_t)((warp & 3) * 32) << 16) + 256u * qt;
+    // (a query tile past the last row has no MMAs: its warps skip the loop)
+    for (int j = 0; ok && qt < qt_live && j < n_tiles; ++j) {
       const int sb = j & 1;
       const bool tree_tile = j >= n_pre;
       const int k_valid = tile_valid(j);
       const uint64_t vis = (tree_tile && row_ok) ? __ldg(t.anc + (int64_t)u * t.n_words + (j - n_pre)) : 0ull;
       // wait outcomes are made warp-uniform: the TMEM accesses below are warp-collective
-      if (!__all_sync(0xffffffffu, wait_or_abort(BAR(kBarSFull + sb), (j >> 1) & 1, abortp))) {
+      if (!__all_sync(0xffffffffu, wait_or_abort(BAR(C::kBarSFull + 2 * qt + sb), (j >> 1) & 1, abortp))) {
         ok = false;
         break;
       }
@@ -524,24 +677,20 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         float sv[kTcKeys];
         tmem_ld32(tmem + lane_base + 64u * sb, sv);
         tmem_ld32(tmem + lane_base + 64u * sb + 32, sv + 32);
-        float mxp[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
         if (tree_tile) {
 #pragma unroll
-          for (int c = 0; c < kTcKeys; ++c) {
-            sv[c] = ((vis >> c) & 1ull) ? sv[c] : -INFINITY;
-            mxp[c & 3] = fmaxf(mxp[c & 3], sv[c]);
-          }
+          for (int c = 0; c < kTcKeys; ++c) sv[c] = ((vis >> c) & 1ull) ? sv[c] : -INFINITY;
         } else if (k_valid < kTcKeys) {
 #pragma unroll
-          for (int c = 0; c < kTcKeys; ++c) {
-            sv[c] = c < k_valid ? sv[c] : -INFINITY;
-            mxp[c & 3] = fmaxf(mxp[c & 3], sv[c]);
-          }
-        } else {
-#pragma unroll
-          for (int c = 0; c < kTcKeys; ++c) mxp[c & 3] = fmaxf(mxp[c & 3], sv[c]);
+          for (int c = 0; c < kTcKeys; ++c) sv[c] = c < k_valid ? sv[c] : -INFINITY;
         }
-        const float mx = fmaxf(fmaxf(mxp[0], mxp[1]), fmaxf(mxp[2], mxp[3]));
+        float mxp[2] = {-INFINITY, -INFINITY};
+#pragma unroll
+        for (int c = 0; c < kTcKeys; c += 4) {
+          mxp[0] = fmax3(mxp[0], sv[c], sv[c + 1]);
+          mxp[1] = fmax3(mxp[1], sv[c + 2], sv[c + 3]);
+        }
+        const float mx = fmaxf(mxp[0], mxp[1]);
         // The TMEM accesses of a rescale are warp-collective: the warp rescales when any
         // of its rows needs it, the other rows scale by 1.  O must hold P V of tile j - 1
         // first (a row that needs a rescale has seen an earlier tile, so j >= 1).
@@ -550,7 +699,7 @@ __global__ void __launch_bounds__(kTcThreads, 2)
         if (first) m_run = mx;                           // O holds nothing yet for this row
         if (__any_sync(0xffffffffu, need)) {
           if (!__all_sync(0xffffffffu,
-                          wait_or_abort(BAR(kBarODone + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abortp))) {
+                          wait_or_abort(BAR(C::kBarODone + 2 * qt + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abortp))) {
             ok = false;
             break;
           }
@@ -568,68 +717,27 @@ __global__ void __launch_bounds__(kTcThreads, 2)
           if (need) m_run = mx;
         }
         const float mref = (m_run == -INFINITY) ? 0.f : m_run;   // a fully masked row keeps P = 0
-        float ps[4] = {0.f, 0.f, 0.f, 0.f};
+        // pairs of keys through the packed fp32x2 adds; four partial sums
+        const float2 nm = make_float2(-mref, -mref);
+        float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
         float pk[kTcKeys / 2];                   // P as fp16 pairs, key 2i in the low half
 #pragma unroll
         for (int i = 0; i < kTcKeys / 2; ++i) {
-          const float p0 = fast_exp2(sv[2 * i] - mref), p1 = fast_exp2(sv[2 * i + 1] - mref);
-          ps[(2 * i) & 3] += p0;
-          ps[(2 * i + 1) & 3] += p1;
-          pk[i] = __uint_as_float(pack_half2(p0, p1));
+          const float2 d = __fadd2_rn(make_float2(sv[2 * i], sv[2 * i + 1]), nm);
+          const float2 pp = make_float2(fast_exp2(d.x), fast_exp2(d.y));
+          ps[i & 3] = __fadd2_rn(ps[i & 3], pp);
+          pk[i] = __uint_as_float(pack_half2(pp.x, pp.y));
         }
-        l_run += (ps[0] + ps[1]) + (ps[2] + ps[3]);
+        const float2 s01 = __fadd2_rn(ps[0], ps[1]), s23 = __fadd2_rn(ps[2], ps[3]);
+        const float2 s4 = __fadd2_rn(s01, s23);
+        l_run += s4.x + s4.y;
         tmem_st32(tmem + lane_base + 64u * sb, pk);
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(kBarPFull + sb));
-    }
-
-    // Stage rotated tree keys and tree values at cache rows L + u.  Split 0 runs the
-    // tree tiles and is the last to finish, so the other splits share this work
-    // (row u goes to split 1 + u mod (n_split - 1)) once their own tiles are done.
-    const int stagers = a.n_split > 1 ? a.n_split - 1 : 1;
-    const int my_stage = a.n_split > 1 ? s - 1 : 0;
-    if (ok && row_ok && (R % g) == 0 && my_stage >= 0 && u % stagers == my_stage) {
-      const int64_t src = (((int64_t)b * N + u) * a.Hkv + kvh) * kDH;
-      const int64_t dst = row_off_tc(a.c, b, kvh, Lb + u);
-      uint16_t* ck = (uint16_t*)a.c.k;
-      uint16_t* cv = (uint16_t*)a.c.v;
-      const int ti0 = __ldg(t.depth + u) * kHalf;
-      uint4 ka[8], kb[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        ka[c] = __ldg(reinterpret_cast<const uint4*>(a.k_new + src + 8 * c));
-        kb[c] = __ldg(reinterpret_cast<const uint4*>(a.k_new + src + kHalf + 8 * c));
-      }
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        float x1[8], x2[8];
-        Elem<uint16_t>::unpack(ka[c], x1);
-        Elem<uint16_t>::unpack(kb[c], x2);
-        uint32_t y1[4], y2[4];
-#pragma unroll
-        for (int e = 0; e < 4; ++e) {
-          const float c0 = tab_c[ti0 + 8 * c + 2 * e], s0 = tab_s[ti0 + 8 * c + 2 * e];
-          const float c1 = tab_c[ti0 + 8 * c + 2 * e + 1], s1 = tab_s[ti0 + 8 * c + 2 * e + 1];
-          const uint32_t a0 = f32_to_bf16_bits(x1[2 * e] * c0 - x2[2 * e] * s0);
-          const uint32_t a1 = f32_to_bf16_bits(x1[2 * e + 1] * c1 - x2[2 * e + 1] * s1);
-          const uint32_t b0 = f32_to_bf16_bits(x2[2 * e] * c0 + x1[2 * e] * s0);
-          const uint32_t b1 = f32_to_bf16_bits(x2[2 * e + 1] * c1 + x1[2 * e + 1] * s1);
-          y1[e] = a0 | (a1 << 16);
-          y2[e] = b0 | (b1 << 16);
-        }
-        *reinterpret_cast<uint4*>(ck + dst + 8 * c) = make_uint4(y1[0], y1[1], y1[2], y1[3]);
-        *reinterpret_cast<uint4*>(ck + dst + kHalf + 8 * c) = make_uint4(y2[0], y2[1], y2[2], y2[3]);
-      }
-      uint4 vv[16];
-#pragma unroll
-      for (int c = 0; c < 16; ++c) vv[c] = __ldg(reinterpret_cast<const uint4*>(a.v_new + src + 8 * c));
-#pragma unroll
-      for (int c = 0; c < 16; ++c) *reinterpret_cast<uint4*>(cv + dst + 8 * c) = vv[c];
+      if (lane == 0) mbar_arrive(BAR(C::kBarPFull + 2 * qt + sb));
     }
   }
-
 
   // ---- join ------------------------------------------------------------------------
   if (!ok) {
@@ -640,17 +748,16 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   const bool failed = *abortp != 0;
   if (failed) {
     // Drain (bounded) what this CTA may still have in flight before its shared memory
-    // and TMEM are reused or released: the last copy into each stage, and all MMAs.
-    if (warp == kProdWarp && lane == 0) {
-      mbar_wait(BAR(kBarQFull), 0, 100000000ull);
-      for (int st = 0; st < kStages; ++st) {
-        const int jl = (n_issued - 1 - st) >= 0 ? ((n_issued - 1 - st) & ~1) + st : -1;
-        if (jl >= 0) mbar_wait(BAR(kBarFull + st), (jl >> 1) & 1, 100000000ull);
-      }
+    // and TMEM are reused or released: the query copies, the last copy into each stage,
+    // and all MMAs.
+    if (warp == C::kProdWarp && lane == 0) {
+      mbar_wait(BAR(C::kBarQFull), 0, 100000000ull);
+      for (int j = n_issued - NS; j < n_issued; ++j)
+        if (j >= 0) mbar_wait(BAR(C::kBarFull + j % NS), (j / NS) & 1, 100000000ull);
     }
-    if (warp == kMmaWarp && lane == 0) {
-      umma_commit(BAR(kBarDrain));
-      mbar_wait(BAR(kBarDrain), 0, 100000000ull);
+    if (warp == C::kMmaWarp && lane == 0) {
+      umma_commit(BAR(C::kBarDrain));
+      mbar_wait(BAR(C::kBarDrain), 0, 100000000ull);
     }
     __syncthreads();
   }
@@ -662,10 +769,10 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   // partials through distributed shared memory.  A second cluster barrier keeps every
   // CTA's partials alive until all readers are done.  Every CTA reaches both barriers
   // on every path.
-  float4* po = reinterpret_cast<float4*>(sm);                  // [128 rows][32] float4, swizzled
-  float2* pml = reinterpret_cast<float2*>(sm + kTcRows * kDH * 4);   // [128] (m, l)
+  float4* po = reinterpret_cast<float4*>(sm);                  // [rows][32] float4, swizzled
+  float2* pml = reinterpret_cast<float2*>(sm + C::kRows * kDH * 4);   // [rows] (m, l)
   if (live) {
-    const uint32_t lane_base = (uint32_t)(warp * 32) << 16;
+    const uint32_t lane_base = ((uint32_t)((warp & 3) * 32) << 16) + 256u * qt;
     if (!failed && n_tiles > 0) {
       tc_fence_after();
 #pragma unroll
@@ -686,47 +793,59 @@ __global__ void __launch_bounds__(kTcThreads, 2)
   }
   tc_fence_before();
   __syncthreads();
-  if (warp == kMmaWarp) {
+  if (warp == C::kMmaWarp) {
     tc_fence_after();
-    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(kTmemCols) : "memory");
+    asm volatile("tcgen05.dealloc.cta_group::1.sync.aligned.b32 %0, %1;" ::"r"(tmem), "r"(C::kTmemCols) : "memory");
   }
   cluster_sync_all();
 
   const uint32_t po_base = smem_u32(po), pml_base = smem_u32(pml);
-  constexpr int kWarps = kTcThreads / 32;
-  for (int r = s + warp * ns; r < rows_valid; r += kWarps * ns) {
-    const int Rr = mt * kTcRows + r;
-    // (m, l) of split `lane` and this lane's float4 of every split's O, all requested
-    // before any is used: one round trip through distributed shared memory.
-    const uint32_t off = po_base + (uint32_t)(r * 32 + (lane ^ (r & 31))) * 16;
-    float2 ml = make_float2(-INFINITY, 0.f);
-    if (lane < ns) ml = ld_dsmem_f2(dsmem_addr(pml_base + r * 8, lane));
-    float4 v[kMaxClusterSplits];
+  constexpr int kWarps = C::kThreads / 32;
+  constexpr int kPair = 2;                   // rows per warp per pass: their loads overlap
+  const int stride = kWarps * ns;
+  for (int r0 = s + warp * ns; r0 < rows_valid; r0 += kPair * stride) {
+    // (m, l) of split `lane` and this lane's float4 of every split's O, for both rows,
+    // all requested before any is used: one round trip through distributed shared memory.
+    float2 ml[kPair];
+    float4 v[kPair][kMaxClusterSplits];
 #pragma unroll
-    for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
-      v[s2] = s2 < ns ? ld_dsmem_f4(dsmem_addr(off, s2)) : make_float4(0.f, 0.f, 0.f, 0.f);
-    float Mx = ml.x;
+    for (int h = 0; h < kPair; ++h) {
+      const int r = r0 + h * stride;
+      const bool in = r < rows_valid;
+      const uint32_t off = po_base + (uint32_t)(r * 32 + (lane ^ (r & 31))) * 16;
+      ml[h] = (in && lane < ns) ? ld_dsmem_f2(dsmem_addr(pml_base + r * 8, lane)) : make_float2(-INFINITY, 0.f);
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
-    const float w_l = (ml.x == -INFINITY) ? 0.f : fast_exp2(ml.x - Mx);
-    float l = w_l * ml.y;
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
-    float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll
-    for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
-      const float w = __shfl_sync(0xffffffffu, w_l, s2);
-      acc.x = fmaf(v[s2].x, w, acc.x);
-      acc.y = fmaf(v[s2].y, w, acc.y);
-      acc.z = fmaf(v[s2].z, w, acc.z);
-      acc.w = fmaf(v[s2].w, w, acc.w);
+      for (int s2 = 0; s2 < kMaxClusterSplits; ++s2)
+        v[h][s2] = (in && s2 < ns) ? ld_dsmem_f4(dsmem_addr(off, s2)) : make_float4(0.f, 0.f, 0.f, 0.f);
     }
-    const float il = 1.f / l;
-    const int ur = Rr / g, hr = kvh * g + Rr % g;
-    if (!failed) {
-      reinterpret_cast<float4*>(a.out + (((int64_t)b * N + ur) * a.Hq + hr) * kDH)[lane] =
-          make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
-      if (a.lse && lane == 0) a.lse[((int64_t)b * N + ur) * a.Hq + hr] = (Mx + log2f(l)) * kLn2;
+#pragma unroll
+    for (int h = 0; h < kPair; ++h) {
+      const int r = r0 + h * stride;
+      if (r >= rows_valid) break;                   // warp-uniform
+      float Mx = ml[h].x;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) Mx = fmaxf(Mx, __shfl_xor_sync(0xffffffffu, Mx, o));
+      const float w_l = (ml[h].x == -INFINITY) ? 0.f : fast_exp2(ml[h].x - Mx);
+      float l = w_l * ml[h].y;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) l += __shfl_xor_sync(0xffffffffu, l, o);
+      float4 acc = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+      for (int s2 = 0; s2 < kMaxClusterSplits; ++s2) {
+        const float w = __shfl_sync(0xffffffffu, w_l, s2);
+        acc.x = fmaf(v[h][s2].x, w, acc.x);
+        acc.y = fmaf(v[h][s2].y, w, acc.y);
+        acc.z = fmaf(v[h][s2].z, w, acc.z);
+        acc.w = fmaf(v[h][s2].w, w, acc.w);
+      }
+      const float il = 1.f / l;
+      const int Rr = row0 + r;
+      const int ur = Rr / g, hr = kvh * g + Rr % g;
+      if (!failed) {
+        reinterpret_cast<float4*>(a.out + (((int64_t)b * N + ur) * a.Hq + hr) * kDH)[lane] =
+            make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
+        if (a.lse && lane == 0) a.lse[((int64_t)b * N + ur) * a.Hq + hr] = (Mx + log2f(l)) * kLn2;
+      }
     }
   }
   cluster_sync_all();
@@ -771,8 +890,10 @@ bool encode_rows_map(CUtensorMap* map, const void* base, int B, int N, int H, in
   return r == CUDA_SUCCESS;
 }
 
+template <int QT, int NS>
 size_t tc_smem_bytes(int D) {
-  return 1024 + kOffTable + (size_t)2 * (D + 1) * kHalf * sizeof(float) + 8 + kNumBars * 8;
+  using C = TcCfg<QT, NS>;
+  return 1024 + C::kOffTable + (size_t)2 * (D + 1) * kHalf * sizeof(float) + 8 + C::kNumBars * 8;
 }
 
 }  // namespace
@@ -799,19 +920,35 @@ bool attn_tc_supported(const medusa_tree_t& t, int Hq, const medusa_kv_t& c) {
          kTcRows % g == 0 && encode_fn() != nullptr;
 }
 
-// Split choice: enough CTAs to fill the SMs two per SM, in whole waves where possible,
-// with at most kMaxClusterSplits splits (one cluster) per unit and at least rows/16
-// tiles per split.  The tree tiles count as work of split 0, which takes that many
-// fewer prefix tiles, so that the splits end together.
+// Kernel shape and split choice.  With four or more query tiles per unit, one CTA
+// takes two of them (QT = 2) so that every K/V tile is copied and converted once for
+// 256 rows, with three stages in flight (one CTA per SM: 192 KB of shared memory).
+// Fewer query tiles run two CTAs per SM with two stages each, which overlaps one CTA's
+// prologue and merge with the other's main loop.  The splits: enough CTAs to fill the
+// SM slots, in whole waves where possible, with at most kMaxClusterSplits splits (one
+// cluster) per unit and at least rows/16 tiles per split.  The tree tiles count as
+// work of split 0, which takes that many fewer prefix tiles, so that the splits end
+// together.  MEDUSA_ATTN_TC_SHAPE="QT,NS" (one of 1,2 / 1,4 / 2,3) overrides the shape.
 void attn_tc_plan(AttnPlan& p) {
-  p.mt_rows = kTcRows;
-  p.key_tile = kTcKeys;
   const int M = p.N * p.g;
-  p.n_mt = (M + kTcRows - 1) / kTcRows;
+  const int n_tiles_q = (M + kTcRows - 1) / kTcRows;
+  int qt = n_tiles_q >= 4 ? 2 : 1, stages = qt == 2 ? 3 : 2;
+  if (const char* e = std::getenv("MEDUSA_ATTN_TC_SHAPE")) {
+    int a = 0, b = 0;
+    if (std::sscanf(e, "%d,%d", &a, &b) == 2 && ((a == 1 && (b == 2 || b == 4)) || (a == 2 && b == 3))) {
+      qt = a;
+      stages = b;
+    }
+  }
+  p.qt = qt;
+  p.stages = stages;
+  p.mt_rows = kTcRows * qt;
+  p.key_tile = kTcKeys;
+  p.n_mt = (M + p.mt_rows - 1) / p.mt_rows;
   const int units = p.B * p.Hkv * p.n_mt;
   int sms = 148, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const double slots = 2.0 * sms;
+  const double slots = (qt == 1 && stages == 2 ? 2.0 : 1.0) * sms;
   const int tiles_unit = (p.max_prefix + kTcKeys - 1) / kTcKeys;
   const int n_tree = (p.N + kTcKeys - 1) / kTcKeys;
   const int rows = M < kTcRows ? M : kTcRows;
@@ -839,6 +976,30 @@ void attn_tc_plan(AttnPlan& p) {
   p.chunk = chunk_tiles * kTcKeys;
   p.n_split = 1 + (rest + chunk_tiles - 1) / chunk_tiles;
 }
+
+namespace {
+
+template <bool PAGED, int QT, int NS>
+cudaError_t launch_shape(cudaLaunchConfig_t& cfg, int D, const CUtensorMap& mk, const CUtensorMap& mv,
+                         const CUtensorMap& mkn, const CUtensorMap& mvn, const CUtensorMap& mq, const TcArgs& a) {
+  const size_t smem = tc_smem_bytes<QT, NS>(D);
+  cfg.blockDim = dim3(TcCfg<QT, NS>::kThreads);
+  cfg.dynamicSmemBytes = smem;
+  cudaError_t e = cudaFuncSetAttribute(attn_tc_kernel<PAGED, QT, NS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)smem);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, attn_tc_kernel<PAGED, QT, NS>, mk, mv, mkn, mvn, mq, a);
+}
+
+template <bool PAGED>
+cudaError_t launch_paged(const AttnPlan& p, cudaLaunchConfig_t& cfg, const CUtensorMap& mk, const CUtensorMap& mv,
+                         const CUtensorMap& mkn, const CUtensorMap& mvn, const CUtensorMap& mq, const TcArgs& a) {
+  if (p.qt == 2) return launch_shape<PAGED, 2, 3>(cfg, p.D, mk, mv, mkn, mvn, mq, a);
+  if (p.stages == 4) return launch_shape<PAGED, 1, 4>(cfg, p.D, mk, mv, mkn, mvn, mq, a);
+  return launch_shape<PAGED, 1, 2>(cfg, p.D, mk, mv, mkn, mvn, mq, a);
+}
+
+}  // namespace
 
 cudaError_t launch_attn_tc(const AttnPlan& p, const medusa_tree_t& t, const void* q,
                            const void* k_new, const void* v_new, const medusa_kv_t& c,
@@ -874,11 +1035,8 @@ cudaError_t launch_attn_tc(const AttnPlan& p, const medusa_tree_t& t, const void
     a.th_hi[i] = th_hi[i];
     a.th_lo[i] = th_lo[i];
   }
-  const size_t smem = tc_smem_bytes(p.D);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_mt, p.n_split, p.B * p.Hkv);
-  cfg.blockDim = dim3(kTcThreads);
-  cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -887,16 +1045,8 @@ cudaError_t launch_attn_tc(const AttnPlan& p, const medusa_tree_t& t, const void
   attr[0].val.clusterDim.z = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  cudaError_t e;
-  if (c.page_size == 0) {
-    e = cudaFuncSetAttribute(attn_tc_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<false>, mk, mv, mkn, mvn, mq, a);
-  } else {
-    e = cudaFuncSetAttribute(attn_tc_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-    if (e != cudaSuccess) return e;
-    e = cudaLaunchKernelEx(&cfg, attn_tc_kernel<true>, mk, mv, mkn, mvn, mq, a);
-  }
+  const cudaError_t e = c.page_size == 0 ? launch_paged<false>(p, cfg, mk, mv, mkn, mvn, mq, a)
+                                         : launch_paged<true>(p, cfg, mk, mv, mkn, mvn, mq, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -53,6 +53,7 @@ struct AttnPlan {
   int n_split;           // CTAs along the prefix per (b, kv head, m tile)
   int chunk;             // prefix keys per split (multiple of key_tile)
   int first;             // prefix keys of split 0 (tensor-core path; split 0 also runs the tree rows)
+  int qt, stages;        // tensor-core path: 128-row query tiles per CTA, K/V stages in the ring
   size_t off_counter, off_part_o, off_part_ml, off_tmap, bytes;
 };
 // Bytes reserved for split-KV ticket counters at the start of the attention workspace.
