@@ -46,15 +46,12 @@ namespace medusa {
 namespace {
 
 constexpr int kTcRows = 128;        // query rows per CTA
-constexpr int kTcKeys = 64;         // keys per tile
+constexpr int kTcKeys = 64;         // rows of a K/V copy box (and keys per tile with one query tile)
 constexpr int kDH = 128;
 constexpr int kHalf = kDH / 2;
 constexpr uint32_t kTmemO = 128;   // per query tile: S buffers in columns [0, 64), [64, 128); O in [128, 256)
 
 constexpr int kQBytes = kTcRows * kDH * 2;       // 2 K-blocks of [128 rows x 128 B]
-constexpr int kKBytes = kTcKeys * kDH * 2;       // 2 K-blocks of [64 rows x 128 B]
-constexpr int kVBytes = kTcKeys * kDH * 2;       // 2 MN-blocks of [64 keys x 128 B]
-constexpr int kStageBytes = kKBytes + kVBytes;
 
 constexpr int kErrTimeout = MEDUSA_ETIMEOUT;
 constexpr int kMaxClusterSplits = 8;   // splits of a unit form one portable cluster
@@ -167,42 +164,42 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
   }
 }
 
-// Re-encode one K or V tile (2 blocks of [64 rows x 128 B], bf16) to fp16 in place;
+// Re-encode one K or V tile (2 blocks of [KT rows x 128 B], bf16) to fp16 in place;
 // rows of keys >= k_valid become zero.  Thread ct of the kConvThreads converter
 // threads; all its loads are issued before the first store, so their latencies overlap.
-template <int kConvThreads>
+template <int kConvThreads, int KT>
 __device__ __forceinline__ void convert_tile(uint8_t* tile, int k_valid, int ct) {
   uint4* p = reinterpret_cast<uint4*>(tile);
-  constexpr int kIter = (kKBytes / 16) / kConvThreads;
+  constexpr int kIter = (KT * kDH * 2 / 16) / kConvThreads;
   uint4 v[kIter];
 #pragma unroll
   for (int i = 0; i < kIter; ++i) v[i] = p[i * kConvThreads + ct];
 #pragma unroll
   for (int i = 0; i < kIter; ++i) {
     const int idx = i * kConvThreads + ct;
-    const int row = (idx % (kKBytes / 32)) / 8;      // 16-byte chunks: 8 per row, 512 per block
+    const int row = (idx % (KT * 8)) / 8;             // 16-byte chunks: 8 per row, 8 KT per block
     p[idx] = row < k_valid ? bf16x8_to_f16x8(v[i]) : make_uint4(0, 0, 0, 0);
   }
 }
 
-// Tree-row key tile: bf16 -> RoPE at L + depth[v] (fp32) -> fp16, in place.  Row r of
-// the tile is tree row v0 + r; dims i and i + 64 sit in the two blocks at the same
+// Tree-row key tile of KT rows: bf16 -> RoPE at L + depth[v] (fp32) -> fp16, in place.
+// Row r of the tile is tree row v0 + r; dims i and i + 64 sit in the two blocks at the same
 // swizzled position.  Rows >= n_valid become zero.  `dep[i]` is the depth of the row
 // that iteration i of thread ct touches (loaded before the tile landed).
 template <int kConvThreads>
 __device__ __forceinline__ int rotate_row(int i, int ct) { return (i * kConvThreads + ct) >> 3; }
 
-template <int kConvThreads>
+template <int kConvThreads, int KT>
 __device__ __forceinline__ void convert_rotate_tile(uint8_t* tile, int n_valid, const int* dep,
                                                     const float* tab_c, const float* tab_s, int ct) {
-  constexpr int kRotIter = (kTcKeys * 8) / kConvThreads;
+  constexpr int kRotIter = (KT * 8) / kConvThreads;
 #pragma unroll
   for (int i = 0; i < kRotIter; ++i) {
     const int idx = i * kConvThreads + ct;
     const int row = idx >> 3, c = idx & 7;
     const int off = row * 128 + ((c ^ (row & 7)) * 16);
     uint4* p0 = reinterpret_cast<uint4*>(tile + off);
-    uint4* p1 = reinterpret_cast<uint4*>(tile + 8192 + off);
+    uint4* p1 = reinterpret_cast<uint4*>(tile + KT * 128 + off);
     if (row < n_valid) {
       float x1[8], x2[8];
       Elem<uint16_t>::unpack(*p0, x1);
@@ -227,32 +224,48 @@ __device__ __forceinline__ void convert_rotate_tile(uint8_t* tile, int n_valid, 
 }
 
 // Kernel configuration: QT query tiles of 128 rows per CTA share every K/V tile (one
-// conversion, one copy); NS stages of 64 keys in the ring.
+// copy, one conversion); NS stages of KT keys in the ring.
+//  QT = 1: KT = 64, two S buffers per query tile (S of the next tile is computed while
+//          the softmax works on this one); two CTAs per SM.
+//  QT = 2: KT = 128, one S buffer per query tile; the two tiles alternate on the tensor
+//          cores (S and P V of one tile while the softmax works on the other).  128-key
+//          tiles make the S MMAs 128 wide, which the tensor cores run about twice as
+//          efficiently per key as 64-wide ones.  One CTA per SM.
 template <int QT, int NS>
 struct TcCfg {
+  static constexpr int kKT = 64 * QT;                // keys per tile
+  static constexpr int kSB = QT == 1 ? 2 : 1;        // S buffers per query tile
+  static constexpr int kKBytes = kKT * kDH * 2;      // one K (or V) tile: 2 dim blocks of [KT rows x 128 B]
+  static constexpr int kStageBytes = 2 * kKBytes;
   static constexpr int kSoftWarps = 4 * QT;          // warps [0, 4 QT): one thread per query row
   static constexpr int kProdWarp = 4 * QT;           // TMA producer
   static constexpr int kMmaWarp = 4 * QT + 1;        // TMEM owner and MMA issuer
   static constexpr int kConvWarp0 = 4 * QT + 2;      // converter warps: one per SM sub-partition
   static constexpr int kConvWarps = QT == 2 ? 4 : 2; // (two when two CTAs share an SM)
   static constexpr int kConvThreads = 32 * kConvWarps;
-  static constexpr int kRotIter = (kTcKeys * 8) / kConvThreads;
+  static constexpr int kRotIter = (kKT * 8) / kConvThreads;
   static constexpr int kThreads = 32 * (4 * QT + 2 + kConvWarps);
   static constexpr int kRows = kTcRows * QT;
-  static constexpr uint32_t kTmemCols = 256u * QT;   // per query tile: S0 [0,64), S1 [64,128), O [128,256)
-  static constexpr int kOffStage = kQBytes * QT;
-  static constexpr int kOffTable = kOffStage + NS * kStageBytes;   // rope cos/sin, then barriers
+  static constexpr uint32_t kTmemCols = 256u * QT;   // per query tile: S [0, 128) (two 64-wide or one 128-wide), O [128, 256)
+  static constexpr int kOffK = kQBytes * QT;                    // K ring: NS slots of kKBytes
+  static constexpr int kOffV = kOffK + NS * kKBytes;            // V ring: NS slots of kKBytes
+  static constexpr int kOffTable = kOffV + NS * kKBytes;        // rope cos/sin, then barriers
+  static constexpr int kPages = kKT / 16;            // pages of a paged tile
   // barrier slots
-  static constexpr int kBarFull = 0;                 // [NS] stage landed (TMA transaction bytes)
-  static constexpr int kBarConvK = NS;               // [NS] K tile converted (64 converter arrivals)
-  static constexpr int kBarConvV = 2 * NS;           // [NS] V tile converted
-  static constexpr int kBarEmpty = 3 * NS;           // [NS] stage consumed by the P V MMAs (tcgen05.commit)
-  static constexpr int kBarSFull = 4 * NS;           // [QT][2] S buffers written (tcgen05.commit)
-  static constexpr int kBarPFull = 4 * NS + 2 * QT;  // [QT][2] P written over S (one arrival per softmax warp)
-  static constexpr int kBarODone = 4 * NS + 4 * QT;  // [QT][2] P V MMAs of (q, j) complete, slot j & 1
-  static constexpr int kBarQReady = 4 * NS + 6 * QT; // queries staged (one arrival per softmax warp)
-  static constexpr int kBarDrain = kBarQReady + 1;   // final commit on the error path
-  static constexpr int kBarQFull = kBarQReady + 2;   // query tiles landed
+  // K and V have rings of their own: a K slot is released when the S MMAs that read it
+  // complete, well before the P V MMAs release the V slot of the same tile.
+  static constexpr int kBarFullK = 0;                // [NS] K slot landed (TMA transaction bytes)
+  static constexpr int kBarFullV = NS;               // [NS] V slot landed
+  static constexpr int kBarConvK = 2 * NS;           // [NS] K tile converted (one arrival per converter thread)
+  static constexpr int kBarConvV = 3 * NS;           // [NS] V tile converted
+  static constexpr int kBarEmptyK = 4 * NS;          // [NS] K slot consumed by the S MMAs (tcgen05.commit)
+  static constexpr int kBarEmptyV = 5 * NS;          // [NS] V slot consumed by the P V MMAs
+  static constexpr int kBarSFull = 6 * NS;                   // [QT][kSB] S buffer written (tcgen05.commit)
+  static constexpr int kBarPFull = kBarSFull + QT * kSB;     // [QT][kSB] P written over S (one arrival per softmax warp)
+  static constexpr int kBarODone = kBarPFull + QT * kSB;     // [QT][kSB] P V MMAs complete
+  static constexpr int kBarQReady = kBarODone + QT * kSB;    // queries staged (one arrival per softmax warp)
+  static constexpr int kBarDrain = kBarQReady + 1;           // final commit on the error path
+  static constexpr int kBarQFull = kBarQReady + 2;           // query tiles landed
   static constexpr int kNumBars = kBarQReady + 3;
   // the merge reuses the query and stage buffers: [rows][32] float4 O, then (m, l)
   static_assert(QT * kQBytes + NS * kStageBytes >= kRows * (kDH * 4 + 8), "merge buffers do not fit");
@@ -307,70 +320,76 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
   const uint32_t bar0 = smem_u32(bars);
   auto BAR = [&](int i) -> uint32_t { return bar0 + 8u * (uint32_t)i; };
 
-  // Keys of this split.  Each sequence spreads its own ceil(L / 64) prefix tiles over
+  // Keys of this split.  Each sequence spreads its own ceil(L / KT) prefix tiles over
   // the n_split splits, so a short sequence does not leave splits idle while one of
   // them streams everything.  The tree tiles count as work of split 0, which takes
   // that many fewer prefix tiles.
+  constexpr int KT = C::kKT;
   const int ns = a.n_split;
-  const int tiles_b = (Lb + kTcKeys - 1) / kTcKeys;
-  const int n_tree_all = (N + kTcKeys - 1) / kTcKeys;
+  const int tiles_b = (Lb + KT - 1) / KT;
+  const int n_tree_all = (N + KT - 1) / KT;
   const int first_t = ns > 1 ? min(max((tiles_b + n_tree_all + ns - 1) / ns - n_tree_all, 0), tiles_b) : tiles_b;
   const int chunk_t = ns > 1 ? (tiles_b - first_t + ns - 2) / (ns - 1) : 0;
   const int t_begin = s == 0 ? 0 : min(tiles_b, first_t + (s - 1) * chunk_t);
   const int t_end = s == 0 ? first_t : min(tiles_b, first_t + s * chunk_t);
-  const int k_begin = t_begin * kTcKeys;
-  const int k_end = min(Lb, t_end * kTcKeys);
-  // Tiles: the split's prefix keys, then (split 0 only) the N tree rows, 64 per tile.
-  // A tree tile t covers rows [64t, 64t + 64), exactly ancestor-mask word t.
-  const int n_pre = k_end > k_begin ? (k_end - k_begin + kTcKeys - 1) / kTcKeys : 0;
-  const int n_tree = (s == 0) ? (N + kTcKeys - 1) / kTcKeys : 0;
+  const int k_begin = t_begin * KT;
+  const int k_end = min(Lb, t_end * KT);
+  // Tiles: the split's prefix keys, then (split 0 only) the N tree rows, KT per tile.
+  // A tree tile t covers rows [KT t, KT t + KT), exactly ancestor-mask words
+  // (KT / 64) t .. (KT / 64) t + KT / 64 - 1.
+  const int n_pre = k_end > k_begin ? (k_end - k_begin + KT - 1) / KT : 0;
+  const int n_tree = (s == 0) ? (N + KT - 1) / KT : 0;
   const int n_tiles = n_pre + n_tree;
   auto tile_valid = [&](int j) -> int {        // rows of tile j before the end of its range
-    return j >= n_pre ? N - (j - n_pre) * kTcKeys : k_end - (k_begin + j * kTcKeys);
+    return j >= n_pre ? N - (j - n_pre) * KT : k_end - (k_begin + j * KT);
   };
   // Pages of a paged prefix tile j (block-table entries), loaded ahead of its copy.
   auto load_pages = [&](int j, int* pg) {
     if (PAGED && j < n_pre) {
-      const int k0 = k_begin + j * kTcKeys;
-      const int np = (min(kTcKeys, k_end - k0) + 15) / 16;
+      const int k0 = k_begin + j * KT;
+      const int np = (min(KT, k_end - k0) + 15) / 16;
       const int32_t* bt = a.c.block_table + (int64_t)b * a.c.max_blocks + k0 / 16;
 #pragma unroll
-      for (int p = 0; p < 4; ++p) pg[p] = p < np ? __ldg(bt + p) : 0;
+      for (int p = 0; p < C::kPages; ++p) pg[p] = p < np ? __ldg(bt + p) : 0;
     } else {
 #pragma unroll
-      for (int p = 0; p < 4; ++p) pg[p] = 0;
+      for (int p = 0; p < C::kPages; ++p) pg[p] = 0;
     }
   };
-  // TMA of tile j into stage j % NS (its full barrier counts the bytes).
-  auto issue_tile = [&](int j, const int* page) {
+  // TMA of K (kv = 0) or V (kv = 1) of tile j into slot j % NS of its ring (the slot's
+  // full barrier counts the bytes).  A slot holds 2 dim blocks (dims [0, 64), [64, 128))
+  // of [KT rows x 128 B]; a copy box is 64 rows (a page of 16 rows when paged).
+  auto issue_kv = [&](int kv, int j, const int* page) {
     const int st = j % NS;
-    const uint32_t bar = BAR(C::kBarFull + st);
-    const uint32_t dK = smem_u32(sm + C::kOffStage + st * kStageBytes);
-    const uint32_t dV = dK + kKBytes;
-    const int k0 = k_begin + j * kTcKeys;
+    const uint32_t bar = BAR((kv ? C::kBarFullV : C::kBarFullK) + st);
+    const uint32_t dst = smem_u32(sm + (kv ? C::kOffV : C::kOffK) + st * C::kKBytes);
+    const CUtensorMap* tm = kv ? &tmV : &tmK;
+    const CUtensorMap* tmn = kv ? &tmVn : &tmKn;
+    constexpr uint32_t kBlk = KT * 128;         // bytes of one dim block
+    const int k0 = k_begin + j * KT;
     if (j >= n_pre) {
-      const int v0 = (j - n_pre) * kTcKeys;
-      mbar_expect_tx(bar, 4 * 8192);
-      tma_load_4d(dK, &tmKn, 0, kvh, v0, b, bar);
-      tma_load_4d(dK + 8192, &tmKn, 64, kvh, v0, b, bar);
-      tma_load_4d(dV, &tmVn, 0, kvh, v0, b, bar);
-      tma_load_4d(dV + 8192, &tmVn, 64, kvh, v0, b, bar);
-    } else if (!PAGED) {
-      mbar_expect_tx(bar, 4 * 8192);
-      tma_load_4d(dK, &tmK, 0, k0, kvh, b, bar);
-      tma_load_4d(dK + 8192, &tmK, 64, k0, kvh, b, bar);
-      tma_load_4d(dV, &tmV, 0, k0, kvh, b, bar);
-      tma_load_4d(dV + 8192, &tmV, 64, k0, kvh, b, bar);
-    } else {
-      const int np = (min(kTcKeys, k_end - k0) + 15) / 16;
-      mbar_expect_tx(bar, (uint32_t)np * 4 * 2048);
+      const int v0 = (j - n_pre) * KT;
+      mbar_expect_tx(bar, C::kKBytes);
 #pragma unroll
-      for (int p = 0; p < 4; ++p) {
+      for (int h = 0; h < KT / 64; ++h) {
+        tma_load_4d(dst + h * 8192, tmn, 0, kvh, v0 + 64 * h, b, bar);
+        tma_load_4d(dst + kBlk + h * 8192, tmn, 64, kvh, v0 + 64 * h, b, bar);
+      }
+    } else if (!PAGED) {
+      mbar_expect_tx(bar, C::kKBytes);
+#pragma unroll
+      for (int h = 0; h < KT / 64; ++h) {
+        tma_load_4d(dst + h * 8192, tm, 0, k0 + 64 * h, kvh, b, bar);
+        tma_load_4d(dst + kBlk + h * 8192, tm, 64, k0 + 64 * h, kvh, b, bar);
+      }
+    } else {
+      const int np = (min(KT, k_end - k0) + 15) / 16;
+      mbar_expect_tx(bar, (uint32_t)np * 2 * 2048);
+#pragma unroll
+      for (int p = 0; p < C::kPages; ++p) {
         if (p < np) {
-          tma_load_4d(dK + p * 2048, &tmK, 0, 0, kvh, page[p], bar);
-          tma_load_4d(dK + 8192 + p * 2048, &tmK, 64, 0, kvh, page[p], bar);
-          tma_load_4d(dV + p * 2048, &tmV, 0, 0, kvh, page[p], bar);
-          tma_load_4d(dV + 8192 + p * 2048, &tmV, 64, 0, kvh, page[p], bar);
+          tma_load_4d(dst + p * 2048, tm, 0, 0, kvh, page[p], bar);
+          tma_load_4d(dst + kBlk + p * 2048, tm, 64, 0, kvh, page[p], bar);
         }
       }
     }
@@ -378,16 +397,19 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
 
   // The producer lane initialises the barriers and starts the first copies at once;
   // the other threads touch the barriers only after the __syncthreads below.
-  int n_issued = 0;
+  int n_issued = 0;                // tiles whose K and V copies have both been issued
+  int n_issued_k = -1;             // on an abort between the K and V copies of a tile: K's count
   if (tid == C::kProdWarp * 32) {
     abort_flag = 0;
     for (int st = 0; st < NS; ++st) {
-      mbar_init(BAR(C::kBarFull + st), 1);
+      mbar_init(BAR(C::kBarFullK + st), 1);
+      mbar_init(BAR(C::kBarFullV + st), 1);
       mbar_init(BAR(C::kBarConvK + st), C::kConvThreads);
       mbar_init(BAR(C::kBarConvV + st), C::kConvThreads);
-      mbar_init(BAR(C::kBarEmpty + st), 1);
+      mbar_init(BAR(C::kBarEmptyK + st), 1);
+      mbar_init(BAR(C::kBarEmptyV + st), 1);
     }
-    for (int p = 0; p < 2 * QT; ++p) {
+    for (int p = 0; p < QT * C::kSB; ++p) {
       mbar_init(BAR(C::kBarSFull + p), 1);
       mbar_init(BAR(C::kBarPFull + p), 4);
       mbar_init(BAR(C::kBarODone + p), 1);
@@ -404,12 +426,15 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
       tma_load_4d(sQ, &tmQ, 0, kvh * g, u0, b, BAR(C::kBarQFull));
       tma_load_4d(sQ + 16384, &tmQ, 64, kvh * g, u0, b, BAR(C::kBarQFull));
     }
-    int pgs[NS][4];                // all first-stage lookups in flight together
+    int pgs[NS][C::kPages];        // all first-stage lookups in flight together
 #pragma unroll
     for (int k = 0; k < NS; ++k) load_pages(k, pgs[k]);
 #pragma unroll
     for (int k = 0; k < NS; ++k)
-      if (k < n_tiles) issue_tile(k, pgs[k]);
+      if (k < n_tiles) {
+        issue_kv(0, k, pgs[k]);
+        issue_kv(1, k, pgs[k]);
+      }
     n_issued = min(n_tiles, NS);
   }
   if (warp == C::kMmaWarp) {
@@ -431,144 +456,191 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
   const uint32_t tmem = tmem_slot;
   const volatile int* abortp = &abort_flag;
 
-  constexpr uint32_t kIdS = idesc_f16(kTcRows, kTcKeys, false);
+  constexpr uint32_t kIdS = idesc_f16(kTcRows, KT, false);
   constexpr uint32_t kIdO = idesc_f16(kTcRows, kDH, true);
   bool ok = true;
   float m_run = -INFINITY, l_run = 0.f;
 
   if (warp == C::kProdWarp) {
-    // ---- TMA producer: tile j >= NS once the P V MMAs of tile j - NS freed its stage ----
-    // The block-table entries of a paged tile are loaded one tile ahead of its copy.
+    // ---- TMA producer: K of tile j >= NS once the S MMAs of tile j - NS freed its K
+    //      slot, then V once the P V MMAs of tile j - NS freed its V slot ----------------
+    // The block-table entries of a paged tile are loaded one tile ahead of its copies.
     if (lane == 0) {
-      int pa[4], pb[4];
+      int pa[C::kPages], pb[C::kPages];
       load_pages(n_issued, pa);
       load_pages(n_issued + 1, pb);
       for (int j = n_issued; j < n_tiles; ++j) {
-        if (!wait_or_abort(BAR(C::kBarEmpty + j % NS), ((j / NS) - 1) & 1, abortp)) {
+        if (!wait_or_abort(BAR(C::kBarEmptyK + j % NS), ((j / NS) - 1) & 1, abortp)) {
           ok = false;
           break;
         }
-        issue_tile(j, pa);
+        issue_kv(0, j, pa);
+        if (!wait_or_abort(BAR(C::kBarEmptyV + j % NS), ((j / NS) - 1) & 1, abortp)) {
+          ok = false;
+          n_issued_k = j + 1;
+          break;
+        }
+        issue_kv(1, j, pa);
         n_issued = j + 1;
 #pragma unroll
-        for (int p = 0; p < 4; ++p) pa[p] = pb[p];
+        for (int p = 0; p < C::kPages; ++p) pa[p] = pb[p];
         load_pages(j + 2, pb);
       }
     }
   } else if (warp == C::kMmaWarp) {
     // ---- MMA issue ------------------------------------------------------------------
-    // Per query tile q: S(q, j) = Q_q K_j^T into TMEM buffer (q, j & 1) once K_j is
-    // converted and the P V MMAs of (q, j - 2), whose P occupied that buffer, have
-    // completed; O_q += P(q, j) V_j once the softmax of tile q has written P(q, j) and V_j
-    // is converted.  The query tiles run independently, so that the tensor cores work on
-    // one tile while the softmax warps of the other run.  Whichever MMA is ready goes
-    // first, S before P V when both are.  Completion of P V(q, j) is signalled on slot
-    // (q, j & 1), so that a slot's phase never runs more than one ahead of its waiters;
-    // the stage of K_j / V_j is released after the last query tile's P V(j).  Every
-    // commit covers all MMAs issued before it.
-    if (lane == 0) {
-      if (!wait_or_abort(BAR(C::kBarQReady), 0, abortp)) ok = false;
-      int js[QT], jp[QT];
-#pragma unroll
-      for (int q = 0; q < QT; ++q) js[q] = jp[q] = (q < qt_live) ? 0 : n_tiles;
-      uint64_t t_idle = global_ns();
-      auto jp_min = [&]() {
-        int m = jp[0];
-#pragma unroll
-        for (int q = 1; q < QT; ++q) m = min(m, jp[q]);
-        return m;
-      };
-      for (uint32_t spin = 0; ok && jp_min() < n_tiles;) {
-        bool did = false;
-        // every condition of every candidate MMA, tested in one round trip (a test of
-        // a tile that does not exist reads a barrier harmlessly and is ignored)
-        uint32_t tb[8], tp[8];
-#pragma unroll
-        for (int q = 0; q < 2; ++q) {
-          const int qq = q < QT ? q : 0;
-          const int a_ = js[qq], p_ = jp[qq];
-          tb[4 * q + 0] = BAR(C::kBarConvK + a_ % NS);
-          tp[4 * q + 0] = (a_ / NS) & 1;
-          tb[4 * q + 1] = BAR(C::kBarODone + 2 * qq + (a_ & 1));
-          tp[4 * q + 1] = ((a_ - 2) >> 1) & 1;
-          tb[4 * q + 2] = BAR(C::kBarPFull + 2 * qq + (p_ & 1));
-          tp[4 * q + 2] = (p_ >> 1) & 1;
-          tb[4 * q + 3] = BAR(C::kBarConvV + p_ % NS);
-          tp[4 * q + 3] = (p_ / NS) & 1;
-        }
-        const uint32_t ready = mbar_test8(tb, tp);
-#pragma unroll
-        for (int q = 0; q < QT; ++q) {
-          const uint32_t rq = ready >> (4 * q);
-          if (js[q] < n_tiles && js[q] <= jp[q] + 1 && (rq & 1u) && (js[q] < 2 || (rq & 2u))) {
-            const int j = js[q], st = j % NS, sb = j & 1;
+    if constexpr (QT == 1) {
+      // S(j) = Q K_j^T into TMEM buffer j & 1 once K_j is converted and the P V MMAs of
+      // tile j - 2, whose P occupied that buffer, have completed; O += P(j) V_j once the
+      // softmax has written P(j) and V_j is converted.  Whichever is ready goes first,
+      // S before P V when both are; all conditions are tested in one round trip.
+      // Completion of P V(j) is signalled on slot j & 1, so that a slot's phase never
+      // runs more than one ahead of its waiters.  Every commit covers all MMAs issued
+      // before it.
+      if (lane == 0) {
+        if (!wait_or_abort(BAR(C::kBarQReady), 0, abortp)) ok = false;
+        int js = 0, jp = 0;
+        uint64_t t_idle = global_ns();
+        for (uint32_t spin = 0; ok && jp < n_tiles;) {
+          bool did = false;
+          // (a test of a tile that does not exist reads a barrier harmlessly and is ignored)
+          const uint32_t tb[8] = {BAR(C::kBarConvK + js % NS), BAR(C::kBarODone + (js & 1)),
+                                  BAR(C::kBarPFull + (jp & 1)), BAR(C::kBarConvV + jp % NS),
+                                  BAR(C::kBarConvK + js % NS), BAR(C::kBarConvK + js % NS),
+                                  BAR(C::kBarConvK + js % NS), BAR(C::kBarConvK + js % NS)};
+          const uint32_t tp[8] = {(uint32_t)(js / NS) & 1u, (uint32_t)((js - 2) >> 1) & 1u, (uint32_t)(jp >> 1) & 1u,
+                                  (uint32_t)(jp / NS) & 1u, 0u, 0u, 0u, 0u};
+          const uint32_t ready = mbar_test8(tb, tp);
+          if (js < n_tiles && js <= jp + 1 && (ready & 1u) && (js < 2 || (ready & 2u))) {
+            const int st = js % NS, sb = js & 1;
             tc_fence_after();
-            const uint32_t aK = smem_u32(sm + C::kOffStage + st * kStageBytes);
-            const uint32_t sQ = smem_u32(sm + q * kQBytes);
+            const uint32_t aK = smem_u32(sm + C::kOffK + st * C::kKBytes);
+            const uint32_t sQ = smem_u32(sm);
 #pragma unroll
             for (int kk = 0; kk < kDH / 16; ++kk) {
               const uint64_t ad = sw128_desc(sQ + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024);
-              const uint64_t bd = sw128_desc(aK + (kk / 4) * 8192 + (kk % 4) * 32, 16, 1024);
-              umma_f16(tmem + 256u * q + 64u * sb, ad, bd, kIdS, kk > 0 ? 1u : 0u);
+              const uint64_t bd = sw128_desc(aK + (kk / 4) * (KT * 128) + (kk % 4) * 32, 16, 1024);
+              umma_f16(tmem + 64u * sb, ad, bd, kIdS, kk > 0 ? 1u : 0u);
             }
-            umma_commit(BAR(C::kBarSFull + 2 * q + sb));
-            ++js[q];
+            umma_commit(BAR(C::kBarSFull + sb));
+            umma_commit(BAR(C::kBarEmptyK + st));
+            ++js;
             did = true;
           }
-          if (jp[q] < js[q] && (rq & 4u) && (rq & 8u)) {
-            const int j = jp[q], st = j % NS, sb = j & 1;
+          if (jp < js && (ready & 4u) && (ready & 8u)) {
+            const int st = jp % NS, sb = jp & 1;
             tc_fence_after();
-            const uint32_t aV = smem_u32(sm + C::kOffStage + st * kStageBytes + kKBytes);
+            const uint32_t aV = smem_u32(sm + C::kOffV + st * C::kKBytes);
 #pragma unroll
-            for (int kk = 0; kk < kTcKeys / 16; ++kk) {
-              const uint64_t bd = sw128_desc(aV + kk * 2048, 8192, 1024);   // MN-major: dim blocks 8 KiB apart
-              umma_f16_ts(tmem + 256u * q + kTmemO, tmem + 256u * q + 64u * sb + 8u * kk, bd, kIdO,
-                          (j > 0 || kk > 0) ? 1u : 0u);
+            for (int kk = 0; kk < KT / 16; ++kk) {
+              const uint64_t bd = sw128_desc(aV + kk * 2048, KT * 128, 1024);   // MN-major: dim blocks KT x 128 B apart
+              umma_f16_ts(tmem + kTmemO, tmem + 64u * sb + 8u * kk, bd, kIdO, (jp > 0 || kk > 0) ? 1u : 0u);
             }
-            umma_commit(BAR(C::kBarODone + 2 * q + sb));
-            ++jp[q];
-            if (jp_min() > j) umma_commit(BAR(C::kBarEmpty + st));
+            umma_commit(BAR(C::kBarEmptyV + st));
+            umma_commit(BAR(C::kBarODone + sb));
+            ++jp;
             did = true;
+          }
+          if (did) {
+            spin = 0;
+            t_idle = global_ns();
+          } else if (*abortp || ((++spin & 255u) == 0 && global_ns() - t_idle > 2000000000ull)) {
+            ok = false;
           }
         }
-        if (did) {
-          spin = 0;
-          t_idle = global_ns();
-        } else if (*abortp || ((++spin & 255u) == 0 && global_ns() - t_idle > 2000000000ull)) {
+        // O is final once the last P V MMAs have completed.
+        if (ok && n_tiles > 0 &&
+            !wait_or_abort(BAR(C::kBarODone + ((n_tiles - 1) & 1)), ((n_tiles - 1) >> 1) & 1, abortp))
           ok = false;
+      }
+    } else {
+      // Two query tiles, one S buffer each, in a fixed order with blocking waits:
+      //   S(0, 0), S(1, 0), then for every tile j: P V(0, j), S(0, j + 1), P V(1, j),
+      //   S(1, j + 1).
+      // S(q, j + 1) overwrites the P of (q, j), so it waits for P V(q, j) to complete;
+      // while one query tile's softmax runs, the tensor cores work on the other's MMAs.
+      // A K slot is released after the last query tile's S of its tile, a V slot after
+      // the last P V.  Each S / P V barrier completes once per tile: the phase of tile j
+      // is j & 1.  (A fixed order with waits that suspend the thread measured faster
+      // than issuing in readiness order by polling.)
+      if (lane == 0) {
+        if (!wait_or_abort(BAR(C::kBarQReady), 0, abortp)) ok = false;
+        auto issue_s = [&](int q, int j) -> bool {
+          const int st = j % NS;
+          if (q == 0 && !wait_or_abort(BAR(C::kBarConvK + st), (j / NS) & 1, abortp)) return false;
+          if (j > 0 && !wait_or_abort(BAR(C::kBarODone + q), (j - 1) & 1, abortp)) return false;
+          tc_fence_after();
+          const uint32_t aK = smem_u32(sm + C::kOffK + st * C::kKBytes);
+          const uint32_t sQ = smem_u32(sm + q * kQBytes);
+#pragma unroll
+          for (int kk = 0; kk < kDH / 16; ++kk) {
+            const uint64_t ad = sw128_desc(sQ + (kk / 4) * 16384 + (kk % 4) * 32, 16, 1024);
+            const uint64_t bd = sw128_desc(aK + (kk / 4) * (KT * 128) + (kk % 4) * 32, 16, 1024);
+            umma_f16(tmem + 256u * q, ad, bd, kIdS, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(BAR(C::kBarSFull + q));
+          if (q == qt_live - 1) umma_commit(BAR(C::kBarEmptyK + st));
+          return true;
+        };
+        auto issue_pv = [&](int q, int j) -> bool {
+          const int st = j % NS;
+          if (q == 0 && !wait_or_abort(BAR(C::kBarConvV + st), (j / NS) & 1, abortp)) return false;
+          if (!wait_or_abort(BAR(C::kBarPFull + q), j & 1, abortp)) return false;
+          tc_fence_after();
+          const uint32_t aV = smem_u32(sm + C::kOffV + st * C::kKBytes);
+#pragma unroll
+          for (int kk = 0; kk < KT / 16; ++kk) {
+            const uint64_t bd = sw128_desc(aV + kk * 2048, KT * 128, 1024);   // MN-major: dim blocks KT x 128 B apart
+            umma_f16_ts(tmem + 256u * q + kTmemO, tmem + 256u * q + 8u * kk, bd, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
+          }
+          umma_commit(BAR(C::kBarODone + q));
+          if (q == qt_live - 1) umma_commit(BAR(C::kBarEmptyV + st));
+          return true;
+        };
+        // a query tile past the last row (qt_live == 1) is skipped entirely
+        if (ok && n_tiles > 0) {
+          for (int q = 0; q < qt_live && ok; ++q) ok = issue_s(q, 0);
+          for (int j = 0; ok && j < n_tiles; ++j) {
+            for (int q = 0; q < qt_live && ok; ++q) {
+              ok = issue_pv(q, j);
+              if (ok && j + 1 < n_tiles) ok = issue_s(q, j + 1);
+            }
+          }
+          // O is final once the last P V MMAs have completed.
+          for (int q = 0; q < qt_live && ok; ++q)
+            ok = wait_or_abort(BAR(C::kBarODone + q), (n_tiles - 1) & 1, abortp);
         }
       }
-      // O is final once the last P V MMAs have completed.
-      for (int q = 0; q < qt_live; ++q)
-        if (ok && n_tiles > 0 &&
-            !wait_or_abort(BAR(C::kBarODone + 2 * q + ((n_tiles - 1) & 1)), ((n_tiles - 1) >> 1) & 1, abortp))
-          ok = false;
     }
   } else if (warp >= C::kConvWarp0) {
     // ---- bf16 -> fp16 conversion (tree keys also rotated) ------------------------------
     const int ct = tid - C::kConvWarp0 * 32;
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j % NS;
-      uint8_t* tK = sm + C::kOffStage + st * kStageBytes;
-      uint8_t* tV = tK + kKBytes;
+      uint8_t* tK = sm + C::kOffK + st * C::kKBytes;
+      uint8_t* tV = sm + C::kOffV + st * C::kKBytes;
       const int k_valid = tile_valid(j);
       int dep[C::kRotIter];
       if (j >= n_pre) {
 #pragma unroll
         for (int i = 0; i < C::kRotIter; ++i) {
           const int r = rotate_row<C::kConvThreads>(i, ct);
-          dep[i] = r < k_valid ? __ldg(t.depth + (j - n_pre) * kTcKeys + r) : 0;
+          dep[i] = r < k_valid ? __ldg(t.depth + (j - n_pre) * KT + r) : 0;
         }
       }
-      if (!wait_or_abort(BAR(C::kBarFull + st), (j / NS) & 1, abortp)) {
+      if (!wait_or_abort(BAR(C::kBarFullK + st), (j / NS) & 1, abortp)) {
         ok = false;
         break;
       }
-      if (j >= n_pre) convert_rotate_tile<C::kConvThreads>(tK, k_valid, dep, tab_c, tab_s, ct);
-      else convert_tile<C::kConvThreads>(tK, k_valid, ct);
+      if (j >= n_pre) convert_rotate_tile<C::kConvThreads, KT>(tK, k_valid, dep, tab_c, tab_s, ct);
+      else convert_tile<C::kConvThreads, KT>(tK, k_valid, ct);
       fence_proxy_async();
       mbar_arrive(BAR(C::kBarConvK + st));
-      convert_tile<C::kConvThreads>(tV, k_valid, ct);
+      if (!wait_or_abort(BAR(C::kBarFullV + st), (j / NS) & 1, abortp)) {
+        ok = false;
+        break;
+      }
+      convert_tile<C::kConvThreads, KT>(tV, k_valid, ct);
       fence_proxy_async();
       mbar_arrive(BAR(C::kBarConvV + st));
     }
@@ -662,13 +734,14 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
     constexpr float kRescale = 8.f;
     const uint32_t lane_base = ((uint32_t)((warp & 3) * 32) << 16) + 256u * qt;
     // (a query tile past the last row has no MMAs: its warps skip the loop)
-    for (int j = 0; ok && qt < qt_live && j < n_tiles; ++j) {
+    if constexpr (QT == 1) {
+    for (int j = 0; ok && j < n_tiles; ++j) {
       const int sb = j & 1;
       const bool tree_tile = j >= n_pre;
       const int k_valid = tile_valid(j);
       const uint64_t vis = (tree_tile && row_ok) ? __ldg(t.anc + (int64_t)u * t.n_words + (j - n_pre)) : 0ull;
       // wait outcomes are made warp-uniform: the TMEM accesses below are warp-collective
-      if (!__all_sync(0xffffffffu, wait_or_abort(BAR(C::kBarSFull + 2 * qt + sb), (j >> 1) & 1, abortp))) {
+      if (!__all_sync(0xffffffffu, wait_or_abort(BAR(C::kBarSFull + sb), (j >> 1) & 1, abortp))) {
         ok = false;
         break;
       }
@@ -699,7 +772,7 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
         if (first) m_run = mx;                           // O holds nothing yet for this row
         if (__any_sync(0xffffffffu, need)) {
           if (!__all_sync(0xffffffffu,
-                          wait_or_abort(BAR(C::kBarODone + 2 * qt + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abortp))) {
+                          wait_or_abort(BAR(C::kBarODone + ((j - 1) & 1)), ((j - 1) >> 1) & 1, abortp))) {
             ok = false;
             break;
           }
@@ -735,7 +808,99 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
       }
       tc_fence_before();
       __syncwarp();
-      if (lane == 0) mbar_arrive(BAR(C::kBarPFull + 2 * qt + sb));
+      if (lane == 0) mbar_arrive(BAR(C::kBarPFull + sb));
+    }
+    } else {
+    // Two query tiles of 128-key tiles, one S buffer each.  When S(q, j) lands, the P V
+    // MMAs of (q, j - 1) have completed (S(q, j) was issued after them), so O may be
+    // rescaled at once.  The row's 128 scores are read twice from TMEM, 64 at a time:
+    // once for the max, once for P, which is written as fp16 pairs over the S columns
+    // already read.
+    const uint32_t sbase = tmem + lane_base;
+    for (int j = 0; ok && qt < qt_live && j < n_tiles; ++j) {
+      const bool tree_tile = j >= n_pre;
+      const int k_valid = tile_valid(j);
+      uint64_t vis0 = 0ull, vis1 = 0ull;
+      if (tree_tile && row_ok) {
+        const int w0 = 2 * (j - n_pre);
+        vis0 = __ldg(t.anc + (int64_t)u * t.n_words + w0);
+        vis1 = w0 + 1 < t.n_words ? __ldg(t.anc + (int64_t)u * t.n_words + w0 + 1) : 0ull;
+      }
+      // wait outcomes are made warp-uniform: the TMEM accesses below are warp-collective
+      if (!__all_sync(0xffffffffu, wait_or_abort(BAR(C::kBarSFull + qt), j & 1, abortp))) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      if (live) {
+        auto load_half = [&](int h, float* sv) {     // scores of keys [64h, 64h + 64), masked
+          tmem_ld32(sbase + 64u * h, sv);
+          tmem_ld32(sbase + 64u * h + 32, sv + 32);
+          if (tree_tile) {
+            const uint64_t vh = h ? vis1 : vis0;
+#pragma unroll
+            for (int c = 0; c < 64; ++c) sv[c] = ((vh >> c) & 1ull) ? sv[c] : -INFINITY;
+          } else if (k_valid < KT) {
+#pragma unroll
+            for (int c = 0; c < 64; ++c) sv[c] = 64 * h + c < k_valid ? sv[c] : -INFINITY;
+          }
+        };
+        float mxp[2] = {-INFINITY, -INFINITY};
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          float sv[64];
+          load_half(h, sv);
+#pragma unroll
+          for (int c = 0; c < 64; c += 4) {
+            mxp[0] = fmax3(mxp[0], sv[c], sv[c + 1]);
+            mxp[1] = fmax3(mxp[1], sv[c + 2], sv[c + 3]);
+          }
+        }
+        const float mx = fmaxf(mxp[0], mxp[1]);
+        // The TMEM accesses of a rescale are warp-collective: the warp rescales when any
+        // of its rows needs it, the other rows scale by 1.
+        const bool first = (m_run == -INFINITY);
+        const bool need = !first && (mx > m_run + kRescale);
+        if (first) m_run = mx;                           // O holds nothing yet for this row
+        if (__any_sync(0xffffffffu, need)) {
+          const float alpha = need ? fast_exp2(m_run - mx) : 1.f;
+          l_run *= alpha;
+#pragma unroll 1
+          for (int q8 = 0; q8 < kDH / 16; ++q8) {
+            float ov[16];
+            tmem_ld16(sbase + kTmemO + 16 * q8, ov);
+#pragma unroll
+            for (int i = 0; i < 16; ++i) ov[i] *= alpha;
+            tmem_st16(sbase + kTmemO + 16 * q8, ov);
+          }
+          if (need) m_run = mx;
+        }
+        const float mref = (m_run == -INFINITY) ? 0.f : m_run;   // a fully masked row keeps P = 0
+        const float2 nm = make_float2(-mref, -mref);
+        float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
+#pragma unroll 1
+        for (int h = 0; h < 2; ++h) {
+          float sv[64];
+          load_half(h, sv);
+          float pk[32];                            // P as fp16 pairs, key 2i in the low half
+#pragma unroll
+          for (int i = 0; i < 32; ++i) {
+            const float2 d = __fadd2_rn(make_float2(sv[2 * i], sv[2 * i + 1]), nm);
+            const float2 pp = make_float2(fast_exp2(d.x), fast_exp2(d.y));
+            ps[i & 3] = __fadd2_rn(ps[i & 3], pp);
+            pk[i] = __uint_as_float(pack_half2(pp.x, pp.y));
+          }
+          tmem_st32_nowait(sbase + 32u * h, pk);   // over S columns [32h, 32h + 32), already read
+        }
+        tmem_wait_st();
+        const float2 s01 = __fadd2_rn(ps[0], ps[1]), s23 = __fadd2_rn(ps[2], ps[3]);
+        const float2 s4 = __fadd2_rn(s01, s23);
+        l_run += s4.x + s4.y;
+      }
+      tc_fence_before();
+      __syncwarp();
+      if (lane == 0) mbar_arrive(BAR(C::kBarPFull + qt));
+    }
     }
   }
 
@@ -752,8 +917,11 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
     // and all MMAs.
     if (warp == C::kProdWarp && lane == 0) {
       mbar_wait(BAR(C::kBarQFull), 0, 100000000ull);
+      const int nk = n_issued_k >= 0 ? n_issued_k : n_issued;
+      for (int j = nk - NS; j < nk; ++j)
+        if (j >= 0) mbar_wait(BAR(C::kBarFullK + j % NS), (j / NS) & 1, 100000000ull);
       for (int j = n_issued - NS; j < n_issued; ++j)
-        if (j >= 0) mbar_wait(BAR(C::kBarFull + j % NS), (j / NS) & 1, 100000000ull);
+        if (j >= 0) mbar_wait(BAR(C::kBarFullV + j % NS), (j / NS) & 1, 100000000ull);
     }
     if (warp == C::kMmaWarp && lane == 0) {
       umma_commit(BAR(C::kBarDrain));
@@ -921,21 +1089,22 @@ bool attn_tc_supported(const medusa_tree_t& t, int Hq, const medusa_kv_t& c) {
 }
 
 // Kernel shape and split choice.  With four or more query tiles per unit, one CTA
-// takes two of them (QT = 2) so that every K/V tile is copied and converted once for
-// 256 rows, with three stages in flight (one CTA per SM: 192 KB of shared memory).
-// Fewer query tiles run two CTAs per SM with two stages each, which overlaps one CTA's
-// prologue and merge with the other's main loop.  The splits: enough CTAs to fill the
-// SM slots, in whole waves where possible, with at most kMaxClusterSplits splits (one
-// cluster) per unit and at least rows/16 tiles per split.  The tree tiles count as
-// work of split 0, which takes that many fewer prefix tiles, so that the splits end
-// together.  MEDUSA_ATTN_TC_SHAPE="QT,NS" (one of 1,2 / 1,4 / 2,3) overrides the shape.
+// takes two of them (QT = 2, 128-key tiles, two stages: 192 KB of shared memory, one
+// CTA per SM), so that every K/V tile is copied and converted once for 256 rows and the
+// two tiles keep the tensor cores busy in turn.  Fewer query tiles run two CTAs per SM
+// (QT = 1, 64-key tiles, two stages), which overlaps one CTA's prologue and merge with
+// the other's main loop.  The splits: enough CTAs to fill the SM slots, in whole waves
+// where possible, with at most kMaxClusterSplits splits (one cluster) per unit and at
+// least rows/16 tiles of 64 keys per split.  The tree tiles count as work of split 0,
+// which takes that many fewer prefix tiles, so that the splits end together.
+// MEDUSA_ATTN_TC_SHAPE="QT,NS" (one of 1,2 / 1,4 / 2,2) overrides the shape.
 void attn_tc_plan(AttnPlan& p) {
   const int M = p.N * p.g;
   const int n_tiles_q = (M + kTcRows - 1) / kTcRows;
-  int qt = n_tiles_q >= 4 ? 2 : 1, stages = qt == 2 ? 3 : 2;
+  int qt = n_tiles_q >= 4 ? 2 : 1, stages = 2;
   if (const char* e = std::getenv("MEDUSA_ATTN_TC_SHAPE")) {
     int a = 0, b = 0;
-    if (std::sscanf(e, "%d,%d", &a, &b) == 2 && ((a == 1 && (b == 2 || b == 4)) || (a == 2 && b == 3))) {
+    if (std::sscanf(e, "%d,%d", &a, &b) == 2 && ((a == 1 && (b == 2 || b == 4)) || (a == 2 && b == 2))) {
       qt = a;
       stages = b;
     }
@@ -943,16 +1112,17 @@ void attn_tc_plan(AttnPlan& p) {
   p.qt = qt;
   p.stages = stages;
   p.mt_rows = kTcRows * qt;
-  p.key_tile = kTcKeys;
+  const int KT = 64 * qt;
+  p.key_tile = KT;
   p.n_mt = (M + p.mt_rows - 1) / p.mt_rows;
   const int units = p.B * p.Hkv * p.n_mt;
   int sms = 148, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   const double slots = (qt == 1 && stages == 2 ? 2.0 : 1.0) * sms;
-  const int tiles_unit = (p.max_prefix + kTcKeys - 1) / kTcKeys;
-  const int n_tree = (p.N + kTcKeys - 1) / kTcKeys;
+  const int tiles_unit = (p.max_prefix + KT - 1) / KT;
+  const int n_tree = (p.N + KT - 1) / KT;
   const int rows = M < kTcRows ? M : kTcRows;
-  int min_tiles = (rows + 15) / 16;
+  int min_tiles = ((rows + 15) / 16 + qt - 1) / qt;
   if (min_tiles < 2) min_tiles = 2;
   int max_split = tiles_unit / min_tiles;
   if (max_split > kMaxClusterSplits) max_split = kMaxClusterSplits;
@@ -972,8 +1142,8 @@ void attn_tc_plan(AttnPlan& p) {
   const int rest = tiles_unit - first_tiles;
   int chunk_tiles = best > 1 ? (rest + best - 2) / (best - 1) : 1;
   if (chunk_tiles < 1) chunk_tiles = 1;
-  p.first = first_tiles * kTcKeys;
-  p.chunk = chunk_tiles * kTcKeys;
+  p.first = first_tiles * KT;
+  p.chunk = chunk_tiles * KT;
   p.n_split = 1 + (rest + chunk_tiles - 1) / chunk_tiles;
 }
 
@@ -994,7 +1164,7 @@ cudaError_t launch_shape(cudaLaunchConfig_t& cfg, int D, const CUtensorMap& mk, 
 template <bool PAGED>
 cudaError_t launch_paged(const AttnPlan& p, cudaLaunchConfig_t& cfg, const CUtensorMap& mk, const CUtensorMap& mv,
                          const CUtensorMap& mkn, const CUtensorMap& mvn, const CUtensorMap& mq, const TcArgs& a) {
-  if (p.qt == 2) return launch_shape<PAGED, 2, 3>(cfg, p.D, mk, mv, mkn, mvn, mq, a);
+  if (p.qt == 2) return launch_shape<PAGED, 2, 2>(cfg, p.D, mk, mv, mkn, mvn, mq, a);
   if (p.stages == 4) return launch_shape<PAGED, 1, 4>(cfg, p.D, mk, mv, mkn, mvn, mq, a);
   return launch_shape<PAGED, 1, 2>(cfg, p.D, mk, mv, mkn, mvn, mq, a);
 }
