@@ -254,7 +254,7 @@ class Round:
 
 # DRAM bytes (read + write) of one heads launch, from an ncu capture of the current
 # kernel on that workload; absent for workloads not captured.
-HEADS_TRAFFIC = {"vicuna7b-64": 1_445_122_000 + 4_736_256}
+HEADS_TRAFFIC = {"vicuna7b-64": 1_445_265_000 + 4_523_008}
 
 
 def time_loop(fn, steps, stream):
