@@ -263,7 +263,7 @@ struct TcCfg {
   static constexpr int kBarSFull = 6 * NS;                   // [QT][kSB] S buffer written (tcgen05.commit)
   static constexpr int kBarPFull = kBarSFull + QT * kSB;     // [QT][kSB] P written over S (one arrival per softmax warp)
   static constexpr int kBarODone = kBarPFull + QT * kSB;     // [QT][kSB] P V MMAs complete
-  static constexpr int kBarQReady = kBarODone + QT * kSB;    // queries staged (one arrival per softmax warp)
+  static constexpr int kBarQReady = kBarODone + QT * kSB;    // queries staged (one arrival per warp)
   static constexpr int kBarDrain = kBarQReady + 1;           // final commit on the error path
   static constexpr int kBarQFull = kBarQReady + 2;           // query tiles landed
   static constexpr int kNumBars = kBarQReady + 3;
@@ -414,7 +414,7 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
       mbar_init(BAR(C::kBarPFull + p), 4);
       mbar_init(BAR(C::kBarODone + p), 1);
     }
-    mbar_init(BAR(C::kBarQReady), C::kSoftWarps);
+    mbar_init(BAR(C::kBarQReady), C::kThreads / 32);
     mbar_init(BAR(C::kBarDrain), 1);
     mbar_init(BAR(C::kBarQFull), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
@@ -460,6 +460,39 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
   constexpr uint32_t kIdO = idesc_f16(kTcRows, kDH, true);
   bool ok = true;
   float m_run = -INFINITY, l_run = 0.f;
+
+  // ---- queries: every warp of the CTA takes part ----------------------------------
+  // The query tiles landed by TMA as bf16, K-major with the 128-byte swizzle (dims i
+  // and i + 64 of a row at the same position of the two 64-dim blocks).  Each row is
+  // rotated in place at L + depth, pre-multiplied by scale * log2 e and stored as fp16.
+  // An item is one row's dims [8c, 8c + 8) and [64 + 8c, 64 + 8c + 8).
+  // (wait outcomes are made warp-uniform: the softmax's TMEM accesses are warp-collective)
+  if (!__all_sync(0xffffffffu, wait_or_abort(BAR(C::kBarQFull), 0, abortp))) ok = false;
+  if (ok) {
+    for (int it = tid; it < rows_valid * 8; it += C::kThreads) {
+      const int r = it >> 3, c = it & 7;
+      const int tr = r & (kTcRows - 1);
+      const int ti0 = __ldg(t.depth + (row0 + r) / g) * kHalf + 8 * c;
+      uint4* q0 = reinterpret_cast<uint4*>(sm + (r / kTcRows) * kQBytes + tr * 128) + (c ^ (tr & 7));
+      uint4* q1 = reinterpret_cast<uint4*>(reinterpret_cast<uint8_t*>(q0) + 16384);
+      float x1[8], x2[8], y1[8], y2[8];
+      Elem<uint16_t>::unpack(*q0, x1);
+      Elem<uint16_t>::unpack(*q1, x2);
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        const float cs = tab_c[ti0 + e], sn = tab_s[ti0 + e];
+        y1[e] = (x1[e] * cs - x2[e] * sn) * a.scale_log2;
+        y2[e] = (x2[e] * cs + x1[e] * sn) * a.scale_log2;
+      }
+      *q0 = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]), pack_half2(y1[4], y1[5]),
+                       pack_half2(y1[6], y1[7]));
+      *q1 = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]), pack_half2(y2[4], y2[5]),
+                       pack_half2(y2[6], y2[7]));
+    }
+  }
+  fence_proxy_async();
+  __syncwarp();
+  if (lane == 0) mbar_arrive(BAR(C::kBarQReady));
 
   if (warp == C::kProdWarp) {
     // ---- TMA producer: K of tile j >= NS once the S MMAs of tile j - NS freed its K
@@ -690,42 +723,6 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
   } else {
     // ---- softmax warps: thread tid owns CTA row tid; warp w reads TMEM lanes of
     //      quadrant w % 4 of query tile w / 4 --------------------------------------------
-    // The query tiles landed by TMA as bf16, K-major with the 128-byte swizzle (dims
-    // i and i + 64 of a row at the same position of the two 64-dim blocks).  Rotate
-    // each row in place at L + depth, pre-multiply by scale * log2 e, store fp16.
-    if (!__all_sync(0xffffffffu, wait_or_abort(BAR(C::kBarQFull), 0, abortp))) ok = false;
-    const int tr = tid & (kTcRows - 1);                     // row within its query tile
-    if (ok && live) {
-      const int ti0 = __ldg(t.depth + u) * kHalf;
-      uint4* q0 = reinterpret_cast<uint4*>(sm + qt * kQBytes + tr * 128);
-      uint4* q1 = reinterpret_cast<uint4*>(sm + qt * kQBytes + 16384 + tr * 128);
-      uint4 qa[8], qb[8];
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {
-        qa[c] = q0[c ^ (tr & 7)];
-        qb[c] = q1[c ^ (tr & 7)];
-      }
-#pragma unroll
-      for (int c = 0; c < 8; ++c) {            // dims [8c, 8c+8) and [64+8c, 64+8c+8)
-        float x1[8], x2[8], y1[8], y2[8];
-        Elem<uint16_t>::unpack(qa[c], x1);
-        Elem<uint16_t>::unpack(qb[c], x2);
-#pragma unroll
-        for (int e = 0; e < 8; ++e) {
-          const float cs = tab_c[ti0 + 8 * c + e], sn = tab_s[ti0 + 8 * c + e];
-          y1[e] = (x1[e] * cs - x2[e] * sn) * a.scale_log2;
-          y2[e] = (x2[e] * cs + x1[e] * sn) * a.scale_log2;
-        }
-        q0[c ^ (tr & 7)] = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]),
-                                      pack_half2(y1[4], y1[5]), pack_half2(y1[6], y1[7]));
-        q1[c ^ (tr & 7)] = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]),
-                                      pack_half2(y2[4], y2[5]), pack_half2(y2[6], y2[7]));
-      }
-    }
-    fence_proxy_async();
-    __syncwarp();
-    if (lane == 0) mbar_arrive(BAR(C::kBarQReady));
-
     // Online softmax.  O accumulates in TMEM across tiles.  The running max m_run is
     // raised only when a tile's max exceeds it by more than 2^8 (log2 units); then O
     // and l are rescaled.  Otherwise P = 2^(s - m_run) <= 256, which fp16 and the fp32

@@ -329,6 +329,7 @@ __global__ void __launch_bounds__(kThreads) topk_rows_kernel(const float* __rest
                                                              int* __restrict__ tick, int32_t* __restrict__ root,
                                                              int32_t* __restrict__ pool, const int* __restrict__ err) {
   __shared__ Cand lists[kWarps][32];
+  __shared__ Cand spans[kTopkMaxSpans * 32];
   __shared__ float mv[32];
   __shared__ int mi[32];
   __shared__ int last;
@@ -340,27 +341,67 @@ __global__ void __launch_bounds__(kThreads) topk_rows_kernel(const float* __rest
   const int c_lo = c * span, c_hi = min(V, c_lo + span);
   float lv = -INFINITY;
   int li = INT_MAX;
+  // The current k-th entry (the admission threshold) is kept in registers and
+  // refreshed only after an insertion.
+  float tv = -INFINITY;
+  int ti = INT_MAX;
+  bool filled = false;            // warp-uniform: the list has been seeded
   // warp w scans part of [c_lo, c_hi); 128 values per step as one float4 per lane when
   // rows are 16-byte aligned (span is a multiple of 128 then)
   auto offer = [&](float v, int i, bool valid) {
-    const float tv = __shfl_sync(0xffffffffu, lv, kk - 1);   // the current k-th entry
-    const int ti = __shfl_sync(0xffffffffu, li, kk - 1);
+    if (!filled) {
+      // the first 32 values seed the list: one bitonic sort across the warp (best
+      // first) instead of up to 32 single insertions
+      float sv = valid ? v : -INFINITY;
+      int si = valid ? i : INT_MAX;
+#pragma unroll
+      for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+          const float ov = __shfl_xor_sync(0xffffffffu, sv, j);
+          const int oi = __shfl_xor_sync(0xffffffffu, si, j);
+          const bool best_first = (lane & k) == 0 || k == 32;   // direction of this block
+          const bool lower = (lane & j) == 0;
+          const bool o_better = ranks_before(ov, oi, sv, si);
+          if ((lower == best_first) ? o_better : (!o_better && (ov != sv || oi != si))) { sv = ov; si = oi; }
+        }
+      lv = lane < kk ? sv : -INFINITY;
+      li = lane < kk ? si : INT_MAX;
+      tv = __shfl_sync(0xffffffffu, lv, kk - 1);
+      ti = __shfl_sync(0xffffffffu, li, kk - 1);
+      filled = true;
+      return;
+    }
     unsigned cm = __ballot_sync(0xffffffffu, valid && ranks_before(v, i, tv, ti));
-    while (cm) {
-      const int sl = __ffs(cm) - 1;
-      cm &= cm - 1;
-      topk_insert(__shfl_sync(0xffffffffu, v, sl), __shfl_sync(0xffffffffu, i, sl), kk, lv, li);
+    if (cm) {
+      do {
+        const int sl = __ffs(cm) - 1;
+        cm &= cm - 1;
+        topk_insert(__shfl_sync(0xffffffffu, v, sl), __shfl_sync(0xffffffffu, i, sl), kk, lv, li);
+      } while (cm);
+      tv = __shfl_sync(0xffffffffu, lv, kk - 1);
+      ti = __shfl_sync(0xffffffffu, li, kk - 1);
     }
   };
   if ((V & 3) == 0) {
-#pragma unroll 2
-    for (int base = c_lo + 128 * warp; base < c_hi; base += 128 * kWarps) {
-      const int i0 = base + 4 * lane;
-      const float4 q = i0 < c_hi ? __ldg(reinterpret_cast<const float4*>(src + i0)) : make_float4(0.f, 0.f, 0.f, 0.f);
-      offer(q.x, i0, i0 < c_hi);
-      offer(q.y, i0 + 1, i0 + 1 < c_hi);
-      offer(q.z, i0 + 2, i0 + 2 < c_hi);
-      offer(q.w, i0 + 3, i0 + 3 < c_hi);
+    // kBatch float4 per lane are loaded before any is offered: one memory round trip
+    // per 128 kBatch values of the warp
+    constexpr int kBatch = 4;
+    for (int base = c_lo + 128 * warp; base < c_hi; base += 128 * kWarps * kBatch) {
+      float4 q[kBatch];
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int i0 = base + 128 * kWarps * u + 4 * lane;
+        q[u] = i0 < c_hi ? __ldg(reinterpret_cast<const float4*>(src + i0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+      }
+#pragma unroll
+      for (int u = 0; u < kBatch; ++u) {
+        const int i0 = base + 128 * kWarps * u + 4 * lane;
+        offer(q[u].x, i0, i0 < c_hi);
+        offer(q[u].y, i0 + 1, i0 + 1 < c_hi);
+        offer(q[u].z, i0 + 2, i0 + 2 < c_hi);
+        offer(q[u].w, i0 + 3, i0 + 3 < c_hi);
+      }
     }
   } else {
     for (int base = c_lo + 32 * warp; base < c_hi; base += 32 * kWarps) {
@@ -383,14 +424,19 @@ __global__ void __launch_bounds__(kThreads) topk_rows_kernel(const float* __rest
     last = tk == ns - 1;
   }
   __syncthreads();
-  if (!last || warp != 0) return;
-  // the last CTA of the row: merge every span's list
+  if (!last) return;
+  // the last CTA of the row: stage every span's list in shared memory (all loads in
+  // flight at once), then merge them
   __threadfence();
   const Cand* rl = cand + (int64_t)row * ns * topk;
-  merge_lists(ns, kk, [&](int l, int e) {
-    const float2 f = __ldcg(reinterpret_cast<const float2*>(rl + (int64_t)l * topk + e));
-    return Cand{f.x, __float_as_int(f.y)};
-  }, mv, mi);
+  for (int e = threadIdx.x; e < ns * kk; e += kThreads) {
+    const int l = e / kk, r = e % kk;
+    const float2 f = __ldcg(reinterpret_cast<const float2*>(rl + (int64_t)l * topk + r));
+    spans[l * kk + r] = Cand{f.x, __float_as_int(f.y)};
+  }
+  __syncthreads();
+  if (warp != 0) return;
+  merge_lists(ns, kk, [&](int l, int e) { return spans[l * kk + e]; }, mv, mi);
   __syncwarp();
   if (lane == 0) {
     const bool bad = *reinterpret_cast<const volatile int*>(err) != 0;   // a weight-stream wait gave up
