@@ -240,8 +240,9 @@ class Round:
         T = w.batch
         if bf16 and T == 1 and w.hidden % 256 == 0 and w.hidden <= 4096 and w.n_heads >= 1:
             heads = 1                                   # one persistent weight stream with top-k
-        elif bf16 and 2 <= T <= 128 and w.hidden % 64 == 0 and w.n_heads >= 1:
-            heads = 3                                   # input pairs, tensor-core stream, top-k
+        elif bf16 and T >= 2 and w.hidden % 64 == 0 and w.n_heads >= 1:
+            heads = 2 * math.ceil(T / 128) + 1         # per pass of <= 128 rows: input pairs and
+                                                        # tensor-core stream; then top-k
         else:
             tpp = 1
             fit = max(1, min(16, (160 * 1024) // (w.hidden * 4)))
@@ -255,6 +256,29 @@ class Round:
 # DRAM bytes (read + write) of one heads launch, from an ncu capture of the current
 # kernel on that workload; absent for workloads not captured.
 HEADS_TRAFFIC = {"vicuna7b-64": 1_445_265_000 + 4_523_008}
+
+
+def heads_all_rows(rd, stream, peak_tflops):
+    """medusa_heads_topk with every tree row as a hidden row (T = B N), the variant in which
+    the heads are a tensor-core contraction.  bf16 with T >= 2 runs on the tensor cores
+    with each input row as a bf16 pair (hi, lo), so the MMAs execute twice the useful
+    2 T flops per weight element; both rates are reported."""
+    w = rd.w
+    T = w.batch * rd.N                                  # every tree row of every sequence
+    h = synth.normal((T, w.hidden), 1.0, w.seed, "h", rd.dev, w.torch_dtype, sub=1)
+    call = lambda: rd.m.medusa_heads_topk(h, rd.w1, rd.w2, rd.w_lm, w.topk)
+    for _ in range(3):
+        call()
+    torch.cuda.synchronize(rd.dev)
+    n = 5
+    us = 1e3 * time_loop(call, n, stream) / n
+    elems = rd.w1.numel() + rd.w2.numel() + rd.w_lm.numel()
+    useful = 2.0 * T * elems / (us * 1e-6) / 1e12
+    pairs = 2 if (w.dtype == "bf16" and T >= 2) else 1
+    passes = math.ceil(T / 128) if pairs == 2 else 1
+    return {"T": T, "us": us, "useful_tflops": useful, "tensor_tflops": useful * pairs,
+            "peak_tflops": peak_tflops, "frac": useful * pairs / peak_tflops, "weight_passes": passes,
+            "hbm_gbs": passes * rd.head_bytes() / (us * 1e-6) / 1e9}
 
 
 def time_loop(fn, steps, stream):
@@ -478,6 +502,7 @@ def main():
     heads_gbs = rd.head_bytes() / (heads_us * 1e-6) / 1e9
     e2e_ms, h2d, d2h = e2e_loop(rd, max(10, args.steps // 4), stream)
     e2e_ms = max_over_ranks(e2e_ms, ws, dev)
+    all_rows = heads_all_rows(rd, stream, bf16) if rank == 0 else None
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -498,6 +523,7 @@ def main():
                          "bound": "hbm", "achieved": heads_gbs, "peak": hbm, "unit": "GB/s",
                          "frac": heads_gbs / hbm, "traffic": HEADS_TRAFFIC.get(w.name), "peak_source": src,
                          "algorithmic_bytes": rd.head_bytes(), "launch_us": heads_us},
+            "heads_all_rows": all_rows,
             "tree_attn_roofline": {"kernel": "medusa_tree_attn_verify", "bound": "hbm", "achieved": attn_gbs,
                                    "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm, "traffic": None,
                                    "peak_source": src, "algorithmic_bytes": rd.attn_bytes()},

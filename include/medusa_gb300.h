@@ -64,6 +64,7 @@ typedef int32_t medusa_dtype;
 #define MEDUSA_MAX_ROWS   4096   /* packed tree rows N, root included */
 #define MEDUSA_MAX_DEPTH  16     /* Medusa depth D (paths hold D + 1 rows) */
 #define MEDUSA_MAX_TOPK   32     /* candidate pool width TOPK */
+#define MEDUSA_MAX_HEAD_ROWS 1024 /* hidden rows T of one medusa_heads_topk call */
 
 /*
  * Compiled tree template: the four coupled buffers of [M7.2] §0x04A plus the
@@ -165,7 +166,10 @@ size_t medusa_heads_topk_workspace(int32_t T, int32_t d, int32_t V, int32_t K, i
  *   heads, [M7.2] §0x02D); w_lm [V][d].  All in dtype `dt`.
  *   root [T]; pool [T][K][topk]; logits_out [T][K+1][V] fp32 or NULL (slot 0 =
  *   LM head, slot 1+k = head k).
- * Limits: 1 <= T <= 64, d % 8 == 0, topk <= MEDUSA_MAX_TOPK, topk <= V. */
+ * T may be every tree row (the all-rows variant, e.g. T = N = 341); bf16 with
+ * T >= 2 runs on the tensor cores in passes of up to 128 rows, each reading the
+ * weights once.
+ * Limits: 1 <= T <= MEDUSA_MAX_HEAD_ROWS, d % 8 == 0, topk <= MEDUSA_MAX_TOPK, topk <= V. */
 medusa_status medusa_heads_topk(const void *h, int32_t T, int32_t d, int32_t V, int32_t K,
                                 const void *w1, const void *b1, const void *w2,
                                 int64_t w2_head_stride, const void *w_lm, int32_t topk,

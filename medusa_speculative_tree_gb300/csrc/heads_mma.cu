@@ -368,7 +368,8 @@ bool encode_w2(CUtensorMap* map, const void* base, int d, int V, int K, int64_t 
 bool heads_mma_supported(int T, int d, int V, int K, medusa_dtype dt, const void* h, const void* w1, const void* w2,
                          int64_t w2_stride, const void* w_lm) {
   auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  if (T < 2 || T > 128 || dt != MEDUSA_BF16 || K < 1 || d % kMKc != 0 || V < 1) return false;
+  if (T < 2 || dt != MEDUSA_BF16 || K < 1 || d % kMKc != 0 || V < 1) return false;
+  if (T > kHeadsMmaMaxRows) T = kHeadsMmaMaxRows;          // more rows run in passes of this many
   if (!h || !w1 || !w2 || !w_lm || !al(h) || !al(w1) || !al(w2) || !al(w_lm)) return false;
   if (w2_stride < 0 || (w2_stride * 2) % 16 != 0 || (w2_stride != 0 && w2_stride < (int64_t)V * d)) return false;
   if (!encode_fn()) return false;

@@ -18,6 +18,8 @@ struct HeadsPlan {
 };
 // Weight-stream path (heads_stream.cu): at most this many CTAs, and an error flag plus
 // completion counters in the first kHeadsCounterBytes at off_err (zeroed every call).
+// Hidden rows per pass of the tensor-core heads stream (more rows run in passes).
+constexpr int kHeadsMmaMaxRows = 128;
 constexpr int kHeadsStreamMaxGrid = 256;
 constexpr size_t kHeadsCounterBytes = 256;
 HeadsPlan plan_heads(int T, int d, int V, int K, int topk);

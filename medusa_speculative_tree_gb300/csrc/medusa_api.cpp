@@ -303,7 +303,7 @@ medusa_status medusa_heads_topk(const void* h, int32_t T, int32_t d, int32_t V, 
                                 int64_t w2_head_stride, const void* w_lm, int32_t topk,
                                 medusa_dtype dt, int32_t* root, int32_t* pool,
                                 float* logits_out, void* ws, size_t ws_bytes, void* stream) {
-  if (!h || !w_lm || !root || !ws || !dtype_ok(dt) || T < 1 || T > 64 || d < 8 || d % 8 != 0 ||
+  if (!h || !w_lm || !root || !ws || !dtype_ok(dt) || T < 1 || T > MEDUSA_MAX_HEAD_ROWS || d < 8 || d % 8 != 0 ||
       V < 1 || K < 0 || K > MEDUSA_MAX_DEPTH || topk < 1 || topk > MEDUSA_MAX_TOPK || topk > V ||
       w2_head_stride < 0)
     return MEDUSA_EINVAL;
