@@ -32,6 +32,7 @@
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <cmath>
 #include <cstdio>
 #include <cstdlib>
@@ -1085,20 +1086,69 @@ bool attn_tc_supported(const medusa_tree_t& t, int Hq, const medusa_kv_t& c) {
          kTcRows % g == 0 && encode_fn() != nullptr;
 }
 
-// Kernel shape and split choice.  With four or more query tiles per unit, one CTA
-// takes two of them (QT = 2, 128-key tiles, two stages: 192 KB of shared memory, one
-// CTA per SM), so that every K/V tile is copied and converted once for 256 rows and the
-// two tiles keep the tensor cores busy in turn.  Fewer query tiles run two CTAs per SM
-// (QT = 1, 64-key tiles, two stages), which overlaps one CTA's prologue and merge with
-// the other's main loop.  The splits: enough CTAs to fill the SM slots, in whole waves
-// where possible, with at most kMaxClusterSplits splits (one cluster) per unit and at
-// least rows/16 tiles of 64 keys per split.  The tree tiles count as work of split 0,
-// which takes that many fewer prefix tiles, so that the splits end together.
-// MEDUSA_ATTN_TC_SHAPE="QT,NS" (one of 1,2 / 1,4 / 2,2) overrides the shape.
+namespace {
+
+// Co-resident clusters of n CTAs of one kernel shape, from the occupancy calculator
+// (thread-block clusters live inside one GPC, so n CTAs that need a whole SM each fit
+// floor(SMs of the GPC / n) times per GPC); cached per shape and n.
+template <int QT, int NS>
+int max_clusters(int n, int D) {
+  static std::mutex mu;
+  static int cache[kMaxClusterSplits + 1] = {};
+  std::lock_guard<std::mutex> lock(mu);
+  if (cache[n] != 0) return cache[n];
+  const size_t smem = tc_smem_bytes<QT, NS>(D);
+  auto kern = attn_tc_kernel<false, QT, NS>;
+  int c = 0;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) == cudaSuccess) {
+    cudaLaunchConfig_t cfg = {};
+    cfg.gridDim = dim3(1, n, 1);
+    cfg.blockDim = dim3(TcCfg<QT, NS>::kThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 1;
+    attr[0].val.clusterDim.y = n;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    if (cudaOccupancyMaxActiveClusters(&c, kern, &cfg) != cudaSuccess) c = 0;
+  }
+  cudaGetLastError();                 // a failed query leaves no sticky error behind
+  cache[n] = c > 0 ? c : -1;
+  return cache[n];
+}
+
+int clusters_for(int qt, int stages, int n, int D) {
+  if (qt == 2) return max_clusters<2, 2>(n, D);
+  if (stages == 4) return max_clusters<1, 4>(n, D);
+  return max_clusters<1, 2>(n, D);
+}
+
+}  // namespace
+
+// Kernel shape and split choice.  With two or more row tiles per unit, one CTA takes
+// two of them (QT = 2, 128-key tiles, two stages: 192 KB of shared memory, one CTA
+// per SM), so that every K/V tile is copied and converted once for 256 rows and the
+// two tiles keep the tensor cores busy in turn.  A single row tile runs two CTAs per
+// SM (QT = 1, 64-key tiles, two stages), which overlaps one CTA's prologue and merge
+// with the other's main loop.
+// The number of splits n (one cluster of n CTAs per unit, n <= kMaxClusterSplits,
+// at least rows/16 keys' worth of tiles per split) minimises a time model measured on
+// GB300: a CTA costs F + T_t per tile (F: prologue, merge and launch; T_t: one tile;
+// QT = 1: 10 + 1.8 us per 64 keys, QT = 2: 15 + 2.2 us per 128 keys), and only
+// `clusters(n)` clusters run at once (occupancy calculator for one CTA per SM; with
+// two CTAs per SM, 2 x SMs / n).  One sequence: whole
+// waves of identical clusters.  Several sequences of unknown lengths (at most the
+// maximum prefix; taken as half of it on average): the longest split or the total
+// work over the cluster slots, whichever is larger.  The tree tiles count as work of
+// split 0, which takes that many fewer prefix tiles, so that the splits end together.
+// MEDUSA_ATTN_TC_SHAPE="QT,NS" (one of 1,2 / 1,4 / 2,2) overrides the shape and
+// MEDUSA_ATTN_TC_SPLITS=n the number of splits (at most the plan's maximum).
 void attn_tc_plan(AttnPlan& p) {
   const int M = p.N * p.g;
   const int n_tiles_q = (M + kTcRows - 1) / kTcRows;
-  int qt = n_tiles_q >= 4 ? 2 : 1, stages = 2;
+  int qt = n_tiles_q >= 2 ? 2 : 1, stages = 2;
   if (const char* e = std::getenv("MEDUSA_ATTN_TC_SHAPE")) {
     int a = 0, b = 0;
     if (std::sscanf(e, "%d,%d", &a, &b) == 2 && ((a == 1 && (b == 2 || b == 4)) || (a == 2 && b == 2))) {
@@ -1115,7 +1165,7 @@ void attn_tc_plan(AttnPlan& p) {
   const int units = p.B * p.Hkv * p.n_mt;
   int sms = 148, dev = 0;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  const double slots = (qt == 1 && stages == 2 ? 2.0 : 1.0) * sms;
+  const int per_sm = (qt == 1 && stages == 2) ? 2 : 1;
   const int tiles_unit = (p.max_prefix + KT - 1) / KT;
   const int n_tree = (p.N + KT - 1) / KT;
   const int rows = M < kTcRows ? M : kTcRows;
@@ -1124,13 +1174,30 @@ void attn_tc_plan(AttnPlan& p) {
   int max_split = tiles_unit / min_tiles;
   if (max_split > kMaxClusterSplits) max_split = kMaxClusterSplits;
   if (max_split < 1) max_split = 1;
+  const double F = qt == 2 ? 15.0 : 10.0, Tt = qt == 2 ? 2.2 : 1.8;
+  const int tiles = tiles_unit + n_tree;
   int best = 1;
-  double best_score = -1e9;
+  double best_t = 1e300;
   for (int n = 1; n <= max_split; ++n) {
-    const double waves = units * (double)n / slots;
-    const double eff = waves / std::ceil(waves);
-    const double score = eff - 0.004 * n;
-    if (score > best_score + 1e-9) { best_score = score; best = n; }
+    // Clusters of CTAs that need a whole SM are limited by the GPCs (occupancy
+    // calculator); with two CTAs per SM the clusters fill the SMs' second slots too,
+    // which the calculator does not count (measured: 32 clusters of 8 co-resident).
+    int cl = per_sm > 1 ? per_sm * sms / n : clusters_for(qt, stages, n, p.D);
+    if (cl < 1) cl = per_sm * sms / n;           // occupancy query unavailable: an estimate
+    if (cl < 1) cl = 1;
+    const double per_max = F + Tt * ((tiles + n - 1) / n);
+    double t;
+    if (p.B == 1) {
+      t = std::ceil(units / (double)cl) * per_max;
+    } else {
+      const double per_avg = F + Tt * std::ceil(0.5 * tiles / n);
+      t = std::max(per_max, units * per_avg / cl);
+    }
+    if (t <= best_t * (1.0 + 1e-9)) { best_t = t; best = n; }   // ties: more, smaller splits
+  }
+  if (const char* e = std::getenv("MEDUSA_ATTN_TC_SPLITS")) {   // tuning override
+    const int n = std::atoi(e);
+    if (n >= 1 && n <= max_split) best = n;
   }
   const int per = (tiles_unit + n_tree + best - 1) / best;
   int first_tiles = per - n_tree;
