@@ -20,6 +20,9 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
+constexpr int kLoads = 4;          // 16-byte loads in flight per thread in row_stats
+constexpr int kSelThreads = 1024;  // select: one warp per internal row, 32 rows at a time
+constexpr int kSelWarps = kSelThreads / 32;
 
 struct RowPart {
   float m;      // max of x / T over the chunk
@@ -100,12 +103,26 @@ __global__ void __launch_bounds__(kThreads) row_stats_kernel(medusa_tree_t t, in
   const bool vec = (reinterpret_cast<uintptr_t>(row + start) & 15u) == 0;
   int i = start;
   if (vec) {
+    // kLoads 16-byte loads per thread are issued before any is folded (a chunk is
+    // kLoads vectors per thread), so one memory round trip covers the chunk
     const int nvec = (end - start) / EPV;
     const uint4* rv = reinterpret_cast<const uint4*>(row + start);
-    for (int q = threadIdx.x; q < nvec; q += kThreads) {
-      float x[EPV];
-      Elem<EL>::unpack(__ldg(rv + q), x);
-      fold<TYP, EPV>(x, start + q * EPV, inv_temp, m, z, s1, av, ai);
+    for (int q0 = threadIdx.x; q0 < nvec; q0 += kThreads * kLoads) {
+      uint4 raw[kLoads];
+#pragma unroll
+      for (int l = 0; l < kLoads; ++l) {
+        const int q = q0 + l * kThreads;
+        raw[l] = q < nvec ? __ldg(rv + q) : make_uint4(0, 0, 0, 0);
+      }
+#pragma unroll
+      for (int l = 0; l < kLoads; ++l) {
+        const int q = q0 + l * kThreads;
+        if (q < nvec) {
+          float x[EPV];
+          Elem<EL>::unpack(raw[l], x);
+          fold<TYP, EPV>(x, start + q * EPV, inv_temp, m, z, s1, av, ai);
+        }
+      }
     }
     i = start + nvec * EPV;
   }
@@ -176,10 +193,10 @@ __global__ void __launch_bounds__(kThreads) guard_kernel(medusa_tree_t t, int V,
 // node the acceptance of its incoming edge and its log-probability; the retrieval
 // table when it fits.
 struct SelectSmem {
-  size_t off_lp, off_ok, off_ret, bytes;
-  bool ret_staged;
+  size_t off_lp, off_ok, off_ret, off_part, bytes;
+  bool ret_staged, part_staged;
 };
-inline SelectSmem select_smem(const medusa_tree_t& t) {
+inline SelectSmem select_smem(const medusa_tree_t& t, int n_chunks, bool guard) {
   SelectSmem L{};
   const size_t ni = t.n_internal > 0 ? t.n_internal : 1;
   L.off_lp = align_up(4 * ni * sizeof(float), 16);
@@ -187,12 +204,16 @@ inline SelectSmem select_smem(const medusa_tree_t& t) {
   L.off_ret = align_up(L.off_ok + (size_t)t.n_rows, 16);
   const size_t ret = (size_t)t.n_paths * (t.max_depth + 1) * sizeof(int32_t);
   L.ret_staged = L.off_ret + ret <= 96 * 1024;
-  L.bytes = L.ret_staged ? L.off_ret + ret : L.off_ret;
+  L.off_part = align_up(L.ret_staged ? L.off_ret + ret : L.off_ret, 16);
+  // the chunk statistics of every internal row (and their guard terms), when they fit
+  const size_t parts = ni * n_chunks * (sizeof(RowPart) + (guard ? sizeof(float) : 0));
+  L.part_staged = L.off_part + parts <= 160 * 1024;
+  L.bytes = L.part_staged ? L.off_part + parts : L.off_part;
   return L;
 }
 
 template <typename EL>
-__global__ void __launch_bounds__(kThreads) select_kernel(
+__global__ void __launch_bounds__(kSelThreads) select_kernel(
     medusa_tree_t t, int V, int n_chunks, const EL* __restrict__ logits,
     const int32_t* __restrict__ tokens, int mode, float inv_temp, float epsilon, float delta,
     const RowPart* __restrict__ part, const float* __restrict__ guard, SelectSmem lay,
@@ -213,26 +234,91 @@ __global__ void __launch_bounds__(kThreads) select_kernel(
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool typ = mode != MEDUSA_ACCEPT_GREEDY;
   const int32_t* tok = tokens + (int64_t)b * N;
+  // 0. the inputs of every edge parent(v) -> v (a thread's edges are v = 1 + tid +
+  //    k kSelThreads, k < kEdges since N <= MEDUSA_MAX_ROWS): parent, its internal row,
+  //    the candidate token and (typical) its raw logit, all requested up front so that
+  //    their latency overlaps the statistics below.
+  constexpr int kEdges = (MEDUSA_MAX_ROWS + kSelThreads - 1) / kSelThreads;
+  int e_ii[kEdges], e_ct[kEdges];
+  float e_x[kEdges];
+  {
+    int e_u[kEdges];
+#pragma unroll
+    for (int k = 0; k < kEdges; ++k) {
+      const int v = 1 + threadIdx.x + k * kSelThreads;
+      e_u[k] = v < N ? t.parent[v] : 0;
+      e_ct[k] = v < N ? tok[v] : -1;
+    }
+#pragma unroll
+    for (int k = 0; k < kEdges; ++k) {
+      const int v = 1 + threadIdx.x + k * kSelThreads;
+      e_ii[k] = v < N ? t.internal_index[e_u[k]] : 0;
+      const bool need = typ && v < N && e_ct[k] >= 0 && e_ct[k] < V;
+      e_x[k] = need ? Elem<EL>::load(logits, ((int64_t)b * N + e_u[k]) * V + e_ct[k]) * inv_temp : 0.f;
+    }
+  }
   // 1. merged statistics per internal row (one warp per row, one lane per chunk) and
-  //    the retrieval table into shared memory
+  //    the retrieval table into shared memory.  The chunk statistics of every row are
+  //    staged first, four loads per thread in flight, so that the per-row merges do
+  //    not wait on global memory one row after another.
   if (lay.ret_staged)
-    for (int i = threadIdx.x; i < t.n_paths * W; i += kThreads) s_ret[i] = t.retrieve[i];
-  for (int ii = warp; ii < NI; ii += kWarps) {
-    const RowPart* rp = part + (((int64_t)b * NI) + ii) * n_chunks;
+    for (int i = threadIdx.x; i < t.n_paths * W; i += kSelThreads) s_ret[i] = t.retrieve[i];
+  const RowPart* part_b = part + (int64_t)b * NI * n_chunks;
+  const float* guard_b = guard ? guard + (int64_t)b * NI * n_chunks : nullptr;
+  if (lay.part_staged) {
+    RowPart* sp = reinterpret_cast<RowPart*>(smem_sel + lay.off_part);
+    float* sg = reinterpret_cast<float*>(sp + NI * n_chunks);
+    const int np = NI * n_chunks;
+    for (int i0 = threadIdx.x; i0 < np; i0 += 4 * kSelThreads) {
+      RowPart q[4];
+      float g4[4];
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int i = i0 + r * kSelThreads;
+        if (i < np) {
+          q[r] = part_b[i];
+          g4[r] = guard_b ? guard_b[i] : 0.f;
+        }
+      }
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const int i = i0 + r * kSelThreads;
+        if (i < np) {
+          sp[i] = q[r];
+          if (guard_b) sg[i] = g4[r];
+        }
+      }
+    }
+    part_b = sp;
+    if (guard_b) guard_b = sg;
+    __syncthreads();
+  }
+  for (int ii = warp; ii < NI; ii += kSelWarps) {
+    const RowPart* rp = part_b + (int64_t)ii * n_chunks;
     float m = -INFINITY, z = 0.f, s1 = 0.f, av = -INFINITY, g = 0.f;
     int ai = INT_MAX;
     for (int c = lane; c < n_chunks; c += 32) {
       const RowPart q = rp[c];
-      merge_stats(m, z, s1, q.m, q.z, q.s1);
+      if (typ) merge_stats(m, z, s1, q.m, q.z, q.s1);
       if (ranks_before(q.amax_v, q.amax_i, av, ai)) { av = q.amax_v; ai = q.amax_i; }
-      if (guard) g += guard[(((int64_t)b * NI) + ii) * n_chunks + c];
+      if (guard_b) g += guard_b[(int64_t)ii * n_chunks + c];
     }
+    if (typ) {
 #pragma unroll
-    for (int o = 16; o > 0; o >>= 1) shfl_merge(m, z, s1, av, ai, o);
-    if (guard) g = warp_sum(g);
-    if (lane == 0) {
+      for (int o = 16; o > 0; o >>= 1) shfl_merge(m, z, s1, av, ai, o);
+    } else {                                        // greedy needs the argmax only
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        const float ov = __shfl_xor_sync(0xffffffffu, av, o);
+        const int oi = __shfl_xor_sync(0xffffffffu, ai, o);
+        if (ranks_before(ov, oi, av, ai)) { av = ov; ai = oi; }
+      }
+    }
+    if (guard_b) g = warp_sum(g);
+    if (lane == 0 && !typ) s_am[ii] = ai;
+    if (lane == 0 && typ) {
       const float lz = logf(z);
-      const float H = guard ? g : lz - s1 / z;     // -sum p ln p = ln Z - sum p (x/T - m)
+      const float H = guard_b ? g : lz - s1 / z;   // -sum p ln p = ln Z - sum p (x/T - m)
       s_m[ii] = m;
       s_lz[ii] = lz;
       s_tau[ii] = fminf(epsilon, delta * expf(-H));
@@ -241,18 +327,18 @@ __global__ void __launch_bounds__(kThreads) select_kernel(
   }
   __syncthreads();
   // 2. every edge parent(v) -> v at once: accepted? and log p_parent(token of v)
-  for (int v = 1 + threadIdx.x; v < N; v += kThreads) {
-    const int u = t.parent[v];
-    const int ii = t.internal_index[u];
-    const int ct = tok[v];
+#pragma unroll
+  for (int k = 0; k < kEdges; ++k) {
+    const int v = 1 + threadIdx.x + k * kSelThreads;
+    if (v >= N) break;
+    const int ii = e_ii[k], ct = e_ct[k];
     bool ok = false;
     float lp = 0.f;
     if (ct >= 0 && ct < V) {                     // else: not a vocabulary id, never accepted
       if (!typ) {
         ok = ct == s_am[ii];
       } else {
-        const float x = Elem<EL>::load(logits, ((int64_t)b * N + u) * V + ct) * inv_temp;
-        lp = x - s_m[ii] - s_lz[ii];
+        lp = e_x[k] - s_m[ii] - s_lz[ii];
         ok = expf(lp) > s_tau[ii];
       }
     }
@@ -263,7 +349,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(
   // 3. every retrieval path: accepted prefix length and its log-probability
   int best_p = INT_MAX, best_a = -1;
   float best_s = -INFINITY;
-  for (int p = threadIdx.x; p < t.n_paths; p += kThreads) {
+  for (int p = threadIdx.x; p < t.n_paths; p += kSelThreads) {
     const int32_t* r = lay.ret_staged ? s_ret + p * W : t.retrieve + (int64_t)p * W;
     int a = 0;
     float score = 0.f;
@@ -278,8 +364,8 @@ __global__ void __launch_bounds__(kThreads) select_kernel(
     if (take) { best_a = a; best_s = score; best_p = p; }
   }
   // 3. block arg-best over paths
-  __shared__ int r_a[kWarps], r_p[kWarps];
-  __shared__ float r_s[kWarps];
+  __shared__ int r_a[kSelWarps], r_p[kSelWarps];
+  __shared__ float r_s[kSelWarps];
   auto better = [&](int a1, float s1, int p1, int a2, float s2, int p2) {
     if (a1 != a2) return a1 > a2;
     if (mode != MEDUSA_ACCEPT_GREEDY && s1 != s2) return s1 > s2;
@@ -295,7 +381,7 @@ __global__ void __launch_bounds__(kThreads) select_kernel(
   if (lane == 0) { r_a[warp] = best_a; r_s[warp] = best_s; r_p[warp] = best_p; }
   __syncthreads();
   if (threadIdx.x == 0) {
-    for (int w = 1; w < kWarps; ++w)
+    for (int w = 1; w < kSelWarps; ++w)
       if (better(r_a[w], r_s[w], r_p[w], best_a, best_s, best_p)) {
         best_a = r_a[w]; best_s = r_s[w]; best_p = r_p[w];
       }
@@ -317,7 +403,7 @@ AcceptPlan plan_accept(const medusa_tree_t& t, int B, int V) {
   AcceptPlan p{};
   p.B = B;
   p.V = V;
-  int chunk = 4096;
+  int chunk = kThreads * kLoads * 8;                      // bf16: 8 per 16-byte vector
   if (V < chunk) chunk = (V + 255) / 256 * 256;
   p.chunk = chunk;
   p.n_chunks = (V + chunk - 1) / chunk;
@@ -353,18 +439,18 @@ cudaError_t launch_accept(const AcceptPlan& p, const medusa_tree_t& t, const voi
     }
   }
   const float* gptr = (entropy_guard && typ) ? guard : nullptr;
-  const SelectSmem lay = select_smem(t);
+  const SelectSmem lay = select_smem(t, p.n_chunks, gptr != nullptr);
   cudaError_t e;
   if (bf) {
     e = cudaFuncSetAttribute(select_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lay.bytes);
     if (e != cudaSuccess) return e;
-    select_kernel<uint16_t><<<p.B, kThreads, lay.bytes, st>>>(t, p.V, p.n_chunks, (const uint16_t*)logits, tokens,
+    select_kernel<uint16_t><<<p.B, kSelThreads, lay.bytes, st>>>(t, p.V, p.n_chunks, (const uint16_t*)logits, tokens,
                                                               mode, inv_t, epsilon, delta, part, gptr, lay, best_path,
                                                               accept_len, out_tokens, out_rows, frontier_row);
   } else {
     e = cudaFuncSetAttribute(select_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lay.bytes);
     if (e != cudaSuccess) return e;
-    select_kernel<float><<<p.B, kThreads, lay.bytes, st>>>(t, p.V, p.n_chunks, (const float*)logits, tokens, mode,
+    select_kernel<float><<<p.B, kSelThreads, lay.bytes, st>>>(t, p.V, p.n_chunks, (const float*)logits, tokens, mode,
                                                            inv_t, epsilon, delta, part, gptr, lay, best_path,
                                                            accept_len, out_tokens, out_rows, frontier_row);
   }
