@@ -324,6 +324,15 @@ __device__ __forceinline__ void merge_lists(int n, int kk, Load load, float* out
   }
 }
 
+// Orderable 64-bit key of a candidate: a larger key ranks before (higher value, then
+// lower id); -0 counts as +0, as in ranks_before.
+__device__ __forceinline__ unsigned long long rank_key(float v, int i) {
+  if (v == 0.f) v = 0.f;
+  const uint32_t b = __float_as_uint(v);
+  const uint32_t ord = (b & 0x80000000u) ? ~b : (b | 0x80000000u);
+  return ((unsigned long long)ord << 32) | (0xFFFFFFFFu - (uint32_t)i);
+}
+
 __global__ void __launch_bounds__(kThreads) topk_rows_kernel(const float* __restrict__ logits, int V, int topk,
                                                              int Kp1, int span, Cand* __restrict__ cand,
                                                              int* __restrict__ tick, int32_t* __restrict__ root,
@@ -333,6 +342,12 @@ __global__ void __launch_bounds__(kThreads) topk_rows_kernel(const float* __rest
   __shared__ float mv[32];
   __shared__ int mi[32];
   __shared__ int last;
+  // The best k-th entry over the warps' lists: every warp's k-th entry is beaten by k
+  // values of the span, so no value that does not beat the best of them is in the
+  // span's top k.  Warps publish theirs (atomicMax of rank_key) and filter by it.
+  __shared__ unsigned long long s_thr;
+  if (threadIdx.x == 0) s_thr = 0ull;
+  __syncthreads();
   const int row = blockIdx.y, c = blockIdx.x, ns = gridDim.x;
   const int t = row / Kp1, m = row % Kp1;
   const int kk = m == 0 ? 1 : topk;
@@ -345,6 +360,7 @@ __global__ void __launch_bounds__(kThreads) topk_rows_kernel(const float* __rest
   // refreshed only after an insertion.
   float tv = -INFINITY;
   int ti = INT_MAX;
+  unsigned long long own = 0ull;  // rank_key of (tv, ti) once the list is full
   bool filled = false;            // warp-uniform: the list has been seeded
   // warp w scans part of [c_lo, c_hi); 128 values per step as one float4 per lane when
   // rows are 16-byte aligned (span is a multiple of 128 then)
@@ -369,10 +385,16 @@ __global__ void __launch_bounds__(kThreads) topk_rows_kernel(const float* __rest
       li = lane < kk ? si : INT_MAX;
       tv = __shfl_sync(0xffffffffu, lv, kk - 1);
       ti = __shfl_sync(0xffffffffu, li, kk - 1);
+      if (ti != INT_MAX) {
+        own = rank_key(tv, ti);
+        if (lane == 0) atomicMax(&s_thr, own);
+      }
       filled = true;
       return;
     }
-    unsigned cm = __ballot_sync(0xffffffffu, valid && ranks_before(v, i, tv, ti));
+    const unsigned long long shared_thr = *reinterpret_cast<volatile unsigned long long*>(&s_thr);
+    const unsigned long long thr = own > shared_thr ? own : shared_thr;
+    unsigned cm = __ballot_sync(0xffffffffu, valid && rank_key(v, i) > thr && ranks_before(v, i, tv, ti));
     if (cm) {
       do {
         const int sl = __ffs(cm) - 1;
@@ -381,26 +403,65 @@ __global__ void __launch_bounds__(kThreads) topk_rows_kernel(const float* __rest
       } while (cm);
       tv = __shfl_sync(0xffffffffu, lv, kk - 1);
       ti = __shfl_sync(0xffffffffu, li, kk - 1);
+      if (ti != INT_MAX) {
+        own = rank_key(tv, ti);
+        if (lane == 0) atomicMax(&s_thr, own);
+      }
     }
   };
   if ((V & 3) == 0) {
-    // kBatch float4 per lane are loaded before any is offered: one memory round trip
-    // per 128 kBatch values of the warp
-    constexpr int kBatch = 4;
-    for (int base = c_lo + 128 * warp; base < c_hi; base += 128 * kWarps * kBatch) {
-      float4 q[kBatch];
+    // Chunks of 32 values per lane (eight float4, all loaded before any is used).  The
+    // k-th largest of the 32 lanes' maxima bounds the chunk's k-th best from below (k
+    // distinct values reach it), so only values at or above it can enter the list:
+    // about k per chunk instead of every value that beats a fresh list's threshold.
+    constexpr int kVec = 8;
+    filled = true;                 // the lists start empty: the bound seeds them
+    for (int base = c_lo + 128 * warp; base < c_hi; base += 128 * kWarps * kVec) {
+      float x[4 * kVec];
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
+      for (int u = 0; u < kVec; ++u) {
         const int i0 = base + 128 * kWarps * u + 4 * lane;
-        q[u] = i0 < c_hi ? __ldg(reinterpret_cast<const float4*>(src + i0)) : make_float4(0.f, 0.f, 0.f, 0.f);
+        const float4 q = i0 < c_hi ? __ldg(reinterpret_cast<const float4*>(src + i0))
+                                   : make_float4(-INFINITY, -INFINITY, -INFINITY, -INFINITY);
+        x[4 * u] = q.x; x[4 * u + 1] = q.y; x[4 * u + 2] = q.z; x[4 * u + 3] = q.w;
       }
+      float lm = -INFINITY;
 #pragma unroll
-      for (int u = 0; u < kBatch; ++u) {
-        const int i0 = base + 128 * kWarps * u + 4 * lane;
-        offer(q[u].x, i0, i0 < c_hi);
-        offer(q[u].y, i0 + 1, i0 + 1 < c_hi);
-        offer(q[u].z, i0 + 2, i0 + 2 < c_hi);
-        offer(q[u].w, i0 + 3, i0 + 3 < c_hi);
+      for (int e = 0; e < 4 * kVec; ++e) lm = fmaxf(lm, x[e]);
+      // k-th largest lane maximum: bitonic sort of the 32 maxima, largest first
+#pragma unroll
+      for (int k = 2; k <= 32; k <<= 1)
+#pragma unroll
+        for (int j = k >> 1; j > 0; j >>= 1) {
+          const float o = __shfl_xor_sync(0xffffffffu, lm, j);
+          const bool best_first = (lane & k) == 0 || k == 32;
+          const bool lower = (lane & j) == 0;
+          lm = (lower == best_first) ? fmaxf(lm, o) : fminf(lm, o);
+        }
+      const float bound = __shfl_sync(0xffffffffu, lm, kk - 1);
+#pragma unroll
+      for (int e = 0; e < 4 * kVec; ++e) {
+        const int id = base + 128 * kWarps * (e >> 2) + 4 * lane + (e & 3);
+        unsigned cm = __ballot_sync(0xffffffffu, x[e] >= bound && id < c_hi);
+        if (cm) {
+          const unsigned long long shared_thr = *reinterpret_cast<volatile unsigned long long*>(&s_thr);
+          const unsigned long long thr = own > shared_thr ? own : shared_thr;
+          cm = __ballot_sync(0xffffffffu, ((cm >> lane) & 1u) && rank_key(x[e], id) > thr &&
+                                              ranks_before(x[e], id, tv, ti));
+          if (cm) {
+            do {
+              const int sl = __ffs(cm) - 1;
+              cm &= cm - 1;
+              topk_insert(__shfl_sync(0xffffffffu, x[e], sl), __shfl_sync(0xffffffffu, id, sl), kk, lv, li);
+            } while (cm);
+            tv = __shfl_sync(0xffffffffu, lv, kk - 1);
+            ti = __shfl_sync(0xffffffffu, li, kk - 1);
+            if (ti != INT_MAX) {
+              own = rank_key(tv, ti);
+              if (lane == 0) atomicMax(&s_thr, own);
+            }
+          }
+        }
       }
     }
   } else {
