@@ -256,6 +256,8 @@ class Round:
 # DRAM bytes (read + write) of one heads launch, from an ncu capture of the current
 # kernel on that workload; absent for workloads not captured.
 HEADS_TRAFFIC = {"vicuna7b-64": 1_445_265_000 + 4_523_008}
+# the same for the attention launch (dram__bytes_read.sum + dram__bytes_write.sum)
+ATTN_TRAFFIC = {"vicuna7b-64": 35_210_752 + 0}
 
 
 def heads_all_rows(rd, stream, peak_tflops):
@@ -525,7 +527,8 @@ def main():
                          "algorithmic_bytes": rd.head_bytes(), "launch_us": heads_us},
             "heads_all_rows": all_rows,
             "tree_attn_roofline": {"kernel": "medusa_tree_attn_verify", "bound": "hbm", "achieved": attn_gbs,
-                                   "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm, "traffic": None,
+                                   "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm,
+                                   "traffic": ATTN_TRAFFIC.get(w.name),
                                    "peak_source": src, "algorithmic_bytes": rd.attn_bytes()},
             "cpu_baseline": cpu,
             "e2e": {"value": 1e3 * e2e_ms / ws, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
