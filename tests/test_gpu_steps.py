@@ -173,6 +173,20 @@ def test_attn_paged_batch(m):
     attn_case(m, w, otree.greedy_tree(acc, 63), synth.prefix_lengths(w), paged=True, fill_tail=float("nan"))
 
 
+@pytest.mark.parametrize("shape", ["1,2", "1,4", "2,2"])
+@pytest.mark.parametrize("splits", [1, 2, 3, 5, 8])
+def test_attn_every_shape_and_split_count(m, monkeypatch, shape, splits):
+    """The tensor-core kernel in each of its shapes (query tiles per CTA, stages) and at
+    several split counts, on a paged GQA batch of ragged lengths with a NaN tail: the
+    splits' cluster merge and the per-sequence spreading of tiles over them."""
+    monkeypatch.setenv("MEDUSA_ATTN_TC_SHAPE", shape)
+    monkeypatch.setenv("MEDUSA_ATTN_TC_SPLITS", str(splits))
+    w = synth.small_variant(synth.WORKLOADS["serving-b16-paged"], batch=3, seed=700 + splits)
+    acc = synth.rank_accuracy(4, 10)
+    lengths = np.array([1337, 3, 650])   # 21 / 1 / 11 tiles of 64 keys: some splits get none
+    attn_case(m, w, otree.greedy_tree(acc, 63), lengths, paged=True, fill_tail=float("nan"))
+
+
 def test_attn_head_dim_64_bf16(m):
     w = synth.small_variant(synth.WORKLOADS["vicuna7b-64"], n_q_heads=8, n_kv_heads=2, head_dim=64,
                             prefix_len=513, seed=61)
