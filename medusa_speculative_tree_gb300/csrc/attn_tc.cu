@@ -67,12 +67,11 @@ struct TcArgs {
   float* out;
   float* lse;
   int32_t* status;
-  int Hq, Hkv, g, n_mt, n_split, chunk, first;
+  int B, Hq, Hkv, g, n_mt, n_split, chunk, first;
   float scale_log2;
   float th_hi[64], th_lo[64];
 };
 
-// 2^x on the MUFU unit (ex2.approx, relative error ~2^-22); 2^-inf = +0.
 // Eight non-blocking phase tests in one round trip: all tests are issued before any
 // result is used.  Bit i of the result: phase parity p[i] of barrier b[i] has completed.
 __device__ __forceinline__ uint32_t mbar_test8(const uint32_t (&b)[8], const uint32_t (&p)[8]) {
@@ -104,6 +103,7 @@ __device__ __forceinline__ float fmax3(float a, float b, float c) {
   return d;
 }
 
+// 2^x on the MUFU unit (ex2.approx, relative error ~2^-22); 2^-inf = +0.
 __device__ __forceinline__ float fast_exp2(float x) {
   float y;
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
@@ -290,7 +290,25 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
   __shared__ int abort_flag;
 
   const int ct_idx = blockIdx.x, s = blockIdx.y;     // ct_idx: which QT row tiles
-  const int b = blockIdx.z / a.Hkv, kvh = blockIdx.z % a.Hkv;
+  // Units of longer sequences start first (longest-processing-time order, which packs
+  // the SMs better when the prefix lengths differ): blockIdx.z / Hkv counts the
+  // sequences by decreasing length, ties by index.  Thread t < B ranks sequence t.
+  __shared__ int sel_b;
+  const int kvh = blockIdx.z % a.Hkv;
+  int b = blockIdx.z / a.Hkv;
+  if (a.B > 1 && a.B <= C::kThreads) {
+    if (threadIdx.x < a.B) {
+      const int Lt = a.L[threadIdx.x];
+      int rank = 0;
+      for (int o = 0; o < a.B; ++o) {
+        const int Lo = a.L[o];
+        rank += (Lo > Lt || (Lo == Lt && o < (int)threadIdx.x)) ? 1 : 0;
+      }
+      if (rank == b) sel_b = threadIdx.x;
+    }
+    __syncthreads();
+    b = sel_b;
+  }
   const int N = t.n_rows, g = a.g, M = N * g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int Lb = a.L[b];
@@ -1257,6 +1275,7 @@ cudaError_t launch_attn_tc(const AttnPlan& p, const medusa_tree_t& t, const void
   a.lse = lse;
   a.status = status;
   (void)ws;                                        // the cluster merge needs no workspace
+  a.B = p.B;
   a.Hq = p.Hq;
   a.Hkv = p.Hkv;
   a.g = p.g;
