@@ -109,6 +109,40 @@ def test_heads_full_size_sampled(m, name):
     torch.cuda.empty_cache()
 
 
+@pytest.mark.parametrize("name", ["llama3-8b-256", "longctx-341"])
+def test_heads_all_rows_full_size_sampled(m, name):
+    """The all-rows variant (every tree row a hidden row: 256 and 341 rows, two and
+    three tensor-core passes) on the full weights: sampled logits of rows in every
+    pass against the fp64 oracle, and the top-k of every sampled row exact on the
+    kernel's own logits."""
+    w = synth.WORKLOADS[name]
+    t_o, _, _ = templates(m, w)
+    T = t_o.n_rows
+    _, w1, w2, w_lm = synth.head_weights(w, device="cuda")
+    h = synth.normal((T, w.hidden), 1.0, w.seed, "h", "cuda", w.torch_dtype, sub=1)
+    logits = torch.empty((T, w.n_heads + 1, w.vocab), dtype=torch.float32, device="cuda")
+    root, pool = m.medusa_heads_topk(h, w1, w2, w_lm, w.topk, logits_out=logits)
+    torch.cuda.synchronize()
+    rng = np.random.default_rng(11)
+    root, pool = root.cpu().numpy(), pool.cpu().numpy()
+    for t in [0, 127, 128, T - 1]:
+        rows = []
+        for mm in range(w.n_heads + 1):
+            ids = list(rng.integers(0, w.vocab, size=8))
+            ids += [int(root[t])] if mm == 0 else [int(x) for x in pool[t, mm - 1]]
+            rows += [(mm, int(i)) for i in ids]
+        want = oheads.head_logit_rows(gu.to64(h[t]), lambda kk: gu.to64(w1[kk]),
+                                      lambda kk, vv: gu.to64(w2[kk, vv]), lambda vv: gu.to64(w_lm[vv]), rows)
+        got = np.array([float(logits[t, mm, v]) for mm, v in rows])
+        gu.float_parity(got, want, False, f"{name} all-rows sampled head logits, row {t}")
+        gl = logits[t].cpu().numpy().astype(np.float64)
+        assert root[t] == np.lexsort((np.arange(w.vocab), -gl[0]))[0]
+        for k in range(w.n_heads):
+            assert list(pool[t, k]) == list(np.lexsort((np.arange(w.vocab), -gl[1 + k]))[:w.topk])
+    del w1, w2, w_lm, logits
+    torch.cuda.empty_cache()
+
+
 @pytest.mark.parametrize("name", synth.WORKLOAD_ORDER)
 def test_attention_full_size_sampled(m, name):
     w = synth.WORKLOADS[name]
