@@ -238,7 +238,8 @@ class Round:
         w = self.w
         bf16 = w.dtype == "bf16"
         T = w.batch
-        if bf16 and T == 1 and w.hidden % 256 == 0 and w.hidden <= 4096 and w.n_heads >= 1:
+        stream_d = (w.hidden <= 4096 and w.hidden % 256 == 0) or (w.hidden <= 8192 and w.hidden % 512 == 0)
+        if bf16 and T == 1 and stream_d and w.n_heads >= 1:
             heads = 1                                   # one persistent weight stream with top-k
         elif bf16 and T >= 2 and w.hidden % 64 == 0 and w.n_heads >= 1:
             heads = 2 * math.ceil(T / 128) + 1         # per pass of <= 128 rows: input pairs and

@@ -22,6 +22,13 @@
 //     per-warp top-k list kept sorted across the warp's lanes (value desc, id asc);
 //   - warp 9 merges the 8 warp lists of a matrix into the CTA's top-k and publishes
 //     it; the CTA that completes a matrix merges all CTAs' lists into root or pool.
+// Rows longer than 8 KiB (4096 < d <= 8192) are split in two halves (SPLIT = 2): a
+// group is then 4 rows, warps 0-3 dot the first halves and own the rows, warps 4-7 dot
+// the second halves against the second half of the input row and hand their partial
+// sums to the owners through shared memory, so that every warp still holds at most
+// 4096 input elements in registers and a stage still holds 64 KiB of 8 KiB segments.
+// (Quarter rows, 2 rows per group in 5 stages of 32 KiB, measured 1.6x slower: the
+// per-group overheads of 4 KiB segments dominate.)
 // All waits are bounded; on a timeout the call records an error and root / pool
 // become -1.
 #include <float.h>
@@ -34,11 +41,12 @@ namespace medusa {
 
 namespace {
 
-constexpr int kSConsumers = 8;                 // consumer warps = rows per group
+constexpr int kSConsumers = 8;                 // consumer warps = row parts per group
 constexpr int kSProducer = 8;                  // warp index
 constexpr int kSMerger = 9;                    // warp index
 constexpr int kSThreads = 10 * 32;
-constexpr int kSStages = 3;
+// stages of the ring: 3 x 64 KiB, with whole rows or halves
+__host__ __device__ constexpr int stream_stages(int) { return 3; }
 constexpr int kSMaxU4 = 16;                    // 16-byte pieces of a row per lane (d <= 4096)
 constexpr int kSMaxGrid = kHeadsStreamMaxGrid;
 
@@ -137,44 +145,53 @@ __device__ __forceinline__ void list_insert(float v, int id, int kk, float& lv, 
 }
 
 // 10 warps: the register file is shared as if by 12, 168 registers each; the input
-// row takes 128 of them.
+// row (or its half) takes 128 of them.
+template <int SPLIT>
 __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const StreamArgs a) {
-  extern __shared__ __align__(1024) uint8_t smem_s[];
+  extern __shared__ __align__(16) uint8_t smem_s[];        // (bulk copies need 16 bytes)
+  constexpr int RPG = kSConsumers / SPLIT;                 // rows per group (= owner warps)
+  constexpr int NSTG = stream_stages(SPLIT);
   const int d = a.d, K = a.K, V = a.V;
-  const int seg = 2 * d;                                    // bytes of one row
+  const int dp = d / SPLIT;                                 // elements of one row part
+  const int seg = 2 * dp;                                   // bytes of one row part
   const int u4c = seg / 512;                                // 16-byte pieces per lane (<= 16)
   uint8_t* ring = smem_s;                                  // [stages][8][seg]
-  uint8_t* xbuf = ring + kSStages * kSConsumers * seg;      // input row of the current matrix (h bf16 or z_k fp32)
-  SCand* lists = reinterpret_cast<SCand*>(xbuf + 4 * d);   // [2][consumers][32]
-  uint64_t* bars = reinterpret_cast<uint64_t*>(lists + 2 * kSConsumers * 32);
+  uint8_t* xbuf = ring + NSTG * kSConsumers * seg;      // input row of the current matrix (h bf16 or z_k fp32)
+  SCand* lists = reinterpret_cast<SCand*>(xbuf + 4 * d);   // [2][owners][32]
+  float* partial = reinterpret_cast<float*>(lists + 2 * RPG * 32);   // [2][stages][parts - 1][RPG] part sums
+  uint64_t* bars = reinterpret_cast<uint64_t*>(
+      (reinterpret_cast<uintptr_t>(partial + 2 * NSTG * (SPLIT - 1) * RPG) + 7) & ~uintptr_t(7));
   __shared__ int abort_flag;
-  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[kSStages]);
-  const uint32_t lfull0 = smem_u32(&bars[2 * kSStages]), lfree0 = smem_u32(&bars[2 * kSStages + 2]);
-  const uint32_t xfull = smem_u32(&bars[2 * kSStages + 4]), xempty = smem_u32(&bars[2 * kSStages + 5]);
+  const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[NSTG]);
+  const uint32_t lfull0 = smem_u32(&bars[2 * NSTG]), lfree0 = smem_u32(&bars[2 * NSTG + 2]);
+  const uint32_t xfull = smem_u32(&bars[2 * NSTG + 4]), xempty = smem_u32(&bars[2 * NSTG + 5]);
+  const uint32_t pdone0 = smem_u32(&bars[2 * NSTG + 6]);      // [stages] other parts summed
   const volatile int* abortp = &abort_flag;
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = gridDim.x, c = blockIdx.x;
   Layout L;
   L.K = K;
-  L.g1 = (d + kSConsumers - 1) / kSConsumers;
-  L.gv = (V + kSConsumers - 1) / kSConsumers;
+  L.g1 = (d + RPG - 1) / RPG;
+  L.gv = (V + RPG - 1) / RPG;
   L.ga = L.gv / 2;
   const int n_items = L.total();
-  __shared__ int stage_item[kSStages];                      // group in each stage, -1 = no more
+  __shared__ int stage_item[NSTG];                      // group in each stage, -1 = no more
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
-    for (int s = 0; s < kSStages; ++s) {
+    for (int s = 0; s < NSTG; ++s) {
       mbar_init(full0 + 8 * s, 1);
       mbar_init(empty0 + 8 * s, kSConsumers);
     }
     for (int p = 0; p < 2; ++p) {
-      mbar_init(lfull0 + 8 * p, kSConsumers);
+      mbar_init(lfull0 + 8 * p, RPG);
       mbar_init(lfree0 + 8 * p, 1);
     }
     mbar_init(xfull, 1);
     mbar_init(xempty, kSConsumers);
+    if (SPLIT > 1)
+      for (int s = 0; s < NSTG; ++s) mbar_init(pdone0 + 8 * s, kSConsumers - RPG);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
@@ -190,8 +207,8 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
     int slot = 0, x_loads = 0, x_src = -2;
     bool z_ready = false;
     auto take_slot = [&](int& s) -> bool {
-      s = slot % kSStages;
-      return s_wait(empty0 + 8 * s, (uint32_t)(((slot / kSStages) & 1) ^ 1), abortp);
+      s = slot % NSTG;
+      return s_wait(empty0 + 8 * s, (uint32_t)(((slot / NSTG) & 1) ^ 1), abortp);
     };
     int next = atomicAdd(&a.cnt[K + 2], 1);
     for (;;) {
@@ -242,17 +259,18 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
       const uint16_t* base = it.kind == 0 ? a.w1 + (int64_t)it.k * d * d
                            : it.kind == 1 ? a.w_lm : a.w2 + (int64_t)it.k * a.w2_stride;
       const int n_rows = it.kind == 0 ? d : V;
-      const int row0 = it.grp * kSConsumers;
-      const int rows = min(kSConsumers, n_rows - row0);
-      mbar_expect_tx(full0 + 8 * s, (uint32_t)(rows * seg));
-      for (int r = 0; r < rows; ++r)
-        bulk_copy_g2s(smem_u32(ring + (s * kSConsumers + r) * seg), base + (int64_t)(row0 + r) * d, (uint32_t)seg,
-                      full0 + 8 * s);
+      const int row0 = it.grp * RPG;
+      const int rows = min(RPG, n_rows - row0);
+      mbar_expect_tx(full0 + 8 * s, (uint32_t)(rows * SPLIT * seg));
+      for (int h = 0; h < SPLIT; ++h)                       // slot h * RPG + r: part h of row r
+        for (int r = 0; r < rows; ++r)
+          bulk_copy_g2s(smem_u32(ring + (s * kSConsumers + h * RPG + r) * seg),
+                        base + (int64_t)(row0 + r) * d + (int64_t)h * dp, (uint32_t)seg, full0 + 8 * s);
       ++slot;
     }
     // Copies still in flight (only after giving up) must land before the CTA exits.
-    for (int n = slot - kSStages; n < slot; ++n)
-      if (n >= 0) mbar_wait(full0 + 8 * (n % kSStages), (uint32_t)((n / kSStages) & 1), 100000000ull);
+    for (int n = slot - NSTG; n < slot; ++n)
+      if (n >= 0) mbar_wait(full0 + 8 * (n % NSTG), (uint32_t)((n / NSTG) & 1), 100000000ull);
     if (x_loads > 0) mbar_wait(xfull, (uint32_t)((x_loads - 1) & 1), 100000000ull);
     return;
   }
@@ -274,16 +292,16 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
       }
       SCand* out = a.scand + ((int64_t)t * G + c) * a.topk;
       if (ok) {
-        // one sorted list of kk entries per consumer warp: entry e of warp w at lists[p][w][e]
+        // one sorted list of kk entries per owner warp: entry e of warp w at lists[p][w][e]
         float ev[8];
         int ei[8];
 #pragma unroll
         for (int q = 0; q < 8; ++q) {
           const int f = lane + 32 * q;                  // flattened index w * kk + e
           const int w = f / kk, e = f % kk;
-          const bool valid = f < kSConsumers * kk;
-          ev[q] = valid ? lists[(p * kSConsumers + w) * 32 + e].v : -INFINITY;
-          ei[q] = valid ? lists[(p * kSConsumers + w) * 32 + e].i : INT_MAX;
+          const bool valid = f < RPG * kk;
+          ev[q] = valid ? lists[(p * RPG + w) * 32 + e].v : -INFINITY;
+          ei[q] = valid ? lists[(p * RPG + w) * 32 + e].i : INT_MAX;
         }
         __syncwarp();
         if (lane == 0) mbar_arrive(lfree0 + 8 * p);     // the lists buffer may be refilled
@@ -372,8 +390,11 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
   }
 
   // ---- consumer warps: one row of each group ------------------------------------------
-  const int nv = d / 256;                                   // 16-byte pieces per lane
-  float2 xr[kSMaxU4][4];                                    // input row, element pairs
+  const int nv = dp / 256;                                  // 16-byte pieces per lane
+  const int part = SPLIT == 1 ? 0 : warp / RPG;            // this warp's row part
+  const int rw = SPLIT == 1 ? warp : warp % RPG;            // and row within the group
+  const bool owner = SPLIT == 1 || part == 0;               // owners finish rows and keep lists
+  float2 xr[kSMaxU4][4];                                    // input row (part), element pairs
   int cur_seq = -1, x_src = -2, x_loads = 0, cur_t = -1;
   bool w1_signalled = false;
   float lv = -INFINITY, lvm = -INFINITY;                    // this lane's entry of the W2 / W_LM list
@@ -387,7 +408,7 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
       // warp arrives once for every t in order, so that is phase (t - 2) / 2.
       if (!__all_sync(0xffffffffu, s_wait(lfree0 + 8 * p, ((t - 2) >> 1) & 1, abortp))) return false;
     }
-    lists[(p * kSConsumers + warp) * 32 + lane] = SCand{pv, pi};
+    lists[(p * RPG + warp) * 32 + lane] = SCand{pv, pi};
     __syncwarp();
     if (lane == 0) mbar_arrive(lfull0 + 8 * p);
     pv = -INFINITY;
@@ -414,13 +435,16 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
     return true;
   };
   for (int n = 0; ok; ++n) {
-    const int s = n % kSStages;
-    if (!__all_sync(0xffffffffu, s_wait(full0 + 8 * s, (uint32_t)((n / kSStages) & 1), abortp))) {
+    const int s = n % NSTG;
+    if (!__all_sync(0xffffffffu, s_wait(full0 + 8 * s, (uint32_t)((n / NSTG) & 1), abortp))) {
       if (lane == 0) give_up();
       ok = false;
       break;
     }
     const int idx = stage_item[s];
+    // (second-half warps arrive on the stage's partial-sum barrier at every use of the
+    // stage, so that its phase counts stage uses)
+    if (SPLIT > 1 && !owner && idx < 0 && lane == 0) mbar_arrive(pdone0 + 8 * s);
     if (idx == -1) break;                                   // no groups left
     if (idx == -2) {                                        // marker: leave the W1 phase
       if (!w1_signalled) signal_w1();
@@ -430,7 +454,7 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
     }
     const Item it = map_item(idx, L);
     if (it.seq != cur_seq) {
-      if (!publish_upto(it.kind == 2 ? it.k : (it.seq == 2 * K + 1 ? K : 0))) {
+      if (owner && !publish_upto(it.kind == 2 ? it.k : (it.seq == 2 * K + 1 ? K : 0))) {
         if (lane == 0) give_up();
         ok = false;
         break;
@@ -447,7 +471,7 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
           break;
         }
         if (src >= 0) {
-          const float* zk = reinterpret_cast<const float*>(xbuf);
+          const float* zk = reinterpret_cast<const float*>(xbuf) + part * dp;
 #pragma unroll
           for (int q = 0; q < kSMaxU4; ++q) {
             if (q < nv) {
@@ -464,7 +488,7 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
           for (int q = 0; q < kSMaxU4; ++q) {
             if (q < nv) {
               float f[8];
-              Elem<uint16_t>::unpack(*reinterpret_cast<const uint4*>(xbuf + 16 * (lane + 32 * q)), f);
+              Elem<uint16_t>::unpack(*reinterpret_cast<const uint4*>(xbuf + 2 * part * dp + 16 * (lane + 32 * q)), f);
 #pragma unroll
               for (int e = 0; e < 4; ++e) xr[q][e] = make_float2(f[2 * e], f[2 * e + 1]);
             }
@@ -478,7 +502,7 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
       cur_seq = it.seq;
     }
     const int n_rows = it.kind == 0 ? d : V;
-    const int row = it.grp * kSConsumers + warp;
+    const int row = it.grp * RPG + rw;
     float2 p[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
     if (row < n_rows) {
       const uint8_t* w = ring + (s * kSConsumers + warp) * seg;
@@ -496,11 +520,36 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
       }
     }
     __syncwarp();
-    if (lane == 0) mbar_arrive(empty0 + 8 * s);            // this warp is done with the stage
-    if (row >= n_rows) continue;
+    // this warp is done with the stage (an owner of split rows only once it has read
+    // the part sums, so that no part warp reaches the stage's next use before that)
+    if ((SPLIT == 1 || !owner) && lane == 0) mbar_arrive(empty0 + 8 * s);
+    if (SPLIT == 1 && row >= n_rows) continue;
     float acc = ((p[0].x + p[0].y) + (p[1].x + p[1].y)) + ((p[2].x + p[2].y) + (p[3].x + p[3].y));
     acc = warp_sum(acc);
     acc = __shfl_sync(0xffffffffu, acc, 0);                 // one value for every lane
+    if (SPLIT > 1) {
+      const int pb = (n / NSTG) & 1;                        // part-sum buffer of this use
+      if (!owner) {                                         // other part: hand the sum over
+        if (lane == 0) {
+          partial[((pb * NSTG + s) * (SPLIT - 1) + part - 1) * RPG + rw] = acc;
+          mbar_arrive(pdone0 + 8 * s);                      // (release: the sum is visible)
+        }
+        __syncwarp();
+        continue;
+      }
+      if (row < n_rows) {
+        if (!__all_sync(0xffffffffu, s_wait(pdone0 + 8 * s, (uint32_t)((n / NSTG) & 1), abortp))) {
+          if (lane == 0) give_up();
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int q = 1; q < SPLIT; ++q) acc += partial[((pb * NSTG + s) * (SPLIT - 1) + q - 1) * RPG + rw];
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(empty0 + 8 * s);
+      if (row >= n_rows) continue;
+    }
     if (it.kind == 0) {
       if (lane == 0) {
         float v = acc;
@@ -516,22 +565,27 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
       list_insert(acc, row, 1, lvm, lim);
     }
   }
-  if (ok && (!publish_upto(K) || !publish(K, lvm, lim))) { if (lane == 0) give_up(); ok = false; }
+  if (owner && ok && (!publish_upto(K) || !publish(K, lvm, lim))) { if (lane == 0) give_up(); ok = false; }
   if (!w1_signalled) signal_w1();
 }
 
 }  // namespace
 
+int heads_stream_split(int d) { return d <= 4096 ? 1 : 2; }
+
 size_t heads_stream_smem(int d) {
-  return (size_t)kSStages * kSConsumers * 2 * d + 4 * (size_t)d + 2 * kSConsumers * 32 * sizeof(SCand) +
-         (2 * kSStages + 8) * sizeof(uint64_t);
+  const int split = heads_stream_split(d), rpg = kSConsumers / split, stg = stream_stages(split);
+  const size_t part = ((size_t)2 * stg * (split - 1) * rpg * sizeof(float) + 7) & ~(size_t)7;
+  return (size_t)stg * kSConsumers * 2 * (d / split) + 4 * (size_t)d + 2 * rpg * 32 * sizeof(SCand) + part +
+         (3 * stg + 6) * sizeof(uint64_t);
 }
 
 bool heads_stream_supported(int T, int d, int V, int K, int topk, medusa_dtype dt, const void* h, const void* w1,
                             const void* w2, int64_t w2_stride, const void* w_lm, const void* b1) {
   auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
-  // one stage segment per row: d <= 4096 (8 KiB rows)
-  if (T != 1 || dt != MEDUSA_BF16 || K < 1 || d % 256 != 0 || d > 4096 || V < 2 || topk > 32) return false;
+  // one stage segment per row (d <= 4096, 8 KiB rows) or per half row (d <= 8192)
+  if (T != 1 || dt != MEDUSA_BF16 || K < 1 || d % 256 != 0 || d > 8192 || V < 2 || topk > 32) return false;
+  if (d > 4096 && d % 512 != 0) return false;
   if (!h || !w1 || !w2 || !w_lm || !al(h) || !al(w1) || !al(w2) || !al(w_lm) || (w2_stride * 2) % 16 != 0 ||
       w2_stride < 0)
     return false;
@@ -542,12 +596,12 @@ bool heads_stream_supported(int T, int d, int V, int K, int topk, medusa_dtype d
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   if (coop == 0 || sms < 1 || heads_stream_smem(d) > 227 * 1024) return false;
   // every CTA must be resident at once (one per SM)
-  if (cudaFuncSetAttribute(heads_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                           (int)heads_stream_smem(d)) != cudaSuccess)
+  auto kern = heads_stream_split(d) == 1 ? heads_stream_kernel<1> : heads_stream_kernel<2>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)heads_stream_smem(d)) !=
+      cudaSuccess)
     return false;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, heads_stream_kernel, kSThreads, heads_stream_smem(d)) !=
-      cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kSThreads, heads_stream_smem(d)) != cudaSuccess)
     return false;
   return per_sm >= 1;
 }
@@ -575,7 +629,8 @@ cudaError_t launch_heads_stream(const HeadsPlan& p, const void* h, const void* w
   a.root = root;
   a.pool = pool;
   const size_t smem = heads_stream_smem(p.d);
-  cudaError_t e = cudaFuncSetAttribute(heads_stream_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = heads_stream_split(p.d) == 1 ? heads_stream_kernel<1> : heads_stream_kernel<2>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
@@ -594,7 +649,7 @@ cudaError_t launch_heads_stream(const HeadsPlan& p, const void* h, const void* w
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, heads_stream_kernel, a);
+  e = cudaLaunchKernelEx(&cfg, kern, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

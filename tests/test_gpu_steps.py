@@ -58,6 +58,7 @@ def test_tree_fill(m, name):
 @pytest.mark.parametrize("case", [
     dict(T=1, d=256, V=1000, K=2, topk=3, dt=torch.float32),
     dict(T=1, d=512, V=5003, K=4, topk=10, dt=torch.bfloat16),
+    dict(T=1, d=6144, V=3001, K=3, topk=10, dt=torch.bfloat16),   # weight stream, rows in two halves
     dict(T=3, d=1024, V=4000, K=3, topk=10, dt=torch.bfloat16),
     dict(T=16, d=4096, V=2048, K=2, topk=10, dt=torch.bfloat16),
     dict(T=150, d=256, V=1000, K=2, topk=5, dt=torch.bfloat16),   # tensor-core stream in two passes
