@@ -229,6 +229,19 @@ class Round:
         outb = w.batch * self.N * w.n_q_heads * w.head_dim * 4
         return prefix + tree_in + staged + outb
 
+    def round_bytes(self, accept_len):
+        """Algorithmic HBM bytes of the whole round: the head weights and hidden rows,
+        the template fill, the attention call, the logits of the internal rows that
+        acceptance reads, and the K/V rows that compaction reads and writes (a + 1 rows
+        per sequence, all KV heads)."""
+        w = self.w
+        eb = 4 if w.dtype == "f32" else 2
+        fill = w.batch * (self.N * 8 + (1 + w.n_heads * w.topk) * 4 + 4)
+        accept = w.batch * (self.tmpl.n_internal * w.vocab * eb + self.N * 4)
+        published = int((accept_len.to(torch.int64) + 1).sum())
+        compact = published * 2 * w.n_kv_heads * w.head_dim * eb * 2
+        return self.head_bytes() + fill + self.attn_bytes() + accept + compact
+
     def attn_flops(self):
         w = self.w
         return 4.0 * w.head_dim * float(self.lengths.sum()) * self.N * w.n_q_heads
@@ -296,8 +309,9 @@ def time_loop(fn, steps, stream):
 
 
 class RoundGraphs:
-    """The round captured as CUDA graphs: one graph of the whole round (the timed step)
-    and one graph per stage (for the per-stage split).  The library's calls are
+    """The timed step is the library's own round graph (medusa_round_create records
+    the five calls; each step is one medusa_round_launch).  For the per-stage split
+    each call is also captured alone in a torch CUDA graph: the library's calls are
     stream-ordered and neither allocate nor synchronise, so they capture as they are;
     workspaces and outputs are created by the warm-up calls before capture."""
 
@@ -311,9 +325,10 @@ class RoundGraphs:
                 rd.step()
         torch.cuda.current_stream(dev).wait_stream(side)
         torch.cuda.synchronize(dev)
-        self.full = torch.cuda.CUDAGraph()
-        with torch.cuda.graph(self.full):
-            self._keep = rd.step()
+        w = rd.w
+        self.native = rd.m.MedusaRound(rd.tmpl, rd.h, rd.w1, rd.w2, rd.w_lm, w.topk, rd.L, rd.q, rd.k, rd.v,
+                                       rd.cache, rd.max_L, rd.logits, mode=rd.mode, rope_base=w.rope_base,
+                                       epsilon=w.epsilon, delta=w.delta)
         self.stage = {n: torch.cuda.CUDAGraph() for n in self.NAMES}
         with torch.cuda.graph(self.stage["heads"]):
             root, pool = rd.heads()
@@ -329,7 +344,7 @@ class RoundGraphs:
         torch.cuda.synchronize(dev)
 
     def step(self):
-        self.full.replay()
+        self.native.launch()
 
     def stage_times(self, reps: int, stream, flush):
         """Per-stage device time (µs, mean), CUDA events on the replay stream, with the
@@ -446,7 +461,8 @@ def config_of(w: synth.Workload, rd):
          "paged": bool(w.page_size),
          "l2": "inputs larger than L2: each step streams the head weights (>= 1.4 GB) before the KV; "
                "stage timings flush L2 with a 512 MB write",
-         "launch": "each step replays a CUDA graph of the five library calls; e2e calls the API eagerly"}
+         "launch": "each step is one medusa_round_launch (the library's CUDA graph of the five calls); "
+                   "e2e calls the five API functions eagerly"}
     if rd is not None:
         c["tree_rows"] = rd.N
     return c
@@ -498,6 +514,8 @@ def main():
     stages = graphs.stage_times(20, stream, flush)
     hbm, bf16, src = peaks()
     attn_us = stages["attn"]
+    round_b = rd.round_bytes(graphs.native.accept_len)
+    round_gbs = round_b / (ms_step * 1e-3) / 1e9      # one round per GPU per step
     attn_gbs = rd.attn_bytes() / (attn_us * 1e-6) / 1e9
     # the dominant kernel: heads launches back to back (the head weights exceed L2, so
     # every launch streams them from HBM), events on the replay stream
@@ -527,6 +545,9 @@ def main():
                          "frac": heads_gbs / hbm, "traffic": HEADS_TRAFFIC.get(w.name), "peak_source": src,
                          "algorithmic_bytes": rd.head_bytes(), "launch_us": heads_us},
             "heads_all_rows": all_rows,
+            "round_roofline": {"bound": "hbm", "achieved": round_gbs, "peak": hbm, "unit": "GB/s",
+                               "frac": round_gbs / hbm, "peak_source": src, "algorithmic_bytes": round_b,
+                               "note": "all five steps' algorithmic bytes over one round's device time"},
             "tree_attn_roofline": {"kernel": "medusa_tree_attn_verify", "bound": "hbm", "achieved": attn_gbs,
                                    "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm,
                                    "traffic": ATTN_TRAFFIC.get(w.name),

@@ -28,8 +28,17 @@
  *     see is invalid.  Conditions only the device can see (a prefix length past
  *     the cache capacity, a corrupt accepted path) are reported per sequence in
  *     `status[b]`, and that sequence is left unmodified.
- *   - No kernel waits on another kernel, a flag or a peer; there are no spin
- *     loops.  Split work is merged by the last CTA to finish (an atomic ticket).
+ *   - No kernel waits on another kernel launch.  Inside one launch, waits are
+ *     bounded: the persistent heads kernels (one CTA per SM, cooperative launch,
+ *     so every CTA is resident) wait on counters that other CTAs of the same
+ *     launch advance, and the pipelined kernels wait on their own mbarriers; a
+ *     wait that exceeds about two seconds gives up and the call reports an error
+ *     (MEDUSA_ETIMEOUT per sequence, or -1 ids from the heads).  Split-KV
+ *     attention merges its splits inside a thread-block cluster (bf16 tensor-core
+ *     path) or in the last CTA to finish a unit (an atomic ticket, fp32 path).
+ *   - medusa_round_create captures the five device calls of one round into a
+ *     CUDA graph; medusa_round_launch replays it with one launch and no host
+ *     synchronisation.
  */
 #ifndef MEDUSA_GB300_H
 #define MEDUSA_GB300_H
@@ -300,6 +309,78 @@ medusa_status medusa_kv_compact(const medusa_kv_t *cache, const medusa_tree_t *t
                                 const int32_t *L, const int32_t *accept_len,
                                 const int32_t *out_rows, int32_t *L_out, int32_t *status,
                                 void *stream);
+
+/* ---------------------------------------------------------------------------
+ * Whole round: the five calls as one CUDA graph
+ * ------------------------------------------------------------------------- */
+
+/* A replayable round over fixed buffers, with acceptance decided on the device and no
+ * host round trip between the steps ([CN] "把 Python 控制流赶出热路径" ranks this above
+ * adding heads; [CN] "Mask、位置和 KV 必须一起验证": fixed buffer addresses are what
+ * allow a CUDA graph).
+ *
+ * Every argument of the five calls of one round (steps 1-5 above), with one frontier
+ * row per sequence for the heads (T = B).  Pointers are device buffers that the
+ * caller keeps alive and fixed while the round exists: the graph records the
+ * addresses, so new inputs are written into the same buffers before each launch.
+ * `tree` and `cache` are copied at creation (their device arrays are referenced).
+ * Fields have the meaning they have in the call they belong to. */
+typedef struct {
+  medusa_tree_t tree;        /* device template */
+  int32_t B;                 /* sequences */
+  medusa_dtype dtype;        /* heads weights, hidden rows, logits (the cache has its own) */
+  /* step 1: medusa_heads_topk with T = B */
+  const void *h;             /* [B][d] */
+  int32_t d, V, K, topk;
+  const void *w1, *b1, *w2;  /* b1 may be NULL */
+  int64_t w2_head_stride;
+  const void *w_lm;
+  int32_t *root, *pool;      /* [B], [B][K][topk] */
+  /* step 2: medusa_tree_fill */
+  const int32_t *L;          /* [B] */
+  int32_t *tokens, *pos;     /* [B][N] */
+  /* step 3: medusa_tree_attn_verify */
+  int32_t n_q_heads;
+  const void *q, *k_new, *v_new;
+  medusa_kv_t cache;
+  int32_t max_prefix;
+  float rope_base, scale;
+  float *out, *lse;          /* lse may be NULL */
+  int32_t *attn_status;      /* [B] */
+  /* step 4: medusa_tree_accept on logits [B][N][V] in dtype */
+  const void *logits;
+  int32_t mode;
+  float temperature, epsilon, delta;
+  int32_t entropy_guard;
+  int32_t *best_path, *accept_len, *out_tokens, *out_rows, *frontier_row;
+  /* step 5: medusa_kv_compact */
+  int32_t *L_out, *compact_status;   /* [B], [B] */
+} medusa_round_desc;
+
+typedef struct medusa_round_s *medusa_round_t;
+
+/* Workspace bytes of a round: the heads, attention and acceptance workspaces, each
+ * 256-byte aligned, back to back.  0 when the descriptor is invalid. */
+size_t medusa_round_workspace(const medusa_round_desc *r);
+
+/* Checks the descriptor as the five calls would, zero-fills the workspace, then
+ * records the five calls (on a private stream under thread-local stream capture) and
+ * instantiates the graph.  ws: medusa_round_workspace(r) bytes, 16-byte aligned,
+ * owned by the caller and used only by this round's launches.  `stream` orders the
+ * workspace clearing before the capture; creation returns after that clearing
+ * completed.  Creation allocates the graph objects (host memory and driver
+ * resources; no device buffers).  Any status of the recorded calls is returned as is,
+ * with no round created. */
+medusa_status medusa_round_create(const medusa_round_desc *r, void *ws, size_t ws_bytes, void *stream,
+                                  medusa_round_t *round_out);
+
+/* Enqueues the whole round on `stream`: one graph launch, no host synchronisation.
+ * Launches of one round must not overlap each other (they share the workspace and
+ * the output buffers): launch on one stream, or order the streams. */
+medusa_status medusa_round_launch(medusa_round_t round, void *stream);
+
+/* Frees the graph objects.  The caller must make sure no launch is still running. */
+medusa_status medusa_round_destroy(medusa_round_t round);
 
 /* ---------------------------------------------------------------------------
  * Misc

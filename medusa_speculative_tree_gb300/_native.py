@@ -22,7 +22,8 @@ EXPORTED = [
     "medusa_tree_upload", "medusa_heads_topk_workspace", "medusa_heads_topk", "medusa_tree_fill",
     "medusa_tree_attn_workspace", "medusa_tree_attn_verify", "medusa_tree_attn_verify_static",
     "medusa_tree_accept_workspace",
-    "medusa_tree_accept", "medusa_kv_compact", "medusa_status_string", "medusa_abi_version",
+    "medusa_tree_accept", "medusa_kv_compact", "medusa_round_workspace", "medusa_round_create",
+    "medusa_round_launch", "medusa_round_destroy", "medusa_status_string", "medusa_abi_version",
 ]
 
 
@@ -41,6 +42,25 @@ class MedusaKV(C.Structure):
         ("k", C.c_void_p), ("v", C.c_void_p), ("dtype", C.c_int32), ("n_kv_heads", C.c_int32),
         ("head_dim", C.c_int32), ("capacity", C.c_int32), ("page_size", C.c_int32),
         ("block_table", C.c_void_p), ("max_blocks", C.c_int32), ("n_pages", C.c_int32),
+    ]
+
+
+class MedusaRoundDesc(C.Structure):
+    """medusa_round_desc: every argument of the five calls of one round."""
+    _fields_ = [
+        ("tree", MedusaTree), ("B", C.c_int32), ("dtype", C.c_int32),
+        ("h", C.c_void_p), ("d", C.c_int32), ("V", C.c_int32), ("K", C.c_int32), ("topk", C.c_int32),
+        ("w1", C.c_void_p), ("b1", C.c_void_p), ("w2", C.c_void_p), ("w2_head_stride", C.c_int64),
+        ("w_lm", C.c_void_p), ("root", C.c_void_p), ("pool", C.c_void_p),
+        ("L", C.c_void_p), ("tokens", C.c_void_p), ("pos", C.c_void_p),
+        ("n_q_heads", C.c_int32), ("q", C.c_void_p), ("k_new", C.c_void_p), ("v_new", C.c_void_p),
+        ("cache", MedusaKV), ("max_prefix", C.c_int32), ("rope_base", C.c_float), ("scale", C.c_float),
+        ("out", C.c_void_p), ("lse", C.c_void_p), ("attn_status", C.c_void_p),
+        ("logits", C.c_void_p), ("mode", C.c_int32), ("temperature", C.c_float), ("epsilon", C.c_float),
+        ("delta", C.c_float), ("entropy_guard", C.c_int32),
+        ("best_path", C.c_void_p), ("accept_len", C.c_void_p), ("out_tokens", C.c_void_p),
+        ("out_rows", C.c_void_p), ("frontier_row", C.c_void_p),
+        ("L_out", C.c_void_p), ("compact_status", C.c_void_p),
     ]
 
 
@@ -82,6 +102,10 @@ def lib() -> C.CDLL:
         "medusa_tree_accept": (I32, [P(MedusaTree), I32, I32, VP, I32, VP, I32, F, F, F, I32, VP, VP,
                                      VP, VP, VP, VP, SZ, VP]),
         "medusa_kv_compact": (I32, [P(MedusaKV), P(MedusaTree), I32, VP, VP, VP, VP, VP, VP]),
+        "medusa_round_workspace": (SZ, [P(MedusaRoundDesc)]),
+        "medusa_round_create": (I32, [P(MedusaRoundDesc), VP, SZ, VP, P(VP)]),
+        "medusa_round_launch": (I32, [VP, VP]),
+        "medusa_round_destroy": (I32, [VP]),
         "medusa_status_string": (C.c_char_p, [I32]),
         "medusa_abi_version": (I32, []),
     }

@@ -287,3 +287,105 @@ def medusa_kv_compact(cache: KVCache, tmpl: Template, L, accept_len, out_rows):
           lib().medusa_kv_compact(C.byref(d), C.byref(tmpl.dev), B, _ptr(L), _ptr(accept_len),
                                   _ptr(out_rows), _ptr(L_out), _ptr(status), _stream(dev)))
     return L_out, status
+
+
+# ----------------------------------------------------------------------------- whole round
+
+class MedusaRound:
+    """One verify round recorded as a CUDA graph of the five calls
+    (medusa_round_create); launch() replays it with one graph launch.
+
+    The inputs are the device tensors given here, referenced by address: write new
+    values into them (copy_) before a launch.  The outputs are tensors allocated here
+    and overwritten by every launch: root, pool, tokens, pos, out, lse (or None),
+    attn_status, best_path, accept_len, out_tokens, out_rows, frontier_row, L_out,
+    compact_status.  The heads run on one frontier row per sequence (h is [B, d])."""
+
+    _OUT = ("root", "pool", "tokens", "pos", "out", "lse", "attn_status", "best_path", "accept_len",
+            "out_tokens", "out_rows", "frontier_row", "L_out", "compact_status")
+
+    def __init__(self, tmpl: Template, h, w1, w2, w_lm, topk: int, L, q, k_new, v_new, cache: KVCache,
+                 max_prefix: int, logits, mode: str = "greedy", rope_base: float = 10000.0,
+                 scale: Optional[float] = None, temperature: float = 1.0, epsilon: float = 0.09,
+                 delta: float = 0.3, entropy_guard: bool = False, b1=None, shared_w2: bool = False,
+                 want_lse: bool = False):
+        _need_cuda(h, w1, w2, w_lm, b1, L, q, k_new, v_new, logits)
+        B, d = h.shape
+        V, K, N = w_lm.shape[0], w1.shape[0], tmpl.n_rows
+        Bq, Nq, Hq, dh = q.shape
+        if Bq != B or Nq != N or tuple(logits.shape) != (B, N, V) or tuple(L.shape) != (B,):
+            raise ValueError("inconsistent round shapes")
+        if logits.dtype != h.dtype:
+            raise ValueError("logits and hidden rows must share a dtype")
+        dev = h.device
+        i32 = dict(dtype=torch.int32, device=dev)
+        W = tmpl.max_depth + 1
+        self.root = torch.empty(B, **i32)
+        self.pool = torch.empty((B, K, topk), **i32)
+        self.tokens = torch.empty((B, N), **i32)
+        self.pos = torch.empty((B, N), **i32)
+        self.out = torch.empty(tuple(q.shape), dtype=torch.float32, device=dev)
+        self.lse = torch.empty((B, N, Hq), dtype=torch.float32, device=dev) if want_lse else None
+        self.attn_status = torch.empty(B, **i32)
+        self.best_path = torch.empty(B, **i32)
+        self.accept_len = torch.empty(B, **i32)
+        self.out_tokens = torch.empty((B, W), **i32)
+        self.out_rows = torch.empty((B, W), **i32)
+        self.frontier_row = torch.empty(B, **i32)
+        self.L_out = torch.empty(B, **i32)
+        self.compact_status = torch.empty(B, **i32)
+        # the graph records addresses: keep every input alive as long as the round
+        self._inputs = (tmpl, h, w1, w2, w_lm, b1, L, q, k_new, v_new, cache, logits)
+        r = nat.MedusaRoundDesc()
+        r.tree = tmpl.dev
+        r.B, r.dtype = B, _dtype_code(h.dtype)
+        r.h, r.d, r.V, r.K, r.topk = h.data_ptr(), d, V, K, topk
+        r.w1, r.b1, r.w2 = w1.data_ptr(), (b1.data_ptr() if b1 is not None else None), w2.data_ptr()
+        r.w2_head_stride = 0 if shared_w2 else V * d
+        r.w_lm, r.root, r.pool = w_lm.data_ptr(), self.root.data_ptr(), self.pool.data_ptr()
+        r.L, r.tokens, r.pos = L.data_ptr(), self.tokens.data_ptr(), self.pos.data_ptr()
+        r.n_q_heads, r.q, r.k_new, r.v_new = Hq, q.data_ptr(), k_new.data_ptr(), v_new.data_ptr()
+        r.cache = cache.desc()
+        r.max_prefix = int(max_prefix)
+        r.rope_base = float(rope_base)
+        r.scale = float(scale) if scale is not None else 1.0 / float(dh) ** 0.5
+        r.out, r.lse = self.out.data_ptr(), (self.lse.data_ptr() if self.lse is not None else None)
+        r.attn_status = self.attn_status.data_ptr()
+        r.logits = logits.data_ptr()
+        r.mode = nat.GREEDY if mode == "greedy" else nat.TYPICAL
+        r.temperature, r.epsilon, r.delta = float(temperature), float(epsilon), float(delta)
+        r.entropy_guard = int(entropy_guard)
+        r.best_path, r.accept_len = self.best_path.data_ptr(), self.accept_len.data_ptr()
+        r.out_tokens, r.out_rows = self.out_tokens.data_ptr(), self.out_rows.data_ptr()
+        r.frontier_row = self.frontier_row.data_ptr()
+        r.L_out, r.compact_status = self.L_out.data_ptr(), self.compact_status.data_ptr()
+        self.desc = r
+        nb = lib().medusa_round_workspace(C.byref(r))
+        if nb == 0:
+            raise ValueError("invalid round arguments")
+        self.ws = torch.empty(nb, dtype=torch.uint8, device=dev)
+        self.device = dev
+        self._handle = C.c_void_p()
+        check("medusa_round_create",
+              lib().medusa_round_create(C.byref(r), _ptr(self.ws), nb, _stream(dev), C.byref(self._handle)))
+
+    def launch(self, stream: Optional[torch.cuda.Stream] = None):
+        """Enqueue the whole round on `stream` (default: the current stream)."""
+        s = C.c_void_p((stream or torch.cuda.current_stream(self.device)).cuda_stream)
+        check("medusa_round_launch", lib().medusa_round_launch(self._handle, s))
+
+    def results(self) -> dict:
+        return {k: getattr(self, k) for k in self._OUT}
+
+    def close(self):
+        """Free the graph (after the device has finished every launch)."""
+        if self._handle is not None and self._handle.value:
+            torch.cuda.synchronize(self.device)
+            check("medusa_round_destroy", lib().medusa_round_destroy(self._handle))
+        self._handle = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass

@@ -6,6 +6,7 @@
 #include <cmath>
 #include <cstring>
 #include <map>
+#include <new>
 #include <vector>
 
 #include "kernels.h"
@@ -92,7 +93,7 @@ bool kv_ok(const medusa_kv_t* c) {
 
 extern "C" {
 
-int32_t medusa_abi_version(void) { return 1; }
+int32_t medusa_abi_version(void) { return 2; }
 
 const char* medusa_status_string(medusa_status s) {
   switch (s) {
@@ -411,6 +412,112 @@ medusa_status medusa_kv_compact(const medusa_kv_t* cache, const medusa_tree_t* t
     return MEDUSA_EINVAL;
   return cuda_status(medusa::launch_kv_compact(*cache, *t, B, L, accept_len, out_rows, L_out, status,
                                                as_stream(stream)));
+}
+
+// ---- whole round as one CUDA graph ------------------------------------------------
+
+struct medusa_round_s {
+  cudaGraph_t graph;
+  cudaGraphExec_t exec;
+};
+
+namespace {
+
+// Offsets of the three workspaces inside a round's workspace (256-byte aligned).
+struct RoundWs {
+  size_t attn, accept, total;
+};
+
+bool round_ws(const medusa_round_desc* r, RoundWs& w) {
+  if (!r || !tree_ok(&r->tree) || !kv_ok(&r->cache) || r->B < 1) return false;
+  const size_t h = medusa_heads_topk_workspace(r->B, r->d, r->V, r->K, r->topk);
+  const size_t a = medusa_tree_attn_workspace(&r->tree, r->B, r->n_q_heads, &r->cache, r->max_prefix);
+  const size_t c = medusa_tree_accept_workspace(&r->tree, r->B, r->V);
+  if (h == 0 || a == 0 || c == 0) return false;
+  w.attn = align_up(h, 256);
+  w.accept = w.attn + align_up(a, 256);
+  w.total = w.accept + align_up(c, 256);
+  return true;
+}
+
+// The five calls in round order on `st`; the first failing status is returned.
+medusa_status record_round(const medusa_round_desc* r, char* ws, const RoundWs& w, void* st) {
+  medusa_status s = medusa_heads_topk(r->h, r->B, r->d, r->V, r->K, r->w1, r->b1, r->w2, r->w2_head_stride,
+                                      r->w_lm, r->topk, r->dtype, r->root, r->pool, nullptr, ws, w.attn, st);
+  if (s != MEDUSA_OK) return s;
+  s = medusa_tree_fill(&r->tree, r->B, r->K, r->root, r->pool, r->L, r->tokens, r->pos, st);
+  if (s != MEDUSA_OK) return s;
+  s = medusa_tree_attn_verify(&r->tree, r->B, r->n_q_heads, r->q, r->k_new, r->v_new, &r->cache, r->L,
+                              r->max_prefix, r->rope_base, r->scale, r->out, r->lse, r->attn_status,
+                              ws + w.attn, w.accept - w.attn, st);
+  if (s != MEDUSA_OK) return s;
+  s = medusa_tree_accept(&r->tree, r->B, r->V, r->logits, r->dtype, r->tokens, r->mode, r->temperature,
+                         r->epsilon, r->delta, r->entropy_guard, r->best_path, r->accept_len, r->out_tokens,
+                         r->out_rows, r->frontier_row, ws + w.accept, w.total - w.accept, st);
+  if (s != MEDUSA_OK) return s;
+  return medusa_kv_compact(&r->cache, &r->tree, r->B, r->L, r->accept_len, r->out_rows, r->L_out,
+                           r->compact_status, st);
+}
+
+}  // namespace
+
+size_t medusa_round_workspace(const medusa_round_desc* r) {
+  RoundWs w;
+  return round_ws(r, w) ? w.total : 0;
+}
+
+medusa_status medusa_round_create(const medusa_round_desc* r, void* ws, size_t ws_bytes, void* stream,
+                                  medusa_round_t* round_out) {
+  if (!round_out) return MEDUSA_EINVAL;
+  *round_out = nullptr;
+  RoundWs w;
+  if (!round_ws(r, w) || !ws || !aligned16(ws)) return MEDUSA_EINVAL;
+  if (ws_bytes < w.total) return MEDUSA_EWORKSPACE;
+  const cudaStream_t user = as_stream(stream);
+  if (cudaMemsetAsync(ws, 0, w.total, user) != cudaSuccess || cudaStreamSynchronize(user) != cudaSuccess)
+    return MEDUSA_ECUDA;
+  // Record on a private stream: capture needs a stream other than the legacy default,
+  // and thread-local mode leaves other threads' CUDA calls alone meanwhile.
+  cudaStream_t cs = nullptr;
+  if (cudaStreamCreateWithFlags(&cs, cudaStreamNonBlocking) != cudaSuccess) return MEDUSA_ECUDA;
+  medusa_status s = MEDUSA_OK;
+  cudaGraph_t g = nullptr;
+  if (cudaStreamBeginCapture(cs, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    s = MEDUSA_ECUDA;
+  } else {
+    s = record_round(r, static_cast<char*>(ws), w, cs);
+    const cudaError_t e = cudaStreamEndCapture(cs, &g);   // ends the capture on every path
+    if (s == MEDUSA_OK && e != cudaSuccess) s = MEDUSA_ECUDA;
+  }
+  cudaGraphExec_t ex = nullptr;
+  if (s == MEDUSA_OK && cudaGraphInstantiate(&ex, g, 0) != cudaSuccess) s = MEDUSA_ECUDA;
+  medusa_round_s* rr = nullptr;
+  if (s == MEDUSA_OK) {
+    rr = new (std::nothrow) medusa_round_s{g, ex};
+    if (!rr) s = MEDUSA_ECUDA;
+  }
+  cudaStreamDestroy(cs);
+  if (s != MEDUSA_OK) {
+    if (ex) cudaGraphExecDestroy(ex);
+    if (g) cudaGraphDestroy(g);
+    cudaGetLastError();              // leave no sticky error behind a failed creation
+    return s;
+  }
+  *round_out = rr;
+  return MEDUSA_OK;
+}
+
+medusa_status medusa_round_launch(medusa_round_t round, void* stream) {
+  if (!round) return MEDUSA_EINVAL;
+  return cuda_status(cudaGraphLaunch(round->exec, as_stream(stream)));
+}
+
+medusa_status medusa_round_destroy(medusa_round_t round) {
+  if (!round) return MEDUSA_EINVAL;
+  const cudaError_t a = cudaGraphExecDestroy(round->exec);
+  const cudaError_t b = cudaGraphDestroy(round->graph);
+  delete round;
+  return (a == cudaSuccess && b == cudaSuccess) ? MEDUSA_OK : MEDUSA_ECUDA;
 }
 
 }  // extern "C"

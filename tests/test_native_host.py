@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(native):
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(native.EXPORTED)
-    assert native.lib().medusa_abi_version() == 1
+    assert native.lib().medusa_abi_version() == 2
     assert native.lib().medusa_status_string(-2).decode() == "cache capacity exceeded"
 
 
@@ -114,3 +114,51 @@ def test_root_only_and_limits(native):
     assert lib.medusa_tree_greedy(None, 1, 1, 1, None, None) == native.EINVAL
     out = native.MedusaTree()
     assert lib.medusa_tree_compile(None, 1, 1, 4, 0, None, 0, C.byref(out)) == native.EINVAL
+
+
+def test_round_desc_layout_matches_header(native, tmp_path):
+    """The ctypes medusa_round_desc (and the structs inside it) has the C layout:
+    size and every field offset, from a program compiled against the header."""
+    import shutil
+    import subprocess
+    cc = shutil.which("gcc") or shutil.which("cc")
+    if cc is None:
+        pytest.skip("no C compiler")
+    structs = [("medusa_round_desc", native.MedusaRoundDesc), ("medusa_tree_t", native.MedusaTree),
+               ("medusa_kv_t", native.MedusaKV)]
+    lines = ["#include <stdio.h>", "#include <stddef.h>", '#include "medusa_gb300.h"', "int main(void) {"]
+    for cname, py in structs:
+        lines.append('printf("%s size %%zu\\n", sizeof(%s));' % (cname, cname))
+        for f, _ in py._fields_:
+            lines.append('printf("%s %s %%zu\\n", offsetof(%s, %s));' % (cname, f, cname, f))
+    lines += ["return 0;", "}"]
+    src = tmp_path / "layout.c"
+    src.write_text("\n".join(lines) + "\n")
+    exe = tmp_path / "layout"
+    subprocess.check_call([cc, "-std=c99", "-I", os.path.join(ROOT, "include"), str(src), "-o", str(exe)])
+    out = subprocess.check_output([str(exe)]).decode().split("\n")
+    got = {}
+    for ln in out:
+        if ln.strip():
+            a, b, c = ln.split()
+            got[(a, b)] = int(c)
+    for cname, py in structs:
+        assert got[(cname, "size")] == C.sizeof(py), cname
+        for f, _ in py._fields_:
+            assert got[(cname, f)] == getattr(py, f).offset, (cname, f)
+
+
+def test_round_create_rejects_bad_arguments_without_a_gpu(native):
+    """Host-visible checks come before any CUDA call: a missing descriptor, output
+    handle or workspace is refused with MEDUSA_EINVAL and no round."""
+    lib = native.lib()
+    handle = C.c_void_p(1234)
+    assert lib.medusa_round_create(None, None, 0, None, C.byref(handle)) == native.EINVAL
+    assert handle.value is None
+    desc = native.MedusaRoundDesc()
+    assert lib.medusa_round_workspace(C.byref(desc)) == 0
+    assert lib.medusa_round_workspace(None) == 0
+    assert lib.medusa_round_create(C.byref(desc), None, 0, None, None) == native.EINVAL
+    assert lib.medusa_round_create(C.byref(desc), None, 0, None, C.byref(handle)) == native.EINVAL
+    assert lib.medusa_round_launch(None, None) == native.EINVAL
+    assert lib.medusa_round_destroy(None) == native.EINVAL
