@@ -74,6 +74,7 @@ typedef int32_t medusa_dtype;
 #define MEDUSA_MAX_DEPTH  16     /* Medusa depth D (paths hold D + 1 rows) */
 #define MEDUSA_MAX_TOPK   32     /* candidate pool width TOPK */
 #define MEDUSA_MAX_HEAD_ROWS 1024 /* hidden rows T of one medusa_heads_topk call */
+#define MEDUSA_MAX_LAYERS 4096   /* layers of one medusa_kv_compact_layers call */
 
 /*
  * Compiled tree template: the four coupled buffers of [M7.2] §0x04A plus the
@@ -309,6 +310,19 @@ medusa_status medusa_kv_compact(const medusa_kv_t *cache, const medusa_tree_t *t
                                 const int32_t *L, const int32_t *accept_len,
                                 const int32_t *out_rows, int32_t *L_out, int32_t *status,
                                 void *stream);
+
+/* medusa_kv_compact for every layer of the model at once ([M7.2] §0x06B: the accepted
+ * rows are committed in each layer's cache, and uncommitted rows are never
+ * published).  caches [host] [n_layers] descriptors that differ only in k and v: the
+ * same dtype, head counts, capacity, page size and block table (a paged cache shares
+ * its block table across layers).  The path of each sequence is validated once, as in
+ * medusa_kv_compact; a rejected sequence is left untouched in every layer.  One
+ * kernel launch per 128 layers.  L_out must not alias L.
+ * Limits: 1 <= n_layers <= MEDUSA_MAX_LAYERS. */
+medusa_status medusa_kv_compact_layers(const medusa_kv_t *caches, int32_t n_layers, const medusa_tree_t *t,
+                                       int32_t B, const int32_t *L, const int32_t *accept_len,
+                                       const int32_t *out_rows, int32_t *L_out, int32_t *status,
+                                       void *stream);
 
 /* ---------------------------------------------------------------------------
  * Whole round: the five calls as one CUDA graph

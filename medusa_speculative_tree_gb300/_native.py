@@ -15,6 +15,7 @@ OK, EINVAL, ECAPACITY, EUNSUPPORTED, ETEMPLATE, ECUDA, EWORKSPACE, EPATH, ETIMEO
 F32, BF16 = 0, 1
 GREEDY, TYPICAL = 0, 1
 MAX_ROWS, MAX_DEPTH, MAX_TOPK = 4096, 16, 32
+MAX_LAYERS = 4096
 ATTN_STATIC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 EXPORTED = [
@@ -22,7 +23,7 @@ EXPORTED = [
     "medusa_tree_upload", "medusa_heads_topk_workspace", "medusa_heads_topk", "medusa_tree_fill",
     "medusa_tree_attn_workspace", "medusa_tree_attn_verify", "medusa_tree_attn_verify_static",
     "medusa_tree_accept_workspace",
-    "medusa_tree_accept", "medusa_kv_compact", "medusa_round_workspace", "medusa_round_create",
+    "medusa_tree_accept", "medusa_kv_compact", "medusa_kv_compact_layers", "medusa_round_workspace", "medusa_round_create",
     "medusa_round_launch", "medusa_round_destroy", "medusa_status_string", "medusa_abi_version",
 ]
 
@@ -102,6 +103,7 @@ def lib() -> C.CDLL:
         "medusa_tree_accept": (I32, [P(MedusaTree), I32, I32, VP, I32, VP, I32, F, F, F, I32, VP, VP,
                                      VP, VP, VP, VP, SZ, VP]),
         "medusa_kv_compact": (I32, [P(MedusaKV), P(MedusaTree), I32, VP, VP, VP, VP, VP, VP]),
+        "medusa_kv_compact_layers": (I32, [P(MedusaKV), I32, P(MedusaTree), I32, VP, VP, VP, VP, VP, VP]),
         "medusa_round_workspace": (SZ, [P(MedusaRoundDesc)]),
         "medusa_round_create": (I32, [P(MedusaRoundDesc), VP, SZ, VP, P(VP)]),
         "medusa_round_launch": (I32, [VP, VP]),

@@ -289,6 +289,20 @@ def medusa_kv_compact(cache: KVCache, tmpl: Template, L, accept_len, out_rows):
     return L_out, status
 
 
+def medusa_kv_compact_layers(caches: Sequence[KVCache], tmpl: Template, L, accept_len, out_rows):
+    """medusa_kv_compact for every layer's cache at once; L_out [B], status [B] int32."""
+    _need_cuda(L, accept_len, out_rows)
+    B = L.shape[0]
+    dev = L.device
+    L_out = torch.empty(B, dtype=torch.int32, device=dev)
+    status = torch.empty(B, dtype=torch.int32, device=dev)
+    arr = (nat.MedusaKV * len(caches))(*[c.desc() for c in caches])
+    check("medusa_kv_compact_layers",
+          lib().medusa_kv_compact_layers(arr, len(caches), C.byref(tmpl.dev), B, _ptr(L), _ptr(accept_len),
+                                         _ptr(out_rows), _ptr(L_out), _ptr(status), _stream(dev)))
+    return L_out, status
+
+
 # ----------------------------------------------------------------------------- whole round
 
 class MedusaRound:

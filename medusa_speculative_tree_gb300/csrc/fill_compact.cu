@@ -34,21 +34,32 @@ __device__ __forceinline__ int64_t cache_row_offset(const medusa_kv_t& c, int b,
   return (((int64_t)page * c.n_kv_heads + kvh) * c.page_size + row % c.page_size) * c.head_dim;
 }
 
-// One CTA per (kv head, sequence).  The whole path is validated first (lane j of warp
-// 0 checks row j: 0 for the root, else a child of row j - 1); the G source rows of K
-// and V are then read into shared memory before any destination row is written, so
-// overlapping source/destination rows are safe.  Rows move as 16-byte vectors when
-// their length allows.
-template <typename EL>
-__global__ void kv_compact_kernel(medusa_kv_t c, medusa_tree_t t, const int32_t* __restrict__ L,
-                                  const int32_t* __restrict__ accept_len,
+// K and V base pointers of the layers that one launch commits ([M7.2] §0x06B: the
+// accepted rows are committed in every layer's cache); blockIdx.z picks the layer.
+// The other fields of the cache descriptor are common to all of them.
+template <int NL>
+struct LayerPtrs {
+  void* k[NL];
+  void* v[NL];
+};
+
+// One CTA per (kv head, sequence, layer).  The whole path is validated first (lane j
+// of warp 0 checks row j: 0 for the root, else a child of row j - 1); the G source
+// rows of K and V are then read into shared memory before any destination row is
+// written, so overlapping source/destination rows are safe.  Rows move as 16-byte
+// vectors when their length allows.  status and L_out are written once per sequence
+// (kv head 0 of layer 0, in the launch that has write_meta set).
+template <typename EL, int NL>
+__global__ void kv_compact_kernel(medusa_kv_t c, LayerPtrs<NL> lp, int write_meta, medusa_tree_t t,
+                                  const int32_t* __restrict__ L, const int32_t* __restrict__ accept_len,
                                   const int32_t* __restrict__ out_rows, int32_t* __restrict__ L_out,
                                   int32_t* __restrict__ status) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   EL* snap = reinterpret_cast<EL*>(smem_raw);       // [2][D+1][dh]
   __shared__ int rows_s[MEDUSA_MAX_DEPTH + 1];
   __shared__ int verdict;
-  const int kvh = blockIdx.x, b = blockIdx.y;
+  const int kvh = blockIdx.x, b = blockIdx.y, layer = blockIdx.z;
+  const bool meta = write_meta && kvh == 0 && layer == 0 && threadIdx.x == 0;
   const int dh = c.head_dim, W = t.max_depth + 1;
   const int Lb = L[b];
   const int a = accept_len[b];
@@ -75,15 +86,15 @@ __global__ void kv_compact_kernel(medusa_kv_t c, medusa_tree_t t, const int32_t*
   __syncthreads();
   const int v = verdict;
   if (v != MEDUSA_OK) {
-    if (kvh == 0 && threadIdx.x == 0) {
+    if (meta) {
       status[b] = v;
       L_out[b] = Lb;
     }
     return;
   }
   const int G = a + 1;
-  EL* ck = (EL*)c.k;
-  EL* cv = (EL*)c.v;
+  EL* ck = (EL*)lp.k[layer];
+  EL* cv = (EL*)lp.v[layer];
   if ((dh * (int)sizeof(EL)) % 16 == 0) {
     const int pr = dh * (int)sizeof(EL) / 16;           // 16-byte pieces per row
     uint4* s4 = reinterpret_cast<uint4*>(snap);
@@ -115,7 +126,7 @@ __global__ void kv_compact_kernel(medusa_kv_t c, medusa_tree_t t, const int32_t*
       cv[dst] = snap[(W + j) * dh + e];
     }
   }
-  if (kvh == 0 && threadIdx.x == 0) {
+  if (meta) {
     status[b] = MEDUSA_OK;
     L_out[b] = Lb + G;
   }
@@ -138,12 +149,42 @@ cudaError_t launch_kv_compact(const medusa_kv_t& c, const medusa_tree_t& t, int 
                               cudaStream_t st) {
   const size_t esz = c.dtype == MEDUSA_BF16 ? 2 : 4;
   const size_t smem = 2 * (size_t)(t.max_depth + 1) * c.head_dim * esz;
-  dim3 grid(c.n_kv_heads, B);
+  dim3 grid(c.n_kv_heads, B, 1);
+  LayerPtrs<1> lp;
+  lp.k[0] = c.k;
+  lp.v[0] = c.v;
   if (c.dtype == MEDUSA_BF16)
-    kv_compact_kernel<uint16_t><<<grid, 128, smem, st>>>(c, t, L, accept_len, out_rows, L_out, status);
+    kv_compact_kernel<uint16_t, 1><<<grid, 128, smem, st>>>(c, lp, 1, t, L, accept_len, out_rows, L_out, status);
   else
-    kv_compact_kernel<float><<<grid, 128, smem, st>>>(c, t, L, accept_len, out_rows, L_out, status);
+    kv_compact_kernel<float, 1><<<grid, 128, smem, st>>>(c, lp, 1, t, L, accept_len, out_rows, L_out, status);
   return cudaGetLastError();
+}
+
+cudaError_t launch_kv_compact_layers(const medusa_kv_t* layers, int n_layers, const medusa_tree_t& t, int B,
+                                     const int32_t* L, const int32_t* accept_len, const int32_t* out_rows,
+                                     int32_t* L_out, int32_t* status, cudaStream_t st) {
+  const medusa_kv_t& c = layers[0];
+  const size_t esz = c.dtype == MEDUSA_BF16 ? 2 : 4;
+  const size_t smem = 2 * (size_t)(t.max_depth + 1) * c.head_dim * esz;
+  for (int l0 = 0; l0 < n_layers; l0 += kCompactLayersPerLaunch) {
+    const int n = n_layers - l0 < kCompactLayersPerLaunch ? n_layers - l0 : kCompactLayersPerLaunch;
+    LayerPtrs<kCompactLayersPerLaunch> lp = {};
+    for (int i = 0; i < n; ++i) {
+      lp.k[i] = layers[l0 + i].k;
+      lp.v[i] = layers[l0 + i].v;
+    }
+    dim3 grid(c.n_kv_heads, B, n);
+    const int meta = l0 == 0 ? 1 : 0;
+    if (c.dtype == MEDUSA_BF16)
+      kv_compact_kernel<uint16_t, kCompactLayersPerLaunch>
+          <<<grid, 128, smem, st>>>(c, lp, meta, t, L, accept_len, out_rows, L_out, status);
+    else
+      kv_compact_kernel<float, kCompactLayersPerLaunch>
+          <<<grid, 128, smem, st>>>(c, lp, meta, t, L, accept_len, out_rows, L_out, status);
+    const cudaError_t e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+  }
+  return cudaSuccess;
 }
 
 }  // namespace medusa

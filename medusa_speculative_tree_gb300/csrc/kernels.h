@@ -88,6 +88,13 @@ cudaError_t launch_kv_compact(const medusa_kv_t& c, const medusa_tree_t& t, int 
                               const int32_t* L, const int32_t* accept_len,
                               const int32_t* out_rows, int32_t* L_out, int32_t* status,
                               cudaStream_t st);
+// All layers' caches in launches of up to kCompactLayersPerLaunch layers (their K/V
+// pointers travel in the kernel parameters); the other descriptor fields are those of
+// layers[0], which the caller has checked to be common to every layer.
+constexpr int kCompactLayersPerLaunch = 128;
+cudaError_t launch_kv_compact_layers(const medusa_kv_t* layers, int n_layers, const medusa_tree_t& t, int B,
+                                     const int32_t* L, const int32_t* accept_len, const int32_t* out_rows,
+                                     int32_t* L_out, int32_t* status, cudaStream_t st);
 
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 

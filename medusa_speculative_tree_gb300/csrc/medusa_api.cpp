@@ -414,6 +414,27 @@ medusa_status medusa_kv_compact(const medusa_kv_t* cache, const medusa_tree_t* t
                                                as_stream(stream)));
 }
 
+medusa_status medusa_kv_compact_layers(const medusa_kv_t* caches, int32_t n_layers, const medusa_tree_t* t,
+                                       int32_t B, const int32_t* L, const int32_t* accept_len,
+                                       const int32_t* out_rows, int32_t* L_out, int32_t* status,
+                                       void* stream) {
+  if (!caches || n_layers < 1 || n_layers > MEDUSA_MAX_LAYERS || !tree_ok(t) || B < 1 || !L || !accept_len ||
+      !out_rows || !L_out || !status || L_out == L)
+    return MEDUSA_EINVAL;
+  const medusa_kv_t& c0 = caches[0];
+  for (int32_t i = 0; i < n_layers; ++i) {
+    const medusa_kv_t& c = caches[i];
+    if (!kv_ok(&c)) return MEDUSA_EINVAL;
+    // every layer shares the layout: one row offset serves them all
+    if (c.dtype != c0.dtype || c.n_kv_heads != c0.n_kv_heads || c.head_dim != c0.head_dim ||
+        c.capacity != c0.capacity || c.page_size != c0.page_size || c.block_table != c0.block_table ||
+        c.max_blocks != c0.max_blocks || c.n_pages != c0.n_pages)
+      return MEDUSA_EINVAL;
+  }
+  return cuda_status(medusa::launch_kv_compact_layers(caches, n_layers, *t, B, L, accept_len, out_rows, L_out,
+                                                      status, as_stream(stream)));
+}
+
 // ---- whole round as one CUDA graph ------------------------------------------------
 
 struct medusa_round_s {

@@ -338,6 +338,80 @@ def test_kv_compact(m, paged):
         assert (ka == kb).all() and (va == vb).all()
 
 
+@pytest.mark.parametrize("paged,n_layers", [(False, 5), (True, 3), (False, 130)])
+def test_kv_compact_layers(m, paged, n_layers):
+    """Every layer's cache compacted by one call, against the oracle's compaction of
+    each layer; a sequence with an invalid path stays untouched in every layer; more
+    than 128 layers take several launches with status and L_out written once."""
+    if n_layers > 8:      # many small layers: fp32, one KV head of 64 dims
+        w = synth.small_variant(synth.WORKLOADS["tiny-fp32"], batch=4, n_kv_heads=1, n_q_heads=1,
+                                prefix_len=None, prefix_range=(1, 120), seed=141)
+    else:
+        w = synth.small_variant(synth.WORKLOADS["serving-b16-paged"], batch=4, prefix_range=(1, 300),
+                                seed=131 + n_layers, page_size=16 if paged else 0)
+    acc = synth.rank_accuracy(4, 10)
+    t_o = otree.compile_template(otree.greedy_tree(acc, 63), 10)
+    t_g = m.Template(t_o.paths[1:], 10, device="cuda")
+    lengths = synth.prefix_lengths(w)
+    N, W = t_o.n_rows, t_o.max_depth + 1
+    g = torch.Generator(device="cpu").manual_seed(17 + n_layers)
+    caches, Ks, Vs = [], [], []
+    bt = None
+    for layer in range(n_layers):
+        if paged:
+            K, V, bt_l, lay, _, _ = gu.paged_cache(w, lengths, N)
+            bt = bt_l if bt is None else bt            # one block table for every layer
+            caches.append(m.KVCache(K, V, block_table=bt))
+        else:
+            K, V, _, _ = gu.contiguous_cache(w, lengths, N)
+            caches.append(m.KVCache(K, V))
+        K.copy_(torch.randn(K.shape, generator=g).to(K.dtype))
+        V.copy_(torch.randn(V.shape, generator=g).to(V.dtype))
+        Ks.append(K)
+        Vs.append(V)
+    rng = np.random.default_rng(7 + n_layers)
+    rows = np.full((w.batch, W), -1, dtype=np.int32)
+    alen = np.zeros(w.batch, dtype=np.int32)
+    for b in range(w.batch):
+        p = int(rng.integers(0, t_o.n_paths))
+        nodes = [x for x in t_o.retrieve[p] if x >= 0]
+        a = int(rng.integers(1, len(nodes))) if len(nodes) > 1 else 0
+        alen[b] = a
+        rows[b, :a + 1] = nodes[:a + 1]
+    bad = w.batch - 1                    # its second row is not a child of the root
+    deep = next(u for u in range(1, N) if t_o.parent[u] != 0)
+    rows[bad] = -1
+    rows[bad, :2] = [0, deep]
+    alen[bad] = 1
+    before = [(K.cpu().clone(), V.cpu().clone()) for K, V in zip(Ks, Vs)]
+    Ld = gu.device_tensor(lengths, torch.int32)
+    L_out, status = m.medusa_kv_compact_layers(caches, t_g, Ld, gu.device_tensor(alen, torch.int32),
+                                               gu.device_tensor(rows, torch.int32))
+    torch.cuda.synchronize()
+    st = status.cpu().numpy()
+    assert st[bad] == -7 and (np.delete(st, bad) == 0).all()
+    want_L = lengths + alen + 1
+    want_L[bad] = lengths[bad]
+    assert list(L_out.cpu().numpy()) == list(want_L)
+    for layer in range(n_layers):
+        Kb, Vb = before[layer]
+        Ka, Va = Ks[layer].cpu(), Vs[layer].cpu()
+        for b in range(w.batch):
+            L = int(lengths[b])
+            cap = L + N + 16 if not paged else L + N
+            if paged:
+                kb = np.stack([gu.to64(gu.read_paged_row(Kb, bt.cpu(), b, r)) for r in range(cap)], axis=1)
+                vb = np.stack([gu.to64(gu.read_paged_row(Vb, bt.cpu(), b, r)) for r in range(cap)], axis=1)
+                ka = np.stack([gu.to64(gu.read_paged_row(Ka, bt.cpu(), b, r)) for r in range(cap)], axis=1)
+                va = np.stack([gu.to64(gu.read_paged_row(Va, bt.cpu(), b, r)) for r in range(cap)], axis=1)
+            else:
+                kb, vb = gu.to64(Kb[b, :, :cap]), gu.to64(Vb[b, :, :cap])
+                ka, va = gu.to64(Ka[b, :, :cap]), gu.to64(Va[b, :, :cap])
+            if b != bad:
+                ocomp.kv_compact(kb, vb, L, rows[b, :alen[b] + 1])
+            assert np.array_equal(ka, kb) and np.array_equal(va, vb), (layer, b)
+
+
 def test_kv_compact_rejects_bad_paths(m):
     w = synth.small_variant(synth.WORKLOADS["tiny-fp32"], batch=4, seed=111)
     t_o = otree.compile_template(otree.regular_paths((2, 3)), 3)

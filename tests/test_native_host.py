@@ -162,3 +162,25 @@ def test_round_create_rejects_bad_arguments_without_a_gpu(native):
     assert lib.medusa_round_create(C.byref(desc), None, 0, None, C.byref(handle)) == native.EINVAL
     assert lib.medusa_round_launch(None, None) == native.EINVAL
     assert lib.medusa_round_destroy(None) == native.EINVAL
+
+
+def test_kv_compact_layers_checks_layers_without_a_gpu(native):
+    """Host-visible checks of medusa_kv_compact_layers come before any CUDA call:
+    layers that differ in anything but k and v, no layers, or L_out aliasing L are
+    refused with MEDUSA_EINVAL."""
+    from medusa_speculative_tree_gb300.api import Template
+    lib = native.lib()
+    t = Template([(0,), (1,), (0, 0)], 2)
+    fake = lambda i: C.c_void_p(4096 * (i + 1))       # never dereferenced: the checks fail first
+    def layer(i, head_dim=64):
+        c = native.MedusaKV()
+        c.k, c.v, c.dtype, c.n_kv_heads, c.head_dim, c.capacity = fake(2 * i).value, fake(2 * i + 1).value, 0, 2, head_dim, 64
+        c.page_size, c.block_table, c.max_blocks, c.n_pages = 0, None, 0, 0
+        return c
+    L, a, rows, L_out, st = (fake(100 + i) for i in range(5))
+    arr = (native.MedusaKV * 3)(layer(0), layer(1), layer(2, head_dim=128))
+    assert lib.medusa_kv_compact_layers(arr, 3, C.byref(t.host), 2, L, a, rows, L_out, st, None) == native.EINVAL
+    arr = (native.MedusaKV * 2)(layer(0), layer(1))
+    assert lib.medusa_kv_compact_layers(arr, 0, C.byref(t.host), 2, L, a, rows, L_out, st, None) == native.EINVAL
+    assert lib.medusa_kv_compact_layers(arr, 2, C.byref(t.host), 2, L, a, rows, L, st, None) == native.EINVAL
+    assert lib.medusa_kv_compact_layers(None, 2, C.byref(t.host), 2, L, a, rows, L_out, st, None) == native.EINVAL
