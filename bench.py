@@ -297,6 +297,46 @@ def heads_all_rows(rd, stream, peak_tflops):
             "hbm_gbs": passes * rd.head_bytes() / (us * 1e-6) / 1e9}
 
 
+def compact_all_layers(rd, results, stream, flush, n_layers=32):
+    """The winning rows committed in n_layers caches of this workload's layout: one
+    medusa_kv_compact_layers call against n_layers medusa_kv_compact calls, each side a
+    CUDA graph replayed after an L2 flush."""
+    m = rd.m
+    caches = [m.KVCache(torch.empty_like(rd.K), torch.empty_like(rd.V), block_table=rd.cache.block_table)
+              for _ in range(n_layers)]
+    a, rows = results.accept_len, results.out_rows
+    one = lambda: m.medusa_kv_compact_layers(caches, rd.tmpl, rd.L, a, rows)
+    each = lambda: [m.medusa_kv_compact(c, rd.tmpl, rd.L, a, rows) for c in caches]
+    one()
+    each()
+    torch.cuda.synchronize(rd.dev)
+    graphs = {}
+    for name, fn in (("one", one), ("each", each)):
+        g = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(g):
+            fn()
+        graphs[name] = g
+    us = {}
+    for name, g in graphs.items():
+        tot = 0.0
+        for _ in range(10):
+            flush()
+            e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            e0.record(stream)
+            g.replay()
+            e1.record(stream)
+            e1.synchronize()
+            tot += e0.elapsed_time(e1) * 1e3
+        us[name] = tot / 10
+    w = rd.w
+    eb = 4 if w.dtype == "f32" else 2
+    moved = int((a.to(torch.int64) + 1).sum()) * 2 * w.n_kv_heads * w.head_dim * eb * 2 * n_layers
+    del caches, graphs
+    torch.cuda.empty_cache()
+    return {"layers": n_layers, "one_call_us": us["one"], "per_layer_calls_us": us["each"],
+            "bytes_read_and_written": moved}
+
+
 def time_loop(fn, steps, stream):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -524,6 +564,7 @@ def main():
     e2e_ms, h2d, d2h = e2e_loop(rd, max(10, args.steps // 4), stream)
     e2e_ms = max_over_ranks(e2e_ms, ws, dev)
     all_rows = heads_all_rows(rd, stream, bf16) if rank == 0 else None
+    layers = compact_all_layers(rd, graphs.native, stream, flush) if rank == 0 else None
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -545,6 +586,7 @@ def main():
                          "frac": heads_gbs / hbm, "traffic": HEADS_TRAFFIC.get(w.name), "peak_source": src,
                          "algorithmic_bytes": rd.head_bytes(), "launch_us": heads_us},
             "heads_all_rows": all_rows,
+            "kv_compact_layers": layers,
             "round_roofline": {"bound": "hbm", "achieved": round_gbs, "peak": hbm, "unit": "GB/s",
                                "frac": round_gbs / hbm, "peak_source": src, "algorithmic_bytes": round_b,
                                "note": "all five steps' algorithmic bytes over one round's device time"},
