@@ -139,3 +139,29 @@ def accept(logits, tokens, retrieve, mode: str = "greedy", temperature: float = 
     return AcceptResult(best_path=best, accept_len=best_len, out_rows=rows,
                         out_tokens=tokens[rows], frontier_row=int(rows[-1]),
                         per_path_len=lens, per_path_score=scores, margins=margins)
+
+
+def target_logits(hidden, w_lm, rows=None) -> np.ndarray:
+    """The target's vocabulary projection of the tree rows, logits[u] = W_LM hidden[u],
+    in float64 ([M7.2] §0x07B: C_LMproj(N) with F_LMproj = 2 N d V; §0x07C: dense
+    target logits hold N V elements).  Only `rows` are computed (default: every row);
+    the others are NaN, since acceptance reads internal rows only.
+
+    hidden [N, d]; w_lm [V, d].
+    """
+    h = np.asarray(hidden, dtype=np.float64)
+    w = np.asarray(w_lm, dtype=np.float64)
+    out = np.full((h.shape[0], w.shape[0]), np.nan)
+    for u in (range(h.shape[0]) if rows is None else rows):
+        out[int(u)] = w @ h[int(u)]
+    return out
+
+
+def accept_hidden(hidden, w_lm, tokens, retrieve, internal, mode: str = "greedy", temperature: float = 1.0,
+                  epsilon: float = 0.09, delta: float = 0.3) -> AcceptResult:
+    """Acceptance with the target's vocabulary projection folded in: the projection of
+    every internal row (`internal`: rows with children), then `accept` on those rows.
+    Leaves are never projected; no other row is read by acceptance ([M7.2] §0x07B:
+    a unique-row posterior instead of gathered path logits)."""
+    logits = target_logits(hidden, w_lm, internal)
+    return accept(logits, tokens, retrieve, mode, temperature, epsilon, delta)

@@ -184,3 +184,77 @@ def test_compact_overlap_needs_snapshot():
     cv = ck.copy()
     compact.kv_compact(ck, cv, 0, [0, 2, 5])
     assert list(ck[0, :3, 0]) == [0.0, 2.0, 5.0]
+
+
+# ---- the target's vocabulary projection folded into acceptance -----------------------
+
+def _internal(t):
+    return [u for u in range(t.n_rows) if (np.asarray(t.parent) == u).any()]
+
+
+def test_target_logits_identity_projection_reduces_to_accept():
+    """W_LM = I (V = d): the projection returns the internal hidden rows themselves
+    (leaves stay NaN: acceptance must never read them), so acceptance on hidden rows
+    equals acceptance on those rows taken as logits, which the fixtures above pin."""
+    rng = np.random.default_rng(5)
+    t = tree.compile_template(tree.regular_paths((2, 3)), 3)
+    N, d = t.n_rows, 16
+    hidden = rng.normal(size=(N, d))
+    internal = _internal(t)
+    lg = accept.target_logits(hidden, np.eye(d), internal)
+    for u in range(N):
+        if u in internal:
+            assert np.array_equal(lg[u], hidden[u])
+        else:
+            assert np.isnan(lg[u]).all()
+    tokens = rng.integers(0, d, size=N)
+    for v in range(1, N):                      # half the candidates are the parent's argmax
+        if rng.random() < 0.5:
+            tokens[v] = int(np.argmax(hidden[t.parent[v]]))
+    for mode in ("greedy", "typical"):
+        a = accept.accept_hidden(hidden, np.eye(d), tokens, t.retrieve, internal, mode)
+        b = accept.accept(np.where(np.isnan(lg), 0.0, lg), tokens, t.retrieve, mode)
+        assert (a.best_path, a.accept_len, a.frontier_row) == (b.best_path, b.accept_len, b.frontier_row)
+        assert list(a.out_rows) == list(b.out_rows) and list(a.out_tokens) == list(b.out_tokens)
+
+
+def test_target_logits_one_hot_closed_form():
+    """Orthonormal rows of W_LM (V = 8 < d = 12) and hidden[u] = alpha W_LM[t_u]: the
+    logits are alpha at t_u and 0 elsewhere, so argmax = t_u,
+    p(t_u) = e^alpha / (e^alpha + V - 1) and
+    H = ln(e^alpha + V - 1) - alpha e^alpha / (e^alpha + V - 1).
+    With alpha = 5: p(t_u) = .955 > min(.09, .3 e^-H) = .09, while every other token has
+    p = .0064 < .09.  Child 0 of each internal row carries t_u, the others a different
+    token, so both greedy and typical accept exactly the all-zero-rank path: rows
+    [0, row(0), row(0, 0)], a = 2."""
+    V_, d, alpha = 8, 12, 5.0
+    rng = np.random.default_rng(9)
+    q, _ = np.linalg.qr(rng.normal(size=(d, d)))
+    W = q[:V_]                                  # orthonormal rows
+    t = tree.compile_template(tree.regular_paths((2, 3)), 3)
+    N = t.n_rows
+    internal = _internal(t)
+    target = {u: int(rng.integers(0, V_)) for u in internal}
+    hidden = np.zeros((N, d))
+    for u in internal:
+        hidden[u] = alpha * W[target[u]]
+    tokens = np.zeros(N, dtype=np.int64)
+    for v in range(1, N):
+        p = int(t.parent[v])
+        rank = t.paths[v][-1]
+        tokens[v] = target[p] if rank == 0 else (target[p] + 1 + rank) % V_
+    lg = accept.target_logits(hidden, W, internal)
+    ea = math.exp(alpha)
+    for u in internal:
+        want = np.zeros(V_)
+        want[target[u]] = alpha
+        assert np.allclose(lg[u], want, atol=1e-12)
+        st = accept.row_stats(lg[u])
+        assert st.argmax == target[u]
+        assert math.isclose(st.entropy, math.log(ea + V_ - 1) - alpha * ea / (ea + V_ - 1), rel_tol=1e-12)
+    row = {tuple(p): i for i, p in enumerate(t.paths)}
+    for mode in ("greedy", "typical"):
+        r = accept.accept_hidden(hidden, W, tokens, t.retrieve, internal, mode, epsilon=EPS, delta=DELTA)
+        assert r.accept_len == 2
+        assert list(r.out_rows) == [0, row[(0,)], row[(0, 0)]]
+        assert list(r.out_tokens) == [tokens[0], target[0], target[row[(0,)]]]
