@@ -294,6 +294,33 @@ medusa_status medusa_tree_accept(const medusa_tree_t *t, int32_t B, int32_t V, c
                                  int32_t *out_tokens, int32_t *out_rows, int32_t *frontier_row,
                                  void *ws, size_t ws_bytes, void *stream);
 
+size_t medusa_tree_accept_hidden_workspace(const medusa_tree_t *t, int32_t B, int32_t V, int32_t d);
+
+/* medusa_tree_accept with the target's vocabulary projection folded in ([M7.2] §0x07B:
+ * the projection C_LMproj with F_LMproj = 2 N d V and a unique-row posterior; §0x07C:
+ * dense target logits hold N V elements).  For each internal row u of sequence b the
+ * logits x = W_LM hidden[b][u] are computed on the tensor cores (bf16 operands, fp32
+ * accumulation) and reduced at once to what acceptance reads: the argmax, and for
+ * typical acceptance the max, partition function and first moment of x / T and x at
+ * the token of each child of u.  The [rows x V] logits are never written; leaves are
+ * not projected.  Decisions are those of medusa_tree_accept on the same fp32 logits,
+ * up to the summation order of the projection.
+ *   hidden [B][N][d] bf16: the target's final hidden state of every tree row;
+ *   w_lm [V][d] bf16; tokens, mode, temperature, epsilon, delta and the outputs as in
+ *   medusa_tree_accept (the guarded entropy is not offered: it needs a second pass
+ *   over the logits).  W_LM is streamed once per 256 internal rows of the batch.
+ * A bounded device wait that gives up makes every sequence publish nothing:
+ * best_path = accept_len = frontier_row = -1 and out_rows, out_tokens all -1 (the
+ * following medusa_kv_compact then rejects the sequence).
+ * ws: medusa_tree_accept_hidden_workspace(...) bytes, 16-byte aligned.
+ * Limits: d a multiple of 64; MEDUSA_EUNSUPPORTED otherwise. */
+medusa_status medusa_tree_accept_hidden(const medusa_tree_t *t, int32_t B, int32_t V, int32_t d,
+                                        const void *hidden, const void *w_lm, const int32_t *tokens,
+                                        int32_t mode, float temperature, float epsilon, float delta,
+                                        int32_t *best_path, int32_t *accept_len, int32_t *out_tokens,
+                                        int32_t *out_rows, int32_t *frontier_row, void *ws, size_t ws_bytes,
+                                        void *stream);
+
 /* ---------------------------------------------------------------------------
  * Round step 5: winning-path K/V compaction
  * ------------------------------------------------------------------------- */

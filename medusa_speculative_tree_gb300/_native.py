@@ -23,7 +23,7 @@ EXPORTED = [
     "medusa_tree_upload", "medusa_heads_topk_workspace", "medusa_heads_topk", "medusa_tree_fill",
     "medusa_tree_attn_workspace", "medusa_tree_attn_verify", "medusa_tree_attn_verify_static",
     "medusa_tree_accept_workspace",
-    "medusa_tree_accept", "medusa_kv_compact", "medusa_kv_compact_layers", "medusa_round_workspace", "medusa_round_create",
+    "medusa_tree_accept", "medusa_tree_accept_hidden_workspace", "medusa_tree_accept_hidden", "medusa_kv_compact", "medusa_kv_compact_layers", "medusa_round_workspace", "medusa_round_create",
     "medusa_round_launch", "medusa_round_destroy", "medusa_status_string", "medusa_abi_version",
 ]
 
@@ -102,6 +102,9 @@ def lib() -> C.CDLL:
         "medusa_tree_accept_workspace": (SZ, [P(MedusaTree), I32, I32]),
         "medusa_tree_accept": (I32, [P(MedusaTree), I32, I32, VP, I32, VP, I32, F, F, F, I32, VP, VP,
                                      VP, VP, VP, VP, SZ, VP]),
+        "medusa_tree_accept_hidden_workspace": (SZ, [P(MedusaTree), I32, I32, I32]),
+        "medusa_tree_accept_hidden": (I32, [P(MedusaTree), I32, I32, I32, VP, VP, VP, I32, F, F, F, VP, VP, VP, VP,
+                                            VP, VP, SZ, VP]),
         "medusa_kv_compact": (I32, [P(MedusaKV), P(MedusaTree), I32, VP, VP, VP, VP, VP, VP]),
         "medusa_kv_compact_layers": (I32, [P(MedusaKV), I32, P(MedusaTree), I32, VP, VP, VP, VP, VP, VP]),
         "medusa_round_workspace": (SZ, [P(MedusaRoundDesc)]),

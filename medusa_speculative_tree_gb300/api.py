@@ -275,6 +275,31 @@ def medusa_tree_accept(tmpl: Template, logits, tokens, mode: str = "greedy", tem
     return r
 
 
+def medusa_tree_accept_hidden(tmpl: Template, hidden, w_lm, tokens, mode: str = "greedy",
+                              temperature: float = 1.0, epsilon: float = 0.09, delta: float = 0.3):
+    """medusa_tree_accept on the target's final hidden states: the vocabulary projection
+    of the internal rows is folded in (hidden [B, N, d] bf16, w_lm [V, d] bf16)."""
+    _need_cuda(hidden, w_lm, tokens)
+    B, N, d = hidden.shape
+    V = w_lm.shape[0]
+    dev = hidden.device
+    W = tmpl.max_depth + 1
+    r = {k: torch.empty(B, dtype=torch.int32, device=dev) for k in ("best_path", "accept_len", "frontier_row")}
+    r["out_tokens"] = torch.empty((B, W), dtype=torch.int32, device=dev)
+    r["out_rows"] = torch.empty((B, W), dtype=torch.int32, device=dev)
+    nb = lib().medusa_tree_accept_hidden_workspace(C.byref(tmpl.dev), B, V, d)
+    if nb == 0:
+        raise ValueError("invalid acceptance shapes")
+    ws = _WS.get("accept_hidden", nb, dev)
+    m = nat.GREEDY if mode == "greedy" else nat.TYPICAL
+    check("medusa_tree_accept_hidden",
+          lib().medusa_tree_accept_hidden(C.byref(tmpl.dev), B, V, d, _ptr(hidden), _ptr(w_lm), _ptr(tokens), m,
+                                          float(temperature), float(epsilon), float(delta), _ptr(r["best_path"]),
+                                          _ptr(r["accept_len"]), _ptr(r["out_tokens"]), _ptr(r["out_rows"]),
+                                          _ptr(r["frontier_row"]), _ptr(ws), ws.numel(), _stream(dev)))
+    return r
+
+
 def medusa_kv_compact(cache: KVCache, tmpl: Template, L, accept_len, out_rows):
     """L_out [B], status [B] int32; the cache is compacted in place."""
     _need_cuda(L, accept_len, out_rows)

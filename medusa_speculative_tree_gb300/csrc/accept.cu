@@ -24,15 +24,6 @@ constexpr int kLoads = 4;          // 16-byte loads in flight per thread in row_
 constexpr int kSelThreads = 1024;  // select: one warp per internal row, 32 rows at a time
 constexpr int kSelWarps = kSelThreads / 32;
 
-struct RowPart {
-  float m;      // max of x / T over the chunk
-  float z;      // sum exp(x/T - m)
-  float s1;     // sum exp(x/T - m) * (x/T - m)
-  float amax_v; // largest raw logit
-  int amax_i;   // its id (lowest among equal values)
-  int pad[3];
-};
-
 // Merge two partial statistics (log-sum-exp with first moment).
 __device__ __forceinline__ void merge_stats(float& m, float& z, float& s1, float m2, float z2, float s12) {
   if (z2 <= 0.f) return;
@@ -217,6 +208,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     medusa_tree_t t, int V, int n_chunks, const EL* __restrict__ logits,
     const int32_t* __restrict__ tokens, int mode, float inv_temp, float epsilon, float delta,
     const RowPart* __restrict__ part, const float* __restrict__ guard, SelectSmem lay,
+    const float* __restrict__ edge_x, const int* __restrict__ err,
     int32_t* __restrict__ best_path, int32_t* __restrict__ accept_len,
     int32_t* __restrict__ out_tokens, int32_t* __restrict__ out_rows,
     int32_t* __restrict__ frontier_row) {
@@ -234,6 +226,19 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool typ = mode != MEDUSA_ACCEPT_GREEDY;
   const int32_t* tok = tokens + (int64_t)b * N;
+  if (err && *reinterpret_cast<const volatile int*>(err) != 0) {
+    // the statistics were not completed (a bounded wait gave up): publish nothing
+    if (threadIdx.x == 0) {
+      best_path[b] = -1;
+      accept_len[b] = -1;
+      frontier_row[b] = -1;
+    }
+    for (int j = threadIdx.x; j < W; j += kSelThreads) {
+      out_rows[(int64_t)b * W + j] = -1;
+      out_tokens[(int64_t)b * W + j] = -1;
+    }
+    return;
+  }
   // 0. the inputs of every edge parent(v) -> v (a thread's edges are v = 1 + tid +
   //    k kSelThreads, k < kEdges since N <= MEDUSA_MAX_ROWS): parent, its internal row,
   //    the candidate token and (typical) its raw logit, all requested up front so that
@@ -254,7 +259,11 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
       const int v = 1 + threadIdx.x + k * kSelThreads;
       e_ii[k] = v < N ? t.internal_index[e_u[k]] : 0;
       const bool need = typ && v < N && e_ct[k] >= 0 && e_ct[k] < V;
-      e_x[k] = need ? Elem<EL>::load(logits, ((int64_t)b * N + e_u[k]) * V + e_ct[k]) * inv_temp : 0.f;
+      // the logit of v's token at its parent: from the logits, or (projection folded
+      // in) the value the statistics kernel recorded for this edge
+      e_x[k] = !need ? 0.f
+                     : (edge_x ? edge_x[(int64_t)b * N + v]
+                               : Elem<EL>::load(logits, ((int64_t)b * N + e_u[k]) * V + e_ct[k])) * inv_temp;
     }
   }
   // 1. merged statistics per internal row (one warp per row, one lane per chunk) and
@@ -445,15 +454,32 @@ cudaError_t launch_accept(const AcceptPlan& p, const medusa_tree_t& t, const voi
     e = cudaFuncSetAttribute(select_kernel<uint16_t>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lay.bytes);
     if (e != cudaSuccess) return e;
     select_kernel<uint16_t><<<p.B, kSelThreads, lay.bytes, st>>>(t, p.V, p.n_chunks, (const uint16_t*)logits, tokens,
-                                                              mode, inv_t, epsilon, delta, part, gptr, lay, best_path,
-                                                              accept_len, out_tokens, out_rows, frontier_row);
+                                                              mode, inv_t, epsilon, delta, part, gptr, lay, nullptr,
+                                                              nullptr, best_path, accept_len, out_tokens, out_rows,
+                                                              frontier_row);
   } else {
     e = cudaFuncSetAttribute(select_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lay.bytes);
     if (e != cudaSuccess) return e;
     select_kernel<float><<<p.B, kSelThreads, lay.bytes, st>>>(t, p.V, p.n_chunks, (const float*)logits, tokens, mode,
-                                                           inv_t, epsilon, delta, part, gptr, lay, best_path,
-                                                           accept_len, out_tokens, out_rows, frontier_row);
+                                                           inv_t, epsilon, delta, part, gptr, lay, nullptr, nullptr,
+                                                           best_path, accept_len, out_tokens, out_rows, frontier_row);
   }
+  return cudaGetLastError();
+}
+
+cudaError_t launch_select_parts(const medusa_tree_t& t, int B, int V, int n_chunks, const RowPart* part,
+                                const float* edge_x, const int* err, const int32_t* tokens, int mode,
+                                float temperature, float epsilon, float delta, int32_t* best_path,
+                                int32_t* accept_len, int32_t* out_tokens, int32_t* out_rows,
+                                int32_t* frontier_row, cudaStream_t st) {
+  const SelectSmem lay = select_smem(t, n_chunks, false);
+  cudaError_t e = cudaFuncSetAttribute(select_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       (int)lay.bytes);
+  if (e != cudaSuccess) return e;
+  select_kernel<float><<<B, kSelThreads, lay.bytes, st>>>(t, V, n_chunks, nullptr, tokens, mode, 1.f / temperature,
+                                                         epsilon, delta, part, nullptr, lay, edge_x, err,
+                                                         best_path, accept_len, out_tokens, out_rows,
+                                                         frontier_row);
   return cudaGetLastError();
 }
 

@@ -72,6 +72,16 @@ cudaError_t launch_attn(const AttnPlan& p, const medusa_tree_t& t, const void* q
                         int32_t* status, void* ws, cudaStream_t st);
 
 // ---- acceptance -------------------------------------------------------------------
+// Statistics of one chunk of one internal row's logits, merged by the select kernel.
+struct RowPart {
+  float m;      // max of x / T over the chunk
+  float z;      // sum exp(x/T - m)
+  float s1;     // sum exp(x/T - m) * (x/T - m)
+  float amax_v; // largest raw logit
+  int amax_i;   // its id (lowest among equal values)
+  int pad[3];
+};
+
 struct AcceptPlan {
   int B, V, chunk, n_chunks;
   size_t off_part, off_guard, bytes;
@@ -82,6 +92,27 @@ cudaError_t launch_accept(const AcceptPlan& p, const medusa_tree_t& t, const voi
                           float epsilon, float delta, int entropy_guard, int32_t* best_path,
                           int32_t* accept_len, int32_t* out_tokens, int32_t* out_rows,
                           int32_t* frontier_row, void* ws, cudaStream_t st);
+
+// The select step alone, on chunk statistics and per-edge logits written by another
+// kernel (edge_x [B][N]: the logit of row v's token at its parent); err (nullable)
+// non-zero makes every sequence publish nothing (accept_len = -1).
+cudaError_t launch_select_parts(const medusa_tree_t& t, int B, int V, int n_chunks, const RowPart* part,
+                                const float* edge_x, const int* err, const int32_t* tokens, int mode,
+                                float temperature, float epsilon, float delta, int32_t* best_path,
+                                int32_t* accept_len, int32_t* out_tokens, int32_t* out_rows,
+                                int32_t* frontier_row, cudaStream_t st);
+
+// Acceptance with the target's vocabulary projection folded in (lm_accept.cu).
+struct LmAcceptPlan {
+  int B, V, d, NI, cols, cols_pad, n_chunks;
+  size_t off_x, off_etok, off_erow, off_ecnt, off_edge_x, off_part, off_err, bytes;
+};
+LmAcceptPlan plan_lm_accept(const medusa_tree_t& t, int B, int V, int d);
+bool lm_accept_supported(int d, int V);
+cudaError_t launch_lm_accept(const LmAcceptPlan& p, const medusa_tree_t& t, const void* hidden, const void* w_lm,
+                             const int32_t* tokens, int mode, float temperature, float epsilon, float delta,
+                             int32_t* best_path, int32_t* accept_len, int32_t* out_tokens, int32_t* out_rows,
+                             int32_t* frontier_row, void* ws, cudaStream_t st);
 
 // ---- compaction -----------------------------------------------------------------------
 cudaError_t launch_kv_compact(const medusa_kv_t& c, const medusa_tree_t& t, int B,

@@ -404,6 +404,30 @@ medusa_status medusa_tree_accept(const medusa_tree_t* t, int32_t B, int32_t V, c
                                            out_rows, frontier_row, ws, as_stream(stream)));
 }
 
+size_t medusa_tree_accept_hidden_workspace(const medusa_tree_t* t, int32_t B, int32_t V, int32_t d) {
+  if (!tree_ok(t) || B < 1 || V < 1 || d < 1) return 0;
+  return medusa::plan_lm_accept(*t, B, V, d).bytes;
+}
+
+medusa_status medusa_tree_accept_hidden(const medusa_tree_t* t, int32_t B, int32_t V, int32_t d,
+                                        const void* hidden, const void* w_lm, const int32_t* tokens, int32_t mode,
+                                        float temperature, float epsilon, float delta, int32_t* best_path,
+                                        int32_t* accept_len, int32_t* out_tokens, int32_t* out_rows,
+                                        int32_t* frontier_row, void* ws, size_t ws_bytes, void* stream) {
+  if (!tree_ok(t) || B < 1 || V < 1 || d < 1 || !hidden || !w_lm || !tokens || !best_path || !accept_len ||
+      !out_tokens || !out_rows || !frontier_row || !ws ||
+      (mode != MEDUSA_ACCEPT_GREEDY && mode != MEDUSA_ACCEPT_TYPICAL) || !(temperature > 0.0f) ||
+      !std::isfinite(temperature) || !(epsilon >= 0.0f) || !(delta >= 0.0f))
+    return MEDUSA_EINVAL;
+  if (!aligned16(hidden) || !aligned16(w_lm) || !aligned16(ws)) return MEDUSA_EINVAL;
+  if (!medusa::lm_accept_supported(d, V)) return MEDUSA_EUNSUPPORTED;
+  const medusa::LmAcceptPlan p = medusa::plan_lm_accept(*t, B, V, d);
+  if (ws_bytes < p.bytes) return MEDUSA_EWORKSPACE;
+  return cuda_status(medusa::launch_lm_accept(p, *t, hidden, w_lm, tokens, mode, temperature, epsilon, delta,
+                                              best_path, accept_len, out_tokens, out_rows, frontier_row, ws,
+                                              as_stream(stream)));
+}
+
 medusa_status medusa_kv_compact(const medusa_kv_t* cache, const medusa_tree_t* t, int32_t B,
                                 const int32_t* L, const int32_t* accept_len,
                                 const int32_t* out_rows, int32_t* L_out, int32_t* status,
