@@ -337,6 +337,44 @@ def compact_all_layers(rd, results, stream, flush, n_layers=32):
             "bytes_read_and_written": moved}
 
 
+def accept_hidden(rd, results, stream, flush, hbm_peak):
+    """Acceptance with the target's vocabulary projection folded in (hidden states of
+    every tree row, bf16, seeded N(0, 1)) on this workload's W_LM and tree tokens: a
+    CUDA graph replayed after an L2 flush.  Bound: W_LM streamed once per 256 internal
+    rows of the batch."""
+    w = rd.w
+    if w.dtype != "bf16":
+        return None
+    m = rd.m
+    hidden = synth.normal((w.batch, rd.N, w.hidden), 1.0, w.seed, "h", rd.dev, w.torch_dtype, sub=2)
+    tokens = results.tokens
+    call = lambda: m.medusa_tree_accept_hidden(rd.tmpl, hidden, rd.w_lm, tokens, rd.mode, epsilon=w.epsilon,
+                                               delta=w.delta)
+    call()
+    torch.cuda.synchronize(rd.dev)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        call()
+    tot = 0.0
+    reps = 10
+    for _ in range(reps):
+        flush()
+        e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        g.replay()
+        e1.record(stream)
+        e1.synchronize()
+        tot += e0.elapsed_time(e1) * 1e3
+    us = tot / reps
+    rows = w.batch * rd.tmpl.n_internal
+    passes = math.ceil(rows / 256)
+    wbytes = passes * rd.w_lm.numel() * rd.w_lm.element_size()
+    gbs = wbytes / (us * 1e-6) / 1e9
+    del g
+    return {"internal_rows": rows, "us": us, "w_lm_passes": passes, "bytes": wbytes, "hbm_gbs": gbs,
+            "frac": gbs / hbm_peak, "tflops": 2.0 * rows * w.hidden * w.vocab / (us * 1e-6) / 1e12}
+
+
 def time_loop(fn, steps, stream):
     start = torch.cuda.Event(enable_timing=True)
     end = torch.cuda.Event(enable_timing=True)
@@ -565,6 +603,7 @@ def main():
     e2e_ms = max_over_ranks(e2e_ms, ws, dev)
     all_rows = heads_all_rows(rd, stream, bf16) if rank == 0 else None
     layers = compact_all_layers(rd, graphs.native, stream, flush) if rank == 0 else None
+    acc_h = accept_hidden(rd, graphs.native, stream, flush, hbm) if rank == 0 else None
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
@@ -587,6 +626,7 @@ def main():
                          "algorithmic_bytes": rd.head_bytes(), "launch_us": heads_us},
             "heads_all_rows": all_rows,
             "kv_compact_layers": layers,
+            "accept_hidden": acc_h,
             "round_roofline": {"bound": "hbm", "achieved": round_gbs, "peak": hbm, "unit": "GB/s",
                                "frac": round_gbs / hbm, "peak_source": src, "algorithmic_bytes": round_b,
                                "note": "all five steps' algorithmic bytes over one round's device time"},
