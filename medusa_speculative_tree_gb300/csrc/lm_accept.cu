@@ -73,11 +73,13 @@ __device__ __forceinline__ bool l_wait(uint32_t bar, uint32_t parity, const vola
 
 // One block per column: its hidden row into X (zeros for padding columns) and its
 // children, found by one warp scanning the parent array in ascending row order.
+// Block 0 also clears the error flag of this call.
 __global__ void lm_gather_kernel(medusa_tree_t t, int B, int d, const uint16_t* __restrict__ hidden,
                                  const int32_t* __restrict__ tokens, uint16_t* __restrict__ X,
                                  int32_t* __restrict__ e_tok, int32_t* __restrict__ e_row,
-                                 int32_t* __restrict__ e_cnt) {
+                                 int32_t* __restrict__ e_cnt, int* __restrict__ err) {
   const int col = blockIdx.x;
+  if (col == 0 && threadIdx.x == 0) *err = 0;
   const int NI = t.n_internal, N = t.n_rows;
   const bool valid = col < B * NI;
   const int b = valid ? col / NI : 0;
@@ -456,12 +458,13 @@ cudaError_t launch_lm_accept(const LmAcceptPlan& p, const medusa_tree_t& t, cons
   float* edge_x = reinterpret_cast<float*>(base + p.off_edge_x);
   RowPart* part = reinterpret_cast<RowPart*>(base + p.off_part);
   int* err = reinterpret_cast<int*>(base + p.off_err);
-  cudaError_t e = cudaMemsetAsync(err, 0, sizeof(int), st);
-  if (e != cudaSuccess) return e;
+  cudaError_t e;
   const bool typ = mode == MEDUSA_ACCEPT_TYPICAL;
-  if (p.cols > 0) {
+  if (p.cols == 0) {
+    if ((e = cudaMemsetAsync(err, 0, sizeof(int), st)) != cudaSuccess) return e;
+  } else {
     lm_gather_kernel<<<p.cols_pad, 256, 0, st>>>(t, p.B, p.d, (const uint16_t*)hidden, tokens, X, e_tok, e_row,
-                                                 e_cnt);
+                                                 e_cnt, err);
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     CUtensorMap mw;
     if (!encode_rows(&mw, w_lm, p.d, p.V, kLRows)) return cudaErrorInvalidValue;
