@@ -396,6 +396,10 @@ typedef struct {
   int32_t *best_path, *accept_len, *out_tokens, *out_rows, *frontier_row;
   /* step 5: medusa_kv_compact */
   int32_t *L_out, *compact_status;   /* [B], [B] */
+  /* step 4 alternative: when non-NULL, acceptance is medusa_tree_accept_hidden on the
+   * target's final hidden states [B][N][d] (bf16, the heads' d) with the same w_lm,
+   * and `logits` is not read (it may be NULL) */
+  const void *hidden_target;
 } medusa_round_desc;
 
 typedef struct medusa_round_s *medusa_round_t;

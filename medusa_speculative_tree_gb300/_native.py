@@ -61,7 +61,7 @@ class MedusaRoundDesc(C.Structure):
         ("delta", C.c_float), ("entropy_guard", C.c_int32),
         ("best_path", C.c_void_p), ("accept_len", C.c_void_p), ("out_tokens", C.c_void_p),
         ("out_rows", C.c_void_p), ("frontier_row", C.c_void_p),
-        ("L_out", C.c_void_p), ("compact_status", C.c_void_p),
+        ("L_out", C.c_void_p), ("compact_status", C.c_void_p), ("hidden_target", C.c_void_p),
     ]
 
 

@@ -338,7 +338,10 @@ class MedusaRound:
     values into them (copy_) before a launch.  The outputs are tensors allocated here
     and overwritten by every launch: root, pool, tokens, pos, out, lse (or None),
     attn_status, best_path, accept_len, out_tokens, out_rows, frontier_row, L_out,
-    compact_status.  The heads run on one frontier row per sequence (h is [B, d])."""
+    compact_status.  The heads run on one frontier row per sequence (h is [B, d]).
+    With hidden_target ([B, N, d] bf16, the target's final hidden states of the tree
+    rows) acceptance projects the internal rows through w_lm itself
+    (medusa_tree_accept_hidden) and logits may be None."""
 
     _OUT = ("root", "pool", "tokens", "pos", "out", "lse", "attn_status", "best_path", "accept_len",
             "out_tokens", "out_rows", "frontier_row", "L_out", "compact_status")
@@ -347,15 +350,18 @@ class MedusaRound:
                  max_prefix: int, logits, mode: str = "greedy", rope_base: float = 10000.0,
                  scale: Optional[float] = None, temperature: float = 1.0, epsilon: float = 0.09,
                  delta: float = 0.3, entropy_guard: bool = False, b1=None, shared_w2: bool = False,
-                 want_lse: bool = False):
-        _need_cuda(h, w1, w2, w_lm, b1, L, q, k_new, v_new, logits)
+                 want_lse: bool = False, hidden_target=None):
+        _need_cuda(h, w1, w2, w_lm, b1, L, q, k_new, v_new, logits, hidden_target)
         B, d = h.shape
         V, K, N = w_lm.shape[0], w1.shape[0], tmpl.n_rows
         Bq, Nq, Hq, dh = q.shape
-        if Bq != B or Nq != N or tuple(logits.shape) != (B, N, V) or tuple(L.shape) != (B,):
+        if Bq != B or Nq != N or tuple(L.shape) != (B,):
             raise ValueError("inconsistent round shapes")
-        if logits.dtype != h.dtype:
-            raise ValueError("logits and hidden rows must share a dtype")
+        if hidden_target is None:
+            if logits is None or tuple(logits.shape) != (B, N, V) or logits.dtype != h.dtype:
+                raise ValueError("logits must be [B, N, V] in the dtype of the hidden rows")
+        elif tuple(hidden_target.shape) != (B, N, d) or hidden_target.dtype != h.dtype:
+            raise ValueError("hidden_target must be [B, N, d] in the dtype of the hidden rows")
         dev = h.device
         i32 = dict(dtype=torch.int32, device=dev)
         W = tmpl.max_depth + 1
@@ -374,7 +380,7 @@ class MedusaRound:
         self.L_out = torch.empty(B, **i32)
         self.compact_status = torch.empty(B, **i32)
         # the graph records addresses: keep every input alive as long as the round
-        self._inputs = (tmpl, h, w1, w2, w_lm, b1, L, q, k_new, v_new, cache, logits)
+        self._inputs = (tmpl, h, w1, w2, w_lm, b1, L, q, k_new, v_new, cache, logits, hidden_target)
         r = nat.MedusaRoundDesc()
         r.tree = tmpl.dev
         r.B, r.dtype = B, _dtype_code(h.dtype)
@@ -390,7 +396,8 @@ class MedusaRound:
         r.scale = float(scale) if scale is not None else 1.0 / float(dh) ** 0.5
         r.out, r.lse = self.out.data_ptr(), (self.lse.data_ptr() if self.lse is not None else None)
         r.attn_status = self.attn_status.data_ptr()
-        r.logits = logits.data_ptr()
+        r.logits = logits.data_ptr() if logits is not None else None
+        r.hidden_target = hidden_target.data_ptr() if hidden_target is not None else None
         r.mode = nat.GREEDY if mode == "greedy" else nat.TYPICAL
         r.temperature, r.epsilon, r.delta = float(temperature), float(epsilon), float(delta)
         r.entropy_guard = int(entropy_guard)

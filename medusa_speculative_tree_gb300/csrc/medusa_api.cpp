@@ -477,7 +477,8 @@ bool round_ws(const medusa_round_desc* r, RoundWs& w) {
   if (!r || !tree_ok(&r->tree) || !kv_ok(&r->cache) || r->B < 1) return false;
   const size_t h = medusa_heads_topk_workspace(r->B, r->d, r->V, r->K, r->topk);
   const size_t a = medusa_tree_attn_workspace(&r->tree, r->B, r->n_q_heads, &r->cache, r->max_prefix);
-  const size_t c = medusa_tree_accept_workspace(&r->tree, r->B, r->V);
+  const size_t c = r->hidden_target ? medusa_tree_accept_hidden_workspace(&r->tree, r->B, r->V, r->d)
+                                    : medusa_tree_accept_workspace(&r->tree, r->B, r->V);
   if (h == 0 || a == 0 || c == 0) return false;
   w.attn = align_up(h, 256);
   w.accept = w.attn + align_up(a, 256);
@@ -496,9 +497,14 @@ medusa_status record_round(const medusa_round_desc* r, char* ws, const RoundWs& 
                               r->max_prefix, r->rope_base, r->scale, r->out, r->lse, r->attn_status,
                               ws + w.attn, w.accept - w.attn, st);
   if (s != MEDUSA_OK) return s;
-  s = medusa_tree_accept(&r->tree, r->B, r->V, r->logits, r->dtype, r->tokens, r->mode, r->temperature,
-                         r->epsilon, r->delta, r->entropy_guard, r->best_path, r->accept_len, r->out_tokens,
-                         r->out_rows, r->frontier_row, ws + w.accept, w.total - w.accept, st);
+  if (r->hidden_target)
+    s = medusa_tree_accept_hidden(&r->tree, r->B, r->V, r->d, r->hidden_target, r->w_lm, r->tokens, r->mode,
+                                  r->temperature, r->epsilon, r->delta, r->best_path, r->accept_len,
+                                  r->out_tokens, r->out_rows, r->frontier_row, ws + w.accept, w.total - w.accept, st);
+  else
+    s = medusa_tree_accept(&r->tree, r->B, r->V, r->logits, r->dtype, r->tokens, r->mode, r->temperature,
+                           r->epsilon, r->delta, r->entropy_guard, r->best_path, r->accept_len, r->out_tokens,
+                           r->out_rows, r->frontier_row, ws + w.accept, w.total - w.accept, st);
   if (s != MEDUSA_OK) return s;
   return medusa_kv_compact(&r->cache, &r->tree, r->B, r->L, r->accept_len, r->out_rows, r->L_out,
                            r->compact_status, st);

@@ -68,3 +68,30 @@ def test_accept_hidden_matches_oracle(m, B, d, V, mode):
         assert (r["out_rows"][b, G:].cpu().numpy() == -1).all()
         accepted += o.accept_len
     assert accepted > 0                       # the planted candidates are accepted somewhere
+
+
+@pytest.mark.parametrize("B,d,V,mode", [(64, 128, 100, "greedy"), (64, 128, 256, "typical"),
+                                        (65, 128, 1000, "typical"), (65, 192, 777, "greedy")])
+def test_accept_hidden_pass_and_vocabulary_edges(m, B, d, V, mode):
+    """Regular (3, 2) tree: 4 internal rows per sequence, so B = 64 fills exactly one
+    256-column pass and B = 65 needs a second pass of 4 columns; V = 100 is a single
+    partial group of W_LM (most CTAs have no group), V = 256 two whole groups."""
+    t_o = otree.compile_template(otree.regular_paths((3, 2)), 3)
+    t_g = m.Template(t_o.paths[1:], 3, device="cuda")
+    hidden, W, tokens, internal = planted_inputs(t_o, B, d, V, seed=77 + B + V)
+    assert len(internal) == 4
+    r = m.medusa_tree_accept_hidden(t_g, hidden.cuda(), W.cuda(), torch.as_tensor(tokens).cuda(), mode)
+    torch.cuda.synchronize()
+    W64 = gu.to64(W)
+    checked = 0
+    for b in range(B):
+        o = oacc.accept_hidden(gu.to64(hidden[b]), W64, tokens[b], t_o.retrieve, internal, mode)
+        if mode == "typical" and gu.typical_ambiguous(o):
+            continue
+        G = o.accept_len + 1
+        assert int(r["accept_len"][b]) == o.accept_len, b
+        assert int(r["best_path"][b]) == o.best_path, b
+        assert list(r["out_rows"][b, :G].cpu().numpy()) == list(o.out_rows), b
+        assert list(r["out_tokens"][b, :G].cpu().numpy()) == list(o.out_tokens), b
+        checked += 1
+    assert checked >= B - 2

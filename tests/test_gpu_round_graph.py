@@ -97,3 +97,30 @@ def test_round_create_reports_a_bad_call(m):
     # the context is still usable
     ref = eager(rd)
     assert int(ref["attn_status"][0]) == 0
+
+
+def test_round_graph_with_hidden_state_acceptance(m):
+    """Step 4 as medusa_tree_accept_hidden (the target's hidden states instead of
+    logits): the graph equals the five eager calls bit for bit, logits unused."""
+    w = synth.WORKLOADS["vicuna7b-64"]
+    rd = bench.Round(m, w, torch.device("cuda"))
+    hid = synth.normal((w.batch, rd.N, w.hidden), 1.0, w.seed, "h", rd.dev, w.torch_dtype, sub=3)
+    root, pool = rd.heads()
+    tokens, pos = rd.fill(root, pool)
+    out, _, st = rd.attn()
+    r = m.medusa_tree_accept_hidden(rd.tmpl, hid, rd.w_lm, tokens, "typical", epsilon=w.epsilon, delta=w.delta)
+    L_out, st2 = rd.compact(r)
+    torch.cuda.synchronize()
+    ref = {"root": root, "pool": pool, "tokens": tokens, "pos": pos, "out": out, "attn_status": st,
+           "L_out": L_out, "compact_status": st2}
+    ref.update(r)
+    ref = {k: v.clone() for k, v in ref.items()}
+    rnd = m.MedusaRound(rd.tmpl, rd.h, rd.w1, rd.w2, rd.w_lm, w.topk, rd.L, rd.q, rd.k, rd.v, rd.cache, rd.max_L,
+                        None, mode="typical", rope_base=w.rope_base, epsilon=w.epsilon, delta=w.delta,
+                        hidden_target=hid)
+    for rep in range(2):
+        rnd.launch()
+        torch.cuda.synchronize()
+        same(rnd, ref, f"hidden-state round, launch {rep}")
+    assert int(rnd.accept_len[0]) >= 0
+    rnd.close()
