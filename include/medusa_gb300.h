@@ -15,7 +15,9 @@
  *
  * Conventions shared by every call
  *   - Pointers are device memory unless the comment says [host].  All device
- *     buffers are owned by the caller; no call allocates or frees memory.
+ *     buffers are owned by the caller; no call allocates or frees memory, except
+ *     that medusa_round_create allocates its CUDA graph objects (no device buffers)
+ *     and medusa_round_destroy frees them.
  *   - Arrays are row-major with the last dimension contiguous.  Float tensors
  *     read with 128-bit loads must be 16-byte aligned (the base pointer and
  *     every row); medusa_tree_attn_verify's bf16 path also needs the KV cache

@@ -50,7 +50,6 @@ struct LmArgs {
   int col0;               // first column of this pass (column = b * NI + internal index)
   int n_cols;             // valid columns of this pass
   int n_mma;              // MMA N: n_cols rounded up to 32 (32-column TMEM loads stay aligned)
-  int typical;
   float inv_temp;
   const int32_t* e_tok;   // [cols_pad][kLKids] child tokens
   const int32_t* e_row;   // [cols_pad][kLKids] child rows
@@ -107,8 +106,7 @@ __global__ void lm_gather_kernel(medusa_tree_t t, int B, int d, const uint16_t* 
   }
 }
 
-// Fold one value (raw x, id) into running statistics: argmax of x (lowest id on
-// ties); with TYP also max, partition function and first moment of y = x / T.
+// Argmax of the raw logits, the lowest id among equal values.
 __device__ __forceinline__ void lm_fold_argmax(float x, int id, float& av, int& ai) {
   if (ranks_before(x, id, av, ai)) {
     av = x;
@@ -116,6 +114,7 @@ __device__ __forceinline__ void lm_fold_argmax(float x, int id, float& av, int& 
   }
 }
 
+// Merge chunk statistics q into (m, z, s1) and the argmax (log-sum-exp with first moment).
 __device__ __forceinline__ void lm_merge(float& m, float& z, float& s1, float& av, int& ai, const RowPart& q) {
   if (ranks_before(q.amax_v, q.amax_i, av, ai)) {
     av = q.amax_v;
@@ -481,7 +480,6 @@ cudaError_t launch_lm_accept(const LmAcceptPlan& p, const medusa_tree_t& t, cons
       a.col0 = c0;
       a.n_cols = n_cols;
       a.n_mma = NM;
-      a.typical = typ ? 1 : 0;
       a.inv_temp = 1.f / temperature;
       a.e_tok = e_tok;
       a.e_row = e_row;
