@@ -296,6 +296,20 @@ medusa_status medusa_tree_accept(const medusa_tree_t *t, int32_t B, int32_t V, c
                                  int32_t *out_tokens, int32_t *out_rows, int32_t *frontier_row,
                                  void *ws, size_t ws_bytes, void *stream);
 
+/* medusa_tree_accept followed by medusa_kv_compact of the winning rows, in the same
+ * kernel that picks the winner ([CN] "把 Python 控制流赶出热路径" ranks a fused index
+ * and K/V commit among the changes worth most): the acceptance outputs are those of
+ * medusa_tree_accept, and cache, L_out and status end as medusa_kv_compact leaves them
+ * (same validation; a rejected sequence is untouched).  One launch fewer per round.
+ * ws: medusa_tree_accept_workspace(...) bytes.  L_out must not alias L. */
+medusa_status medusa_tree_accept_commit(const medusa_tree_t *t, int32_t B, int32_t V, const void *logits,
+                                        medusa_dtype dt, const int32_t *tokens, int32_t mode, float temperature,
+                                        float epsilon, float delta, int32_t entropy_guard,
+                                        const medusa_kv_t *cache, const int32_t *L, int32_t *best_path,
+                                        int32_t *accept_len, int32_t *out_tokens, int32_t *out_rows,
+                                        int32_t *frontier_row, int32_t *L_out, int32_t *status, void *ws,
+                                        size_t ws_bytes, void *stream);
+
 size_t medusa_tree_accept_hidden_workspace(const medusa_tree_t *t, int32_t B, int32_t V, int32_t d);
 
 /* medusa_tree_accept with the target's vocabulary projection folded in ([M7.2] §0x07B:
@@ -334,7 +348,7 @@ medusa_status medusa_tree_accept_hidden(const medusa_tree_t *t, int32_t B, int32
  * L + N <= capacity); an invalid sequence gets status[b] = MEDUSA_EPATH or
  * MEDUSA_ECAPACITY, L_out[b] = L[b] and no cache write.
  *   t: device template (its parent array validates the chain); L, accept_len [B];
- *   out_rows [B][D+1]; L_out [B]; status [B]. */
+ *   out_rows [B][D+1]; L_out [B] (must not alias L); status [B]. */
 medusa_status medusa_kv_compact(const medusa_kv_t *cache, const medusa_tree_t *t, int32_t B,
                                 const int32_t *L, const int32_t *accept_len,
                                 const int32_t *out_rows, int32_t *L_out, int32_t *status,
@@ -402,6 +416,9 @@ typedef struct {
    * target's final hidden states [B][N][d] (bf16, the heads' d) with the same w_lm,
    * and `logits` is not read (it may be NULL) */
   const void *hidden_target;
+  /* non-zero: steps 4 and 5 as one (medusa_tree_accept_commit: the winning rows are
+   * committed by the acceptance kernel; L_out and compact_status as in step 5) */
+  int32_t fuse_commit;
 } medusa_round_desc;
 
 typedef struct medusa_round_s *medusa_round_t;

@@ -23,7 +23,7 @@ EXPORTED = [
     "medusa_tree_upload", "medusa_heads_topk_workspace", "medusa_heads_topk", "medusa_tree_fill",
     "medusa_tree_attn_workspace", "medusa_tree_attn_verify", "medusa_tree_attn_verify_static",
     "medusa_tree_accept_workspace",
-    "medusa_tree_accept", "medusa_tree_accept_hidden_workspace", "medusa_tree_accept_hidden", "medusa_kv_compact", "medusa_kv_compact_layers", "medusa_round_workspace", "medusa_round_create",
+    "medusa_tree_accept", "medusa_tree_accept_commit", "medusa_tree_accept_hidden_workspace", "medusa_tree_accept_hidden", "medusa_kv_compact", "medusa_kv_compact_layers", "medusa_round_workspace", "medusa_round_create",
     "medusa_round_launch", "medusa_round_destroy", "medusa_status_string", "medusa_abi_version",
 ]
 
@@ -62,6 +62,7 @@ class MedusaRoundDesc(C.Structure):
         ("best_path", C.c_void_p), ("accept_len", C.c_void_p), ("out_tokens", C.c_void_p),
         ("out_rows", C.c_void_p), ("frontier_row", C.c_void_p),
         ("L_out", C.c_void_p), ("compact_status", C.c_void_p), ("hidden_target", C.c_void_p),
+        ("fuse_commit", C.c_int32),
     ]
 
 
@@ -102,6 +103,8 @@ def lib() -> C.CDLL:
         "medusa_tree_accept_workspace": (SZ, [P(MedusaTree), I32, I32]),
         "medusa_tree_accept": (I32, [P(MedusaTree), I32, I32, VP, I32, VP, I32, F, F, F, I32, VP, VP,
                                      VP, VP, VP, VP, SZ, VP]),
+        "medusa_tree_accept_commit": (I32, [P(MedusaTree), I32, I32, VP, I32, VP, I32, F, F, F, I32, P(MedusaKV), VP,
+                                            VP, VP, VP, VP, VP, VP, VP, VP, SZ, VP]),
         "medusa_tree_accept_hidden_workspace": (SZ, [P(MedusaTree), I32, I32, I32]),
         "medusa_tree_accept_hidden": (I32, [P(MedusaTree), I32, I32, I32, VP, VP, VP, I32, F, F, F, VP, VP, VP, VP,
                                             VP, VP, SZ, VP]),

@@ -275,6 +275,33 @@ def medusa_tree_accept(tmpl: Template, logits, tokens, mode: str = "greedy", tem
     return r
 
 
+def medusa_tree_accept_commit(tmpl: Template, logits, tokens, cache: KVCache, L, mode: str = "greedy",
+                              temperature: float = 1.0, epsilon: float = 0.09, delta: float = 0.3,
+                              entropy_guard: bool = False):
+    """medusa_tree_accept and medusa_kv_compact of the winner in one: the acceptance dict
+    plus L_out and status (int32 device tensors); the cache is compacted in place."""
+    _need_cuda(logits, tokens, L)
+    B, N, V = logits.shape
+    dev = logits.device
+    W = tmpl.max_depth + 1
+    r = {k: torch.empty(B, dtype=torch.int32, device=dev)
+         for k in ("best_path", "accept_len", "frontier_row", "L_out", "status")}
+    r["out_tokens"] = torch.empty((B, W), dtype=torch.int32, device=dev)
+    r["out_rows"] = torch.empty((B, W), dtype=torch.int32, device=dev)
+    nb = lib().medusa_tree_accept_workspace(C.byref(tmpl.dev), B, V)
+    ws = _WS.get("accept", nb, dev)
+    m = nat.GREEDY if mode == "greedy" else nat.TYPICAL
+    d = cache.desc()
+    check("medusa_tree_accept_commit",
+          lib().medusa_tree_accept_commit(C.byref(tmpl.dev), B, V, _ptr(logits), _dtype_code(logits.dtype),
+                                          _ptr(tokens), m, float(temperature), float(epsilon), float(delta),
+                                          int(entropy_guard), C.byref(d), _ptr(L), _ptr(r["best_path"]),
+                                          _ptr(r["accept_len"]), _ptr(r["out_tokens"]), _ptr(r["out_rows"]),
+                                          _ptr(r["frontier_row"]), _ptr(r["L_out"]), _ptr(r["status"]), _ptr(ws),
+                                          ws.numel(), _stream(dev)))
+    return r
+
+
 def medusa_tree_accept_hidden(tmpl: Template, hidden, w_lm, tokens, mode: str = "greedy",
                               temperature: float = 1.0, epsilon: float = 0.09, delta: float = 0.3):
     """medusa_tree_accept on the target's final hidden states: the vocabulary projection
@@ -341,7 +368,9 @@ class MedusaRound:
     compact_status.  The heads run on one frontier row per sequence (h is [B, d]).
     With hidden_target ([B, N, d] bf16, the target's final hidden states of the tree
     rows) acceptance projects the internal rows through w_lm itself
-    (medusa_tree_accept_hidden) and logits may be None."""
+    (medusa_tree_accept_hidden) and logits may be None.  With fuse_commit the winning
+    rows are committed by the acceptance kernel itself (medusa_tree_accept_commit):
+    one launch fewer, the same results."""
 
     _OUT = ("root", "pool", "tokens", "pos", "out", "lse", "attn_status", "best_path", "accept_len",
             "out_tokens", "out_rows", "frontier_row", "L_out", "compact_status")
@@ -350,7 +379,7 @@ class MedusaRound:
                  max_prefix: int, logits, mode: str = "greedy", rope_base: float = 10000.0,
                  scale: Optional[float] = None, temperature: float = 1.0, epsilon: float = 0.09,
                  delta: float = 0.3, entropy_guard: bool = False, b1=None, shared_w2: bool = False,
-                 want_lse: bool = False, hidden_target=None):
+                 want_lse: bool = False, hidden_target=None, fuse_commit: bool = False):
         _need_cuda(h, w1, w2, w_lm, b1, L, q, k_new, v_new, logits, hidden_target)
         B, d = h.shape
         V, K, N = w_lm.shape[0], w1.shape[0], tmpl.n_rows
@@ -398,6 +427,7 @@ class MedusaRound:
         r.attn_status = self.attn_status.data_ptr()
         r.logits = logits.data_ptr() if logits is not None else None
         r.hidden_target = hidden_target.data_ptr() if hidden_target is not None else None
+        r.fuse_commit = 1 if fuse_commit else 0
         r.mode = nat.GREEDY if mode == "greedy" else nat.TYPICAL
         r.temperature, r.epsilon, r.delta = float(temperature), float(epsilon), float(delta)
         r.entropy_guard = int(entropy_guard)

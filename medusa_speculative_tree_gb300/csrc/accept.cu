@@ -23,6 +23,8 @@ constexpr int kWarps = kThreads / 32;
 constexpr int kLoads = 4;          // 16-byte loads in flight per thread in row_stats
 constexpr int kSelThreads = 1024;  // select: one warp per internal row, 32 rows at a time
 constexpr int kSelWarps = kSelThreads / 32;
+constexpr int kCommitPieces = 2;   // 16-byte pieces a select thread holds while moving rows
+
 
 // Merge two partial statistics (log-sum-exp with first moment).
 __device__ __forceinline__ void merge_stats(float& m, float& z, float& s1, float m2, float z2, float s12) {
@@ -208,7 +210,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     medusa_tree_t t, int V, int n_chunks, const EL* __restrict__ logits,
     const int32_t* __restrict__ tokens, int mode, float inv_temp, float epsilon, float delta,
     const RowPart* __restrict__ part, const float* __restrict__ guard, SelectSmem lay,
-    const float* __restrict__ edge_x, const int* __restrict__ err,
+    const float* __restrict__ edge_x, const int* __restrict__ err, CommitArgs cm,
     int32_t* __restrict__ best_path, int32_t* __restrict__ accept_len,
     int32_t* __restrict__ out_tokens, int32_t* __restrict__ out_rows,
     int32_t* __restrict__ frontier_row) {
@@ -232,6 +234,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
       best_path[b] = -1;
       accept_len[b] = -1;
       frontier_row[b] = -1;
+      if (cm.on) {                               // nothing to commit: the cache is untouched
+        cm.status[b] = MEDUSA_EPATH;
+        cm.L_out[b] = cm.L[b];
+      }
     }
     for (int j = threadIdx.x; j < W; j += kSelThreads) {
       out_rows[(int64_t)b * W + j] = -1;
@@ -404,6 +410,77 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     }
     frontier_row[b] = r[best_a];
   }
+  if (!cm.on) return;
+
+  // ---- fused commit: medusa_kv_compact of this sequence --------------------------------
+  // Thread 0 validates as the compaction kernel does (capacity, then the chain of
+  // published rows); then every KV head's G rows of K and V move as 16-byte pieces,
+  // a group of heads at a time: all pieces of the group are read into registers before
+  // any is written, so overlapping source and destination rows are safe (rows of
+  // different heads never overlap).
+  __shared__ int c_rows[MEDUSA_MAX_DEPTH + 1];
+  __shared__ int c_verdict, c_G, c_L;
+  if (threadIdx.x == 0) {
+    const int a = best_a;
+    const int32_t* r = lay.ret_staged ? s_ret + best_p * W : t.retrieve + (int64_t)best_p * W;
+    const int Lb = cm.L[b];
+    int v = MEDUSA_OK;
+    if (Lb < 0 || !seq_rows_ok(cm.c, b, (int64_t)Lb + N)) {
+      v = MEDUSA_ECAPACITY;
+    } else if (a < 0 || a > t.max_depth) {
+      v = MEDUSA_EPATH;
+    } else {
+      for (int j = 0; j <= a; ++j) {
+        const int u = r[j];
+        c_rows[j] = u;
+        if (u < 0 || u >= N || (j == 0 ? u != 0 : t.parent[u] != r[j - 1])) v = MEDUSA_EPATH;
+      }
+    }
+    c_verdict = v;
+    c_G = a + 1;
+    c_L = Lb;
+    cm.status[b] = v;
+    cm.L_out[b] = v == MEDUSA_OK ? Lb + a + 1 : Lb;
+  }
+  __syncthreads();
+  if (c_verdict != MEDUSA_OK) return;
+  const int G = c_G, Lb = c_L;
+  const int esz = cm.c.dtype == MEDUSA_BF16 ? 2 : 4;
+  const int pr = cm.c.head_dim * esz / 16;                  // pieces per row
+  const int per_head = 2 * G * pr;                          // K and V rows of one head
+  int hg = (kSelThreads * kCommitPieces) / per_head;         // heads per group
+  if (hg < 1) hg = 1;
+  char* kb = static_cast<char*>(cm.c.k);
+  char* vb = static_cast<char*>(cm.c.v);
+  for (int h0 = 0; h0 < cm.c.n_kv_heads; h0 += hg) {
+    const int nh = min(hg, cm.c.n_kv_heads - h0);
+    const int n = nh * per_head;
+    uint4 piece[kCommitPieces];
+#pragma unroll
+    for (int k = 0; k < kCommitPieces; ++k) {
+      const int i = threadIdx.x + k * kSelThreads;
+      if (i < n) {
+        const int h = h0 + i / per_head, rem = i % per_head;
+        const int kv = rem / (G * pr), j = (rem / pr) % G, e = rem % pr;
+        const char* base = kv ? vb : kb;
+        const int64_t off = cache_row_offset(cm.c, b, h, Lb + c_rows[j]) * esz + 16 * e;
+        piece[k] = *reinterpret_cast<const uint4*>(base + off);
+      }
+    }
+    __syncthreads();
+#pragma unroll
+    for (int k = 0; k < kCommitPieces; ++k) {
+      const int i = threadIdx.x + k * kSelThreads;
+      if (i < n) {
+        const int h = h0 + i / per_head, rem = i % per_head;
+        const int kv = rem / (G * pr), j = (rem / pr) % G, e = rem % pr;
+        char* base = kv ? vb : kb;
+        const int64_t off = cache_row_offset(cm.c, b, h, Lb + j) * esz + 16 * e;
+        *reinterpret_cast<uint4*>(base + off) = piece[k];
+      }
+    }
+    __syncthreads();
+  }
 }
 
 }  // namespace
@@ -427,7 +504,7 @@ cudaError_t launch_accept(const AcceptPlan& p, const medusa_tree_t& t, const voi
                           medusa_dtype dt, const int32_t* tokens, int mode, float temperature,
                           float epsilon, float delta, int entropy_guard, int32_t* best_path,
                           int32_t* accept_len, int32_t* out_tokens, int32_t* out_rows,
-                          int32_t* frontier_row, void* ws, cudaStream_t st) {
+                          int32_t* frontier_row, void* ws, cudaStream_t st, const CommitArgs& cm) {
   RowPart* part = (RowPart*)((char*)ws + p.off_part);
   float* guard = (float*)((char*)ws + p.off_guard);
   const float inv_t = 1.f / temperature;
@@ -455,14 +532,15 @@ cudaError_t launch_accept(const AcceptPlan& p, const medusa_tree_t& t, const voi
     if (e != cudaSuccess) return e;
     select_kernel<uint16_t><<<p.B, kSelThreads, lay.bytes, st>>>(t, p.V, p.n_chunks, (const uint16_t*)logits, tokens,
                                                               mode, inv_t, epsilon, delta, part, gptr, lay, nullptr,
-                                                              nullptr, best_path, accept_len, out_tokens, out_rows,
-                                                              frontier_row);
+                                                              nullptr, cm, best_path, accept_len, out_tokens,
+                                                              out_rows, frontier_row);
   } else {
     e = cudaFuncSetAttribute(select_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)lay.bytes);
     if (e != cudaSuccess) return e;
     select_kernel<float><<<p.B, kSelThreads, lay.bytes, st>>>(t, p.V, p.n_chunks, (const float*)logits, tokens, mode,
                                                            inv_t, epsilon, delta, part, gptr, lay, nullptr, nullptr,
-                                                           best_path, accept_len, out_tokens, out_rows, frontier_row);
+                                                           cm, best_path, accept_len, out_tokens, out_rows,
+                                                           frontier_row);
   }
   return cudaGetLastError();
 }
@@ -471,13 +549,13 @@ cudaError_t launch_select_parts(const medusa_tree_t& t, int B, int V, int n_chun
                                 const float* edge_x, const int* err, const int32_t* tokens, int mode,
                                 float temperature, float epsilon, float delta, int32_t* best_path,
                                 int32_t* accept_len, int32_t* out_tokens, int32_t* out_rows,
-                                int32_t* frontier_row, cudaStream_t st) {
+                                int32_t* frontier_row, cudaStream_t st, const CommitArgs& cm) {
   const SelectSmem lay = select_smem(t, n_chunks, false);
   cudaError_t e = cudaFuncSetAttribute(select_kernel<float>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        (int)lay.bytes);
   if (e != cudaSuccess) return e;
   select_kernel<float><<<B, kSelThreads, lay.bytes, st>>>(t, V, n_chunks, nullptr, tokens, mode, 1.f / temperature,
-                                                         epsilon, delta, part, nullptr, lay, edge_x, err,
+                                                         epsilon, delta, part, nullptr, lay, edge_x, err, cm,
                                                          best_path, accept_len, out_tokens, out_rows,
                                                          frontier_row);
   return cudaGetLastError();

@@ -104,6 +104,14 @@ __device__ __forceinline__ bool seq_rows_ok(const medusa_kv_t& c, int b, int64_t
   return page >= 0 && page < c.n_pages;
 }
 
+// Element offset of (sequence b, kv head, row) in a contiguous or paged cache.
+__device__ __forceinline__ int64_t cache_row_offset(const medusa_kv_t& c, int b, int kvh, int row) {
+  if (c.page_size == 0)
+    return (((int64_t)b * c.n_kv_heads + kvh) * c.capacity + row) * c.head_dim;
+  const int page = c.block_table[(int64_t)b * c.max_blocks + row / c.page_size];
+  return (((int64_t)page * c.n_kv_heads + kvh) * c.page_size + row % c.page_size) * c.head_dim;
+}
+
 // ---- mbarrier helpers (shared by the TMA-fed kernels) ----------------------------
 
 __device__ __forceinline__ uint32_t smem_u32(const void* p) {

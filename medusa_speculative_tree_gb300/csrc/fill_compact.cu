@@ -27,13 +27,6 @@ __global__ void tree_fill_kernel(medusa_tree_t t, int K, const int32_t* __restri
   pos[(int64_t)b * t.n_rows + u] = L[b] + t.depth[u];
 }
 
-__device__ __forceinline__ int64_t cache_row_offset(const medusa_kv_t& c, int b, int kvh, int row) {
-  if (c.page_size == 0)
-    return (((int64_t)b * c.n_kv_heads + kvh) * c.capacity + row) * c.head_dim;
-  const int page = c.block_table[(int64_t)b * c.max_blocks + row / c.page_size];
-  return (((int64_t)page * c.n_kv_heads + kvh) * c.page_size + row % c.page_size) * c.head_dim;
-}
-
 // K and V base pointers of the layers that one launch commits ([M7.2] §0x06B: the
 // accepted rows are committed in every layer's cache); blockIdx.z picks the layer.
 // The other fields of the cache descriptor are common to all of them.

@@ -82,6 +82,17 @@ struct RowPart {
   int pad[3];
 };
 
+// Fused index + K/V commit ([CN] "把 Python 控制流赶出热路径"): when `on`, the select
+// kernel also performs medusa_kv_compact for its sequence, with the same validation
+// and status.  Default: off.
+struct CommitArgs {
+  medusa_kv_t c;
+  int on;
+  const int32_t* L;
+  int32_t* L_out;
+  int32_t* status;
+};
+
 struct AcceptPlan {
   int B, V, chunk, n_chunks;
   size_t off_part, off_guard, bytes;
@@ -91,7 +102,7 @@ cudaError_t launch_accept(const AcceptPlan& p, const medusa_tree_t& t, const voi
                           medusa_dtype dt, const int32_t* tokens, int mode, float temperature,
                           float epsilon, float delta, int entropy_guard, int32_t* best_path,
                           int32_t* accept_len, int32_t* out_tokens, int32_t* out_rows,
-                          int32_t* frontier_row, void* ws, cudaStream_t st);
+                          int32_t* frontier_row, void* ws, cudaStream_t st, const CommitArgs& cm = CommitArgs{});
 
 // The select step alone, on chunk statistics and per-edge logits written by another
 // kernel (edge_x [B][N]: the logit of row v's token at its parent); err (nullable)
@@ -100,7 +111,7 @@ cudaError_t launch_select_parts(const medusa_tree_t& t, int B, int V, int n_chun
                                 const float* edge_x, const int* err, const int32_t* tokens, int mode,
                                 float temperature, float epsilon, float delta, int32_t* best_path,
                                 int32_t* accept_len, int32_t* out_tokens, int32_t* out_rows,
-                                int32_t* frontier_row, cudaStream_t st);
+                                int32_t* frontier_row, cudaStream_t st, const CommitArgs& cm = CommitArgs{});
 
 // Acceptance with the target's vocabulary projection folded in (lm_accept.cu).
 struct LmAcceptPlan {
@@ -112,7 +123,7 @@ bool lm_accept_supported(int d, int V);
 cudaError_t launch_lm_accept(const LmAcceptPlan& p, const medusa_tree_t& t, const void* hidden, const void* w_lm,
                              const int32_t* tokens, int mode, float temperature, float epsilon, float delta,
                              int32_t* best_path, int32_t* accept_len, int32_t* out_tokens, int32_t* out_rows,
-                             int32_t* frontier_row, void* ws, cudaStream_t st);
+                             int32_t* frontier_row, void* ws, cudaStream_t st, const CommitArgs& cm = CommitArgs{});
 
 // ---- compaction -----------------------------------------------------------------------
 cudaError_t launch_kv_compact(const medusa_kv_t& c, const medusa_tree_t& t, int B,

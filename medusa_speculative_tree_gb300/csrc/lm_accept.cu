@@ -448,7 +448,7 @@ LmAcceptPlan plan_lm_accept(const medusa_tree_t& t, int B, int V, int d) {
 cudaError_t launch_lm_accept(const LmAcceptPlan& p, const medusa_tree_t& t, const void* hidden, const void* w_lm,
                              const int32_t* tokens, int mode, float temperature, float epsilon, float delta,
                              int32_t* best_path, int32_t* accept_len, int32_t* out_tokens, int32_t* out_rows,
-                             int32_t* frontier_row, void* ws, cudaStream_t st) {
+                             int32_t* frontier_row, void* ws, cudaStream_t st, const CommitArgs& cm) {
   char* base = static_cast<char*>(ws);
   uint16_t* X = reinterpret_cast<uint16_t*>(base + p.off_x);
   int32_t* e_tok = reinterpret_cast<int32_t*>(base + p.off_etok);
@@ -499,7 +499,7 @@ cudaError_t launch_lm_accept(const LmAcceptPlan& p, const medusa_tree_t& t, cons
     }
   }
   return launch_select_parts(t, p.B, p.V, p.n_chunks, part, edge_x, err, tokens, mode, temperature, epsilon, delta,
-                             best_path, accept_len, out_tokens, out_rows, frontier_row, st);
+                             best_path, accept_len, out_tokens, out_rows, frontier_row, st, cm);
 }
 
 }  // namespace medusa

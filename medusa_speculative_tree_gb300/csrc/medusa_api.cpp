@@ -89,11 +89,17 @@ bool kv_ok(const medusa_kv_t* c) {
   return true;
 }
 
+medusa_status accept_logits_impl(const medusa_tree_t* t, int32_t B, int32_t V, const void* logits, medusa_dtype dt,
+                                 const int32_t* tokens, int32_t mode, float temperature, float epsilon,
+                                 float delta, int32_t entropy_guard, int32_t* best_path, int32_t* accept_len,
+                                 int32_t* out_tokens, int32_t* out_rows, int32_t* frontier_row, void* ws,
+                                 size_t ws_bytes, void* stream, const medusa::CommitArgs& cm);
+
 }  // namespace
 
 extern "C" {
 
-int32_t medusa_abi_version(void) { return 2; }
+int32_t medusa_abi_version(void) { return 3; }
 
 const char* medusa_status_string(medusa_status s) {
   switch (s) {
@@ -392,16 +398,9 @@ medusa_status medusa_tree_accept(const medusa_tree_t* t, int32_t B, int32_t V, c
                                  int32_t entropy_guard, int32_t* best_path, int32_t* accept_len,
                                  int32_t* out_tokens, int32_t* out_rows, int32_t* frontier_row,
                                  void* ws, size_t ws_bytes, void* stream) {
-  if (!tree_ok(t) || B < 1 || V < 1 || !logits || !dtype_ok(dt) || !tokens || !best_path ||
-      !accept_len || !out_tokens || !out_rows || !frontier_row || !ws ||
-      (mode != MEDUSA_ACCEPT_GREEDY && mode != MEDUSA_ACCEPT_TYPICAL) || !(temperature > 0.0f) ||
-      !std::isfinite(temperature) || !(epsilon >= 0.0f) || !(delta >= 0.0f))
-    return MEDUSA_EINVAL;
-  const medusa::AcceptPlan p = medusa::plan_accept(*t, B, V);
-  if (ws_bytes < p.bytes) return MEDUSA_EWORKSPACE;
-  return cuda_status(medusa::launch_accept(p, *t, logits, dt, tokens, mode, temperature, epsilon,
-                                           delta, entropy_guard, best_path, accept_len, out_tokens,
-                                           out_rows, frontier_row, ws, as_stream(stream)));
+  return accept_logits_impl(t, B, V, logits, dt, tokens, mode, temperature, epsilon, delta, entropy_guard,
+                            best_path, accept_len, out_tokens, out_rows, frontier_row, ws, ws_bytes, stream,
+                            medusa::CommitArgs{});
 }
 
 size_t medusa_tree_accept_hidden_workspace(const medusa_tree_t* t, int32_t B, int32_t V, int32_t d) {
@@ -409,11 +408,19 @@ size_t medusa_tree_accept_hidden_workspace(const medusa_tree_t* t, int32_t B, in
   return medusa::plan_lm_accept(*t, B, V, d).bytes;
 }
 
-medusa_status medusa_tree_accept_hidden(const medusa_tree_t* t, int32_t B, int32_t V, int32_t d,
-                                        const void* hidden, const void* w_lm, const int32_t* tokens, int32_t mode,
-                                        float temperature, float epsilon, float delta, int32_t* best_path,
-                                        int32_t* accept_len, int32_t* out_tokens, int32_t* out_rows,
-                                        int32_t* frontier_row, void* ws, size_t ws_bytes, void* stream) {
+}  // extern "C"
+
+namespace {
+
+bool commit_ok(const medusa_kv_t* cache, const int32_t* L, const int32_t* L_out, const int32_t* status) {
+  return kv_ok(cache) && L && L_out && status && L_out != L;
+}
+
+medusa_status accept_hidden_impl(const medusa_tree_t* t, int32_t B, int32_t V, int32_t d, const void* hidden,
+                                 const void* w_lm, const int32_t* tokens, int32_t mode, float temperature,
+                                 float epsilon, float delta, int32_t* best_path, int32_t* accept_len,
+                                 int32_t* out_tokens, int32_t* out_rows, int32_t* frontier_row, void* ws,
+                                 size_t ws_bytes, void* stream, const medusa::CommitArgs& cm) {
   if (!tree_ok(t) || B < 1 || V < 1 || d < 1 || !hidden || !w_lm || !tokens || !best_path || !accept_len ||
       !out_tokens || !out_rows || !frontier_row || !ws ||
       (mode != MEDUSA_ACCEPT_GREEDY && mode != MEDUSA_ACCEPT_TYPICAL) || !(temperature > 0.0f) ||
@@ -425,14 +432,68 @@ medusa_status medusa_tree_accept_hidden(const medusa_tree_t* t, int32_t B, int32
   if (ws_bytes < p.bytes) return MEDUSA_EWORKSPACE;
   return cuda_status(medusa::launch_lm_accept(p, *t, hidden, w_lm, tokens, mode, temperature, epsilon, delta,
                                               best_path, accept_len, out_tokens, out_rows, frontier_row, ws,
-                                              as_stream(stream)));
+                                              as_stream(stream), cm));
+}
+
+medusa_status accept_logits_impl(const medusa_tree_t* t, int32_t B, int32_t V, const void* logits, medusa_dtype dt,
+                                 const int32_t* tokens, int32_t mode, float temperature, float epsilon,
+                                 float delta, int32_t entropy_guard, int32_t* best_path, int32_t* accept_len,
+                                 int32_t* out_tokens, int32_t* out_rows, int32_t* frontier_row, void* ws,
+                                 size_t ws_bytes, void* stream, const medusa::CommitArgs& cm) {
+  if (!tree_ok(t) || B < 1 || V < 1 || !logits || !dtype_ok(dt) || !tokens || !best_path ||
+      !accept_len || !out_tokens || !out_rows || !frontier_row || !ws ||
+      (mode != MEDUSA_ACCEPT_GREEDY && mode != MEDUSA_ACCEPT_TYPICAL) || !(temperature > 0.0f) ||
+      !std::isfinite(temperature) || !(epsilon >= 0.0f) || !(delta >= 0.0f))
+    return MEDUSA_EINVAL;
+  const medusa::AcceptPlan p = medusa::plan_accept(*t, B, V);
+  if (ws_bytes < p.bytes) return MEDUSA_EWORKSPACE;
+  return cuda_status(medusa::launch_accept(p, *t, logits, dt, tokens, mode, temperature, epsilon,
+                                           delta, entropy_guard, best_path, accept_len, out_tokens,
+                                           out_rows, frontier_row, ws, as_stream(stream), cm));
+}
+
+medusa::CommitArgs commit_args(const medusa_kv_t* cache, const int32_t* L, int32_t* L_out, int32_t* status) {
+  medusa::CommitArgs cm{};
+  cm.c = *cache;
+  cm.on = 1;
+  cm.L = L;
+  cm.L_out = L_out;
+  cm.status = status;
+  return cm;
+}
+
+}  // namespace
+
+extern "C" {
+
+medusa_status medusa_tree_accept_hidden(const medusa_tree_t* t, int32_t B, int32_t V, int32_t d,
+                                        const void* hidden, const void* w_lm, const int32_t* tokens, int32_t mode,
+                                        float temperature, float epsilon, float delta, int32_t* best_path,
+                                        int32_t* accept_len, int32_t* out_tokens, int32_t* out_rows,
+                                        int32_t* frontier_row, void* ws, size_t ws_bytes, void* stream) {
+  return accept_hidden_impl(t, B, V, d, hidden, w_lm, tokens, mode, temperature, epsilon, delta, best_path,
+                            accept_len, out_tokens, out_rows, frontier_row, ws, ws_bytes, stream,
+                            medusa::CommitArgs{});
+}
+
+medusa_status medusa_tree_accept_commit(const medusa_tree_t* t, int32_t B, int32_t V, const void* logits,
+                                        medusa_dtype dt, const int32_t* tokens, int32_t mode, float temperature,
+                                        float epsilon, float delta, int32_t entropy_guard,
+                                        const medusa_kv_t* cache, const int32_t* L, int32_t* best_path,
+                                        int32_t* accept_len, int32_t* out_tokens, int32_t* out_rows,
+                                        int32_t* frontier_row, int32_t* L_out, int32_t* status, void* ws,
+                                        size_t ws_bytes, void* stream) {
+  if (!commit_ok(cache, L, L_out, status)) return MEDUSA_EINVAL;
+  return accept_logits_impl(t, B, V, logits, dt, tokens, mode, temperature, epsilon, delta, entropy_guard,
+                            best_path, accept_len, out_tokens, out_rows, frontier_row, ws, ws_bytes, stream,
+                            commit_args(cache, L, L_out, status));
 }
 
 medusa_status medusa_kv_compact(const medusa_kv_t* cache, const medusa_tree_t* t, int32_t B,
                                 const int32_t* L, const int32_t* accept_len,
                                 const int32_t* out_rows, int32_t* L_out, int32_t* status,
                                 void* stream) {
-  if (!kv_ok(cache) || !tree_ok(t) || B < 1 || !L || !accept_len || !out_rows || !L_out || !status)
+  if (!kv_ok(cache) || !tree_ok(t) || B < 1 || !L || !accept_len || !out_rows || !L_out || !status || L_out == L)
     return MEDUSA_EINVAL;
   return cuda_status(medusa::launch_kv_compact(*cache, *t, B, L, accept_len, out_rows, L_out, status,
                                                as_stream(stream)));
@@ -497,15 +558,21 @@ medusa_status record_round(const medusa_round_desc* r, char* ws, const RoundWs& 
                               r->max_prefix, r->rope_base, r->scale, r->out, r->lse, r->attn_status,
                               ws + w.attn, w.accept - w.attn, st);
   if (s != MEDUSA_OK) return s;
+  // steps 4 and 5: acceptance, then compaction, or both in one (the fused commit)
+  medusa::CommitArgs cm{};
+  if (r->fuse_commit) {
+    if (!commit_ok(&r->cache, r->L, r->L_out, r->compact_status)) return MEDUSA_EINVAL;
+    cm = commit_args(&r->cache, r->L, r->L_out, r->compact_status);
+  }
   if (r->hidden_target)
-    s = medusa_tree_accept_hidden(&r->tree, r->B, r->V, r->d, r->hidden_target, r->w_lm, r->tokens, r->mode,
-                                  r->temperature, r->epsilon, r->delta, r->best_path, r->accept_len,
-                                  r->out_tokens, r->out_rows, r->frontier_row, ws + w.accept, w.total - w.accept, st);
+    s = accept_hidden_impl(&r->tree, r->B, r->V, r->d, r->hidden_target, r->w_lm, r->tokens, r->mode,
+                           r->temperature, r->epsilon, r->delta, r->best_path, r->accept_len, r->out_tokens,
+                           r->out_rows, r->frontier_row, ws + w.accept, w.total - w.accept, st, cm);
   else
-    s = medusa_tree_accept(&r->tree, r->B, r->V, r->logits, r->dtype, r->tokens, r->mode, r->temperature,
+    s = accept_logits_impl(&r->tree, r->B, r->V, r->logits, r->dtype, r->tokens, r->mode, r->temperature,
                            r->epsilon, r->delta, r->entropy_guard, r->best_path, r->accept_len, r->out_tokens,
-                           r->out_rows, r->frontier_row, ws + w.accept, w.total - w.accept, st);
-  if (s != MEDUSA_OK) return s;
+                           r->out_rows, r->frontier_row, ws + w.accept, w.total - w.accept, st, cm);
+  if (s != MEDUSA_OK || r->fuse_commit) return s;
   return medusa_kv_compact(&r->cache, &r->tree, r->B, r->L, r->accept_len, r->out_rows, r->L_out,
                            r->compact_status, st);
 }

@@ -124,3 +124,54 @@ def test_round_graph_with_hidden_state_acceptance(m):
         same(rnd, ref, f"hidden-state round, launch {rep}")
     assert int(rnd.accept_len[0]) >= 0
     rnd.close()
+
+
+@pytest.mark.parametrize("name", ["tiny-fp32", "vicuna7b-64", "serving-b16-paged"])
+def test_fused_commit_equals_accept_then_compact(m, name):
+    """medusa_tree_accept_commit against medusa_tree_accept + medusa_kv_compact: the
+    acceptance outputs, L_out, status and every cache row the same; a sequence whose
+    L + N exceeds the capacity gets MEDUSA_ECAPACITY and is left untouched; and the
+    round graph with the fused commit equals the five eager calls."""
+    w = synth.WORKLOADS[name]
+    rd = bench.Round(m, w, torch.device("cuda"))
+    ref = eager(rd)                          # stages the tree rows, separate compaction
+    upto = rd.max_L + rd.tmpl.n_rows
+    k0, v0 = cache_rows(rd, upto)
+    rnd = m.MedusaRound(rd.tmpl, rd.h, rd.w1, rd.w2, rd.w_lm, w.topk, rd.L, rd.q, rd.k, rd.v, rd.cache, rd.max_L,
+                        rd.logits, mode=rd.mode, rope_base=w.rope_base, epsilon=w.epsilon, delta=w.delta,
+                        fuse_commit=True)
+    rnd.launch()
+    torch.cuda.synchronize()
+    same(rnd, ref, f"{name} fused-commit round")
+    k1, v1 = cache_rows(rd, upto)
+    assert torch.equal(k1, k0) and torch.equal(v1, v0)
+    rnd.close()
+
+    # the standalone call, after restaging the tree rows (attention) each time
+    tokens = ref["tokens"]
+    rd.attn()
+    r_sep = rd.accept(tokens)
+    L_sep, st_sep = rd.compact(r_sep)
+    torch.cuda.synchronize()
+    k_sep, v_sep = cache_rows(rd, upto)
+    rd.attn()
+    r_f = m.medusa_tree_accept_commit(rd.tmpl, rd.logits, tokens, rd.cache, rd.L, rd.mode, epsilon=w.epsilon,
+                                      delta=w.delta)
+    torch.cuda.synchronize()
+    for k in ("best_path", "accept_len", "out_tokens", "out_rows", "frontier_row"):
+        assert torch.equal(r_f[k], r_sep[k]), k
+    assert torch.equal(r_f["L_out"], L_sep) and torch.equal(r_f["status"], st_sep)
+    k_f, v_f = cache_rows(rd, upto)
+    assert torch.equal(k_f, k_sep) and torch.equal(v_f, v_sep)
+
+    # capacity failure: sequence 0 claims a prefix that leaves no room for the tree
+    if not w.page_size:
+        cap = rd.K.shape[2]
+        L_bad = rd.L.clone()
+        L_bad[0] = cap - rd.tmpl.n_rows + 1
+        before_k, before_v = rd.K.clone(), rd.V.clone()
+        r_b = m.medusa_tree_accept_commit(rd.tmpl, rd.logits, tokens, rd.cache, L_bad, rd.mode, epsilon=w.epsilon,
+                                          delta=w.delta)
+        torch.cuda.synchronize()
+        assert int(r_b["status"][0]) == -2 and int(r_b["L_out"][0]) == int(L_bad[0])
+        assert torch.equal(rd.K[0], before_k[0]) and torch.equal(rd.V[0], before_v[0])
