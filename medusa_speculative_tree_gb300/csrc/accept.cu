@@ -419,7 +419,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   // any is written, so overlapping source and destination rows are safe (rows of
   // different heads never overlap).
   __shared__ int c_rows[MEDUSA_MAX_DEPTH + 1];
-  __shared__ int c_verdict, c_G, c_L;
+  __shared__ int c_status, c_G, c_L;
   if (threadIdx.x == 0) {
     const int a = best_a;
     const int32_t* r = lay.ret_staged ? s_ret + best_p * W : t.retrieve + (int64_t)best_p * W;
@@ -436,14 +436,14 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
         if (u < 0 || u >= N || (j == 0 ? u != 0 : t.parent[u] != r[j - 1])) v = MEDUSA_EPATH;
       }
     }
-    c_verdict = v;
+    c_status = v;
     c_G = a + 1;
     c_L = Lb;
     cm.status[b] = v;
     cm.L_out[b] = v == MEDUSA_OK ? Lb + a + 1 : Lb;
   }
   __syncthreads();
-  if (c_verdict != MEDUSA_OK) return;
+  if (c_status != MEDUSA_OK) return;
   const int G = c_G, Lb = c_L;
   const int esz = cm.c.dtype == MEDUSA_BF16 ? 2 : 4;
   const int pr = cm.c.head_dim * esz / 16;                  // pieces per row

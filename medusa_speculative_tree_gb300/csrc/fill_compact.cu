@@ -50,7 +50,7 @@ __global__ void kv_compact_kernel(medusa_kv_t c, LayerPtrs<NL> lp, int write_met
   extern __shared__ __align__(16) unsigned char smem_raw[];
   EL* snap = reinterpret_cast<EL*>(smem_raw);       // [2][D+1][dh]
   __shared__ int rows_s[MEDUSA_MAX_DEPTH + 1];
-  __shared__ int verdict;
+  __shared__ int seq_status;
   const int kvh = blockIdx.x, b = blockIdx.y, layer = blockIdx.z;
   const bool meta = write_meta && kvh == 0 && layer == 0 && threadIdx.x == 0;
   const int dh = c.head_dim, W = t.max_depth + 1;
@@ -73,11 +73,11 @@ __global__ void kv_compact_kernel(medusa_kv_t c, LayerPtrs<NL> lp, int write_met
       int v = MEDUSA_OK;
       if (Lb < 0 || !seq_rows_ok(c, b, (int64_t)Lb + t.n_rows)) v = MEDUSA_ECAPACITY;
       else if (a < 0 || a > t.max_depth || any_bad) v = MEDUSA_EPATH;
-      verdict = v;
+      seq_status = v;
     }
   }
   __syncthreads();
-  const int v = verdict;
+  const int v = seq_status;
   if (v != MEDUSA_OK) {
     if (meta) {
       status[b] = v;
