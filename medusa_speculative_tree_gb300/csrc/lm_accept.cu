@@ -11,7 +11,12 @@
 //                      (bf16, zero padding columns), and every internal row's children
 //                      (row, token) in ascending row order;
 //   lm_stats_kernel    one persistent CTA per SM over 128-row groups of W_LM (the MMA's
-//                      M; groups blockIdx.x, blockIdx.x + gridDim.x, ...):
+//                      M).  With more than 256 columns the CTAs form P interleaved
+//                      sets, one per pass of up to 256 columns (CTA i serves pass
+//                      i % P); every set walks the same group order, so the sets read
+//                      each group of W_LM at about the same time and all but the first
+//                      read mostly hit L2.  Within a set, CTA c takes groups c, c + n,
+//                      2n + c, ... (n CTAs per set):
 //                        warp 0 (one lane)  TMA of W_LM boxes and of the packed rows;
 //                        warp 1             owns TMEM; one lane issues tcgen05.mma
 //                                           (kind::f16, bf16 operands, fp32 accumulate)
@@ -24,7 +29,7 @@
 //                      at the end the four warps' statistics are merged per column and
 //                      written as that CTA's chunk of the row;
 //   select (accept.cu) merges the CTAs' chunks per row and decides the paths.
-// Passes of at most 256 columns (B x n_internal rows) each stream W_LM once.
+// Up to four passes of 256 columns (B x n_internal rows) run in one launch.
 // All waits are bounded; a timeout sets an error flag and every sequence then
 // publishes nothing (accept_len = -1).
 #include <climits>
@@ -41,24 +46,27 @@ constexpr int kLThreads = 6 * 32;
 constexpr int kLRows = 128;           // vocabulary rows per group (MMA M)
 constexpr int kLKc = 64;              // K columns per TMA box (one 128-byte swizzle row)
 constexpr int kLMaxCols = 256;        // columns per pass (MMA N)
+constexpr int kLMaxPass = 4;          // passes (CTA sets) of one launch
 constexpr int kLKids = MEDUSA_MAX_TOPK;   // children of a row: distinct ranks of one head
 constexpr int kTileStride = 33;       // epilogue tile row stride (floats): conflict-free columns
 constexpr size_t kLMergeBytes = (size_t)4 * kLMaxCols * sizeof(RowPart);   // per-warp statistics at the end
 
 struct LmArgs {
   int V, d, N, NI;
-  int col0;               // first column of this pass (column = b * NI + internal index)
-  int n_cols;             // valid columns of this pass
-  int n_mma;              // MMA N: n_cols rounded up to 32 (32-column TMEM loads stay aligned)
+  int n_pass;                   // CTA sets of this launch, one per pass
+  int col0[kLMaxPass];          // first column of each pass (column = b * NI + internal index)
+  int n_cols[kLMaxPass];        // valid columns of each pass
+  int n_mma[kLMaxPass];         // MMA N: n_cols rounded up to 32 (32-column TMEM loads stay aligned)
+  int n_cta;                    // CTAs per set: the statistics chunks of a column
   float inv_temp;
   const int32_t* e_tok;   // [cols_pad][kLKids] child tokens
   const int32_t* e_row;   // [cols_pad][kLKids] child rows
   const int32_t* e_cnt;   // [cols_pad]
   float* edge_x;          // [B][N] logit of row v's token at its parent
-  RowPart* part;          // [B * NI][gridDim.x]
+  RowPart* part;          // [B * NI][n_cta]
   int* err;
   int n_stages, bps;
-  uint32_t stage_bytes;
+  uint32_t stage_bytes;         // stage stride, sized for the widest pass
 };
 
 __device__ __forceinline__ bool l_wait(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
@@ -136,11 +144,15 @@ __device__ __forceinline__ void lm_merge(float& m, float& z, float& s1, float& a
 
 template <bool TYP>
 __global__ void __launch_bounds__(kLThreads, 1)
-    lm_stats_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX,
-                    const LmArgs a) {
+    lm_stats_kernel(const __grid_constant__ CUtensorMap tmW, const __grid_constant__ CUtensorMap tmX0,
+                    const __grid_constant__ CUtensorMap tmX1, const __grid_constant__ CUtensorMap tmX2,
+                    const __grid_constant__ CUtensorMap tmX3, const LmArgs a) {
   extern __shared__ uint8_t smem_l[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_l) + 1023) & ~uintptr_t(1023));
-  const int S = a.n_stages, NM = a.n_mma, bps = a.bps;
+  const int pass = blockIdx.x % a.n_pass, cta = blockIdx.x / a.n_pass, n_cta = a.n_cta;
+  const int S = a.n_stages, NM = a.n_mma[pass], bps = a.bps;
+  const int col0 = a.col0[pass], n_cols = a.n_cols[pass];
+  const CUtensorMap* tmX = pass == 0 ? &tmX0 : pass == 1 ? &tmX1 : pass == 2 ? &tmX2 : &tmX3;
   // stages, then (at the end) the merge buffer in the same bytes, then the tiles
   const size_t region = (size_t)S * a.stage_bytes > kLMergeBytes ? (size_t)S * a.stage_bytes : kLMergeBytes;
   float* tiles = reinterpret_cast<float*>(sm + region);                          // [4][32][33]
@@ -190,7 +202,8 @@ __global__ void __launch_bounds__(kLThreads, 1)
   if (warp == 0) {
     // ---- TMA producer: every group of this CTA, n_k stages each ----------------------
     if (lane == 0) {
-      for (int g = blockIdx.x; g < n_groups && ok; g += gridDim.x) {
+      const uint32_t tx = (uint32_t)bps * (a_bytes + b_bytes);   // bytes of this pass's stage
+      for (int g = cta; g < n_groups && ok; g += n_cta) {
         for (int kc = 0; kc < n_k; ++kc) {
           const int s = slot % S;
           if (!l_wait(empty0 + 8 * s, (uint32_t)(((slot / S) & 1) ^ 1), abortp)) {
@@ -199,11 +212,11 @@ __global__ void __launch_bounds__(kLThreads, 1)
           }
           const uint32_t sA = smem_u32(sm + (size_t)s * a.stage_bytes), sB = sA + bps * a_bytes;
           const uint32_t bar = full0 + 8 * s;
-          mbar_expect_tx(bar, a.stage_bytes);
+          mbar_expect_tx(bar, tx);
           for (int bx = 0; bx < bps; ++bx) {
             const int col = (kc * bps + bx) * kLKc;
             tma_load_2d(sA + bx * a_bytes, &tmW, col, g * kLRows, bar);
-            tma_load_2d(sB + bx * b_bytes, &tmX, col, a.col0, bar);
+            tma_load_2d(sB + bx * b_bytes, tmX, col, col0, bar);
           }
           ++slot;
         }
@@ -215,7 +228,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
     if (lane == 0) {
       const uint32_t idesc = idesc_bf16(kLRows, NM);
       int u = 0;
-      for (int gl = 0; ok && (int)blockIdx.x + gl * (int)gridDim.x < n_groups; ++gl) {
+      for (int gl = 0; ok && cta + gl * n_cta < n_groups; ++gl) {
         const int db = gl & 1;
         // the accumulator must have been read out (group gl - 2) before it is reused
         if (gl >= 2 && !l_wait(dempty0 + 8 * db, (uint32_t)(((gl >> 1) - 1) & 1), abortp)) {
@@ -259,8 +272,8 @@ __global__ void __launch_bounds__(kLThreads, 1)
       st_av[ch] = -INFINITY;
       st_ai[ch] = INT_MAX;
     }
-    for (int gl = 0; (int)blockIdx.x + gl * (int)gridDim.x < n_groups; ++gl) {
-      const int g = blockIdx.x + gl * gridDim.x;
+    for (int gl = 0; cta + gl * n_cta < n_groups; ++gl) {
+      const int g = cta + gl * n_cta;
       const int db = gl & 1;
       if (!__all_sync(0xffffffffu, l_wait(dfull0 + 8 * db, (uint32_t)((gl >> 1) & 1), abortp))) {
         ok = false;
@@ -277,7 +290,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
         for (int j = 0; j < 32; ++j) tile[lane * kTileStride + j] = v[j];   // row = lane (one vocabulary id)
         __syncwarp();
         const int c = 32 * ch + lane;                  // this lane's column
-        if (c < a.n_cols) {
+        if (c < n_cols) {
           const int n_valid = min(32, a.V - id0);      // ids past V are padding rows of W_LM
           float av = st_av[ch];
           int ai = st_ai[ch];
@@ -306,7 +319,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
             st_z[ch] = z;
             st_s1[ch] = s1;
             // the logit of each child's token, where that token is one of these ids
-            const int cg = a.col0 + c;
+            const int cg = col0 + c;
             const int nk = a.e_cnt[cg];
             for (int e = 0; e < nk; ++e) {
               const int r = a.e_tok[cg * kLKids + e] - id0;
@@ -343,7 +356,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
       mg[q * kLMaxCols + 32 * ch + lane] = r;
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
-    for (int c = (warp - 2) * 32 + lane; intact && c < a.n_cols; c += 128) {
+    for (int c = (warp - 2) * 32 + lane; intact && c < n_cols; c += 128) {
       float m = -INFINITY, z = 0.f, s1 = 0.f, av = -INFINITY;
       int ai = INT_MAX;
       for (int w = 0; w < 4; ++w) lm_merge(m, z, s1, av, ai, mg[w * kLMaxCols + c]);
@@ -354,7 +367,7 @@ __global__ void __launch_bounds__(kLThreads, 1)
       out.amax_v = av;
       out.amax_i = ai;
       out.pad[0] = out.pad[1] = out.pad[2] = 0;
-      a.part[(int64_t)(a.col0 + c) * gridDim.x + blockIdx.x] = out;
+      a.part[(int64_t)(col0 + c) * n_cta + cta] = out;
     }
   }
 
@@ -425,7 +438,11 @@ LmAcceptPlan plan_lm_accept(const medusa_tree_t& t, int B, int V, int d) {
   p.cols_pad = (p.cols + 31) / 32 * 32;
   int dev = 0, sms = 148;
   if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
-  p.n_chunks = sms;
+  // CTAs per pass set: the SMs shared by the sets of the widest launch
+  int sets = (p.cols + kLMaxCols - 1) / kLMaxCols;
+  if (sets > kLMaxPass) sets = kLMaxPass;
+  if (sets < 1) sets = 1;
+  p.n_chunks = sms / sets;
   size_t off = 0;
   p.off_x = off;
   off = align_up(off + (size_t)p.cols_pad * d * 2, 256);
@@ -467,19 +484,26 @@ cudaError_t launch_lm_accept(const LmAcceptPlan& p, const medusa_tree_t& t, cons
     if ((e = cudaGetLastError()) != cudaSuccess) return e;
     CUtensorMap mw;
     if (!encode_rows(&mw, w_lm, p.d, p.V, kLRows)) return cudaErrorInvalidValue;
-    for (int c0 = 0; c0 < p.cols; c0 += kLMaxCols) {
-      const int n_cols = p.cols - c0 < kLMaxCols ? p.cols - c0 : kLMaxCols;
-      const int NM = (n_cols + 31) / 32 * 32;
-      CUtensorMap mx;
-      if (!encode_rows(&mx, X, p.d, p.cols_pad, NM)) return cudaErrorInvalidValue;
+    // launches of up to kLMaxPass passes; the first pass of a launch is its widest
+    for (int l0 = 0; l0 < p.cols; l0 += kLMaxPass * kLMaxCols) {
       LmArgs a{};
+      CUtensorMap mx[kLMaxPass];
+      a.n_pass = 0;
+      for (int c0 = l0; c0 < p.cols && a.n_pass < kLMaxPass; c0 += kLMaxCols, ++a.n_pass) {
+        const int n_cols = p.cols - c0 < kLMaxCols ? p.cols - c0 : kLMaxCols;
+        const int NM = (n_cols + 31) / 32 * 32;
+        if (!encode_rows(&mx[a.n_pass], X, p.d, p.cols_pad, NM)) return cudaErrorInvalidValue;
+        a.col0[a.n_pass] = c0;
+        a.n_cols[a.n_pass] = n_cols;
+        a.n_mma[a.n_pass] = NM;
+      }
+      for (int i = a.n_pass; i < kLMaxPass; ++i) mx[i] = mx[0];
+      const int NM = a.n_mma[0];
       a.V = p.V;
       a.d = p.d;
       a.N = t.n_rows;
       a.NI = p.NI;
-      a.col0 = c0;
-      a.n_cols = n_cols;
-      a.n_mma = NM;
+      a.n_cta = p.n_chunks;
       a.inv_temp = 1.f / temperature;
       a.e_tok = e_tok;
       a.e_row = e_row;
@@ -494,7 +518,7 @@ cudaError_t launch_lm_accept(const LmAcceptPlan& p, const medusa_tree_t& t, cons
       auto kern = typ ? lm_stats_kernel<true> : lm_stats_kernel<false>;
       if ((e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem)) != cudaSuccess)
         return e;
-      kern<<<p.n_chunks, kLThreads, smem, st>>>(mw, mx, a);
+      kern<<<p.n_chunks * a.n_pass, kLThreads, smem, st>>>(mw, mx[0], mx[1], mx[2], mx[3], a);
       if ((e = cudaGetLastError()) != cudaSuccess) return e;
     }
   }
