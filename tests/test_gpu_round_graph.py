@@ -124,6 +124,18 @@ def test_round_graph_with_hidden_state_acceptance(m):
         same(rnd, ref, f"hidden-state round, launch {rep}")
     assert int(rnd.accept_len[0]) >= 0
     rnd.close()
+    # the same with the commit fused into the acceptance kernel
+    upto = rd.max_L + rd.tmpl.n_rows
+    k0, v0 = cache_rows(rd, upto)
+    rnd = m.MedusaRound(rd.tmpl, rd.h, rd.w1, rd.w2, rd.w_lm, w.topk, rd.L, rd.q, rd.k, rd.v, rd.cache, rd.max_L,
+                        None, mode="typical", rope_base=w.rope_base, epsilon=w.epsilon, delta=w.delta,
+                        hidden_target=hid, fuse_commit=True)
+    rnd.launch()
+    torch.cuda.synchronize()
+    same(rnd, ref, "hidden-state round with the fused commit")
+    k1, v1 = cache_rows(rd, upto)
+    assert torch.equal(k1, k0) and torch.equal(v1, v0)
+    rnd.close()
 
 
 @pytest.mark.parametrize("name", ["tiny-fp32", "vicuna7b-64", "serving-b16-paged"])
