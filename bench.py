@@ -445,7 +445,11 @@ class RoundGraphs:
 
 def e2e_loop(rd: Round, steps: int, stream):
     """Same round through the public API with per-step inputs copied from pinned host
-    memory and the published result read back (both inside the timed region)."""
+    memory and the published result read back (both inside the timed region).  The
+    frontier rows and lengths are copied first, on the round's stream (the heads and
+    the fill read them); the attention and acceptance inputs follow on a second stream,
+    after the previous step's reads of those buffers, and overlap the heads; the round
+    waits for them before the attention call."""
     w = rd.w
     h_host = rd.h.cpu().pin_memory()
     q_host, k_host, v_host = (x.cpu().pin_memory() for x in (rd.q, rd.k, rd.v))
@@ -458,11 +462,21 @@ def e2e_loop(rd: Round, steps: int, stream):
     d2h = res_host.numel() * res_host.element_size()
     m = rd.m
 
+    side = torch.cuda.Stream(rd.dev)
+    ready = torch.cuda.Event()
+
     def one():
-        for dst, src in ((h_d, h_host), (q_d, q_host), (k_d, k_host), (v_d, v_host), (lg_d, lg_host), (L_d, L_host)):
+        main = torch.cuda.current_stream(rd.dev)
+        for dst, src in ((h_d, h_host), (L_d, L_host)):
             dst.copy_(src, non_blocking=True)
+        side.wait_stream(main)                       # the previous step has read q, k, v, logits
+        with torch.cuda.stream(side):
+            for dst, src in ((q_d, q_host), (k_d, k_host), (v_d, v_host), (lg_d, lg_host)):
+                dst.copy_(src, non_blocking=True)
+            ready.record(side)
         root, pool = m.medusa_heads_topk(h_d, rd.w1, rd.w2, rd.w_lm, w.topk)
         tokens, _ = m.medusa_tree_fill(rd.tmpl, root, pool, L_d)
+        main.wait_event(ready)
         m.medusa_tree_attn_verify(rd.tmpl, q_d, k_d, v_d, rd.cache, L_d, rd.max_L, rope_base=w.rope_base,
                                   out=rd.out, ws=rd.attn_ws)
         r = m.medusa_tree_accept(rd.tmpl, lg_d, tokens, rd.mode, epsilon=w.epsilon, delta=w.delta)
