@@ -184,3 +184,27 @@ def test_kv_compact_layers_checks_layers_without_a_gpu(native):
     assert lib.medusa_kv_compact_layers(arr, 0, C.byref(t.host), 2, L, a, rows, L_out, st, None) == native.EINVAL
     assert lib.medusa_kv_compact_layers(arr, 2, C.byref(t.host), 2, L, a, rows, L, st, None) == native.EINVAL
     assert lib.medusa_kv_compact_layers(None, 2, C.byref(t.host), 2, L, a, rows, L_out, st, None) == native.EINVAL
+
+
+def test_commit_and_hidden_acceptance_checks_without_a_gpu(native):
+    """Host-visible checks that return before any CUDA call: compaction and the fused
+    commit refuse L_out aliasing L (the kv-head CTAs of a sequence would race on it);
+    acceptance from hidden states refuses a hidden size that is not a multiple of 64."""
+    from medusa_speculative_tree_gb300.api import Template
+    lib = native.lib()
+    t = Template([(0,), (1,), (0, 0)], 2)
+    fake = lambda i: C.c_void_p(4096 * (i + 1))       # never dereferenced: the checks fail first
+    c = native.MedusaKV()
+    c.k, c.v, c.dtype, c.n_kv_heads, c.head_dim, c.capacity = fake(0).value, fake(1).value, 0, 2, 64, 64
+    c.page_size, c.block_table, c.max_blocks, c.n_pages = 0, None, 0, 0
+    L, a, rows, st = fake(10), fake(11), fake(12), fake(13)
+    assert lib.medusa_kv_compact(C.byref(c), C.byref(t.host), 2, L, a, rows, L, st, None) == native.EINVAL
+    outs = [fake(20 + i) for i in range(5)]
+    ws = fake(30)
+    assert lib.medusa_tree_accept_commit(C.byref(t.host), 2, 100, fake(31), native.F32, fake(32), native.GREEDY,
+                                         1.0, 0.09, 0.3, 0, C.byref(c), L, *outs, L, st, ws, 1 << 20,
+                                         None) == native.EINVAL
+    assert lib.medusa_tree_accept_hidden(C.byref(t.host), 2, 100, 100, fake(40), fake(41), fake(42), native.GREEDY,
+                                         1.0, 0.09, 0.3, *outs, ws, 1 << 20, None) == native.EUNSUPPORTED
+    assert lib.medusa_tree_accept_hidden(C.byref(t.host), 2, 100, 128, None, fake(41), fake(42), native.GREEDY,
+                                         1.0, 0.09, 0.3, *outs, ws, 1 << 20, None) == native.EINVAL
