@@ -6,6 +6,7 @@ library next to this file.  No CMake; only nvcc and the host compiler.
 from __future__ import annotations
 
 import concurrent.futures as cf
+import fcntl
 import os
 import shutil
 import subprocess
@@ -39,7 +40,7 @@ def _compile(src: str) -> str:
         cmd[1:1] = ["-x", "cu"]
     if os.environ.get("MEDUSA_PTXAS_VERBOSE"):
         cmd.insert(1, "-Xptxas=-v")
-    deps = [path, os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "kernels.h"),
+    deps = [path, os.path.join(CSRC, "common.cuh"), os.path.join(CSRC, "kernels.h"), os.path.join(CSRC, "tc.cuh"),
             os.path.join(INCLUDE, "medusa_gb300.h")]
     if os.path.exists(obj) and all(os.path.getmtime(obj) >= os.path.getmtime(d) for d in deps):
         return obj
@@ -52,7 +53,19 @@ def _compile(src: str) -> str:
 
 
 def build(verbose: bool = False) -> str:
+    """Compile what is out of date and link.  Processes that build at the same time (one
+    per rank of a multi-process launch) take turns on a lock file, so each finds the
+    objects and the library either complete or still to be built."""
     os.makedirs(BUILD, exist_ok=True)
+    with open(os.path.join(BUILD, "build.lock"), "w") as lock:
+        fcntl.flock(lock, fcntl.LOCK_EX)
+        try:
+            return _build_locked(verbose)
+        finally:
+            fcntl.flock(lock, fcntl.LOCK_UN)
+
+
+def _build_locked(verbose: bool) -> str:
     with cf.ThreadPoolExecutor(max_workers=min(len(SOURCES), os.cpu_count() or 4)) as ex:
         objs = list(ex.map(_compile, SOURCES))
     if os.path.exists(LIB) and all(os.path.getmtime(LIB) >= os.path.getmtime(o) for o in objs):
