@@ -28,6 +28,11 @@ Pinning status (what each function is checked against, in tests/):
                             N=1 = single-query attention; RoPE relative-phase identity
   accept.accept             [M7.2] §0x04G / §0x06B traces; [PartII] Part 7 cumprod
                             example; closed-form entropy of the Part 8 distribution
+  accept.row_stats          exact entropy: uniform, one-hot, two-point closed forms;
+                            guarded entropy ([M7.2] §0x04E): the same three cases worked
+                            by hand, and an edge whose typical decision the guard flips
+  accept.log_prob           temperature 2 against a hand-computed softmax
+  accept.target_logits      identity and orthonormal projections (closed forms)
   compact.kv_compact        [M7.2] §0x06B trace; overlap case against a snapshot-free copy
   cost                      [M7.2] §0x02E / §0x06 printed parameter and byte counts
 """

@@ -258,3 +258,63 @@ def test_target_logits_one_hot_closed_form():
         assert r.accept_len == 2
         assert list(r.out_rows) == [0, row[(0,)], row[(0, 0)]]
         assert list(r.out_tokens) == [tokens[0], target[0], target[row[(0,)]]]
+
+
+# ---- the guarded entropy and the temperature ----------------------------------------
+
+def test_guarded_entropy_closed_forms():
+    """[M7.2] §0x04E's guarded entropy -sum p ln(p + 1e-5) in special cases worked out
+    by hand:
+      uniform over n = 1000:  every p = 1/n, so H_g = -ln(1/n + 1e-5) = -ln(0.00101)
+                              = 6.897804948128969 (the exact entropy is ln 1000 = 6.907755);
+      one-hot:                the zero entries contribute 0 * ln(1e-5) = 0, so
+                              H_g = -ln(1 + 1e-5) = -9.99995e-6 (negative: the guard, not p,
+                              sits in the logarithm);
+      two-point (.2, .8):     ln(.20001) = ln .2 + ln 1.00005 = -1.6093879136840586,
+                              ln(.80001) = ln .8 + ln 1.0000125 = -0.2231310513923341,
+                              H_g = .2 * 1.6093879136840586 + .8 * 0.2231310513923341
+                                  = 0.500382423850679 (exact: 0.5004024235381879)."""
+    st = accept.row_stats(np.zeros(1000), entropy_guard=True)
+    assert st.entropy == pytest.approx(6.897804948128969, rel=1e-13)
+    one = np.full(50, -1e4)                      # e^-1e4 underflows to an exact 0
+    one[3] = 0.0
+    assert accept.row_stats(one, entropy_guard=True).entropy == pytest.approx(-9.999950000398841e-06, rel=1e-9)
+    two = np.array([0.0, math.log(4.0)])          # p = (.2, .8)
+    assert accept.row_stats(two, entropy_guard=True).entropy == pytest.approx(0.500382423850679, rel=1e-13)
+    assert accept.row_stats(two).entropy == pytest.approx(0.5004024235381879, rel=1e-13)
+
+
+def guard_decision_case():
+    """One edge whose typical decision the guard flips.  Row 0 over V = 1000 ids: the
+    candidate (token 7) has p = 3.02e-4, the other 999 ids share the rest equally
+    (1.0006987e-3 each).  Exact entropy H = 6.9074186283, threshold
+    tau = min(.09, .3 e^-H) = 3.0010101e-4 < p: accepted.  Guarded entropy
+    H_g = 6.8974683754, tau_g = .3 e^-H_g = 3.0310200e-4 > p: rejected."""
+    V_ = 1000
+    p = np.full(V_, (1.0 - 3.02e-4) / (V_ - 1))
+    p[7] = 3.02e-4
+    t = tree.compile_template([(0,)], topk=1)
+    logits = np.zeros((2, V_))
+    logits[0] = np.log(p)
+    tokens = np.array([0, 7])
+    return logits, tokens, t
+
+
+def test_typical_decision_follows_the_guard():
+    logits, tokens, t = guard_decision_case()
+    exact = accept.accept(logits, tokens, t.retrieve, "typical", epsilon=EPS, delta=DELTA)
+    guarded = accept.accept(logits, tokens, t.retrieve, "typical", epsilon=EPS, delta=DELTA, entropy_guard=True)
+    assert exact.accept_len == 1 and list(exact.out_tokens) == [0, 7]
+    assert guarded.accept_len == 0 and list(guarded.out_tokens) == [0]
+
+
+def test_temperature_two_closed_form():
+    """logits (0, ln 4) at T = 2 are (0, ln 2) after scaling, so p = (1/3, 2/3):
+    log p(1) = ln(2/3) = -0.40546510810816444, log p(0) = ln(1/3) = -1.0986122886681098,
+    H = ln 3 - (2/3) ln 2 = 0.6365141682948128, argmax 1."""
+    x = np.array([0.0, math.log(4.0)])
+    st = accept.row_stats(x, temperature=2.0)
+    assert st.argmax == 1
+    assert accept.log_prob(x, 1, st, 2.0) == pytest.approx(-0.40546510810816444, rel=1e-14)
+    assert accept.log_prob(x, 0, st, 2.0) == pytest.approx(-1.0986122886681098, rel=1e-14)
+    assert st.entropy == pytest.approx(0.6365141682948128, rel=1e-13)

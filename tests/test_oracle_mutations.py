@@ -150,3 +150,47 @@ def test_contiguous_commit_by_length(monkeypatch):
 def test_greedy_tree_wrong_tie_rule(monkeypatch):
     monkeypatch.setattr(tree, "_before", lambda wa, pa, wb, pb, rel=1e-12: wa < wb)
     assert fails(TT.test_greedy_toy_order)
+
+
+def _row_stats_with_entropy(entropy_fn):
+    """row_stats whose guarded entropy is computed by `entropy_fn(p)` (mutated copies)."""
+    real = accept.row_stats
+
+    def mutated(logits_row, temperature=1.0, entropy_guard=False):
+        st = real(logits_row, temperature, entropy_guard)
+        if entropy_guard:
+            x = np.asarray(logits_row, dtype=np.float64) / float(temperature)
+            e = np.exp(x - x.max())
+            st.entropy = float(entropy_fn(e / e.sum()))
+        return st
+    return mutated
+
+
+def test_guard_added_outside_the_log(monkeypatch):
+    # -sum p (ln p + 1e-5): the guard added after the logarithm
+    monkeypatch.setattr(accept, "row_stats", _row_stats_with_entropy(
+        lambda p: -(p[p > 0] * (np.log(p[p > 0]) + 1e-5)).sum()))
+    assert fails(AC.test_guarded_entropy_closed_forms)
+    assert fails(AC.test_typical_decision_follows_the_guard)
+
+
+def test_guard_only_on_zero_probabilities(monkeypatch):
+    # the guard applied only where p = 0, i.e. the exact entropy everywhere else
+    monkeypatch.setattr(accept, "row_stats", _row_stats_with_entropy(
+        lambda p: -(p * np.log(np.where(p > 0, p, 1e-5))).sum()))
+    assert fails(AC.test_guarded_entropy_closed_forms)
+    assert fails(AC.test_typical_decision_follows_the_guard)
+
+
+def test_guard_weighting_the_guard_too(monkeypatch):
+    # -sum (p + 1e-5) ln(p + 1e-5): the guard also in the weight
+    monkeypatch.setattr(accept, "row_stats", _row_stats_with_entropy(
+        lambda p: -((p + 1e-5) * np.log(p + 1e-5)).sum()))
+    assert fails(AC.test_guarded_entropy_closed_forms)
+
+
+def test_log_prob_without_temperature(monkeypatch):
+    # the candidate's logit taken unscaled while the statistics are scaled by 1 / T
+    monkeypatch.setattr(accept, "log_prob",
+                        lambda row, tok, st, temperature=1.0: float(np.float64(row[tok]) - st.m - st.log_z))
+    assert fails(AC.test_temperature_two_closed_form)
