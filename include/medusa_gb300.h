@@ -63,6 +63,9 @@ typedef int32_t medusa_status;
 #define MEDUSA_EPATH        -7   /* per-sequence: accepted path is not a valid tree chain */
 #define MEDUSA_ETIMEOUT     -8   /* per-sequence: a bounded device wait gave up; the sequence's
                                     outputs are invalid and the workspace must be re-zeroed */
+#define MEDUSA_ERANGE       -9   /* per-sequence: an input outside the range of the kernel's
+                                    arithmetic (bf16 attention: a K/V value with |x| >= 65536 or a
+                                    scaled rotated query beyond fp16); the outputs are invalid */
 
 typedef int32_t medusa_dtype;
 #define MEDUSA_F32  0
@@ -126,7 +129,8 @@ typedef struct {
 /* All rank paths of a regular Cartesian tree with widths s_1..s_K, in canonical
  * order ([M7.2] §0x02B; [CN] "多个 Medusa Head 如何产生候选树"; [Math] "From heads
  * to a candidate tree").  paths_out [host] [max_paths][K], -1 padded.  *n_out gets
- * sum_k prod_{i<=k} s_i.  MEDUSA_EWORKSPACE if max_paths is too small. */
+ * sum_k prod_{i<=k} s_i.  MEDUSA_EWORKSPACE if max_paths is too small.  With
+ * paths_out NULL and max_paths 0 the call is a size query: it sets *n_out only. */
 medusa_status medusa_tree_regular(const int32_t *widths /*[host] K*/, int32_t K,
                                   int32_t *paths_out, int32_t max_paths, int32_t *n_out);
 
@@ -222,16 +226,20 @@ size_t medusa_tree_attn_workspace(const medusa_tree_t *t, int32_t B, int32_t n_q
  *   cache dtype; L [B]; max_prefix >= every L[b] (sizes the split-KV grid);
  *   out [B][N][n_q_heads][head_dim] fp32 (the accumulation precision: a bf16 output
  *   would add ~1.6e-3 relative rounding error); lse [B][N][n_q_heads] fp32
- *   natural-log log-sum-exp, or NULL; status [B] (0, or MEDUSA_ECAPACITY when
- *   L[b] + N > capacity, in which case sequence b is not touched).
+ *   natural-log log-sum-exp, or NULL; status [B]: 0, or MEDUSA_ECAPACITY when
+ *   L[b] + N > capacity (sequence b is not touched), MEDUSA_ETIMEOUT when a bounded
+ *   wait gave up, MEDUSA_ERANGE (bf16 tensor-core path) when a K/V value or a
+ *   scaled rotated query lies outside fp16's range (|x| > 65504), so that the output
+ *   of b may hold inf or NaN.
  *   ws: workspace of medusa_tree_attn_workspace(...) bytes (16-byte aligned),
  *   zero-filled once before its first use.  Its first 256 KiB hold split-KV ticket
  *   counters that every call returns to zero, so one workspace can serve later
  *   calls of any shape without clearing; the rest is scratch.  Calls that share a
  *   workspace must not run concurrently.
- * Arithmetic: fp32 kernels for MEDUSA_F32; for MEDUSA_BF16 the prefix part runs
- * on tcgen05 tensor cores with fp16 operands (q' and P rounded to fp16, bf16 K/V
- * converted exactly) and fp32 accumulation, the tree part in fp32. */
+ * Arithmetic: fp32 kernels for MEDUSA_F32; for MEDUSA_BF16 with head_dim 128 the
+ * prefix and the tree rows run on tcgen05 tensor cores with fp16 operands (q' and P
+ * rounded to fp16, bf16 K/V converted exactly for |x| in [2^-14, 65504]) and fp32
+ * accumulation and softmax. */
 medusa_status medusa_tree_attn_verify(const medusa_tree_t *t, int32_t B, int32_t n_q_heads,
                                       const void *q, const void *k_new, const void *v_new,
                                       const medusa_kv_t *cache, const int32_t *L,
@@ -256,12 +264,14 @@ medusa_status medusa_tree_attn_verify(const medusa_tree_t *t, int32_t B, int32_t
  * medusa_tree_attn_verify with a caller workspace for such shapes.
  * The call allocates nothing: no cudaMalloc, no cudaFree, no allocating library
  * routine.  The first call on a device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and caches it; make that first
- * call before any stream capture.  Each call clears the ticket counters it will use
- * (one cudaMemsetAsync on `stream`) and otherwise reuses whatever the previous call
- * left in the array.  All calls share that one array, so calls that can overlap on
- * the GPU (different streams without ordering between them) race and must not be
- * issued. */
+ * (cudaGetSymbolAddress, with that device current) and caches it for the life of the
+ * process; make that first call before any stream capture.  A cudaDeviceReset of that
+ * device invalidates the cached address: make no further call of this entry point on
+ * a device after resetting it.  Each call clears, with cudaMemsetAsync on `stream`,
+ * what must start at zero (the ticket counters it will use, and `status`) and
+ * otherwise reuses whatever the previous call left in the array.  All calls share
+ * that one array, so calls that can overlap on the GPU (different streams without
+ * ordering between them) race and must not be issued. */
 medusa_status medusa_tree_attn_verify_static(const medusa_tree_t *t, int32_t B, int32_t n_q_heads,
                                              const void *q, const void *k_new, const void *v_new,
                                              const medusa_kv_t *cache, const int32_t *L,
@@ -452,6 +462,16 @@ medusa_status medusa_round_destroy(medusa_round_t round);
 
 const char *medusa_status_string(medusa_status s);
 int32_t medusa_abi_version(void);
+
+/* Testing only: makes the timeout path of the bounded device waits observable without
+ * a fault.  With ns > 0, every later launch of the bf16 tensor-core tree attention and
+ * of the one-row heads weight stream first waits on a flag that nothing sets; after ns
+ * nanoseconds the wait gives up and the launch takes its error path (attention:
+ * status[b] = MEDUSA_ETIMEOUT with no output, staged row or cache write; heads: root
+ * and pool -1, no logits written).  ns = 0 (the default) turns it off.  A process-wide
+ * setting read when a call is enqueued; not for use while other threads issue calls.
+ * The pages have no counterpart: it exists to test this library. */
+void medusa_test_set_stall_ns(uint64_t ns);
 
 #ifdef __cplusplus
 }

@@ -12,6 +12,7 @@ _PKG = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_PKG, "libmedusa_gb300.so")
 
 OK, EINVAL, ECAPACITY, EUNSUPPORTED, ETEMPLATE, ECUDA, EWORKSPACE, EPATH, ETIMEOUT = 0, -1, -2, -3, -4, -5, -6, -7, -8
+ERANGE = -9
 F32, BF16 = 0, 1
 GREEDY, TYPICAL = 0, 1
 MAX_ROWS, MAX_DEPTH, MAX_TOPK = 4096, 16, 32
@@ -25,6 +26,7 @@ EXPORTED = [
     "medusa_tree_accept_workspace",
     "medusa_tree_accept", "medusa_tree_accept_commit", "medusa_tree_accept_hidden_workspace", "medusa_tree_accept_hidden", "medusa_kv_compact", "medusa_kv_compact_layers", "medusa_round_workspace", "medusa_round_create",
     "medusa_round_launch", "medusa_round_destroy", "medusa_status_string", "medusa_abi_version",
+    "medusa_test_set_stall_ns",
 ]
 
 
@@ -116,6 +118,7 @@ def lib() -> C.CDLL:
         "medusa_round_destroy": (I32, [VP]),
         "medusa_status_string": (C.c_char_p, [I32]),
         "medusa_abi_version": (I32, []),
+        "medusa_test_set_stall_ns": (None, [C.c_uint64]),
     }
     for name, (res, args) in sig.items():
         fn = getattr(L, name)

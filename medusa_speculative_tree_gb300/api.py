@@ -66,12 +66,8 @@ def medusa_tree_regular(widths: Sequence[int]) -> list:
     K = len(widths)
     n = C.c_int32(0)
     w = np.ascontiguousarray(widths, dtype=np.int32)
-    cap = 1
-    total, prod = 0, 1
-    for s in widths:
-        prod *= int(s)
-        total += prod
-    cap = max(total, 1)
+    check("medusa_tree_regular", lib().medusa_tree_regular(w.ctypes.data, K, None, 0, C.byref(n)))
+    cap = max(n.value, 1)
     out = np.full((cap, max(K, 1)), -1, dtype=np.int32)
     check("medusa_tree_regular", lib().medusa_tree_regular(w.ctypes.data, K, out.ctypes.data, cap,
                                                            C.byref(n)))

@@ -24,6 +24,10 @@ constexpr int kLoads = 4;          // 16-byte loads in flight per thread in row_
 constexpr int kSelThreads = 1024;  // select: one warp per internal row, 32 rows at a time
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kCommitPieces = 2;   // 16-byte pieces a select thread holds while moving rows
+// The fused commit moves one KV head's K and V rows (2 G rows of head_dim elements, G <=
+// D + 1, head_dim <= 128, at most 4 bytes each) in one batch of pieces.
+static_assert(2 * (MEDUSA_MAX_DEPTH + 1) * (128 * 4 / 16) <= kSelThreads * kCommitPieces,
+              "one head's published K/V rows must fit the select kernel's pieces");
 
 
 // Merge two partial statistics (log-sum-exp with first moment).

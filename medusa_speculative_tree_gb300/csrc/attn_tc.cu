@@ -69,6 +69,7 @@ struct TcArgs {
   int32_t* status;
   int B, Hq, Hkv, g, n_mt, n_split, chunk, first;
   float scale_log2;
+  uint64_t stall_ns;     // test hook (0 = off): wait this long on a barrier nothing completes
   float th_hi[64], th_lo[64];
 };
 
@@ -154,33 +155,49 @@ __device__ __forceinline__ int64_t row_off_tc(const medusa_kv_t& c, int b, int k
 }
 
 
-// Wait for a phase; gives up (false) after ~2 s or as soon as another role of the CTA
-// has set the abort flag.
-__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const volatile int* abort_flag) {
+// Wait for a phase; gives up (false) after ~limit_ns (2 s by default) or as soon as
+// another role of the CTA has set the abort flag.
+__device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, const volatile int* abort_flag,
+                                              uint64_t limit_ns = 2000000000ull) {
   const uint64_t t0 = global_ns();
   for (uint32_t it = 0;; ++it) {
     if (mbar_try(bar, parity)) return true;
     if (*abort_flag) return false;
-    if ((it & 255u) == 255u && global_ns() - t0 > 2000000000ull) return false;
+    if ((it & 255u) == 255u && global_ns() - t0 > limit_ns) return false;
   }
+}
+
+// True when either fp16 of a packed pair is infinite or NaN (exponent field all ones):
+// the value was outside fp16's range (|x| > 65504) or not finite to begin with.
+__device__ __forceinline__ bool f16x2_nonfinite(uint32_t w) {
+  const uint32_t e = w & 0x7C007C00u;
+  return (e & 0xFFFFu) == 0x7C00u || (e >> 16) == 0x7C00u;
+}
+__device__ __forceinline__ bool f16x8_nonfinite(const uint4& v) {
+  return f16x2_nonfinite(v.x) | f16x2_nonfinite(v.y) | f16x2_nonfinite(v.z) | f16x2_nonfinite(v.w);
 }
 
 // Re-encode one K or V tile (2 blocks of [KT rows x 128 B], bf16) to fp16 in place;
 // rows of keys >= k_valid become zero.  Thread ct of the kConvThreads converter
 // threads; all its loads are issued before the first store, so their latencies overlap.
+// Returns true when a converted value is not finite in fp16.
 template <int kConvThreads, int KT>
-__device__ __forceinline__ void convert_tile(uint8_t* tile, int k_valid, int ct) {
+__device__ __forceinline__ bool convert_tile(uint8_t* tile, int k_valid, int ct) {
   uint4* p = reinterpret_cast<uint4*>(tile);
   constexpr int kIter = (KT * kDH * 2 / 16) / kConvThreads;
   uint4 v[kIter];
+  bool bad = false;
 #pragma unroll
   for (int i = 0; i < kIter; ++i) v[i] = p[i * kConvThreads + ct];
 #pragma unroll
   for (int i = 0; i < kIter; ++i) {
     const int idx = i * kConvThreads + ct;
     const int row = (idx % (KT * 8)) / 8;             // 16-byte chunks: 8 per row, 8 KT per block
-    p[idx] = row < k_valid ? bf16x8_to_f16x8(v[i]) : make_uint4(0, 0, 0, 0);
+    const uint4 o = row < k_valid ? bf16x8_to_f16x8(v[i]) : make_uint4(0, 0, 0, 0);
+    bad |= f16x8_nonfinite(o);
+    p[idx] = o;
   }
+  return bad;
 }
 
 // Tree-row key tile of KT rows: bf16 -> RoPE at L + depth[v] (fp32) -> fp16, in place.
@@ -191,9 +208,10 @@ template <int kConvThreads>
 __device__ __forceinline__ int rotate_row(int i, int ct) { return (i * kConvThreads + ct) >> 3; }
 
 template <int kConvThreads, int KT>
-__device__ __forceinline__ void convert_rotate_tile(uint8_t* tile, int n_valid, const int* dep,
+__device__ __forceinline__ bool convert_rotate_tile(uint8_t* tile, int n_valid, const int* dep,
                                                     const float* tab_c, const float* tab_s, int ct) {
   constexpr int kRotIter = (KT * 8) / kConvThreads;
+  bool bad = false;
 #pragma unroll
   for (int i = 0; i < kRotIter; ++i) {
     const int idx = i * kConvThreads + ct;
@@ -213,15 +231,19 @@ __device__ __forceinline__ void convert_rotate_tile(uint8_t* tile, int n_valid, 
         y1[e] = x1[e] * cs - x2[e] * sn;
         y2[e] = x2[e] * cs + x1[e] * sn;
       }
-      *p0 = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]), pack_half2(y1[4], y1[5]),
-                       pack_half2(y1[6], y1[7]));
-      *p1 = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]), pack_half2(y2[4], y2[5]),
-                       pack_half2(y2[6], y2[7]));
+      const uint4 o0 = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]), pack_half2(y1[4], y1[5]),
+                                  pack_half2(y1[6], y1[7]));
+      const uint4 o1 = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]), pack_half2(y2[4], y2[5]),
+                                  pack_half2(y2[6], y2[7]));
+      bad |= f16x8_nonfinite(o0) | f16x8_nonfinite(o1);
+      *p0 = o0;
+      *p1 = o1;
     } else {
       *p0 = make_uint4(0, 0, 0, 0);
       *p1 = make_uint4(0, 0, 0, 0);
     }
   }
+  return bad;
 }
 
 // Kernel configuration: QT query tiles of 128 rows per CTA share every K/V tile (one
@@ -267,7 +289,8 @@ struct TcCfg {
   static constexpr int kBarQReady = kBarODone + QT * kSB;    // queries staged (one arrival per warp)
   static constexpr int kBarDrain = kBarQReady + 1;           // final commit on the error path
   static constexpr int kBarQFull = kBarQReady + 2;           // query tiles landed
-  static constexpr int kNumBars = kBarQReady + 3;
+  static constexpr int kBarNever = kBarQReady + 3;           // test hook: never completes
+  static constexpr int kNumBars = kBarQReady + 4;
   // the merge reuses the query and stage buffers: [rows][32] float4 O, then (m, l)
   static_assert(QT * kQBytes + NS * kStageBytes >= kRows * (kDH * 4 + 8), "merge buffers do not fit");
 };
@@ -288,6 +311,7 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
       (reinterpret_cast<uintptr_t>(tab_s + (D + 1) * kHalf) + 7) & ~uintptr_t(7));
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  __shared__ int range_flag;       // an fp16 operand was not finite (value outside fp16's range)
 
   const int ct_idx = blockIdx.x, s = blockIdx.y;     // ct_idx: which QT row tiles
   // Units of longer sequences start first (longest-processing-time order, which packs
@@ -321,7 +345,8 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
     if (first_cta) a.status[b] = MEDUSA_EINVAL;
     return;
   }
-  if (first_cta) a.status[b] = MEDUSA_OK;
+  // (status[b] was cleared before the launch; CTAs write errors only, so no CTA can
+  // overwrite another's error with success)
 
   // Rows of this CTA: tiles QT * ct_idx .. + QT - 1 of 128 rows; CTA row r (= softmax
   // thread r) is global row R = 128 * QT * ct_idx + r.  A softmax warp whose 32 rows
@@ -420,6 +445,7 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
   int n_issued_k = -1;             // on an abort between the K and V copies of a tile: K's count
   if (tid == C::kProdWarp * 32) {
     abort_flag = 0;
+    range_flag = 0;
     for (int st = 0; st < NS; ++st) {
       mbar_init(BAR(C::kBarFullK + st), 1);
       mbar_init(BAR(C::kBarFullV + st), 1);
@@ -436,6 +462,7 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
     mbar_init(BAR(C::kBarQReady), C::kThreads / 32);
     mbar_init(BAR(C::kBarDrain), 1);
     mbar_init(BAR(C::kBarQFull), 1);
+    mbar_init(BAR(C::kBarNever), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     // the query tiles first: rows (u, group member) of each tile, 64 dims per copy
     mbar_expect_tx(BAR(C::kBarQFull), kQBytes * QT);
@@ -486,8 +513,17 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
   // rotated in place at L + depth, pre-multiplied by scale * log2 e and stored as fp16.
   // An item is one row's dims [8c, 8c + 8) and [64 + 8c, 64 + 8c + 8).
   // (wait outcomes are made warp-uniform: the softmax's TMEM accesses are warp-collective)
+  if (a.stall_ns != 0) {
+    // Test hook: a wait on a barrier that nothing completes runs out after stall_ns;
+    // the CTA then takes its error path at once (every role sees the abort flag).
+    if (!wait_or_abort(BAR(C::kBarNever), 0, abortp, a.stall_ns)) {
+      ok = false;
+      *const_cast<volatile int*>(abortp) = 1;
+    }
+  }
   if (!__all_sync(0xffffffffu, wait_or_abort(BAR(C::kBarQFull), 0, abortp))) ok = false;
   if (ok) {
+    bool bad = false;
     for (int it = tid; it < rows_valid * 8; it += C::kThreads) {
       const int r = it >> 3, c = it & 7;
       const int tr = r & (kTcRows - 1);
@@ -503,11 +539,15 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
         y1[e] = (x1[e] * cs - x2[e] * sn) * a.scale_log2;
         y2[e] = (x2[e] * cs + x1[e] * sn) * a.scale_log2;
       }
-      *q0 = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]), pack_half2(y1[4], y1[5]),
-                       pack_half2(y1[6], y1[7]));
-      *q1 = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]), pack_half2(y2[4], y2[5]),
-                       pack_half2(y2[6], y2[7]));
+      const uint4 o0 = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]), pack_half2(y1[4], y1[5]),
+                                  pack_half2(y1[6], y1[7]));
+      const uint4 o1 = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]), pack_half2(y2[4], y2[5]),
+                                  pack_half2(y2[6], y2[7]));
+      bad |= f16x8_nonfinite(o0) | f16x8_nonfinite(o1);
+      *q0 = o0;
+      *q1 = o1;
     }
+    if (bad) range_flag = 1;
   }
   fence_proxy_async();
   __syncwarp();
@@ -684,15 +724,16 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
         ok = false;
         break;
       }
-      if (j >= n_pre) convert_rotate_tile<C::kConvThreads, KT>(tK, k_valid, dep, tab_c, tab_s, ct);
-      else convert_tile<C::kConvThreads, KT>(tK, k_valid, ct);
+      const bool bad_k = j >= n_pre ? convert_rotate_tile<C::kConvThreads, KT>(tK, k_valid, dep, tab_c, tab_s, ct)
+                                    : convert_tile<C::kConvThreads, KT>(tK, k_valid, ct);
+      if (bad_k) range_flag = 1;
       fence_proxy_async();
       mbar_arrive(BAR(C::kBarConvK + st));
       if (!wait_or_abort(BAR(C::kBarFullV + st), (j / NS) & 1, abortp)) {
         ok = false;
         break;
       }
-      convert_tile<C::kConvThreads, KT>(tV, k_valid, ct);
+      if (convert_tile<C::kConvThreads, KT>(tV, k_valid, ct)) range_flag = 1;
       fence_proxy_async();
       mbar_arrive(BAR(C::kBarConvV + st));
     }
@@ -927,6 +968,9 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
   }
   __syncthreads();
   const bool failed = *abortp != 0;
+  // An operand outside fp16's range made the sequence's result invalid (it may hold
+  // inf or NaN): report it, unless the CTA gave up anyway.
+  if (tid == 0 && !failed && range_flag) atomicExch(&a.status[b], MEDUSA_ERANGE);
   if (failed) {
     // Drain (bounded) what this CTA may still have in flight before its shared memory
     // and TMEM are reused or released: the query copies, the last copy into each stage,
@@ -1284,10 +1328,14 @@ cudaError_t launch_attn_tc(const AttnPlan& p, const medusa_tree_t& t, const void
   a.chunk = p.chunk;
   a.first = p.first;
   a.scale_log2 = scale_log2;
+  a.stall_ns = test_stall_ns();
   for (int i = 0; i < 64; ++i) {
     a.th_hi[i] = th_hi[i];
     a.th_lo[i] = th_lo[i];
   }
+  // every CTA of a sequence may record an error; none records success
+  cudaError_t ce = cudaMemsetAsync(status, 0, sizeof(int32_t) * (size_t)p.B, st);
+  if (ce != cudaSuccess) return ce;
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(p.n_mt, p.n_split, p.B * p.Hkv);
   cfg.stream = st;

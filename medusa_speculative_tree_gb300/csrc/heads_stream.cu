@@ -71,7 +71,13 @@ struct StreamArgs {
                               // [K + 2] next group to hand out
   int32_t* root;
   int32_t* pool;              // [K][topk]
+  uint64_t stall_ns;          // test hook (0 = off): wait this long for a counter nothing advances
 };
+
+// A counter slot of the zeroed counter block that no code path advances (the test hook
+// waits on it).
+constexpr int kStallSlot = (int)(kHeadsCounterBytes / sizeof(int)) - 5;
+static_assert(MEDUSA_MAX_DEPTH + 2 < kStallSlot, "the counters of K heads reach cnt[K + 2]");
 
 // Stream segments: W1 (K * g1 groups), W_LM first half (ga), W2 (K * gv), W_LM rest (gv - ga).
 // Top-k matrix t: W2_t for t < K, W_LM for t = K; they publish in that order.
@@ -195,14 +201,27 @@ __global__ void __launch_bounds__(kSThreads, 1) heads_stream_kernel(const Stream
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   __syncthreads();
-  auto give_up = [&]() {
-    *const_cast<volatile int*>(abortp) = 1;
+  auto give_up = [&]() {          // the error flag first: whoever sees the abort sees it
     atomicExch(a.err, 1);
+    __threadfence();
+    *const_cast<volatile int*>(abortp) = 1;
   };
 
   if (warp == kSProducer) {
     // ---- weight stream --------------------------------------------------------------
     if (lane != 0) return;
+    if (a.stall_ns != 0) {
+      // Test hook: wait for a counter that nothing advances; after stall_ns give up
+      // before any copy is issued, so the CTA's error path has nothing to drain.
+      const uint64_t t0 = global_ns();
+      for (;;) {
+        int v;
+        asm volatile("ld.acquire.gpu.global.b32 %0, [%1];" : "=r"(v) : "l"(a.cnt + kStallSlot) : "memory");
+        if (v != 0 || global_ns() - t0 > a.stall_ns) break;
+      }
+      give_up();
+      return;
+    }
     // Stage slots carry a group index, -2 (a marker: leave the W1 phase) or -1 (the end).
     int slot = 0, x_loads = 0, x_src = -2;
     bool z_ready = false;
@@ -628,6 +647,7 @@ cudaError_t launch_heads_stream(const HeadsPlan& p, const void* h, const void* w
   a.cnt = a.err + 4;
   a.root = root;
   a.pool = pool;
+  a.stall_ns = test_stall_ns();
   const size_t smem = heads_stream_smem(p.d);
   auto kern = heads_stream_split(p.d) == 1 ? heads_stream_kernel<1> : heads_stream_kernel<2>;
   cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);

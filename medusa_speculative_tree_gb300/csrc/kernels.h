@@ -8,7 +8,15 @@
 
 #include "medusa_gb300.h"
 
+#include <atomic>
+
 namespace medusa {
+
+// Test hook of medusa_test_set_stall_ns: when non-zero, the tensor-core attention and
+// the heads weight stream first wait this many nanoseconds on a flag that nothing
+// sets, then take their error path.  0 (the default) in normal operation.
+extern std::atomic<uint64_t> g_test_stall_ns;
+uint64_t test_stall_ns();
 
 // ---- heads + top-k ---------------------------------------------------------
 struct HeadsPlan {

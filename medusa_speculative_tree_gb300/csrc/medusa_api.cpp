@@ -3,6 +3,7 @@
 #include <cuda_runtime.h>
 
 #include <algorithm>
+#include <atomic>
 #include <cmath>
 #include <cstring>
 #include <map>
@@ -13,6 +14,11 @@
 #include "medusa_gb300.h"
 
 using medusa::align_up;
+
+namespace medusa {
+std::atomic<uint64_t> g_test_stall_ns{0};
+uint64_t test_stall_ns() { return g_test_stall_ns.load(std::memory_order_relaxed); }
+}  // namespace medusa
 
 namespace {
 
@@ -99,7 +105,9 @@ medusa_status accept_logits_impl(const medusa_tree_t* t, int32_t B, int32_t V, c
 
 extern "C" {
 
-int32_t medusa_abi_version(void) { return 3; }
+int32_t medusa_abi_version(void) { return 4; }
+
+void medusa_test_set_stall_ns(uint64_t ns) { medusa::g_test_stall_ns.store(ns, std::memory_order_relaxed); }
 
 const char* medusa_status_string(medusa_status s) {
   switch (s) {
@@ -112,6 +120,7 @@ const char* medusa_status_string(medusa_status s) {
     case MEDUSA_EWORKSPACE: return "workspace or output buffer too small";
     case MEDUSA_EPATH: return "accepted path is not a valid tree chain";
     case MEDUSA_ETIMEOUT: return "a bounded device wait gave up";
+    case MEDUSA_ERANGE: return "a value outside the range of the kernel's fp16 operands";
     default: return "unknown status";
   }
 }
@@ -135,6 +144,7 @@ medusa_status medusa_tree_regular(const int32_t* widths, int32_t K, int32_t* pat
     level.swap(next);
   }
   *n_out = (int32_t)all.size();
+  if (!paths_out && max_paths == 0) return MEDUSA_OK;          // a size query
   if ((int32_t)all.size() > max_paths) return MEDUSA_EWORKSPACE;
   for (size_t i = 0; i < all.size(); ++i)
     for (int j = 0; j < K; ++j) paths_out[i * K + j] = j < (int)all[i].size() ? all[i][j] : -1;

@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(native):
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(native.EXPORTED)
-    assert native.lib().medusa_abi_version() == 3
+    assert native.lib().medusa_abi_version() == 4
     assert native.lib().medusa_status_string(-2).decode() == "cache capacity exceeded"
 
 

@@ -78,9 +78,17 @@ def test_static_scratch_matches_workspace_entry(m, name):
         out = torch.full((B, N, w.n_q_heads, w.head_dim), float("nan"), device="cuda")
         lse = torch.full((B, N, w.n_q_heads), float("nan"), device="cuda")
         status = torch.full((B,), 99, dtype=torch.int32, device="cuda")
-        rc = _static_call(m, t_g, q, k, v, m.KVCache(K_s, V_s), L, max_prefix, w.rope_base, out, lse, status)
+        cache_s = m.KVCache(K_s, V_s)
+        torch.cuda.synchronize()
+        torch_bytes, (free_bytes, _) = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()
+        rc = _static_call(m, t_g, q, k, v, cache_s, L, max_prefix, w.rope_base, out, lse, status)
         assert rc == nat.OK, nat.lib().medusa_status_string(rc)
         torch.cuda.synchronize()
+        if call == 1:
+            # nothing allocated by the call: neither through torch nor from the device
+            # (the first call may still load kernels lazily, so the second is measured)
+            assert torch.cuda.memory_allocated() == torch_bytes
+            assert torch.cuda.mem_get_info()[0] == free_bytes
         assert (status.cpu().numpy() == 0).all()
         gu.float_parity(out, ref, is_f32, f"static entry, call {call}")
         gu.float_parity(lse, ref_lse, True, f"static entry lse, call {call}")
