@@ -2,9 +2,10 @@
 
 A step is one whole round of the hot path on one batch of synthetic input:
 medusa_heads_topk -> medusa_tree_fill -> medusa_tree_attn_verify ->
-medusa_tree_accept -> medusa_kv_compact.  The default workload is the
-Vicuna-7B-shaped round (bf16, batch 1, 64-row greedy tree, L = 2048, K = 4
-heads over d = 4096 and V = 32000).
+medusa_tree_accept -> medusa_kv_compact.  The headline workload is the
+long-context round, the largest configuration (bf16, batch 1, the full 341-row
+Cartesian tree (4,4,4,4), GQA 64/8 heads, L = 32768, K = 4 heads over d = 8192 and
+V = 128256); the line also carries the other four workloads under `per_workload`.
 
   python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME] [--impl native|reference]
 
@@ -276,9 +277,11 @@ ATTN_TRAFFIC = {"vicuna7b-64": 35_210_752 + 0}
 
 def heads_all_rows(rd, stream, peak_tflops):
     """medusa_heads_topk with every tree row as a hidden row (T = B N), the variant in which
-    the heads are a tensor-core contraction.  bf16 with T >= 2 runs on the tensor cores
-    with each input row as a bf16 pair (hi, lo), so the MMAs execute twice the useful
-    2 T flops per weight element; both rates are reported."""
+    the heads are a tensor-core contraction.  `frac` is the method's useful rate, 2 T
+    flops per weight element, over the bf16 peak.  bf16 with T >= 2 runs on the tensor
+    cores with each input row of W2 (z, an fp32 value) as a bf16 pair (hi, lo), so the
+    MMAs execute twice the useful flops on W2; the rows of W1 and W_LM (h, exactly bf16)
+    are single.  The executed rate is reported beside the useful one."""
     w = rd.w
     T = w.batch * rd.N                                  # every tree row of every sequence
     h = synth.normal((T, w.hidden), 1.0, w.seed, "h", rd.dev, w.torch_dtype, sub=1)
@@ -290,11 +293,13 @@ def heads_all_rows(rd, stream, peak_tflops):
     us = 1e3 * time_loop(call, n, stream) / n
     elems = rd.w1.numel() + rd.w2.numel() + rd.w_lm.numel()
     useful = 2.0 * T * elems / (us * 1e-6) / 1e12
-    pairs = 2 if (w.dtype == "bf16" and T >= 2) else 1
-    passes = math.ceil(T / 128) if pairs == 2 else 1
-    return {"T": T, "us": us, "useful_tflops": useful, "tensor_tflops": useful * pairs,
-            "peak_tflops": peak_tflops, "frac": useful * pairs / peak_tflops, "weight_passes": passes,
-            "hbm_gbs": passes * rd.head_bytes() / (us * 1e-6) / 1e9}
+    mma = w.dtype == "bf16" and T >= 2
+    executed = 2.0 * T * (rd.w1.numel() + 2 * rd.w2.numel() + rd.w_lm.numel()) / (us * 1e-6) / 1e12 if mma \
+        else useful
+    passes = math.ceil(T / 128) if mma else 1
+    return {"T": T, "us": us, "useful_tflops": useful, "executed_tflops": executed,
+            "peak_tflops": peak_tflops, "frac": useful / peak_tflops, "executed_frac": executed / peak_tflops,
+            "weight_passes": passes, "hbm_gbs": passes * rd.head_bytes() / (us * 1e-6) / 1e9}
 
 
 def compact_all_layers(rd, results, stream, flush, n_layers=32):
@@ -493,33 +498,171 @@ def e2e_loop(rd: Round, steps: int, stream):
 
 # ----------------------------------------------------------------------------- CPU oracle
 
-def oracle_round_seconds(w: synth.Workload, reps: int = 1):
-    """Time the fp64 oracle (as it stands) on a full round of the workload, host only.
-    Returns (seconds per round, threads, description)."""
-    from oracle import round as oround
-    acc = synth.rank_accuracy(w.n_heads, 10)
-    t_o = oround.template_for(w.template, w.topk, w.n_heads, acc)
-    N = t_o.n_rows
-    h, w1, w2, w_lm = synth.head_weights(w)
-    q, k, v = synth.tree_qkv(w, N)
-    lengths = synth.prefix_lengths(w)
-    ks, vs = synth.prefix_kv(w, lengths)
-    logits = synth.target_logits(w, N)
-    f64 = lambda t: t.detach().double().numpy()
-    times = []
-    for _ in range(reps):
-        t0 = time.perf_counter()
-        for b in range(w.batch):
-            L = int(lengths[b])
+def _blas_threads():
+    """Threads of the BLAS that NumPy loaded, asked from the library itself where it
+    exports a query (OpenBLAS builds do), else the environment's setting, else None."""
+    import ctypes
+    names = ["openblas_get_num_threads", "openblas_get_num_threads64_", "scipy_openblas_get_num_threads64_",
+             "scipy_openblas_get_num_threads"]
+    libs = set()
+    try:
+        with open("/proc/self/maps") as f:
+            for ln in f:
+                path = ln.split()[-1]
+                base = os.path.basename(path).lower()
+                if "blas" in base and ".so" in base:
+                    libs.add(path)
+    except OSError:
+        pass
+    libs = sorted(libs)
+    for path in libs:
+        if not os.path.exists(path):
+            continue
+        try:
+            lib = ctypes.CDLL(path)
+        except OSError:
+            continue
+        for n in names:
+            fn = getattr(lib, n, None)
+            if fn is not None:
+                fn.restype = ctypes.c_int
+                return int(fn())
+    for var in ("OPENBLAS_NUM_THREADS", "OMP_NUM_THREADS", "MKL_NUM_THREADS"):
+        if os.environ.get(var):
+            return int(os.environ[var])
+    return None
+
+
+class OracleSample:
+    """A bounded sample of one verify round of a workload for the fp64 oracle (as it
+    stands), and the per-stage times it gives, each scaled to the whole round by the
+    stage's share of work that the sample covers:
+
+      heads      medusa_heads on every frontier row with head 0 only and the first
+                 `v_rows` rows of W2_0 and W_LM (W1_0 whole): scaled by the weight
+                 elements of the round over those of the sample;
+      fill       every sequence, whole;
+      attention  tree_attention of every sequence for the query heads of KV head 0:
+                 scaled by the number of KV heads;
+      accept     every sequence, whole (unplanted N(0, 1) target logits);
+      compact    every sequence, whole, on the KV head 0 cache.
+
+    The inputs come from the workload's own seeded generators on the host (the leading
+    rows of a seeded draw are the rows of the full draw), converted to float64 before
+    the clock starts."""
+
+    def __init__(self, w: synth.Workload, v_rows: int):
+        from oracle import round as oround
+        self.w = w
+        acc = synth.rank_accuracy(w.n_heads, 10)
+        self.t = oround.template_for(w.template, w.topk, w.n_heads, acc)
+        N = self.N = self.t.n_rows
+        d, V, K = w.hidden, w.vocab, w.n_heads
+        self.v_rows = vr = max(w.topk, min(V, v_rows))
+        f64 = lambda x: x.detach().double().numpy()
+        self.h = f64(synth.normal((w.batch, d), 1.0, w.seed, "h", "cpu", w.torch_dtype))
+        self.w1 = f64(synth.normal((1, d, d), 0.02, w.seed, "w1", "cpu", w.torch_dtype))
+        self.w2 = f64(synth.normal((vr, d), 1.0 / math.sqrt(d), w.seed, "w2", "cpu", w.torch_dtype, sub=0))[None]
+        self.w_lm = f64(synth.normal((vr, d), 1.0 / math.sqrt(d), w.seed, "w_lm", "cpu", w.torch_dtype))
+        self.head_scale = (K * d * d + (K + 1) * V * d) / float(d * d + 2 * vr * d)
+        g = w.group
+        q, k, v = synth.tree_qkv(w, N)
+        self.q, self.k, self.v = f64(q[:, :, :g]), f64(k[:, :, :1]), f64(v[:, :, :1])
+        self.lengths = synth.prefix_lengths(w)
+        self.ck, self.cv = [], []
+        for b, L in enumerate(self.lengths):
+            L = int(L)
             cap = L + N + 1
-            ck = np.zeros((w.n_kv_heads, cap, w.head_dim))
+            ck = np.zeros((1, cap, w.head_dim))
             cv = np.zeros_like(ck)
-            ck[:, :L], cv[:, :L] = f64(ks[b]), f64(vs[b])
-            oround.run_sequence(t_o, f64(h[b]), f64(w1), f64(w2), f64(w_lm), f64(q[b]), f64(k[b]), f64(v[b]),
-                                ck, cv, L, f64(logits[b]), w.accept[0], w.rope_base, epsilon=w.epsilon,
-                                delta=w.delta)
-        times.append(time.perf_counter() - t0)
-    return min(times), torch.get_num_threads(), f"{reps} full oracle round(s) of {w.name}, best taken"
+            ck[:, :L] = f64(synth.normal((1, L, w.head_dim), 1.0, w.seed, "cache_k", "cpu", w.torch_dtype, sub=b))
+            cv[:, :L] = f64(synth.normal((1, L, w.head_dim), 1.0, w.seed, "cache_v", "cpu", w.torch_dtype, sub=b))
+            self.ck.append(ck)
+            self.cv.append(cv)
+        self.logits = f64(synth.target_logits(w, N))
+        self.attn_scale = float(w.n_kv_heads)
+
+    def run(self):
+        """Per-stage µs of one round (scaled), the oracle called as it stands."""
+        from oracle import accept as oacc
+        from oracle import attention as oatt
+        from oracle import compact as ocomp
+        from oracle import heads as oheads
+        from oracle import round as oround
+        w, t = self.w, self.t
+        clock = time.perf_counter
+        t0 = clock()
+        root, pool, _ = oheads.medusa_heads(self.h, self.w1, self.w2, self.w_lm, w.topk)
+        t1 = clock()
+        pool_full = np.tile(pool, (1, w.n_heads, 1))          # the sample's pool stands in for every head
+        tokens = [oround.tree_fill(t, root[b], pool_full[b], int(self.lengths[b])) for b in range(w.batch)]
+        t2 = clock()
+        for b in range(w.batch):
+            oatt.tree_attention(self.q[b], self.k[b], self.v[b], self.ck[b], self.cv[b], int(self.lengths[b]),
+                                t.depth, t.mask, w.rope_base)
+        t3 = clock()
+        res = [oacc.accept(self.logits[b], tokens[b][0], t.retrieve, w.accept[0], 1.0, w.epsilon, w.delta)
+               for b in range(w.batch)]
+        t4 = clock()
+        for b in range(w.batch):
+            ocomp.kv_compact(self.ck[b], self.cv[b], int(self.lengths[b]), res[b].out_rows)
+        t5 = clock()
+        us = lambda a, b_: 1e6 * (b_ - a)
+        return {"heads": us(t0, t1) * self.head_scale, "fill": us(t1, t2), "attn": us(t2, t3) * self.attn_scale,
+                "accept": us(t3, t4), "compact": us(t4, t5)}
+
+    def describe(self):
+        w = self.w
+        return (f"{w.name}: heads on head 0 with W1_0 and the first {self.v_rows} of {w.vocab} rows of W2_0 and "
+                f"W_LM (x{self.head_scale:.1f}), attention for KV head 0's {w.group} query heads of every sequence "
+                f"(x{int(self.attn_scale)}), fill, acceptance and compaction whole; fp64 NumPy")
+
+
+def oracle_stages(w: synth.Workload, v_rows: int, reps: int = 1):
+    """Best of `reps` sampled oracle rounds: (per-stage µs, description)."""
+    smp = OracleSample(w, v_rows)
+    best = None
+    for _ in range(reps):
+        st = smp.run()
+        if best is None or sum(st.values()) < sum(best.values()):
+            best = st
+    return best, smp.describe()
+
+
+def cpu_baseline_of(w: synth.Workload, v_rows: int, one_thread: bool):
+    """The sampled oracle round on all host cores, and (one_thread) again in a child
+    process whose BLAS and torch use one thread (set before NumPy loads)."""
+    stages, desc = oracle_stages(w, v_rows)
+    out = {"value": sum(stages.values()), "unit": UNIT, "cores": os.cpu_count(), "kind": "oracle",
+           "sample": desc, "all_cores": {"us": sum(stages.values()), "stages_us": stages,
+                                         "blas_threads": _blas_threads(), "torch_threads": torch.get_num_threads()},
+           "cpu_count": os.cpu_count()}
+    if one_thread:
+        env = dict(os.environ, OMP_NUM_THREADS="1", OPENBLAS_NUM_THREADS="1", MKL_NUM_THREADS="1")
+        r = subprocess.run([sys.executable, os.path.abspath(__file__), "--oracle-sample", w.name,
+                            "--oracle-v-rows", str(v_rows)], env=env, capture_output=True, text=True, timeout=900)
+        if r.returncode == 0 and r.stdout.strip():
+            one = json.loads(r.stdout.strip().splitlines()[-1])
+            out["one_thread"] = {"us": sum(one["stages_us"].values()), "stages_us": one["stages_us"],
+                                 "blas_threads": one["blas_threads"], "torch_threads": one["torch_threads"]}
+        else:
+            out["one_thread"] = {"error": (r.stderr or "no output").strip().splitlines()[-1:]}
+    return out
+
+
+def run_oracle_sample(args):
+    """Child process of the one-thread baseline: prints the sampled stage times."""
+    torch.set_num_threads(1)
+    w = synth.WORKLOADS[args.oracle_sample]
+    stages, desc = oracle_stages(w, args.oracle_v_rows)
+    print(json.dumps({"stages_us": stages, "sample": desc, "blas_threads": _blas_threads(),
+                      "torch_threads": torch.get_num_threads()}))
+
+
+# rows of W2_0 / W_LM in the sampled heads stage: the benchmark's CPU baseline, and the
+# smaller per-step sample of the reference arm (which repeats it warmup + steps times)
+BASELINE_V_ROWS = 8192
+REFERENCE_V_ROWS = 4096
 
 
 def run_reference(args):
@@ -527,19 +670,22 @@ def run_reference(args):
     if rank != 0:
         return
     w = synth.WORKLOADS[args.workload]
-    secs = []
+    smp = OracleSample(w, REFERENCE_V_ROWS)
+    rounds = []
     for i in range(args.warmup + args.steps):
-        s, cores, _ = oracle_round_seconds(w, 1)
+        st = smp.run()
         if i >= args.warmup:
-            secs.append(s)
-    us = 1e6 * sum(secs) / len(secs)
+            rounds.append(st)
+    us = sum(sum(st.values()) for st in rounds) / len(rounds)
+    stages = {k: sum(st[k] for st in rounds) / len(rounds) for k in rounds[0]}
     line = {
         "impl": "reference", "metric": METRIC, "value": us, "unit": UNIT, "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": us / 1e3, "higher_is_better": False,
         "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
         "config": config_of(w, None),
-        "cpu_baseline": {"kind": "oracle", "value": us, "unit": UNIT, "cores": cores,
-                         "sample": f"one full fp64 oracle round of {w.name} per step"},
+        "cpu_baseline": {"kind": "oracle", "value": us, "unit": UNIT, "cores": os.cpu_count(),
+                         "blas_threads": _blas_threads(), "torch_threads": torch.get_num_threads(),
+                         "sample": "each step: " + smp.describe(), "stages_us": stages},
         "e2e": {"value": us, "unit": UNIT, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -550,14 +696,104 @@ def config_of(w: synth.Workload, rd):
          "q_heads": w.n_q_heads, "kv_heads": w.n_kv_heads, "head_dim": w.head_dim,
          "prefix_len": w.prefix_len if w.prefix_len else f"U{list(w.prefix_range)}",
          "medusa_heads": w.n_heads, "hidden": w.hidden, "vocab": w.vocab, "accept": w.accept[0],
-         "paged": bool(w.page_size),
+         "paged": bool(w.page_size), "tree_rows": tree_rows(w),
          "l2": "inputs larger than L2: each step streams the head weights (>= 1.4 GB) before the KV; "
                "stage timings flush L2 with a 512 MB write",
          "launch": "each step is one medusa_round_launch (the library's CUDA graph of the five calls); "
                    "e2e calls the five API functions eagerly"}
-    if rd is not None:
-        c["tree_rows"] = rd.N
     return c
+
+
+def tree_rows(w: synth.Workload) -> int:
+    """Rows of the workload's template (root included): the regular tree's sum of
+    products of widths plus the root, or the greedy budget plus the root."""
+    if w.template[0] == "regular":
+        n, prod = 1, 1
+        for s in w.template[1]:
+            prod *= s
+            n += prod
+        return n
+    return 1 + w.template[1]
+
+
+# ----------------------------------------------------------------------------- measurement
+
+def measure(m, w: synth.Workload, dev, steps: int, warmup: int, flush, ws: int, local: int, rank: int,
+            extras: bool):
+    """One workload: the timed round-graph steps (clocks sampled meanwhile), then the
+    per-stage split, the heads launch, the end-to-end loop and (extras) the variants."""
+    hbm, bf16, src = peaks()
+    rd = Round(m, w, dev)
+    stream = torch.cuda.current_stream(dev)
+    for _ in range(warmup):
+        rd.step()
+    graphs = RoundGraphs(rd, dev)
+    for _ in range(warmup):
+        graphs.step()
+    torch.cuda.synchronize(dev)
+    barrier(ws)
+    torch.cuda.synchronize(dev)
+    with ClockSampler(local) as clk:
+        ms = time_loop(graphs.step, steps, stream)
+        torch.cuda.synchronize(dev)
+    barrier(ws)
+    ms_step = max_over_ranks(ms / steps, ws, dev)
+    us_round = 1e3 * ms_step / ws                      # whole job: ws rounds per step
+
+    stages = graphs.stage_times(20, stream, flush)
+    attn_us = stages["attn"]
+    round_b = rd.round_bytes(graphs.native.accept_len)
+    round_gbs = round_b / (ms_step * 1e-3) / 1e9      # one round per GPU per step
+    attn_gbs = rd.attn_bytes() / (attn_us * 1e-6) / 1e9
+    attn_tf = rd.attn_flops() / (attn_us * 1e-6) / 1e12
+    # the dominant kernel: heads launches back to back (the head weights exceed L2, so
+    # every launch streams them from HBM), events on the replay stream
+    heads_us = 1e3 * time_loop(graphs.stage["heads"].replay, 20, stream) / 20
+    heads_gbs = rd.head_bytes() / (heads_us * 1e-6) / 1e9
+    e2e_ms, h2d, d2h = e2e_loop(rd, max(10, steps // 4), stream)
+    e2e_ms = max_over_ranks(e2e_ms, ws, dev)
+    tensor_bound = w.name in ATTN_TENSOR_BOUND
+    res = {
+        "value": us_round, "ms_per_step": ms_step, "nodes_per_s": ws * w.batch * rd.N / (ms_step * 1e-3),
+        "stages_us": stages,
+        "roofline": {"kernel": "medusa_heads_topk (head-weight stream with top-k)",
+                     "bound": "hbm", "achieved": heads_gbs, "peak": hbm, "unit": "GB/s",
+                     "frac": heads_gbs / hbm, "traffic": HEADS_TRAFFIC.get(w.name), "peak_source": src,
+                     "algorithmic_bytes": rd.head_bytes(), "launch_us": heads_us},
+        "tree_attn": {"us": attn_us, "hbm_gbs": attn_gbs, "frac_of_hbm_peak": attn_gbs / hbm, "tflops": attn_tf,
+                      "frac_of_tensor_peak": attn_tf / bf16},
+        "tree_attn_roofline": ({"kernel": "medusa_tree_attn_verify", "bound": "tensor", "achieved": attn_tf,
+                                "peak": bf16, "unit": "TFLOP/s", "frac": attn_tf / bf16,
+                                "algorithmic_flops": rd.attn_flops(), "peak_source": src,
+                                "note": "fp16 operands: the fp16 dense rate equals the bf16 one"}
+                               if tensor_bound else
+                               {"kernel": "medusa_tree_attn_verify", "bound": "hbm", "achieved": attn_gbs,
+                                "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm,
+                                "traffic": ATTN_TRAFFIC.get(w.name), "peak_source": src,
+                                "algorithmic_bytes": rd.attn_bytes()}),
+        "round_roofline": {"bound": "hbm", "achieved": round_gbs, "peak": hbm, "unit": "GB/s",
+                           "frac": round_gbs / hbm, "peak_source": src, "algorithmic_bytes": round_b,
+                           "note": "all five steps' algorithmic bytes over one round's device time"},
+        "e2e": {"value": 1e3 * e2e_ms / ws, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": rd.launches_per_step() * steps,
+        "clocks": clk.summary(),
+        "tree_rows": rd.N,
+    }
+    if extras and rank == 0:
+        res["heads_all_rows"] = heads_all_rows(rd, stream, bf16)
+        res["kv_compact_layers"] = compact_all_layers(rd, graphs.native, stream, flush)
+        res["accept_hidden"] = accept_hidden(rd, graphs.native, stream, flush, hbm)
+    del graphs, rd
+    torch.cuda.synchronize(dev)
+    torch.cuda.empty_cache()
+    return res
+
+
+# workloads whose tree attention is bound by the tensor cores (wide trees: arithmetic
+# intensity above the ridge) rather than by the prefix K/V stream
+ATTN_TENSOR_BOUND = ("llama3-8b-256", "longctx-341")
+
+HEADLINE = "longctx-341"
 
 
 # ----------------------------------------------------------------------------- main
@@ -565,12 +801,17 @@ def config_of(w: synth.Workload, rd):
 def main():
     ap = argparse.ArgumentParser()
     ap.add_argument("--gpus", type=int, default=1)
-    ap.add_argument("--steps", type=int, default=2000)
+    ap.add_argument("--steps", type=int, default=200)
     ap.add_argument("--warmup", type=int, default=10)
-    ap.add_argument("--workload", default="vicuna7b-64", choices=synth.WORKLOAD_ORDER)
+    ap.add_argument("--workload", default=HEADLINE, choices=synth.WORKLOAD_ORDER)
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-per-workload", action="store_true", help="measure the headline workload only")
+    ap.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
+    ap.add_argument("--oracle-v-rows", type=int, default=BASELINE_V_ROWS, help=argparse.SUPPRESS)
     args = ap.parse_args()
+    if args.oracle_sample:
+        return run_oracle_sample(args)
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         return run_reference(args)
@@ -583,75 +824,48 @@ def main():
     import medusa_speculative_tree_gb300 as m
 
     w = synth.WORKLOADS[args.workload]
-    rd = Round(m, w, dev)
-    stream = torch.cuda.current_stream(dev)
     flush_buf = torch.empty(512 * 1024 * 1024 // 4, dtype=torch.float32, device=dev)
     flush = lambda: flush_buf.fill_(1.0)
 
-    for _ in range(args.warmup):
-        rd.step()
-    graphs = RoundGraphs(rd, dev)
-    for _ in range(args.warmup):
-        graphs.step()
-    torch.cuda.synchronize(dev)
-    barrier(ws)
-    torch.cuda.synchronize(dev)
-    with ClockSampler(local) as clk:
-        ms = time_loop(graphs.step, args.steps, stream)
-        torch.cuda.synchronize(dev)
-    barrier(ws)
-    ms_step = max_over_ranks(ms / args.steps, ws, dev)
-    us_round = 1e3 * ms_step / ws                      # whole job: ws rounds per step
-
-    stages = graphs.stage_times(20, stream, flush)
-    hbm, bf16, src = peaks()
-    attn_us = stages["attn"]
-    round_b = rd.round_bytes(graphs.native.accept_len)
-    round_gbs = round_b / (ms_step * 1e-3) / 1e9      # one round per GPU per step
-    attn_gbs = rd.attn_bytes() / (attn_us * 1e-6) / 1e9
-    # the dominant kernel: heads launches back to back (the head weights exceed L2, so
-    # every launch streams them from HBM), events on the replay stream
-    heads_us = 1e3 * time_loop(graphs.stage["heads"].replay, 20, stream) / 20
-    heads_gbs = rd.head_bytes() / (heads_us * 1e-6) / 1e9
-    e2e_ms, h2d, d2h = e2e_loop(rd, max(10, args.steps // 4), stream)
-    e2e_ms = max_over_ranks(e2e_ms, ws, dev)
-    all_rows = heads_all_rows(rd, stream, bf16) if rank == 0 else None
-    layers = compact_all_layers(rd, graphs.native, stream, flush) if rank == 0 else None
-    acc_h = accept_hidden(rd, graphs.native, stream, flush, hbm) if rank == 0 else None
+    head = measure(m, w, dev, args.steps, args.warmup, flush, ws, local, rank, extras=True)
+    per = {}
+    if not args.no_per_workload:
+        for name in synth.WORKLOAD_ORDER:
+            if name == w.name:
+                continue
+            r = measure(m, synth.WORKLOADS[name], dev, max(args.steps, 20), args.warmup, flush, ws, local, rank,
+                        extras=True)
+            per[name] = r
 
     cpu = None
     if rank == 0 and ws == 1 and not args.no_cpu_baseline:
-        s, cores, desc = oracle_round_seconds(w, 1)
-        cpu = {"value": 1e6 * s, "unit": UNIT, "cores": cores, "kind": "oracle", "sample": desc}
+        cpu = cpu_baseline_of(w, BASELINE_V_ROWS, one_thread=True)
+        for name, r in per.items():
+            st, desc = oracle_stages(synth.WORKLOADS[name], BASELINE_V_ROWS)
+            r["cpu_baseline"] = {"value": sum(st.values()), "unit": UNIT, "cores": os.cpu_count(),
+                                 "kind": "oracle", "sample": desc, "stages_us": st}
 
     if rank == 0:
         line = {
-            "metric": METRIC, "value": us_round, "unit": UNIT, "n_gpus": ws, "steps": args.steps,
-            "warmup": args.warmup, "ms_per_step": ms_step, "higher_is_better": False, "scaling": "weak",
-            "vs_baseline": None, "dtype": w.dtype, "data": "synthetic (seeded generators, random-init weights)",
-            "config": config_of(w, rd),
-            "nodes_per_s": ws * w.batch * rd.N / (ms_step * 1e-3),
-            "tree_attn": {"us": attn_us, "hbm_gbs": attn_gbs, "frac_of_hbm_peak": attn_gbs / hbm,
-                          "tflops": rd.attn_flops() / (attn_us * 1e-6) / 1e12},
-            "stages_us": stages,
-            "roofline": {"kernel": "medusa_heads_topk (head-weight stream with top-k)",
-                         "bound": "hbm", "achieved": heads_gbs, "peak": hbm, "unit": "GB/s",
-                         "frac": heads_gbs / hbm, "traffic": HEADS_TRAFFIC.get(w.name), "peak_source": src,
-                         "algorithmic_bytes": rd.head_bytes(), "launch_us": heads_us},
-            "heads_all_rows": all_rows,
-            "kv_compact_layers": layers,
-            "accept_hidden": acc_h,
-            "round_roofline": {"bound": "hbm", "achieved": round_gbs, "peak": hbm, "unit": "GB/s",
-                               "frac": round_gbs / hbm, "peak_source": src, "algorithmic_bytes": round_b,
-                               "note": "all five steps' algorithmic bytes over one round's device time"},
-            "tree_attn_roofline": {"kernel": "medusa_tree_attn_verify", "bound": "hbm", "achieved": attn_gbs,
-                                   "peak": hbm, "unit": "GB/s", "frac": attn_gbs / hbm,
-                                   "traffic": ATTN_TRAFFIC.get(w.name),
-                                   "peak_source": src, "algorithmic_bytes": rd.attn_bytes()},
+            "metric": METRIC, "value": head["value"], "unit": UNIT, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": head["ms_per_step"], "higher_is_better": False,
+            "scaling": "weak", "vs_baseline": None, "dtype": w.dtype,
+            "data": "synthetic (seeded generators, random-init weights)",
+            "config": config_of(w, None),
+            "nodes_per_s": head["nodes_per_s"],
+            "tree_attn": head["tree_attn"],
+            "stages_us": head["stages_us"],
+            "roofline": head["roofline"],
+            "heads_all_rows": head.get("heads_all_rows"),
+            "kv_compact_layers": head.get("kv_compact_layers"),
+            "accept_hidden": head.get("accept_hidden"),
+            "round_roofline": head["round_roofline"],
+            "tree_attn_roofline": head["tree_attn_roofline"],
             "cpu_baseline": cpu,
-            "e2e": {"value": 1e3 * e2e_ms / ws, "unit": UNIT, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
-            "gpu_launches": rd.launches_per_step() * args.steps,
-            "clocks": clk.summary(),
+            "e2e": head["e2e"],
+            "gpu_launches": head["gpu_launches"],
+            "clocks": head["clocks"],
+            "per_workload": per,
         }
         print(json.dumps(line))
     if ws > 1:

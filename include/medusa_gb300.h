@@ -63,9 +63,9 @@ typedef int32_t medusa_status;
 #define MEDUSA_EPATH        -7   /* per-sequence: accepted path is not a valid tree chain */
 #define MEDUSA_ETIMEOUT     -8   /* per-sequence: a bounded device wait gave up; the sequence's
                                     outputs are invalid and the workspace must be re-zeroed */
-#define MEDUSA_ERANGE       -9   /* per-sequence: an input outside the range of the kernel's
-                                    arithmetic (bf16 attention: a K/V value with |x| >= 65536 or a
-                                    scaled rotated query beyond fp16); the outputs are invalid */
+#define MEDUSA_ERANGE       -9   /* per-sequence: an output that is not finite, from an input
+                                    outside the range of the kernel's arithmetic (bf16 attention:
+                                    fp16 operands, |x| > 65504); the outputs are invalid */
 
 typedef int32_t medusa_dtype;
 #define MEDUSA_F32  0
@@ -228,9 +228,11 @@ size_t medusa_tree_attn_workspace(const medusa_tree_t *t, int32_t B, int32_t n_q
  *   would add ~1.6e-3 relative rounding error); lse [B][N][n_q_heads] fp32
  *   natural-log log-sum-exp, or NULL; status [B]: 0, or MEDUSA_ECAPACITY when
  *   L[b] + N > capacity (sequence b is not touched), MEDUSA_ETIMEOUT when a bounded
- *   wait gave up, MEDUSA_ERANGE (bf16 tensor-core path) when a K/V value or a
- *   scaled rotated query lies outside fp16's range (|x| > 65504), so that the output
- *   of b may hold inf or NaN.
+ *   wait gave up, MEDUSA_ERANGE (bf16 tensor-core path) when an output of b is not
+ *   finite: a K/V value or a scaled rotated query outside fp16's range (|x| > 65504)
+ *   becomes inf, which makes the softmax of every row whose score of that key is +inf
+ *   (or whose value row or query is inf) NaN.  A key that overflows only to scores of
+ *   -inf drops out of those rows' softmax without a report.
  *   ws: workspace of medusa_tree_attn_workspace(...) bytes (16-byte aligned),
  *   zero-filled once before its first use.  Its first 256 KiB hold split-KV ticket
  *   counters that every call returns to zero, so one workspace can serve later

@@ -167,37 +167,24 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, con
   }
 }
 
-// True when either fp16 of a packed pair is infinite or NaN (exponent field all ones):
-// the value was outside fp16's range (|x| > 65504) or not finite to begin with.
-__device__ __forceinline__ bool f16x2_nonfinite(uint32_t w) {
-  const uint32_t e = w & 0x7C007C00u;
-  return (e & 0xFFFFu) == 0x7C00u || (e >> 16) == 0x7C00u;
-}
-__device__ __forceinline__ bool f16x8_nonfinite(const uint4& v) {
-  return f16x2_nonfinite(v.x) | f16x2_nonfinite(v.y) | f16x2_nonfinite(v.z) | f16x2_nonfinite(v.w);
-}
+
 
 // Re-encode one K or V tile (2 blocks of [KT rows x 128 B], bf16) to fp16 in place;
 // rows of keys >= k_valid become zero.  Thread ct of the kConvThreads converter
 // threads; all its loads are issued before the first store, so their latencies overlap.
-// Returns true when a converted value is not finite in fp16.
 template <int kConvThreads, int KT>
-__device__ __forceinline__ bool convert_tile(uint8_t* tile, int k_valid, int ct) {
+__device__ __forceinline__ void convert_tile(uint8_t* tile, int k_valid, int ct) {
   uint4* p = reinterpret_cast<uint4*>(tile);
   constexpr int kIter = (KT * kDH * 2 / 16) / kConvThreads;
   uint4 v[kIter];
-  bool bad = false;
 #pragma unroll
   for (int i = 0; i < kIter; ++i) v[i] = p[i * kConvThreads + ct];
 #pragma unroll
   for (int i = 0; i < kIter; ++i) {
     const int idx = i * kConvThreads + ct;
     const int row = (idx % (KT * 8)) / 8;             // 16-byte chunks: 8 per row, 8 KT per block
-    const uint4 o = row < k_valid ? bf16x8_to_f16x8(v[i]) : make_uint4(0, 0, 0, 0);
-    bad |= f16x8_nonfinite(o);
-    p[idx] = o;
+    p[idx] = row < k_valid ? bf16x8_to_f16x8(v[i]) : make_uint4(0, 0, 0, 0);
   }
-  return bad;
 }
 
 // Tree-row key tile of KT rows: bf16 -> RoPE at L + depth[v] (fp32) -> fp16, in place.
@@ -208,10 +195,9 @@ template <int kConvThreads>
 __device__ __forceinline__ int rotate_row(int i, int ct) { return (i * kConvThreads + ct) >> 3; }
 
 template <int kConvThreads, int KT>
-__device__ __forceinline__ bool convert_rotate_tile(uint8_t* tile, int n_valid, const int* dep,
+__device__ __forceinline__ void convert_rotate_tile(uint8_t* tile, int n_valid, const int* dep,
                                                     const float* tab_c, const float* tab_s, int ct) {
   constexpr int kRotIter = (KT * 8) / kConvThreads;
-  bool bad = false;
 #pragma unroll
   for (int i = 0; i < kRotIter; ++i) {
     const int idx = i * kConvThreads + ct;
@@ -231,19 +217,15 @@ __device__ __forceinline__ bool convert_rotate_tile(uint8_t* tile, int n_valid, 
         y1[e] = x1[e] * cs - x2[e] * sn;
         y2[e] = x2[e] * cs + x1[e] * sn;
       }
-      const uint4 o0 = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]), pack_half2(y1[4], y1[5]),
-                                  pack_half2(y1[6], y1[7]));
-      const uint4 o1 = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]), pack_half2(y2[4], y2[5]),
-                                  pack_half2(y2[6], y2[7]));
-      bad |= f16x8_nonfinite(o0) | f16x8_nonfinite(o1);
-      *p0 = o0;
-      *p1 = o1;
+      *p0 = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]), pack_half2(y1[4], y1[5]),
+                       pack_half2(y1[6], y1[7]));
+      *p1 = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]), pack_half2(y2[4], y2[5]),
+                       pack_half2(y2[6], y2[7]));
     } else {
       *p0 = make_uint4(0, 0, 0, 0);
       *p1 = make_uint4(0, 0, 0, 0);
     }
   }
-  return bad;
 }
 
 // Kernel configuration: QT query tiles of 128 rows per CTA share every K/V tile (one
@@ -311,7 +293,6 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
       (reinterpret_cast<uintptr_t>(tab_s + (D + 1) * kHalf) + 7) & ~uintptr_t(7));
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
-  __shared__ int range_flag;       // an fp16 operand was not finite (value outside fp16's range)
 
   const int ct_idx = blockIdx.x, s = blockIdx.y;     // ct_idx: which QT row tiles
   // Units of longer sequences start first (longest-processing-time order, which packs
@@ -445,7 +426,6 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
   int n_issued_k = -1;             // on an abort between the K and V copies of a tile: K's count
   if (tid == C::kProdWarp * 32) {
     abort_flag = 0;
-    range_flag = 0;
     for (int st = 0; st < NS; ++st) {
       mbar_init(BAR(C::kBarFullK + st), 1);
       mbar_init(BAR(C::kBarFullV + st), 1);
@@ -523,7 +503,6 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
   }
   if (!__all_sync(0xffffffffu, wait_or_abort(BAR(C::kBarQFull), 0, abortp))) ok = false;
   if (ok) {
-    bool bad = false;
     for (int it = tid; it < rows_valid * 8; it += C::kThreads) {
       const int r = it >> 3, c = it & 7;
       const int tr = r & (kTcRows - 1);
@@ -539,15 +518,11 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
         y1[e] = (x1[e] * cs - x2[e] * sn) * a.scale_log2;
         y2[e] = (x2[e] * cs + x1[e] * sn) * a.scale_log2;
       }
-      const uint4 o0 = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]), pack_half2(y1[4], y1[5]),
-                                  pack_half2(y1[6], y1[7]));
-      const uint4 o1 = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]), pack_half2(y2[4], y2[5]),
-                                  pack_half2(y2[6], y2[7]));
-      bad |= f16x8_nonfinite(o0) | f16x8_nonfinite(o1);
-      *q0 = o0;
-      *q1 = o1;
+      *q0 = make_uint4(pack_half2(y1[0], y1[1]), pack_half2(y1[2], y1[3]), pack_half2(y1[4], y1[5]),
+                       pack_half2(y1[6], y1[7]));
+      *q1 = make_uint4(pack_half2(y2[0], y2[1]), pack_half2(y2[2], y2[3]), pack_half2(y2[4], y2[5]),
+                       pack_half2(y2[6], y2[7]));
     }
-    if (bad) range_flag = 1;
   }
   fence_proxy_async();
   __syncwarp();
@@ -724,16 +699,15 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
         ok = false;
         break;
       }
-      const bool bad_k = j >= n_pre ? convert_rotate_tile<C::kConvThreads, KT>(tK, k_valid, dep, tab_c, tab_s, ct)
-                                    : convert_tile<C::kConvThreads, KT>(tK, k_valid, ct);
-      if (bad_k) range_flag = 1;
+      if (j >= n_pre) convert_rotate_tile<C::kConvThreads, KT>(tK, k_valid, dep, tab_c, tab_s, ct);
+      else convert_tile<C::kConvThreads, KT>(tK, k_valid, ct);
       fence_proxy_async();
       mbar_arrive(BAR(C::kBarConvK + st));
       if (!wait_or_abort(BAR(C::kBarFullV + st), (j / NS) & 1, abortp)) {
         ok = false;
         break;
       }
-      if (convert_tile<C::kConvThreads, KT>(tV, k_valid, ct)) range_flag = 1;
+      convert_tile<C::kConvThreads, KT>(tV, k_valid, ct);
       fence_proxy_async();
       mbar_arrive(BAR(C::kBarConvV + st));
     }
@@ -968,9 +942,6 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
   }
   __syncthreads();
   const bool failed = *abortp != 0;
-  // An operand outside fp16's range made the sequence's result invalid (it may hold
-  // inf or NaN): report it, unless the CTA gave up anyway.
-  if (tid == 0 && !failed && range_flag) atomicExch(&a.status[b], MEDUSA_ERANGE);
   if (failed) {
     // Drain (bounded) what this CTA may still have in flight before its shared memory
     // and TMEM are reused or released: the query copies, the last copy into each stage,
@@ -1070,9 +1041,14 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
       const int Rr = row0 + r;
       const int ur = Rr / g, hr = kvh * g + Rr % g;
       if (!failed) {
-        reinterpret_cast<float4*>(a.out + (((int64_t)b * N + ur) * a.Hq + hr) * kDH)[lane] =
-            make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
+        const float4 o = make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
+        reinterpret_cast<float4*>(a.out + (((int64_t)b * N + ur) * a.Hq + hr) * kDH)[lane] = o;
         if (a.lse && lane == 0) a.lse[((int64_t)b * N + ur) * a.Hq + hr] = (Mx + log2f(l)) * kLn2;
+        // An fp16 operand that overflowed (|x| > 65504 in K, V or a scaled rotated query)
+        // becomes inf, and a score of +inf, a value of inf or a query of inf turns the
+        // row's softmax into NaN: an output that is not finite reports MEDUSA_ERANGE.
+        const bool fin = isfinite(o.x) && isfinite(o.y) && isfinite(o.z) && isfinite(o.w);
+        if (__any_sync(0xffffffffu, !fin) && lane == 0) atomicExch(&a.status[b], MEDUSA_ERANGE);
       }
     }
   }

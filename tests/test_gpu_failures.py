@@ -10,8 +10,9 @@ call returns, what it reports, that nothing of the sequence was written, and tha
 next call without the hook is correct again.
 
 Range.  The bf16 tensor-core attention multiplies in fp16; a K/V value or a scaled
-rotated query outside fp16's range becomes inf.  The kernel must then report
-MEDUSA_ERANGE for that sequence instead of returning inf/NaN with status 0.
+rotated query outside fp16's range becomes inf, which turns the softmax of the rows
+that see it into NaN.  The kernel must then report MEDUSA_ERANGE for that sequence
+instead of returning inf/NaN with status 0.
 """
 import numpy as np
 import pytest
@@ -134,7 +135,7 @@ def test_attention_reports_fp16_range(m, where):
     elif where == "prefix_v":
         V[bad, 1, 200, 64] = 7e4
     elif where == "tree_k":
-        k[bad, 3, 0, 9] = 2e5
+        k[bad, 0, 0, 9] = 2e5                 # the root's key: every row sees it
     elif where == "tree_v":
         v[bad, 5, 2, 100] = -7e4
     else:
