@@ -101,3 +101,28 @@ def typical_ambiguous(o, rel: float = 1e-5) -> bool:
     if len(sc) >= 2 and sc[0] != sc[1] and sc[0] - sc[1] < rel * max(1.0, abs(sc[0])):
         return True
     return False
+
+
+def oracle_heads_blocked(h, w1, w2, w_lm, topk: int, block: int = 4096):
+    """The oracle's medusa_heads on device-resident weights, with the vocabulary rows of
+    W2 and W_LM brought to the host in blocks: the fp64 copies of the larger workloads'
+    weights (up to 44 GB) do not fit in host memory at once.  The same oracle functions
+    run on slices of their inputs (residual on all of W1; head_logits on each block of
+    W2, and on each block of W_LM as a one-head shared projection); ranked_ids then
+    selects root and pools from the assembled fp64 logits, as medusa_heads does.
+    Returns (root [T], pool [T, K, topk], logits [T, K + 1, V] fp64)."""
+    from oracle import heads as oheads
+    h64 = to64(h)
+    z = oheads.residual(h64, to64(w1))
+    T, K, V = h64.shape[0], w1.shape[0], w_lm.shape[0]
+    logits = np.empty((T, K + 1, V))
+    for v0 in range(0, V, block):
+        v1 = min(V, v0 + block)
+        logits[:, 1:, v0:v1] = oheads.head_logits(z, to64(w2[:, v0:v1]))
+        logits[:, 0, v0:v1] = oheads.head_logits(h64[:, None, :], to64(w_lm[v0:v1]))[:, 0]
+    root = np.array([oheads.ranked_ids(logits[t, 0], 1)[0] for t in range(T)], dtype=np.int64)
+    pool = np.zeros((T, K, topk), dtype=np.int64)
+    for t in range(T):
+        for k in range(K):
+            pool[t, k] = oheads.ranked_ids(logits[t, 1 + k], topk)
+    return root, pool, logits

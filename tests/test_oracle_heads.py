@@ -83,3 +83,21 @@ def test_head_logit_rows_matches_full():
     rows = [(0, 3), (1, 7), (2, 39), (2, 0)]
     got = heads.head_logit_rows(h[0], lambda k: w1[k], lambda k, v: w2[k, v], lambda v: w_lm[v], rows)
     np.testing.assert_allclose(got, [full[0, m, v] for m, v in rows], rtol=1e-12)
+
+
+def test_blocked_heads_helper_equals_medusa_heads():
+    """The parity tests' blocked evaluation of the heads (vocabulary rows in blocks) is the
+    oracle's medusa_heads: same root, pools and logits on a tiny case with a ragged
+    last block."""
+    import torch
+    from tests import gpu_util as gu
+    rng = np.random.default_rng(3)
+    T, K, d, V, topk = 3, 2, 16, 37, 4
+    h = torch.tensor(rng.normal(size=(T, d)))
+    w1 = torch.tensor(rng.normal(size=(K, d, d)) * 0.1)
+    w2 = torch.tensor(rng.normal(size=(K, V, d)))
+    w_lm = torch.tensor(rng.normal(size=(V, d)))
+    r1, p1, l1 = heads.medusa_heads(h.numpy(), w1.numpy(), w2.numpy(), w_lm.numpy(), topk)
+    r2, p2, l2 = gu.oracle_heads_blocked(h, w1, w2, w_lm, topk, block=10)
+    assert (r1 == r2).all() and (p1 == p2).all()
+    assert np.allclose(l1, l2, rtol=1e-13, atol=1e-12)
