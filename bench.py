@@ -278,10 +278,10 @@ ATTN_TRAFFIC = {"vicuna7b-64": 35_210_752 + 0}
 def heads_all_rows(rd, stream, peak_tflops):
     """medusa_heads_topk with every tree row as a hidden row (T = B N), the variant in which
     the heads are a tensor-core contraction.  `frac` is the method's useful rate, 2 T
-    flops per weight element, over the bf16 peak.  bf16 with T >= 2 runs on the tensor
-    cores with each input row of W2 (z, an fp32 value) as a bf16 pair (hi, lo), so the
-    MMAs execute twice the useful flops on W2; the rows of W1 and W_LM (h, exactly bf16)
-    are single.  The executed rate is reported beside the useful one."""
+    flops per weight element, over the bf16 peak.  bf16 with 2 <= T <= 128 runs on the
+    tensor cores with every input row as a bf16 pair (hi, lo), so the MMAs execute twice
+    the useful flops; more rows run wide passes of up to 256 single rows (z in fp16),
+    which execute the useful flops.  The executed rate is reported beside the useful one."""
     w = rd.w
     T = w.batch * rd.N                                  # every tree row of every sequence
     h = synth.normal((T, w.hidden), 1.0, w.seed, "h", rd.dev, w.torch_dtype, sub=1)
@@ -294,9 +294,9 @@ def heads_all_rows(rd, stream, peak_tflops):
     elems = rd.w1.numel() + rd.w2.numel() + rd.w_lm.numel()
     useful = 2.0 * T * elems / (us * 1e-6) / 1e12
     mma = w.dtype == "bf16" and T >= 2
-    executed = 2.0 * T * (rd.w1.numel() + 2 * rd.w2.numel() + rd.w_lm.numel()) / (us * 1e-6) / 1e12 if mma \
-        else useful
-    passes = math.ceil(T / 128) if mma else 1
+    wide = mma and T > 128
+    executed = useful * (2 if mma and not wide else 1)
+    passes = (math.ceil(T / 256) if wide else math.ceil(T / 128)) if mma else 1
     return {"T": T, "us": us, "useful_tflops": useful, "executed_tflops": executed,
             "peak_tflops": peak_tflops, "frac": useful / peak_tflops, "executed_frac": executed / peak_tflops,
             "weight_passes": passes, "hbm_gbs": passes * rd.head_bytes() / (us * 1e-6) / 1e9}

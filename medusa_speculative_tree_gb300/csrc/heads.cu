@@ -600,12 +600,15 @@ HeadsPlan plan_heads(int T, int d, int V, int K, int topk) {
   off = align_up(off + (size_t)T * (K + 1) * V * sizeof(float), 256);
   p.off_scand = off;                                       // weight-stream path: per-CTA lists
   off = align_up(off + (size_t)(K + 1) * kHeadsStreamMaxGrid * topk * sizeof(Cand), 256);
-  // tensor-core path: input rows of one pass (at most kHeadsMmaMaxRows) as bf16 pairs
-  const int Tp = T < kHeadsMmaMaxRows ? T : kHeadsMmaMaxRows;
+  // tensor-core path: input rows of one pass (bf16 pairs of at most kHeadsMmaMaxRows
+  // rows, or wide: single rows, at most kHeadsMmaWideRows)
+  const bool wide = heads_mma_wide(T);
+  const int per_pass = wide ? kHeadsMmaWideRows : kHeadsMmaMaxRows;
+  const int Tp = T < per_pass ? T : per_pass;
   p.off_hhl = off;
-  off = align_up(off + (T >= 2 ? heads_mma_rows(Tp) * d * 2 : 0), 256);
+  off = align_up(off + (T >= 2 ? heads_mma_rows(Tp, wide) * d * 2 : 0), 256);
   p.off_zhl = off;
-  off = align_up(off + (T >= 2 ? (size_t)K * heads_mma_rows(Tp) * d * 2 : 0), 256);
+  off = align_up(off + (T >= 2 ? (size_t)K * heads_mma_rows(Tp, wide) * d * 2 : 0), 256);
   p.off_cand = off;                                        // top-k: per-span sorted lists
   off = align_up(off + (size_t)T * (K + 1) * kTopkMaxSpans * topk * sizeof(Cand), 256);
   p.off_err = off;                                         // error flag and counters, then tickets
@@ -634,15 +637,18 @@ cudaError_t launch_heads(const HeadsPlan& p, const void* h, const void* w1, cons
   if (e != cudaSuccess) return e;
   if (heads_mma_supported(T, d, V, K, dt, h, w1, w2, w2_stride, w_lm)) {
     // several bf16 hidden rows: tensor-core weight stream (passes of at most
-    // kHeadsMmaMaxRows rows, each reading the weights once), then top-k on the logits
-    for (int t0 = 0; t0 < T; t0 += kHeadsMmaMaxRows) {
+    // kHeadsMmaMaxRows rows as pairs, or kHeadsMmaWideRows wide, each reading the weights
+    // once), then top-k on the logits
+    const bool wide = heads_mma_wide(T);
+    const int per_pass = wide ? kHeadsMmaWideRows : kHeadsMmaMaxRows;
+    for (int t0 = 0; t0 < T; t0 += per_pass) {
       HeadsPlan pp = p;
-      pp.T = (T - t0) < kHeadsMmaMaxRows ? (T - t0) : kHeadsMmaMaxRows;
+      pp.T = (T - t0) < per_pass ? (T - t0) : per_pass;
       if (t0 > 0) {                // the pass's work counters start at zero; the error flag stays
         e = cudaMemsetAsync(err + 4, 0, kHeadsCounterBytes - 4 * sizeof(int), st);
         if (e != cudaSuccess) return e;
       }
-      e = launch_heads_mma(pp, (const uint16_t*)h + (size_t)t0 * d, w1, b1, w2, w2_stride, w_lm,
+      e = launch_heads_mma(pp, wide, (const uint16_t*)h + (size_t)t0 * d, w1, b1, w2, w2_stride, w_lm,
                            logits + (size_t)t0 * (K + 1) * V, ws, st);
       if (e != cudaSuccess) return e;
     }

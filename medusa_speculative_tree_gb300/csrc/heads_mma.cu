@@ -9,6 +9,13 @@
 // 2t holds bf16(x_t), row 2t + 1 holds bf16(x_t - bf16(x_t)), so the sum of the two
 // columns carries x_t to ~2^-16 relative (h itself is bf16: its second part is 0).
 //
+// Passes of more than 128 rows (up to 256: the all-rows variant) would need 512 input
+// columns as pairs, more than one MMA takes.  They run "wide" instead: the input rows are
+// single (h is exactly bf16; z is stored as fp16, ~2^-11 relative) and the W2 tiles are
+// re-encoded in shared memory from bf16 to fp16 (exact for |w| in [2^-14, 65504]) by
+// four converter warps, so that W2 z is one fp16 MMA; W1 h and W_LM h stay bf16 MMAs.
+// A pass then reads the weights once for twice as many rows.
+//
 // One persistent CTA per SM (cooperative launch) takes 128-row groups from a global
 // counter in stream order: W1_0..W1_{K-1}, the first half of W_LM, W2_0..W2_{K-1}, the
 // rest of W_LM.
@@ -23,6 +30,8 @@
 //     row writes its T logits.  Top-k then runs on the logits.
 // All waits are bounded; on a timeout the call records an error (the top-k merge then
 // writes -1).
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 #include "tc.cuh"
@@ -32,15 +41,18 @@ namespace medusa {
 namespace {
 
 constexpr int kMThreads = 6 * 32;
+constexpr int kMConvWarp0 = 6;               // wide passes: converter warps 6-9
+constexpr int kMConvWarps = 4;
+constexpr int kMThreadsWide = (6 + kMConvWarps) * 32;
 constexpr int kMRows = 128;                  // rows of W per group (MMA M)
 constexpr int kMKc = 64;                     // K columns per stage (one 128-byte swizzle row)
 
 struct MmaArgs {
   const uint16_t* h;          // [T][d] bf16
   const uint16_t* b1;         // [K][d] or null
-  int d, V, K, T, N;          // N = input rows of the MMA (2T rounded up to 32)
+  int d, V, K, T, N;          // N = input rows of the MMA (2T, or T when wide, rounded up to 32)
   int w2_shared;              // W2 heads share one matrix
-  uint16_t* z_hl;             // [K][N][d] bf16 pairs of z
+  uint16_t* z_hl;             // [K][N][d] bf16 pairs of z, or (wide) fp16 z
   float* logits;              // [T][K + 1][V]
   int* err;
   int* cnt;                   // [0] W1 row quarters written (4 per group), [1] next group to hand out
@@ -87,7 +99,23 @@ __device__ __forceinline__ bool m_wait(uint32_t bar, uint32_t parity, const vola
   }
 }
 
-__global__ void __launch_bounds__(kMThreads, 1)
+// bf16 x8 (uint4) -> fp16 x8, exact for magnitudes in [2^-14, 65504].
+__device__ __forceinline__ uint32_t f16x2_of(float a, float b) {
+  uint32_t r;
+  asm("cvt.rn.f16x2.f32 %0, %1, %2;" : "=r"(r) : "f"(b), "f"(a));
+  return r;
+}
+__device__ __forceinline__ uint4 bf16x8_to_f16x8_m(uint4 v) {
+  uint4 o;
+  o.x = f16x2_of(__uint_as_float(v.x << 16), __uint_as_float(v.x & 0xFFFF0000u));
+  o.y = f16x2_of(__uint_as_float(v.y << 16), __uint_as_float(v.y & 0xFFFF0000u));
+  o.z = f16x2_of(__uint_as_float(v.z << 16), __uint_as_float(v.z & 0xFFFF0000u));
+  o.w = f16x2_of(__uint_as_float(v.w << 16), __uint_as_float(v.w & 0xFFFF0000u));
+  return o;
+}
+
+template <bool WIDE>
+__global__ void __launch_bounds__(WIDE ? kMThreadsWide : kMThreads, 1)
     heads_mma_kernel(const __grid_constant__ CUtensorMap tmW1, const __grid_constant__ CUtensorMap tmLM,
                      const __grid_constant__ CUtensorMap tmW2, const __grid_constant__ CUtensorMap tmH,
                      const __grid_constant__ CUtensorMap tmZ, const MmaArgs a) {
@@ -102,6 +130,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
   const uint32_t full0 = smem_u32(&bars[0]), empty0 = smem_u32(&bars[S]);
   const uint32_t dfull0 = smem_u32(&bars[2 * S]), dempty0 = smem_u32(&bars[2 * S + 2]);
   const uint32_t drain = smem_u32(&bars[2 * S + 4]);
+  const uint32_t conv0 = smem_u32(&bars[2 * S + 5]);            // wide: [S] stage converted
   const volatile int* abortp = &abort_flag;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   MLayout L;
@@ -126,6 +155,8 @@ __global__ void __launch_bounds__(kMThreads, 1)
       mbar_init(dempty0 + 8 * p, 4);                 // the four epilogue warps
     }
     mbar_init(drain, 1);
+    if (WIDE)
+      for (int s = 0; s < S; ++s) mbar_init(conv0 + 8 * s, kMConvWarps);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
   }
   if (warp == 1) {
@@ -206,13 +237,16 @@ __global__ void __launch_bounds__(kMThreads, 1)
   } else if (warp == 1) {
     // ---- MMA issue: one group = n_k stages into accumulator g & 1 ------------------------
     if (lane == 0) {
-      const uint32_t idesc = idesc_bf16(kMRows, N);
+      const uint32_t idesc_b = idesc_bf16(kMRows, N);
+      const uint32_t idesc_h = idesc_f16(kMRows, N, false);
+      uint32_t idesc = idesc_b;
       int u = 0;
       for (int g = 0; ok; ++g) {
         const int db = g & 1;
         for (int kc = 0; kc < n_k; ++kc, ++u) {
           const int s = u % S;
-          if (!m_wait(full0 + 8 * s, (uint32_t)((u / S) & 1), abortp)) { ok = false; break; }
+          // (wide: the converter warps pass every stage on, W2 stages re-encoded to fp16)
+          if (!m_wait((WIDE ? conv0 : full0) + 8 * s, (uint32_t)((u / S) & 1), abortp)) { ok = false; break; }
           if (kc == 0) {
             const int idx = stage_item[s];
             // the accumulator must have been read out (group g - 2) before it is reused
@@ -225,6 +259,7 @@ __global__ void __launch_bounds__(kMThreads, 1)
             }
             dgrp[db] = idx;
             __threadfence_block();
+            idesc = (WIDE && mmap_item(idx, L).kind == 2) ? idesc_h : idesc_b;
           }
           tc_fence_after();
           const uint32_t sA = smem_u32(sm + (size_t)s * a.stage_bytes), sB = sA + bps * a_bytes;
@@ -241,6 +276,24 @@ __global__ void __launch_bounds__(kMThreads, 1)
       }
       if (!ok) give_up();
     }
+  } else if (WIDE && warp >= kMConvWarp0) {
+    // ---- wide: W2 tiles bf16 -> fp16 in place; every stage is passed on -----------------
+    const int ct = threadIdx.x - kMConvWarp0 * 32;
+    for (int u = 0;; ++u) {
+      const int s = u % S;
+      if (!__all_sync(0xffffffffu, m_wait(full0 + 8 * s, (uint32_t)((u / S) & 1), abortp))) { ok = false; break; }
+      const int idx = *reinterpret_cast<volatile int*>(&stage_item[s]);
+      if (idx >= 0 && mmap_item(idx, L).kind == 2) {
+        uint4* p = reinterpret_cast<uint4*>(sm + (size_t)s * a.stage_bytes);
+        const int n4 = bps * (int)(a_bytes / 16);
+        for (int i = ct; i < n4; i += kMConvWarps * 32) p[i] = bf16x8_to_f16x8_m(p[i]);
+        fence_proxy_async();                         // the MMA reads these through the async proxy
+      }
+      __syncwarp();
+      if (lane == 0) mbar_arrive(conv0 + 8 * s);
+      if (idx < 0) break;                            // the end marker: no more stages
+    }
+    if (!ok && lane == 0) give_up();
   } else {
     // ---- epilogue: thread = output row ---------------------------------------------------
     const int q = warp & 3;                            // TMEM lane quadrant of this warp
@@ -257,7 +310,28 @@ __global__ void __launch_bounds__(kMThreads, 1)
       for (int c0 = 0; c0 < N; c0 += 32) {
         float v[32];
         tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(db * N + c0), v);
-        if (row < n_rows) {
+        if (WIDE && row < n_rows) {
+          // single input columns: column t is row t
+          bool bad = false;
+#pragma unroll
+          for (int j = 0; j < 32; ++j) {
+            const int t = c0 + j;
+            if (t >= T) break;
+            const float x = v[j];
+            if (it.kind == 0) {
+              float zv = x;
+              if (a.b1) zv += Elem<uint16_t>::load(a.b1, (int64_t)it.k * d + row);
+              const float z = Elem<uint16_t>::load(a.h, (int64_t)t * d + row) + zv / (1.f + expf(-zv));
+              const __half zh = __float2half_rn(z);
+              bad |= !(fabsf(z) <= 65504.f);           // z outside fp16's range (or not finite)
+              a.z_hl[((int64_t)it.k * N + t) * d + row] = __half_as_ushort(zh);
+            } else {
+              const int m = it.kind == 1 ? 0 : 1 + it.k;
+              a.logits[((int64_t)t * (K + 1) + m) * V + row] = x;
+            }
+          }
+          if (bad) atomicExch(a.err, 1);
+        } else if (row < n_rows) {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
             const int t = c0 / 2 + j;
@@ -311,26 +385,36 @@ __global__ void __launch_bounds__(kMThreads, 1)
 }
 
 // Input rows as bf16 pairs: H[2t] = h_t, H[2t + 1] = 0 (h is bf16), padding rows 0;
-// the padding rows of every z_k are cleared too.
-__global__ void heads_mma_prep_kernel(const uint16_t* __restrict__ h, int T, int d, int N, int K,
+// the padding rows of every z_k are cleared too.  Wide: H[t] = h_t (single rows).
+__global__ void heads_mma_prep_kernel(const uint16_t* __restrict__ h, int T, int d, int N, int K, int wide,
                                       uint16_t* __restrict__ h_hl, uint16_t* __restrict__ z_hl) {
   const int i = blockIdx.x * blockDim.x + threadIdx.x;
   if (i >= d) return;
-  for (int n = 0; n < N; ++n) h_hl[(int64_t)n * d + i] = (n < 2 * T && (n & 1) == 0) ? h[(int64_t)(n >> 1) * d + i] : 0;
+  const int used = wide ? T : 2 * T;
+  for (int n = 0; n < N; ++n) {
+    uint16_t v = 0;
+    if (wide) v = n < T ? h[(int64_t)n * d + i] : 0;
+    else v = (n < 2 * T && (n & 1) == 0) ? h[(int64_t)(n >> 1) * d + i] : 0;
+    h_hl[(int64_t)n * d + i] = v;
+  }
   for (int k = 0; k < K; ++k)
-    for (int n = 2 * T; n < N; ++n) z_hl[((int64_t)k * N + n) * d + i] = 0;
+    for (int n = used; n < N; ++n) z_hl[((int64_t)k * N + n) * d + i] = 0;
 }
 
 }  // namespace
 
-size_t heads_mma_rows(int T) { return (size_t)((2 * T + 31) / 32 * 32); }
+size_t heads_mma_rows(int T, bool wide) {
+  if (wide) return (size_t)((T + 31) / 32 * 32);                     // single rows
+  return (size_t)((2 * T + 31) / 32 * 32);                           // bf16 pairs
+}
 
 namespace {
 // A stage holds bps boxes of weights (128 x 64) and of inputs (N x 64): as many K
 // chunks per stage as still leave four stages, else two (fewer, larger stages cost
 // the MMA lane fewer waits per byte; more stages keep more bytes in flight).
 size_t mma_stage_bytes(int N, int bps) { return (size_t)bps * ((size_t)kMRows * kMKc * 2 + (size_t)N * kMKc * 2); }
-constexpr size_t kMBudget = 227 * 1024 - 1024 - 32 * 8;
+constexpr int kMBarSlots = 64;              // mbarriers after the stages: full, empty, 2 x 2 accumulator, drain, conv
+constexpr size_t kMBudget = 227 * 1024 - 1024 - kMBarSlots * 8;
 int mma_bps(int N, int d) {
   // at least four stages in flight when two or more chunks per stage allow it
   // (measured: 16 rows, 2 chunks x 5 stages beat 4 chunks x 2 stages by 2%)
@@ -344,15 +428,19 @@ int mma_stages(int N, int d) {
   int s = (int)(kMBudget / mma_stage_bytes(N, mma_bps(N, d)));
   return s > 12 ? 12 : s;
 }
-size_t mma_smem(int N, int d) { return 1024 + (size_t)mma_stages(N, d) * mma_stage_bytes(N, mma_bps(N, d)) + 32 * 8; }
+size_t mma_smem(int N, int d) {
+  return 1024 + (size_t)mma_stages(N, d) * mma_stage_bytes(N, mma_bps(N, d)) + kMBarSlots * 8;
+}
+static_assert(3 * 12 + 5 <= kMBarSlots, "barrier slots of the most stages");
 
-bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows) {
+bool encode_2d(CUtensorMap* map, const void* base, uint64_t inner, uint64_t rows, uint32_t box_rows,
+               CUtensorMapDataType dt = CU_TENSOR_MAP_DATA_TYPE_BFLOAT16) {
   auto fn = encode_fn();
   if (!fn) return false;
   cuuint64_t dims[2] = {inner, rows};
   cuuint64_t strides[1] = {inner * 2};
   cuuint32_t box[2] = {(cuuint32_t)kMKc, box_rows}, estr[2] = {1, 1};
-  return fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+  return fn(map, dt, 2, const_cast<void*>(base), dims, strides, box, estr,
             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
@@ -373,30 +461,33 @@ bool heads_mma_supported(int T, int d, int V, int K, medusa_dtype dt, const void
                          int64_t w2_stride, const void* w_lm) {
   auto al = [](const void* p) { return (reinterpret_cast<uintptr_t>(p) & 15u) == 0; };
   if (T < 2 || dt != MEDUSA_BF16 || K < 1 || d % kMKc != 0 || V < 1) return false;
-  if (T > kHeadsMmaMaxRows) T = kHeadsMmaMaxRows;          // more rows run in passes of this many
+  const bool wide = heads_mma_wide(T);
+  const int per_pass = wide ? kHeadsMmaWideRows : kHeadsMmaMaxRows;
+  if (T > per_pass) T = per_pass;                          // more rows run in passes of this many
   if (!h || !w1 || !w2 || !w_lm || !al(h) || !al(w1) || !al(w2) || !al(w_lm)) return false;
   if (w2_stride < 0 || (w2_stride * 2) % 16 != 0 || (w2_stride != 0 && w2_stride < (int64_t)V * d)) return false;
   if (!encode_fn()) return false;
   int dev = 0, coop = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-  const int N = (int)heads_mma_rows(T);
+  const int N = (int)heads_mma_rows(T, wide);
   if (coop == 0 || mma_stages(N, d) < 2) return false;
-  if (cudaFuncSetAttribute(heads_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mma_smem(N, d)) !=
-      cudaSuccess)
+  auto kern = wide ? heads_mma_kernel<true> : heads_mma_kernel<false>;
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mma_smem(N, d)) != cudaSuccess)
     return false;
   int per_sm = 0;
-  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, heads_mma_kernel, kMThreads, mma_smem(N, d)) !=
-      cudaSuccess)
+  if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, wide ? kMThreadsWide : kMThreads,
+                                                    mma_smem(N, d)) != cudaSuccess)
     return false;
   return per_sm >= 1;
 }
 
-cudaError_t launch_heads_mma(const HeadsPlan& p, const void* h, const void* w1, const void* b1, const void* w2,
-                             int64_t w2_stride, const void* w_lm, float* logits, void* ws, cudaStream_t st) {
+cudaError_t launch_heads_mma(const HeadsPlan& p, bool wide, const void* h, const void* w1, const void* b1,
+                             const void* w2, int64_t w2_stride, const void* w_lm, float* logits, void* ws,
+                             cudaStream_t st) {
   char* base = (char*)ws;
   const int T = p.T, d = p.d, V = p.V, K = p.K;
-  const int N = (int)heads_mma_rows(T);
+  const int N = (int)heads_mma_rows(T, wide);
   uint16_t* h_hl = (uint16_t*)(base + p.off_hhl);
   uint16_t* z_hl = (uint16_t*)(base + p.off_zhl);
   int* err = (int*)(base + p.off_err);
@@ -404,7 +495,9 @@ cudaError_t launch_heads_mma(const HeadsPlan& p, const void* h, const void* w1, 
   const bool shared = w2_stride == 0;
   if (!encode_2d(&mw1, w1, d, (uint64_t)K * d, kMRows) || !encode_2d(&mlm, w_lm, d, V, kMRows) ||
       !(shared ? encode_2d(&mw2, w2, d, V, kMRows) : encode_w2(&mw2, w2, d, V, K, w2_stride)) ||
-      !encode_2d(&mh, h_hl, d, N, N) || !encode_2d(&mz, z_hl, d, (uint64_t)K * N, N))
+      !encode_2d(&mh, h_hl, d, N, N) ||
+      !encode_2d(&mz, z_hl, d, (uint64_t)K * N, N,
+                 wide ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
     return cudaErrorInvalidValue;
   MmaArgs a{};
   a.h = (const uint16_t*)h;
@@ -419,17 +512,19 @@ cudaError_t launch_heads_mma(const HeadsPlan& p, const void* h, const void* w1, 
   a.n_stages = mma_stages(N, d);
   a.stage_bytes = (uint32_t)mma_stage_bytes(N, a.bps);
   cudaError_t e;
-  heads_mma_prep_kernel<<<(d + 255) / 256, 256, 0, st>>>((const uint16_t*)h, T, d, N, K, h_hl, z_hl);
+  heads_mma_prep_kernel<<<(d + 255) / 256, 256, 0, st>>>((const uint16_t*)h, T, d, N, K, wide ? 1 : 0, h_hl,
+                                                          z_hl);
   if ((e = cudaGetLastError()) != cudaSuccess) return e;
   const size_t smem = mma_smem(N, d);
-  e = cudaFuncSetAttribute(heads_mma_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  auto kern = wide ? heads_mma_kernel<true> : heads_mma_kernel<false>;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;
   int dev = 0, sms = 0;
   cudaGetDevice(&dev);
   cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
   cudaLaunchConfig_t cfg = {};
   cfg.gridDim = dim3(sms);
-  cfg.blockDim = dim3(kMThreads);
+  cfg.blockDim = dim3(wide ? kMThreadsWide : kMThreads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute attr[1];
@@ -437,7 +532,7 @@ cudaError_t launch_heads_mma(const HeadsPlan& p, const void* h, const void* w1, 
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, heads_mma_kernel, mw1, mlm, mw2, mh, mz, a);
+  e = cudaLaunchKernelEx(&cfg, kern, mw1, mlm, mw2, mh, mz, a);
   if (e != cudaSuccess) return e;
   return cudaGetLastError();
 }

@@ -26,8 +26,12 @@ struct HeadsPlan {
 };
 // Weight-stream path (heads_stream.cu): at most this many CTAs, and an error flag plus
 // completion counters in the first kHeadsCounterBytes at off_err (zeroed every call).
-// Hidden rows per pass of the tensor-core heads stream (more rows run in passes).
+// Hidden rows per pass of the tensor-core heads stream (more rows run in passes): up to
+// 128 rows as bf16 pairs; calls of more rows run "wide" passes of up to 256 single rows
+// (z in fp16, W2 re-encoded to fp16 in shared memory).
 constexpr int kHeadsMmaMaxRows = 128;
+constexpr int kHeadsMmaWideRows = 256;
+inline bool heads_mma_wide(int T) { return T > kHeadsMmaMaxRows; }
 constexpr int kHeadsStreamMaxGrid = 256;
 constexpr size_t kHeadsCounterBytes = 256;
 HeadsPlan plan_heads(int T, int d, int V, int K, int topk);
@@ -36,13 +40,15 @@ bool heads_stream_supported(int T, int d, int V, int K, int topk, medusa_dtype d
 cudaError_t launch_heads_stream(const HeadsPlan& p, const void* h, const void* w1, const void* b1, const void* w2,
                                 int64_t w2_stride, const void* w_lm, int32_t* root, int32_t* pool,
                                 float* logits_out, void* ws, cudaStream_t st);
-// Tensor-core path for 2 <= T <= 128 hidden rows (heads_mma.cu): writes all logits,
-// the top-k kernels then select.  Input rows of the MMA: 2T rounded up to 32.
-size_t heads_mma_rows(int T);
+// Tensor-core path for T >= 2 hidden rows (heads_mma.cu), one pass of at most 128 (or,
+// wide, 256) rows: writes all logits, the top-k kernels then select.  Input rows of the
+// MMA: 2T (pairs) or T (wide) rounded up to 32.
+size_t heads_mma_rows(int T, bool wide);
 bool heads_mma_supported(int T, int d, int V, int K, medusa_dtype dt, const void* h, const void* w1, const void* w2,
                          int64_t w2_stride, const void* w_lm);
-cudaError_t launch_heads_mma(const HeadsPlan& p, const void* h, const void* w1, const void* b1, const void* w2,
-                             int64_t w2_stride, const void* w_lm, float* logits, void* ws, cudaStream_t st);
+cudaError_t launch_heads_mma(const HeadsPlan& p, bool wide, const void* h, const void* w1, const void* b1,
+                             const void* w2, int64_t w2_stride, const void* w_lm, float* logits, void* ws,
+                             cudaStream_t st);
 cudaError_t launch_heads(const HeadsPlan& p, const void* h, const void* w1, const void* b1,
                          const void* w2, int64_t w2_stride, const void* w_lm, medusa_dtype dt,
                          int32_t* root, int32_t* pool, float* logits_out, void* ws,

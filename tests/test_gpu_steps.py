@@ -61,7 +61,9 @@ def test_tree_fill(m, name):
     dict(T=1, d=6144, V=3001, K=3, topk=10, dt=torch.bfloat16),   # weight stream, rows in two halves
     dict(T=3, d=1024, V=4000, K=3, topk=10, dt=torch.bfloat16),
     dict(T=16, d=4096, V=2048, K=2, topk=10, dt=torch.bfloat16),
-    dict(T=150, d=256, V=1000, K=2, topk=5, dt=torch.bfloat16),   # tensor-core stream in two passes
+    dict(T=128, d=256, V=1000, K=2, topk=5, dt=torch.bfloat16),   # tensor-core stream, one pass of pairs
+    dict(T=150, d=256, V=1000, K=2, topk=5, dt=torch.bfloat16),   # one wide pass (single rows, fp16 z)
+    dict(T=300, d=512, V=777, K=3, topk=8, dt=torch.bfloat16),    # two wide passes, ragged vocabulary group
     dict(T=5, d=128, V=300, K=1, topk=32, dt=torch.float32),
 ])
 def test_heads_topk(m, case):
@@ -76,10 +78,15 @@ def test_heads_topk(m, case):
     o_root, o_pool, o_logits = oheads.medusa_heads(gu.to64(h), gu.to64(w1), gu.to64(w2), gu.to64(w_lm), topk)
     gu.float_parity(logits, o_logits, dt == torch.float32, "head logits")
     root, pool = root.cpu().numpy(), pool.cpu().numpy()
+    # Near ties the fp32 and fp64 rankings may order differently.  Pairs (T <= 128) keep z
+    # to ~2^-16, so logits agree to ~1e-5.  Wide passes (T > 128) keep z in fp16: each
+    # element carries a relative rounding of at most 2^-11, so a logit errs by about
+    # 2^-11 / sqrt(3) * ||W2 o z||_2 ~ 3e-4 (std) here, and ranks within 4e-3 are near ties.
+    tol = 4e-3 if (dt == torch.bfloat16 and T > 128) else 1e-4
     for t in range(T):
-        gu.topk_parity([root[t]], o_logits[t, 0], 1, tol=1e-4)
+        gu.topk_parity([root[t]], o_logits[t, 0], 1, tol=tol)
         for k in range(K):
-            gu.topk_parity(pool[t, k], o_logits[t, 1 + k], topk, tol=1e-4)
+            gu.topk_parity(pool[t, k], o_logits[t, 1 + k], topk, tol=tol)
         # the top-k kernel itself is exact on its own fp32 inputs
         gl = logits[t].cpu().numpy().astype(np.float64)
         assert root[t] == np.lexsort((np.arange(V), -gl[0]))[0]

@@ -111,10 +111,10 @@ def test_heads_full_size_sampled(m, name):
 
 @pytest.mark.parametrize("name", ["llama3-8b-256", "longctx-341"])
 def test_heads_all_rows_full_size_sampled(m, name):
-    """The all-rows variant (every tree row a hidden row: 256 and 341 rows, two and
-    three tensor-core passes) on the full weights: sampled logits of rows in every
-    pass against the fp64 oracle, and the top-k of every sampled row exact on the
-    kernel's own logits."""
+    """The all-rows variant (every tree row a hidden row: 256 and 341 rows, one and two
+    wide tensor-core passes of up to 256 rows) on the full weights: sampled logits of
+    rows in every pass against the fp64 oracle, and the top-k of every sampled row exact
+    on the kernel's own logits."""
     w = synth.WORKLOADS[name]
     t_o, _, _ = templates(m, w)
     T = t_o.n_rows
@@ -125,7 +125,7 @@ def test_heads_all_rows_full_size_sampled(m, name):
     torch.cuda.synchronize()
     rng = np.random.default_rng(11)
     root, pool = root.cpu().numpy(), pool.cpu().numpy()
-    for t in [0, 127, 128, T - 1]:
+    for t in sorted({0, 127, 128, min(255, T - 1), min(256, T - 1), T - 1}):
         rows = []
         for mm in range(w.n_heads + 1):
             ids = list(rng.integers(0, w.vocab, size=8))
