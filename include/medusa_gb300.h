@@ -90,8 +90,20 @@ typedef int32_t medusa_dtype;
  * The struct is a host value whose array pointers point either into a host
  * buffer (after medusa_tree_compile) or into a device buffer (after
  * medusa_tree_upload).  Device calls take the device form.
+ *
+ * Per-sequence templates ([M7.2] §0x07D: sequences of a batch may verify different
+ * trees; [CN] notes that the best tree moves with the context length): when per_seq
+ * is not NULL it points to a device array of B device-form templates, one per
+ * sequence (each with per_seq NULL and the batch's topk), and the counts of this
+ * struct are bounds over them (n_rows, n_words, max_depth, n_paths and n_internal at
+ * least those of every sequence; topk equal); its arrays are not read.  Per-row
+ * tensors of the device calls are then laid out with the bound: tokens, pos [B][n_rows],
+ * q [B][n_rows][H][dh], logits [B][n_rows][V], out_rows [B][max_depth + 1]; rows past a
+ * sequence's own n_rows are not read as tree rows (tokens and pos get -1 there, the
+ * attention output is not written there).  medusa_tree_batch builds such a struct;
+ * medusa_tree_greedy_device builds a tree per sequence on the GPU.
  */
-typedef struct {
+typedef struct medusa_tree_s {
   int32_t n_rows;       /* N = 1 + number of rank paths */
   int32_t n_words;      /* ceil(N / 64): 64-bit words per ancestor mask row */
   int32_t max_depth;    /* D = longest path */
@@ -105,6 +117,7 @@ typedef struct {
   const int32_t *internal;       /* [n_internal] rows with children, ascending */
   const int32_t *internal_index; /* [N] position of a row in `internal`, -1 for leaves */
   const uint64_t *anc;           /* [N][n_words] bit (v % 64) of word v / 64 set iff path(v) is a prefix of path(u) ([M7.2] §0x04A) */
+  const struct medusa_tree_s *per_seq; /* NULL, or [B] device templates, one per sequence (see above) */
 } medusa_tree_t;
 
 /* One layer's KV cache, contiguous or paged. */
@@ -145,6 +158,25 @@ medusa_status medusa_tree_regular(const int32_t *widths /*[host] K*/, int32_t K,
 medusa_status medusa_tree_greedy(const double *acc, int32_t K, int32_t R, int32_t budget,
                                  int32_t *paths_out, int32_t *n_out);
 
+/* Greedy trees built on the GPU, one per sequence, from per-sequence rank
+ * accuracies ([M7.2] §0x04C; [PartII] Part 3; [CN]: the best tree moves with the
+ * context): the search of medusa_tree_greedy (same weights, same tie rule, so the same
+ * paths) followed by the compilation of medusa_tree_compile (same arrays, same canonical
+ * order), in one kernel with one CTA per sequence, with no host round trip.
+ *   acc [B][K][R] device doubles in [0, 1] (a sequence with a value outside gets the
+ *   root-only template and status MEDUSA_EINVAL); ranks r < R <= topk; budget >= 0
+ *   non-root paths per sequence, R * (budget + 1) <= 6144;
+ *   dev_buf: medusa_tree_greedy_device_bytes(B, K, R, budget) bytes (16-byte aligned)
+ *   that receive the B template arrays; per_seq [B] device medusa_tree_t (8-byte
+ *   aligned), written by the kernel; status [B] device or NULL (0, or MEDUSA_EINVAL);
+ *   batch_out [host]: the per-sequence batch to pass to the device calls (counts are
+ *   the bounds budget + 1 rows, depth min(K, budget); per_seq set).
+ * Returns after enqueueing; MEDUSA_EUNSUPPORTED when R * (budget + 1) > 6144. */
+size_t medusa_tree_greedy_device_bytes(int32_t B, int32_t K, int32_t R, int32_t budget);
+medusa_status medusa_tree_greedy_device(const double *acc, int32_t B, int32_t K, int32_t R, int32_t budget,
+                                        int32_t topk, void *dev_buf, size_t dev_bytes, medusa_tree_t *per_seq,
+                                        int32_t *status, medusa_tree_t *batch_out, void *stream);
+
 /* Bytes of the template blob for up to n_paths rank paths of length <= max_len. */
 size_t medusa_tree_bytes(int32_t n_paths, int32_t max_len);
 
@@ -163,6 +195,15 @@ medusa_status medusa_tree_compile(const int32_t *paths, int32_t n_paths, int32_t
 medusa_status medusa_tree_upload(const medusa_tree_t *host_tree, const void *host_buf,
                                  void *dev_buf, size_t dev_bytes, medusa_tree_t *dev,
                                  void *stream);
+
+/* A per-sequence batch of device templates (see medusa_tree_t): copies the B
+ * descriptors seq [host] [B] (device form, per_seq NULL, equal topk) into dev_descs
+ * (device, B * sizeof(medusa_tree_t) bytes, 8-byte aligned; one cudaMemcpyAsync on
+ * `stream`, seq must stay alive until it completes) and fills *out with the bounds of
+ * their counts and out->per_seq = dev_descs.  The same device template may serve
+ * several sequences.  MEDUSA_EINVAL on a mismatch of topk or a nested batch. */
+medusa_status medusa_tree_batch(const medusa_tree_t *seq, int32_t B, void *dev_descs, size_t dev_bytes,
+                                medusa_tree_t *out, void *stream);
 
 /* ---------------------------------------------------------------------------
  * Round step 1: heads + top-k

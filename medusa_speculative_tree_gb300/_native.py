@@ -21,7 +21,8 @@ ATTN_STATIC_SCRATCH_BYTES = 32 * 1024 * 1024
 
 EXPORTED = [
     "medusa_tree_regular", "medusa_tree_greedy", "medusa_tree_bytes", "medusa_tree_compile",
-    "medusa_tree_upload", "medusa_heads_topk_workspace", "medusa_heads_topk", "medusa_tree_fill",
+    "medusa_tree_upload", "medusa_tree_batch", "medusa_tree_greedy_device_bytes", "medusa_tree_greedy_device",
+    "medusa_heads_topk_workspace", "medusa_heads_topk", "medusa_tree_fill",
     "medusa_tree_attn_workspace", "medusa_tree_attn_verify", "medusa_tree_attn_verify_static",
     "medusa_tree_accept_workspace",
     "medusa_tree_accept", "medusa_tree_accept_commit", "medusa_tree_accept_hidden_workspace", "medusa_tree_accept_hidden", "medusa_kv_compact", "medusa_kv_compact_layers", "medusa_round_workspace", "medusa_round_create",
@@ -36,7 +37,7 @@ class MedusaTree(C.Structure):
         ("n_paths", C.c_int32), ("topk", C.c_int32), ("n_internal", C.c_int32),
         ("slot", C.c_void_p), ("depth", C.c_void_p), ("parent", C.c_void_p),
         ("retrieve", C.c_void_p), ("internal", C.c_void_p), ("internal_index", C.c_void_p),
-        ("anc", C.c_void_p),
+        ("anc", C.c_void_p), ("per_seq", C.c_void_p),
     ]
 
 
@@ -93,6 +94,9 @@ def lib() -> C.CDLL:
         "medusa_tree_bytes": (SZ, [I32, I32]),
         "medusa_tree_compile": (I32, [VP, I32, I32, I32, I32, VP, SZ, P(MedusaTree)]),
         "medusa_tree_upload": (I32, [P(MedusaTree), VP, VP, SZ, P(MedusaTree), VP]),
+        "medusa_tree_batch": (I32, [P(MedusaTree), I32, VP, SZ, P(MedusaTree), VP]),
+        "medusa_tree_greedy_device_bytes": (SZ, [I32, I32, I32, I32]),
+        "medusa_tree_greedy_device": (I32, [VP, I32, I32, I32, I32, I32, VP, SZ, VP, VP, P(MedusaTree), VP]),
         "medusa_heads_topk_workspace": (SZ, [I32, I32, I32, I32, I32]),
         "medusa_heads_topk": (I32, [VP, I32, I32, I32, I32, VP, VP, VP, I64, VP, I32, I32, VP, VP,
                                     VP, VP, SZ, VP]),

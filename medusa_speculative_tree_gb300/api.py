@@ -154,6 +154,96 @@ class Template:
         return self
 
 
+class TemplateBatch:
+    """Per-sequence templates of one batch (medusa_tree_batch): sequence b verifies
+    templates[index[b]].  Usable wherever a Template is: per-row tensors are laid out
+    with the batch's bound n_rows (and max_depth + 1 for published rows)."""
+
+    def __init__(self, templates: Sequence[Template], index: Sequence[int], device=None):
+        device = torch.device(device) if device is not None else templates[0].device
+        B = len(index)
+        self._templates = list(templates)
+        self._descs = (nat.MedusaTree * B)(*[templates[int(i)].dev for i in index])
+        nbytes = B * C.sizeof(nat.MedusaTree)
+        self._dev_descs = torch.empty(nbytes, dtype=torch.uint8, device=device)
+        self.dev = nat.MedusaTree()
+        check("medusa_tree_batch",
+              lib().medusa_tree_batch(self._descs, B, C.c_void_p(self._dev_descs.data_ptr()), nbytes,
+                                      C.byref(self.dev), _stream(device)))
+        torch.cuda.current_stream(device).synchronize()     # host descriptors copied
+        self.index = [int(i) for i in index]
+        self.device = device
+        self.n_rows = self.dev.n_rows
+        self.n_words = self.dev.n_words
+        self.max_depth = self.dev.max_depth
+        self.n_paths = self.dev.n_paths
+        self.topk = self.dev.topk
+        self.n_internal = self.dev.n_internal
+
+    @classmethod
+    def from_device(cls, dev: "nat.MedusaTree", keep=(), device=None):
+        """A batch descriptor built on the device (medusa_tree_greedy_device)."""
+        self = cls.__new__(cls)
+        self._templates = []
+        self._keep = keep
+        self.dev = dev
+        self.index = None
+        self.device = torch.device(device) if device is not None else None
+        self.n_rows = dev.n_rows
+        self.n_words = dev.n_words
+        self.max_depth = dev.max_depth
+        self.n_paths = dev.n_paths
+        self.topk = dev.topk
+        self.n_internal = dev.n_internal
+        return self
+
+
+def medusa_tree_greedy_device(acc, budget: int, topk: int):
+    """Greedy trees built on the GPU, one per sequence (medusa_tree_greedy_device):
+    acc [B, K, R] float64 CUDA tensor of rank accuracies.  Returns (TemplateBatch, status [B])."""
+    _need_cuda(acc)
+    if acc.dtype != torch.float64 or acc.dim() != 3:
+        raise ValueError("acc must be a [B, K, R] float64 CUDA tensor")
+    B, K, R = acc.shape
+    dev = acc.device
+    nb = lib().medusa_tree_greedy_device_bytes(B, K, R, budget)
+    if nb == 0:
+        raise ValueError("invalid greedy tree shape")
+    buf = torch.empty(nb, dtype=torch.uint8, device=dev)
+    descs = torch.empty(B * C.sizeof(nat.MedusaTree), dtype=torch.uint8, device=dev)
+    status = torch.empty(B, dtype=torch.int32, device=dev)
+    out = nat.MedusaTree()
+    check("medusa_tree_greedy_device",
+          lib().medusa_tree_greedy_device(_ptr(acc), B, K, R, budget, topk, _ptr(buf), nb, _ptr(descs), _ptr(status),
+                                          C.byref(out), _stream(dev)))
+    return TemplateBatch.from_device(out, keep=(buf, descs, acc), device=dev), status
+
+
+def batch_template_arrays(batch, b: int) -> dict:
+    """Host copies of sequence b's template arrays of a batch built by
+    medusa_tree_greedy_device (read from the blob buffer that holds them)."""
+    buf, descs = batch._keep[0], batch._keep[1]
+    sz = C.sizeof(nat.MedusaTree)
+    raw = descs[b * sz:(b + 1) * sz].cpu().numpy().tobytes()
+    t = nat.MedusaTree.from_buffer_copy(raw)
+    host = buf.cpu().numpy()
+    base = buf.data_ptr()
+
+    def arr(addr, count, dtype):
+        off = int(addr) - base
+        nbytes = count * np.dtype(dtype).itemsize
+        return host[off:off + nbytes].view(dtype).copy()
+    N, W = t.n_rows, t.max_depth + 1
+    return {"n_rows": N, "n_words": t.n_words, "max_depth": t.max_depth, "n_paths": t.n_paths,
+            "topk": t.topk, "n_internal": t.n_internal,
+            "slot": arr(t.slot, N, np.int32), "depth": arr(t.depth, N, np.int32),
+            "parent": arr(t.parent, N, np.int32),
+            "retrieve": arr(t.retrieve, t.n_paths * W, np.int32).reshape(t.n_paths, W),
+            "internal": arr(t.internal, t.n_internal, np.int32),
+            "internal_index": arr(t.internal_index, N, np.int32),
+            "anc": arr(t.anc, N * t.n_words, np.uint64).reshape(N, t.n_words)}
+
+
 # ----------------------------------------------------------------------------- KV cache
 
 @dataclass

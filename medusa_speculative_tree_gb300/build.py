@@ -19,7 +19,7 @@ INCLUDE = os.path.join(ROOT, "include")
 BUILD = os.path.join(PKG, "_build")
 LIB = os.path.join(PKG, "libmedusa_gb300.so")
 
-SOURCES = ["medusa_api.cpp", "heads.cu", "heads_stream.cu", "heads_mma.cu", "fill_compact.cu", "accept.cu",
+SOURCES = ["medusa_api.cpp", "heads.cu", "heads_stream.cu", "heads_mma.cu", "fill_compact.cu", "accept.cu", "tree_build.cu",
            "lm_accept.cu", "attn.cu", "attn_tc.cu"]
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 

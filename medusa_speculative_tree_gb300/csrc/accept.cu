@@ -92,7 +92,9 @@ __global__ void __launch_bounds__(kThreads) row_stats_kernel(medusa_tree_t t, in
                                                              RowPart* __restrict__ part) {
   constexpr int EPV = Elem<EL>::kPerVec;
   const int c = blockIdx.x, ii = blockIdx.y, b = blockIdx.z;
-  const int u = t.internal[ii];
+  const medusa_tree_t tb = seq_tree(t, b);
+  if (ii >= tb.n_internal) return;                 // (per-sequence templates: past this one's rows)
+  const int u = tb.internal[ii];
   const EL* row = logits + ((int64_t)b * t.n_rows + u) * V;
   const int start = c * chunk, end = min(V, start + chunk);
   float m = -INFINITY, z = 0.f, s1 = 0.f, av = -INFINITY;
@@ -162,7 +164,9 @@ __global__ void __launch_bounds__(kThreads) guard_kernel(medusa_tree_t t, int V,
                                                          const RowPart* __restrict__ part,
                                                          float* __restrict__ guard) {
   const int c = blockIdx.x, ii = blockIdx.y, b = blockIdx.z;
-  const int u = t.internal[ii];
+  const medusa_tree_t tb = seq_tree(t, b);
+  if (ii >= tb.n_internal) return;
+  const int u = tb.internal[ii];
   const RowPart* rp = part + (((int64_t)b * t.n_internal) + ii) * gridDim.x;
   float m, z, s1, av;
   int ai;
@@ -221,17 +225,21 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   extern __shared__ __align__(16) unsigned char smem_sel[];
   float* s_m = reinterpret_cast<float*>(smem_sel);
   const int b = blockIdx.x;
-  const int NI = t.n_internal, N = t.n_rows;
+  // Strides of the per-row tensors and of the chunk statistics come from t (a bound over
+  // the batch when templates are per sequence); the tree itself from this sequence's.
+  const int NIS = t.n_internal, NS = t.n_rows, WS = t.max_depth + 1;
+  const medusa_tree_t tq = seq_tree(t, b);
+  const int NI = tq.n_internal, N = tq.n_rows;
   float* s_lz = s_m + NI;                        // [NI] log Z
   float* s_tau = s_m + 2 * NI;                   // [NI] typical threshold
   int* s_am = reinterpret_cast<int*>(s_m + 3 * NI);   // [NI] argmax id
   float* s_lp = reinterpret_cast<float*>(smem_sel + lay.off_lp);   // [N] log p of the edge into v
   uint8_t* s_ok = smem_sel + lay.off_ok;         // [N] edge into v accepted
   int32_t* s_ret = reinterpret_cast<int32_t*>(smem_sel + lay.off_ret);
-  const int W = t.max_depth + 1;
+  const int W = tq.max_depth + 1;                 // retrieval width of this template
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool typ = mode != MEDUSA_ACCEPT_GREEDY;
-  const int32_t* tok = tokens + (int64_t)b * N;
+  const int32_t* tok = tokens + (int64_t)b * NS;
   if (err && *reinterpret_cast<const volatile int*>(err) != 0) {
     // the statistics were not completed (a bounded wait gave up): publish nothing
     if (threadIdx.x == 0) {
@@ -243,9 +251,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
         cm.L_out[b] = cm.L[b];
       }
     }
-    for (int j = threadIdx.x; j < W; j += kSelThreads) {
-      out_rows[(int64_t)b * W + j] = -1;
-      out_tokens[(int64_t)b * W + j] = -1;
+    for (int j = threadIdx.x; j < WS; j += kSelThreads) {
+      out_rows[(int64_t)b * WS + j] = -1;
+      out_tokens[(int64_t)b * WS + j] = -1;
     }
     return;
   }
@@ -261,19 +269,19 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
 #pragma unroll
     for (int k = 0; k < kEdges; ++k) {
       const int v = 1 + threadIdx.x + k * kSelThreads;
-      e_u[k] = v < N ? t.parent[v] : 0;
+      e_u[k] = v < N ? tq.parent[v] : 0;
       e_ct[k] = v < N ? tok[v] : -1;
     }
 #pragma unroll
     for (int k = 0; k < kEdges; ++k) {
       const int v = 1 + threadIdx.x + k * kSelThreads;
-      e_ii[k] = v < N ? t.internal_index[e_u[k]] : 0;
+      e_ii[k] = v < N ? tq.internal_index[e_u[k]] : 0;
       const bool need = typ && v < N && e_ct[k] >= 0 && e_ct[k] < V;
       // the logit of v's token at its parent: from the logits, or (projection folded
       // in) the value the statistics kernel recorded for this edge
       e_x[k] = !need ? 0.f
-                     : (edge_x ? edge_x[(int64_t)b * N + v]
-                               : Elem<EL>::load(logits, ((int64_t)b * N + e_u[k]) * V + e_ct[k])) * inv_temp;
+                     : (edge_x ? edge_x[(int64_t)b * NS + v]
+                               : Elem<EL>::load(logits, ((int64_t)b * NS + e_u[k]) * V + e_ct[k])) * inv_temp;
     }
   }
   // 1. merged statistics per internal row (one warp per row, one lane per chunk) and
@@ -281,9 +289,9 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   //    staged first, four loads per thread in flight, so that the per-row merges do
   //    not wait on global memory one row after another.
   if (lay.ret_staged)
-    for (int i = threadIdx.x; i < t.n_paths * W; i += kSelThreads) s_ret[i] = t.retrieve[i];
-  const RowPart* part_b = part + (int64_t)b * NI * n_chunks;
-  const float* guard_b = guard ? guard + (int64_t)b * NI * n_chunks : nullptr;
+    for (int i = threadIdx.x; i < tq.n_paths * W; i += kSelThreads) s_ret[i] = tq.retrieve[i];
+  const RowPart* part_b = part + (int64_t)b * NIS * n_chunks;
+  const float* guard_b = guard ? guard + (int64_t)b * NIS * n_chunks : nullptr;
   if (lay.part_staged) {
     RowPart* sp = reinterpret_cast<RowPart*>(smem_sel + lay.off_part);
     float* sg = reinterpret_cast<float*>(sp + NI * n_chunks);
@@ -368,8 +376,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   // 3. every retrieval path: accepted prefix length and its log-probability
   int best_p = INT_MAX, best_a = -1;
   float best_s = -INFINITY;
-  for (int p = threadIdx.x; p < t.n_paths; p += kSelThreads) {
-    const int32_t* r = lay.ret_staged ? s_ret + p * W : t.retrieve + (int64_t)p * W;
+  for (int p = threadIdx.x; p < tq.n_paths; p += kSelThreads) {
+    const int32_t* r = lay.ret_staged ? s_ret + p * W : tq.retrieve + (int64_t)p * W;
     int a = 0;
     float score = 0.f;
     for (int j = 1; j < W; ++j) {
@@ -404,13 +412,13 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
       if (better(r_a[w], r_s[w], r_p[w], best_a, best_s, best_p)) {
         best_a = r_a[w]; best_s = r_s[w]; best_p = r_p[w];
       }
-    const int32_t* r = lay.ret_staged ? s_ret + best_p * W : t.retrieve + (int64_t)best_p * W;
+    const int32_t* r = lay.ret_staged ? s_ret + best_p * W : tq.retrieve + (int64_t)best_p * W;
     best_path[b] = best_p;
     accept_len[b] = best_a;
-    for (int j = 0; j < W; ++j) {
+    for (int j = 0; j < WS; ++j) {
       const bool in = j <= best_a;
-      out_rows[(int64_t)b * W + j] = in ? r[j] : -1;
-      out_tokens[(int64_t)b * W + j] = in ? tok[r[j]] : -1;
+      out_rows[(int64_t)b * WS + j] = in ? r[j] : -1;
+      out_tokens[(int64_t)b * WS + j] = in ? tok[r[j]] : -1;
     }
     frontier_row[b] = r[best_a];
   }
@@ -426,18 +434,18 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   __shared__ int c_status, c_G, c_L;
   if (threadIdx.x == 0) {
     const int a = best_a;
-    const int32_t* r = lay.ret_staged ? s_ret + best_p * W : t.retrieve + (int64_t)best_p * W;
+    const int32_t* r = lay.ret_staged ? s_ret + best_p * W : tq.retrieve + (int64_t)best_p * W;
     const int Lb = cm.L[b];
     int v = MEDUSA_OK;
     if (Lb < 0 || !seq_rows_ok(cm.c, b, (int64_t)Lb + N)) {
       v = MEDUSA_ECAPACITY;
-    } else if (a < 0 || a > t.max_depth) {
+    } else if (a < 0 || a > tq.max_depth) {
       v = MEDUSA_EPATH;
     } else {
       for (int j = 0; j <= a; ++j) {
         const int u = r[j];
         c_rows[j] = u;
-        if (u < 0 || u >= N || (j == 0 ? u != 0 : t.parent[u] != r[j - 1])) v = MEDUSA_EPATH;
+        if (u < 0 || u >= N || (j == 0 ? u != 0 : tq.parent[u] != r[j - 1])) v = MEDUSA_EPATH;
       }
     }
     c_status = v;

@@ -68,8 +68,7 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(SimtArgs a) {
   constexpr int PER_LANE = DH / 32;
   constexpr int EPV = Elem<EL>::kPerVec;
   extern __shared__ __align__(16) float smem[];
-  const medusa_tree_t& t = a.t;
-  const int D = t.max_depth;
+  const int D = a.t.max_depth;                        // (a bound over the batch with per-sequence templates)
   float* tab_c = smem;                                // [(D+1)][HALF]
   float* tab_s = tab_c + (D + 1) * HALF;
   float* qs = tab_s + (D + 1) * HALF;                 // [kSimtRows][DH]
@@ -79,9 +78,12 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(SimtArgs a) {
 
   const int s = blockIdx.x, mt = blockIdx.y;
   const int b = blockIdx.z / a.Hkv, kvh = blockIdx.z % a.Hkv;
-  const int N = t.n_rows, g = a.g, M = N * g;
+  // NS: row stride of q, k_new, v_new, out (the batch's bound); N: this sequence's rows
+  const medusa_tree_t t = seq_tree(a.t, b);
+  const int NS = a.t.n_rows, N = t.n_rows, g = a.g, M = N * g;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int Lb = a.L[b];
+  if (mt * kSimtRows >= M) return;        // a row tile past this sequence's rows: the whole unit
   const bool first_cta = (s == 0 && mt == 0 && kvh == 0 && tid == 0);
   if (Lb < 0 || !seq_rows_ok(a.c, b, (int64_t)Lb + N)) {
     if (first_cta) a.status[b] = MEDUSA_ECAPACITY;
@@ -113,7 +115,7 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(SimtArgs a) {
     float y1 = 0.f, y2 = 0.f;
     if (R < M) {
       const int u = R / g, h = kvh * g + R % g;
-      const int64_t base = (((int64_t)b * N + u) * a.Hq + h) * DH;
+      const int64_t base = (((int64_t)b * NS + u) * a.Hq + h) * DH;
       const float x1 = Elem<EL>::load(q, base + i), x2 = Elem<EL>::load(q, base + i + HALF);
       const int ti = t.depth[u] * HALF + i;
       y1 = x1 * tab_c[ti] - x2 * tab_s[ti];
@@ -131,7 +133,7 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(SimtArgs a) {
       const int R = mt * kSimtRows + r;
       if (R >= M || R % g != 0) continue;
       const int u = R / g;
-      const int64_t src = (((int64_t)b * N + u) * a.Hkv + kvh) * DH;
+      const int64_t src = (((int64_t)b * NS + u) * a.Hkv + kvh) * DH;
       const float x1 = Elem<EL>::load(kn, src + i), x2 = Elem<EL>::load(kn, src + i + HALF);
       const int ti = t.depth[u] * HALF + i;
       const int64_t dst = row_off(a.c, b, kvh, Lb + u);
@@ -258,7 +260,7 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(SimtArgs a) {
       while (bits) {
         const int v = wd * 64 + __ffsll((long long)bits) - 1;
         bits &= bits - 1;
-        const int64_t kb = (((int64_t)b * N + v) * a.Hkv + kvh) * DH;
+        const int64_t kb = (((int64_t)b * NS + v) * a.Hkv + kvh) * DH;
         const int ti0 = t.depth[v] * HALF;
         float kr[PER_LANE];
 #pragma unroll
@@ -283,10 +285,10 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(SimtArgs a) {
       }
     }
     const float inv_l = 1.f / l;
-    const int64_t ob = (((int64_t)b * N + u) * a.Hq + h) * DH;
+    const int64_t ob = (((int64_t)b * NS + u) * a.Hq + h) * DH;
 #pragma unroll
     for (int c = 0; c < PER_LANE; ++c) out[ob + lane + 32 * c] = o[c] * inv_l;
-    if (a.lse && lane == 0) a.lse[((int64_t)b * N + u) * a.Hq + h] = (Mx + log2f(l)) * kLn2;
+    if (a.lse && lane == 0) a.lse[((int64_t)b * NS + u) * a.Hq + h] = (Mx + log2f(l)) * kLn2;
   }
 }
 

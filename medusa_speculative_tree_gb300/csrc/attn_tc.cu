@@ -285,14 +285,14 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
   using C = TcCfg<QT, NS>;
   extern __shared__ uint8_t smem_raw[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
-  const medusa_tree_t& t = a.t;
-  const int D = t.max_depth;
+  const int D = a.t.max_depth;                        // (a bound over the batch with per-sequence templates)
   float* tab_c = reinterpret_cast<float*>(sm + C::kOffTable);     // [(D+1)][64]
   float* tab_s = tab_c + (D + 1) * kHalf;
   uint64_t* bars = reinterpret_cast<uint64_t*>(
       (reinterpret_cast<uintptr_t>(tab_s + (D + 1) * kHalf) + 7) & ~uintptr_t(7));
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
+  __shared__ medusa_tree_t s_tree;                  // this sequence's template
 
   const int ct_idx = blockIdx.x, s = blockIdx.y;     // ct_idx: which QT row tiles
   // Units of longer sequences start first (longest-processing-time order, which packs
@@ -314,8 +314,13 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
     __syncthreads();
     b = sel_b;
   }
-  const int N = t.n_rows, g = a.g, M = N * g;
+  if (threadIdx.x == 0) s_tree = seq_tree(a.t, b);
+  __syncthreads();
+  const medusa_tree_t& t = s_tree;
+  // NSTR: row stride of q, k_new, v_new and out (the batch's bound); N: this sequence's rows
+  const int NSTR = a.t.n_rows, N = t.n_rows, g = a.g, M = N * g;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  if (C::kRows * ct_idx >= M) return;               // row tiles past this sequence's rows: the whole cluster
   const int Lb = a.L[b];
   const bool first_cta = (s == 0 && ct_idx == 0 && kvh == 0 && tid == 0);
   if (Lb < 0 || !seq_rows_ok(a.c, b, (int64_t)Lb + N)) {
@@ -726,7 +731,7 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
       uint16_t* cv = (uint16_t*)a.c.v;
       for (int it = ct; it < n_mine * 8; it += C::kConvThreads) {
         const int uu = u_first + (it >> 3) * stagers, c = it & 7;
-        const int64_t src = (((int64_t)b * N + uu) * a.Hkv + kvh) * kDH + 8 * c;
+        const int64_t src = (((int64_t)b * NSTR + uu) * a.Hkv + kvh) * kDH + 8 * c;
         const uint4 ka = __ldg(reinterpret_cast<const uint4*>(a.k_new + src));
         const uint4 kb = __ldg(reinterpret_cast<const uint4*>(a.k_new + src + kHalf));
         const uint4 va = __ldg(reinterpret_cast<const uint4*>(a.v_new + src));
@@ -1042,8 +1047,8 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
       const int ur = Rr / g, hr = kvh * g + Rr % g;
       if (!failed) {
         const float4 o = make_float4(acc.x * il, acc.y * il, acc.z * il, acc.w * il);
-        reinterpret_cast<float4*>(a.out + (((int64_t)b * N + ur) * a.Hq + hr) * kDH)[lane] = o;
-        if (a.lse && lane == 0) a.lse[((int64_t)b * N + ur) * a.Hq + hr] = (Mx + log2f(l)) * kLn2;
+        reinterpret_cast<float4*>(a.out + (((int64_t)b * NSTR + ur) * a.Hq + hr) * kDH)[lane] = o;
+        if (a.lse && lane == 0) a.lse[((int64_t)b * NSTR + ur) * a.Hq + hr] = (Mx + log2f(l)) * kLn2;
         // An fp16 operand that overflowed (|x| > 65504 in K, V or a scaled rotated query)
         // becomes inf, and a score of +inf, a value of inf or a query of inf turns the
         // row's softmax into NaN: an output that is not finite reports MEDUSA_ERANGE.

@@ -92,6 +92,14 @@ __device__ __forceinline__ float rope_angle(int pos, float theta_hi, float theta
   return r;
 }
 
+// The template of sequence b: its own when t is a per-sequence batch (t.per_seq set;
+// t's counts are then bounds over the batch and the row stride of per-row tensors),
+// else t itself.
+__device__ __forceinline__ medusa_tree_t seq_tree(const medusa_tree_t& t, int b) {
+  if (t.per_seq == nullptr) return t;
+  return t.per_seq[b];
+}
+
 // Rows [0, rows_end) of sequence b exist in the cache.  Contiguous caches check the
 // capacity; paged caches also need a valid page for the last row (a sequence owns
 // a prefix of its block-table row; unused entries are negative).

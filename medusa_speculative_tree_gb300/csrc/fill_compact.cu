@@ -9,22 +9,28 @@ namespace {
 
 // tokens[b][u] = cand_b[slot[u]], cand_b = [root[b], pool[b][0][:], pool[b][1][:], ...]
 // pos[b][u]    = L[b] + depth[u]
+// With per-sequence templates the rows of sequence b are those of its own template;
+// the rows past them (up to the batch bound, the row stride) get -1.
 __global__ void tree_fill_kernel(medusa_tree_t t, int K, const int32_t* __restrict__ root,
                                  const int32_t* __restrict__ pool, const int32_t* __restrict__ L,
                                  int32_t* __restrict__ tokens, int32_t* __restrict__ pos) {
   const int b = blockIdx.y;
   const int u = blockIdx.x * blockDim.x + threadIdx.x;
   if (u >= t.n_rows) return;
-  const int s = t.slot[u];
-  int tok;
-  if (s == 0) {
-    tok = root[b];
-  } else {
-    const int head = (s - 1) / t.topk, rank = (s - 1) % t.topk;
-    tok = pool[((int64_t)b * K + head) * t.topk + rank];
+  const medusa_tree_t tb = seq_tree(t, b);
+  int tok = -1, p = -1;
+  if (u < tb.n_rows) {
+    const int s = tb.slot[u];
+    if (s == 0) {
+      tok = root[b];
+    } else {
+      const int head = (s - 1) / tb.topk, rank = (s - 1) % tb.topk;
+      tok = (head < K && rank < t.topk) ? pool[((int64_t)b * K + head) * t.topk + rank] : -1;
+    }
+    p = L[b] + tb.depth[u];
   }
   tokens[(int64_t)b * t.n_rows + u] = tok;
-  pos[(int64_t)b * t.n_rows + u] = L[b] + t.depth[u];
+  pos[(int64_t)b * t.n_rows + u] = p;
 }
 
 // K and V base pointers of the layers that one launch commits ([M7.2] §0x06B: the
@@ -53,26 +59,27 @@ __global__ void kv_compact_kernel(medusa_kv_t c, LayerPtrs<NL> lp, int write_met
   __shared__ int seq_status;
   const int kvh = blockIdx.x, b = blockIdx.y, layer = blockIdx.z;
   const bool meta = write_meta && kvh == 0 && layer == 0 && threadIdx.x == 0;
-  const int dh = c.head_dim, W = t.max_depth + 1;
+  const int dh = c.head_dim, W = t.max_depth + 1;             // row stride of out_rows
+  const medusa_tree_t tb = seq_tree(t, b);                     // this sequence's template
   const int Lb = L[b];
   const int a = accept_len[b];
   if (threadIdx.x < 32) {
     const int j = threadIdx.x;
     const int u = j < W ? out_rows[(int64_t)b * W + j] : -1;
     const int prev = (j >= 1 && j < W) ? out_rows[(int64_t)b * W + j - 1] : -1;
-    const bool in = a >= 0 && a <= t.max_depth && j <= a;
+    const bool in = a >= 0 && a <= tb.max_depth && j <= a;
     bool bad = false;
     if (in) {
       rows_s[j] = u;
-      if (u < 0 || u >= t.n_rows) bad = true;
+      if (u < 0 || u >= tb.n_rows) bad = true;
       else if (j == 0) bad = u != 0;
-      else bad = t.parent[u] != prev;
+      else bad = tb.parent[u] != prev;
     }
     const bool any_bad = __any_sync(0xffffffffu, bad);
     if (j == 0) {
       int v = MEDUSA_OK;
-      if (Lb < 0 || !seq_rows_ok(c, b, (int64_t)Lb + t.n_rows)) v = MEDUSA_ECAPACITY;
-      else if (a < 0 || a > t.max_depth || any_bad) v = MEDUSA_EPATH;
+      if (Lb < 0 || !seq_rows_ok(c, b, (int64_t)Lb + tb.n_rows)) v = MEDUSA_ECAPACITY;
+      else if (a < 0 || a > tb.max_depth || any_bad) v = MEDUSA_EPATH;
       seq_status = v;
     }
   }

@@ -54,6 +54,21 @@ cudaError_t launch_heads(const HeadsPlan& p, const void* h, const void* w1, cons
                          int32_t* root, int32_t* pool, float* logits_out, void* ws,
                          cudaStream_t st);
 
+// ---- tree templates on the device (tree_build.cu) --------------------------------
+// Offsets of the template arrays inside one blob (the layout of medusa_tree_compile).
+struct TreeBlobLayout {
+  size_t slot, depth, parent, internal, internal_index, retrieve, anc, total;
+};
+TreeBlobLayout tree_blob_layout(int n_rows, int max_depth, int n_paths);
+// Entries (paths created) of one greedy search: R per admitted path plus the first R.
+constexpr int kMaxGreedyEntries = 6144;
+size_t tree_greedy_smem(int R, int budget);
+// One CTA per sequence: greedy frontier search on acc [B][K][R], then the template of the
+// chosen paths into blob b of dev_buf (blob_stride bytes each, layout for budget + 1
+// rows); per_seq[b] and status[b] (nullable) are written by the kernel.
+cudaError_t launch_tree_greedy(const double* acc, int B, int K, int R, int budget, int topk, void* dev_buf,
+                               size_t blob_stride, medusa_tree_t* per_seq, int32_t* status, cudaStream_t st);
+
 // ---- tree fill ----------------------------------------------------------------
 cudaError_t launch_tree_fill(const medusa_tree_t& t, int B, int K, const int32_t* root,
                              const int32_t* pool, const int32_t* L, int32_t* tokens,

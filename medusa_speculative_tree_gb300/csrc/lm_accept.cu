@@ -87,19 +87,23 @@ __global__ void lm_gather_kernel(medusa_tree_t t, int B, int d, const uint16_t* 
                                  int32_t* __restrict__ e_cnt, int* __restrict__ err) {
   const int col = blockIdx.x;
   if (col == 0 && threadIdx.x == 0) *err = 0;
+  // Columns b * NI + ii: internal row ii of sequence b (NI, N: the batch's bounds when
+  // templates are per sequence; a column past its sequence's internal rows is padding).
   const int NI = t.n_internal, N = t.n_rows;
-  const bool valid = col < B * NI;
-  const int b = valid ? col / NI : 0;
-  const int u = valid ? t.internal[col % NI] : 0;
+  const int b = col < B * NI ? col / NI : 0;
+  const medusa_tree_t tb = seq_tree(t, b);
+  const bool valid = col < B * NI && col % NI < tb.n_internal;
+  const int u = valid ? tb.internal[col % NI] : 0;
+  const int Nb = tb.n_rows;
   const uint4* src = reinterpret_cast<const uint4*>(hidden + ((int64_t)b * N + u) * d);
   uint4* dst = reinterpret_cast<uint4*>(X + (int64_t)col * d);
   for (int i = threadIdx.x; i < d / 8; i += blockDim.x) dst[i] = valid ? src[i] : make_uint4(0u, 0u, 0u, 0u);
   if (threadIdx.x < 32) {
     const int lane = threadIdx.x;
     int cnt = 0;
-    for (int v0 = 1; valid && v0 < N; v0 += 32) {
+    for (int v0 = 1; valid && v0 < Nb; v0 += 32) {
       const int v = v0 + lane;
-      const bool kid = v < N && t.parent[v] == u;
+      const bool kid = v < Nb && tb.parent[v] == u;
       const unsigned m = __ballot_sync(0xffffffffu, kid);
       if (kid) {
         const int slot = cnt + __popc(m & ((1u << lane) - 1u));

@@ -52,36 +52,23 @@ double path_weight(const Path& p, const double* acc, int R) {
   return w;
 }
 
-struct BlobLayout {
-  size_t slot, depth, parent, internal, internal_index, retrieve, anc, total;
-};
-
-BlobLayout blob_layout(int n_rows, int max_depth, int n_paths) {
-  BlobLayout l{};
-  size_t off = 0;
-  const size_t n = (size_t)n_rows * sizeof(int32_t);
-  l.slot = off; off += n;
-  l.depth = off; off += n;
-  l.parent = off; off += n;
-  l.internal = off; off += n;
-  l.internal_index = off; off += n;
-  l.retrieve = off; off += (size_t)n_paths * (max_depth + 1) * sizeof(int32_t);
-  off = align_up(off, 16);
-  l.anc = off; off += (size_t)n_rows * ((n_rows + 63) / 64) * sizeof(uint64_t);
-  l.total = align_up(off, 16);
-  return l;
-}
+using BlobLayout = medusa::TreeBlobLayout;
+BlobLayout blob_layout(int n_rows, int max_depth, int n_paths) { return medusa::tree_blob_layout(n_rows, max_depth, n_paths); }
 
 size_t blob_end(const medusa_tree_t* t, const void* base) {
   const char* anc_end = reinterpret_cast<const char*>(t->anc + (size_t)t->n_rows * t->n_words);
   return align_up((size_t)(anc_end - reinterpret_cast<const char*>(base)), 16);
 }
 
+// A template, or a per-sequence batch (per_seq set: the counts are bounds, the arrays
+// are not read; the per-sequence templates live in device memory, out of the host's view).
 bool tree_ok(const medusa_tree_t* t) {
-  return t && t->n_rows >= 1 && t->n_rows <= MEDUSA_MAX_ROWS && t->max_depth >= 0 &&
-         t->max_depth <= MEDUSA_MAX_DEPTH && t->n_paths >= 1 && t->topk >= 1 &&
-         t->topk <= MEDUSA_MAX_TOPK && t->n_words == (t->n_rows + 63) / 64 && t->slot &&
-         t->depth && t->parent && t->retrieve && t->internal && t->internal_index && t->anc;
+  if (!t || t->n_rows < 1 || t->n_rows > MEDUSA_MAX_ROWS || t->max_depth < 0 || t->max_depth > MEDUSA_MAX_DEPTH ||
+      t->n_paths < 1 || t->topk < 1 || t->topk > MEDUSA_MAX_TOPK || t->n_words != (t->n_rows + 63) / 64 ||
+      t->n_internal < 0 || t->n_internal > t->n_rows)
+    return false;
+  if (t->per_seq) return (reinterpret_cast<uintptr_t>(t->per_seq) & 7u) == 0;
+  return t->slot && t->depth && t->parent && t->retrieve && t->internal && t->internal_index && t->anc;
 }
 
 bool kv_ok(const medusa_kv_t* c) {
@@ -285,12 +272,76 @@ medusa_status medusa_tree_compile(const int32_t* paths, int32_t n_paths, int32_t
   out->internal = o_internal;
   out->internal_index = o_iidx;
   out->anc = o_anc;
+  out->per_seq = nullptr;
+  return MEDUSA_OK;
+}
+
+namespace {
+bool greedy_args_ok(int32_t B, int32_t K, int32_t R, int32_t budget, int32_t topk) {
+  return B >= 1 && K >= 1 && K <= MEDUSA_MAX_DEPTH && R >= 1 && topk >= 1 && topk <= MEDUSA_MAX_TOPK && R <= topk &&
+         budget >= 0 && budget < MEDUSA_MAX_ROWS;
+}
+size_t greedy_blob_stride(int32_t K, int32_t budget) {
+  return align_up(blob_layout(budget + 1, K, budget > 0 ? budget : 1).total, 256);
+}
+}  // namespace
+
+size_t medusa_tree_greedy_device_bytes(int32_t B, int32_t K, int32_t R, int32_t budget) {
+  if (!greedy_args_ok(B, K, R, budget, MEDUSA_MAX_TOPK)) return 0;
+  return (size_t)B * greedy_blob_stride(K, budget);
+}
+
+medusa_status medusa_tree_greedy_device(const double* acc, int32_t B, int32_t K, int32_t R, int32_t budget,
+                                        int32_t topk, void* dev_buf, size_t dev_bytes, medusa_tree_t* per_seq,
+                                        int32_t* status, medusa_tree_t* batch_out, void* stream) {
+  if (!acc || !dev_buf || !per_seq || !batch_out || !greedy_args_ok(B, K, R, budget, topk) || !aligned16(dev_buf) ||
+      (reinterpret_cast<uintptr_t>(per_seq) & 7u))
+    return MEDUSA_EINVAL;
+  if ((int64_t)R * (budget + 1) > medusa::kMaxGreedyEntries) return MEDUSA_EUNSUPPORTED;
+  const size_t stride = greedy_blob_stride(K, budget);
+  if (dev_bytes < (size_t)B * stride) return MEDUSA_EWORKSPACE;
+  if (cuda_status(medusa::launch_tree_greedy(acc, B, K, R, budget, topk, dev_buf, stride, per_seq, status,
+                                             as_stream(stream))) != MEDUSA_OK)
+    return MEDUSA_ECUDA;
+  medusa_tree_t bnd{};
+  bnd.n_rows = budget + 1;
+  bnd.n_words = (bnd.n_rows + 63) / 64;
+  bnd.max_depth = std::min<int32_t>(K, budget);
+  bnd.n_paths = budget > 0 ? budget : 1;
+  bnd.topk = topk;
+  bnd.n_internal = budget;
+  bnd.per_seq = per_seq;
+  *batch_out = bnd;
+  return MEDUSA_OK;
+}
+
+medusa_status medusa_tree_batch(const medusa_tree_t* seq, int32_t B, void* dev_descs, size_t dev_bytes,
+                                medusa_tree_t* out, void* stream) {
+  if (!seq || B < 1 || !dev_descs || !out || (reinterpret_cast<uintptr_t>(dev_descs) & 7u)) return MEDUSA_EINVAL;
+  if (dev_bytes < (size_t)B * sizeof(medusa_tree_t)) return MEDUSA_EWORKSPACE;
+  medusa_tree_t bnd{};
+  for (int b = 0; b < B; ++b) {
+    const medusa_tree_t& q = seq[b];
+    if (!tree_ok(&q) || q.per_seq || q.topk != seq[0].topk) return MEDUSA_EINVAL;
+    bnd.n_rows = std::max(bnd.n_rows, q.n_rows);
+    bnd.max_depth = std::max(bnd.max_depth, q.max_depth);
+    bnd.n_paths = std::max(bnd.n_paths, q.n_paths);
+    bnd.n_internal = std::max(bnd.n_internal, q.n_internal);
+  }
+  bnd.n_words = (bnd.n_rows + 63) / 64;
+  bnd.topk = seq[0].topk;
+  bnd.per_seq = static_cast<const medusa_tree_t*>(dev_descs);
+  if (cudaMemcpyAsync(dev_descs, seq, (size_t)B * sizeof(medusa_tree_t), cudaMemcpyHostToDevice,
+                      as_stream(stream)) != cudaSuccess)
+    return MEDUSA_ECUDA;
+  *out = bnd;
   return MEDUSA_OK;
 }
 
 medusa_status medusa_tree_upload(const medusa_tree_t* host_tree, const void* host_buf,
                                  void* dev_buf, size_t dev_bytes, medusa_tree_t* dev, void* stream) {
-  if (!tree_ok(host_tree) || !host_buf || !dev_buf || !dev || !aligned16(dev_buf)) return MEDUSA_EINVAL;
+  if (!tree_ok(host_tree) || host_tree->per_seq || !host_buf || !dev_buf || !dev || !aligned16(dev_buf))
+    return MEDUSA_EINVAL;
   const char* hb = static_cast<const char*>(host_buf);
   if (reinterpret_cast<const char*>(host_tree->slot) < hb) return MEDUSA_EINVAL;
   const size_t bytes = blob_end(host_tree, host_buf);

@@ -208,3 +208,50 @@ def test_commit_and_hidden_acceptance_checks_without_a_gpu(native):
                                          1.0, 0.09, 0.3, *outs, ws, 1 << 20, None) == native.EUNSUPPORTED
     assert lib.medusa_tree_accept_hidden(C.byref(t.host), 2, 100, 128, None, fake(41), fake(42), native.GREEDY,
                                          1.0, 0.09, 0.3, *outs, ws, 1 << 20, None) == native.EINVAL
+
+
+def test_template_batches_check_arguments_without_a_gpu(native):
+    """Host-visible checks of the per-sequence template calls come before any CUDA call:
+    medusa_tree_greedy_device refuses bad shapes (MEDUSA_EINVAL), a search larger than
+    its shared-memory frontier (MEDUSA_EUNSUPPORTED) and a short buffer
+    (MEDUSA_EWORKSPACE); medusa_tree_batch refuses mixed topk and nested batches;
+    medusa_tree_upload refuses a batch descriptor."""
+    lib = native.lib()
+    fake = C.c_void_p(1 << 20)                  # never dereferenced: every call below fails its checks
+    out = native.MedusaTree()
+    K, R, budget = 4, 10, 63
+    need = lib.medusa_tree_greedy_device_bytes(2, K, R, budget)
+    assert need > 0
+    assert lib.medusa_tree_greedy_device_bytes(2, 0, R, budget) == 0
+    g = lambda B, K_, R_, bud, topk, nbytes: lib.medusa_tree_greedy_device(fake, B, K_, R_, bud, topk, fake, nbytes,
+                                                                          fake, None, C.byref(out), None)
+    assert g(2, K, R, budget, 10, need - 1) == native.EWORKSPACE
+    assert g(2, K, 11, budget, 10, need) == native.EINVAL          # ranks beyond topk
+    assert g(0, K, R, budget, 10, need) == native.EINVAL
+    assert g(2, K, 32, 255, 32, 1 << 30) == native.EUNSUPPORTED     # 32 x 256 entries > 6144
+    host = m_tree(native, [(0,), (1,)], 2)
+    other = m_tree(native, [(0,)], 3)
+    arr = (native.MedusaTree * 2)(host, other)
+    assert lib.medusa_tree_batch(arr, 2, fake, 2 * C.sizeof(native.MedusaTree), C.byref(out), None) == native.EINVAL
+    nested = native.MedusaTree.from_buffer_copy(bytes(host))
+    nested.per_seq = fake.value
+    arr2 = (native.MedusaTree * 1)(nested)
+    assert lib.medusa_tree_batch(arr2, 1, fake, C.sizeof(native.MedusaTree), C.byref(out), None) == native.EINVAL
+    assert lib.medusa_tree_upload(C.byref(nested), fake, fake, 1 << 20, C.byref(out), None) == native.EINVAL
+
+
+_KEEP = []
+
+
+def m_tree(native, paths, topk):
+    """A host-compiled template (its blob kept alive for the test)."""
+    lib = native.lib()
+    n, L = len(paths), max(len(p) for p in paths)
+    arr = np.full((n, L), -1, dtype=np.int32)
+    for i, p in enumerate(paths):
+        arr[i, :len(p)] = p
+    blob = np.zeros(lib.medusa_tree_bytes(n, L) // 8 + 2, dtype=np.uint64)
+    t = native.MedusaTree()
+    assert lib.medusa_tree_compile(arr.ctypes.data, n, L, topk, 0, blob.ctypes.data, blob.nbytes, C.byref(t)) == 0
+    _KEEP.append(blob)
+    return t
