@@ -270,7 +270,7 @@ class Round:
 
 # DRAM bytes (read + write) of one heads launch, from an ncu capture of the current
 # kernel on that workload; absent for workloads not captured.
-HEADS_TRAFFIC = {"vicuna7b-64": 1_445_265_000 + 4_523_008}
+HEADS_TRAFFIC = {"vicuna7b-64": 1_445_265_000 + 4_523_008, "longctx-341": 11_040_000_000 + 6_980_000}
 # the same for the attention launch (dram__bytes_read.sum + dram__bytes_write.sum)
 ATTN_TRAFFIC = {"vicuna7b-64": 35_210_752 + 0}
 
@@ -796,6 +796,54 @@ ATTN_TENSOR_BOUND = ("llama3-8b-256", "longctx-341")
 HEADLINE = "longctx-341"
 
 
+# ----------------------------------------------------------------------------- one stage alone
+
+def run_stage(args):
+    """One step of the round alone on the workload's inputs (only those inputs are
+    built): `heads` (medusa_heads_topk on the frontier rows) or `attn`
+    (medusa_tree_attn_verify).  Prints the mean device time of --steps calls after
+    --warmup calls; for profiling a single kernel (ncu -k ... -s <warmup> -c 1)."""
+    dev = torch.device("cuda", 0)
+    torch.cuda.set_device(dev)
+    from medusa_speculative_tree_gb300 import build
+    build.build()
+    import medusa_speculative_tree_gb300 as m
+    w = synth.WORKLOADS[args.workload]
+    if args.stage == "heads":
+        h, w1, w2, w_lm = synth.head_weights(w, device=dev)
+        call = lambda: m.medusa_heads_topk(h, w1, w2, w_lm, w.topk)
+    else:
+        acc = synth.rank_accuracy(w.n_heads, 10)
+        if w.template[0] == "regular":
+            paths = m.medusa_tree_regular(w.template[1])
+        else:
+            paths = m.medusa_tree_greedy(acc[:, :w.template[2]], w.template[1])
+        tmpl = m.Template(paths, w.topk, w.n_heads, device=dev)
+        N = tmpl.n_rows
+        q, k, v = synth.tree_qkv(w, N, device=dev)
+        lengths = synth.prefix_lengths(w)
+        L = torch.tensor(lengths, dtype=torch.int32, device=dev)
+        gen = torch.Generator(device=dev).manual_seed(w.seed)
+        if w.page_size:
+            lay = synth.paged_layout(w, lengths, N)
+            K = torch.randn((lay.n_pages, w.n_kv_heads, 16, w.head_dim), generator=gen, device=dev).to(w.torch_dtype)
+            cache_bt = torch.tensor(lay.block_table, dtype=torch.int32, device=dev)
+        else:
+            cap = int(lengths.max()) + N + 16
+            K = torch.randn((w.batch, w.n_kv_heads, cap, w.head_dim), generator=gen, device=dev).to(w.torch_dtype)
+            cache_bt = None
+        V = torch.randn(K.shape, generator=gen, device=dev).to(w.torch_dtype)
+        cache = m.KVCache(K, V, block_table=cache_bt)
+        out = torch.empty((w.batch, N, w.n_q_heads, w.head_dim), dtype=torch.float32, device=dev)
+        call = lambda: m.medusa_tree_attn_verify(tmpl, q, k, v, cache, L, int(lengths.max()), rope_base=w.rope_base,
+                                                 out=out)
+    for _ in range(args.warmup):
+        call()
+    torch.cuda.synchronize(dev)
+    ms = time_loop(call, args.steps, torch.cuda.current_stream(dev))
+    print(json.dumps({"stage": args.stage, "workload": w.name, "calls": args.steps, "us_per_call": 1e3 * ms / args.steps}))
+
+
 # ----------------------------------------------------------------------------- main
 
 def main():
@@ -807,11 +855,15 @@ def main():
     ap.add_argument("--impl", default="native", choices=["native", "reference"])
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-per-workload", action="store_true", help="measure the headline workload only")
+    ap.add_argument("--stage", default="round", choices=["round", "heads", "attn"],
+                    help="time one step alone (for single-kernel profiles) instead of the round")
     ap.add_argument("--oracle-sample", default=None, help=argparse.SUPPRESS)
     ap.add_argument("--oracle-v-rows", type=int, default=BASELINE_V_ROWS, help=argparse.SUPPRESS)
     args = ap.parse_args()
     if args.oracle_sample:
         return run_oracle_sample(args)
+    if args.stage != "round":
+        return run_stage(args)
     args.warmup = max(args.warmup, 3)
     if args.impl == "reference":
         return run_reference(args)
