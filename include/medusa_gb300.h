@@ -92,7 +92,7 @@ typedef int32_t medusa_dtype;
  * medusa_tree_upload).  Device calls take the device form.
  *
  * Per-sequence templates ([M7.2] §0x07D: sequences of a batch may verify different
- * trees; [CN] notes that the best tree moves with the context length): when per_seq
+ * trees; [CN] "局限与适用场景": the best node count moves with the context length): when per_seq
  * is not NULL it points to a device array of B device-form templates, one per
  * sequence (each with per_seq NULL and the batch's topk), and the counts of this
  * struct are bounds over them (n_rows, n_words, max_depth, n_paths and n_internal at

@@ -1,6 +1,6 @@
 // Greedy tree templates built on the GPU, one per sequence ([M7.2] §0x04C, [PartII] Part 3
-// "grow a prefix-closed tree under a budget"; [CN] notes that the best tree moves with the
-// context, so a serving loop rebuilds trees from per-context rank accuracies).
+// "grow a prefix-closed tree under a budget"; [CN] "局限与适用场景": the best node count moves
+// with the context length, so a serving loop rebuilds trees from per-context rank accuracies).
 //
 // One CTA per sequence runs the frontier search and then compiles the chosen paths into
 // the template arrays of medusa_tree_compile, in the same layout and canonical order:

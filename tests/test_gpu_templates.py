@@ -1,7 +1,8 @@
 """Per-sequence templates and trees built on the GPU.
 
 [M7.2] §0x07D leaves a batch whose sequences verify different trees to continuous
-batching, and [CN] notes that the best tree moves with the context; the library takes
+batching, and [CN] "局限与适用场景" notes that the best tree size moves with the context
+length; the library takes
 one template per sequence (a TemplateBatch: the shared descriptor's counts become
 bounds and each sequence reads its own template from device memory), and builds the
 greedy tree of each sequence's rank accuracies on the GPU
