@@ -346,24 +346,38 @@ __global__ void __launch_bounds__(kLThreads, 1)
     // (the stage buffers are free: the last accumulator was complete, so every copy and
     // MMA has finished)
     // (after a failure copies may still be landing: the statistics are void anyway)
-    RowPart* mg = reinterpret_cast<RowPart*>(sm);      // [4][kLMaxCols]
+    // One array per statistic ([4][kLMaxCols] each): a warp's stores and a thread's
+    // loads touch consecutive 4-byte words, free of bank conflicts.
+    float* mg_m = reinterpret_cast<float*>(sm);
+    float* mg_z = mg_m + 4 * kLMaxCols;
+    float* mg_s1 = mg_z + 4 * kLMaxCols;
+    float* mg_av = mg_s1 + 4 * kLMaxCols;
+    int* mg_ai = reinterpret_cast<int*>(mg_av + 4 * kLMaxCols);
     const bool intact = *abortp == 0;
 #pragma unroll
     for (int ch = 0; ch < kLMaxCols / 32; ++ch) {
       if (32 * ch >= NM || !intact) break;
-      RowPart r;
-      r.m = st_m[ch];
-      r.z = st_z[ch];
-      r.s1 = st_s1[ch];
-      r.amax_v = st_av[ch];
-      r.amax_i = st_ai[ch];
-      mg[q * kLMaxCols + 32 * ch + lane] = r;
+      const int e = q * kLMaxCols + 32 * ch + lane;
+      mg_m[e] = st_m[ch];
+      mg_z[e] = st_z[ch];
+      mg_s1[e] = st_s1[ch];
+      mg_av[e] = st_av[ch];
+      mg_ai[e] = st_ai[ch];
     }
     asm volatile("bar.sync 1, 128;" ::: "memory");   // the four epilogue warps
     for (int c = (warp - 2) * 32 + lane; intact && c < n_cols; c += 128) {
       float m = -INFINITY, z = 0.f, s1 = 0.f, av = -INFINITY;
       int ai = INT_MAX;
-      for (int w = 0; w < 4; ++w) lm_merge(m, z, s1, av, ai, mg[w * kLMaxCols + c]);
+      for (int w = 0; w < 4; ++w) {
+        const int e = w * kLMaxCols + c;
+        RowPart r;
+        r.m = mg_m[e];
+        r.z = mg_z[e];
+        r.s1 = mg_s1[e];
+        r.amax_v = mg_av[e];
+        r.amax_i = mg_ai[e];
+        lm_merge(m, z, s1, av, ai, r);
+      }
       RowPart out;
       out.m = m;
       out.z = z;

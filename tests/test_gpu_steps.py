@@ -195,6 +195,50 @@ def test_attn_every_shape_and_split_count(m, monkeypatch, shape, splits):
     attn_case(m, w, otree.greedy_tree(acc, 63), lengths, paged=True, fill_tail=float("nan"))
 
 
+@pytest.mark.parametrize("shape", ["1,2", "2,2"])
+@pytest.mark.parametrize("splits", [1, 3])
+def test_attn_rising_scores_rescale(m, monkeypatch, shape, splits):
+    """Prefix scores that rise by about 12 (log2 units) every 64 keys: the row max of every
+    half of a 128-key tile exceeds the running reference by more than 2^8, so the online
+    softmax raises its reference again and again (rescaling O, l and, in the second half
+    of a tile, the P already written).  The rise comes from dimension 63 of the queries
+    and prefix keys (the lowest-frequency rotary pair, which barely turns at these
+    positions); the last keys dominate the tree block, and the scores stay small enough
+    for the fp16 operands."""
+    monkeypatch.setenv("MEDUSA_ATTN_TC_SHAPE", shape)
+    monkeypatch.setenv("MEDUSA_ATTN_TC_SPLITS", str(splits))
+    w = synth.small_variant(synth.WORKLOADS["llama3-8b-256"], batch=2, n_q_heads=8, n_kv_heads=2,
+                            prefix_len=700, seed=77)
+    acc = synth.rank_accuracy(4, 10)
+    t_g, t_o = make_template(m, otree.greedy_tree(acc, 40), w.topk)
+    N = t_o.n_rows
+    lengths = np.array([704, 700])
+    q, k, v = synth.tree_qkv(w, N)
+    ks, vs = synth.prefix_kv(w, lengths)
+    c = w.head_dim ** -0.5 * np.log2(np.e)               # score (log2 units) per unit of q . k
+    q[..., 63], q[..., 127] = 8.0, 0.0
+    for b, L in enumerate(lengths):
+        level = -112.0 + 12.0 * (np.arange(L) // 64)      # log2 units, rising per 64 keys to +8
+        ks[b][:, :, 63] = torch.as_tensor(level / (8.0 * c), dtype=torch.float64).to(ks[b].dtype)
+        ks[b][:, :, 127] = 0.0
+    cap = int(lengths.max()) + N + 16
+    K = torch.zeros((w.batch, w.n_kv_heads, cap, w.head_dim), dtype=w.torch_dtype)
+    V = torch.zeros_like(K)
+    for b, L in enumerate(lengths):
+        K[b, :, :L], V[b, :, :L] = ks[b], vs[b]
+    cache = m.KVCache(K.cuda(), V.cuda())
+    out, lse, status = m.medusa_tree_attn_verify(t_g, q.cuda(), k.cuda(), v.cuda(), cache,
+                                                 gu.device_tensor(lengths, torch.int32), int(lengths.max()),
+                                                 rope_base=w.rope_base, want_lse=True)
+    torch.cuda.synchronize()
+    assert (status.cpu().numpy() == 0).all()
+    for b, L in enumerate(lengths):
+        o_out, o_lse, _ = oatt.tree_attention(gu.to64(q[b]), gu.to64(k[b]), gu.to64(v[b]), gu.to64(ks[b]),
+                                              gu.to64(vs[b]), int(L), t_o.depth, t_o.mask, w.rope_base)
+        gu.float_parity(out[b], o_out, False, f"attn out b={b}")
+        gu.float_parity(lse[b], o_lse, False, f"lse b={b}")
+
+
 def test_attn_head_dim_64_bf16(m):
     w = synth.small_variant(synth.WORKLOADS["vicuna7b-64"], n_q_heads=8, n_kv_heads=2, head_dim=64,
                             prefix_len=513, seed=61)
