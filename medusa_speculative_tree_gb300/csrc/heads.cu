@@ -600,13 +600,11 @@ HeadsPlan plan_heads(int T, int d, int V, int K, int topk) {
   off = align_up(off + (size_t)T * (K + 1) * V * sizeof(float), 256);
   p.off_scand = off;                                       // weight-stream path: per-CTA lists
   off = align_up(off + (size_t)(K + 1) * kHeadsStreamMaxGrid * topk * sizeof(Cand), 256);
-  // tensor-core path: input rows of one pass (bf16 pairs of at most kHeadsMmaMaxRows
-  // rows, or wide: single rows, at most kHeadsMmaWideRows)
+  // tensor-core path: z of one pass (bf16 pairs of at most kHeadsMmaMaxRows rows, or
+  // wide: single fp16 rows, at most kHeadsMmaWideRows); h is read in place
   const bool wide = heads_mma_wide(T);
   const int per_pass = wide ? kHeadsMmaWideRows : kHeadsMmaMaxRows;
   const int Tp = T < per_pass ? T : per_pass;
-  p.off_hhl = off;
-  off = align_up(off + (T >= 2 ? heads_mma_rows(Tp, wide) * d * 2 : 0), 256);
   p.off_zhl = off;
   off = align_up(off + (T >= 2 ? (size_t)K * heads_mma_rows(Tp, wide) * d * 2 : 0), 256);
   p.off_cand = off;                                        // top-k: per-span sorted lists

@@ -5,29 +5,32 @@
 // With T >= 2 rows (batched serving: one frontier row per sequence) each weight row
 // meets T inputs, which the CUDA cores can no longer absorb at HBM speed; the weight
 // stream becomes a skinny GEMM: D[r][n] = sum_k W[r][k] X[n][k] for 128-row groups of
-// W (the M of the MMA) against N = 2T input rows (rounded up to 32).  The input rows are bf16 pairs: row
-// 2t holds bf16(x_t), row 2t + 1 holds bf16(x_t - bf16(x_t)), so the sum of the two
-// columns carries x_t to ~2^-16 relative (h itself is bf16: its second part is 0).
+// W (the M of the MMA) against the input rows.  h is exactly bf16, so W1 h and W_LM h
+// take the T rows of h as they are (N = T rounded up to 16; the rows past T are the
+// copy's zero fill).  z is not: its rows are bf16 pairs (N = 2T rounded up to 32), row
+// 2t holding bf16(z_t) and row 2t + 1 bf16(z_t - bf16(z_t)), so the sum of the two
+// columns carries z_t to ~2^-16 relative.  Columns past the used rows are never read.
 //
 // Passes of more than 128 rows (up to 256: the all-rows variant) would need 512 input
 // columns as pairs, more than one MMA takes.  They run "wide" instead: the input rows are
 // single (h is exactly bf16; z is stored as fp16, ~2^-11 relative) and the W2 tiles are
 // re-encoded in shared memory from bf16 to fp16 (exact for |w| in [2^-14, 65504]) by
-// four converter warps, so that W2 z is one fp16 MMA; W1 h and W_LM h stay bf16 MMAs.
+// four converter warps, so that W2 z is one fp16 MMA; W1 h and W_LM h stay bf16 MMAs
+// on the rows of h.
 // A pass then reads the weights once for twice as many rows.
 //
 // One persistent CTA per SM (cooperative launch) takes 128-row groups from a global
 // counter in stream order: W1_0..W1_{K-1}, the first half of W_LM, W2_0..W2_{K-1}, the
 // rest of W_LM.
 //   - warp 0 (one lane): TMA producer.  Each stage holds up to four 64-column K chunks
-//     of the group (128 x 64 bf16, 16 KiB each) and of the inputs (N x 64 bf16), both
-//     K-major with the 128-byte swizzle; W2 stages wait until every W1 group has
-//     written z;
+//     of the group (128 x 64 bf16, 16 KiB each) and of the inputs (rows of h or of z,
+//     x 64 bf16), both K-major with the 128-byte swizzle; W2 stages wait until every W1
+//     group has written z;
 //   - warp 1: owns TMEM; one lane issues tcgen05.mma (kind::f16, bf16 in, fp32 out)
-//     into one of two TMEM accumulators of N columns;
+//     into one of two TMEM accumulators;
 //   - warps 2-5: epilogue, thread = output row (TMEM lane).  A W1 row writes
-//     z_k = h + SiLU(W1_k h + b1_k) for every input row as a bf16 pair; a vocabulary
-//     row writes its T logits.  Top-k then runs on the logits.
+//     z_k = h + SiLU(W1_k h + b1_k) for every input row (a bf16 pair, or fp16 when
+//     wide); a vocabulary row writes its T logits.  Top-k then runs on the logits.
 // All waits are bounded; on a timeout the call records an error (the top-k merge then
 // writes -1).
 #include <cuda_fp16.h>
@@ -50,7 +53,8 @@ constexpr int kMKc = 64;                     // K columns per stage (one 128-byt
 struct MmaArgs {
   const uint16_t* h;          // [T][d] bf16
   const uint16_t* b1;         // [K][d] or null
-  int d, V, K, T, N;          // N = input rows of the MMA (2T, or T when wide, rounded up to 32)
+  int d, V, K, T, N;          // N = input rows of z (2T, or T when wide, rounded up to 32)
+  int NH;                     // input rows of h (T rounded up to 16)
   int w2_shared;              // W2 heads share one matrix
   uint16_t* z_hl;             // [K][N][d] bf16 pairs of z, or (wide) fp16 z
   float* logits;              // [T][K + 1][V]
@@ -121,7 +125,8 @@ __global__ void __launch_bounds__(WIDE ? kMThreadsWide : kMThreads, 1)
                      const __grid_constant__ CUtensorMap tmZ, const MmaArgs a) {
   extern __shared__ uint8_t smem_m[];
   uint8_t* sm = reinterpret_cast<uint8_t*>((reinterpret_cast<uintptr_t>(smem_m) + 1023) & ~uintptr_t(1023));
-  const int S = a.n_stages, N = a.N, d = a.d, K = a.K, V = a.V, T = a.T;
+  const int S = a.n_stages, N = a.N, NH = a.NH, d = a.d, K = a.K, V = a.V, T = a.T;
+  const int NA = N > NH ? N : NH;                    // accumulator columns (and B box rows of a stage)
   uint64_t* bars = reinterpret_cast<uint64_t*>(sm + (size_t)S * a.stage_bytes);
   __shared__ uint32_t tmem_slot;
   __shared__ int abort_flag;
@@ -141,8 +146,8 @@ __global__ void __launch_bounds__(WIDE ? kMThreadsWide : kMThreads, 1)
   const int n_items = L.total();
   const int bps = a.bps;
   const int n_k = d / (kMKc * bps);                  // stages per group
-  const uint32_t a_bytes = kMRows * kMKc * 2, b_bytes = (uint32_t)N * kMKc * 2;   // one box each
-  const uint32_t tmem_cols = (uint32_t)(2 * N <= 32 ? 32 : 2 * N <= 64 ? 64 : 2 * N <= 128 ? 128 : 2 * N <= 256 ? 256 : 512);
+  const uint32_t a_bytes = kMRows * kMKc * 2, b_bytes = (uint32_t)NA * kMKc * 2;   // one box slot each
+  const uint32_t tmem_cols = (uint32_t)(2 * NA <= 32 ? 32 : 2 * NA <= 64 ? 64 : 2 * NA <= 128 ? 128 : 2 * NA <= 256 ? 256 : 512);
 
   if (threadIdx.x == 0) {
     abort_flag = 0;
@@ -216,7 +221,7 @@ __global__ void __launch_bounds__(WIDE ? kMThreadsWide : kMThreads, 1)
           // A boxes (weights) first, then B boxes (inputs), bps of each
           const uint32_t sA = smem_u32(sm + (size_t)s * a.stage_bytes), sB = sA + bps * a_bytes;
           const uint32_t bar = full0 + 8 * s;
-          mbar_expect_tx(bar, a.stage_bytes);
+          mbar_expect_tx(bar, (uint32_t)bps * (a_bytes + (uint32_t)(it.kind == 2 ? N : NH) * kMKc * 2));
           const int r0 = it.grp * kMRows;
           for (int bx = 0; bx < bps; ++bx) {
             const int col = (kc * bps + bx) * kMKc;
@@ -237,9 +242,9 @@ __global__ void __launch_bounds__(WIDE ? kMThreadsWide : kMThreads, 1)
   } else if (warp == 1) {
     // ---- MMA issue: one group = n_k stages into accumulator g & 1 ------------------------
     if (lane == 0) {
-      const uint32_t idesc_b = idesc_bf16(kMRows, N);
-      const uint32_t idesc_h = idesc_f16(kMRows, N, false);
-      uint32_t idesc = idesc_b;
+      const uint32_t idesc_z = WIDE ? idesc_f16(kMRows, N, false) : idesc_bf16(kMRows, N);
+      const uint32_t idesc_x = idesc_bf16(kMRows, NH);            // W1 h, W_LM h
+      uint32_t idesc = idesc_x;
       int u = 0;
       for (int g = 0; ok; ++g) {
         const int db = g & 1;
@@ -259,14 +264,14 @@ __global__ void __launch_bounds__(WIDE ? kMThreadsWide : kMThreads, 1)
             }
             dgrp[db] = idx;
             __threadfence_block();
-            idesc = (WIDE && mmap_item(idx, L).kind == 2) ? idesc_h : idesc_b;
+            idesc = mmap_item(idx, L).kind == 2 ? idesc_z : idesc_x;
           }
           tc_fence_after();
           const uint32_t sA = smem_u32(sm + (size_t)s * a.stage_bytes), sB = sA + bps * a_bytes;
           for (int bx = 0; bx < bps; ++bx) {
 #pragma unroll
             for (int kk = 0; kk < kMKc / 16; ++kk)
-              umma_f16(tmem + (uint32_t)(db * N), sw128_desc(sA + bx * a_bytes + kk * 32, 16, 1024),
+              umma_f16(tmem + (uint32_t)(db * NA), sw128_desc(sA + bx * a_bytes + kk * 32, 16, 1024),
                        sw128_desc(sB + bx * b_bytes + kk * 32, 16, 1024), idesc, (kc > 0 || bx > 0 || kk > 0) ? 1u : 0u);
           }
           umma_commit(empty0 + 8 * s);                   // the stage is free once these MMAs are done
@@ -307,51 +312,49 @@ __global__ void __launch_bounds__(WIDE ? kMThreadsWide : kMThreads, 1)
       const MItem it = mmap_item(idx, L);
       const int n_rows = it.kind == 0 ? d : V;
       const int row = it.grp * kMRows + r;
-      for (int c0 = 0; c0 < N; c0 += 32) {
+      // one accumulator column per input row, except z's bf16 pairs (two columns)
+      const bool single = WIDE || it.kind != 2;
+      const int ncol = it.kind == 2 ? N : NH;
+      bool bad = false;
+      auto emit = [&](int t, float x) {
+        if (it.kind == 0) {
+          float zv = x;
+          if (a.b1) zv += Elem<uint16_t>::load(a.b1, (int64_t)it.k * d + row);
+          const float z = Elem<uint16_t>::load(a.h, (int64_t)t * d + row) + zv / (1.f + expf(-zv));
+          if (WIDE) {
+            const __half zh = __float2half_rn(z);
+            bad |= !(fabsf(z) <= 65504.f);             // z outside fp16's range (or not finite)
+            a.z_hl[((int64_t)it.k * N + t) * d + row] = __half_as_ushort(zh);
+          } else {
+            const uint16_t hi = f32_to_bf16_bits(z);
+            const uint16_t lo = f32_to_bf16_bits(z - __uint_as_float((uint32_t)hi << 16));
+            a.z_hl[((int64_t)it.k * N + 2 * t) * d + row] = hi;
+            a.z_hl[((int64_t)it.k * N + 2 * t + 1) * d + row] = lo;
+          }
+        } else {
+          const int m = it.kind == 1 ? 0 : 1 + it.k;
+          a.logits[((int64_t)t * (K + 1) + m) * V + row] = x;
+        }
+      };
+      for (int c0 = 0; c0 < ncol; c0 += 32) {
         float v[32];
-        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(db * N + c0), v);
-        if (WIDE && row < n_rows) {
-          // single input columns: column t is row t
-          bool bad = false;
+        tmem_ld32(tmem + ((uint32_t)(32 * q) << 16) + (uint32_t)(db * NA + c0), v);
+        if (row >= n_rows) continue;
+        if (single) {
 #pragma unroll
           for (int j = 0; j < 32; ++j) {
-            const int t = c0 + j;
-            if (t >= T) break;
-            const float x = v[j];
-            if (it.kind == 0) {
-              float zv = x;
-              if (a.b1) zv += Elem<uint16_t>::load(a.b1, (int64_t)it.k * d + row);
-              const float z = Elem<uint16_t>::load(a.h, (int64_t)t * d + row) + zv / (1.f + expf(-zv));
-              const __half zh = __float2half_rn(z);
-              bad |= !(fabsf(z) <= 65504.f);           // z outside fp16's range (or not finite)
-              a.z_hl[((int64_t)it.k * N + t) * d + row] = __half_as_ushort(zh);
-            } else {
-              const int m = it.kind == 1 ? 0 : 1 + it.k;
-              a.logits[((int64_t)t * (K + 1) + m) * V + row] = x;
-            }
+            if (c0 + j >= T) break;
+            emit(c0 + j, v[j]);
           }
-          if (bad) atomicExch(a.err, 1);
-        } else if (row < n_rows) {
+        } else {
 #pragma unroll
           for (int j = 0; j < 16; ++j) {
-            const int t = c0 / 2 + j;
-            if (t >= T) break;
-            const float x = v[2 * j] + v[2 * j + 1];
-            if (it.kind == 0) {
-              float zv = x;
-              if (a.b1) zv += Elem<uint16_t>::load(a.b1, (int64_t)it.k * d + row);
-              const float z = Elem<uint16_t>::load(a.h, (int64_t)t * d + row) + zv / (1.f + expf(-zv));
-              const uint16_t hi = f32_to_bf16_bits(z);
-              const uint16_t lo = f32_to_bf16_bits(z - __uint_as_float((uint32_t)hi << 16));
-              a.z_hl[((int64_t)it.k * N + 2 * t) * d + row] = hi;
-              a.z_hl[((int64_t)it.k * N + 2 * t + 1) * d + row] = lo;
-            } else {
-              const int m = it.kind == 1 ? 0 : 1 + it.k;
-              a.logits[((int64_t)t * (K + 1) + m) * V + row] = x;
-            }
+            if (c0 / 2 + j >= T) break;
+            emit(c0 / 2 + j, v[2 * j] + v[2 * j + 1]);
           }
         }
       }
+      if (bad) atomicExch(a.err, 1);
       tc_fence_before();
       __syncwarp();
       if (lane == 0) mbar_arrive(dempty0 + 8 * db);
@@ -384,29 +387,22 @@ __global__ void __launch_bounds__(WIDE ? kMThreadsWide : kMThreads, 1)
   }
 }
 
-// Input rows as bf16 pairs: H[2t] = h_t, H[2t + 1] = 0 (h is bf16), padding rows 0;
-// the padding rows of every z_k are cleared too.  Wide: H[t] = h_t (single rows).
-__global__ void heads_mma_prep_kernel(const uint16_t* __restrict__ h, int T, int d, int N, int K, int wide,
-                                      uint16_t* __restrict__ h_hl, uint16_t* __restrict__ z_hl) {
-  const int i = blockIdx.x * blockDim.x + threadIdx.x;
-  if (i >= d) return;
-  const int used = wide ? T : 2 * T;
-  for (int n = 0; n < N; ++n) {
-    uint16_t v = 0;
-    if (wide) v = n < T ? h[(int64_t)n * d + i] : 0;
-    else v = (n < 2 * T && (n & 1) == 0) ? h[(int64_t)(n >> 1) * d + i] : 0;
-    h_hl[(int64_t)n * d + i] = v;
-  }
-  for (int k = 0; k < K; ++k)
-    for (int n = used; n < N; ++n) z_hl[((int64_t)k * N + n) * d + i] = 0;
-}
-
 }  // namespace
 
 size_t heads_mma_rows(int T, bool wide) {
   if (wide) return (size_t)((T + 31) / 32 * 32);                     // single rows
   return (size_t)((2 * T + 31) / 32 * 32);                           // bf16 pairs
 }
+
+namespace {
+// Rows of h as the MMA input (16 per instruction step) and the larger of the two row
+// counts, which sizes the stage slots and the accumulators.
+int heads_mma_h_rows(int T) { return (T + 15) / 16 * 16; }
+int heads_mma_acc_rows(int T, bool wide) {
+  const int N = (int)heads_mma_rows(T, wide), NH = heads_mma_h_rows(T);
+  return N > NH ? N : NH;
+}
+}  // namespace
 
 namespace {
 // A stage holds bps boxes of weights (128 x 64) and of inputs (N x 64): as many K
@@ -470,14 +466,14 @@ bool heads_mma_supported(int T, int d, int V, int K, medusa_dtype dt, const void
   int dev = 0, coop = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return false;
   cudaDeviceGetAttribute(&coop, cudaDevAttrCooperativeLaunch, dev);
-  const int N = (int)heads_mma_rows(T, wide);
-  if (coop == 0 || mma_stages(N, d) < 2) return false;
+  const int NA = heads_mma_acc_rows(T, wide);
+  if (coop == 0 || mma_stages(NA, d) < 2) return false;
   auto kern = wide ? heads_mma_kernel<true> : heads_mma_kernel<false>;
-  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mma_smem(N, d)) != cudaSuccess)
+  if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)mma_smem(NA, d)) != cudaSuccess)
     return false;
   int per_sm = 0;
   if (cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, wide ? kMThreadsWide : kMThreads,
-                                                    mma_smem(N, d)) != cudaSuccess)
+                                                    mma_smem(NA, d)) != cudaSuccess)
     return false;
   return per_sm >= 1;
 }
@@ -487,35 +483,31 @@ cudaError_t launch_heads_mma(const HeadsPlan& p, bool wide, const void* h, const
                              cudaStream_t st) {
   char* base = (char*)ws;
   const int T = p.T, d = p.d, V = p.V, K = p.K;
-  const int N = (int)heads_mma_rows(T, wide);
-  uint16_t* h_hl = (uint16_t*)(base + p.off_hhl);
+  const int N = (int)heads_mma_rows(T, wide), NH = heads_mma_h_rows(T), NA = heads_mma_acc_rows(T, wide);
   uint16_t* z_hl = (uint16_t*)(base + p.off_zhl);
   int* err = (int*)(base + p.off_err);
   CUtensorMap mw1, mlm, mw2, mh, mz;
   const bool shared = w2_stride == 0;
   if (!encode_2d(&mw1, w1, d, (uint64_t)K * d, kMRows) || !encode_2d(&mlm, w_lm, d, V, kMRows) ||
       !(shared ? encode_2d(&mw2, w2, d, V, kMRows) : encode_w2(&mw2, w2, d, V, K, w2_stride)) ||
-      !encode_2d(&mh, h_hl, d, N, N) ||
+      !encode_2d(&mh, h, d, T, NH) ||                      // rows past T: the copy's zero fill
       !encode_2d(&mz, z_hl, d, (uint64_t)K * N, N,
                  wide ? CU_TENSOR_MAP_DATA_TYPE_FLOAT16 : CU_TENSOR_MAP_DATA_TYPE_BFLOAT16))
     return cudaErrorInvalidValue;
   MmaArgs a{};
   a.h = (const uint16_t*)h;
   a.b1 = (const uint16_t*)b1;
-  a.d = d; a.V = V; a.K = K; a.T = T; a.N = N;
+  a.d = d; a.V = V; a.K = K; a.T = T; a.N = N; a.NH = NH;
   a.w2_shared = shared ? 1 : 0;
   a.z_hl = z_hl;
   a.logits = logits;
   a.err = err;
   a.cnt = err + 4;
-  a.bps = mma_bps(N, d);
-  a.n_stages = mma_stages(N, d);
-  a.stage_bytes = (uint32_t)mma_stage_bytes(N, a.bps);
+  a.bps = mma_bps(NA, d);
+  a.n_stages = mma_stages(NA, d);
+  a.stage_bytes = (uint32_t)mma_stage_bytes(NA, a.bps);
   cudaError_t e;
-  heads_mma_prep_kernel<<<(d + 255) / 256, 256, 0, st>>>((const uint16_t*)h, T, d, N, K, wide ? 1 : 0, h_hl,
-                                                          z_hl);
-  if ((e = cudaGetLastError()) != cudaSuccess) return e;
-  const size_t smem = mma_smem(N, d);
+  const size_t smem = mma_smem(NA, d);
   auto kern = wide ? heads_mma_kernel<true> : heads_mma_kernel<false>;
   e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
   if (e != cudaSuccess) return e;

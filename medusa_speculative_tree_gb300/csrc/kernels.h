@@ -22,7 +22,7 @@ uint64_t test_stall_ns();
 struct HeadsPlan {
   int T, d, V, K, topk;
   int tokens_per_pass;   // tokens whose fp32 x rows fit in shared memory at once
-  size_t off_z, off_logits, off_scand, off_hhl, off_zhl, off_cand, off_err, bytes;
+  size_t off_z, off_logits, off_scand, off_zhl, off_cand, off_err, bytes;
 };
 // Weight-stream path (heads_stream.cu): at most this many CTAs, and an error flag plus
 // completion counters in the first kHeadsCounterBytes at off_err (zeroed every call).
