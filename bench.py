@@ -279,9 +279,10 @@ def heads_all_rows(rd, stream, peak_tflops):
     """medusa_heads_topk with every tree row as a hidden row (T = B N), the variant in which
     the heads are a tensor-core contraction.  `frac` is the method's useful rate, 2 T
     flops per weight element, over the bf16 peak.  bf16 with 2 <= T <= 128 runs on the
-    tensor cores with every input row as a bf16 pair (hi, lo), so the MMAs execute twice
-    the useful flops; more rows run wide passes of up to 256 single rows (z in fp16),
-    which execute the useful flops.  The executed rate is reported beside the useful one."""
+    tensor cores with W1 h and W_LM h on the rows of h and W2 z on z as bf16 pairs (hi,
+    lo), so the W2 MMAs execute twice the useful flops; more rows run wide passes of up
+    to 256 single rows (z in fp16), which execute the useful flops.  The executed rate is
+    reported beside the useful one."""
     w = rd.w
     T = w.batch * rd.N                                  # every tree row of every sequence
     h = synth.normal((T, w.hidden), 1.0, w.seed, "h", rd.dev, w.torch_dtype, sub=1)
@@ -295,7 +296,8 @@ def heads_all_rows(rd, stream, peak_tflops):
     useful = 2.0 * T * elems / (us * 1e-6) / 1e12
     mma = w.dtype == "bf16" and T >= 2
     wide = mma and T > 128
-    executed = useful * (2 if mma and not wide else 1)
+    w2_share = rd.w2.numel() / elems
+    executed = useful * ((1.0 + w2_share) if mma and not wide else 1.0)
     passes = (math.ceil(T / 256) if wide else math.ceil(T / 128)) if mma else 1
     return {"T": T, "us": us, "useful_tflops": useful, "executed_tflops": executed,
             "peak_tflops": peak_tflops, "frac": useful / peak_tflops, "executed_frac": executed / peak_tflops,
