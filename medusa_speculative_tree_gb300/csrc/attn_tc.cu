@@ -234,8 +234,9 @@ __device__ __forceinline__ void convert_rotate_tile(uint8_t* tile, int n_valid, 
 //          the softmax works on this one); two CTAs per SM.
 //  QT = 2: KT = 128, one S buffer per query tile; the two tiles alternate on the tensor
 //          cores (S and P V of one tile while the softmax works on the other).  128-key
-//          tiles make the S MMAs 128 wide, which the tensor cores run about twice as
-//          efficiently per key as 64-wide ones.  One CTA per SM.
+//          tiles make the S MMAs 128 wide, which run at the full rate, where 64-wide
+//          ones, with both operands in shared memory, are held to about two thirds
+//          of it by their operand traffic.  One CTA per SM.
 template <int QT, int NS>
 struct TcCfg {
   static constexpr int kKT = 64 * QT;                // keys per tile
