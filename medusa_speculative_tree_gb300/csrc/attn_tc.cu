@@ -273,7 +273,8 @@ struct TcCfg {
   static constexpr int kBarDrain = kBarQReady + 1;           // final commit on the error path
   static constexpr int kBarQFull = kBarQReady + 2;           // query tiles landed
   static constexpr int kBarNever = kBarQReady + 3;           // test hook: never completes
-  static constexpr int kNumBars = kBarQReady + 4;
+  static constexpr int kBarOFinal = kBarQReady + 4;          // QT = 2: every MMA complete (one commit)
+  static constexpr int kNumBars = kBarQReady + 5;
   // the merge reuses the query and stage buffers: [rows][32] float4 O, then (m, l)
   static_assert(QT * kQBytes + NS * kStageBytes >= kRows * (kDH * 4 + 8), "merge buffers do not fit");
 };
@@ -449,6 +450,7 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
     mbar_init(BAR(C::kBarDrain), 1);
     mbar_init(BAR(C::kBarQFull), 1);
     mbar_init(BAR(C::kBarNever), 1);
+    mbar_init(BAR(C::kBarOFinal), 1);
     asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
     // the query tiles first: rows (u, group member) of each tile, 64 dims per copy
     mbar_expect_tx(BAR(C::kBarQFull), kQBytes * QT);
@@ -627,21 +629,23 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
           ok = false;
       }
     } else {
-      // Two query tiles, one S buffer each, in a fixed order with blocking waits:
+      // Two query tiles, one S buffer each, in a fixed order:
       //   S(0, 0), S(1, 0), then for every tile j: P V(0, j), S(0, j + 1), P V(1, j),
       //   S(1, j + 1).
-      // S(q, j + 1) overwrites the P of (q, j), so it waits for P V(q, j) to complete;
-      // while one query tile's softmax runs, the tensor cores work on the other's MMAs.
-      // A K slot is released after the last query tile's S of its tile, a V slot after
-      // the last P V.  Each S / P V barrier completes once per tile: the phase of tile j
-      // is j & 1.  (A fixed order with waits that suspend the thread measured faster
-      // than issuing in readiness order by polling.)
+      // S(q, j + 1) overwrites the P of (q, j) in TMEM.  The MMAs of this one issuing
+      // thread run in the order it issues them, so S(q, j + 1), issued after P V(q, j),
+      // writes those columns only after P V(q, j) has read them: it is issued at once,
+      // and the tensor cores go from one query tile's MMAs to the other's without a
+      // round trip through a completion barrier.  (When S(q, j + 1) lands, every MMA
+      // issued before it has completed, P V(q, j) included: the softmax's rescale of O
+      // relies on that.)  A K slot is released after the last query tile's S of its
+      // tile, a V slot after the last P V; one final commit tells when O is complete.
+      // Each S / P barrier completes once per tile: the phase of tile j is j & 1.
       if (lane == 0) {
         if (!wait_or_abort(BAR(C::kBarQReady), 0, abortp)) ok = false;
         auto issue_s = [&](int q, int j) -> bool {
           const int st = j % NS;
           if (q == 0 && !wait_or_abort(BAR(C::kBarConvK + st), (j / NS) & 1, abortp)) return false;
-          if (j > 0 && !wait_or_abort(BAR(C::kBarODone + q), (j - 1) & 1, abortp)) return false;
           tc_fence_after();
           const uint32_t aK = smem_u32(sm + C::kOffK + st * C::kKBytes);
           const uint32_t sQ = smem_u32(sm + q * kQBytes);
@@ -666,7 +670,6 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
             const uint64_t bd = sw128_desc(aV + kk * 2048, KT * 128, 1024);   // MN-major: dim blocks KT x 128 B apart
             umma_f16_ts(tmem + 256u * q + kTmemO, tmem + 256u * q + 8u * kk, bd, kIdO, (j > 0 || kk > 0) ? 1u : 0u);
           }
-          umma_commit(BAR(C::kBarODone + q));
           if (q == qt_live - 1) umma_commit(BAR(C::kBarEmptyV + st));
           return true;
         };
@@ -679,9 +682,11 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
               if (ok && j + 1 < n_tiles) ok = issue_s(q, j + 1);
             }
           }
-          // O is final once the last P V MMAs have completed.
-          for (int q = 0; q < qt_live && ok; ++q)
-            ok = wait_or_abort(BAR(C::kBarODone + q), (n_tiles - 1) & 1, abortp);
+          // O is final once every MMA issued above has completed.
+          if (ok) {
+            umma_commit(BAR(C::kBarOFinal));
+            ok = wait_or_abort(BAR(C::kBarOFinal), 0, abortp);
+          }
         }
       }
     }
