@@ -566,8 +566,10 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
     // ---- MMA issue ------------------------------------------------------------------
     if constexpr (QT == 1) {
       // S(j) = Q K_j^T into TMEM buffer j & 1 once K_j is converted and the P V MMAs of
-      // tile j - 2, whose P occupied that buffer, have completed; O += P(j) V_j once the
-      // softmax has written P(j) and V_j is converted.  Whichever is ready goes first,
+      // tile j - 2, whose P occupied that buffer, have been issued (this thread's MMAs
+      // run in the order it issues them, so S(j) writes the buffer only after they have
+      // read it); O += P(j) V_j once the softmax has written P(j) and V_j is converted.
+      // Whichever is ready goes first,
       // S before P V when both are; all conditions are tested in one round trip.
       // Completion of P V(j) is signalled on slot j & 1, so that a slot's phase never
       // runs more than one ahead of its waiters.  Every commit covers all MMAs issued
@@ -579,14 +581,14 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
         for (uint32_t spin = 0; ok && jp < n_tiles;) {
           bool did = false;
           // (a test of a tile that does not exist reads a barrier harmlessly and is ignored)
-          const uint32_t tb[8] = {BAR(C::kBarConvK + js % NS), BAR(C::kBarODone + (js & 1)),
+          const uint32_t tb[8] = {BAR(C::kBarConvK + js % NS), BAR(C::kBarConvK + js % NS),
                                   BAR(C::kBarPFull + (jp & 1)), BAR(C::kBarConvV + jp % NS),
                                   BAR(C::kBarConvK + js % NS), BAR(C::kBarConvK + js % NS),
                                   BAR(C::kBarConvK + js % NS), BAR(C::kBarConvK + js % NS)};
-          const uint32_t tp[8] = {(uint32_t)(js / NS) & 1u, (uint32_t)((js - 2) >> 1) & 1u, (uint32_t)(jp >> 1) & 1u,
+          const uint32_t tp[8] = {(uint32_t)(js / NS) & 1u, (uint32_t)(js / NS) & 1u, (uint32_t)(jp >> 1) & 1u,
                                   (uint32_t)(jp / NS) & 1u, 0u, 0u, 0u, 0u};
           const uint32_t ready = mbar_test8(tb, tp);
-          if (js < n_tiles && js <= jp + 1 && (ready & 1u) && (js < 2 || (ready & 2u))) {
+          if (js < n_tiles && js <= jp + 1 && (ready & 1u)) {
             const int st = js % NS, sb = js & 1;
             tc_fence_after();
             const uint32_t aK = smem_u32(sm + C::kOffK + st * C::kKBytes);
@@ -855,9 +857,12 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
     } else {
     // Two query tiles of 128-key tiles, one S buffer each.  When S(q, j) lands, the P V
     // MMAs of (q, j - 1) have completed (S(q, j) was issued after them), so O may be
-    // rescaled at once.  The row's 128 scores are read twice from TMEM, 64 at a time:
-    // once for the max, once for P, which is written as fp16 pairs over the S columns
-    // already read.
+    // rescaled at once.  P is written as fp16 pairs over the S columns already read.
+    // While a row has no reference yet (its first tile with keys) the tile is read twice
+    // from TMEM, 64 scores at a time: once for the max, once for P.  After that each half
+    // is read once: its max is taken from the same registers, and only when it exceeds
+    // the reference by more than 2^8 is the reference raised (rare), which rescales O, l,
+    // the partial sums and the P of the first half already written by the same factor.
     const uint32_t sbase = tmem + lane_base;
     for (int j = 0; ok && qt < qt_live && j < n_tiles; ++j) {
       const bool tree_tile = j >= n_pre;
@@ -887,26 +892,17 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
             for (int c = 0; c < 64; ++c) sv[c] = 64 * h + c < k_valid ? sv[c] : -INFINITY;
           }
         };
-        float mxp[2] = {-INFINITY, -INFINITY};
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          float sv[64];
-          load_half(h, sv);
+        auto max64 = [&](const float* sv) -> float {
+          float m0 = -INFINITY, m1 = -INFINITY;
 #pragma unroll
           for (int c = 0; c < 64; c += 4) {
-            mxp[0] = fmax3(mxp[0], sv[c], sv[c + 1]);
-            mxp[1] = fmax3(mxp[1], sv[c + 2], sv[c + 3]);
+            m0 = fmax3(m0, sv[c], sv[c + 1]);
+            m1 = fmax3(m1, sv[c + 2], sv[c + 3]);
           }
-        }
-        const float mx = fmaxf(mxp[0], mxp[1]);
-        // The TMEM accesses of a rescale are warp-collective: the warp rescales when any
-        // of its rows needs it, the other rows scale by 1.
-        const bool first = (m_run == -INFINITY);
-        const bool need = !first && (mx > m_run + kRescale);
-        if (first) m_run = mx;                           // O holds nothing yet for this row
-        if (__any_sync(0xffffffffu, need)) {
-          const float alpha = need ? fast_exp2(m_run - mx) : 1.f;
-          l_run *= alpha;
+          return fmaxf(m0, m1);
+        };
+        // O *= alpha (per row) in TMEM; warp-collective.
+        auto rescale_o = [&](float alpha) {
 #pragma unroll 1
           for (int q8 = 0; q8 < kDH / 16; ++q8) {
             float ov[16];
@@ -915,16 +911,13 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
             for (int i = 0; i < 16; ++i) ov[i] *= alpha;
             tmem_st16(sbase + kTmemO + 16 * q8, ov);
           }
-          if (need) m_run = mx;
-        }
-        const float mref = (m_run == -INFINITY) ? 0.f : m_run;   // a fully masked row keeps P = 0
-        const float2 nm = make_float2(-mref, -mref);
+        };
         float2 ps[4] = {make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f), make_float2(0.f, 0.f)};
-#pragma unroll 1
-        for (int h = 0; h < 2; ++h) {
-          float sv[64];
-          load_half(h, sv);
-          float pk[32];                            // P as fp16 pairs, key 2i in the low half
+        // P = 2^(s - m_run) of one half as fp16 pairs over S columns [32h, 32h + 32)
+        auto write_p = [&](int h, const float* sv) {
+          const float mref = (m_run == -INFINITY) ? 0.f : m_run;   // a fully masked row keeps P = 0
+          const float2 nm = make_float2(-mref, -mref);
+          float pk[32];                            // key 2i in the low half
 #pragma unroll
           for (int i = 0; i < 32; ++i) {
             const float2 d = __fadd2_rn(make_float2(sv[2 * i], sv[2 * i + 1]), nm);
@@ -932,7 +925,61 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
             ps[i & 3] = __fadd2_rn(ps[i & 3], pp);
             pk[i] = __uint_as_float(pack_half2(pp.x, pp.y));
           }
-          tmem_st32_nowait(sbase + 32u * h, pk);   // over S columns [32h, 32h + 32), already read
+          tmem_st32_nowait(sbase + 32u * h, pk);
+        };
+        if (__any_sync(0xffffffffu, m_run == -INFINITY)) {
+          // no reference yet for some row: the tile's max first
+          float mx = -INFINITY;
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            float sv[64];
+            load_half(h, sv);
+            mx = fmaxf(mx, max64(sv));
+          }
+          const bool first = (m_run == -INFINITY);
+          const bool need = !first && (mx > m_run + kRescale);
+          if (first) m_run = mx;                         // O holds nothing yet for this row
+          if (__any_sync(0xffffffffu, need)) {
+            const float alpha = need ? fast_exp2(m_run - mx) : 1.f;
+            l_run *= alpha;
+            rescale_o(alpha);
+            if (need) m_run = mx;
+          }
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            float sv[64];
+            load_half(h, sv);
+            write_p(h, sv);
+          }
+        } else {
+#pragma unroll 1
+          for (int h = 0; h < 2; ++h) {
+            float sv[64];
+            load_half(h, sv);
+            const float mx = max64(sv);
+            const bool need = mx > m_run + kRescale;
+            if (__any_sync(0xffffffffu, need)) {
+              const float alpha = need ? fast_exp2(m_run - mx) : 1.f;
+              l_run *= alpha;
+#pragma unroll
+              for (int i = 0; i < 4; ++i) ps[i] = make_float2(ps[i].x * alpha, ps[i].y * alpha);
+              rescale_o(alpha);
+              if (h == 1) {                              // the first half's P, already written
+                tmem_wait_st();
+                float pk[32];
+                tmem_ld32(sbase, pk);
+#pragma unroll
+                for (int i = 0; i < 32; ++i) {
+                  const uint32_t w = __float_as_uint(pk[i]);
+                  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w));
+                  pk[i] = __uint_as_float(pack_half2(f.x * alpha, f.y * alpha));
+                }
+                tmem_st32(sbase, pk);
+              }
+              if (need) m_run = mx;
+            }
+            write_p(h, sv);
+          }
         }
         tmem_wait_st();
         const float2 s01 = __fadd2_rn(ps[0], ps[1]), s23 = __fadd2_rn(ps[2], ps[3]);
