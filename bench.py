@@ -270,7 +270,7 @@ class Round:
 
 # DRAM bytes (read + write) of one heads launch, from an ncu capture of the current
 # kernel on that workload; absent for workloads not captured.
-HEADS_TRAFFIC = {"vicuna7b-64": 1_445_265_000 + 4_523_008, "longctx-341": 11_040_000_000 + 6_980_000}
+HEADS_TRAFFIC = {"longctx-341": 11_044_705_792 + 7_362_560}
 # the same for the attention launch (dram__bytes_read.sum + dram__bytes_write.sum)
 ATTN_TRAFFIC = {"vicuna7b-64": 35_210_752 + 0}
 
