@@ -792,8 +792,7 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
       tc_fence_after();
       if (live) {
         float sv[kTcKeys];
-        tmem_ld32(tmem + lane_base + 64u * sb, sv);
-        tmem_ld32(tmem + lane_base + 64u * sb + 32, sv + 32);
+        tmem_ld64(tmem + lane_base + 64u * sb, sv);
         if (tree_tile) {
 #pragma unroll
           for (int c = 0; c < kTcKeys; ++c) sv[c] = ((vis >> c) & 1ull) ? sv[c] : -INFINITY;
@@ -881,8 +880,7 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
       tc_fence_after();
       if (live) {
         auto load_half = [&](int h, float* sv) {     // scores of keys [64h, 64h + 64), masked
-          tmem_ld32(sbase + 64u * h, sv);
-          tmem_ld32(sbase + 64u * h + 32, sv + 32);
+          tmem_ld64(sbase + 64u * h, sv);
           if (tree_tile) {
             const uint64_t vh = h ? vis1 : vis0;
 #pragma unroll
