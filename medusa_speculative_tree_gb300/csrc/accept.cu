@@ -52,31 +52,55 @@ __device__ __forceinline__ void shfl_merge(float& m, float& z, float& s1, float&
   if (ranks_before(ov, oi, av, ai)) { av = ov; ai = oi; }
 }
 
-// Fold a batch of n scaled values y[] (ids i0..i0+n-1, raw values x[]) into the running
-// statistics: argmax of x; for typical acceptance also the max m of y, Z = sum e^{y-m}
-// and S1 = sum e^{y-m} (y - m).
+// 2^x on the MUFU unit (ex2.approx, relative error ~2^-22); 2^-inf = +0.
+__device__ __forceinline__ float exp2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
+
+// Fold a batch of n values x[] (ids i0..i0+n-1, all above the ids this thread folded
+// before) into the running statistics.
+//   greedy:  the argmax of x (ties to the lowest id): the batch max first, its first id
+//            only when it beats the running max.
+//   typical: in base-2 units, y = x * c2 with c2 = log2(e) / T: the max m2 of y,
+//            Z = sum 2^(y - m2) (= sum e^{x/T - m} with m = m2 ln 2) and
+//            S1 = sum 2^(y - m2) (y - m2) (= the natural-unit sum / ln 2).
 template <bool TYP, int NB>
-__device__ __forceinline__ void fold(const float* x, int i0, float inv_temp, float& m, float& z, float& s1,
+__device__ __forceinline__ void fold(const float* x, int i0, float c2, float& m2, float& z, float& s1,
                                      float& av, int& ai) {
+  if (!TYP) {
+    float bm = x[0];
 #pragma unroll
-  for (int e = 0; e < NB; ++e)
-    if (ranks_before(x[e], i0 + e, av, ai)) { av = x[e]; ai = i0 + e; }
-  if (TYP) {
+    for (int e = 1; e < NB; ++e) bm = fmaxf(bm, x[e]);
+    // (a NaN never ranks; an equal value folded before keeps its lower id, unless
+    // nothing has been folded yet: -inf ranks by id like any value)
+    if (bm > av || (bm == av && ai == INT_MAX)) {
+      int k = 0;
+#pragma unroll
+      for (int e = NB - 1; e >= 0; --e)
+        if (x[e] == bm) k = e;
+      av = bm;
+      ai = i0 + k;
+    }
+  } else {
     float y[NB], mb = -INFINITY;
 #pragma unroll
-    for (int e = 0; e < NB; ++e) { y[e] = x[e] * inv_temp; mb = fmaxf(mb, y[e]); }
+    for (int e = 0; e < NB; ++e) { y[e] = x[e] * c2; mb = fmaxf(mb, y[e]); }
     if (z == 0.f) {
-      m = mb;
-    } else if (mb > m) {
-      const float sc = expf(m - mb);
-      s1 = sc * (s1 + (m - mb) * z);
+      m2 = mb;
+    } else if (mb > m2) {
+      const float d0 = m2 - mb;
+      const float sc = exp2_approx(d0);
+      s1 = sc * (s1 + d0 * z);
       z *= sc;
-      m = mb;
+      m2 = mb;
     }
 #pragma unroll
     for (int e = 0; e < NB; ++e) {
-      const float d = y[e] - m;
-      const float ev = expf(d);
+      const float d = y[e] - m2;
+      const float ev = exp2_approx(d);
       z += ev;
       s1 = fmaf(ev, d, s1);
     }
@@ -97,7 +121,8 @@ __global__ void __launch_bounds__(kThreads) row_stats_kernel(medusa_tree_t t, in
   const int u = tb.internal[ii];
   const EL* row = logits + ((int64_t)b * t.n_rows + u) * V;
   const int start = c * chunk, end = min(V, start + chunk);
-  float m = -INFINITY, z = 0.f, s1 = 0.f, av = -INFINITY;
+  const float c2 = inv_temp * kLog2e;
+  float m = -INFINITY, z = 0.f, s1 = 0.f, av = -INFINITY;   // (typical: m and s1 in base 2 until the end)
   int ai = INT_MAX;
   const bool vec = (reinterpret_cast<uintptr_t>(row + start) & 15u) == 0;
   int i = start;
@@ -119,7 +144,7 @@ __global__ void __launch_bounds__(kThreads) row_stats_kernel(medusa_tree_t t, in
         if (q < nvec) {
           float x[EPV];
           Elem<EL>::unpack(raw[l], x);
-          fold<TYP, EPV>(x, start + q * EPV, inv_temp, m, z, s1, av, ai);
+          fold<TYP, EPV>(x, start + q * EPV, c2, m, z, s1, av, ai);
         }
       }
     }
@@ -127,7 +152,11 @@ __global__ void __launch_bounds__(kThreads) row_stats_kernel(medusa_tree_t t, in
   }
   for (int k = i + threadIdx.x; k < end; k += kThreads) {
     float x[1] = {Elem<EL>::load(row, k)};
-    fold<TYP, 1>(x, k, inv_temp, m, z, s1, av, ai);
+    fold<TYP, 1>(x, k, c2, m, z, s1, av, ai);
+  }
+  if (TYP) {                                       // back to natural units
+    m *= kLn2;
+    s1 *= kLn2;
   }
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) shfl_merge(m, z, s1, av, ai, o);
@@ -240,23 +269,8 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
   const bool typ = mode != MEDUSA_ACCEPT_GREEDY;
   const int32_t* tok = tokens + (int64_t)b * NS;
-  if (err && *reinterpret_cast<const volatile int*>(err) != 0) {
-    // the statistics were not completed (a bounded wait gave up): publish nothing
-    if (threadIdx.x == 0) {
-      best_path[b] = -1;
-      accept_len[b] = -1;
-      frontier_row[b] = -1;
-      if (cm.on) {                               // nothing to commit: the cache is untouched
-        cm.status[b] = MEDUSA_EPATH;
-        cm.L_out[b] = cm.L[b];
-      }
-    }
-    for (int j = threadIdx.x; j < WS; j += kSelThreads) {
-      out_rows[(int64_t)b * WS + j] = -1;
-      out_tokens[(int64_t)b * WS + j] = -1;
-    }
-    return;
-  }
+  // (the error flag is read now and tested once the loads below are in flight)
+  const int err_v = err ? *reinterpret_cast<const volatile int*>(err) : 0;
   // 0. the inputs of every edge parent(v) -> v (a thread's edges are v = 1 + tid +
   //    k kSelThreads, k < kEdges since N <= MEDUSA_MAX_ROWS): parent, its internal row,
   //    the candidate token and (typical) its raw logit, all requested up front so that
@@ -285,40 +299,61 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     }
   }
   // 1. merged statistics per internal row (one warp per row, one lane per chunk) and
-  //    the retrieval table into shared memory.  The chunk statistics of every row are
-  //    staged first, four loads per thread in flight, so that the per-row merges do
-  //    not wait on global memory one row after another.
-  if (lay.ret_staged)
-    for (int i = threadIdx.x; i < tq.n_paths * W; i += kSelThreads) s_ret[i] = tq.retrieve[i];
+  //    the retrieval table into shared memory.  The chunk statistics of every row and
+  //    the table are staged first, up to two of each per thread in flight, so that the
+  //    per-row merges do not wait on global memory one row after another.
   const RowPart* part_b = part + (int64_t)b * NIS * n_chunks;
   const float* guard_b = guard ? guard + (int64_t)b * NIS * n_chunks : nullptr;
-  if (lay.part_staged) {
+  {
     RowPart* sp = reinterpret_cast<RowPart*>(smem_sel + lay.off_part);
     float* sg = reinterpret_cast<float*>(sp + NI * n_chunks);
-    const int np = NI * n_chunks;
-    for (int i0 = threadIdx.x; i0 < np; i0 += 4 * kSelThreads) {
-      RowPart q[4];
-      float g4[4];
+    const int np = lay.part_staged ? NI * n_chunks : 0;
+    const int nr = lay.ret_staged ? tq.n_paths * W : 0;
+    for (int i0 = threadIdx.x; i0 < max(np, nr); i0 += 2 * kSelThreads) {
+      RowPart q[2];
+      float g4[2];
+      int rv[2];
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
+      for (int r = 0; r < 2; ++r) {
         const int i = i0 + r * kSelThreads;
         if (i < np) {
           q[r] = part_b[i];
           g4[r] = guard_b ? guard_b[i] : 0.f;
         }
+        if (i < nr) rv[r] = tq.retrieve[i];
       }
 #pragma unroll
-      for (int r = 0; r < 4; ++r) {
+      for (int r = 0; r < 2; ++r) {
         const int i = i0 + r * kSelThreads;
         if (i < np) {
           sp[i] = q[r];
           if (guard_b) sg[i] = g4[r];
         }
+        if (i < nr) s_ret[i] = rv[r];
       }
     }
-    part_b = sp;
-    if (guard_b) guard_b = sg;
+    if (lay.part_staged) {
+      part_b = sp;
+      if (guard_b) guard_b = sg;
+    }
     __syncthreads();
+  }
+  if (err_v != 0) {
+    // the statistics were not completed (a bounded wait gave up): publish nothing
+    if (threadIdx.x == 0) {
+      best_path[b] = -1;
+      accept_len[b] = -1;
+      frontier_row[b] = -1;
+      if (cm.on) {                               // nothing to commit: the cache is untouched
+        cm.status[b] = MEDUSA_EPATH;
+        cm.L_out[b] = cm.L[b];
+      }
+    }
+    for (int j = threadIdx.x; j < WS; j += kSelThreads) {
+      out_rows[(int64_t)b * WS + j] = -1;
+      out_tokens[(int64_t)b * WS + j] = -1;
+    }
+    return;
   }
   for (int ii = warp; ii < NI; ii += kSelWarps) {
     const RowPart* rp = part_b + (int64_t)ii * n_chunks;
@@ -331,8 +366,21 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
       if (guard_b) g += guard_b[(int64_t)ii * n_chunks + c];
     }
     if (typ) {
+      // the row max over the lanes, every lane's partial rescaled to it, then plain sums
+      // (typical needs no argmax)
+      float M = m;
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) shfl_merge(m, z, s1, av, ai, o);
+      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      const float a = z > 0.f ? __expf(m - M) : 0.f;
+      float zz = a * z, ss = z > 0.f ? a * (s1 + (m - M) * z) : 0.f;
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        zz += __shfl_xor_sync(0xffffffffu, zz, o);
+        ss += __shfl_xor_sync(0xffffffffu, ss, o);
+      }
+      m = M;
+      z = zz;
+      s1 = ss;
     } else {                                        // greedy needs the argmax only
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) {
@@ -407,20 +455,30 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   }
   if (lane == 0) { r_a[warp] = best_a; r_s[warp] = best_s; r_p[warp] = best_p; }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int w = 1; w < kSelWarps; ++w)
-      if (better(r_a[w], r_s[w], r_p[w], best_a, best_s, best_p)) {
-        best_a = r_a[w]; best_s = r_s[w]; best_p = r_p[w];
-      }
-    const int32_t* r = lay.ret_staged ? s_ret + best_p * W : tq.retrieve + (int64_t)best_p * W;
-    best_path[b] = best_p;
-    accept_len[b] = best_a;
-    for (int j = 0; j < WS; ++j) {
-      const bool in = j <= best_a;
-      out_rows[(int64_t)b * WS + j] = in ? r[j] : -1;
-      out_tokens[(int64_t)b * WS + j] = in ? tok[r[j]] : -1;
+  static_assert(kSelWarps == 32, "one lane per warp in the final reduction");
+  if (warp == 0) {
+    // the warps' winners, one per lane, reduced by the same comparison (a total order on
+    // (length, score, path id)); then the lanes publish the rows in parallel
+    best_a = r_a[lane]; best_s = r_s[lane]; best_p = r_p[lane];
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const int oa = __shfl_xor_sync(0xffffffffu, best_a, o);
+      const float os = __shfl_xor_sync(0xffffffffu, best_s, o);
+      const int op = __shfl_xor_sync(0xffffffffu, best_p, o);
+      if (better(oa, os, op, best_a, best_s, best_p)) { best_a = oa; best_s = os; best_p = op; }
     }
-    frontier_row[b] = r[best_a];
+    const int32_t* r = lay.ret_staged ? s_ret + best_p * W : tq.retrieve + (int64_t)best_p * W;
+    for (int j = lane; j < WS; j += 32) {
+      const bool in = j <= best_a;
+      const int row = in ? r[j] : -1;
+      out_rows[(int64_t)b * WS + j] = row;
+      out_tokens[(int64_t)b * WS + j] = in ? tok[row] : -1;
+    }
+    if (lane == 0) {
+      best_path[b] = best_p;
+      accept_len[b] = best_a;
+      frontier_row[b] = r[best_a];
+    }
   }
   if (!cm.on) return;
 
