@@ -20,7 +20,7 @@ namespace {
 
 constexpr int kThreads = 256;
 constexpr int kWarps = kThreads / 32;
-constexpr int kLoads = 4;          // 16-byte loads in flight per thread in row_stats
+constexpr int kLoads = 8;          // 16-byte loads in flight per thread in row_stats
 constexpr int kSelThreads = 1024;  // select: one warp per internal row, 32 rows at a time
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kCommitPieces = 2;   // 16-byte pieces a select thread holds while moving rows
@@ -39,17 +39,6 @@ __device__ __forceinline__ void merge_stats(float& m, float& z, float& s1, float
   s1 = a * (s1 + (m - mn) * z) + b * (s12 + (m2 - mn) * z2);
   z = a * z + b * z2;
   m = mn;
-}
-
-// Merge (m, z, s1) and the argmax of another lane into this lane's.
-__device__ __forceinline__ void shfl_merge(float& m, float& z, float& s1, float& av, int& ai, int o) {
-  const float om = __shfl_xor_sync(0xffffffffu, m, o);
-  const float oz = __shfl_xor_sync(0xffffffffu, z, o);
-  const float os = __shfl_xor_sync(0xffffffffu, s1, o);
-  const float ov = __shfl_xor_sync(0xffffffffu, av, o);
-  const int oi = __shfl_xor_sync(0xffffffffu, ai, o);
-  merge_stats(m, z, s1, om, oz, os);
-  if (ranks_before(ov, oi, av, ai)) { av = ov; ai = oi; }
 }
 
 // 2^x on the MUFU unit (ex2.approx, relative error ~2^-22); 2^-inf = +0.
@@ -88,6 +77,7 @@ __device__ __forceinline__ void fold(const float* x, int i0, float c2, float& m2
     float y[NB], mb = -INFINITY;
 #pragma unroll
     for (int e = 0; e < NB; ++e) { y[e] = x[e] * c2; mb = fmaxf(mb, y[e]); }
+    if (mb == -INFINITY) return;                   // every value -inf: adds nothing
     if (z == 0.f) {
       m2 = mb;
     } else if (mb > m2) {
@@ -154,26 +144,56 @@ __global__ void __launch_bounds__(kThreads) row_stats_kernel(medusa_tree_t t, in
     float x[1] = {Elem<EL>::load(row, k)};
     fold<TYP, 1>(x, k, c2, m, z, s1, av, ai);
   }
-  if (TYP) {                                       // back to natural units
-    m *= kLn2;
-    s1 *= kLn2;
-  }
-#pragma unroll
-  for (int o = 16; o > 0; o >>= 1) shfl_merge(m, z, s1, av, ai, o);
+  // Block reduction.  Typical: the max over the threads, every partial rescaled to it,
+  // then plain sums (base 2; natural units in the record).  Greedy: the argmax.
   __shared__ float r_m[kWarps], r_z[kWarps], r_s[kWarps], r_v[kWarps];
   __shared__ int r_i[kWarps];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  auto rescale_sum = [&](float& mm, float& zz, float& ss) {
+    float M = mm;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+    const float a = zz > 0.f ? exp2_approx(mm - M) : 0.f;
+    float zs = a * zz, s1s = zz > 0.f ? a * (ss + (mm - M) * zz) : 0.f;
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      zs += __shfl_xor_sync(0xffffffffu, zs, o);
+      s1s += __shfl_xor_sync(0xffffffffu, s1s, o);
+    }
+    mm = M;
+    zz = zs;
+    ss = s1s;
+  };
+  auto argmax_lanes = [&](float& v, int& i) {
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      const float ov = __shfl_xor_sync(0xffffffffu, v, o);
+      const int oi = __shfl_xor_sync(0xffffffffu, i, o);
+      if (ranks_before(ov, oi, v, i)) { v = ov; i = oi; }
+    }
+  };
+  if (TYP) rescale_sum(m, z, s1);
+  else argmax_lanes(av, ai);
   if (lane == 0) { r_m[warp] = m; r_z[warp] = z; r_s[warp] = s1; r_v[warp] = av; r_i[warp] = ai; }
   __syncthreads();
-  if (threadIdx.x == 0) {
-    for (int w = 1; w < kWarps; ++w) {
-      merge_stats(m, z, s1, r_m[w], r_z[w], r_s[w]);
-      if (ranks_before(r_v[w], r_i[w], av, ai)) { av = r_v[w]; ai = r_i[w]; }
+  if (warp == 0) {
+    const bool w = lane < kWarps;
+    m = w ? r_m[lane] : -INFINITY;
+    z = w ? r_z[lane] : 0.f;
+    s1 = w ? r_s[lane] : 0.f;
+    av = w ? r_v[lane] : -INFINITY;
+    ai = w ? r_i[lane] : INT_MAX;
+    if (TYP) rescale_sum(m, z, s1);
+    else argmax_lanes(av, ai);
+    if (lane == 0) {
+      RowPart p;
+      p.m = TYP ? m * kLn2 : -INFINITY;
+      p.z = TYP ? z : 0.f;
+      p.s1 = TYP ? s1 * kLn2 : 0.f;
+      p.amax_v = av; p.amax_i = ai;
+      p.pad[0] = p.pad[1] = p.pad[2] = 0;
+      part[(((int64_t)b * t.n_internal) + ii) * gridDim.x + c] = p;
     }
-    RowPart p;
-    p.m = m; p.z = z; p.s1 = s1; p.amax_v = av; p.amax_i = ai;
-    p.pad[0] = p.pad[1] = p.pad[2] = 0;
-    part[(((int64_t)b * t.n_internal) + ii) * gridDim.x + c] = p;
   }
 }
 
@@ -355,11 +375,18 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
     }
     return;
   }
-  for (int ii = warp; ii < NI; ii += kSelWarps) {
+  // A row takes lpr lanes (the smallest power of two >= the chunk count, at most 32), so a
+  // warp merges 32 / lpr rows at once; the shuffles stay inside each group of lanes.
+  int lpr = 1;
+  while (lpr < n_chunks && lpr < 32) lpr <<= 1;
+  const int rpw = 32 / lpr, sl = lane & (lpr - 1);
+  for (int ii0 = warp * rpw; ii0 < NI; ii0 += kSelWarps * rpw) {
+    const int ii = ii0 + lane / lpr;
+    const bool row = ii < NI;
     const RowPart* rp = part_b + (int64_t)ii * n_chunks;
     float m = -INFINITY, z = 0.f, s1 = 0.f, av = -INFINITY, g = 0.f;
     int ai = INT_MAX;
-    for (int c = lane; c < n_chunks; c += 32) {
+    for (int c = sl; row && c < n_chunks; c += lpr) {
       const RowPart q = rp[c];
       if (typ) merge_stats(m, z, s1, q.m, q.z, q.s1);
       if (ranks_before(q.amax_v, q.amax_i, av, ai)) { av = q.amax_v; ai = q.amax_i; }
@@ -369,12 +396,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
       // the row max over the lanes, every lane's partial rescaled to it, then plain sums
       // (typical needs no argmax)
       float M = m;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
+      for (int o = lpr >> 1; o > 0; o >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, o));
       const float a = z > 0.f ? __expf(m - M) : 0.f;
       float zz = a * z, ss = z > 0.f ? a * (s1 + (m - M) * z) : 0.f;
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
+      for (int o = lpr >> 1; o > 0; o >>= 1) {
         zz += __shfl_xor_sync(0xffffffffu, zz, o);
         ss += __shfl_xor_sync(0xffffffffu, ss, o);
       }
@@ -382,22 +407,23 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
       z = zz;
       s1 = ss;
     } else {                                        // greedy needs the argmax only
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) {
+      for (int o = lpr >> 1; o > 0; o >>= 1) {
         const float ov = __shfl_xor_sync(0xffffffffu, av, o);
         const int oi = __shfl_xor_sync(0xffffffffu, ai, o);
         if (ranks_before(ov, oi, av, ai)) { av = ov; ai = oi; }
       }
     }
-    if (guard_b) g = warp_sum(g);
-    if (lane == 0 && !typ) s_am[ii] = ai;
-    if (lane == 0 && typ) {
-      const float lz = logf(z);
-      const float H = guard_b ? g : lz - s1 / z;   // -sum p ln p = ln Z - sum p (x/T - m)
-      s_m[ii] = m;
-      s_lz[ii] = lz;
-      s_tau[ii] = fminf(epsilon, delta * expf(-H));
+    if (guard_b)
+      for (int o = lpr >> 1; o > 0; o >>= 1) g += __shfl_xor_sync(0xffffffffu, g, o);
+    if (row && sl == 0) {
       s_am[ii] = ai;
+      if (typ) {
+        const float lz = logf(z);
+        const float H = guard_b ? g : lz - s1 / z;   // -sum p ln p = ln Z - sum p (x/T - m)
+        s_m[ii] = m;
+        s_lz[ii] = lz;
+        s_tau[ii] = fminf(epsilon, delta * expf(-H));
+      }
     }
   }
   __syncthreads();
