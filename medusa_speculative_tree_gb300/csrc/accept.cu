@@ -89,7 +89,10 @@ __device__ __forceinline__ void fold(const float* x, int i0, float c2, float& m2
     }
 #pragma unroll
     for (int e = 0; e < NB; ++e) {
-      const float d = y[e] - m2;
+      // below -128 the term is 0 either way; the clamp keeps a -inf logit's e d at 0
+      // instead of 0 * -inf (a NaN input stays NaN)
+      const float d0 = y[e] - m2;
+      const float d = d0 < -128.f ? -128.f : d0;
       const float ev = exp2_approx(d);
       z += ev;
       s1 = fmaf(ev, d, s1);

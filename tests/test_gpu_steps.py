@@ -326,6 +326,59 @@ def test_accept_planted(m, mode, guard, dt):
     assert max(lens) > 0          # planting produced accepted edges
 
 
+@pytest.mark.parametrize("mode", ["greedy", "typical"])
+@pytest.mark.parametrize("dt", ["f32", "bf16"])
+def test_accept_ties_and_masked_runs(m, mode, dt):
+    """Row statistics at their edge cases, decisions equal to the oracle's: runs of
+    -inf logits (masked vocabulary) covering one whole 16384-logit chunk, whole 16-byte
+    vectors and an unaligned stretch, with planted candidates inside them; and every
+    planted maximum repeated at a second id, lower than the candidate's in half of the
+    rows (the lowest id is the argmax, so greedy must then reject that candidate) and
+    higher in the other half, in another chunk or in the same vector."""
+    w = synth.small_variant(synth.WORKLOADS["vicuna7b-64"], batch=4, vocab=40000, dtype="f32", seed=93)
+    acc = synth.rank_accuracy(4, 10)
+    t_o = otree.compile_template(otree.greedy_tree(acc, 63), 10)
+    t_g = m.Template(t_o.paths[1:], 10, device="cuda")
+    root, pool = synth.random_pool(w)
+    tokens = np.stack([o_fill(t_o, root[b], pool[b], 0)[0] for b in range(w.batch)])
+    logits = synth.target_logits(w, t_o.n_rows)
+    for lo, hi in [(16384, 32768), (1024, 1088), (5003, 5011)]:
+        logits[:, :, lo:hi] = -math.inf
+    synth.plant_argmax(logits, pool, t_o.depth, acc, synth.plant_uniforms(w, t_o.n_rows))
+    n_tied = 0
+    for b in range(w.batch):
+        for u in range(t_o.n_rows):
+            row = logits[b, u]
+            p = int(torch.argmax(row))
+            if p == 0 or p == w.vocab - 1:
+                continue
+            # a second id with the same maximum: below p for even rows, above for odd; in
+            # p's own 16-byte vector when there is room, else in another vector or chunk
+            if u % 2 == 0:
+                q = p - 1 if p % 4 != 0 else p // 2
+            else:
+                q = p + 1 if (p + 1) % 4 != 0 else min(w.vocab - 1, p + 16383)
+            row[q] = row[p]
+            n_tied += 1
+    if dt == "bf16":
+        logits = logits.to(torch.bfloat16)
+    r = m.medusa_tree_accept(t_g, logits.cuda(), gu.device_tensor(tokens, torch.int32), mode,
+                             epsilon=w.epsilon, delta=w.delta)
+    r = {k: v.cpu().numpy() for k, v in r.items()}
+    skipped = 0
+    for b in range(w.batch):
+        o = oacc.accept(gu.to64(logits[b]), tokens[b], t_o.retrieve, mode, 1.0, w.epsilon, w.delta, False)
+        if mode == "typical" and gu.typical_ambiguous(o):
+            skipped += 1
+            continue
+        assert r["accept_len"][b] == o.accept_len, b
+        G = o.accept_len + 1
+        assert list(r["out_rows"][b, :G]) == list(o.out_rows)
+        assert list(r["out_tokens"][b, :G]) == list(o.out_tokens)
+        assert r["best_path"][b] == o.best_path
+    assert skipped <= 1 and n_tied > 0
+
+
 def test_accept_root_only_template(m):
     t_g = m.Template([], 4, device="cuda")
     logits = torch.randn(2, 1, 100, device="cuda")
