@@ -413,7 +413,7 @@ class RoundGraphs:
         w = rd.w
         self.native = rd.m.MedusaRound(rd.tmpl, rd.h, rd.w1, rd.w2, rd.w_lm, w.topk, rd.L, rd.q, rd.k, rd.v,
                                        rd.cache, rd.max_L, rd.logits, mode=rd.mode, rope_base=w.rope_base,
-                                       epsilon=w.epsilon, delta=w.delta)
+                                       epsilon=w.epsilon, delta=w.delta, fuse_commit=True)
         self.stage = {n: torch.cuda.CUDAGraph() for n in self.NAMES}
         with torch.cuda.graph(self.stage["heads"]):
             root, pool = rd.heads()
@@ -452,49 +452,78 @@ class RoundGraphs:
 
 def e2e_loop(rd: Round, steps: int, stream):
     """Same round through the public API with per-step inputs copied from pinned host
-    memory and the published result read back (both inside the timed region).  The
-    frontier rows and lengths are copied first, on the round's stream (the heads and
-    the fill read them); the attention and acceptance inputs follow on a second stream,
-    after the previous step's reads of those buffers, and overlap the heads; the round
-    waits for them before the attention call."""
+    memory and the published result read back (both inside the timed region).  Two
+    rounds (medusa_round_create with the fused commit) are bound to two sets of input
+    buffers and take the steps in turn.  On a second stream, once the round two steps
+    back has finished, its published tokens and L_out are copied to the host and this
+    step's inputs into its set, which overlaps the previous step's round; the step's
+    round waits for those copies.  The last two rounds' results are read back before
+    the timed region closes."""
     w = rd.w
-    h_host = rd.h.cpu().pin_memory()
-    q_host, k_host, v_host = (x.cpu().pin_memory() for x in (rd.q, rd.k, rd.v))
-    lg_host = rd.logits.cpu().pin_memory()
-    L_host = rd.L.cpu().pin_memory()
-    res_host = torch.empty((w.batch, rd.tmpl.max_depth + 2), dtype=torch.int32).pin_memory()
-    h_d, q_d, k_d, v_d, lg_d, L_d = (torch.empty_like(x, device=rd.dev) for x in
-                                     (h_host, q_host, k_host, v_host, lg_host, L_host))
-    h2d = sum(x.numel() * x.element_size() for x in (h_host, q_host, k_host, v_host, lg_host, L_host))
-    d2h = res_host.numel() * res_host.element_size()
-    m = rd.m
-
+    hosts = [x.cpu().pin_memory() for x in (rd.h, rd.L, rd.q, rd.k, rd.v, rd.logits)]
+    sets = [[torch.empty_like(x, device=rd.dev) for x in hosts] for _ in range(2)]
+    for st in sets:
+        for dst, src in zip(st, hosts):
+            dst.copy_(src)
+    rounds = [rd.m.MedusaRound(rd.tmpl, st[0], rd.w1, rd.w2, rd.w_lm, w.topk, st[1], st[2], st[3], st[4], rd.cache,
+                               rd.max_L, st[5], mode=rd.mode, rope_base=w.rope_base, epsilon=w.epsilon,
+                               delta=w.delta, fuse_commit=True) for st in sets]
+    tok_host = [torch.empty_like(r.out_tokens, device="cpu").pin_memory() for r in rounds]
+    L_host = [torch.empty_like(r.L_out, device="cpu").pin_memory() for r in rounds]
+    h2d = sum(x.numel() * x.element_size() for x in hosts)
+    d2h = sum(x.numel() * x.element_size() for x in (tok_host[0], L_host[0]))
     side = torch.cuda.Stream(rd.dev)
-    ready = torch.cuda.Event()
+    ready = [torch.cuda.Event(), torch.cuda.Event()]
+    done = [torch.cuda.Event(), torch.cuda.Event()]
+    launched = [False, False]
+    step = [0]
+
+    def read_back(s):
+        # copies only (no kernel on this stream: the heads kernel holds every SM)
+        tok_host[s].copy_(rounds[s].out_tokens, non_blocking=True)
+        L_host[s].copy_(rounds[s].L_out, non_blocking=True)
 
     def one():
+        s = step[0] & 1
+        step[0] += 1
         main = torch.cuda.current_stream(rd.dev)
-        for dst, src in ((h_d, h_host), (L_d, L_host)):
-            dst.copy_(src, non_blocking=True)
-        side.wait_stream(main)                       # the previous step has read q, k, v, logits
         with torch.cuda.stream(side):
-            for dst, src in ((q_d, q_host), (k_d, k_host), (v_d, v_host), (lg_d, lg_host)):
+            side.wait_event(done[s])                 # the round two steps back has finished
+            if launched[s]:
+                read_back(s)
+            for dst, src in zip(sets[s], hosts):
                 dst.copy_(src, non_blocking=True)
-            ready.record(side)
-        root, pool = m.medusa_heads_topk(h_d, rd.w1, rd.w2, rd.w_lm, w.topk)
-        tokens, _ = m.medusa_tree_fill(rd.tmpl, root, pool, L_d)
-        main.wait_event(ready)
-        m.medusa_tree_attn_verify(rd.tmpl, q_d, k_d, v_d, rd.cache, L_d, rd.max_L, rope_base=w.rope_base,
-                                  out=rd.out, ws=rd.attn_ws)
-        r = m.medusa_tree_accept(rd.tmpl, lg_d, tokens, rd.mode, epsilon=w.epsilon, delta=w.delta)
-        L_out, _ = m.medusa_kv_compact(rd.cache, rd.tmpl, L_d, r["accept_len"], r["out_rows"])
-        res = torch.cat([r["out_tokens"], L_out[:, None]], dim=1)
-        res_host.copy_(res, non_blocking=True)
+            ready[s].record(side)
+        main.wait_event(ready[s])
+        rounds[s].launch(main)
+        launched[s] = True
+        done[s].record(main)
+
+    def finish():
+        main = torch.cuda.current_stream(rd.dev)
+        for s in (step[0] & 1, (step[0] + 1) & 1):
+            if launched[s]:
+                with torch.cuda.stream(side):
+                    side.wait_event(done[s])
+                    read_back(s)
+                launched[s] = False
+        main.wait_stream(side)
 
     for _ in range(3):
         one()
+    finish()
     torch.cuda.synchronize()
-    ms = time_loop(one, steps, stream)
+    start = torch.cuda.Event(enable_timing=True)
+    end = torch.cuda.Event(enable_timing=True)
+    start.record(stream)
+    for _ in range(steps):
+        one()
+    finish()
+    end.record(stream)
+    end.synchronize()
+    ms = start.elapsed_time(end)
+    for r in rounds:
+        r.close()
     return ms / steps, h2d, d2h
 
 
@@ -701,8 +730,10 @@ def config_of(w: synth.Workload, rd):
          "paged": bool(w.page_size), "tree_rows": tree_rows(w),
          "l2": "inputs larger than L2: each step streams the head weights (>= 1.4 GB) before the KV; "
                "stage timings flush L2 with a 512 MB write",
-         "launch": "each step is one medusa_round_launch (the library's CUDA graph of the five calls); "
-                   "e2e calls the five API functions eagerly"}
+         "launch": "each step is one medusa_round_launch (the library's CUDA graph of the five calls, "
+                   "the commit fused into acceptance); e2e alternates two such rounds bound to two input "
+                   "sets, each step's inputs copied from pinned host memory during the previous step's "
+                   "round and its published tokens and L_out copied back"}
     return c
 
 

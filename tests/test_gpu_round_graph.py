@@ -138,7 +138,7 @@ def test_round_graph_with_hidden_state_acceptance(m):
     rnd.close()
 
 
-@pytest.mark.parametrize("name", ["tiny-fp32", "vicuna7b-64", "serving-b16-paged"])
+@pytest.mark.parametrize("name", synth.WORKLOAD_ORDER)
 def test_fused_commit_equals_accept_then_compact(m, name):
     """medusa_tree_accept_commit against medusa_tree_accept + medusa_kv_compact: the
     acceptance outputs, L_out, status and every cache row the same; a sequence whose
