@@ -132,9 +132,11 @@ class ClockSampler:
 # ----------------------------------------------------------------------------- workload
 
 class Round:
-    """Device-resident inputs and outputs of one verify round for a workload."""
+    """Device-resident inputs and outputs of one verify round for a workload.  A bf16
+    cache carries an fp16 mirror (filled once here, as a prefill would; every round's
+    cache writes keep it in step) unless mirror=False."""
 
-    def __init__(self, m, w: synth.Workload, dev):
+    def __init__(self, m, w: synth.Workload, dev, mirror=None):
         self.m, self.w, self.dev = m, w, dev
         acc = synth.rank_accuracy(w.n_heads, 10)
         if w.template[0] == "regular":
@@ -176,6 +178,8 @@ class Round:
                 self.K[b, :, :int(L)] = ks[b]
                 self.V[b, :, :int(L)] = vs[b]
             self.cache = m.KVCache(self.K, self.V)
+        if mirror if mirror is not None else w.dtype == "bf16":
+            self.cache.add_mirror()
         # target logits, argmax planted on the candidates the heads actually propose
         root, pool = m.medusa_heads_topk(self.h, self.w1, self.w2, self.w_lm, w.topk)
         logits = synth.target_logits(w, N)
@@ -402,7 +406,7 @@ class RoundGraphs:
 
     NAMES = ["heads", "fill", "attn", "accept", "compact"]
 
-    def __init__(self, rd: Round, dev):
+    def __init__(self, rd: Round, dev, fuse_commit: bool = False):
         side = torch.cuda.Stream(dev)
         side.wait_stream(torch.cuda.current_stream(dev))
         with torch.cuda.stream(side):
@@ -413,7 +417,7 @@ class RoundGraphs:
         w = rd.w
         self.native = rd.m.MedusaRound(rd.tmpl, rd.h, rd.w1, rd.w2, rd.w_lm, w.topk, rd.L, rd.q, rd.k, rd.v,
                                        rd.cache, rd.max_L, rd.logits, mode=rd.mode, rope_base=w.rope_base,
-                                       epsilon=w.epsilon, delta=w.delta, fuse_commit=True)
+                                       epsilon=w.epsilon, delta=w.delta, fuse_commit=fuse_commit)
         self.stage = {n: torch.cuda.CUDAGraph() for n in self.NAMES}
         with torch.cuda.graph(self.stage["heads"]):
             root, pool = rd.heads()
@@ -453,7 +457,7 @@ class RoundGraphs:
 def e2e_loop(rd: Round, steps: int, stream):
     """Same round through the public API with per-step inputs copied from pinned host
     memory and the published result read back (both inside the timed region).  Two
-    rounds (medusa_round_create with the fused commit) are bound to two sets of input
+    rounds (medusa_round_create, as the timed step) are bound to two sets of input
     buffers and take the steps in turn.  On a second stream, once the round two steps
     back has finished, its published tokens and L_out are copied to the host and this
     step's inputs into its set, which overlaps the previous step's round; the step's
@@ -467,7 +471,7 @@ def e2e_loop(rd: Round, steps: int, stream):
             dst.copy_(src)
     rounds = [rd.m.MedusaRound(rd.tmpl, st[0], rd.w1, rd.w2, rd.w_lm, w.topk, st[1], st[2], st[3], st[4], rd.cache,
                                rd.max_L, st[5], mode=rd.mode, rope_base=w.rope_base, epsilon=w.epsilon,
-                               delta=w.delta, fuse_commit=True) for st in sets]
+                               delta=w.delta) for st in sets]
     tok_host = [torch.empty_like(r.out_tokens, device="cpu").pin_memory() for r in rounds]
     L_host = [torch.empty_like(r.L_out, device="cpu").pin_memory() for r in rounds]
     h2d = sum(x.numel() * x.element_size() for x in hosts)
@@ -730,10 +734,12 @@ def config_of(w: synth.Workload, rd):
          "paged": bool(w.page_size), "tree_rows": tree_rows(w),
          "l2": "inputs larger than L2: each step streams the head weights (>= 1.4 GB) before the KV; "
                "stage timings flush L2 with a 512 MB write",
-         "launch": "each step is one medusa_round_launch (the library's CUDA graph of the five calls, "
-                   "the commit fused into acceptance); e2e alternates two such rounds bound to two input "
-                   "sets, each step's inputs copied from pinned host memory during the previous step's "
-                   "round and its published tokens and L_out copied back"}
+         "launch": "each step is one medusa_round_launch (the library's CUDA graph of the five calls); "
+                   "e2e alternates two such rounds bound to two input sets, each step's inputs copied from "
+                   "pinned host memory during the previous step's round and its published tokens and L_out "
+                   "copied back",
+         "kv_cache": "bf16, with the library's fp16 mirror (filled once before timing, as after a prefill; "
+                     "every round's cache writes keep it in step)" if w.dtype == "bf16" else w.dtype}
     return c
 
 
@@ -867,6 +873,8 @@ def run_stage(args):
             cache_bt = None
         V = torch.randn(K.shape, generator=gen, device=dev).to(w.torch_dtype)
         cache = m.KVCache(K, V, block_table=cache_bt)
+        if w.dtype == "bf16":
+            cache.add_mirror()                     # as in the round (Round)
         out = torch.empty((w.batch, N, w.n_q_heads, w.head_dim), dtype=torch.float32, device=dev)
         call = lambda: m.medusa_tree_attn_verify(tmpl, q, k, v, cache, L, int(lengths.max()), rope_base=w.rope_base,
                                                  out=out)

@@ -120,7 +120,17 @@ typedef struct medusa_tree_s {
   const struct medusa_tree_s *per_seq; /* NULL, or [B] device templates, one per sequence (see above) */
 } medusa_tree_t;
 
-/* One layer's KV cache, contiguous or paged. */
+/* One layer's KV cache, contiguous or paged.
+ *
+ * A bf16 cache may carry an fp16 mirror: k_f16 and v_f16, buffers of the same layout
+ * and size as k and v (caller-owned, device, 16-byte aligned), holding every cache
+ * element converted to fp16 (exact for magnitudes in [2^-14, 65504]; smaller ones lose
+ * bits, larger ones become inf).  The tensor-core attention multiplies in fp16: with a
+ * mirror it reads the prefix tiles from it and converts nothing, instead of converting
+ * every prefix row of K and V on every call.  Every call that writes cache rows (the
+ * tree rows staged by medusa_tree_attn_verify, the rows moved by the compaction calls
+ * and by medusa_tree_accept_commit) writes both copies, so a mirror once filled
+ * (medusa_kv_mirror_sync) stays a copy of the cache.  Both NULL: no mirror. */
 typedef struct {
   void *k;                /* contiguous: [B][n_kv_heads][capacity][head_dim];
                              paged:      [n_pages][n_kv_heads][page_size][head_dim] */
@@ -133,6 +143,8 @@ typedef struct {
   const int32_t *block_table; /* paged: [B][max_blocks] physical page of rows [16j, 16j+16) */
   int32_t max_blocks;
   int32_t n_pages;
+  void *k_f16;            /* NULL, or (bf16 caches) the fp16 mirror of k, same layout */
+  void *v_f16;            /* NULL, or the fp16 mirror of v; set both or neither */
 } medusa_kv_t;
 
 /* ---------------------------------------------------------------------------
@@ -419,6 +431,16 @@ medusa_status medusa_kv_compact_layers(const medusa_kv_t *caches, int32_t n_laye
                                        int32_t B, const int32_t *L, const int32_t *accept_len,
                                        const int32_t *out_rows, int32_t *L_out, int32_t *status,
                                        void *stream);
+
+/* Fill a bf16 cache's fp16 mirror (see medusa_kv_t): every element of k and v,
+ * converted to fp16 (round to nearest even; beyond 65504 it becomes inf), written to
+ * k_f16 and v_f16 over the whole buffers: B * n_kv_heads * capacity * head_dim
+ * elements each for a contiguous cache (B: its sequences), n_pages * n_kv_heads * 16 *
+ * head_dim for a paged one (B unused).  For a cache filled outside this library (a
+ * prefill); after that the library's own writes keep the mirror in step.
+ * MEDUSA_EINVAL for a cache without a mirror, not bf16, or B < 1 (contiguous).
+ * Stream-ordered. */
+medusa_status medusa_kv_mirror_sync(const medusa_kv_t *cache, int32_t B, void *stream);
 
 /* ---------------------------------------------------------------------------
  * Whole round: the five calls as one CUDA graph

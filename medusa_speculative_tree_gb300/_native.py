@@ -25,7 +25,7 @@ EXPORTED = [
     "medusa_heads_topk_workspace", "medusa_heads_topk", "medusa_tree_fill",
     "medusa_tree_attn_workspace", "medusa_tree_attn_verify", "medusa_tree_attn_verify_static",
     "medusa_tree_accept_workspace",
-    "medusa_tree_accept", "medusa_tree_accept_commit", "medusa_tree_accept_hidden_workspace", "medusa_tree_accept_hidden", "medusa_kv_compact", "medusa_kv_compact_layers", "medusa_round_workspace", "medusa_round_create",
+    "medusa_tree_accept", "medusa_tree_accept_commit", "medusa_tree_accept_hidden_workspace", "medusa_tree_accept_hidden", "medusa_kv_compact", "medusa_kv_compact_layers", "medusa_kv_mirror_sync", "medusa_round_workspace", "medusa_round_create",
     "medusa_round_launch", "medusa_round_destroy", "medusa_status_string", "medusa_abi_version",
     "medusa_test_set_stall_ns",
 ]
@@ -46,6 +46,7 @@ class MedusaKV(C.Structure):
         ("k", C.c_void_p), ("v", C.c_void_p), ("dtype", C.c_int32), ("n_kv_heads", C.c_int32),
         ("head_dim", C.c_int32), ("capacity", C.c_int32), ("page_size", C.c_int32),
         ("block_table", C.c_void_p), ("max_blocks", C.c_int32), ("n_pages", C.c_int32),
+        ("k_f16", C.c_void_p), ("v_f16", C.c_void_p),
     ]
 
 
@@ -116,6 +117,7 @@ def lib() -> C.CDLL:
                                             VP, VP, SZ, VP]),
         "medusa_kv_compact": (I32, [P(MedusaKV), P(MedusaTree), I32, VP, VP, VP, VP, VP, VP]),
         "medusa_kv_compact_layers": (I32, [P(MedusaKV), I32, P(MedusaTree), I32, VP, VP, VP, VP, VP, VP]),
+        "medusa_kv_mirror_sync": (I32, [P(MedusaKV), I32, VP]),
         "medusa_round_workspace": (SZ, [P(MedusaRoundDesc)]),
         "medusa_round_create": (I32, [P(MedusaRoundDesc), VP, SZ, VP, P(VP)]),
         "medusa_round_launch": (I32, [VP, VP]),

@@ -248,17 +248,42 @@ def batch_template_arrays(batch, b: int) -> dict:
 
 @dataclass
 class KVCache:
-    """One layer's cache: contiguous [B, Hkv, cap, dh] or paged [pages, Hkv, 16, dh]."""
+    """One layer's cache: contiguous [B, Hkv, cap, dh] or paged [pages, Hkv, 16, dh].
+
+    k_f16 / v_f16: an optional fp16 mirror of a bf16 cache (same shapes), which the
+    tensor-core attention reads instead of converting the prefix on every call; the
+    library's own cache writes keep it in step once filled (add_mirror, sync_mirror)."""
 
     k: torch.Tensor
     v: torch.Tensor
     block_table: Optional[torch.Tensor] = None    # int32 [B, max_blocks] for paged caches
     capacity: Optional[int] = None
+    k_f16: Optional[torch.Tensor] = None
+    v_f16: Optional[torch.Tensor] = None
+
+    def add_mirror(self) -> "KVCache":
+        """Allocate the fp16 mirror and fill it from the cache (medusa_kv_mirror_sync)."""
+        self.k_f16 = torch.empty(self.k.shape, dtype=torch.float16, device=self.k.device)
+        self.v_f16 = torch.empty(self.v.shape, dtype=torch.float16, device=self.v.device)
+        self.sync_mirror()
+        return self
+
+    def sync_mirror(self):
+        """Refill the mirror from the cache, stream-ordered (after writes made outside
+        this library)."""
+        B = self.k.shape[0] if self.block_table is None else 1
+        check("medusa_kv_mirror_sync", lib().medusa_kv_mirror_sync(C.byref(self.desc()), B, _stream(self.k.device)))
 
     def desc(self) -> nat.MedusaKV:
-        _need_cuda(self.k, self.v, self.block_table)
+        _need_cuda(self.k, self.v, self.block_table, self.k_f16, self.v_f16)
         d = nat.MedusaKV()
         d.k, d.v = self.k.data_ptr(), self.v.data_ptr()
+        d.k_f16 = self.k_f16.data_ptr() if self.k_f16 is not None else None
+        d.v_f16 = self.v_f16.data_ptr() if self.v_f16 is not None else None
+        if (self.k_f16 is not None) and (self.k_f16.shape != self.k.shape or self.v_f16 is None
+                                         or self.v_f16.shape != self.v.shape
+                                         or self.k_f16.dtype != torch.float16 or self.v_f16.dtype != torch.float16):
+            raise ValueError("the fp16 mirror must be two float16 tensors of the cache's shapes")
         d.dtype = _dtype_code(self.k.dtype)
         if self.block_table is None:
             _, Hkv, cap, dh = self.k.shape

@@ -25,8 +25,10 @@ constexpr int kSelThreads = 1024;  // select: one warp per internal row, 32 rows
 constexpr int kSelWarps = kSelThreads / 32;
 constexpr int kCommitPieces = 2;   // 16-byte pieces a select thread holds while moving rows
 // The fused commit moves one KV head's K and V rows (2 G rows of head_dim elements, G <=
-// D + 1, head_dim <= 128, at most 4 bytes each) in one batch of pieces.
-static_assert(2 * (MEDUSA_MAX_DEPTH + 1) * (128 * 4 / 16) <= kSelThreads * kCommitPieces,
+// D + 1, head_dim <= 128, at most 4 bytes each; a bf16 cache with an fp16 mirror: 4 G
+// rows of 2 bytes) in one batch of pieces.
+static_assert(2 * (MEDUSA_MAX_DEPTH + 1) * (128 * 4 / 16) <= kSelThreads * kCommitPieces &&
+                  4 * (MEDUSA_MAX_DEPTH + 1) * (128 * 2 / 16) <= kSelThreads * kCommitPieces,
               "one head's published K/V rows must fit the select kernel's pieces");
 
 
@@ -47,7 +49,7 @@ __device__ __forceinline__ float exp2_approx(float x) {
   asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
   return y;
 }
-constexpr float kLog2e = 1.4426950408889634f, kLn2 = 0.6931471805599453f;
+constexpr float kLn2 = 0.6931471805599453f;   // (log2(e): kLog2e of the shared helpers)
 
 // Fold a batch of n values x[] (ids i0..i0+n-1, all above the ids this thread folded
 // before) into the running statistics.
@@ -513,10 +515,10 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
 
   // ---- fused commit: medusa_kv_compact of this sequence --------------------------------
   // Thread 0 validates as the compaction kernel does (capacity, then the chain of
-  // published rows); then every KV head's G rows of K and V move as 16-byte pieces,
-  // a group of heads at a time: all pieces of the group are read into registers before
-  // any is written, so overlapping source and destination rows are safe (rows of
-  // different heads never overlap).
+  // published rows); then every KV head's G rows of K and V (and of their fp16 mirror,
+  // if the cache has one) move as 16-byte pieces, a group of heads at a time: all
+  // pieces of the group are read into registers before any is written, so overlapping
+  // source and destination rows are safe (rows of different heads never overlap).
   __shared__ int c_rows[MEDUSA_MAX_DEPTH + 1];
   __shared__ int c_status, c_G, c_L;
   if (threadIdx.x == 0) {
@@ -546,11 +548,13 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
   const int G = c_G, Lb = c_L;
   const int esz = cm.c.dtype == MEDUSA_BF16 ? 2 : 4;
   const int pr = cm.c.head_dim * esz / 16;                  // pieces per row
-  const int per_head = 2 * G * pr;                          // K and V rows of one head
+  const int n_arr = cm.c.k_f16 ? 4 : 2;                     // K, V (, K and V mirrors)
+  const int per_head = n_arr * G * pr;                      // their rows of one head
   int hg = (kSelThreads * kCommitPieces) / per_head;         // heads per group
   if (hg < 1) hg = 1;
-  char* kb = static_cast<char*>(cm.c.k);
-  char* vb = static_cast<char*>(cm.c.v);
+  auto arr = [&](int kv) -> char* {
+    return static_cast<char*>(kv == 0 ? cm.c.k : kv == 1 ? cm.c.v : kv == 2 ? cm.c.k_f16 : cm.c.v_f16);
+  };
   for (int h0 = 0; h0 < cm.c.n_kv_heads; h0 += hg) {
     const int nh = min(hg, cm.c.n_kv_heads - h0);
     const int n = nh * per_head;
@@ -561,7 +565,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
       if (i < n) {
         const int h = h0 + i / per_head, rem = i % per_head;
         const int kv = rem / (G * pr), j = (rem / pr) % G, e = rem % pr;
-        const char* base = kv ? vb : kb;
+        const char* base = arr(kv);
         const int64_t off = cache_row_offset(cm.c, b, h, Lb + c_rows[j]) * esz + 16 * e;
         piece[k] = *reinterpret_cast<const uint4*>(base + off);
       }
@@ -573,7 +577,7 @@ __global__ void __launch_bounds__(kSelThreads) select_kernel(
       if (i < n) {
         const int h = h0 + i / per_head, rem = i % per_head;
         const int kv = rem / (G * pr), j = (rem / pr) % G, e = rem % pr;
-        char* base = kv ? vb : kb;
+        char* base = arr(kv);
         const int64_t off = cache_row_offset(cm.c, b, h, Lb + j) * esz + 16 * e;
         *reinterpret_cast<uint4*>(base + off) = piece[k];
       }

@@ -141,6 +141,16 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(SimtArgs a) {
       Elem<EL>::store(ck, dst + i + HALF, x2 * tab_c[ti] + x1 * tab_s[ti]);
       cv[dst + i] = vn[src + i];
       cv[dst + i + HALF] = vn[src + i + HALF];
+      if constexpr (sizeof(EL) == 2) {
+        if (a.c.k_f16) {                          // the fp16 mirror of the rows just written
+          uint16_t* mk = (uint16_t*)a.c.k_f16;
+          uint16_t* mv = (uint16_t*)a.c.v_f16;
+          mk[dst + i] = bf16_bits_to_f16_bits(ck[dst + i]);
+          mk[dst + i + HALF] = bf16_bits_to_f16_bits(ck[dst + i + HALF]);
+          mv[dst + i] = bf16_bits_to_f16_bits(vn[src + i]);
+          mv[dst + i + HALF] = bf16_bits_to_f16_bits(vn[src + i + HALF]);
+        }
+      }
     }
   }
   __syncthreads();

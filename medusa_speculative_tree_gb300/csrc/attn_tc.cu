@@ -187,6 +187,20 @@ __device__ __forceinline__ void convert_tile(uint8_t* tile, int k_valid, int ct)
   }
 }
 
+// A tile already in fp16 (read from the cache's fp16 mirror): only the rows of keys
+// >= k_valid become zero (rows past a sequence's prefix may hold anything).
+template <int kConvThreads, int KT>
+__device__ __forceinline__ void zero_tail(uint8_t* tile, int k_valid, int ct) {
+  if (k_valid >= KT) return;
+  uint4* p = reinterpret_cast<uint4*>(tile);
+  constexpr int kIter = (KT * kDH * 2 / 16) / kConvThreads;
+#pragma unroll
+  for (int i = 0; i < kIter; ++i) {
+    const int idx = i * kConvThreads + ct;
+    if ((idx % (KT * 8)) / 8 >= k_valid) p[idx] = make_uint4(0, 0, 0, 0);
+  }
+}
+
 // Tree-row key tile of KT rows: bf16 -> RoPE at L + depth[v] (fp32) -> fp16, in place.
 // Row r of the tile is tree row v0 + r; dims i and i + 64 sit in the two blocks at the same
 // swizzled position.  Rows >= n_valid become zero.  `dep[i]` is the depth of the row
@@ -695,6 +709,7 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
   } else if (warp >= C::kConvWarp0) {
     // ---- bf16 -> fp16 conversion (tree keys also rotated) ------------------------------
     const int ct = tid - C::kConvWarp0 * 32;
+    const bool mirror = a.c.k_f16 != nullptr;       // the cache has an fp16 mirror
     for (int j = 0; j < n_tiles; ++j) {
       const int st = j % NS;
       uint8_t* tK = sm + C::kOffK + st * C::kKBytes;
@@ -712,7 +727,9 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
         ok = false;
         break;
       }
+      // (prefix tiles of a cache with an fp16 mirror arrive in fp16 already)
       if (j >= n_pre) convert_rotate_tile<C::kConvThreads, KT>(tK, k_valid, dep, tab_c, tab_s, ct);
+      else if (mirror) zero_tail<C::kConvThreads, KT>(tK, k_valid, ct);
       else convert_tile<C::kConvThreads, KT>(tK, k_valid, ct);
       fence_proxy_async();
       mbar_arrive(BAR(C::kBarConvK + st));
@@ -720,7 +737,8 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
         ok = false;
         break;
       }
-      convert_tile<C::kConvThreads, KT>(tV, k_valid, ct);
+      if (j < n_pre && mirror) zero_tail<C::kConvThreads, KT>(tV, k_valid, ct);
+      else convert_tile<C::kConvThreads, KT>(tV, k_valid, ct);
       fence_proxy_async();
       mbar_arrive(BAR(C::kBarConvV + st));
     }
@@ -761,10 +779,19 @@ __global__ void __launch_bounds__(TcCfg<QT, NS>::kThreads, (QT == 1 && NS == 2) 
           y1[e] = a0 | (a1 << 16);
           y2[e] = b0 | (b1 << 16);
         }
-        *reinterpret_cast<uint4*>(ck + dst) = make_uint4(y1[0], y1[1], y1[2], y1[3]);
-        *reinterpret_cast<uint4*>(ck + dst + kHalf) = make_uint4(y2[0], y2[1], y2[2], y2[3]);
+        const uint4 ya = make_uint4(y1[0], y1[1], y1[2], y1[3]), yb = make_uint4(y2[0], y2[1], y2[2], y2[3]);
+        *reinterpret_cast<uint4*>(ck + dst) = ya;
+        *reinterpret_cast<uint4*>(ck + dst + kHalf) = yb;
         *reinterpret_cast<uint4*>(cv + dst) = va;
         *reinterpret_cast<uint4*>(cv + dst + kHalf) = vb;
+        if (mirror) {                              // the fp16 mirror of the rows just written
+          uint16_t* mk = (uint16_t*)a.c.k_f16;
+          uint16_t* mv = (uint16_t*)a.c.v_f16;
+          *reinterpret_cast<uint4*>(mk + dst) = bf16x8_to_f16x8(ya);
+          *reinterpret_cast<uint4*>(mk + dst + kHalf) = bf16x8_to_f16x8(yb);
+          *reinterpret_cast<uint4*>(mv + dst) = bf16x8_to_f16x8(va);
+          *reinterpret_cast<uint4*>(mv + dst + kHalf) = bf16x8_to_f16x8(vb);
+        }
       }
     }
   } else {
@@ -1335,7 +1362,8 @@ cudaError_t launch_attn_tc(const AttnPlan& p, const medusa_tree_t& t, const void
                            float scale_log2, float* out, float* lse, int32_t* status, void* ws,
                            cudaStream_t st) {
   CUtensorMap mk, mv, mkn, mvn, mq;
-  if (!encode_kv_map(&mk, c.k, c, p.B) || !encode_kv_map(&mv, c.v, c, p.B) ||
+  // prefix tiles come from the fp16 mirror when the cache has one (the same layout)
+  if (!encode_kv_map(&mk, c.k_f16 ? c.k_f16 : c.k, c, p.B) || !encode_kv_map(&mv, c.v_f16 ? c.v_f16 : c.v, c, p.B) ||
       !encode_rows_map(&mkn, k_new, p.B, t.n_rows, p.Hkv, 1, kTcKeys) ||
       !encode_rows_map(&mvn, v_new, p.B, t.n_rows, p.Hkv, 1, kTcKeys) ||
       !encode_rows_map(&mq, q, p.B, t.n_rows, p.Hq, p.g, kTcRows / p.g))

@@ -1,6 +1,7 @@
 // Shared device helpers for the Medusa verify-round kernels (sm_103a).
 #pragma once
 
+#include <cuda_fp16.h>
 #include <cuda_runtime.h>
 #include <stdint.h>
 
@@ -21,6 +22,13 @@ __device__ __forceinline__ uint16_t f32_to_bf16_bits(float f) {
   uint32_t u = __float_as_uint(f);
   uint32_t rounding = 0x7FFFu + ((u >> 16) & 1u);
   return (uint16_t)((u + rounding) >> 16);
+}
+
+// fp16 bits of a bf16 value (exact for magnitudes in [2^-14, 65504]): the value of a
+// bf16 cache's fp16 mirror.
+__device__ __forceinline__ uint16_t bf16_bits_to_f16_bits(uint16_t b) {
+  const __half h = __float2half_rn(__uint_as_float((uint32_t)b << 16));
+  return *reinterpret_cast<const uint16_t*>(&h);
 }
 
 // Element traits: float storage or bf16 storage (raw uint16_t bits).

@@ -1,5 +1,9 @@
 // Tree fill ([M7.2] §0x01B, §0x04A) and winning-path K/V compaction
 // ([M7.2] §0x06A-§0x06B).  Both are small integer / data-movement kernels.
+#include <vector>
+
+#include <cuda_fp16.h>
+
 #include "common.cuh"
 #include "kernels.h"
 
@@ -143,48 +147,93 @@ cudaError_t launch_tree_fill(const medusa_tree_t& t, int B, int K, const int32_t
   return cudaGetLastError();
 }
 
+namespace {
+
+// One launch over n caches' (K, V) pointer pairs that share c's layout; the pair at
+// z = 0 writes status and L_out when meta is set.
+template <int NL>
+cudaError_t compact_launch(const medusa_kv_t& c, void* const* ks, void* const* vs, int n, int meta,
+                           const medusa_tree_t& t, int B, const int32_t* L, const int32_t* accept_len,
+                           const int32_t* out_rows, int32_t* L_out, int32_t* status, cudaStream_t st) {
+  const size_t esz = c.dtype == MEDUSA_BF16 ? 2 : 4;
+  const size_t smem = 2 * (size_t)(t.max_depth + 1) * c.head_dim * esz;
+  LayerPtrs<NL> lp = {};
+  for (int i = 0; i < n; ++i) {
+    lp.k[i] = ks[i];
+    lp.v[i] = vs[i];
+  }
+  dim3 grid(c.n_kv_heads, B, n);
+  if (c.dtype == MEDUSA_BF16)
+    kv_compact_kernel<uint16_t, NL><<<grid, 128, smem, st>>>(c, lp, meta, t, L, accept_len, out_rows, L_out, status);
+  else
+    kv_compact_kernel<float, NL><<<grid, 128, smem, st>>>(c, lp, meta, t, L, accept_len, out_rows, L_out, status);
+  return cudaGetLastError();
+}
+
+// bf16 -> fp16, eight elements per 16-byte vector (bf16 -> fp32 exactly, then one
+// rounding to fp16)
+__global__ void kv_mirror_kernel(const uint4* __restrict__ k, const uint4* __restrict__ v, uint4* __restrict__ k16,
+                                 uint4* __restrict__ v16, int64_t n_vec) {
+  auto conv = [](uint32_t w) {
+    const __half2 h = __floats2half2_rn(__uint_as_float(w << 16), __uint_as_float(w & 0xFFFF0000u));
+    return *reinterpret_cast<const uint32_t*>(&h);
+  };
+  for (int64_t i = blockIdx.x * (int64_t)blockDim.x + threadIdx.x; i < n_vec; i += (int64_t)gridDim.x * blockDim.x) {
+    const uint4 a = k[i], b = v[i];
+    k16[i] = make_uint4(conv(a.x), conv(a.y), conv(a.z), conv(a.w));
+    v16[i] = make_uint4(conv(b.x), conv(b.y), conv(b.z), conv(b.w));
+  }
+}
+
+}  // namespace
+
+// The caches' writes reach their fp16 mirrors too: a mirror is one more (K, V) pair of
+// the same layout and element size, whose rows move as raw bits with the cache's.
 cudaError_t launch_kv_compact(const medusa_kv_t& c, const medusa_tree_t& t, int B,
                               const int32_t* L, const int32_t* accept_len,
                               const int32_t* out_rows, int32_t* L_out, int32_t* status,
                               cudaStream_t st) {
-  const size_t esz = c.dtype == MEDUSA_BF16 ? 2 : 4;
-  const size_t smem = 2 * (size_t)(t.max_depth + 1) * c.head_dim * esz;
-  dim3 grid(c.n_kv_heads, B, 1);
-  LayerPtrs<1> lp;
-  lp.k[0] = c.k;
-  lp.v[0] = c.v;
-  if (c.dtype == MEDUSA_BF16)
-    kv_compact_kernel<uint16_t, 1><<<grid, 128, smem, st>>>(c, lp, 1, t, L, accept_len, out_rows, L_out, status);
-  else
-    kv_compact_kernel<float, 1><<<grid, 128, smem, st>>>(c, lp, 1, t, L, accept_len, out_rows, L_out, status);
-  return cudaGetLastError();
+  void* ks[2] = {c.k, c.k_f16};
+  void* vs[2] = {c.v, c.v_f16};
+  if (c.k_f16) return compact_launch<2>(c, ks, vs, 2, 1, t, B, L, accept_len, out_rows, L_out, status, st);
+  return compact_launch<1>(c, ks, vs, 1, 1, t, B, L, accept_len, out_rows, L_out, status, st);
 }
 
 cudaError_t launch_kv_compact_layers(const medusa_kv_t* layers, int n_layers, const medusa_tree_t& t, int B,
                                      const int32_t* L, const int32_t* accept_len, const int32_t* out_rows,
                                      int32_t* L_out, int32_t* status, cudaStream_t st) {
-  const medusa_kv_t& c = layers[0];
-  const size_t esz = c.dtype == MEDUSA_BF16 ? 2 : 4;
-  const size_t smem = 2 * (size_t)(t.max_depth + 1) * c.head_dim * esz;
-  for (int l0 = 0; l0 < n_layers; l0 += kCompactLayersPerLaunch) {
-    const int n = n_layers - l0 < kCompactLayersPerLaunch ? n_layers - l0 : kCompactLayersPerLaunch;
-    LayerPtrs<kCompactLayersPerLaunch> lp = {};
-    for (int i = 0; i < n; ++i) {
-      lp.k[i] = layers[l0 + i].k;
-      lp.v[i] = layers[l0 + i].v;
+  std::vector<void*> ks, vs;                 // every layer's cache, then its mirror if any
+  ks.reserve(2 * (size_t)n_layers);
+  vs.reserve(2 * (size_t)n_layers);
+  for (int i = 0; i < n_layers; ++i) {
+    ks.push_back(layers[i].k);
+    vs.push_back(layers[i].v);
+    if (layers[i].k_f16) {
+      ks.push_back(layers[i].k_f16);
+      vs.push_back(layers[i].v_f16);
     }
-    dim3 grid(c.n_kv_heads, B, n);
-    const int meta = l0 == 0 ? 1 : 0;
-    if (c.dtype == MEDUSA_BF16)
-      kv_compact_kernel<uint16_t, kCompactLayersPerLaunch>
-          <<<grid, 128, smem, st>>>(c, lp, meta, t, L, accept_len, out_rows, L_out, status);
-    else
-      kv_compact_kernel<float, kCompactLayersPerLaunch>
-          <<<grid, 128, smem, st>>>(c, lp, meta, t, L, accept_len, out_rows, L_out, status);
-    const cudaError_t e = cudaGetLastError();
+  }
+  const int total = (int)ks.size();
+  for (int l0 = 0; l0 < total; l0 += kCompactLayersPerLaunch) {
+    const int n = total - l0 < kCompactLayersPerLaunch ? total - l0 : kCompactLayersPerLaunch;
+    const cudaError_t e = compact_launch<kCompactLayersPerLaunch>(layers[0], ks.data() + l0, vs.data() + l0, n,
+                                                                  l0 == 0 ? 1 : 0, t, B, L, accept_len, out_rows,
+                                                                  L_out, status, st);
     if (e != cudaSuccess) return e;
   }
   return cudaSuccess;
+}
+
+cudaError_t launch_kv_mirror_sync(const medusa_kv_t& c, int64_t n, cudaStream_t st) {
+  const int64_t n_vec = n / 8;                 // head_dim is 64 or 128: whole vectors
+  int sms = 148, dev = 0;
+  if (cudaGetDevice(&dev) == cudaSuccess) cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  int64_t blocks = (n_vec + 255) / 256;
+  if (blocks > 8 * (int64_t)sms) blocks = 8 * (int64_t)sms;
+  if (blocks < 1) blocks = 1;
+  kv_mirror_kernel<<<(unsigned)blocks, 256, 0, st>>>((const uint4*)c.k, (const uint4*)c.v, (uint4*)c.k_f16,
+                                                     (uint4*)c.v_f16, n_vec);
+  return cudaGetLastError();
 }
 
 }  // namespace medusa

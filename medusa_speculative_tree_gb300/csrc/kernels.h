@@ -167,6 +167,9 @@ cudaError_t launch_kv_compact_layers(const medusa_kv_t* layers, int n_layers, co
                                      const int32_t* L, const int32_t* accept_len, const int32_t* out_rows,
                                      int32_t* L_out, int32_t* status, cudaStream_t st);
 
+// The fp16 mirror of a bf16 cache: n elements of k and of v converted (whole buffers).
+cudaError_t launch_kv_mirror_sync(const medusa_kv_t& c, int64_t n, cudaStream_t st);
+
 inline size_t align_up(size_t x, size_t a) { return (x + a - 1) / a * a; }
 
 }  // namespace medusa

@@ -79,6 +79,11 @@ bool kv_ok(const medusa_kv_t* c) {
     if (c->page_size != 16 || !c->block_table || c->max_blocks < 1 || c->n_pages < 1) return false;
     if (c->capacity > c->max_blocks * c->page_size) return false;
   }
+  // an fp16 mirror: both halves, a bf16 cache, aligned like the cache
+  if (c->k_f16 || c->v_f16) {
+    if (!c->k_f16 || !c->v_f16 || c->dtype != MEDUSA_BF16) return false;
+    if (!aligned16(c->k_f16) || !aligned16(c->v_f16)) return false;
+  }
   return true;
 }
 
@@ -92,7 +97,7 @@ medusa_status accept_logits_impl(const medusa_tree_t* t, int32_t B, int32_t V, c
 
 extern "C" {
 
-int32_t medusa_abi_version(void) { return 4; }
+int32_t medusa_abi_version(void) { return 5; }
 
 void medusa_test_set_stall_ns(uint64_t ns) { medusa::g_test_stall_ns.store(ns, std::memory_order_relaxed); }
 
@@ -574,11 +579,20 @@ medusa_status medusa_kv_compact_layers(const medusa_kv_t* caches, int32_t n_laye
     // every layer shares the layout: one row offset serves them all
     if (c.dtype != c0.dtype || c.n_kv_heads != c0.n_kv_heads || c.head_dim != c0.head_dim ||
         c.capacity != c0.capacity || c.page_size != c0.page_size || c.block_table != c0.block_table ||
-        c.max_blocks != c0.max_blocks || c.n_pages != c0.n_pages)
+        c.max_blocks != c0.max_blocks || c.n_pages != c0.n_pages || (c.k_f16 == nullptr) != (c0.k_f16 == nullptr))
       return MEDUSA_EINVAL;
   }
   return cuda_status(medusa::launch_kv_compact_layers(caches, n_layers, *t, B, L, accept_len, out_rows, L_out,
                                                       status, as_stream(stream)));
+}
+
+medusa_status medusa_kv_mirror_sync(const medusa_kv_t* cache, int32_t B, void* stream) {
+  if (!kv_ok(cache) || !cache->k_f16 || cache->dtype != MEDUSA_BF16) return MEDUSA_EINVAL;
+  if (cache->page_size == 0 && B < 1) return MEDUSA_EINVAL;
+  const int64_t rows = cache->page_size == 0 ? (int64_t)B * cache->capacity
+                                             : (int64_t)cache->n_pages * cache->page_size;
+  return cuda_status(medusa::launch_kv_mirror_sync(*cache, rows * cache->n_kv_heads * cache->head_dim,
+                                                   as_stream(stream)));
 }
 
 // ---- whole round as one CUDA graph ------------------------------------------------

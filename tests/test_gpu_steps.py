@@ -111,8 +111,16 @@ def test_heads_shared_projection_and_bias(m):
 
 # ----------------------------------------------------------------------------- attention
 
-def attn_case(m, w, paths, lengths, paged=False, fill_tail=0.0, want_lse=True):
-    """Run GPU tree attention and the dense oracle on the same inputs."""
+def same_as_mirror(cache):
+    """The fp16 mirror holds fp16(bf16 value) of every cache element (NaN where NaN)."""
+    for c16, c in ((cache.k_f16, cache.k), (cache.v_f16, cache.v)):
+        want = c.to(torch.float16)
+        assert bool(((c16 == want) | (c16.isnan() & want.isnan())).all())
+
+
+def attn_case(m, w, paths, lengths, paged=False, fill_tail=0.0, want_lse=True, mirror=False):
+    """Run GPU tree attention and the dense oracle on the same inputs (with mirror, on a
+    bf16 cache carrying an fp16 mirror, which must again mirror the cache afterwards)."""
     t_g, t_o = make_template(m, paths, w.topk)
     N = t_o.n_rows
     q, k, v = synth.tree_qkv(w, N)
@@ -122,11 +130,15 @@ def attn_case(m, w, paths, lengths, paged=False, fill_tail=0.0, want_lse=True):
     else:
         K, V, ks, vs = gu.contiguous_cache(w, lengths, N, fill_tail=fill_tail)
         cache = m.KVCache(K, V)
+    if mirror:
+        cache.add_mirror()
     Ld = gu.device_tensor(lengths, torch.int32)
     out, lse, status = m.medusa_tree_attn_verify(t_g, q.cuda(), k.cuda(), v.cuda(), cache, Ld,
                                                  int(max(lengths)), rope_base=w.rope_base, want_lse=want_lse)
     torch.cuda.synchronize()
     assert (status.cpu().numpy() == 0).all()
+    if mirror:
+        same_as_mirror(cache)
     is_f32 = w.dtype == "f32"
     for b, L in enumerate(lengths):
         o_out, o_lse, o_kr = oatt.tree_attention(gu.to64(q[b]), gu.to64(k[b]), gu.to64(v[b]), gu.to64(ks[b]),
@@ -153,12 +165,12 @@ def test_attn_tiny_fp32(m):
     attn_case(m, w, otree.regular_paths((2, 3)), synth.prefix_lengths(w))
 
 
-@pytest.mark.parametrize("dt", ["f32", "bf16"])
+@pytest.mark.parametrize("dt", ["f32", "bf16", "bf16+mirror"])
 @pytest.mark.parametrize("L", [0, 1, 37, 300])
 def test_attn_ragged_prefix_gqa(m, dt, L):
-    w = synth.small_variant(synth.WORKLOADS["llama3-8b-256"], dtype=dt, prefix_len=L, seed=2000 + L)
+    w = synth.small_variant(synth.WORKLOADS["llama3-8b-256"], dtype=dt.split("+")[0], prefix_len=L, seed=2000 + L)
     acc = synth.rank_accuracy(4, 10)
-    attn_case(m, w, otree.greedy_tree(acc, 40), synth.prefix_lengths(w))
+    attn_case(m, w, otree.greedy_tree(acc, 40), synth.prefix_lengths(w), mirror=dt.endswith("mirror"))
 
 
 def test_attn_root_only_and_deep_chain(m):
@@ -169,16 +181,20 @@ def test_attn_root_only_and_deep_chain(m):
     attn_case(m, w, chain, synth.prefix_lengths(w))
 
 
-def test_attn_multiword_mask_and_nan_tail(m):
+@pytest.mark.parametrize("mirror", [False, True])
+def test_attn_multiword_mask_and_nan_tail(m, mirror):
     """341 rows (six 64-bit mask words); cache rows past L + N hold NaN and must stay unread."""
     w = synth.small_variant(synth.WORKLOADS["longctx-341"], n_q_heads=16, n_kv_heads=2, prefix_len=200, seed=41)
-    attn_case(m, w, otree.regular_paths((4, 4, 4, 4)), synth.prefix_lengths(w), fill_tail=float("nan"))
+    attn_case(m, w, otree.regular_paths((4, 4, 4, 4)), synth.prefix_lengths(w), fill_tail=float("nan"),
+              mirror=mirror)
 
 
-def test_attn_paged_batch(m):
+@pytest.mark.parametrize("mirror", [False, True])
+def test_attn_paged_batch(m, mirror):
     w = synth.small_variant(synth.WORKLOADS["serving-b16-paged"], batch=4, prefix_range=(20, 700), seed=51)
     acc = synth.rank_accuracy(4, 10)
-    attn_case(m, w, otree.greedy_tree(acc, 63), synth.prefix_lengths(w), paged=True, fill_tail=float("nan"))
+    attn_case(m, w, otree.greedy_tree(acc, 63), synth.prefix_lengths(w), paged=True, fill_tail=float("nan"),
+              mirror=mirror)
 
 
 @pytest.mark.parametrize("shape", ["1,2", "1,4", "2,2"])
@@ -186,13 +202,14 @@ def test_attn_paged_batch(m):
 def test_attn_every_shape_and_split_count(m, monkeypatch, shape, splits):
     """The tensor-core kernel in each of its shapes (query tiles per CTA, stages) and at
     several split counts, on a paged GQA batch of ragged lengths with a NaN tail: the
-    splits' cluster merge and the per-sequence spreading of tiles over them."""
+    splits' cluster merge and the per-sequence spreading of tiles over them (with an
+    fp16 mirror at odd split counts)."""
     monkeypatch.setenv("MEDUSA_ATTN_TC_SHAPE", shape)
     monkeypatch.setenv("MEDUSA_ATTN_TC_SPLITS", str(splits))
     w = synth.small_variant(synth.WORKLOADS["serving-b16-paged"], batch=3, seed=700 + splits)
     acc = synth.rank_accuracy(4, 10)
     lengths = np.array([1337, 3, 650])   # 21 / 1 / 11 tiles of 64 keys: some splits get none
-    attn_case(m, w, otree.greedy_tree(acc, 63), lengths, paged=True, fill_tail=float("nan"))
+    attn_case(m, w, otree.greedy_tree(acc, 63), lengths, paged=True, fill_tail=float("nan"), mirror=splits % 2 == 1)
 
 
 @pytest.mark.parametrize("shape", ["1,2", "2,2"])
@@ -391,7 +408,8 @@ def test_accept_root_only_template(m):
 # ----------------------------------------------------------------------------- compaction
 
 @pytest.mark.parametrize("paged", [False, True])
-def test_kv_compact(m, paged):
+@pytest.mark.parametrize("mirror", [False, True])
+def test_kv_compact(m, paged, mirror):
     w = synth.small_variant(synth.WORKLOADS["serving-b16-paged"], batch=5, prefix_range=(1, 300), seed=101,
                             page_size=16 if paged else 0)
     acc = synth.rank_accuracy(4, 10)
@@ -409,6 +427,8 @@ def test_kv_compact(m, paged):
     g = torch.Generator(device="cpu").manual_seed(5)
     K.copy_(torch.randn(K.shape, generator=g).to(K.dtype))
     V.copy_(torch.randn(V.shape, generator=g).to(V.dtype))
+    if mirror:
+        cache.add_mirror()
     rng = np.random.default_rng(3)
     W = t_o.max_depth + 1
     rows = np.full((w.batch, W), -1, dtype=np.int32)
@@ -425,6 +445,8 @@ def test_kv_compact(m, paged):
     torch.cuda.synchronize()
     assert (status.cpu().numpy() == 0).all()
     assert list(L_out.cpu().numpy()) == list(lengths + alen + 1)
+    if mirror:
+        same_as_mirror(cache)
     for b in range(w.batch):
         L = int(lengths[b])
         G = int(alen[b]) + 1
@@ -442,12 +464,14 @@ def test_kv_compact(m, paged):
         assert (ka == kb).all() and (va == vb).all()
 
 
-@pytest.mark.parametrize("paged,n_layers", [(False, 5), (True, 3), (False, 130)])
-def test_kv_compact_layers(m, paged, n_layers):
+@pytest.mark.parametrize("paged,n_layers,mirror", [(False, 5, False), (True, 3, True), (False, 130, False),
+                                                   (False, 70, True)])
+def test_kv_compact_layers(m, paged, n_layers, mirror):
     """Every layer's cache compacted by one call, against the oracle's compaction of
     each layer; a sequence with an invalid path stays untouched in every layer; more
-    than 128 layers take several launches with status and L_out written once."""
-    if n_layers > 8:      # many small layers: fp32, one KV head of 64 dims
+    than 128 layers take several launches with status and L_out written once (70
+    layers with fp16 mirrors are 140 caches: two launches as well)."""
+    if n_layers > 8 and not mirror:      # many small layers: fp32, one KV head of 64 dims
         w = synth.small_variant(synth.WORKLOADS["tiny-fp32"], batch=4, n_kv_heads=1, n_q_heads=1,
                                 prefix_len=None, prefix_range=(1, 120), seed=141)
     else:
@@ -471,6 +495,8 @@ def test_kv_compact_layers(m, paged, n_layers):
             caches.append(m.KVCache(K, V))
         K.copy_(torch.randn(K.shape, generator=g).to(K.dtype))
         V.copy_(torch.randn(V.shape, generator=g).to(V.dtype))
+        if mirror:
+            caches[-1].add_mirror()
         Ks.append(K)
         Vs.append(V)
     rng = np.random.default_rng(7 + n_layers)
@@ -514,6 +540,8 @@ def test_kv_compact_layers(m, paged, n_layers):
             if b != bad:
                 ocomp.kv_compact(kb, vb, L, rows[b, :alen[b] + 1])
             assert np.array_equal(ka, kb) and np.array_equal(va, vb), (layer, b)
+        if mirror:
+            same_as_mirror(caches[layer])
 
 
 def test_kv_compact_rejects_bad_paths(m):

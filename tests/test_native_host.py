@@ -34,7 +34,7 @@ def test_every_declared_symbol_is_exported(native):
     for n in names:
         assert hasattr(lib, n), n
     assert set(names) == set(native.EXPORTED)
-    assert native.lib().medusa_abi_version() == 4
+    assert native.lib().medusa_abi_version() == 5
     assert native.lib().medusa_status_string(-2).decode() == "cache capacity exceeded"
 
 
@@ -184,6 +184,33 @@ def test_kv_compact_layers_checks_layers_without_a_gpu(native):
     assert lib.medusa_kv_compact_layers(arr, 0, C.byref(t.host), 2, L, a, rows, L_out, st, None) == native.EINVAL
     assert lib.medusa_kv_compact_layers(arr, 2, C.byref(t.host), 2, L, a, rows, L, st, None) == native.EINVAL
     assert lib.medusa_kv_compact_layers(None, 2, C.byref(t.host), 2, L, a, rows, L_out, st, None) == native.EINVAL
+
+
+def test_fp16_mirror_checks_without_a_gpu(native):
+    """A cache's fp16 mirror is checked before any CUDA call: half a mirror, a mirror
+    of an fp32 cache, a misaligned mirror, medusa_kv_mirror_sync without a mirror or
+    with B < 1 for a contiguous cache, and layers of which only some have a mirror, are
+    refused with MEDUSA_EINVAL."""
+    from medusa_speculative_tree_gb300.api import Template
+    lib = native.lib()
+    t = Template([(0,), (1,), (0, 0)], 2)
+    fake = lambda i: C.c_void_p(4096 * (i + 1))       # never dereferenced: the checks fail first
+    def cache(i, dtype=native.BF16, k16=True, v16=True, k16_off=0):
+        c = native.MedusaKV()
+        c.k, c.v, c.dtype, c.n_kv_heads, c.head_dim, c.capacity = fake(4 * i).value, fake(4 * i + 1).value, dtype, 2, 128, 64
+        c.page_size, c.block_table, c.max_blocks, c.n_pages = 0, None, 0, 0
+        c.k_f16 = fake(4 * i + 2).value + k16_off if k16 else None
+        c.v_f16 = fake(4 * i + 3).value if v16 else None
+        return c
+    L, a, rows, L_out, st = (fake(100 + i) for i in range(5))
+    for bad in (cache(0, v16=False), cache(0, k16=False), cache(0, dtype=native.F32), cache(0, k16_off=8)):
+        assert lib.medusa_kv_compact(C.byref(bad), C.byref(t.host), 2, L, a, rows, L_out, st, None) == native.EINVAL
+        assert lib.medusa_kv_mirror_sync(C.byref(bad), 2, None) == native.EINVAL
+    assert lib.medusa_kv_mirror_sync(C.byref(cache(0, k16=False, v16=False)), 2, None) == native.EINVAL
+    assert lib.medusa_kv_mirror_sync(C.byref(cache(0)), 0, None) == native.EINVAL
+    assert lib.medusa_kv_mirror_sync(None, 2, None) == native.EINVAL
+    arr = (native.MedusaKV * 2)(cache(0), cache(1, k16=False, v16=False))
+    assert lib.medusa_kv_compact_layers(arr, 2, C.byref(t.host), 2, L, a, rows, L_out, st, None) == native.EINVAL
 
 
 def test_commit_and_hidden_acceptance_checks_without_a_gpu(native):
