@@ -260,8 +260,8 @@ class Round:
         if bf16 and T == 1 and stream_d and w.n_heads >= 1:
             heads = 1                                   # one persistent weight stream with top-k
         elif bf16 and T >= 2 and w.hidden % 64 == 0 and w.n_heads >= 1:
-            heads = 2 * math.ceil(T / 128) + 1         # per pass of <= 128 rows: input pairs and
-                                                        # tensor-core stream; then top-k
+            per_pass = 128 if T <= 128 else 256        # pair passes, else wide passes
+            heads = math.ceil(T / per_pass) + 1        # one tensor-core stream per pass; then top-k
         else:
             tpp = 1
             fit = max(1, min(16, (160 * 1024) // (w.hidden * 4)))
