@@ -8,12 +8,10 @@
 //   - rotates its queries (RoPE at L + depth[u]) and, for split 0, stages the
 //     rotated tree keys and the tree values at cache rows L + u;
 //   - runs an online-softmax pass over its prefix key range (no mask: every
-//     committed key is visible); split 0 then runs the tree rows as key tiles too
-//     (keys rotated at their own depth positions from the inputs, in fp32; each query
-//     row sees its ancestors and itself, from the multiword bitmask); every split
-//     writes an unnormalised partial (O, m, l);
+//     committed key is visible) and writes an unnormalised partial (O, m, l);
 //   - takes a ticket; the last CTA of the (b, kvh, m-tile) unit merges all
-//     partials, normalises and writes the output.  It then resets the unit's counter.
+//     partials, adds the tree block (ancestors from the multiword bitmask, fp32),
+//     normalises and writes the output.  It then resets the unit's counter.
 // Softmax runs in the log2 domain (scores pre-multiplied by scale * log2 e).
 #include <math.h>
 
@@ -170,69 +168,32 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(SimtArgs a) {
   const int k_end = min(Lb, k_begin + a.chunk);
   const EL* ckr = (const EL*)a.c.k;
   const EL* cvr = (const EL*)a.c.v;
-  const int W = t.n_words;
-  // One tile of kSimtKT keys into shared memory, then the online softmax of every row.
-  // Prefix tile: cache rows kt0 .. (committed keys, all visible).  Tree tile: tree rows
-  // kt0 .. of this sequence, key rotated at L + depth[v] (fp32), visible to the rows
-  // whose path starts with v's.
-  const int n_pref = k_end > k_begin ? (k_end - k_begin + kSimtKT - 1) / kSimtKT : 0;
-  const int n_tree = s == 0 ? (N + kSimtKT - 1) / kSimtKT : 0;
-  for (int tile = 0; tile < n_pref + n_tree; ++tile) {
-    const bool tree = tile >= n_pref;
-    const int kt0 = tree ? (tile - n_pref) * kSimtKT : k_begin + tile * kSimtKT;
-    if (!tree) {
-      constexpr int VEC_PER_ROW = DH / EPV;
-      for (int idx = tid; idx < kSimtKT * VEC_PER_ROW; idx += kSimtThreads) {
-        const int j = idx / VEC_PER_ROW, vi = idx % VEC_PER_ROW;
-        const int key = kt0 + j;
-        float kf[EPV], vf[EPV];
-        if (key < k_end) {
-          const int64_t off = row_off(a.c, b, kvh, key) + vi * EPV;
-          Elem<EL>::unpack(*reinterpret_cast<const uint4*>(ckr + off), kf);
-          Elem<EL>::unpack(*reinterpret_cast<const uint4*>(cvr + off), vf);
-        } else {
+  for (int kt0 = k_begin; kt0 < k_end; kt0 += kSimtKT) {
+    constexpr int VEC_PER_ROW = DH / EPV;
+    for (int idx = tid; idx < kSimtKT * VEC_PER_ROW; idx += kSimtThreads) {
+      const int j = idx / VEC_PER_ROW, vi = idx % VEC_PER_ROW;
+      const int key = kt0 + j;
+      float kf[EPV], vf[EPV];
+      if (key < k_end) {
+        const int64_t off = row_off(a.c, b, kvh, key) + vi * EPV;
+        Elem<EL>::unpack(*reinterpret_cast<const uint4*>(ckr + off), kf);
+        Elem<EL>::unpack(*reinterpret_cast<const uint4*>(cvr + off), vf);
+      } else {
 #pragma unroll
-          for (int e = 0; e < EPV; ++e) { kf[e] = 0.f; vf[e] = 0.f; }
-        }
-#pragma unroll
-        for (int e = 0; e < EPV; ++e) {
-          kts[(vi * EPV + e) * (kSimtKT + 1) + j] = kf[e];
-          vs[j * DH + vi * EPV + e] = vf[e];
-        }
+        for (int e = 0; e < EPV; ++e) { kf[e] = 0.f; vf[e] = 0.f; }
       }
-    } else {
-      for (int idx = tid; idx < kSimtKT * HALF; idx += kSimtThreads) {
-        const int j = idx / HALF, i = idx % HALF;
-        const int v = kt0 + j;
-        float k1 = 0.f, k2 = 0.f, v1 = 0.f, v2 = 0.f;
-        if (v < N) {
-          const int64_t src = (((int64_t)b * NS + v) * a.Hkv + kvh) * DH;
-          const float x1 = Elem<EL>::load(kn, src + i), x2 = Elem<EL>::load(kn, src + i + HALF);
-          const int ti = t.depth[v] * HALF + i;
-          k1 = x1 * tab_c[ti] - x2 * tab_s[ti];
-          k2 = x2 * tab_c[ti] + x1 * tab_s[ti];
-          v1 = Elem<EL>::load(vn, src + i);
-          v2 = Elem<EL>::load(vn, src + i + HALF);
-        }
-        kts[i * (kSimtKT + 1) + j] = k1;
-        kts[(i + HALF) * (kSimtKT + 1) + j] = k2;
-        vs[j * DH + i] = v1;
-        vs[j * DH + i + HALF] = v2;
+#pragma unroll
+      for (int e = 0; e < EPV; ++e) {
+        kts[(vi * EPV + e) * (kSimtKT + 1) + j] = kf[e];
+        vs[j * DH + vi * EPV + e] = vf[e];
       }
     }
     __syncthreads();
-    const int key = kt0 + lane;
-    const bool in_range = tree ? key < N : key < k_end;
+    const bool key_ok = kt0 + lane < k_end;
 #pragma unroll
     for (int rr = 0; rr < 4; ++rr) {
       const int r = warp * 4 + rr;
-      const int R = mt * kSimtRows + r;
-      if (R >= M) continue;
-      bool key_ok = in_range;
-      if (tree && key_ok) {
-        const int u = R / g;
-        key_ok = ((t.anc[(int64_t)u * W + (key >> 6)] >> (key & 63)) & 1ull) != 0;
-      }
+      if (mt * kSimtRows + r >= M) continue;
       float sc = 0.f;
 #pragma unroll 16
       for (int i = 0; i < DH; ++i) sc = fmaf(qs[r * DH + i], kts[i * (kSimtKT + 1) + lane], sc);
@@ -278,8 +239,9 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(SimtArgs a) {
   if (tid == 0) a.counter[unit] = 0;       // every split has arrived: ready for the next call
   __threadfence();
 
-  // Merge the splits (split 0's partial holds the tree block).
+  // Merge the splits, then add the tree block.
   float* out = a.out;
+  const int W = t.n_words;
   for (int rr = 0; rr < 4; ++rr) {
     const int r = warp * 4 + rr;
     const int R = mt * kSimtRows + r;
@@ -299,6 +261,38 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(SimtArgs a) {
       l = fmaf(__ldcg(&a.part_ml[pr * 2 + 1]), w, l);
 #pragma unroll
       for (int c = 0; c < PER_LANE; ++c) o[c] = fmaf(__ldcg(&a.part_o[pr * DH + lane + 32 * c]), w, o[c]);
+    }
+    float qv[PER_LANE];
+#pragma unroll
+    for (int c = 0; c < PER_LANE; ++c) qv[c] = qs[r * DH + lane + 32 * c];
+    for (int wd = 0; wd < W; ++wd) {
+      unsigned long long bits = t.anc[(int64_t)u * W + wd];
+      while (bits) {
+        const int v = wd * 64 + __ffsll((long long)bits) - 1;
+        bits &= bits - 1;
+        const int64_t kb = (((int64_t)b * NS + v) * a.Hkv + kvh) * DH;
+        const int ti0 = t.depth[v] * HALF;
+        float kr[PER_LANE];
+#pragma unroll
+        for (int c = 0; c < PER_LANE / 2; ++c) {
+          const int i = lane + 32 * c;
+          const float x1 = Elem<EL>::load(kn, kb + i), x2 = Elem<EL>::load(kn, kb + i + HALF);
+          kr[c] = x1 * tab_c[ti0 + i] - x2 * tab_s[ti0 + i];
+          kr[c + PER_LANE / 2] = x2 * tab_c[ti0 + i] + x1 * tab_s[ti0 + i];
+        }
+        float dot = 0.f;
+#pragma unroll
+        for (int c = 0; c < PER_LANE; ++c) dot = fmaf(qv[c], kr[c], dot);
+        const float sc = warp_sum(dot) * a.scale_log2;
+        const float m_new = fmaxf(Mx, sc);
+        const float alpha = (Mx == -INFINITY) ? 0.f : exp2f(Mx - m_new);
+        const float p = exp2f(sc - m_new);
+        l = l * alpha + p;
+#pragma unroll
+        for (int c = 0; c < PER_LANE; ++c)
+          o[c] = fmaf(o[c], alpha, p * Elem<EL>::load(vn, kb + lane + 32 * c));
+        Mx = m_new;
+      }
     }
     const float inv_l = 1.f / l;
     const int64_t ob = (((int64_t)b * NS + u) * a.Hq + h) * DH;
