@@ -55,8 +55,12 @@ def _static_call(m, t_g, q, k, v, cache, L, max_prefix, rope_base, out, lse, sta
         float(rope_base), float(scale), vp(out), vp(lse), vp(status), stream)
 
 
-@pytest.mark.parametrize("name", ["tiny-fp32", "vicuna7b-64", "llama3-8b-256"])
-def test_static_scratch_matches_workspace_entry(m, name):
+@pytest.mark.parametrize("name,mirror", [("tiny-fp32", False), ("vicuna7b-64", False), ("llama3-8b-256", False),
+                                         ("vicuna7b-64", True), ("llama3-8b-256", True)])
+def test_static_scratch_matches_workspace_entry(m, name, mirror):
+    """With mirror, the static call runs on a cache carrying an fp16 mirror: the mirror
+    holds the values the kernel otherwise converts itself, so the output is bit for bit
+    that of the cache without one, and the mirror still mirrors the cache afterwards."""
     w, t_g, q, k, v, K, V, lengths = _setup(m, name)
     B, N = w.batch, t_g.n_rows
     L = gu.device_tensor(lengths, torch.int32)
@@ -79,6 +83,8 @@ def test_static_scratch_matches_workspace_entry(m, name):
         lse = torch.full((B, N, w.n_q_heads), float("nan"), device="cuda")
         status = torch.full((B,), 99, dtype=torch.int32, device="cuda")
         cache_s = m.KVCache(K_s, V_s)
+        if mirror:
+            cache_s.add_mirror()
         torch.cuda.synchronize()
         torch_bytes, (free_bytes, _) = torch.cuda.memory_allocated(), torch.cuda.mem_get_info()
         rc = _static_call(m, t_g, q, k, v, cache_s, L, max_prefix, w.rope_base, out, lse, status)
@@ -93,6 +99,10 @@ def test_static_scratch_matches_workspace_entry(m, name):
         gu.float_parity(out, ref, is_f32, f"static entry, call {call}")
         gu.float_parity(lse, ref_lse, True, f"static entry lse, call {call}")
         assert torch.equal(K_s, K_ref) and torch.equal(V_s, V_ref)     # same staged rows
+        if mirror:
+            assert torch.equal(out, ref) and torch.equal(lse, ref_lse)
+            for c16, c in ((cache_s.k_f16, K_s), (cache_s.v_f16, V_s)):
+                assert torch.equal(c16, c.to(torch.float16))
 
 
 def test_static_scratch_refuses_oversized_shapes(m):
