@@ -2,8 +2,9 @@
 // §0x04E, §0x07B; [PartII] Part 7; [CN] "接受机制").
 //
 // Only internal rows (rows with children) are read: leaves never score a candidate.
-//   row_stats_kernel   grid (chunks, internal rows, B): per chunk of V the max of
-//                      x/T, sum e^{x/T-m}, sum e^{x/T-m}(x/T-m) and the argmax of x.
+//   row_stats_kernel   grid (chunks, internal rows, B): per chunk of V the argmax of x
+//                      (greedy) or the max of x/T, sum e^{x/T-m} and sum
+//                      e^{x/T-m}(x/T-m) (typical, which reads no argmax).
 //   guard_kernel       (entropy_guard only) per chunk sum of -p ln(p + 1e-5) with the
 //                      row's merged max and partition function.
 //   select_kernel      one CTA per sequence: merge the chunk statistics per row, walk
@@ -102,7 +103,7 @@ __device__ __forceinline__ void fold(const float* x, int i0, float c2, float& m2
   }
 }
 
-// One pass over a chunk of one internal row: argmax (greedy), plus max, partition
+// One pass over a chunk of one internal row: argmax (greedy), or max, partition
 // function and first moment (typical).  16-byte loads when the chunk is aligned.
 template <typename EL, bool TYP>
 __global__ void __launch_bounds__(kThreads) row_stats_kernel(medusa_tree_t t, int V, int chunk,

@@ -106,8 +106,8 @@ struct RowPart {
   float m;      // max of x / T over the chunk
   float z;      // sum exp(x/T - m)
   float s1;     // sum exp(x/T - m) * (x/T - m)
-  float amax_v; // largest raw logit
-  int amax_i;   // its id (lowest among equal values)
+  float amax_v; // largest raw logit (greedy; -inf from the typical statistics)
+  int amax_i;   // its id (lowest among equal values; INT_MAX when not taken)
   int pad[3];
 };
 
