@@ -106,7 +106,7 @@ struct RowPart {
   float m;      // max of x / T over the chunk
   float z;      // sum exp(x/T - m)
   float s1;     // sum exp(x/T - m) * (x/T - m)
-  float amax_v; // largest raw logit (greedy; -inf from the typical statistics)
+  float amax_v; // largest raw logit (-inf from row_stats_kernel's typical pass, which skips it)
   int amax_i;   // its id (lowest among equal values; INT_MAX when not taken)
   int pad[3];
 };
