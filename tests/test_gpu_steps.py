@@ -256,10 +256,13 @@ def test_attn_rising_scores_rescale(m, monkeypatch, shape, splits):
         gu.float_parity(lse[b], o_lse, False, f"lse b={b}")
 
 
-def test_attn_head_dim_64_bf16(m):
+@pytest.mark.parametrize("mirror", [False, True])
+def test_attn_head_dim_64_bf16(m, mirror):
+    """The CUDA-core kernel on a bf16 cache (head_dim 64); with an fp16 mirror its staged
+    tree rows must reach the mirror too."""
     w = synth.small_variant(synth.WORKLOADS["vicuna7b-64"], n_q_heads=8, n_kv_heads=2, head_dim=64,
                             prefix_len=513, seed=61)
-    attn_case(m, w, otree.regular_paths((3, 2)), synth.prefix_lengths(w))
+    attn_case(m, w, otree.regular_paths((3, 2)), synth.prefix_lengths(w), mirror=mirror)
 
 
 def test_attn_capacity_error_leaves_sequence_alone(m):
