@@ -126,3 +126,22 @@ def test_node_attention_rows_matches_dense():
                                                  L, t.depth, t.mask[u], u)
             np.testing.assert_allclose(o, out[u, h], rtol=1e-12)
             assert l == pytest.approx(lse[u, h], rel=1e-12)
+
+
+def test_bf16_values_in_fp16_range_convert_exactly():
+    """The tensor-core attention multiplies bf16 K/V in fp16, and a cache's fp16 mirror
+    stores them so: every bf16 value of magnitude in [2^-14, 65504] has an fp16 twin of
+    the same value (all 65536 bit patterns checked), zero stays zero, and every larger
+    finite value becomes inf (which the attention reports as a range error)."""
+    b = np.arange(65536, dtype=np.uint32)
+    f32 = (b << 16).view(np.float32)
+    with np.errstate(over="ignore"):
+        f16 = f32.astype(np.float16)
+    back = f16.astype(np.float32)
+    fin = np.isfinite(f32)
+    mag = np.abs(f32)
+    in_range = fin & (mag >= 2.0 ** -14) & (mag <= 65504)
+    assert in_range.sum() == 2 * 30 * 128              # sign x 30 exponents x 128 mantissas
+    assert (back[in_range] == f32[in_range]).all()
+    assert (back[f32 == 0] == 0).all()
+    assert np.isinf(f16[fin & (mag > 65504)]).all()
