@@ -36,6 +36,7 @@ namespace {
 constexpr int kSimtThreads = 128;
 constexpr int kSimtRows = 16;   // 4 warps x 4 rows
 constexpr int kSimtKT = 32;     // keys per tile
+constexpr int kAncGroup = 4;    // tree-block ancestors whose rows are loaded together
 
 struct SimtArgs {
   medusa_tree_t t;
@@ -82,6 +83,40 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(SimtArgs a) {
   const medusa_tree_t t = seq_tree(a.t, b);
   const int NS = a.t.n_rows, N = t.n_rows, g = a.g, M = N * g;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const EL* q = (const EL*)a.q;
+  const EL* kn = (const EL*)a.k_new;
+  const EL* vn = (const EL*)a.v_new;
+  // The elements this thread rotates (its query pairs and, in split 0, the pairs of the
+  // tree keys and values it stages) are loaded with L, before anything waits on them:
+  // one memory round trip for the whole prologue instead of one per loop iteration.
+  constexpr int QIT = kSimtRows * HALF / kSimtThreads;
+  static_assert(QIT * kSimtThreads == kSimtRows * HALF, "whole (row, pair) items per thread");
+  float qx1[QIT], qx2[QIT], kx1[QIT], kx2[QIT];
+  EL vx1[QIT], vx2[QIT];
+  int rdep[QIT];
+#pragma unroll
+  for (int it = 0; it < QIT; ++it) {
+    const int idx = tid + it * kSimtThreads;
+    const int r = idx / HALF, i = idx % HALF;
+    const int R = mt * kSimtRows + r;
+    qx1[it] = qx2[it] = kx1[it] = kx2[it] = 0.f;
+    vx1[it] = vx2[it] = EL(0);
+    rdep[it] = 0;
+    if (R < M) {
+      const int u = R / g, h = kvh * g + R % g;
+      const int64_t base = (((int64_t)b * NS + u) * a.Hq + h) * DH;
+      qx1[it] = Elem<EL>::load(q, base + i);
+      qx2[it] = Elem<EL>::load(q, base + i + HALF);
+      rdep[it] = t.depth[u];
+      if (s == 0 && R % g == 0) {
+        const int64_t src = (((int64_t)b * NS + u) * a.Hkv + kvh) * DH;
+        kx1[it] = Elem<EL>::load(kn, src + i);
+        kx2[it] = Elem<EL>::load(kn, src + i + HALF);
+        vx1[it] = vn[src + i];
+        vx2[it] = vn[src + i + HALF];
+      }
+    }
+  }
   const int Lb = a.L[b];
   if (mt * kSimtRows >= M) return;        // a row tile past this sequence's rows: the whole unit
   const bool first_cta = (s == 0 && mt == 0 && kvh == 0 && tid == 0);
@@ -105,50 +140,41 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(SimtArgs a) {
   }
   __syncthreads();
 
-  const EL* q = (const EL*)a.q;
-  const EL* kn = (const EL*)a.k_new;
-  const EL* vn = (const EL*)a.v_new;
-  // Rotated queries of this m-tile.
-  for (int idx = tid; idx < kSimtRows * HALF; idx += kSimtThreads) {
+  // Rotated queries of this m-tile; in split 0 the rotated tree keys and the tree
+  // values at cache rows L + u.  The destination rows are looked up first (a paged
+  // cache reads its block table), then every store follows.
+  EL* ck = (EL*)a.c.k;
+  EL* cv = (EL*)a.c.v;
+  int64_t dst[QIT];
+#pragma unroll
+  for (int it = 0; it < QIT; ++it) {
+    const int R = mt * kSimtRows + (tid + it * kSimtThreads) / HALF;
+    dst[it] = (s == 0 && R < M && R % g == 0) ? row_off(a.c, b, kvh, Lb + R / g) : -1;
+  }
+#pragma unroll
+  for (int it = 0; it < QIT; ++it) {
+    const int idx = tid + it * kSimtThreads;
     const int r = idx / HALF, i = idx % HALF;
     const int R = mt * kSimtRows + r;
-    float y1 = 0.f, y2 = 0.f;
-    if (R < M) {
-      const int u = R / g, h = kvh * g + R % g;
-      const int64_t base = (((int64_t)b * NS + u) * a.Hq + h) * DH;
-      const float x1 = Elem<EL>::load(q, base + i), x2 = Elem<EL>::load(q, base + i + HALF);
-      const int ti = t.depth[u] * HALF + i;
-      y1 = x1 * tab_c[ti] - x2 * tab_s[ti];
-      y2 = x2 * tab_c[ti] + x1 * tab_s[ti];
-    }
-    qs[r * DH + i] = y1;
-    qs[r * DH + i + HALF] = y2;
-  }
-  // Stage rotated tree keys and tree values at cache rows L + u (split 0 only).
-  if (s == 0) {
-    EL* ck = (EL*)a.c.k;
-    EL* cv = (EL*)a.c.v;
-    for (int idx = tid; idx < kSimtRows * HALF; idx += kSimtThreads) {
-      const int r = idx / HALF, i = idx % HALF;
-      const int R = mt * kSimtRows + r;
-      if (R >= M || R % g != 0) continue;
-      const int u = R / g;
-      const int64_t src = (((int64_t)b * NS + u) * a.Hkv + kvh) * DH;
-      const float x1 = Elem<EL>::load(kn, src + i), x2 = Elem<EL>::load(kn, src + i + HALF);
-      const int ti = t.depth[u] * HALF + i;
-      const int64_t dst = row_off(a.c, b, kvh, Lb + u);
-      Elem<EL>::store(ck, dst + i, x1 * tab_c[ti] - x2 * tab_s[ti]);
-      Elem<EL>::store(ck, dst + i + HALF, x2 * tab_c[ti] + x1 * tab_s[ti]);
-      cv[dst + i] = vn[src + i];
-      cv[dst + i + HALF] = vn[src + i + HALF];
+    const int ti = rdep[it] * HALF + i;
+    const float cs = tab_c[ti], sn = tab_s[ti];
+    qs[r * DH + i] = R < M ? qx1[it] * cs - qx2[it] * sn : 0.f;
+    qs[r * DH + i + HALF] = R < M ? qx2[it] * cs + qx1[it] * sn : 0.f;
+    if (dst[it] >= 0) {
+      const int64_t d0 = dst[it];
+      const float y1 = kx1[it] * cs - kx2[it] * sn, y2 = kx2[it] * cs + kx1[it] * sn;
+      Elem<EL>::store(ck, d0 + i, y1);
+      Elem<EL>::store(ck, d0 + i + HALF, y2);
+      cv[d0 + i] = vx1[it];
+      cv[d0 + i + HALF] = vx2[it];
       if constexpr (sizeof(EL) == 2) {
         if (a.c.k_f16) {                          // the fp16 mirror of the rows just written
           uint16_t* mk = (uint16_t*)a.c.k_f16;
           uint16_t* mv = (uint16_t*)a.c.v_f16;
-          mk[dst + i] = bf16_bits_to_f16_bits(ck[dst + i]);
-          mk[dst + i + HALF] = bf16_bits_to_f16_bits(ck[dst + i + HALF]);
-          mv[dst + i] = bf16_bits_to_f16_bits(vn[src + i]);
-          mv[dst + i + HALF] = bf16_bits_to_f16_bits(vn[src + i + HALF]);
+          mk[d0 + i] = bf16_bits_to_f16_bits(f32_to_bf16_bits(y1));
+          mk[d0 + i + HALF] = bf16_bits_to_f16_bits(f32_to_bf16_bits(y2));
+          mv[d0 + i] = bf16_bits_to_f16_bits(vx1[it]);
+          mv[d0 + i + HALF] = bf16_bits_to_f16_bits(vx2[it]);
         }
       }
     }
@@ -169,19 +195,30 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(SimtArgs a) {
   const EL* ckr = (const EL*)a.c.k;
   const EL* cvr = (const EL*)a.c.v;
   for (int kt0 = k_begin; kt0 < k_end; kt0 += kSimtKT) {
+    // The tile's 16-byte vectors of this thread: all loads first (keys past the range
+    // read as zeros), then the stores into shared memory.
     constexpr int VEC_PER_ROW = DH / EPV;
-    for (int idx = tid; idx < kSimtKT * VEC_PER_ROW; idx += kSimtThreads) {
-      const int j = idx / VEC_PER_ROW, vi = idx % VEC_PER_ROW;
-      const int key = kt0 + j;
-      float kf[EPV], vf[EPV];
-      if (key < k_end) {
-        const int64_t off = row_off(a.c, b, kvh, key) + vi * EPV;
-        Elem<EL>::unpack(*reinterpret_cast<const uint4*>(ckr + off), kf);
-        Elem<EL>::unpack(*reinterpret_cast<const uint4*>(cvr + off), vf);
-      } else {
+    constexpr int KIT = kSimtKT * VEC_PER_ROW / kSimtThreads;
+    static_assert(KIT * kSimtThreads == kSimtKT * VEC_PER_ROW, "whole vectors per thread");
+    uint4 kraw[KIT], vraw[KIT];
 #pragma unroll
-        for (int e = 0; e < EPV; ++e) { kf[e] = 0.f; vf[e] = 0.f; }
+    for (int it = 0; it < KIT; ++it) {
+      const int idx = tid + it * kSimtThreads;
+      const int key = kt0 + idx / VEC_PER_ROW;
+      kraw[it] = vraw[it] = make_uint4(0u, 0u, 0u, 0u);
+      if (key < k_end) {
+        const int64_t off = row_off(a.c, b, kvh, key) + (idx % VEC_PER_ROW) * EPV;
+        kraw[it] = *reinterpret_cast<const uint4*>(ckr + off);
+        vraw[it] = *reinterpret_cast<const uint4*>(cvr + off);
       }
+    }
+#pragma unroll
+    for (int it = 0; it < KIT; ++it) {
+      const int idx = tid + it * kSimtThreads;
+      const int j = idx / VEC_PER_ROW, vi = idx % VEC_PER_ROW;
+      float kf[EPV], vf[EPV];
+      Elem<EL>::unpack(kraw[it], kf);
+      Elem<EL>::unpack(vraw[it], vf);
 #pragma unroll
       for (int e = 0; e < EPV; ++e) {
         kts[(vi * EPV + e) * (kSimtKT + 1) + j] = kf[e];
@@ -239,66 +276,110 @@ __global__ void __launch_bounds__(kSimtThreads) attn_simt_kernel(SimtArgs a) {
   if (tid == 0) a.counter[unit] = 0;       // every split has arrived: ready for the next call
   __threadfence();
 
-  // Merge the splits, then add the tree block.
+  // Merge the splits, then add the tree block.  The warp's four rows read their
+  // partials together, split by split, and each row reads the K/V rows of up to
+  // kAncGroup ancestors before it uses the first: the loads of a group share one
+  // memory round trip.  The arithmetic and its order are those of a row-by-row,
+  // ancestor-by-ancestor merge.
   float* out = a.out;
   const int W = t.n_words;
+  bool live[4];
+  float Mx[4], l[4], o[4][PER_LANE];
+#pragma unroll
   for (int rr = 0; rr < 4; ++rr) {
+    live[rr] = mt * kSimtRows + warp * 4 + rr < M;
+    Mx[rr] = -INFINITY;
+    l[rr] = 0.f;
+#pragma unroll
+    for (int c = 0; c < PER_LANE; ++c) o[rr][c] = 0.f;
+  }
+  for (int s2 = 0; s2 < a.n_split; ++s2) {
+    const int64_t pr0 = ((int64_t)unit * a.n_split + s2) * kSimtRows + warp * 4;
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr)
+      if (live[rr]) Mx[rr] = fmaxf(Mx[rr], __ldcg(&a.part_ml[(pr0 + rr) * 2]));
+  }
+  for (int s2 = 0; s2 < a.n_split; ++s2) {
+    const int64_t pr0 = ((int64_t)unit * a.n_split + s2) * kSimtRows + warp * 4;
+#pragma unroll
+    for (int rr = 0; rr < 4; ++rr) {
+      if (!live[rr]) continue;
+      const float ms = __ldcg(&a.part_ml[(pr0 + rr) * 2]);
+      const float ps = __ldcg(&a.part_ml[(pr0 + rr) * 2 + 1]);
+      float po[PER_LANE];
+#pragma unroll
+      for (int c = 0; c < PER_LANE; ++c) po[c] = __ldcg(&a.part_o[(pr0 + rr) * DH + lane + 32 * c]);
+      const bool empty = ms == -INFINITY;     // a split without keys adds nothing
+      const float w = empty ? 0.f : exp2f(ms - Mx[rr]);
+      l[rr] = empty ? l[rr] : fmaf(ps, w, l[rr]);
+#pragma unroll
+      for (int c = 0; c < PER_LANE; ++c) o[rr][c] = empty ? o[rr][c] : fmaf(po[c], w, o[rr][c]);
+    }
+  }
+#pragma unroll
+  for (int rr = 0; rr < 4; ++rr) {
+    if (!live[rr]) continue;
     const int r = warp * 4 + rr;
     const int R = mt * kSimtRows + r;
-    if (R >= M) continue;
     const int u = R / g, h = kvh * g + R % g;
-    float Mx = -INFINITY;
-    for (int s2 = 0; s2 < a.n_split; ++s2)
-      Mx = fmaxf(Mx, __ldcg(&a.part_ml[(((int64_t)unit * a.n_split + s2) * kSimtRows + r) * 2]));
-    float l = 0.f, o[PER_LANE];
-#pragma unroll
-    for (int c = 0; c < PER_LANE; ++c) o[c] = 0.f;
-    for (int s2 = 0; s2 < a.n_split; ++s2) {
-      const int64_t pr = ((int64_t)unit * a.n_split + s2) * kSimtRows + r;
-      const float ms = __ldcg(&a.part_ml[pr * 2]);
-      if (ms == -INFINITY) continue;
-      const float w = exp2f(ms - Mx);
-      l = fmaf(__ldcg(&a.part_ml[pr * 2 + 1]), w, l);
-#pragma unroll
-      for (int c = 0; c < PER_LANE; ++c) o[c] = fmaf(__ldcg(&a.part_o[pr * DH + lane + 32 * c]), w, o[c]);
-    }
+    float mx = Mx[rr], ls = l[rr];
     float qv[PER_LANE];
 #pragma unroll
     for (int c = 0; c < PER_LANE; ++c) qv[c] = qs[r * DH + lane + 32 * c];
     for (int wd = 0; wd < W; ++wd) {
-      unsigned long long bits = t.anc[(int64_t)u * W + wd];
+      unsigned long long bits = t.anc[(int64_t)u * W + wd];    // the same for the whole warp
       while (bits) {
-        const int v = wd * 64 + __ffsll((long long)bits) - 1;
-        bits &= bits - 1;
-        const int64_t kb = (((int64_t)b * NS + v) * a.Hkv + kvh) * DH;
-        const int ti0 = t.depth[v] * HALF;
-        float kr[PER_LANE];
+        int vv[kAncGroup], ti[kAncGroup];
+        float kx[kAncGroup][PER_LANE], vx[kAncGroup][PER_LANE];
 #pragma unroll
-        for (int c = 0; c < PER_LANE / 2; ++c) {
-          const int i = lane + 32 * c;
-          const float x1 = Elem<EL>::load(kn, kb + i), x2 = Elem<EL>::load(kn, kb + i + HALF);
-          kr[c] = x1 * tab_c[ti0 + i] - x2 * tab_s[ti0 + i];
-          kr[c + PER_LANE / 2] = x2 * tab_c[ti0 + i] + x1 * tab_s[ti0 + i];
+        for (int j = 0; j < kAncGroup; ++j) {
+          vv[j] = bits ? wd * 64 + __ffsll((long long)bits) - 1 : -1;
+          bits &= bits - 1;
+          ti[j] = 0;
+#pragma unroll
+          for (int c = 0; c < PER_LANE; ++c) kx[j][c] = vx[j][c] = 0.f;
+          if (vv[j] >= 0) {
+            const int64_t kb = (((int64_t)b * NS + vv[j]) * a.Hkv + kvh) * DH;
+            ti[j] = t.depth[vv[j]] * HALF;
+#pragma unroll
+            for (int c = 0; c < PER_LANE / 2; ++c) {
+              kx[j][c] = Elem<EL>::load(kn, kb + lane + 32 * c);
+              kx[j][c + PER_LANE / 2] = Elem<EL>::load(kn, kb + lane + 32 * c + HALF);
+            }
+#pragma unroll
+            for (int c = 0; c < PER_LANE; ++c) vx[j][c] = Elem<EL>::load(vn, kb + lane + 32 * c);
+          }
         }
-        float dot = 0.f;
 #pragma unroll
-        for (int c = 0; c < PER_LANE; ++c) dot = fmaf(qv[c], kr[c], dot);
-        const float sc = warp_sum(dot) * a.scale_log2;
-        const float m_new = fmaxf(Mx, sc);
-        const float alpha = (Mx == -INFINITY) ? 0.f : exp2f(Mx - m_new);
-        const float p = exp2f(sc - m_new);
-        l = l * alpha + p;
+        for (int j = 0; j < kAncGroup; ++j) {
+          if (vv[j] < 0) continue;
+          float kr[PER_LANE];
 #pragma unroll
-        for (int c = 0; c < PER_LANE; ++c)
-          o[c] = fmaf(o[c], alpha, p * Elem<EL>::load(vn, kb + lane + 32 * c));
-        Mx = m_new;
+          for (int c = 0; c < PER_LANE / 2; ++c) {
+            const int i = lane + 32 * c;
+            const float x1 = kx[j][c], x2 = kx[j][c + PER_LANE / 2];
+            kr[c] = x1 * tab_c[ti[j] + i] - x2 * tab_s[ti[j] + i];
+            kr[c + PER_LANE / 2] = x2 * tab_c[ti[j] + i] + x1 * tab_s[ti[j] + i];
+          }
+          float dot = 0.f;
+#pragma unroll
+          for (int c = 0; c < PER_LANE; ++c) dot = fmaf(qv[c], kr[c], dot);
+          const float sc = warp_sum(dot) * a.scale_log2;
+          const float m_new = fmaxf(mx, sc);
+          const float alpha = (mx == -INFINITY) ? 0.f : exp2f(mx - m_new);
+          const float p = exp2f(sc - m_new);
+          ls = ls * alpha + p;
+#pragma unroll
+          for (int c = 0; c < PER_LANE; ++c) o[rr][c] = fmaf(o[rr][c], alpha, p * vx[j][c]);
+          mx = m_new;
+        }
       }
     }
-    const float inv_l = 1.f / l;
+    const float inv_l = 1.f / ls;
     const int64_t ob = (((int64_t)b * NS + u) * a.Hq + h) * DH;
 #pragma unroll
-    for (int c = 0; c < PER_LANE; ++c) out[ob + lane + 32 * c] = o[c] * inv_l;
-    if (a.lse && lane == 0) a.lse[((int64_t)b * NS + u) * a.Hq + h] = (Mx + log2f(l)) * kLn2;
+    for (int c = 0; c < PER_LANE; ++c) out[ob + lane + 32 * c] = o[rr][c] * inv_l;
+    if (a.lse && lane == 0) a.lse[((int64_t)b * NS + u) * a.Hq + h] = (mx + log2f(ls)) * kLn2;
   }
 }
 
