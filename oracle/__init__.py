@@ -35,4 +35,8 @@ Pinning status (what each function is checked against, in tests/):
   accept.target_logits      identity and orthonormal projections (closed forms)
   compact.kv_compact        [M7.2] §0x06B trace; overlap case against a snapshot-free copy
   cost                      [M7.2] §0x02E / §0x06 printed parameter and byte counts
+  round.tree_fill           [M7.2] §0x04A slot formula worked by hand (widths (2, 2))
+  round.run_sequence        a round worked by hand: W1 = 0 heads read by inspection,
+                            keys (1, 0) rotated to angle L + depth, planted greedy
+                            argmaxes, committed rows and length ([M7.2] §0x06B)
 """
