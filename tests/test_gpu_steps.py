@@ -181,6 +181,19 @@ def test_attn_root_only_and_deep_chain(m):
     attn_case(m, w, chain, synth.prefix_lengths(w))
 
 
+@pytest.mark.parametrize("dh", [64, 128])
+def test_attn_fp32_deep_chain_and_multiword_mask(m, dh):
+    """The CUDA-core kernel (fp32) where a row has many ancestors: a 16-deep chain (17
+    ancestor-or-self rows, read in groups of four with a partial last group) and the
+    341-row Cartesian tree (six mask words, ancestors spread over several words), with
+    NaN in the cache rows past L + N."""
+    w = synth.small_variant(synth.WORKLOADS["longctx-341"], dtype="f32", n_q_heads=4, n_kv_heads=2,
+                            head_dim=dh, prefix_len=150, seed=61 + dh)
+    chain = [tuple([0] * t) for t in range(1, 17)]
+    attn_case(m, w, chain, synth.prefix_lengths(w), fill_tail=float("nan"))
+    attn_case(m, w, otree.regular_paths((4, 4, 4, 4)), synth.prefix_lengths(w), fill_tail=float("nan"))
+
+
 @pytest.mark.parametrize("mirror", [False, True])
 def test_attn_multiword_mask_and_nan_tail(m, mirror):
     """341 rows (six 64-bit mask words); cache rows past L + N hold NaN and must stay unread."""
