@@ -194,3 +194,41 @@ def test_log_prob_without_temperature(monkeypatch):
     monkeypatch.setattr(accept, "log_prob",
                         lambda row, tok, st, temperature=1.0: float(np.float64(row[tok]) - st.m - st.log_z))
     assert fails(AC.test_temperature_two_closed_form)
+
+
+# ---- the whole round (pins in tests/test_oracle_round.py) --------------------------
+
+def test_round_pool_read_rank_major(monkeypatch):
+    """cand taken rank by rank across the heads instead of head by head."""
+    import oracle.round as oround
+    import tests.test_oracle_round as TR
+
+    def mutated(tmpl, root, pool, L):
+        cand = np.concatenate([[int(root)], np.asarray(pool, dtype=np.int64).T.reshape(-1)])
+        return cand[tmpl.slot].astype(np.int64), (int(L) + tmpl.depth).astype(np.int64)
+    monkeypatch.setattr(oround, "tree_fill", mutated)
+    assert fails(TR.test_round_worked_example)
+
+
+def test_round_keys_rotated_without_prefix_offset(monkeypatch):
+    """Staged tree keys rotated at depth(u) instead of L + depth(u)."""
+    import tests.test_oracle_round as TR
+    real = attention.tree_attention
+
+    def mutated(q, k_new, v_new, pk, pv, L, depth, mask, base=10000.0, scale=None):
+        out, lse, _ = real(q, k_new, v_new, pk, pv, L, depth, mask, base, scale)
+        return out, lse, attention.rope(k_new, np.asarray(depth)[:, None], base)
+    monkeypatch.setattr(attention, "tree_attention", mutated)
+    assert fails(TR.test_round_worked_example)
+
+
+def test_round_commits_by_depth(monkeypatch):
+    """The accepted path's rows copied from L + depth instead of their staged rows L + u."""
+    import tests.test_oracle_round as TR
+    real = compact.kv_compact
+
+    def mutated(cache_k, cache_v, L, rows):
+        depth_rows = np.arange(len(rows))        # row j of the path sits at depth j
+        return real(cache_k, cache_v, L, depth_rows)
+    monkeypatch.setattr(compact, "kv_compact", mutated)
+    assert fails(TR.test_round_worked_example)
