@@ -98,6 +98,23 @@ def test_greedy_matches_oracle(native, K, R, budget):
     assert medusa_tree_greedy(acc2, budget) == otree.greedy_tree(acc2, budget)
 
 
+@pytest.mark.parametrize("widths", [(1,), (3,), (2, 3), (4, 4, 4, 4), (10, 1, 2), (1, 1, 1, 1, 1, 1, 1, 1)])
+def test_regular_size_query_and_paths(native, widths):
+    """The size query gives sum_k prod_{i<=k} s_i (the oracle's count of non-root
+    nodes), the paths equal the oracle's, and a buffer one path short is refused."""
+    lib = native.lib()
+    K = len(widths)
+    w = np.ascontiguousarray(widths, dtype=np.int32)
+    n = C.c_int32(-1)
+    assert lib.medusa_tree_regular(w.ctypes.data, K, None, 0, C.byref(n)) == native.OK
+    assert n.value == otree.regular_node_count(widths) == len(otree.regular_paths(widths))
+    out = np.full((n.value, K), -1, dtype=np.int32)
+    assert lib.medusa_tree_regular(w.ctypes.data, K, out.ctypes.data, n.value, C.byref(n)) == native.OK
+    assert [tuple(int(x) for x in row if x >= 0) for row in out] == otree.regular_paths(widths)
+    short = np.full((max(n.value - 1, 1), K), -1, dtype=np.int32)
+    assert lib.medusa_tree_regular(w.ctypes.data, K, short.ctypes.data, n.value - 1, C.byref(n)) == native.EWORKSPACE
+
+
 @pytest.mark.parametrize("bad", [[(0, 1)], [(0,), (0,)], [(0,), (9,)], [(0,), (0, 0), (0, 0, 0)]])
 def test_compile_rejects(native, bad):
     from medusa_speculative_tree_gb300.api import Template
