@@ -228,3 +228,20 @@ def test_workload_greedy_templates(name):
     # depth-1 children receive the most descendants
     kids = [int((t.parent == u).sum()) for u in range(1, 1 + counts[1])]
     assert kids == sorted(kids, reverse=True)
+
+
+@pytest.mark.parametrize("name,depths,leaves", [
+    ("vicuna7b-64", [7, 21, 30, 5], 41),
+    ("llama3-8b-256", [10, 55, 120, 70], 174),
+])
+def test_workload_greedy_tree_shapes(name, depths, leaves):
+    """The greedy workloads' trees (budget 63 or 255 over ranks <= 10 of the synthetic
+    accuracies a_k^(i) = 0.7 * 0.6^(k-1) * 0.45^(i-1), 1e-12 tie rule): nodes per depth and
+    leaf count.  The 63-node cut falls inside a 15-way exact weight tie, so a different
+    tie rule changes the first shape."""
+    from oracle.round import template_for
+    w = synth.WORKLOADS[name]
+    t = template_for(w.template, w.topk, w.n_heads, synth.rank_accuracy(w.n_heads, 10))
+    assert t.n_rows == 1 + sum(depths)
+    assert np.bincount(t.depth)[1:].tolist() == depths
+    assert t.n_paths == leaves
